@@ -1,0 +1,200 @@
+/*
+ * swa_oracle.c -- CPU fp64 oracle for sliding-window attention with a
+ * per-head attention-sink bias.  TEST INFRASTRUCTURE ONLY: it is called by the
+ * tests, by the package's smoke check and by the benchmark's CPU-baseline leg,
+ * never by the library path.  It shares no code with the CUDA kernels.
+ *
+ * What it computes (plain definition, written out):
+ *
+ *   Hybrid attention, "MiMo-V2-Flash Technical Report" summary page, section
+ *   "前置知识" (prerequisites), items "混合注意力机制" and "注意力sink偏置":
+ *   a sliding-window layer lets token i attend only to a local window of W
+ *   tokens, a global layer to the whole (causal) sequence; every head adds a
+ *   learnable bias s_h to its softmax denominator, which acts as a virtual
+ *   "sink" token that takes weight but contributes no value.  The window is
+ *   128 tokens ("wiki-for-amaranth" MiMo-V2 engineering notes, section
+ *   "关键架构决策", item 1).  GQA is used in every attention layer ("MiMo-V2.5"
+ *   ICML 2026 talk write-up, section 02).
+ *
+ *   For batch b, query head h, position i, with G = Hq/Hkv and kv = h / G:
+ *     keys j in [max(0, i-W+1), i]                      (exactly W when i >= W-1)
+ *     x_j  = (sum_d q[b,i,h,d] * k[b,j,kv,d]) / sqrt(D)
+ *     m    = max(s_h, max_j x_j)                        (first pass)
+ *     l    = exp(s_h - m) + sum_j exp(x_j - m)          (second pass)
+ *     o    = sum_j exp(x_j - m) * v[b,j,kv,:] / l
+ *     lse  = m + log(l)                                 (natural log, sink included)
+ *   W >= T is the global (full causal) layer.
+ *
+ *   Decode ("pwwt.cn" MiMo-V2-Flash essay, section 1.1: the sliding-window KV
+ *   cache has fixed size, O(W) memory; ICML talk write-up, Q&A K: position
+ *   indices keep increasing while the window slides): one query at position
+ *   pos against a W-slot ring whose slot s holds position
+ *   p(s) = pos - ((pos - s) mod W); slots with p(s) < 0 are empty and skipped.
+ *   Then the same formula as above over the valid slots.
+ *
+ * Inputs arrive in their storage type (dtype code 0 = fp32, 1 = bf16 bit
+ * patterns, 2 = fp64) and are widened to fp64 exactly; all arithmetic is fp64
+ * with libm exp/log.  Layouts: q [B,T,Hq,D], k/v [B,T,Hkv,D], out [B,T,Hq,D],
+ * lse [B,Hq,T]; decode q [B,Hq,D], rings [B,Hkv,W,D], out [B,Hq,D], lse [B,Hq].
+ * Rows are independent; OpenMP spreads them over host threads.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <omp.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
+
+/* Widen element idx of a typed array to double (bf16 -> upper half of fp32). */
+static double widen(const void* base, int dtype, int64_t idx) {
+  if (dtype == ORC_F64) return ((const double*)base)[idx];
+  if (dtype == ORC_F32) return (double)((const float*)base)[idx];
+  uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* One attention row over an explicit list of key rows (indices into k/v).
+ * qoff: element offset of the query vector; koff[n]: element offset of key /
+ * value vector n.  Writes D outputs to o and returns the lse. */
+static double attend_row(const void* q, int64_t qoff, const void* k, const void* v,
+                         const int64_t* koff, int nkeys, double s_h, int D, int dtype,
+                         double* x /* scratch, nkeys */, double* o) {
+  const double inv_sqrt_d = 1.0 / sqrt((double)D);
+  double m = s_h;
+  for (int n = 0; n < nkeys; ++n) {
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d)
+      dot += widen(q, dtype, qoff + d) * widen(k, dtype, koff[n] + d);
+    x[n] = dot * inv_sqrt_d;
+    if (x[n] > m) m = x[n];
+  }
+  double l = exp(s_h - m);
+  for (int d = 0; d < D; ++d) o[d] = 0.0;
+  for (int n = 0; n < nkeys; ++n) {
+    double e = exp(x[n] - m);
+    l += e;
+    for (int d = 0; d < D; ++d) o[d] += e * widen(v, dtype, koff[n] + d);
+  }
+  for (int d = 0; d < D; ++d) o[d] /= l;
+  return m + log(l);
+}
+
+/* One prefill row (b, h, i). */
+static void prefill_row(const void* q, const void* k, const void* v, const double* sink,
+                        int64_t b, int64_t h, int64_t i, int64_t T, int Hq, int Hkv, int D,
+                        int64_t W, int dtype, int64_t* koff, double* x, double* o,
+                        double* lse_out) {
+  const int64_t G = Hq / Hkv;
+  const int64_t kv = h / G;
+  int64_t j0 = i - W + 1;
+  if (j0 < 0) j0 = 0;
+  int n = 0;
+  for (int64_t j = j0; j <= i; ++j) koff[n++] = ((b * T + j) * Hkv + kv) * D;
+  const int64_t qoff = ((b * T + i) * Hq + h) * D;
+  *lse_out = attend_row(q, qoff, k, v, koff, n, sink[h], D, dtype, x, o);
+}
+
+/* Full prefill: every (b, h, i).  out/lse are fp64. */
+int oracle_swa_sink_fwd(const void* q, const void* k, const void* v, const double* sink,
+                        double* out, double* lse, int64_t B, int64_t T, int Hq, int Hkv,
+                        int D, int64_t W, int dtype, int nthreads) {
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || W <= 0) return -1;
+  const int64_t maxk = W < T ? W : T;
+  const int64_t nrows = B * Hq * T;
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
+  {
+    int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (maxk > 0 ? maxk : 1));
+    double* x = (double*)malloc(sizeof(double) * (maxk > 0 ? maxk : 1));
+    double* o = (double*)malloc(sizeof(double) * D);
+    if (!koff || !x || !o) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 64)
+      for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t b = r / (Hq * T), h = (r / T) % Hq, i = r % T;
+        double l;
+        prefill_row(q, k, v, sink, b, h, i, T, Hq, Hkv, D, W, dtype, koff, x, o, &l);
+        memcpy(out + ((b * T + i) * Hq + h) * D, o, sizeof(double) * D);
+        lse[(b * Hq + h) * T + i] = l;
+      }
+    }
+    free(koff); free(x); free(o);
+  }
+  return bad ? -2 : 0;
+}
+
+/* Selected prefill rows: sel holds nsel (b, h, i) triples; out_rows is
+ * [nsel, D], lse_rows [nsel].  Used for sampled checks at full size. */
+int oracle_swa_sink_fwd_rows(const void* q, const void* k, const void* v, const double* sink,
+                             const int64_t* sel, int64_t nsel, double* out_rows,
+                             double* lse_rows, int64_t B, int64_t T, int Hq, int Hkv, int D,
+                             int64_t W, int dtype, int nthreads) {
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || W <= 0) return -1;
+  for (int64_t s = 0; s < nsel; ++s) {
+    const int64_t b = sel[3 * s], h = sel[3 * s + 1], i = sel[3 * s + 2];
+    if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= T) return -1;
+  }
+  const int64_t maxk = W < T ? W : T;
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
+  {
+    int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (maxk > 0 ? maxk : 1));
+    double* x = (double*)malloc(sizeof(double) * (maxk > 0 ? maxk : 1));
+    if (!koff || !x) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t s = 0; s < nsel; ++s) {
+        prefill_row(q, k, v, sink, sel[3 * s], sel[3 * s + 1], sel[3 * s + 2], T, Hq, Hkv, D,
+                    W, dtype, koff, x, out_rows + s * D, &lse_rows[s]);
+      }
+    }
+    free(koff); free(x);
+  }
+  return bad ? -2 : 0;
+}
+
+/* Decode: one query per sequence against a W-slot ring (slot = position mod W). */
+int oracle_swa_sink_decode(const void* q, const void* k_ring, const void* v_ring,
+                           const int64_t* pos, const double* sink, double* out, double* lse,
+                           int64_t B, int Hq, int Hkv, int D, int64_t W, int dtype,
+                           int nthreads) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || W <= 0) return -1;
+  for (int64_t b = 0; b < B; ++b)
+    if (pos[b] < 0) return -1;
+  const int64_t G = Hq / Hkv;
+  const int64_t nrows = B * Hq;
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
+  {
+    int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * W);
+    double* x = (double*)malloc(sizeof(double) * W);
+    if (!koff || !x) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t b = r / Hq, h = r % Hq, kv = h / G;
+        int n = 0;
+        for (int64_t s = 0; s < W; ++s) {
+          const int64_t p = pos[b] - (((pos[b] - s) % W + W) % W); /* mod in [0, W) */
+          if (p < 0) continue;
+          koff[n++] = ((b * Hkv + kv) * W + s) * D;
+        }
+        lse[b * Hq + h] = attend_row(q, (b * Hq + h) * D, k_ring, v_ring, koff, n, sink[h], D,
+                                     dtype, x, out + (b * Hq + h) * D);
+      }
+    }
+    free(koff); free(x);
+  }
+  return bad ? -2 : 0;
+}
+
+int oracle_num_threads(void) { return omp_get_max_threads(); }

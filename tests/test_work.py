@@ -1,0 +1,33 @@
+"""Work accounting: brute-force pair counts and the pages' ~6x reduction claim."""
+import pytest
+
+from hybrid_sliding_window_02_b300 import work
+
+
+@pytest.mark.parametrize("T,W", [(0, 4), (1, 1), (5, 1), (9, 4), (16, 16), (16, 40), (100, 7)])
+def test_window_pairs_brute(T, W):
+    n = sum(1 for i in range(T) for j in range(T) if j <= i and i - j < W)
+    assert work.window_pairs(T, W) == n
+
+
+def test_decode_bytes_full_size():
+    # 256 sequences, Hq=64, Hkv=8, D=128, W=128 bf16 rings, fp32 out + lse
+    assert work.decode_bytes(256, 64, 8, 128, 128, 2) == 146_868_480
+
+
+def test_prefill_work_full_size():
+    assert work.prefill_flops(4, 8192, 64, 128, 128) == 4 * 128 * 4 * 64 * (
+        128 * 129 // 2 + (8192 - 128) * 128)
+    assert work.prefill_bytes(4, 8192, 64, 8, 128, 2) == (
+        4 * 8192 * 80 * 128 * 2 + 256 + 4 * 8192 * 64 * 128 * 4 + 4 * 64 * 8192 * 4)
+
+
+def test_hybrid_reduction_about_six():
+    # "近6倍" (nearly 6x) KV-cache and attention-FLOP reduction at 5:1, W=128
+    f32k, kv32k = work.hybrid_reduction(32768)
+    f256k, kv256k = work.hybrid_reduction(262144)
+    assert 5.7 < f32k < 6.0 and 5.8 < kv32k < 6.0
+    assert 5.9 < f256k < 6.0 and 5.9 < kv256k < 6.0
+    assert f256k > f32k and kv256k > kv32k          # tends to 6 as T grows
+    f, kv = work.hybrid_reduction(10 ** 9)
+    assert abs(f - 6) < 1e-3 and abs(kv - 6) < 1e-3
