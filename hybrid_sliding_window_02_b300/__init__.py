@@ -1,0 +1,203 @@
+"""Sliding-window attention with a per-head attention sink, on B300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libswasink.so`` (declared in
+``include/swasink.h``).  Functions take torch CUDA tensors, check shapes and
+dtypes, and pass raw device pointers, sizes and the current CUDA stream to the
+library; every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library cannot be loaded, calls raise.
+
+Operation ("MiMo-V2-Flash Technical Report" summary, section 前置知识: hybrid
+sliding-window / global attention, a learnable bias added to each head's softmax
+denominator; section 核心方法: 128-token window, 5:1 window:global layers):
+
+    out[b,i,h] = sum_{j in [i-W+1, i], j >= 0} exp(x_ij - m) v[b,j,h//G]
+                 / (exp(sink[h] - m) + sum_j exp(x_ij - m)),   x_ij = q.k / sqrt(D)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import inputs, work  # noqa: F401  (host-only helpers)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libswasink.so")
+
+SWA_OK, SWA_EINVAL, SWA_EUNSUPPORTED, SWA_ECUDA = 0, -1, -2, -3
+SWA_F32, SWA_BF16 = 0, 1
+
+_lib = None
+_lock = threading.Lock()
+
+
+class SwaError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        msg = f"{fn} failed: {status_str(status)} ({status})"
+        if detail:
+            msg += f": {detail}"
+        super().__init__(msg)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libswasink.so (raises if it is missing or cannot be loaded)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m hybrid_sliding_window_02_b300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            p, i32 = ctypes.c_void_p, ctypes.c_int
+            L.swa_sink_fwd.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p]
+            L.swa_sink_decode.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, p]
+            L.swa_ring_append.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, p]
+            for f in (L.swa_sink_fwd, L.swa_sink_decode, L.swa_ring_append):
+                f.restype = i32
+            L.swa_sink_fwd_path.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.swa_sink_fwd_path.restype = ctypes.c_char_p
+            L.swa_status_str.argtypes = [i32]
+            L.swa_status_str.restype = ctypes.c_char_p
+            L.swa_last_error.restype = ctypes.c_char_p
+            L.swa_device_error.restype = i32
+            L.swa_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().swa_status_str(int(status)).decode()
+
+
+def last_error() -> str:
+    return lib().swa_last_error().decode()
+
+
+def device_error() -> int:
+    """Read and clear the device-side error word (synchronises the device)."""
+    return int(lib().swa_device_error())
+
+
+def version() -> int:
+    return int(lib().swa_version())
+
+
+def _check(fn: str, status: int):
+    if status != SWA_OK:
+        raise SwaError(fn, status, last_error())
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SWA_BF16
+    if t.dtype == torch.float32:
+        return SWA_F32
+    raise TypeError(f"unsupported input dtype {t.dtype} (bfloat16 or float32)")
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cuda_contig(name, t, device=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def fwd_path(B, T, Hq, Hkv, D, W, dtype_code=SWA_BF16) -> str:
+    """Name of the prefill kernel the library selects for these sizes."""
+    return lib().swa_sink_fwd_path(B, T, Hq, Hkv, D, W, dtype_code).decode()
+
+
+def swa_sink_fwd(q, k, v, sink, W: int, out=None, lse=None, *, with_lse: bool = True,
+                 stream=None):
+    """Prefill.  q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16 or fp32), sink [Hq] fp32.
+
+    Returns (out [B,T,Hq,D] fp32, lse [B,Hq,T] fp32 or None).  W >= T is the
+    global (full causal) layer.
+    """
+    import torch
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v), ("sink", sink)):
+        _cuda_contig(n, t, dev)
+    if k.shape != (B, T, Hkv, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, T, Hkv, D] matching q")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if sink.dtype != torch.float32 or sink.shape != (Hq,):
+        raise ValueError("sink must be float32 [Hq]")
+    if out is None:
+        out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=dev)
+    if with_lse and lse is None:
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    _cuda_contig("out", out, dev)
+    if lse is not None:
+        _cuda_contig("lse", lse, dev)
+    st = lib().swa_sink_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
+                            out.data_ptr(), lse.data_ptr() if lse is not None else None,
+                            B, T, Hq, Hkv, D, int(W), _dtype_code(q), _stream_handle(stream, dev))
+    _check("swa_sink_fwd", st)
+    return out, lse
+
+
+def swa_sink_decode(q, k_ring, v_ring, pos, sink, out=None, lse=None, *, with_lse=True,
+                    stream=None):
+    """Decode.  q [B,Hq,D], rings [B,Hkv,W,D], pos [B] int64, sink [Hq] fp32.
+
+    Returns (out [B,Hq,D] fp32, lse [B,Hq] fp32 or None).
+    """
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, W, _ = k_ring.shape
+    dev = q.device
+    for n, t in (("q", q), ("k_ring", k_ring), ("v_ring", v_ring), ("pos", pos),
+                 ("sink", sink)):
+        _cuda_contig(n, t, dev)
+    if k_ring.shape != (B, Hkv, W, D) or v_ring.shape != k_ring.shape:
+        raise ValueError("rings must be [B, Hkv, W, D] matching q")
+    if pos.dtype != torch.int64 or pos.shape != (B,):
+        raise ValueError("pos must be int64 [B]")
+    if k_ring.dtype != q.dtype or v_ring.dtype != q.dtype:
+        raise TypeError("q and rings must share one dtype")
+    if sink.dtype != torch.float32 or sink.shape != (Hq,):
+        raise ValueError("sink must be float32 [Hq]")
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
+    if with_lse and lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    st = lib().swa_sink_decode(q.data_ptr(), k_ring.data_ptr(), v_ring.data_ptr(),
+                               pos.data_ptr(), sink.data_ptr(), out.data_ptr(),
+                               lse.data_ptr() if lse is not None else None,
+                               B, Hq, Hkv, D, W, _dtype_code(q), _stream_handle(stream, dev))
+    _check("swa_sink_decode", st)
+    return out, lse
+
+
+def swa_ring_append(k_new, v_new, k_ring, v_ring, pos, *, stream=None):
+    """Write k_new/v_new [B,Hkv,D] into ring slot pos mod W of k_ring/v_ring [B,Hkv,W,D]."""
+    import torch
+    B, Hkv, W, D = k_ring.shape
+    dev = k_ring.device
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_ring", k_ring), ("v_ring", v_ring),
+                 ("pos", pos)):
+        _cuda_contig(n, t, dev)
+    if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or v_ring.shape != k_ring.shape:
+        raise ValueError("shape mismatch between new tokens and rings")
+    if pos.dtype != torch.int64 or pos.shape != (B,):
+        raise ValueError("pos must be int64 [B]")
+    st = lib().swa_ring_append(k_new.data_ptr(), v_new.data_ptr(), k_ring.data_ptr(),
+                               v_ring.data_ptr(), pos.data_ptr(), B, Hkv, D, W,
+                               _dtype_code(k_ring), _stream_handle(stream, dev))
+    _check("swa_ring_append", st)

@@ -1,0 +1,384 @@
+// swasink.cu -- the C ABI of libswasink.so (see include/swasink.h): argument
+// validation, kernel selection, tensor-map construction and launches.
+//
+// One translation unit holds every kernel so that the device error word is a
+// single symbol without relocatable device code.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/swasink.h"
+#include "decode.cuh"
+#include "device_common.cuh"
+#include "simt_fwd.cuh"
+#include "tc_swa.cuh"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+void set_cuda_error(const char* where, cudaError_t e) {
+  snprintf(g_last_error, sizeof g_last_error, "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+}
+
+void set_error_text(const char* text) { snprintf(g_last_error, sizeof g_last_error, "%s", text); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- per-device facts, looked up once ------------------------------------
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  bool tc_attr = false;
+  bool decode_attr[2][2][5] = {};
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) {
+    set_cuda_error("cudaGetDevice", e);
+    return false;
+  }
+  if (*dev < 0 || *dev >= kMaxDevices) {
+    set_error_text("device index out of range");
+    return false;
+  }
+  return true;
+}
+
+bool device_sms(int dev, int* sms) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev[dev].ready) {
+    int n = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      set_cuda_error("cudaDeviceGetAttribute", e);
+      return false;
+    }
+    g_dev[dev].sms = n;
+    g_dev[dev].ready = true;
+  }
+  *sms = g_dev[dev].sms;
+  return true;
+}
+
+// ---- cuTensorMapEncodeTiled through the runtime's driver entry point ------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D row-major tensor [d3][d2][d1][d0] (d0 innermost), 128-byte swizzle.
+bool make_map_4d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+                 uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3, uint32_t b0, uint32_t b1,
+                 uint32_t b2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error_text("cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
+  const cuuint64_t dims[4] = {d0, d1, d2, d3};
+  const cuuint64_t strides[3] = {d0 * esize, d0 * d1 * esize, d0 * d1 * d2 * esize};
+  const cuuint32_t box[4] = {b0, b1, b2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return false;
+  }
+  return true;
+}
+
+swa_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_cuda_error(what, e);
+    return SWA_ECUDA;
+  }
+  return SWA_OK;
+}
+
+enum FwdPath { kPathInvalid, kPathSimt, kPathTcSwa };
+
+FwdPath select_fwd(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype dt) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return kPathInvalid;
+  if (dt != SWA_F32 && dt != SWA_BF16) return kPathInvalid;
+  if (D != 64 && D != 128) return kPathInvalid;
+  const int G = Hq / Hkv;
+  if (dt == SWA_BF16 && D == swa::tcswa::kD && G == swa::tcswa::kG && W <= swa::tcswa::kMaxW)
+    return kPathTcSwa;
+  return kPathSimt;
+}
+
+template <typename Tin>
+swa_status launch_simt(const void* q, const void* k, const void* v, const float* sink, float* out,
+                       float* lse, int B, int T, int Hq, int Hkv, int D, int W,
+                       cudaStream_t st) {
+  const long long rows = (long long)B * T * Hq;
+  const int warps_per_block = 8;
+  const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
+  if (blocks > 0x7fffffffLL) {
+    set_error_text("problem too large for the general kernel");
+    return SWA_EUNSUPPORTED;
+  }
+  const float scale = (float)(1.0 / std::sqrt((double)D));
+  const Tin* qq = static_cast<const Tin*>(q);
+  const Tin* kk = static_cast<const Tin*>(k);
+  const Tin* vv = static_cast<const Tin*>(v);
+  if (D == 64)
+    swa::simt_fwd_kernel<Tin, 64><<<(unsigned)blocks, warps_per_block * 32, 0, st>>>(
+        qq, kk, vv, sink, out, lse, B, T, Hq, Hkv, W, scale);
+  else
+    swa::simt_fwd_kernel<Tin, 128><<<(unsigned)blocks, warps_per_block * 32, 0, st>>>(
+        qq, kk, vv, sink, out, lse, B, T, Hq, Hkv, W, scale);
+  return check_launch("simt_fwd_kernel");
+}
+
+swa_status launch_tc_swa(const void* q, const void* k, const void* v, const float* sink,
+                         float* out, float* lse, int B, int T, int Hq, int Hkv, int W,
+                         cudaStream_t st) {
+  using namespace swa::tcswa;
+  int dev, sms;
+  if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev[dev].tc_attr) {
+      cudaError_t e = cudaFuncSetAttribute(swa_fwd_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+      if (e != cudaSuccess) {
+        set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_kernel)", e);
+        return SWA_ECUDA;
+      }
+      g_dev[dev].tc_attr = true;
+    }
+  }
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, T, B, 64, kG, kNpos) ||
+      !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, kD, Hkv, T, B, 64, 1, kBlk) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, kD, Hkv, T, B, 64, 1, kBlk) ||
+      !make_map_4d(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, kD, Hq, T, B, 32, kG, kNpos))
+    return SWA_ECUDA;
+  Params p;
+  p.sink = sink;
+  p.lse = lse;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.W = W;
+  p.ntiles_seq = (T + kNpos - 1) / kNpos;
+  p.total_tiles = (long long)B * Hkv * p.ntiles_seq;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  const long long grid = p.total_tiles < sms ? p.total_tiles : sms;
+  swa_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mo, p);
+  return check_launch("swa_fwd_tc_kernel");
+}
+
+template <typename Tin, int D, int G>
+swa_status launch_decode_t(const void* q, const void* kr, const void* vr, const int64_t* pos,
+                           const float* sink, float* out, float* lse, int B, int Hq, int Hkv,
+                           int W, cudaStream_t st, bool* attr_done) {
+  const swa::DecodeSmem L = swa::decode_smem_layout<Tin, D, G>(W);
+  auto kern = swa::decode_kernel<Tin, D, G>;
+  if (!*attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) {
+      set_cuda_error("cudaFuncSetAttribute(decode_kernel)", e);
+      return SWA_ECUDA;
+    }
+    *attr_done = true;
+  }
+  const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  kern<<<(unsigned)(B * Hkv), swa::kDecodeThreads, L.total, st>>>(
+      static_cast<const Tin*>(q), static_cast<const Tin*>(kr), static_cast<const Tin*>(vr), pos,
+      sink, out, lse, Hq, Hkv, W, scale_log2);
+  return check_launch("decode_kernel");
+}
+
+template <typename Tin, int D>
+swa_status launch_decode_g(const void* q, const void* kr, const void* vr, const int64_t* pos,
+                           const float* sink, float* out, float* lse, int B, int Hq, int Hkv,
+                           int W, cudaStream_t st, int dev) {
+  const int G = Hq / Hkv;
+  const int ti = std::is_same<Tin, float>::value ? 0 : 1;
+  const int di = D == 64 ? 0 : 1;
+  bool* attr = nullptr;
+  int gi;
+  switch (G) {
+    case 1: gi = 0; break;
+    case 2: gi = 1; break;
+    case 4: gi = 2; break;
+    case 8: gi = 3; break;
+    case 16: gi = 4; break;
+    default:
+      set_error_text("decode supports Hq/Hkv in {1, 2, 4, 8, 16}");
+      return SWA_EUNSUPPORTED;
+  }
+  bool done;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    done = g_dev[dev].decode_attr[ti][di][gi];
+  }
+  attr = &done;
+  swa_status s;
+  switch (G) {
+    case 1: s = launch_decode_t<Tin, D, 1>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
+    case 2: s = launch_decode_t<Tin, D, 2>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
+    case 4: s = launch_decode_t<Tin, D, 4>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
+    case 8: s = launch_decode_t<Tin, D, 8>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
+    default: s = launch_decode_t<Tin, D, 16>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
+  }
+  if (done) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    g_dev[dev].decode_attr[ti][di][gi] = true;
+  }
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+swa_status swa_sink_fwd(const void* q, const void* k, const void* v, const float* sink,
+                        float* out, float* lse, int B, int T, int Hq, int Hkv, int D, int W,
+                        swa_dtype in_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k || !v || !sink || !out) return SWA_EINVAL;
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return SWA_EINVAL;
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (lse && !aligned16(lse)))
+    return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (select_fwd(B, T, Hq, Hkv, D, W, in_dtype)) {
+    case kPathTcSwa:
+      return launch_tc_swa(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, st);
+    case kPathSimt:
+      if (in_dtype == SWA_F32)
+        return launch_simt<float>(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, st);
+      return launch_simt<__nv_bfloat16>(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, st);
+    default:
+      return SWA_EINVAL;
+  }
+}
+
+swa_status swa_sink_decode(const void* q, const void* k_ring, const void* v_ring,
+                           const int64_t* pos, const float* sink, float* out, float* lse, int B,
+                           int Hq, int Hkv, int D, int W, swa_dtype in_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k_ring || !v_ring || !pos || !sink || !out) return SWA_EINVAL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return SWA_EINVAL;
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
+  if (!aligned16(q) || !aligned16(k_ring) || !aligned16(v_ring) || !aligned16(out) ||
+      (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(pos) & 7u))
+    return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  const int esz = in_dtype == SWA_F32 ? 4 : 2;
+  if (2LL * W * D * esz > swa::kDecodeMaxRingBytes) return SWA_EUNSUPPORTED;
+  if ((long long)B * Hkv > 0x7fffffffLL) return SWA_EUNSUPPORTED;
+  int dev;
+  if (!current_device(&dev)) return SWA_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (in_dtype == SWA_F32) {
+    if (D == 64)
+      return launch_decode_g<float, 64>(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, W, st, dev);
+    return launch_decode_g<float, 128>(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, W, st, dev);
+  }
+  if (D == 64)
+    return launch_decode_g<__nv_bfloat16, 64>(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, W, st, dev);
+  return launch_decode_g<__nv_bfloat16, 128>(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, W, st, dev);
+}
+
+swa_status swa_ring_append(const void* k_new, const void* v_new, void* k_ring, void* v_ring,
+                           const int64_t* pos, int B, int Hkv, int D, int W, swa_dtype dtype,
+                           void* stream) {
+  g_last_error[0] = '\0';
+  if (!k_new || !v_new || !k_ring || !v_ring || !pos) return SWA_EINVAL;
+  if (B < 1 || Hkv < 1 || D < 1 || W < 1) return SWA_EINVAL;
+  if (dtype != SWA_F32 && dtype != SWA_BF16) return SWA_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_ring) || !aligned16(v_ring) ||
+      (reinterpret_cast<uintptr_t>(pos) & 7u))
+    return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int esz = dtype == SWA_F32 ? 4 : 2;
+  const long long total = (long long)B * Hkv * (D * esz / 16);
+  const long long blocks_ll = (total + 255) / 256;
+  const unsigned blocks = (unsigned)(blocks_ll < 4096 ? blocks_ll : 4096);
+  if (dtype == SWA_F32)
+    swa::ring_append_kernel<float><<<blocks, 256, 0, st>>>(
+        static_cast<const float*>(k_new), static_cast<const float*>(v_new),
+        static_cast<float*>(k_ring), static_cast<float*>(v_ring), pos, B, Hkv, D, W);
+  else
+    swa::ring_append_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+        static_cast<__nv_bfloat16*>(k_ring), static_cast<__nv_bfloat16*>(v_ring), pos, B, Hkv,
+        D, W);
+  return check_launch("ring_append_kernel");
+}
+
+const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype) {
+  switch (select_fwd(B, T, Hq, Hkv, D, W, in_dtype)) {
+    case kPathTcSwa: return "tc_swa";
+    case kPathSimt: return "simt";
+    default: return "invalid";
+  }
+}
+
+const char* swa_status_str(swa_status s) {
+  switch (s) {
+    case SWA_OK: return "ok";
+    case SWA_EINVAL: return "invalid argument";
+    case SWA_EUNSUPPORTED: return "unsupported configuration";
+    case SWA_ECUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* swa_last_error(void) { return g_last_error; }
+
+int swa_device_error(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    set_cuda_error("cudaDeviceSynchronize", e);
+    return SWA_ECUDA;
+  }
+  unsigned int v = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&v, swa::g_dev_error, sizeof v);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(swa::g_dev_error, &zero, sizeof zero);
+  if (e != cudaSuccess) {
+    set_cuda_error("device error word", e);
+    return SWA_ECUDA;
+  }
+  return (int)v;
+}
+
+int swa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+"""Shared helpers for the GPU parity tests: tolerances and oracle-on-slices."""
+import numpy as np
+import torch
+
+import oracle
+
+# Tolerances stated for this operation: bf16 inputs with fp32 accumulation to
+# max-abs <= 2e-2 and mean-abs <= 2e-3 on the output; LSE to 1e-3 absolute;
+# fp32 paths to 1e-5 relative (read normwise: max|err| / max|ref|).
+BF16_MAX_ABS = 2e-2
+BF16_MEAN_ABS = 2e-3
+LSE_ABS = 1e-3
+F32_REL = 1e-5
+
+
+def assert_bf16_close(got, ref, what="out"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = np.abs(got - ref)
+    assert err.max() <= BF16_MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= BF16_MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
+
+
+def assert_lse_close(got, ref, tol=LSE_ABS):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), "lse: non-finite values"
+    err = np.abs(got - ref).max()
+    assert err <= tol, f"lse: max abs err {err:.3e}"
+
+
+def assert_f32_close(got, ref, what="out", tol=F32_REL):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rel = np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
+    assert rel <= tol, f"{what}: normwise rel err {rel:.3e}"
+
+
+def oracle_rows_from_slices(q, k, v, sink, W, rows):
+    """Oracle values for selected rows (b, h, i) of a large problem.
+
+    Each row depends only on keys/values in [max(0, i-W+1), i] of its batch
+    entry, so the oracle runs on that slice alone (copied to the host), which
+    gives exactly the same result as running it on the whole input.
+    Returns (out [n, D], lse [n]) in fp64, in the order of ``rows``.
+    """
+    n = len(rows)
+    D = q.shape[-1]
+    out = np.zeros((n, D))
+    lse = np.zeros(n)
+    groups = {}
+    for idx, (b, h, i) in enumerate(rows):
+        groups.setdefault((int(b), int(i)), []).append((idx, int(h)))
+    sink_c = sink.detach().cpu()
+    for (b, i), members in groups.items():
+        j0 = max(0, i - W + 1)
+        L = i - j0 + 1
+        # the oracle reads only query row i: leave the other rows zero
+        qs = torch.zeros((1, L) + tuple(q.shape[2:]), dtype=q.dtype)
+        qs[0, L - 1] = q[b, i].cpu()
+        ks = k[b:b + 1, j0:i + 1].cpu()
+        vs = v[b:b + 1, j0:i + 1].cpu()
+        sel = [[0, h, L - 1] for _, h in members]
+        o, l = oracle.swa_sink_fwd_rows(qs, ks, vs, sink_c, W, sel)
+        for m, (idx, _) in enumerate(members):
+            out[idx] = o[m]
+            lse[idx] = l[m]
+    return out, lse
+
+
+def gather_rows(out, lse, rows):
+    """Kernel outputs at the selected rows, as fp64 numpy arrays."""
+    idx_b = torch.tensor([r[0] for r in rows])
+    idx_h = torch.tensor([r[1] for r in rows])
+    idx_i = torch.tensor([r[2] for r in rows])
+    o = out[idx_b.to(out.device), idx_i.to(out.device), idx_h.to(out.device)]
+    l = lse[idx_b.to(lse.device), idx_h.to(lse.device), idx_i.to(lse.device)]
+    return o.double().cpu().numpy(), l.double().cpu().numpy()
+
+
+def sample_rows(B, T, Hq, n_pos, seed, extra_pos=(), heads=None):
+    """Deterministic sample of (b, h, i): chosen positions with all (or given) heads."""
+    g = np.random.default_rng(seed)
+    pos = set(int(p) for p in extra_pos if 0 <= p < T)
+    pos |= {0, 1, 15, 16, 127, 128, 129, T - 1, T - 2, T - 17}
+    pos = {p for p in pos if 0 <= p < T}
+    while len(pos) < n_pos and len(pos) < T:
+        pos.add(int(g.integers(0, T)))
+    hs = list(range(Hq)) if heads is None else list(heads)
+    rows = []
+    for i in sorted(pos):
+        b = int(g.integers(0, B))
+        for h in hs:
+            rows.append((b, h, i))
+    return rows

@@ -1,0 +1,108 @@
+"""The C-ABI library without a GPU: it loads, exports what the header declares,
+and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import hybrid_sliding_window_02_b300 as swa
+from hybrid_sliding_window_02_b300 import build as swabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swasink.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    swabuild.build()
+    return swa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("swa_sink_fwd", "swa_sink_decode", "swa_ring_append", "swa_status_str"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    assert swa.status_str(swa.SWA_OK) == "ok"
+    assert swa.status_str(swa.SWA_EINVAL) == "invalid argument"
+    assert swa.status_str(swa.SWA_EUNSUPPORTED) == "unsupported configuration"
+    assert swa.status_str(swa.SWA_ECUDA) == "CUDA error"
+    assert swa.version() >= 100
+
+
+def test_path_selection(L):
+    assert swa.fwd_path(4, 8192, 64, 8, 128, 128) == "tc_swa"
+    assert swa.fwd_path(1, 262144, 64, 8, 128, 128) == "tc_swa"
+    assert swa.fwd_path(1, 512, 4, 1, 64, 128, swa.SWA_F32) == "simt"
+    assert swa.fwd_path(1, 512, 64, 8, 128, 128, swa.SWA_F32) == "simt"
+    assert swa.fwd_path(1, 512, 64, 64, 128, 128) == "simt"
+    assert swa.fwd_path(1, 512, 64, 7, 128, 128) == "invalid"
+    assert swa.fwd_path(1, 512, 64, 8, 96, 128) == "invalid"
+    assert swa.fwd_path(0, 512, 64, 8, 128, 128) == "invalid"
+
+
+A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced by these calls
+
+
+def _fwd(L, q=A, k=A, v=A, sink=A, out=A, lse=A, B=1, T=16, Hq=8, Hkv=8, D=128, W=4, dt=1):
+    return L.swa_sink_fwd(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, dt, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1), (dict(k=None), -1), (dict(v=None), -1), (dict(sink=None), -1),
+    (dict(out=None), -1), (dict(B=0), -1), (dict(T=0), -1), (dict(Hq=0), -1),
+    (dict(Hkv=0), -1), (dict(Hq=8, Hkv=3), -1), (dict(W=0), -1), (dict(W=-5), -1),
+    (dict(dt=7), -1), (dict(q=A + 8), -1), (dict(out=A + 4), -1), (dict(lse=A + 2), -1),
+    (dict(D=96), -2), (dict(D=256), -2),
+])
+def test_fwd_rejects_before_launch(L, kw, status):
+    assert _fwd(L, **kw) == status
+
+
+def _dec(L, q=A, kr=A, vr=A, pos=A, sink=A, out=A, lse=A, B=2, Hq=8, Hkv=1, D=128, W=128, dt=1):
+    return L.swa_sink_decode(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, D, W, dt, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1), (dict(kr=None), -1), (dict(vr=None), -1), (dict(pos=None), -1),
+    (dict(sink=None), -1), (dict(out=None), -1), (dict(B=0), -1), (dict(Hq=6, Hkv=4), -1),
+    (dict(W=0), -1), (dict(pos=A + 4), -1), (dict(kr=A + 8), -1), (dict(D=32), -2),
+    (dict(W=321), -2), (dict(W=161, dt=0), -2),
+])
+def test_decode_rejects_before_launch(L, kw, status):
+    assert _dec(L, **kw) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, A, A, A, A, 1, 1, 128, 8, 1), -1),
+    ((A, A, A, A, None, 1, 1, 128, 8, 1), -1),
+    ((A, A, A, A, A, 0, 1, 128, 8, 1), -1),
+    ((A, A, A, A, A, 1, 1, 128, 0, 1), -1),
+    ((A, A, A + 4, A, A, 1, 1, 128, 8, 1), -1),
+    ((A, A, A, A, A, 1, 1, 48, 8, 1), -2),
+])
+def test_ring_append_rejects_before_launch(L, args, status):
+    assert L.swa_ring_append(*args, None) == status
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import importlib
+    mod = importlib.import_module("hybrid_sliding_window_02_b300")
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        mod.lib()

@@ -1,0 +1,107 @@
+"""GPU decode and ring-append parity against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import hybrid_sliding_window_02_b300 as swa
+from hybrid_sliding_window_02_b300 import inputs as gen
+from gpu_helpers import assert_bf16_close, assert_f32_close, assert_lse_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode(x):
+    args = [t.cuda() for t in (x.q, x.k_ring, x.v_ring, x.pos, x.sink)]
+    out, lse = swa.swa_sink_decode(*args)
+    torch.cuda.synchronize()
+    return out.cpu().double().numpy(), lse.cpu().double().numpy()
+
+
+def test_decode_full_size_workload(cuda_ok):
+    # 256 sequences at positions U[128, 262144), Hq=64, Hkv=8, D=128, W=128 ring
+    x = gen.decode_inputs(256, 64, 8, 128, 128, seed=0)
+    o, l = _decode(x)
+    o_ref, l_ref = oracle.swa_sink_decode(x.q, x.k_ring, x.v_ring, x.pos, x.sink)
+    assert_bf16_close(o, o_ref)
+    assert_lse_close(l, l_ref)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,W,dt", [
+    (3, 8, 1, 128, 128, torch.bfloat16), (5, 16, 1, 64, 64, torch.bfloat16),
+    (4, 4, 2, 128, 33, torch.bfloat16), (2, 16, 16, 64, 7, torch.bfloat16),
+    (3, 8, 1, 128, 128, torch.float32), (2, 4, 4, 64, 300, torch.float32),
+])
+def test_decode_shapes(cuda_ok, B, Hq, Hkv, D, W, dt):
+    x = gen.decode_inputs(B, Hq, Hkv, D, W, seed=B + W, dtype=dt, pos_lo=0, pos_hi=4 * W)
+    o, l = _decode(x)
+    o_ref, l_ref = oracle.swa_sink_decode(x.q, x.k_ring, x.v_ring, x.pos, x.sink)
+    if dt == torch.float32:
+        assert_f32_close(o, o_ref)
+        assert_f32_close(l, l_ref, what="lse")
+    else:
+        assert_bf16_close(o, o_ref)
+        assert_lse_close(l, l_ref)
+
+
+def test_decode_empty_slots_ignored_even_if_nan(cuda_ok):
+    W = 128
+    x = gen.decode_inputs(6, 64, 8, 128, W, seed=3, pos_lo=0, pos_hi=W - 1)
+    ref = _decode(x)
+    for b in range(6):
+        p = int(x.pos[b])
+        x.k_ring[b, :, p + 1:] = float("nan")
+        x.v_ring[b, :, p + 1:] = float("nan")
+    got = _decode(x)
+    assert np.all(np.isfinite(got[0])) and np.all(np.isfinite(got[1]))
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+    o_ref, l_ref = oracle.swa_sink_decode(x.q, x.k_ring, x.v_ring, x.pos, x.sink)
+    assert_bf16_close(got[0], o_ref)
+    assert_lse_close(got[1], l_ref)
+
+
+def test_ring_append_bit_exact(cuda_ok):
+    B, Hkv, W, D = 7, 8, 128, 128
+    g = torch.Generator().manual_seed(4)
+    kr = torch.randn(B, Hkv, W, D, generator=g).to(torch.bfloat16)
+    vr = torch.randn(B, Hkv, W, D, generator=g).to(torch.bfloat16)
+    kn = torch.randn(B, Hkv, D, generator=g).to(torch.bfloat16)
+    vn = torch.randn(B, Hkv, D, generator=g).to(torch.bfloat16)
+    pos = torch.tensor([0, 1, 127, 128, 129, 262143, -1], dtype=torch.int64)
+    kr_d, vr_d = kr.cuda(), vr.cuda()
+    swa.swa_ring_append(kn.cuda(), vn.cuda(), kr_d, vr_d, pos.cuda())
+    torch.cuda.synchronize()
+    for b in range(B):
+        p = int(pos[b])
+        if p >= 0:
+            kr[b, :, p % W] = kn[b]
+            vr[b, :, p % W] = vn[b]
+    assert torch.equal(kr_d.cpu(), kr) and torch.equal(vr_d.cpu(), vr)
+
+
+def test_decode_after_appends_equals_prefill_row(cuda_ok):
+    # feed a history token by token through the ring; decode at every step
+    # must match the prefill row at that position (positions only grow)
+    B, T, Hq, Hkv, D, W = 2, 200, 16, 2, 128, 128
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=11, device="cuda")
+    out_pre, lse_pre = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+    kr = torch.full((B, Hkv, W, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vr = torch.full_like(kr, float("nan"))
+    worst = 0.0
+    for t in range(T):
+        pos = torch.full((B,), t, dtype=torch.int64, device="cuda")
+        swa.swa_ring_append(x.k[:, t].contiguous(), x.v[:, t].contiguous(), kr, vr, pos)
+        o, l = swa.swa_sink_decode(x.q[:, t].contiguous(), kr, vr, pos, x.sink)
+        worst = max(worst, (o - out_pre[:, t]).abs().max().item())
+        assert torch.isfinite(o).all()
+        assert (l - lse_pre[:, :, t]).abs().max().item() < 1e-3
+    torch.cuda.synchronize()
+    assert worst < 2e-2
+    # and the last step against the oracle
+    o_ref, l_ref = oracle.swa_sink_fwd_rows(x.q.cpu(), x.k.cpu(), x.v.cpu(), x.sink.cpu(), W,
+                                            [[b, h, T - 1] for b in range(B) for h in range(Hq)])
+    assert_bf16_close(o.cpu().double().numpy().reshape(-1, D), o_ref)
+
+
+def test_decode_no_device_error(cuda_ok):
+    assert swa.device_error() == 0
