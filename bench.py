@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark: sliding-window + sink attention on B300.
+
+One step = one sliding-window prefill call over the B=4, T=8192, Hq=64, Hkv=8,
+D=128, W=128 workload (bf16 q/k/v, fp32 sink, fp32 out + per-row LSE), inputs
+resident in HBM.  ``value`` is algorithmic TFLOP/s (only in-window query/key
+pairs count, 4*D FLOPs each).  The same JSON line also carries the ring-buffer
+decode measurement (256 sequences, W=128, GB/s of algorithmic bytes), the
+roofline of each kernel against the measured peaks, the end-to-end number
+through host buffers, the CPU oracle baseline and the SM clocks seen.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (the only reference for this
+operation) on the host cores, on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs its own replica (no data exchange);
+time is the max over ranks and ``value`` the total over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from hybrid_sliding_window_02_b300 import inputs as gen  # noqa: E402
+from hybrid_sliding_window_02_b300 import work  # noqa: E402
+
+METRIC = "SWA+sink prefill TFLOP/s & decode GB/s on 1 B300, as % of roofline vs CPU oracle"
+PREFILL = dict(B=4, T=8192, Hq=64, Hkv=8, D=128, W=128)
+DECODE = dict(B=256, Hq=64, Hkv=8, D=128, W=128)
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+KERNEL_SOURCES = ("csrc/tc_swa.cuh", "csrc/decode.cuh", "csrc/device_common.cuh")
+
+
+def workload_name(c):
+    return (f"swa_sink_prefill B{c['B']} T{c['T']} Hq{c['Hq']} Hkv{c['Hkv']} D{c['D']} "
+            f"W{c['W']} bf16->fp32+lse")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local_rank])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return reduce_value(self.pg, x, "max")
+
+    def sum(self, x: float) -> float:
+        return reduce_value(self.pg, x, "sum")
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def reduce_value(pg, x: float, op: str) -> float:
+    """Reduce a float over ranks (identity without a process group)."""
+    if pg is None:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if (
+        torch.cuda.is_available() and pg.get_backend() == "nccl") else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX if op == "max" else pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML in a thread."""
+
+    REASONS = {
+        "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+    }
+
+    def __init__(self, device_index: int, period_s: float = 0.02):
+        self.idx = device_index
+        self.period = period_s
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = None
+            try:  # match the CUDA device to its NVML handle by UUID
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+                self._h = pynvml.nvmlDeviceGetHandleByUUID(
+                    uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            except Exception:
+                self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) \
+                or getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:  # NVML missing: report no clocks
+            self._nv = None
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                mask = self._reasons_fn(self._h)
+                for name, bit in self.REASONS.items():
+                    if mask & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# peaks, traffic records
+# ---------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "hybrid_sliding_window_02_b300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if absent
+    or taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#") or ":" not in line:
+                continue
+            key, val = line.split(":", 1)
+            rec[key.strip()] = val.strip()
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    val = rec.get(f"{kernel}.bytes_per_launch")
+    return int(float(val)) if val else None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+def oracle_rows_rate(q, k, v, sink, W, i0, ts):
+    """Run the fp64 oracle on rows i0..i0+ts-1 (all heads) of batch entry 0 and
+    return (seconds, FLOPs, rows).  Only the key range those rows read is
+    copied to the host."""
+    import oracle
+    Hq, D = q.shape[2], q.shape[3]
+    j0 = max(0, i0 - W + 1)
+    qs, ks, vs = (x[0:1, j0:i0 + ts].cpu() for x in (q, k, v))
+    rows = [[0, h, i - j0] for i in range(i0, i0 + ts) for h in range(Hq)]
+    t0 = time.perf_counter()
+    oracle.swa_sink_fwd_rows(qs, ks, vs, sink.cpu(), W, rows)
+    dt = time.perf_counter() - t0
+    npairs = sum(min(i + 1, W) for i in range(i0, i0 + ts))
+    return dt, 4 * D * Hq * npairs, len(rows)
+
+
+def cpu_oracle_sample(q, k, v, sink, W, target_s=12.0):
+    """Time the fp64 oracle on consecutive full-window rows of batch entry 0
+    (all heads), sized for about target_s seconds of host work."""
+    import oracle
+    nthr = oracle.num_threads()
+    T, Hq = q.shape[1], q.shape[2]
+    i0 = min(W, T - 1)
+    ts = min(T - i0, 16)
+    dt, flops, nrows = oracle_rows_rate(q, k, v, sink, W, i0, ts)
+    while dt < target_s / 4 and ts < T - i0:
+        ts = min(T - i0, int(ts * max(2.0, min(8.0, target_s / max(dt, 1e-3) / 2))))
+        dt, flops, nrows = oracle_rows_rate(q, k, v, sink, W, i0, ts)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": nthr, "kind": "oracle",
+            "sample": f"batch entry 0, positions {i0}..{i0 + ts - 1}, all {Hq} heads "
+                      f"({nrows} rows, {flops:.3e} FLOP) in {dt:.2f} s"}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def time_prefill(swa, x, c, steps, warmup, dist, stream):
+    B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
+    out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=x.q.device)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=x.q.device)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for s in range(steps):
+            ev[s][0].record(stream)
+            swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
+            ev[s][1].record(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    total_ms = e0.elapsed_time(e1)
+    per_launch_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    return total_ms, per_launch_ms
+
+
+def time_decode(swa, c, steps, warmup, dev, stream, nsets=4):
+    """Decode calls rotating over input sets whose total exceeds L2."""
+    B, Hq, Hkv, D, W = (c[k] for k in ("B", "Hq", "Hkv", "D", "W"))
+    sets = [gen.decode_inputs(B, Hq, Hkv, D, W, seed=100 + i, device=dev) for i in range(nsets)]
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(warmup * nsets):
+            d = sets[i % nsets]
+            swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink, out, lse, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            d = sets[i % nsets]
+            swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink, out, lse, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def time_e2e(swa, xh, c, steps, dev, stream):
+    """Host (pinned) inputs -> device -> prefill -> host outputs, every step."""
+    B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
+    qd = torch.empty_like(xh.q, device=dev)
+    kd = torch.empty_like(xh.k, device=dev)
+    vd = torch.empty_like(xh.v, device=dev)
+    sd = torch.empty_like(xh.sink, device=dev)
+    out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    out_h = torch.empty(out.shape, dtype=torch.float32, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
+
+    def step():
+        qd.copy_(xh.q, non_blocking=True)
+        kd.copy_(xh.k, non_blocking=True)
+        vd.copy_(xh.v, non_blocking=True)
+        sd.copy_(xh.sink, non_blocking=True)
+        swa.swa_sink_fwd(qd, kd, vd, sd, W, out, lse, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in (xh.q, xh.k, xh.v, xh.sink))
+    d2h = out.numel() * 4 + lse.numel() * 4
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def run_ours(args, dist):
+    import hybrid_sliding_window_02_b300 as swa
+    swa.lib()
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    c = dict(PREFILL, B=args.prefill[0], T=args.prefill[1])
+    x = gen.prefill_inputs(c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], seed=0, device=dev)
+    flops = work.prefill_flops(c["B"], c["T"], c["Hq"], c["D"], c["W"])
+    nbytes = work.prefill_bytes(c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], 2)
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+
+    with ClockSampler(dev.index) as clk:
+        total_ms, launch_ms = time_prefill(swa, x, c, args.steps, args.warmup, dist, stream)
+    total_ms = dist.max(total_ms)
+    ms_per_step = total_ms / args.steps
+    value = dist.sum(flops * args.steps) / (total_ms * 1e-3) / 1e12
+
+    dec_us = time_decode(swa, DECODE, args.decode_steps, 3, dev, stream) * 1e3
+    dec_bytes = work.decode_bytes(DECODE["B"], DECODE["Hq"], DECODE["Hkv"], DECODE["D"],
+                                  DECODE["W"], 2)
+    dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(c), "seed": 0,
+                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step)",
+                   "parallelism": f"replicas x{dist.world}"},
+        "roofline": {
+            "kernel": "swa_fwd_tc_kernel", "bound": "hbm",
+            "achieved": round(nbytes / (launch_ms * 1e-3) / 1e9, 1),
+            "peak": hbm, "unit": "GB/s",
+            "frac": round(nbytes / (launch_ms * 1e-3) / 1e9 / hbm, 4),
+            "peak_source": f"{peak_src} hbm_gbs",
+            "algorithmic_bytes_per_launch": nbytes,
+            "launch_ms": round(launch_ms, 4),
+            "traffic": recorded_traffic("swa_fwd_tc_kernel"),
+            "tflops": round(flops / (launch_ms * 1e-3) / 1e12, 2),
+            "tensor_peak_frac": round(flops / (launch_ms * 1e-3) / 1e12
+                                      / float(peaks["bf16_tflops"]), 4),
+        },
+        "decode": {
+            "workload": "swa_sink_decode B256 Hq64 Hkv8 D128 W128 ring, bf16->fp32+lse, "
+                        "4 rotating input sets (550 MB)",
+            "value": round(dec_gbs, 1), "unit": "GB/s", "us_per_call": round(dec_us, 2),
+            "roofline": {"kernel": "decode_kernel", "bound": "hbm",
+                         "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(dec_gbs / hbm, 4),
+                         "algorithmic_bytes_per_launch": dec_bytes,
+                         "traffic": recorded_traffic("decode_kernel")},
+        },
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e:
+        xh = gen.PrefillInputs(*(t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.sink)))
+        e2e_ms, h2d, d2h = time_e2e(swa, xh, c, max(3, args.steps // 50), dev, stream)
+        e2e_ms = dist.max(e2e_ms)
+        line["e2e"] = {"value": round(dist.sum(flops) / (e2e_ms * 1e-3) / 1e12, 3),
+                       "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e2e_ms, 3)}
+        del xh
+    if dist.rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_oracle_sample(x.q, x.k, x.v, x.sink, c["W"],
+                                                 target_s=args.cpu_seconds)
+    if swa.device_error() != 0:
+        line["device_error"] = True
+    return line
+
+
+def run_reference(args, dist):
+    """The fp64 CPU oracle, timed on the host cores, on bounded samples."""
+    if dist.rank != 0:
+        return None
+    c = PREFILL
+    # same recipe as the GPU arm's workload, first 2048 positions of one sequence
+    x = gen.prefill_inputs(1, 2048, c["Hq"], c["Hkv"], c["D"], seed=0)
+    import oracle
+    oracle.build()
+    nthr = oracle.num_threads()
+    ts, i0 = 24, 1024  # full-window rows per step: about a second of host work
+    for s in range(args.warmup):
+        oracle_rows_rate(x.q, x.k, x.v, x.sink, c["W"], i0, ts)
+    tot, flops = 0.0, 0
+    for s in range(args.steps):
+        dt, f, _ = oracle_rows_rate(x.q, x.k, x.v, x.sink, c["W"], i0, ts)
+        tot += dt
+        flops = f
+    dt = tot / args.steps
+    value = flops / dt / 1e12
+    sample = (f"per step: one sequence of the workload, positions {i0}..{i0 + ts - 1}, "
+              f"all {c['Hq']} heads "
+              f"({flops:.3e} FLOP)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(c), "seed": 0, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthr, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--decode-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--prefill", type=int, nargs=2, metavar=("B", "T"),
+                    default=(PREFILL["B"], PREFILL["T"]),
+                    help="prefill batch and length (default: the headline workload); other "
+                         "values are for profiling small cases")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    dist = Dist()
+    try:
+        line = run_reference(args, dist) if args.impl == "reference" else run_ours(args, dist)
+        if dist.rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()
