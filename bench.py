@@ -99,12 +99,17 @@ def reduce_value(pg, x: float, op: str) -> float:
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML in a thread."""
+    """Samples the SM clock and clock-event (throttle) reasons while the timed
+    region runs: through NVML in a thread, or, if NVML is unavailable, from an
+    ``nvidia-smi -lms`` subprocess."""
 
     REASONS = {
         "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
         "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
     }
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown")
 
     def __init__(self, device_index: int, period_s: float = 0.02):
         self.idx = device_index
@@ -112,28 +117,33 @@ class ClockSampler:
         self.samples = []
         self.reasons = set()
         self.max_mhz = None
+        self.source = None
+        self.error = None
         self._stop = threading.Event()
         self._thread = None
-        self.ok = False
+        self._proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nv = pynvml
-            self._h = None
+            h = None
             try:  # match the CUDA device to its NVML handle by UUID
                 uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-                self._h = pynvml.nvmlDeviceGetHandleByUUID(
+                h = pynvml.nvmlDeviceGetHandleByUUID(
                     uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
             except Exception:
-                self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) \
-                or getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:  # NVML missing: report no clocks
+                h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self._h = h
+            self._reasons_fn = (getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                                or getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons"))
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self.source = "nvml"
+        except Exception as e:  # fall back to nvidia-smi
             self._nv = None
+            self.error = f"nvml: {type(e).__name__}: {e}"
+            self.source = "nvidia-smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self._nv
         while not self._stop.is_set():
             try:
@@ -142,26 +152,53 @@ class ClockSampler:
                 for name, bit in self.REASONS.items():
                     if mask & bit:
                         self.reasons.add(name)
-            except Exception:
-                pass
+            except Exception as e:
+                self.error = f"nvml sample: {e}"
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.ok:
-            self._thread = threading.Thread(target=self._run, daemon=True)
+        if self.source == "nvml":
+            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
             self._thread.start()
+        else:
+            import subprocess
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.SMI_FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "50"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception as e:
+                self.error = (self.error or "") + f"; nvidia-smi: {e}"
         return self
 
     def __exit__(self, *exc):
         if self._thread is not None:
             self._stop.set()
             self._thread.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            names = ("sw_power_cap", "hw_slowdown", "sw_thermal_slowdown", "hw_thermal_slowdown")
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, val in zip(names, f[2:6]):
+                    if val.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        d = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+             "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+             "samples": len(self.samples), "source": self.source}
+        if not self.samples and self.error:
+            d["error"] = self.error
+        return d
 
 
 # ---------------------------------------------------------------------------

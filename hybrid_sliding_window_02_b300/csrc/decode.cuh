@@ -45,6 +45,8 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int W) {
   return s;
 }
 
+__host__ __device__ constexpr int log2i(int x) { return x <= 1 ? 0 : 1 + log2i(x / 2); }
+
 template <typename Tin>
 struct Vec16;  // 16 bytes of input elements, widened to fp32
 template <>
@@ -104,6 +106,10 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
     tma_load_1d(smem_u32(smem + L.v_off), v_ring + (int64_t)bk * ring_elems, ring_bytes, bar_v);
   }
   const int64_t p_now = pos[b];
+  // slot s holds position pos - ((pos - s) mod W): with pos >= W-1 every slot
+  // is filled; otherwise exactly the slots s <= pos are (position s).
+  const bool ring_full = p_now >= (int64_t)W - 1;
+  auto slot_valid = [&](int s) { return ring_full || (int64_t)s <= p_now; };
 
   // ---- scores: warp w takes keys w*KPW + kg, stepping by 8*KPW ----------------
   const int kg = lane / LPK;             // key within the warp instruction
@@ -133,14 +139,34 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
         for (int e = 0; e < EPL; ++e) a = fmaf(qf[g][e], kf[e], a);
         part[g] = a;
       }
+      // Sum the G partial dots over the LPK lanes of this key.  Each step
+      // halves the values a lane keeps (it sends the other half to its
+      // partner), so a lane ends with NV complete sums for heads hoff.. .
+      int hoff = 0;
+      constexpr int NV = (G >> log2i(LPK)) > 0 ? (G >> log2i(LPK)) : 1;
+      const int l = lane % LPK;
 #pragma unroll
-      for (int off = LPK / 2; off > 0; off >>= 1) {
+      for (int off = LPK / 2, c = G; off > 0; off >>= 1) {
+        if (c > 1) {
+          const int half = c / 2;
+          const bool upper = (l & off) != 0;
 #pragma unroll
-        for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
+          for (int j = 0; j < half; ++j) {
+            const float send = upper ? part[j] : part[j + half];
+            const float keep = upper ? part[j + half] : part[j];
+            part[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+          }
+          if (upper) hoff += half;
+          c = half;
+        } else {
+          part[0] += __shfl_xor_sync(0xffffffffu, part[0], off);
+        }
       }
-      if (s < W && (lane % LPK) == 0) {
+      // lanes that share hoff hold identical sums: the lowest of them writes
+      const int dup = LPK / (G / NV);  // lanes per distinct hoff
+      if (s < W && (l % dup) == 0) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) P[s * G + g] = part[g] * scale_log2;
+        for (int j = 0; j < NV; ++j) P[s * G + hoff + j] = part[j] * scale_log2;
       }
     }
   }
@@ -154,15 +180,13 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
       const float sk = sink[h] * 1.4426950408889634f;  // log2(e)
       float m = sk;
       for (int s = lane; s < W; s += 32) {
-        const int64_t ps = p_now - (((p_now - s) % W + W) % W);
-        if (ps >= 0) m = fmaxf(m, P[s * G + g]);
+        if (slot_valid(s)) m = fmaxf(m, P[s * G + g]);
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       float l = 0.f;
       for (int s = lane; s < W; s += 32) {
-        const int64_t ps = p_now - (((p_now - s) % W + W) % W);
-        const float e = (ps >= 0) ? ex2_approx(P[s * G + g] - m) : 0.f;
+        const float e = slot_valid(s) ? ex2_approx(P[s * G + g] - m) : 0.f;
         P[s * G + g] = e;
         l += e;
       }
@@ -191,7 +215,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
     for (int s0 = warp * KPW; s0 < W; s0 += kDecodeWarps * KPW) {
       const int s = s0 + kg;
       // empty slots (position < 0) may hold anything, NaN included: skip them
-      const bool valid = s < W && (p_now - (((p_now - s) % W + W) % W)) >= 0;
+      const bool valid = s < W && slot_valid(s);
       if (valid) {
         float vf[EPL];
         Vec16<Tin>::load(vs + (int64_t)s * D + dc, vf);

@@ -176,25 +176,31 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
       g_dev[dev].tc_attr = true;
     }
   }
-  CUtensorMap mq, mk, mv, mo;
+  const long long ntiles_seq = (T + kNpos - 1) / kNpos;
+  const long long total_tiles = (long long)B * Hkv * ntiles_seq;
+  if (total_tiles >= (1LL << 31)) {
+    set_error_text("problem too large for the tensor-core kernel");
+    return SWA_EUNSUPPORTED;
+  }
+  CUtensorMap mq, mk, mv;
   if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, T, B, 64, kG, kNpos) ||
       !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, kD, Hkv, T, B, 64, 1, kBlk) ||
-      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, kD, Hkv, T, B, 64, 1, kBlk) ||
-      !make_map_4d(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, kD, Hq, T, B, 32, kG, kNpos))
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, kD, Hkv, T, B, 64, 1, kBlk))
     return SWA_ECUDA;
   Params p;
   p.sink = sink;
+  p.out = out;
   p.lse = lse;
   p.B = B;
   p.T = T;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.W = W;
-  p.ntiles_seq = (T + kNpos - 1) / kNpos;
-  p.total_tiles = (long long)B * Hkv * p.ntiles_seq;
+  p.ntiles_seq = (int)ntiles_seq;
+  p.total_tiles = (int)total_tiles;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
-  const long long grid = p.total_tiles < sms ? p.total_tiles : sms;
-  swa_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mo, p);
+  const long long grid = total_tiles < sms ? total_tiles : sms;
+  swa_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
   return check_launch("swa_fwd_tc_kernel");
 }
 

@@ -16,17 +16,23 @@
 //
 // Persistent CTAs (one per SM) walk a contiguous range of tiles in
 // (b, kv head, n) order.  Consecutive tiles of one (b, kv head) share 8 of
-// their 9 key blocks, so keys and values live in a 10-slot ring of 16-key
-// blocks in shared memory and each key/value row is loaded from HBM once per
-// run.  Roles (192 threads):
-//   warp 0      TMA producer: Q tile (2 stages) and new K/V blocks (ring)
-//   warp 1      TMEM owner + single-thread tcgen05.mma issuer:
-//                 S = Q K^T   (M=128, N=144 split at the ring wrap, K=128)
-//                 O = P V     (M=128, N=128, K=16 per block, V MN-major)
-//   warps 2..5  softmax (TMEM -> registers -> bf16 P in shared memory) and
-//               epilogue (TMEM O -> 1/l scaling -> swizzled staging -> TMA store)
-// S is double-buffered in TMEM so QK^T of tile t+1 overlaps softmax of tile t;
-// output stores are asynchronous bulk tensor copies.
+// their 9 key blocks, so keys and values live in a ring of 16-key blocks in
+// shared memory and each key/value row is loaded from HBM once per run.
+//
+// Roles (320 threads), all connected by mbarriers:
+//   warp 8      TMA producer: Q tiles (4 stages, to cover the HBM latency seen
+//               under full load) and new K/V blocks (12-slot ring)
+//   warp 9      TMEM owner + single-thread tcgen05.mma issuer
+//                 S = Q K^T   (SS: M=128, N=144 split at the ring wrap, K=128)
+//                 O = P V     (TS: P from TMEM, V MN-major, N=128, K=16/block)
+//   warps 0..3  softmax: S (TMEM) -> mask, sink-seeded max/sum, normalised
+//               bf16 P -> TMEM; lse -> global
+//   warps 4..7  epilogue: O (TMEM, double-buffered) -> global.  The 16x256b
+//               TMEM read gives each group of 4 threads 32 contiguous bytes of
+//               a row, so every warp store fills 8 whole 32-byte sectors.
+// TMEM: S [0,144), P [160,232) (bf16 pairs), O0 [256,384), O1 [384,512).
+// QK^T of tile t+1 runs while softmax works on tile t (S is read out at once),
+// and the epilogue of tile t overlaps softmax and MMAs of tile t+1.
 #pragma once
 
 #include "device_common.cuh"
@@ -34,65 +40,62 @@
 namespace swa {
 namespace tcswa {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8, kWarpMma = 9;
 constexpr int kG = 8;            // query heads per tile (one kv group)
 constexpr int kNpos = 16;        // positions per tile
 constexpr int kD = 128;
 constexpr int kBlk = 16;         // keys per ring block
 constexpr int kNB = 9;           // blocks per tile window
 constexpr int kN = kNB * kBlk;   // 144 score columns
-constexpr int kRing = 10;        // ring slots
-constexpr int kQStages = 2;
+constexpr uint32_t kRing = 12;   // ring slots
+constexpr uint32_t kQStages = 4;
 constexpr int kMaxW = (kNB - 1) * kBlk + 1;  // 129
 
 // shared-memory map (bytes); swizzled regions 1024-aligned
 constexpr int kQHalf = 128 * 128;                     // 128 rows x 64 bf16
 constexpr int kQStage = 2 * kQHalf;                   // 32 KB
 constexpr int kBlkHalf = kBlk * 128;                  // 16 keys x 64 bf16 = 2 KB
-constexpr int kRingHalf = kRing * kBlkHalf;           // 20 KB
+constexpr int kRingHalf = kRing * kBlkHalf;           // 24 KB
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQStages * kQStage;     // 64 KB
-constexpr int kOffV = kOffK + 2 * kRingHalf;          // +40 KB
-constexpr int kOffP = kOffV + 2 * kRingHalf;          // +40 KB
-constexpr int kPChunk = 128 * 128;                    // 128 rows x 64 keys bf16
-constexpr int kOffStage = kOffP + 3 * kPChunk;        // +48 KB
-constexpr int kStageBytes = 128 * 128;                // 128 rows x 32 fp32
-constexpr int kOffBar = kOffStage + 2 * kStageBytes;  // +32 KB
+constexpr int kOffK = kOffQ + kQStages * kQStage;     // 128 KB
+constexpr int kOffV = kOffK + 2 * kRingHalf;          // +48 KB
+constexpr int kOffBar = kOffV + 2 * kRingHalf;        // +48 KB
 // barriers
-constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKvFull = 4, kBarKvEmpty = 4 + kRing,
-              kBarSFull = 4 + 2 * kRing, kBarSFree = kBarSFull + 2, kBarPFull = kBarSFree + 2,
-              kBarPFree = kBarPFull + 1, kBarOFull = kBarPFree + 1, kBarOFree = kBarOFull + 1,
-              kNumBars = kBarOFree + 1;
+constexpr int kBarQFull = 0, kBarQEmpty = kQStages, kBarKvFull = 2 * kQStages,
+              kBarKvEmpty = kBarKvFull + kRing, kBarSFull = kBarKvEmpty + kRing,
+              kBarSFree = kBarSFull + 1, kBarPFull = kBarSFree + 1, kBarPFree = kBarPFull + 1,
+              kBarOFull = kBarPFree + 1, kBarOFree = kBarOFull + 2, kNumBars = kBarOFree + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;      // + slack for 1024 alignment
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = kN, kColO = 2 * kN;  // 0, 144, 288 (+128 = 416)
+constexpr uint32_t kColS = 0, kColP = 160, kColO0 = 256, kColO1 = 384;
 
 struct Params {
   const float* sink;
+  float* out;
   float* lse;
   int B, T, Hq, Hkv, W;
   int ntiles_seq;       // ceil(T / 16)
-  long long total_tiles;
+  int total_tiles;      // B * Hkv * ntiles_seq (< 2^31, checked on the host)
   float scale_log2;     // log2(e) / sqrt(D)
 };
 
-__device__ __forceinline__ void tile_coords(long long u, const Params& p, int& b, int& kvh,
+__device__ __forceinline__ void tile_coords(uint32_t u, const Params& p, int& b, int& kvh,
                                             int& n) {
-  const long long bk = u / p.ntiles_seq;
-  n = (int)(u - bk * p.ntiles_seq);
-  b = (int)(bk / p.Hkv);
-  kvh = (int)(bk - (long long)b * p.Hkv);
+  const uint32_t bk = u / (uint32_t)p.ntiles_seq;
+  n = (int)(u - bk * (uint32_t)p.ntiles_seq);
+  b = (int)(bk / (uint32_t)p.Hkv);
+  kvh = (int)(bk - (uint32_t)b * (uint32_t)p.Hkv);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k,
-                      const __grid_constant__ CUtensorMap map_v,
-                      const __grid_constant__ CUtensorMap map_o, const Params p) {
+                      const __grid_constant__ CUtensorMap map_v, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -102,53 +105,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
   // contiguous tile range of this CTA
-  const long long per = p.total_tiles / gridDim.x, rem = p.total_tiles % gridDim.x;
-  const long long t_begin = blockIdx.x * per + (blockIdx.x < rem ? blockIdx.x : rem);
-  const long long t_end = t_begin + per + (blockIdx.x < rem ? 1 : 0);
-  const int ntile = (int)(t_end - t_begin);
+  const uint32_t per = (uint32_t)p.total_tiles / gridDim.x;
+  const uint32_t rem = (uint32_t)p.total_tiles % gridDim.x;
+  const uint32_t t_begin = blockIdx.x * per + (blockIdx.x < rem ? blockIdx.x : rem);
+  const int ntile = (int)(per + (blockIdx.x < rem ? 1 : 0));
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (int s = 0; s < 2; ++s) {
+    for (uint32_t s = 0; s < kQStages; ++s) {
       mbar_init(bar(kBarQFull + s), 1);
       mbar_init(bar(kBarQEmpty + s), 1);
-      mbar_init(bar(kBarSFull + s), 1);
-      mbar_init(bar(kBarSFree + s), 128);
     }
-    for (int s = 0; s < kRing; ++s) {
+    for (uint32_t s = 0; s < kRing; ++s) {
       mbar_init(bar(kBarKvFull + s), 1);
       mbar_init(bar(kBarKvEmpty + s), 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarOFull + s), 1);
+      mbar_init(bar(kBarOFree + s), 128);
+    }
+    mbar_init(bar(kBarSFull), 1);
+    mbar_init(bar(kBarSFree), 128);
     mbar_init(bar(kBarPFull), 128);
     mbar_init(bar(kBarPFree), 1);
-    mbar_init(bar(kBarOFull), 1);
-    mbar_init(bar(kBarOFree), 128);
     fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProducer && lane == 0) {
     prefetch_tmap(&map_q);
     prefetch_tmap(&map_k);
     prefetch_tmap(&map_v);
-    prefetch_tmap(&map_o);
-  }
-  if (warp == 1) {
-    tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
 
-  if (warp == 0) {
+  if (warp == kWarpProducer) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      long long seq = 0;  // key blocks loaded so far
+      uint32_t seq = 0;  // key blocks loaded so far
       int prev_bk = -1;
       for (int it = 0; it < ntile; ++it) {
         int b, kvh, n;
         tile_coords(t_begin + it, p, b, kvh, n);
-        const int qs = it & 1;
-        if (!mbar_wait(bar(kBarQEmpty + qs), ((it >> 1) & 1) ^ 1, kErrWaitQEmpty, abort_flag))
-          break;
+        const uint32_t qs = (uint32_t)it % kQStages;
+        const uint32_t qph = ((uint32_t)it / kQStages) & 1;
+        if (!mbar_wait(bar(kBarQEmpty + qs), qph ^ 1, kErrWaitQEmpty, abort_flag)) break;
         const uint32_t qdst = sbase + kOffQ + qs * kQStage;
         mbar_arrive_expect_tx(bar(kBarQFull + qs), kQStage);
         tma_load_4d(qdst, &map_q, 0, kvh * kG, n * kNpos, b, bar(kBarQFull + qs));
@@ -158,8 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prev_bk = bk;
         bool ok = true;
         for (int m = first_blk; m <= n; ++m, ++seq) {
-          const int slot = (int)(seq % kRing);
-          if (!mbar_wait(bar(kBarKvEmpty + slot), (int)((seq / kRing) & 1) ^ 1, kErrWaitKvEmpty,
+          const uint32_t slot = seq % kRing;
+          if (!mbar_wait(bar(kBarKvEmpty + slot), ((seq / kRing) & 1) ^ 1, kErrWaitKvEmpty,
                          abort_flag)) {
             ok = false;
             break;
@@ -176,36 +182,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
     }
-  } else if (warp == 1) {
+    __syncwarp();
+  } else if (warp == kWarpMma) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      const uint32_t idesc_s_unit = umma_idesc_bf16(kBlk, false, false);
-      (void)idesc_s_unit;
       const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
-      long long seq = 0;     // blocks loaded (mirrors the producer)
+      uint32_t seq = 0;      // blocks loaded (mirrors the producer)
       int prev_bk = -1;
       int pending = -1;      // tile whose PV is still to be issued
-      long long pending_ws = 0;
+      uint32_t pending_ws = 0;
       bool pending_run_end = false;
       bool ok = true;
 
-      auto issue_pv = [&](int j, long long ws, bool run_end) -> bool {
+      auto issue_pv = [&](int j, uint32_t ws, bool run_end) -> bool {
+        const int ob = j & 1;
         if (!mbar_wait(bar(kBarPFull), j & 1, kErrWaitPFull, abort_flag)) return false;
-        if (!mbar_wait(bar(kBarOFree), (j & 1) ^ 1, kErrWaitOFree, abort_flag)) return false;
+        if (!mbar_wait(bar(kBarOFree + ob), ((j >> 1) & 1) ^ 1, kErrWaitOFree, abort_flag))
+          return false;
         tc_fence_after();
+        const uint32_t d_o = tmem + (ob ? kColO1 : kColO0);
+        uint32_t slot = ws % kRing;
+#pragma unroll
         for (int kb = 0; kb < kNB; ++kb) {
-          const int slot = (int)((ws + kb) % kRing);
-          const uint64_t adesc =
-              umma_sdesc(sbase + kOffP + (kb >> 2) * kPChunk + (kb & 3) * 32, 16, 1024, 2);
           const uint64_t bdesc =
               umma_sdesc(sbase + kOffV + slot * kBlkHalf, kRingHalf, 1024, 2);
-          umma_bf16_ss(tmem + kColO, adesc, bdesc, idesc_o, kb > 0 ? 1u : 0u);
+          umma_bf16_ts(d_o, tmem + kColP + kb * (kBlk / 2), bdesc, idesc_o, kb > 0 ? 1u : 0u);
+          slot = (slot + 1 == kRing) ? 0 : slot + 1;
         }
-        umma_commit(bar(kBarOFull));
+        umma_commit(bar(kBarOFull + ob));
         umma_commit(bar(kBarPFree));
         // release key blocks no later tile of this run needs
         const int nrel = run_end ? kNB : 1;
-        for (int r = 0; r < nrel; ++r) umma_commit(bar(kBarKvEmpty + (int)((ws + r) % kRing)));
+        slot = ws % kRing;
+        for (int r = 0; r < nrel; ++r) {
+          umma_commit(bar(kBarKvEmpty + slot));
+          slot = (slot + 1 == kRing) ? 0 : slot + 1;
+        }
         return true;
       };
 
@@ -222,45 +234,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           pending = -1;
         }
         // wait for this tile's Q and new key/value blocks
-        const int qs = it & 1;
-        if (!mbar_wait(bar(kBarQFull + qs), (it >> 1) & 1, kErrWaitQFull, abort_flag)) {
+        const uint32_t qs = (uint32_t)it % kQStages;
+        if (!mbar_wait(bar(kBarQFull + qs), ((uint32_t)it / kQStages) & 1, kErrWaitQFull,
+                       abort_flag)) {
           ok = false;
           break;
         }
         for (int r = 0; r < nnew; ++r) {
-          const long long s = seq + r;
-          if (!mbar_wait(bar(kBarKvFull + (int)(s % kRing)), (int)((s / kRing) & 1),
-                         kErrWaitKvFull, abort_flag)) {
+          const uint32_t s = seq + r;
+          if (!mbar_wait(bar(kBarKvFull + s % kRing), (s / kRing) & 1, kErrWaitKvFull,
+                         abort_flag)) {
             ok = false;
             break;
           }
         }
         if (!ok) break;
         seq += nnew;
-        const long long ws = seq - kNB;  // first block of this tile's window
-        const int sb = it & 1;
-        if (!mbar_wait(bar(kBarSFree + sb), ((it >> 1) & 1) ^ 1, kErrWaitSFree, abort_flag)) {
+        const uint32_t ws = seq - kNB;  // first block of this tile's window
+        if (!mbar_wait(bar(kBarSFree), (it & 1) ^ 1, kErrWaitSFree, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         // S = Q K^T; the window's blocks may wrap around the ring end
-        const int slot0 = (int)(ws % kRing);
-        const int seg1 = (slot0 + kNB <= kRing) ? kNB : kRing - slot0;
-        const uint32_t d_s = tmem + (sb ? kColS1 : kColS0);
+        const uint32_t slot0 = ws % kRing;
+        const uint32_t seg1 = (slot0 + kNB <= kRing) ? kNB : kRing - slot0;
+        const uint32_t d_s = tmem + kColS;
         const uint32_t qbase = sbase + kOffQ + qs * kQStage;
+        const uint32_t idesc1 = umma_idesc_bf16(seg1 * kBlk, false, false);
+        const uint32_t idesc2 = umma_idesc_bf16((kNB - seg1) * kBlk, false, false);
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * kRingHalf + (kk & 3) * 32;
           const uint64_t adesc = umma_sdesc(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024, 2);
           const uint64_t b1 = umma_sdesc(sbase + kOffK + slot0 * kBlkHalf + koff, 16, 1024, 2);
-          umma_bf16_ss(d_s, adesc, b1, umma_idesc_bf16(seg1 * kBlk, false, false), kk > 0);
-          if (seg1 < kNB) {
+          umma_bf16_ss(d_s, adesc, b1, idesc1, kk > 0);
+          if (seg1 < (uint32_t)kNB) {
             const uint64_t b2 = umma_sdesc(sbase + kOffK + koff, 16, 1024, 2);
-            umma_bf16_ss(d_s + seg1 * kBlk, adesc, b2,
-                         umma_idesc_bf16((kNB - seg1) * kBlk, false, false), kk > 0);
+            umma_bf16_ss(d_s + seg1 * kBlk, adesc, b2, idesc2, kk > 0);
           }
         }
-        umma_commit(bar(kBarSFull + sb));
+        umma_commit(bar(kBarSFull));
         umma_commit(bar(kBarQEmpty + qs));
         if (pending >= 0) {
           if (!issue_pv(pending, pending_ws, pending_run_end)) { ok = false; break; }
@@ -278,115 +292,131 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok && pending >= 0) issue_pv(pending, pending_ws, true);
     }
-  } else {
-    // ======================= softmax + epilogue (warps 2..5) =======================
-    const int sub = warp & 3;                 // TMEM sub-partition of this warp
-    const int r = sub * 32 + lane;            // tile row = TMEM lane
-    const int ct = tid - 64;                  // 0..127 within the compute group
-    const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
+    __syncwarp();
+  } else if (warp < 4) {
+    // ======================= softmax (warps 0..3) =======================
+    const int r = warp * 32 + lane;           // tile row = TMEM lane
+    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
     const int pos_in_tile = r >> 3, g = r & 7;
     for (int it = 0; it < ntile; ++it) {
       int b, kvh, n;
       tile_coords(t_begin + it, p, b, kvh, n);
-      const int sb = it & 1;
-      if (!mbar_wait(bar(kBarSFull + sb), (it >> 1) & 1, kErrWaitSFull, abort_flag)) break;
-      tc_fence_after();
-      float s[kN];
-      {
-        const uint32_t base = tmem + lane_addr + (sb ? kColS1 : kColS0);
-#pragma unroll
-        for (int c = 0; c < kNB; ++c) {
-          uint32_t v[16];
-          tmem_ld16(base + c * 16, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) s[c * 16 + e] = __uint_as_float(v[e]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bar(kBarSFree + sb));
-
-      // mask + sink-seeded softmax (exact: the whole window is in this row)
-      const int i = n * kNpos + pos_in_tile;            // query position
-      const int key0 = (n - (kNB - 1)) * kBlk;          // key of column 0
-      const int jlo = max(0, i - p.W + 1);
-      const int c_lo = jlo - key0, c_hi = i - key0;     // valid columns [c_lo, c_hi]
       const int h = kvh * kG + g;
       const float sk = p.sink[h] * 1.4426950408889634f;
-      float mx = sk;
-#pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        s[c] = (c >= c_lo && c <= c_hi) ? s[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
-      }
-      float l = (sk == -INFINITY) ? 0.f : ex2_approx(sk - mx);
-#pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        s[c] = ex2_approx(s[c] - mx);
-        l += s[c];
-      }
-      // P (bf16, unnormalised) -> shared memory, K-major 128-byte swizzle
-      if (!mbar_wait(bar(kBarPFree), (it & 1) ^ 1, kErrWaitPFree, abort_flag)) break;
-      {
-        const uint32_t prow = sbase + kOffP + r * 128;
-#pragma unroll
-        for (int u = 0; u < kN / 8; ++u) {
-          const int chunk = u >> 3, unit = u & 7;
-          const uint32_t addr = prow + chunk * kPChunk + ((unit ^ (r & 7)) << 4);
-          st_shared_v4(addr, pack_bf16x2(s[8 * u + 0], s[8 * u + 1]),
-                       pack_bf16x2(s[8 * u + 2], s[8 * u + 3]),
-                       pack_bf16x2(s[8 * u + 4], s[8 * u + 5]),
-                       pack_bf16x2(s[8 * u + 6], s[8 * u + 7]));
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(kBarPFull));
-
-      // epilogue: O (TMEM) -> registers -> scaled, swizzled staging -> TMA store
-      if (!mbar_wait(bar(kBarOFull), it & 1, kErrWaitOFull, abort_flag)) break;
+      const int i = n * kNpos + pos_in_tile;            // query position
+      const int key0 = (n - (kNB - 1)) * kBlk;          // key of column 0
+      const int c_lo = max(0, i - p.W + 1) - key0;      // valid columns [c_lo, c_hi]
+      const int c_hi = i - key0;
+      if (!mbar_wait(bar(kBarSFull), it & 1, kErrWaitSFull, abort_flag)) break;
       tc_fence_after();
-      float o[kD];
+      uint32_t sr[kN];
 #pragma unroll
-      for (int c = 0; c < kD / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_addr + kColO + c * 16, v);
-        tmem_ld_wait();
+      for (int c = 0; c < kNB; ++c)
+        tmem_ld16(tmem + lane_addr + kColS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[c * 16]));
+      tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[c * 16 + e] = __uint_as_float(v[e]);
-      }
+      for (int c = 0; c < kNB; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&sr[c * 16]));
       tc_fence_before();
-      mbar_arrive(bar(kBarOFree));
-      const float inv_l = 1.f / l;
+      mbar_arrive(bar(kBarSFree));
+
+      // Mask.  Columns [16, 128) are inside every row's window whenever the
+      // warp's rows all have c_lo <= 16 and c_hi >= 127 (W = 128, n >= 8): then
+      // only the first and last key blocks need the per-column test.
+      float x[kN];
+      const bool mid_ok = __all_sync(0xffffffffu, c_lo <= 16 && c_hi >= 127);
+      if (mid_ok) {
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int buf = q4 & 1;
-        if (ct == 0) bulk_wait_read<1>();
-        named_bar_sync(1, 128);
-        const uint32_t srow = sbase + kOffStage + buf * kStageBytes + r * 128;
+        for (int c = 0; c < kN; ++c) {
+          const bool edge = c < 16 || c >= 128;
+          x[c] = (!edge || (c >= c_lo && c <= c_hi)) ? __uint_as_float(sr[c]) : -INFINITY;
+        }
+      } else {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float* x = &o[q4 * 32 + u * 4];
-          st_shared_v4(srow + ((u ^ (r & 7)) << 4), __float_as_uint(x[0] * inv_l),
-                       __float_as_uint(x[1] * inv_l), __float_as_uint(x[2] * inv_l),
-                       __float_as_uint(x[3] * inv_l));
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (ct == 0) {
-          tma_store_4d(&map_o, sbase + kOffStage + buf * kStageBytes, q4 * 32, kvh * kG,
-                       n * kNpos, b);
-          bulk_commit();
-        }
+        for (int c = 0; c < kN; ++c)
+          x[c] = (c >= c_lo && c <= c_hi) ? __uint_as_float(sr[c]) : -INFINITY;
       }
+      // max over the row: 8 independent chains, then a tree
+      float m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+      for (int c = 8; c < kN; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mx = fmaxf(mraw * p.scale_log2, sk);  // scale > 0 commutes with max
+      float l8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) l8[k] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kN; ++c) {
+        x[c] = ex2_approx(fmaf(x[c], p.scale_log2, -mx));
+        l8[c & 7] += x[c];
+      }
+      float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      if (sk != -INFINITY) l += ex2_approx(sk - mx);
+      const float inv_l = 1.f / l;
+      uint32_t pk[kN / 2];
+#pragma unroll
+      for (int c = 0; c < kN / 2; ++c) pk[c] = pack_bf16x2(x[2 * c] * inv_l, x[2 * c + 1] * inv_l);
+      // P -> TMEM once the previous tile's PV has consumed it
+      if (!mbar_wait(bar(kBarPFree), (it & 1) ^ 1, kErrWaitPFree, abort_flag)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kNB; ++c)
+        tmem_st8(tmem + lane_addr + kColP + c * 8, *reinterpret_cast<uint32_t(*)[8]>(&pk[c * 8]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPFull));
       if (p.lse != nullptr && i < p.T)
         p.lse[((long long)b * p.Hq + h) * p.T + i] = (mx + __log2f(l)) * 0.6931471805599453f;
     }
-    if (ct == 0) bulk_wait<0>();
+  } else {
+    // ======================= epilogue (warps 4..7) =======================
+    const int sub = warp & 3;                 // TMEM lanes [32 sub, 32 sub + 32)
+    const int quad = lane & 3, rr = lane >> 2;
+    for (int it = 0; it < ntile; ++it) {
+      int b, kvh, n;
+      tile_coords(t_begin + it, p, b, kvh, n);
+      const int ob = it & 1;
+      if (!mbar_wait(bar(kBarOFull + ob), (it >> 1) & 1, kErrWaitOFull, abort_flag)) break;
+      tc_fence_after();
+      uint32_t o0[64], o1[64];
+      const uint32_t col = tmem + (ob ? kColO1 : kColO0);
+      tmem_ld_16x256b_x16(col + ((uint32_t)(sub * 32) << 16), o0);
+      tmem_ld_16x256b_x16(col + ((uint32_t)(sub * 32 + 16) << 16), o1);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o0[c * 16]));
+        reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o1[c * 16]));
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarOFree + ob));
+      // rows of this thread: 32 sub + {0, 8, 16, 24} + rr, i.e. positions
+      // 4 sub + {0, 1, 2, 3}, head rr; columns 8j + 2 quad + {0, 1}
+      const long long row0 = ((long long)b * p.T + n * kNpos + 4 * sub) * p.Hq + kvh * kG + rr;
+      const int pos0 = n * kNpos + 4 * sub;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (pos0 + k < p.T) {
+          float* orow = p.out + (row0 + (long long)k * p.Hq) * kD + 2 * quad;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            st_global_v2(orow + 8 * j, o0[4 * j + 2 * k], o0[4 * j + 2 * k + 1]);
+        }
+        if (pos0 + 2 + k < p.T) {
+          float* orow = p.out + (row0 + (long long)(2 + k) * p.Hq) * kD + 2 * quad;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            st_global_v2(orow + 8 * j, o1[4 * j + 2 * k], o1[4 * j + 2 * k + 1]);
+        }
+      }
+    }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
