@@ -41,7 +41,12 @@ METRIC = "SWA+sink prefill TFLOP/s & decode GB/s on 1 B300, as % of roofline vs 
 PREFILL = dict(B=4, T=8192, Hq=64, Hkv=8, D=128, W=128)
 DECODE = dict(B=256, Hq=64, Hkv=8, D=128, W=128)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-KERNEL_SOURCES = ("csrc/tc_swa.cuh", "csrc/decode.cuh", "csrc/device_common.cuh")
+# sources each kernel is built from (its traffic record is void once they change)
+KERNEL_SOURCES = {
+    "swa_fwd_tc_kernel": ("csrc/tc_swa.cuh", "csrc/device_common.cuh"),
+    "swa_fwd_tc_global_kernel": ("csrc/tc_global.cuh", "csrc/device_common.cuh"),
+    "decode_tc_kernel": ("csrc/decode_tc.cuh", "csrc/device_common.cuh"),
+}
 
 
 def workload_name(c):
@@ -214,19 +219,20 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "hybrid_sliding_window_02_b300", rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None if absent
-    or taken on different kernel sources."""
+    """DRAM bytes (read + write) per launch of the bench workload, from the
+    committed ncu summary ``profiles/dram_traffic.txt``; None if absent or if
+    the kernel's sources have changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
+    if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
     rec = {}
     with open(path) as f:
@@ -236,7 +242,7 @@ def recorded_traffic(kernel: str):
                 continue
             key, val = line.split(":", 1)
             rec[key.strip()] = val.strip()
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get(f"{kernel}.source_hash") != kernel_source_hash(kernel):
         return None
     val = rec.get(f"{kernel}.bytes_per_launch")
     return int(float(val)) if val else None
@@ -330,6 +336,77 @@ def time_decode(swa, c, steps, warmup, dev, stream, nsets=4):
     return e0.elapsed_time(e1) / steps
 
 
+HYBRID = dict(T=32768, Hq=64, Hkv=8, D=128, W=128, n_swa=5, n_ga=1)
+
+
+def time_hybrid(swa, dev, stream, reps):
+    """One 5:1 hybrid block: five W=128 layers then one global layer (W = T),
+    each on its own seeded inputs, one sequence of T=32768.  Returns per-layer
+    mean launch times (ms) measured with events on the launching stream."""
+    c = HYBRID
+    T, Hq, Hkv, D = c["T"], c["Hq"], c["Hkv"], c["D"]
+    layers = gen.hybrid_block_inputs(T, Hq, Hkv, D, n_swa=c["n_swa"], n_ga=c["n_ga"], seed=200,
+                                     device=dev)
+    Ws = [c["W"]] * c["n_swa"] + [T] * c["n_ga"]
+    out = torch.empty(1, T, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(1, Hq, T, dtype=torch.float32, device=dev)
+
+    def block(evs=None):
+        for li, (x, W) in enumerate(zip(layers, Ws)):
+            if evs is not None:
+                evs[li][0].record(stream)
+            swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
+            if evs is not None:
+                evs[li][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            block()
+    torch.cuda.synchronize()
+    per_layer = [0.0] * len(Ws)
+    total = 0.0
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in Ws]
+            block(evs)
+            torch.cuda.synchronize()
+            for li, (a, b) in enumerate(evs):
+                per_layer[li] += a.elapsed_time(b) / reps
+            total += evs[0][0].elapsed_time(evs[-1][1]) / reps
+    del layers, out, lse
+    torch.cuda.empty_cache()
+    return per_layer, total, Ws
+
+
+def hybrid_line(swa, dev, stream, reps, peaks):
+    c = HYBRID
+    T, Hq, D = c["T"], c["Hq"], c["D"]
+    per_layer, total_ms, Ws = time_hybrid(swa, dev, stream, reps)
+    fl = [work.prefill_flops(1, T, Hq, D, W) for W in Ws]
+    ga_ms = sum(t for t, W in zip(per_layer, Ws) if W >= T) / max(1, c["n_ga"])
+    ga_fl = fl[-1]
+    ga_tf = ga_fl / (ga_ms * 1e-3) / 1e12
+    swa_ms = sum(t for t, W in zip(per_layer, Ws) if W < T) / c["n_swa"]
+    flop_ratio, kv_ratio = work.hybrid_reduction(T, c["W"], c["n_swa"], c["n_ga"])
+    return {
+        "workload": f"hybrid block {c['n_swa']}x SWA (W={c['W']}) + {c['n_ga']}x global "
+                    f"(W=T), B1 T{T} Hq{Hq} Hkv{c['Hkv']} D{D} bf16->fp32+lse",
+        "value": round(sum(fl) / (total_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "ms_per_block": round(total_ms, 3), "reps": reps,
+        "layer_ms": [round(t, 4) for t in per_layer],
+        "swa_layer_ms": round(swa_ms, 4), "global_layer_ms": round(ga_ms, 4),
+        "attention_flop_reduction_vs_all_global": round(flop_ratio, 3),
+        "kv_cache_reduction_vs_all_global": round(kv_ratio, 3),
+        "roofline": {"kernel": "swa_fwd_tc_global_kernel", "bound": "tensor",
+                     "achieved": round(ga_tf, 1), "peak": float(peaks["bf16_tflops"]),
+                     "unit": "TFLOP/s", "frac": round(ga_tf / float(peaks["bf16_tflops"]), 4),
+                     "peak_source": "measured bf16_tflops (burst)",
+                     "algorithmic_flops_per_launch": ga_fl,
+                     "traffic": recorded_traffic("swa_fwd_tc_global_kernel")},
+    }
+
+
 def time_e2e(swa, xh, c, steps, dev, stream):
     """Host (pinned) inputs -> device -> prefill -> host outputs, every step."""
     B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
@@ -366,6 +443,32 @@ def time_e2e(swa, xh, c, steps, dev, stream):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
+KERNEL_OF_PATH = {"tc_swa": "swa_fwd_tc_kernel", "tc_global": "swa_fwd_tc_global_kernel",
+                  "simt": "simt_fwd_kernel"}
+
+
+def prefill_roofline(kpath, flops, nbytes, launch_ms, peaks, peak_src):
+    """Roofline of the prefill kernel: HBM-bound for the sliding window (fp32
+    output dominates the bytes), tensor-bound for the global layer."""
+    kernel = KERNEL_OF_PATH.get(kpath, kpath)
+    gbs = nbytes / (launch_ms * 1e-3) / 1e9
+    tfs = flops / (launch_ms * 1e-3) / 1e12
+    common = {"kernel": kernel, "launch_ms": round(launch_ms, 4),
+              "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+              "traffic": recorded_traffic(kernel)}
+    if kpath == "tc_global":
+        peak = float(peaks["bf16_tflops"])
+        return dict({"bound": "tensor", "achieved": round(tfs, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tfs / peak, 4),
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "gbs": round(gbs, 1)}, **common)
+    hbm = float(peaks["hbm_gbs"])
+    return dict({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                 "frac": round(gbs / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
+                 "tflops": round(tfs, 2),
+                 "tensor_peak_frac": round(tfs / float(peaks["bf16_tflops"]), 4)}, **common)
+
+
 def run_ours(args, dist):
     import hybrid_sliding_window_02_b300 as swa
     swa.lib()
@@ -373,6 +476,9 @@ def run_ours(args, dist):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
     c = dict(PREFILL, B=args.prefill[0], T=args.prefill[1])
+    if args.window:
+        c["W"] = args.window
+    kpath = swa.fwd_path(c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], c["W"])
     x = gen.prefill_inputs(c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], seed=0, device=dev)
     flops = work.prefill_flops(c["B"], c["T"], c["Hq"], c["D"], c["W"])
     nbytes = work.prefill_bytes(c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], 2)
@@ -389,6 +495,9 @@ def run_ours(args, dist):
     dec_bytes = work.decode_bytes(DECODE["B"], DECODE["Hq"], DECODE["Hkv"], DECODE["D"],
                                   DECODE["W"], 2)
     dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
+    dec_kernel = ("decode_tc_kernel" if swa.decode_path(DECODE["B"], DECODE["Hq"], DECODE["Hkv"],
+                                                        DECODE["D"], DECODE["W"]) == "tc_decode"
+                  else "decode_kernel")
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
@@ -398,33 +507,23 @@ def run_ours(args, dist):
         "config": {"workload": workload_name(c), "seed": 0,
                    "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step)",
                    "parallelism": f"replicas x{dist.world}"},
-        "roofline": {
-            "kernel": "swa_fwd_tc_kernel", "bound": "hbm",
-            "achieved": round(nbytes / (launch_ms * 1e-3) / 1e9, 1),
-            "peak": hbm, "unit": "GB/s",
-            "frac": round(nbytes / (launch_ms * 1e-3) / 1e9 / hbm, 4),
-            "peak_source": f"{peak_src} hbm_gbs",
-            "algorithmic_bytes_per_launch": nbytes,
-            "launch_ms": round(launch_ms, 4),
-            "traffic": recorded_traffic("swa_fwd_tc_kernel"),
-            "tflops": round(flops / (launch_ms * 1e-3) / 1e12, 2),
-            "tensor_peak_frac": round(flops / (launch_ms * 1e-3) / 1e12
-                                      / float(peaks["bf16_tflops"]), 4),
-        },
+        "roofline": prefill_roofline(kpath, flops, nbytes, launch_ms, peaks, peak_src),
         "decode": {
             "workload": "swa_sink_decode B256 Hq64 Hkv8 D128 W128 ring, bf16->fp32+lse, "
-                        "4 rotating input sets (550 MB)",
+                        "4 rotating input sets (590 MB)",
             "value": round(dec_gbs, 1), "unit": "GB/s", "us_per_call": round(dec_us, 2),
-            "roofline": {"kernel": "decode_kernel", "bound": "hbm",
+            "roofline": {"kernel": dec_kernel, "bound": "hbm",
                          "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(dec_gbs / hbm, 4),
                          "algorithmic_bytes_per_launch": dec_bytes,
-                         "traffic": recorded_traffic("decode_kernel")},
+                         "traffic": recorded_traffic(dec_kernel)},
         },
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
 
+    if not args.no_hybrid:
+        line["hybrid_block"] = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks)
     if not args.no_e2e:
         xh = gen.PrefillInputs(*(t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.sink)))
         e2e_ms, h2d, d2h = time_e2e(swa, xh, c, max(3, args.steps // 50), dev, stream)
@@ -487,6 +586,11 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-hybrid", action="store_true", help="skip the 5:1 hybrid-block line")
+    ap.add_argument("--hybrid-reps", type=int, default=5)
+    ap.add_argument("--window", type=int, default=0,
+                    help="window of the timed prefill (default 128; W >= T is a global layer); "
+                         "for profiling other cases")
     ap.add_argument("--prefill", type=int, nargs=2, metavar=("B", "T"),
                     default=(PREFILL["B"], PREFILL["T"]),
                     help="prefill batch and length (default: the headline workload); other "

@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
                 f.restype = i32
             L.swa_sink_fwd_path.argtypes = [i32, i32, i32, i32, i32, i32, i32]
             L.swa_sink_fwd_path.restype = ctypes.c_char_p
+            L.swa_sink_decode_path.argtypes = [i32, i32, i32, i32, i32, i32]
+            L.swa_sink_decode_path.restype = ctypes.c_char_p
             L.swa_status_str.argtypes = [i32]
             L.swa_status_str.restype = ctypes.c_char_p
             L.swa_last_error.restype = ctypes.c_char_p
@@ -117,6 +119,11 @@ def _cuda_contig(name, t, device=None):
 def fwd_path(B, T, Hq, Hkv, D, W, dtype_code=SWA_BF16) -> str:
     """Name of the prefill kernel the library selects for these sizes."""
     return lib().swa_sink_fwd_path(B, T, Hq, Hkv, D, W, dtype_code).decode()
+
+
+def decode_path(B, Hq, Hkv, D, W, dtype_code=SWA_BF16) -> str:
+    """Name of the decode kernel the library selects for these sizes."""
+    return lib().swa_sink_decode_path(B, Hq, Hkv, D, W, dtype_code).decode()
 
 
 def swa_sink_fwd(q, k, v, sink, W: int, out=None, lse=None, *, with_lse: bool = True,

@@ -1,0 +1,330 @@
+// decode_tc.cuh -- one-token decode against the 128-slot ring cache with the
+// per-group contractions on the 5th-generation tensor cores.
+//
+// Operation: for each sequence b and kv head g, the G = 8 query heads of the
+// group attend to the W = 128 ring slots of (b, g) with the sink-biased
+// softmax ("MiMo-V2-Flash Technical Report" summary, section 前置知识; the
+// fixed-size O(W) sliding-window cache of the "pwwt.cn" essay, section 1.1).
+// Slot s holds position pos - ((pos - s) mod W); while pos < W - 1 the slots
+// s > pos are empty and are ignored whatever they hold.
+//
+// The call moves about 147 MB (two 32 KB rings per group) and is bound by HBM
+// bandwidth, but each group's work is a dense contraction of 8 heads x 128
+// slots x 128 dims twice over: on the CUDA cores the FMAs alone take about
+// two thirds of the transfer time, so they run on the tensor cores instead
+// and the CUDA cores only do the softmax:
+//   S^T = K q^T      M = 128 slots, N = 16 (8 heads + 8 unused), K = 128 dims
+//   O^T = V^T P^T    M = 128 dims (V read MN-major), N = 16, K = 128 slots
+// Persistent CTAs (one per SM) take groups u = blockIdx.x, + gridDim.x, ...;
+// a producer thread keeps three groups' K, V and q in flight through a ring of
+// shared-memory stages (TMA, 128-byte swizzle), so HBM never waits on the
+// math.  Two softmax warpgroups take alternate groups: thread = slot reads
+// its 8 head scores from TMEM, the max and the sum over slots are warp-shuffle
+// reductions finished across the four warps in shared memory, the bf16 P^T
+// goes to shared memory for the second MMA, and after it thread = dim reads
+// O^T from TMEM and writes out[b, h, dim] (each warp 128 contiguous bytes).
+#pragma once
+
+#include "device_common.cuh"
+
+namespace swa {
+namespace dectc {
+
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr int kG = 8;              // query heads per kv head
+constexpr int kN = 16;             // MMA N: heads padded to 16
+constexpr int kW = 128;            // ring slots
+constexpr int kD = 128;
+constexpr uint32_t kStages = 3;
+
+constexpr int kHalf = kW * 128;                 // 128 rows x 64 bf16 = 16 KB
+constexpr int kQHalf = kN * 128;                // 16 rows x 64 bf16 = 2 KB
+constexpr int kStageK = 0, kStageV = 2 * kHalf, kStageQ = 4 * kHalf;
+constexpr int kStageBytes = kStageQ + 2 * kQHalf;   // 68 KB
+constexpr int kLoadBytes = kStageBytes;             // bytes one stage's copies deliver
+constexpr int kPBytes = 2 * kQHalf;                 // P^T: 16 heads x 128 slots bf16
+constexpr int kOffStage = 0;
+constexpr int kOffP = kOffStage + (int)kStages * kStageBytes;   // 2 buffers (one per warpgroup)
+constexpr int kOffRed = kOffP + 2 * kPBytes;                    // [wg][warp][head] floats
+constexpr int kRedBytes = 2 * 4 * kG * 4;
+constexpr int kOffBar = kOffRed + 2 * kRedBytes;
+constexpr int kBarFull = 0, kBarEmpty = kStages, kBarSFull = 2 * kStages,
+              kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarRed = kBarOFull + 2,
+              kBarDrain = kBarRed + 4, kNumBars = kBarDrain + 1;
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 8;
+constexpr int kSmemBytes = kOffAbort + 8 + 1024;
+
+constexpr uint32_t kTmemCols = 64;
+// TMEM columns of S^T and O^T for warpgroup w (16 columns each)
+__host__ __device__ constexpr uint32_t col_s(int w) { return 32u * (uint32_t)w; }
+__host__ __device__ constexpr uint32_t col_o(int w) { return 32u * (uint32_t)w + 16u; }
+
+struct Params {
+  const int64_t* pos;
+  const float* sink;
+  float* out;
+  float* lse;
+  int B, Hq, Hkv;
+  int units;          // B * Hkv
+  float scale_log2;   // log2(e) / sqrt(D)
+};
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void reg_fence8(uint32_t (&r)[8]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+               "+r"(r[6]), "+r"(r[7]));
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap map_k,
+                     const __grid_constant__ CUtensorMap map_v,
+                     const __grid_constant__ CUtensorMap map_q, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  const int nk = p.units > (int)blockIdx.x
+                     ? (p.units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                     : 0;  // groups of this CTA
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (uint32_t s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarFull + s), 1);
+      mbar_init(bar(kBarEmpty + s), 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(bar(kBarSFull + w), 1);
+      mbar_init(bar(kBarPFull + w), 128);
+      mbar_init(bar(kBarOFull + w), 1);
+      mbar_init(bar(kBarRed + 2 * w), 128);
+      mbar_init(bar(kBarRed + 2 * w + 1), 128);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    fence_mbar_init();
+  }
+  // P^T rows 8..15 (the padding heads) stay zero for the whole kernel
+  for (int i = tid; i < 2 * kPBytes / 16; i += kThreads)
+    st_shared_v4(sbase + kOffP + 16 * i, 0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == kWarpMma) {
+    tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProducer && lane == 0) {
+    prefetch_tmap(&map_k);
+    prefetch_tmap(&map_v);
+    prefetch_tmap(&map_q);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+
+  if (warp == kWarpProducer) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      int k = 0;
+      for (; k < nk; ++k) {
+        const int u = (int)blockIdx.x + k * (int)gridDim.x;
+        const int b = u / p.Hkv, g = u - b * p.Hkv;
+        const uint32_t s = (uint32_t)k % kStages;
+        if (!mbar_wait(bar(kBarEmpty + s), (((uint32_t)k / kStages) & 1) ^ 1, kErrWaitKvEmpty,
+                       abort_flag))
+          break;
+        const uint32_t st = sbase + kOffStage + s * kStageBytes;
+        const uint32_t fb = bar(kBarFull + s);
+        mbar_arrive_expect_tx(fb, kLoadBytes);
+        tma_load_4d(st + kStageK, &map_k, 0, u * kW, 0, 0, fb);
+        tma_load_4d(st + kStageK + kHalf, &map_k, 64, u * kW, 0, 0, fb);
+        tma_load_4d(st + kStageV, &map_v, 0, u * kW, 0, 0, fb);
+        tma_load_4d(st + kStageV + kHalf, &map_v, 64, u * kW, 0, 0, fb);
+        tma_load_4d(st + kStageQ, &map_q, 0, b * p.Hq + g * kG, 0, 0, fb);
+        tma_load_4d(st + kStageQ + kQHalf, &map_q, 64, b * p.Hq + g * kG, 0, 0, fb);
+      }
+      if (k < nk) {  // stopped early: let the copies already issued land
+        for (int j = (k > (int)kStages ? k - (int)kStages : 0); j < k; ++j)
+          mbar_wait_drain(bar(kBarFull + (uint32_t)j % kStages), ((uint32_t)j / kStages) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc_bf16(kN, false, false);
+      const uint32_t idesc_o = umma_idesc_bf16(kN, true, false);
+      for (int k = 0; k < nk; ++k) {
+        const uint32_t s = (uint32_t)k % kStages;
+        const int w = k & 1;
+        if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
+                       abort_flag))
+          break;
+        tc_fence_after();
+        const uint32_t st = sbase + kOffStage + s * kStageBytes;
+        const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
+        const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t a_off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+          const uint32_t b_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+          umma_bf16_ss(tmem + col_s(w), kdesc + a_off, qdesc + b_off, idesc_s, kk > 0);
+        }
+        umma_commit(bar(kBarSFull + w));
+        // O^T = V^T P^T once the softmax of this group has written P^T
+        if (!mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag))
+          break;
+        tc_fence_after();
+        const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
+        const uint64_t pdesc = umma_sdesc(sbase + kOffP + w * kPBytes, 16, 1024, 2);
+#pragma unroll
+        for (int kb = 0; kb < kW / 16; ++kb) {
+          const uint32_t a_off = (kb * 16 * 128) >> 4;
+          const uint32_t b_off = ((kb >> 2) * kQHalf + (kb & 3) * 32) >> 4;
+          umma_bf16_ss(tmem + col_o(w), vdesc + a_off, pdesc + b_off, idesc_o, kb > 0);
+        }
+        umma_commit(bar(kBarOFull + w));
+        umma_commit(bar(kBarEmpty + s));
+      }
+      umma_commit(bar(kBarDrain));
+      mbar_wait_drain(bar(kBarDrain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax + output (warps 0..7) =======================
+    const int w = warp >> 2;                   // warpgroup: takes groups k with k % 2 == w
+    const int quad = warp & 3;
+    const int t = quad * 32 + lane;            // slot (softmax) / dim (output)
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    float* red = reinterpret_cast<float*>(smem + kOffRed) + w * (4 * kG * 2);
+    const uint32_t pbuf = sbase + kOffP + w * kPBytes;
+    // P^T[h][t] lives at half (t / 64), row h, 16-byte chunk ((t % 64) / 8) ^ h,
+    // element t % 8 (128-byte swizzle, rows of 64 slots)
+    const uint32_t p_off = (t >> 6) * kQHalf + 2 * (t & 7);
+    const int p_chunk = (t & 63) >> 3;
+    // The cross-warp exchanges of a warpgroup go through two mbarriers (one
+    // per reduction) rather than bar.sync, so that a timed-out wait elsewhere
+    // can never leave the other warps blocked.
+    const uint32_t bar_max = bar(kBarRed + 2 * w), bar_sum = bar(kBarRed + 2 * w + 1);
+    for (int k = w; k < nk; k += 2) {
+      const int u = (int)blockIdx.x + k * (int)gridDim.x;
+      const int b = u / p.Hkv, g = u - b * p.Hkv;
+      const uint32_t s = (uint32_t)k % kStages;
+      const int64_t pnow = p.pos[b];
+      const bool full_ring = pnow >= kW - 1;
+      const bool valid = full_ring || (int64_t)t <= pnow;
+      if (!mbar_wait(bar(kBarSFull + w), ((uint32_t)k >> 1) & 1, kErrWaitSFull, abort_flag))
+        break;
+      tc_fence_after();
+      uint32_t sr[8];
+      tmem_ld8(tmem + lane_addr + col_s(w), sr);
+      tmem_ld_wait();
+      reg_fence8(sr);
+      float x[kG], m[kG];
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        x[h] = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
+        m[h] = x[h];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int h = 0; h < kG; ++h) m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], off));
+      {
+        float mine = m[0];  // lane h < 8 publishes head h
+#pragma unroll
+        for (int h = 1; h < kG; ++h) mine = lane == h ? m[h] : mine;
+        if (lane < kG) red[quad * kG + lane] = mine;
+      }
+      mbar_arrive(bar_max);
+      if (!mbar_wait(bar_max, ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag)) break;
+      float sk[kG], l[kG];
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        sk[h] = p.sink[g * kG + h] * 1.4426950408889634f;
+        m[h] = fmaxf(fmaxf(fmaxf(red[h], red[kG + h]), fmaxf(red[2 * kG + h], red[3 * kG + h])),
+                     sk[h]);
+        // with no valid slot and no sink (not reachable for pos >= 0) keep m finite
+        const float mb = m[h] == -INFINITY ? 0.f : m[h];
+        x[h] = ex2_approx(x[h] - mb);
+        l[h] = x[h];
+      }
+      // bf16 P^T to shared memory for the second MMA
+#pragma unroll
+      for (int h = 0; h < kG; ++h)
+        st_shared_u16(pbuf + p_off + h * 128 + (((p_chunk ^ h) & 7) << 4),
+                      __bfloat16_as_ushort(__float2bfloat16_rn(x[h])));
+      // empty slots may hold anything (NaN included): zero their values so
+      // that 0 * V stays 0 in the MMA
+      if (!full_ring && !valid) {
+        const uint32_t vrow = sbase + kOffStage + s * kStageBytes + kStageV + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          st_shared_v4(vrow + 16 * c, 0u, 0u, 0u, 0u);
+          st_shared_v4(vrow + kHalf + 16 * c, 0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPFull + w));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int h = 0; h < kG; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+      {
+        float mine = l[0];
+#pragma unroll
+        for (int h = 1; h < kG; ++h) mine = lane == h ? l[h] : mine;
+        if (lane < kG) red[4 * kG + quad * kG + lane] = mine;
+      }
+      mbar_arrive(bar_sum);
+      if (!mbar_wait(bar_sum, ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag)) break;
+      float inv_l[kG];
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        float lt = (red[4 * kG + h] + red[5 * kG + h]) + (red[6 * kG + h] + red[7 * kG + h]);
+        if (sk[h] != -INFINITY) lt += ex2_approx(sk[h] - m[h]);
+        inv_l[h] = lt > 0.f ? 1.f / lt : 0.f;
+        if (t == h && p.lse != nullptr)
+          p.lse[(int64_t)b * p.Hq + g * kG + h] = (m[h] + __log2f(lt)) * 0.6931471805599453f;
+      }
+      // O^T[dim t][h] -> out[b, g*8 + h, t]
+      if (!mbar_wait(bar(kBarOFull + w), ((uint32_t)k >> 1) & 1, kErrWaitOFull, abort_flag))
+        break;
+      tc_fence_after();
+      uint32_t o[8];
+      tmem_ld8(tmem + lane_addr + col_o(w), o);
+      tmem_ld_wait();
+      reg_fence8(o);
+      tc_fence_before();
+      float* ob = p.out + ((int64_t)b * p.Hq + g * kG) * kD + t;
+#pragma unroll
+      for (int h = 0; h < kG; ++h) ob[h * kD] = __uint_as_float(o[h]) * inv_l[h];
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace dectc
+}  // namespace swa

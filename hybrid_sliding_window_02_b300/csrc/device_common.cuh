@@ -28,7 +28,9 @@ enum DevErr : unsigned int {
   kErrWaitPFree = 0x108,
   kErrWaitQEmpty = 0x109,
   kErrWaitKvEmpty = 0x10a,
+  kErrWaitPvDone = 0x10b,
   kErrWaitDecode = 0x201,
+  kErrDrain = 0x301,
 };
 
 // Wall-clock limit for one wait: far beyond any legitimate wait inside a CTA
@@ -93,6 +95,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
       return false;
     }
   }
+}
+
+// Limit for the waits a CTA makes on its way out after an error: copies and
+// MMAs it issued are allowed this long to land before it releases its memory.
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
+// Bounded wait used only while winding down: returns false (recording
+// kErrDrain) if the phase has not completed within kDrainLimitNs.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kDrainLimitNs) {
+      atomicCAS(&g_dev_error, 0u, (unsigned)kErrDrain);
+      return false;
+    }
+  }
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -311,6 +330,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void st_global_v8(float* p, const uint32_t* r) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
                "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(float* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d)
                : "memory");
 }
 

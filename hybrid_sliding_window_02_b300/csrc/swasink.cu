@@ -13,8 +13,10 @@
 
 #include "../../include/swasink.h"
 #include "decode.cuh"
+#include "decode_tc.cuh"
 #include "device_common.cuh"
 #include "simt_fwd.cuh"
+#include "tc_global.cuh"
 #include "tc_swa.cuh"
 
 namespace {
@@ -35,6 +37,8 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   bool tc_attr = false;
+  bool tcg_attr = false;
+  bool dectc_attr = false;
   bool decode_attr[2][2][5] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -121,15 +125,15 @@ swa_status check_launch(const char* what) {
   return SWA_OK;
 }
 
-enum FwdPath { kPathInvalid, kPathSimt, kPathTcSwa };
+enum FwdPath { kPathInvalid, kPathSimt, kPathTcSwa, kPathTcGlobal };
 
 FwdPath select_fwd(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype dt) {
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return kPathInvalid;
   if (dt != SWA_F32 && dt != SWA_BF16) return kPathInvalid;
   if (D != 64 && D != 128) return kPathInvalid;
   const int G = Hq / Hkv;
-  if (dt == SWA_BF16 && D == swa::tcswa::kD && G == swa::tcswa::kG && W <= swa::tcswa::kMaxW)
-    return kPathTcSwa;
+  if (dt == SWA_BF16 && D == swa::tcswa::kD && G == swa::tcswa::kG)
+    return W <= swa::tcswa::kMaxW ? kPathTcSwa : kPathTcGlobal;
   return kPathSimt;
 }
 
@@ -204,6 +208,53 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
   return check_launch("swa_fwd_tc_kernel");
 }
 
+swa_status launch_tc_global(const void* q, const void* k, const void* v, const float* sink,
+                            float* out, float* lse, int B, int T, int Hq, int Hkv, int W,
+                            cudaStream_t st) {
+  using namespace swa::tcglobal;
+  int dev, sms;
+  if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev[dev].tcg_attr) {
+      cudaError_t e = cudaFuncSetAttribute(swa_fwd_tc_global_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+      if (e != cudaSuccess) {
+        set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_global_kernel)", e);
+        return SWA_ECUDA;
+      }
+      g_dev[dev].tcg_attr = true;
+    }
+  }
+  const long long nitem_seq = (T + kItemPos - 1) / kItemPos;
+  const long long total = (long long)B * Hkv * nitem_seq;
+  if (total >= (1LL << 31)) {
+    set_error_text("problem too large for the tensor-core kernel");
+    return SWA_EUNSUPPORTED;
+  }
+  CUtensorMap mq, mk, mv;
+  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, T, B, 64, kG, kNpos) ||
+      !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, kD, Hkv, T, B, 64, 1, kBlk) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, kD, Hkv, T, B, 64, 1, kBlk))
+    return SWA_ECUDA;
+  Params p;
+  p.sink = sink;
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.W = W;
+  p.nitem_seq = (int)nitem_seq;
+  p.total_items = (int)total;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  const long long grid = total < sms ? total : sms;
+  swa_fwd_tc_global_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+  return check_launch("swa_fwd_tc_global_kernel");
+}
+
 template <typename Tin, int D, int G>
 swa_status launch_decode_t(const void* q, const void* kr, const void* vr, const int64_t* pos,
                            const float* sink, float* out, float* lse, int B, int Hq, int Hkv,
@@ -224,6 +275,57 @@ swa_status launch_decode_t(const void* q, const void* kr, const void* vr, const 
       static_cast<const Tin*>(q), static_cast<const Tin*>(kr), static_cast<const Tin*>(vr), pos,
       sink, out, lse, Hq, Hkv, W, scale_log2);
   return check_launch("decode_kernel");
+}
+
+// Tensor-core decode: bf16, D = 128, W = 128, groups of 8 query heads.
+bool decode_tc_applies(int Hq, int Hkv, int D, int W, swa_dtype dt) {
+  return dt == SWA_BF16 && D == swa::dectc::kD && W == swa::dectc::kW &&
+         Hq == Hkv * swa::dectc::kG;
+}
+
+swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const int64_t* pos,
+                            const float* sink, float* out, float* lse, int B, int Hq, int Hkv,
+                            cudaStream_t st, int dev) {
+  using namespace swa::dectc;
+  int sms;
+  if (!device_sms(dev, &sms)) return SWA_ECUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev[dev].dectc_attr) {
+      cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+      if (e != cudaSuccess) {
+        set_cuda_error("cudaFuncSetAttribute(decode_tc_kernel)", e);
+        return SWA_ECUDA;
+      }
+      g_dev[dev].dectc_attr = true;
+    }
+  }
+  const long long units = (long long)B * Hkv;
+  if (units * kW >= (1LL << 31) || (long long)B * Hq >= (1LL << 31)) {
+    set_error_text("problem too large for the tensor-core decode kernel");
+    return SWA_EUNSUPPORTED;
+  }
+  CUtensorMap mk, mv, mq;
+  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, kD, units * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, kD, units * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, (uint64_t)B * Hq, 1, 1, 64, kN,
+                   1))
+    return SWA_ECUDA;
+  Params p;
+  p.pos = pos;
+  p.sink = sink;
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.units = (int)units;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  const long long grid = units < sms ? units : sms;
+  decode_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, p);
+  return check_launch("decode_tc_kernel");
 }
 
 template <typename Tin, int D>
@@ -285,6 +387,8 @@ swa_status swa_sink_fwd(const void* q, const void* k, const void* v, const float
   switch (select_fwd(B, T, Hq, Hkv, D, W, in_dtype)) {
     case kPathTcSwa:
       return launch_tc_swa(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, st);
+    case kPathTcGlobal:
+      return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, st);
     case kPathSimt:
       if (in_dtype == SWA_F32)
         return launch_simt<float>(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, st);
@@ -311,6 +415,8 @@ swa_status swa_sink_decode(const void* q, const void* k_ring, const void* v_ring
   int dev;
   if (!current_device(&dev)) return SWA_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (decode_tc_applies(Hq, Hkv, D, W, in_dtype))
+    return launch_decode_tc(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, st, dev);
   if (in_dtype == SWA_F32) {
     if (D == 64)
       return launch_decode_g<float, 64>(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, W, st, dev);
@@ -352,9 +458,19 @@ swa_status swa_ring_append(const void* k_new, const void* v_new, void* k_ring, v
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype) {
   switch (select_fwd(B, T, Hq, Hkv, D, W, in_dtype)) {
     case kPathTcSwa: return "tc_swa";
+    case kPathTcGlobal: return "tc_global";
     case kPathSimt: return "simt";
     default: return "invalid";
   }
+}
+
+const char* swa_sink_decode_path(int B, int Hq, int Hkv, int D, int W, swa_dtype in_dtype) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || W < 1 || Hq % Hkv) return "invalid";
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return "invalid";
+  if (D != 64 && D != 128) return "invalid";
+  const int esz = in_dtype == SWA_F32 ? 4 : 2;
+  if (2LL * W * D * esz > swa::kDecodeMaxRingBytes) return "invalid";
+  return decode_tc_applies(Hq, Hkv, D, W, in_dtype) ? "tc_decode" : "simt_decode";
 }
 
 const char* swa_status_str(swa_status s) {

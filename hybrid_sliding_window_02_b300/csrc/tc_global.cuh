@@ -1,0 +1,462 @@
+// tc_global.cuh -- global (full causal) attention, and any window wider than
+// the sliding-window kernel covers, on the 5th-generation tensor cores.
+//
+// Operation: the same sink-biased softmax attention as the sliding-window
+// kernel ("MiMo-V2-Flash Technical Report" summary, section 前置知识: the
+// global layers of the hybrid stack attend to the whole causal prefix; every
+// head adds a learnable bias to its softmax denominator), for bf16 inputs,
+// D = 128 and groups of 8 query heads per kv head, any window W (W >= T is the
+// global layer).  Keys are visited in blocks of 128 with an online softmax:
+// the running max starts at the sink logit and the running denominator at
+// exp(sink - max), so the sink is counted exactly once whatever the order.
+//
+// Work item = one kv head of one sequence x 32 consecutive positions, split
+// into two Q tiles of 16 positions x 8 query heads (128 MMA rows each, row r =
+// position r / 8, head r % 8).  Both tiles share every K/V block the CTA
+// loads, which halves the K/V traffic out of L2 against one tile per block.
+// Items go to persistent CTAs (one per SM) in order of decreasing length
+// (longest causal prefix first), dealt round by round in alternating
+// direction, which keeps the per-CTA totals within about one item of each
+// other without any shared counter.
+//
+// Roles (320 threads):
+//   warp 8      TMA producer: the two Q tiles of an item, then K_j and V_j for
+//               every key block j into a ring of 32 KB slots
+//   warp 9      TMEM owner + single-thread tcgen05.mma issuer; per block j:
+//                 S_i = Q_i K_j^T  (SS, M = 128, N = 128, K = 128)   i = 0, 1
+//                 O_i += P_i V_j   (TS, P from TMEM, V MN-major, N = 128)
+//   warps 0..3  softmax of tile 0, warps 4..7 softmax of tile 1: thread =
+//               row; S -> mask -> running max / sum -> bf16 P written over S
+//               in TMEM; after the last block O / l -> out and the lse.
+// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i takes the
+// first 64 columns of S_i (bf16 pairs).  Because S_i(j+1) overwrites P_i(j),
+// it is issued only once O_i += P_i(j) V_j has completed (an MMA to another
+// accumulator is not ordered after it), so the order per block is
+// S0 S1 PV0 PV1 with the other tile's MMA in flight during every wait.
+//
+// Rescaling: the running max m only moves when a block's max exceeds it by
+// more than 8 (log2 units).  Otherwise p = 2^(x - m) <= 256 and the stale m
+// is kept; the final O / l is the same quotient.  When a row's max does move
+// after block 0, its warp rescales O in TMEM (read, multiply, write) before
+// releasing P: at that point every earlier PV of the tile has completed (the
+// S that the softmax just read was issued after it) and the next is not issued
+// until P is released.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace swa {
+namespace tcglobal {
+
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr int kG = 8;                   // query heads per tile (one kv group)
+constexpr int kD = 128;
+constexpr int kNpos = 16;               // positions per Q tile
+constexpr int kTiles = 2;               // Q tiles per work item
+constexpr int kItemPos = kNpos * kTiles;
+constexpr int kBlk = 128;               // keys per block
+constexpr uint32_t kSlots = 4;          // K/V ring slots (one K or V block each)
+constexpr float kRescaleLog2 = 8.0f;    // move the running max only past this
+
+// shared memory (bytes); swizzled operands 1024-aligned
+constexpr int kQHalf = 128 * 128;           // 128 rows x 64 bf16
+constexpr int kQTile = 2 * kQHalf;          // 32 KB
+constexpr int kSlotHalf = kBlk * 128;       // 128 keys x 64 bf16
+constexpr int kSlotBytes = 2 * kSlotHalf;   // 32 KB
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kTiles * kQTile;
+constexpr int kOffBar = kOffKV + (int)kSlots * kSlotBytes;
+constexpr int kBarQFull = 0, kBarQEmpty = kBarQFull + kTiles, kBarKvFull = kBarQEmpty + kTiles,
+              kBarKvEmpty = kBarKvFull + kSlots, kBarSFull = kBarKvEmpty + kSlots,
+              kBarPFull = kBarSFull + kTiles, kBarPvDone = kBarPFull + kTiles,
+              kBarOFull = kBarPvDone + kTiles, kBarDrain = kBarOFull + kTiles,
+              kNumBars = kBarDrain + 1;
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 8;
+constexpr int kSmemBytes = kOffAbort + 8 + 1024;  // + slack for 1024 alignment
+
+constexpr uint32_t kTmemCols = 512;
+// TMEM column of S_i / P_i and of O_i
+__host__ __device__ constexpr uint32_t col_s(int i) { return 128u * (uint32_t)i; }
+__host__ __device__ constexpr uint32_t col_o(int i) { return 256u + 128u * (uint32_t)i; }
+
+struct Params {
+  const float* sink;
+  float* out;
+  float* lse;
+  int B, T, Hq, Hkv, W;
+  int nitem_seq;      // ceil(T / 32)
+  int total_items;    // B * Hkv * nitem_seq (< 2^31, checked on the host)
+  float scale_log2;   // log2(e) / sqrt(D)
+};
+
+struct Item {
+  int b, kvh, p0;     // first position of tile 0
+  int jlo, nb;        // key blocks jlo .. jlo + nb - 1
+};
+
+// u-th item in order of decreasing causal length.
+__device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
+  Item it;
+  const uint32_t bkn = (uint32_t)(p.B * p.Hkv);
+  const uint32_t r = u / bkn;
+  const uint32_t bk = u - r * bkn;
+  const int n2 = p.nitem_seq - 1 - (int)r;
+  it.b = (int)(bk / (uint32_t)p.Hkv);
+  it.kvh = (int)(bk - (uint32_t)it.b * (uint32_t)p.Hkv);
+  it.p0 = n2 * kItemPos;
+  const int last = min(it.p0 + kItemPos - 1, p.T - 1);
+  const int first_key = max(0, it.p0 - p.W + 1);
+  it.jlo = first_key / kBlk;
+  it.nb = last / kBlk - it.jlo + 1;
+  return it;
+}
+
+// The k-th item of CTA c: rounds of gridDim.x items, dealt in alternating
+// direction.  Returns false past the end.
+__device__ __forceinline__ bool cta_item(int k, const Params& p, Item& it) {
+  const uint32_t g = gridDim.x;
+  const uint32_t idx = (k & 1) ? (g - 1 - blockIdx.x) : blockIdx.x;
+  const uint64_t u = (uint64_t)k * g + idx;
+  if (u >= (uint64_t)p.total_items) return false;
+  it = item_coords((uint32_t)u, p);
+  return true;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+  reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(r));
+  reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    swa_fwd_tc_global_kernel(const __grid_constant__ CUtensorMap map_q,
+                             const __grid_constant__ CUtensorMap map_k,
+                             const __grid_constant__ CUtensorMap map_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < kTiles; ++i) {
+      mbar_init(bar(kBarQFull + i), 1);
+      mbar_init(bar(kBarQEmpty + i), 1);
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarPFull + i), 128);
+      mbar_init(bar(kBarPvDone + i), 1);
+      mbar_init(bar(kBarOFull + i), 1);
+    }
+    for (uint32_t s = 0; s < kSlots; ++s) {
+      mbar_init(bar(kBarKvFull + s), 1);
+      mbar_init(bar(kBarKvEmpty + s), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProducer && lane == 0) {
+    prefetch_tmap(&map_q);
+    prefetch_tmap(&map_k);
+    prefetch_tmap(&map_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+
+  if (warp == kWarpProducer) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      uint32_t seq = 0;  // K/V blocks loaded so far (K and V count separately)
+      uint32_t q_armed[kTiles] = {};  // Q loads issued per tile
+      Item it;
+      bool ok = true;
+      for (int k = 0; ok && cta_item(k, p, it); ++k) {
+        for (int i = 0; i < kTiles; ++i) {
+          if (!mbar_wait(bar(kBarQEmpty + i), (k & 1) ^ 1, kErrWaitQEmpty, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t qdst = sbase + kOffQ + i * kQTile;
+          const int pos = it.p0 + i * kNpos;
+          mbar_arrive_expect_tx(bar(kBarQFull + i), kQTile);
+          tma_load_4d(qdst, &map_q, 0, it.kvh * kG, pos, it.b, bar(kBarQFull + i));
+          tma_load_4d(qdst + kQHalf, &map_q, 64, it.kvh * kG, pos, it.b, bar(kBarQFull + i));
+          ++q_armed[i];
+        }
+        for (int t = 0; ok && t < 2 * it.nb; ++t, ++seq) {
+          const uint32_t slot = seq % kSlots;
+          if (!mbar_wait(bar(kBarKvEmpty + slot), ((seq / kSlots) & 1) ^ 1, kErrWaitKvEmpty,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = (t & 1) ? &map_v : &map_k;
+          const int key = (it.jlo + (t >> 1)) * kBlk;
+          const uint32_t dst = sbase + kOffKV + slot * kSlotBytes;
+          const uint32_t fb = bar(kBarKvFull + slot);
+          mbar_arrive_expect_tx(fb, kSlotBytes);
+          tma_load_4d(dst, map, 0, it.kvh, key, it.b, fb);
+          tma_load_4d(dst + kSlotHalf, map, 64, it.kvh, key, it.b, fb);
+        }
+      }
+      // Copies still in flight must land before the CTA exits: wait (bounded)
+      // for the last phase armed on every barrier a copy signals.
+      if (!ok) {
+        for (int i = 0; i < kTiles; ++i)
+          if (q_armed[i] > 0) mbar_wait_drain(bar(kBarQFull + i), (q_armed[i] - 1) & 1);
+        for (uint32_t s = (seq > kSlots ? seq - kSlots : 0); s < seq; ++s)
+          mbar_wait_drain(bar(kBarKvFull + s % kSlots), (s / kSlots) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc_bf16(kBlk, false, false);
+      const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
+      const uint64_t qdesc0 = umma_sdesc(sbase + kOffQ, 16, 1024, 2);
+      const uint64_t kdesc0 = umma_sdesc(sbase + kOffKV, 16, 1024, 2);
+      const uint64_t vdesc0 = umma_sdesc(sbase + kOffKV, kSlotHalf, 1024, 2);
+      uint32_t seq = 0;
+      uint32_t npv = 0;  // PV groups issued per tile (identical for both tiles)
+      bool ok = true;
+      Item it;
+      for (int k = 0; ok && cta_item(k, p, it); ++k) {
+        for (int i = 0; i < kTiles && ok; ++i)
+          ok = mbar_wait(bar(kBarQFull + i), k & 1, kErrWaitQFull, abort_flag);
+        for (int t = 0; ok && t < it.nb; ++t) {
+          // ---- S_i = Q_i K^T ----
+          const uint32_t ks = seq % kSlots;
+          if (!mbar_wait(bar(kBarKvFull + ks), (seq / kSlots) & 1, kErrWaitKvFull, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ++seq;
+          for (int i = 0; i < kTiles; ++i) {
+            // S_i overwrites P_i of the previous block: its PV must be done
+            if (npv > 0 &&
+                !mbar_wait(bar(kBarPvDone + i), (npv - 1) & 1, kErrWaitPvDone, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t qd = qdesc0 + (uint32_t)(i * kQTile >> 4);
+            const uint64_t kd = kdesc0 + (ks * kSlotBytes >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+              const uint32_t b_off = ((kk >> 2) * kSlotHalf + (kk & 3) * 32) >> 4;
+              umma_bf16_ss(tmem + col_s(i), qd + a_off, kd + b_off, idesc_s, kk > 0);
+            }
+            umma_commit(bar(kBarSFull + i));
+          }
+          if (!ok) break;
+          umma_commit(bar(kBarKvEmpty + ks));
+          if (t == it.nb - 1)
+            for (int i = 0; i < kTiles; ++i) umma_commit(bar(kBarQEmpty + i));
+          // ---- O_i += P_i V ----
+          const uint32_t vs = seq % kSlots;
+          if (!mbar_wait(bar(kBarKvFull + vs), (seq / kSlots) & 1, kErrWaitKvFull, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ++seq;
+          for (int i = 0; i < kTiles; ++i) {
+            if (!mbar_wait(bar(kBarPFull + i), npv & 1, kErrWaitPFull, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vd = vdesc0 + (vs * kSlotBytes >> 4);
+#pragma unroll
+            for (int kb = 0; kb < kBlk / 16; ++kb)
+              umma_bf16_ts(tmem + col_o(i), tmem + col_s(i) + kb * 8,
+                           vd + (uint32_t)(kb * 16 * 128 >> 4), idesc_o, (t > 0 || kb > 0));
+            umma_commit(bar(kBarPvDone + i));
+            if (t == it.nb - 1) umma_commit(bar(kBarOFull + i));
+          }
+          if (!ok) break;
+          ++npv;
+          umma_commit(bar(kBarKvEmpty + vs));
+        }
+      }
+      // every MMA issued so far completes before TMEM is released
+      umma_commit(bar(kBarDrain));
+      mbar_wait_drain(bar(kBarDrain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax + epilogue (warps 0..7) =======================
+    const int ti = warp >> 2;                       // Q tile of this warpgroup
+    const int quad = warp & 3;                      // TMEM lanes [32 quad, 32 quad + 32)
+    const int r = quad * 32 + lane;                 // tile row
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + col_s(ti);
+    const uint32_t o_addr = tmem + lane_addr + col_o(ti);
+    const int g = r & 7;
+    uint32_t npv = 0;
+    Item it;
+    for (int k = 0; cta_item(k, p, it); ++k) {
+      const int h = it.kvh * kG + g;
+      const int pos = it.p0 + ti * kNpos + (r >> 3);
+      const float sk = p.sink[h] * 1.4426950408889634f;  // log2 units
+      float m_run = sk;                                   // -inf for no sink
+      float l = (sk == -INFINITY) ? 0.f : 1.f;            // exp2(sk - m_run)
+      // valid keys of this row: [key_lo, pos]
+      const int key_lo = max(0, pos - p.W + 1);
+      bool ok = true;
+      for (int t = 0; t < it.nb; ++t, ++npv) {
+        const int key0 = (it.jlo + t) * kBlk;
+        const int c_lo = key_lo - key0, c_hi = pos - key0;
+        if (!mbar_wait(bar(kBarSFull + ti), npv & 1, kErrWaitSFull, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[kBlk];
+#pragma unroll
+        for (int c = 0; c < kBlk / 32; ++c) tmem_ld32(s_addr + c * 32, sr + c * 32);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < kBlk / 32; ++c) reg_fence32(sr + c * 32);
+        // mask in place: scores outside [c_lo, c_hi] become -inf
+        const bool full = __all_sync(0xffffffffu, c_lo <= 0 && c_hi >= kBlk - 1);
+        if (!full) {
+#pragma unroll
+          for (int c = 0; c < kBlk; ++c)
+            if (c < c_lo || c > c_hi) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // block max: 8 independent chains of 3-input max, then a tree
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(__uint_as_float(sr[e]), __uint_as_float(sr[e + 8]));
+#pragma unroll
+        for (int c = 16; c < kBlk; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            m8[e] = max3f(m8[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
+        const float mraw = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                                 fmaxf(m8[6], m8[7]));
+        const float m_cand = mraw * p.scale_log2;  // scale > 0 commutes with max
+        const bool grow = m_cand > m_run + kRescaleLog2;  // false for -inf
+        float f = 1.f;                                    // factor for O and l
+        if (grow) {
+          f = ex2_approx(m_run - m_cand);
+          l *= f;
+          m_run = m_cand;
+        }
+        const float mb = (m_run == -INFINITY) ? 0.f : m_run;
+        // p = 2^(x - m) -> bf16 pairs over the first 64 columns of S, 16 at a time
+        float l8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) l8[e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < kBlk / 16; ++c) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float a = ex2_approx(fmaf(__uint_as_float(sr[16 * c + 2 * e]), p.scale_log2, -mb));
+            const float b = ex2_approx(fmaf(__uint_as_float(sr[16 * c + 2 * e + 1]), p.scale_log2, -mb));
+            l8[e] += a + b;
+            pk[e] = pack_bf16x2(a, b);
+          }
+          tmem_st8(s_addr + c * 8, pk);
+        }
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        // A moved max also rescales O, which holds the earlier blocks complete
+        // (every PV before this block's S has finished); block 0 has no O yet.
+        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + c * 32, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(o_addr + c * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull + ti));
+      }
+      if (!ok) break;
+      // ---- epilogue: out = O / l, lse ----
+      if (!mbar_wait(bar(kBarOFull + ti), k & 1, kErrWaitOFull, abort_flag)) break;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      float* orow = p.out + (((long long)it.b * p.T + pos) * p.Hq + h) * kD;
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + c * 32, o);
+        tmem_ld_wait();
+        reg_fence32(o);
+        if (pos < p.T) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            st_global_v4(orow + c * 32 + 4 * e, o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        }
+      }
+      tc_fence_before();
+      if (p.lse != nullptr && pos < p.T)
+        p.lse[((long long)it.b * p.Hq + h) * p.T + pos] =
+            (m_run + __log2f(l)) * 0.6931471805599453f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace tcglobal
+}  // namespace swa

@@ -103,6 +103,11 @@ swa_status swa_ring_append(const void* k_new, const void* v_new, void* k_ring, v
  * ("tc_swa", "tc_global", "simt"), or "invalid". */
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
+/* Name of the decode kernel swa_sink_decode would launch for these sizes
+ * ("tc_decode" for bf16, D = 128, W = 128, Hq = 8 Hkv; "simt_decode"
+ * otherwise), or "invalid". */
+const char* swa_sink_decode_path(int B, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
+
 /* Static text for a status code. */
 const char* swa_status_str(swa_status s);
 

@@ -47,12 +47,25 @@ def test_status_strings_and_version(L):
 def test_path_selection(L):
     assert swa.fwd_path(4, 8192, 64, 8, 128, 128) == "tc_swa"
     assert swa.fwd_path(1, 262144, 64, 8, 128, 128) == "tc_swa"
+    assert swa.fwd_path(1, 512, 64, 8, 128, 129) == "tc_swa"
+    assert swa.fwd_path(1, 512, 64, 8, 128, 130) == "tc_global"
+    assert swa.fwd_path(1, 32768, 64, 8, 128, 32768) == "tc_global"
     assert swa.fwd_path(1, 512, 4, 1, 64, 128, swa.SWA_F32) == "simt"
     assert swa.fwd_path(1, 512, 64, 8, 128, 128, swa.SWA_F32) == "simt"
     assert swa.fwd_path(1, 512, 64, 64, 128, 128) == "simt"
     assert swa.fwd_path(1, 512, 64, 7, 128, 128) == "invalid"
     assert swa.fwd_path(1, 512, 64, 8, 96, 128) == "invalid"
     assert swa.fwd_path(0, 512, 64, 8, 128, 128) == "invalid"
+
+
+def test_decode_path_selection(L):
+    assert swa.decode_path(256, 64, 8, 128, 128) == "tc_decode"
+    assert swa.decode_path(256, 64, 8, 128, 128, swa.SWA_F32) == "simt_decode"
+    assert swa.decode_path(256, 64, 8, 64, 128) == "simt_decode"
+    assert swa.decode_path(256, 32, 8, 128, 128) == "simt_decode"
+    assert swa.decode_path(256, 64, 8, 128, 320) == "simt_decode"
+    assert swa.decode_path(256, 64, 8, 128, 321) == "invalid"
+    assert swa.decode_path(256, 64, 7, 128, 128) == "invalid"
 
 
 A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced by these calls

@@ -103,5 +103,34 @@ def test_decode_after_appends_equals_prefill_row(cuda_ok):
     assert_bf16_close(o.cpu().double().numpy().reshape(-1, D), o_ref)
 
 
+def test_tc_decode_selected_for_the_workload_shape(cuda_ok):
+    assert swa.decode_path(256, 64, 8, 128, 128) == "tc_decode"
+    assert swa.decode_path(3, 8, 1, 128, 128) == "tc_decode"
+    assert swa.decode_path(3, 8, 1, 128, 64) == "simt_decode"
+
+
+def test_tc_decode_negative_position_is_empty(cuda_ok):
+    # a negative position leaves every slot empty: out = 0, lse = sink
+    x = gen.decode_inputs(3, 16, 2, 128, 128, seed=9, pos_lo=0, pos_hi=500)
+    x.pos[1] = -1
+    o, l = _decode(x)
+    assert np.all(o[1] == 0.0)
+    assert np.allclose(l[1], x.sink.double().numpy(), atol=1e-6)
+    keep = [0, 2]
+    o_ref, l_ref = oracle.swa_sink_decode(x.q[keep], x.k_ring[keep], x.v_ring[keep],
+                                          x.pos[keep], x.sink)
+    assert_bf16_close(o[keep], o_ref)
+    assert_lse_close(l[keep], l_ref)
+
+
+def test_tc_decode_uneven_groups_per_cta(cuda_ok):
+    # more groups than SMs and not a multiple of them: CTAs take 2 or 3 groups
+    x = gen.decode_inputs(37, 64, 8, 128, 128, seed=10)
+    o, l = _decode(x)
+    o_ref, l_ref = oracle.swa_sink_decode(x.q, x.k_ring, x.v_ring, x.pos, x.sink)
+    assert_bf16_close(o, o_ref)
+    assert_lse_close(l, l_ref)
+
+
 def test_decode_no_device_error(cuda_ok):
     assert swa.device_error() == 0
