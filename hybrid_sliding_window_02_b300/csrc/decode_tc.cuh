@@ -169,12 +169,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_bf16(kN, false, false);
       const uint32_t idesc_o = umma_idesc_bf16(kN, true, false);
-      for (int k = 0; k < nk; ++k) {
+      // S^T of group k into TMEM buffer k % 2 once its stage has landed.  The
+      // buffer was last read by the softmax of group k - 2, which released it
+      // (P full) before this thread issued the PV of group k - 2.
+      auto issue_s = [&](int k) -> bool {
         const uint32_t s = (uint32_t)k % kStages;
-        const int w = k & 1;
         if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
                        abort_flag))
-          break;
+          return false;
         tc_fence_after();
         const uint32_t st = sbase + kOffStage + s * kStageBytes;
         const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
@@ -183,13 +185,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t a_off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
           const uint32_t b_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + col_s(w), kdesc + a_off, qdesc + b_off, idesc_s, kk > 0);
+          umma_bf16_ss(tmem + col_s(k & 1), kdesc + a_off, qdesc + b_off, idesc_s, kk > 0);
         }
-        umma_commit(bar(kBarSFull + w));
+        umma_commit(bar(kBarSFull + (k & 1)));
+        return true;
+      };
+      // S of the next group goes in before the wait for this group's P, so
+      // that the two softmax warpgroups work on consecutive groups at once.
+      bool ok = nk > 0 && issue_s(0);
+      for (int k = 0; ok && k < nk; ++k) {
+        if (k + 1 < nk && !issue_s(k + 1)) break;
+        const uint32_t s = (uint32_t)k % kStages;
+        const int w = k & 1;
         // O^T = V^T P^T once the softmax of this group has written P^T
         if (!mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag))
           break;
         tc_fence_after();
+        const uint32_t st = sbase + kOffStage + s * kStageBytes;
         const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
         const uint64_t pdesc = umma_sdesc(sbase + kOffP + w * kPBytes, 16, 1024, 2);
 #pragma unroll

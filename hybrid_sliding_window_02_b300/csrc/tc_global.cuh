@@ -388,23 +388,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = m_cand;
         }
         const float mb = (m_run == -INFINITY) ? 0.f : m_run;
-        // p = 2^(x - m) -> bf16 pairs over the first 64 columns of S, 16 at a time
-        float l8[8];
+        // p = 2^(x - m) -> bf16 pairs over the first 64 columns of S, 16 at a
+        // time; the scale-and-subtract and the running sum go two columns per
+        // instruction (f32x2)
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nmb2 = make_float2(-mb, -mb);
+        float2 l2[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) l8[e] = 0.f;
+        for (int e = 0; e < 4; ++e) l2[e] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kBlk / 16; ++c) {
           uint32_t pk[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float a = ex2_approx(fmaf(__uint_as_float(sr[16 * c + 2 * e]), p.scale_log2, -mb));
-            const float b = ex2_approx(fmaf(__uint_as_float(sr[16 * c + 2 * e + 1]), p.scale_log2, -mb));
-            l8[e] += a + b;
-            pk[e] = pack_bf16x2(a, b);
+            const float2 xx = ffma2(make_float2(__uint_as_float(sr[16 * c + 2 * e]),
+                                                __uint_as_float(sr[16 * c + 2 * e + 1])),
+                                    sc2, nmb2);
+            const float2 pp = make_float2(ex2_approx(xx.x), ex2_approx(xx.y));
+            l2[e & 3] = fadd2(l2[e & 3], pp);
+            pk[e] = pack_bf16x2(pp.x, pp.y);
           }
           tmem_st8(s_addr + c * 8, pk);
         }
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        {
+          const float2 a = fadd2(fadd2(l2[0], l2[1]), fadd2(l2[2], l2[3]));
+          l += a.x + a.y;
+        }
         // A moved max also rescales O, which holds the earlier blocks complete
         // (every PV before this block's S has finished); block 0 has no O yet.
         if (t > 0 && __any_sync(0xffffffffu, grow)) {
