@@ -10,14 +10,15 @@ Every function follows the definition quoted in ``swa_oracle.c``:
 sliding-window causal attention (window W, W >= T = global layer) with GQA and
 a learnable per-head bias added to the softmax denominator ("MiMo-V2-Flash
 Technical Report" summary, section 前置知识: 混合注意力机制, 注意力sink偏置),
-and one-token decode against a W-slot ring cache ("pwwt.cn" MiMo-V2-Flash essay,
-section 1.1: fixed-size sliding-window KV cache).
+one-token decode against a W-slot ring cache ("pwwt.cn" MiMo-V2-Flash essay,
+section 1.1: fixed-size sliding-window KV cache), and the multi-token verify of
+drafted tokens against that ring.
 
 Pins (what ties these functions to something other than themselves) live in
 ``tests/test_oracle_pins.py``: brute force with explicit score matrices, the
 sink -> -inf / +inf limits, W >= T against a library causal-attention routine,
 weights + sink summing to one, the closed form at W = 1, decode = prefill row,
-and poisoned out-of-window keys.
+verify = prefill rows, and poisoned out-of-window keys.
 """
 from __future__ import annotations
 
@@ -60,8 +61,10 @@ def _load():
                                                      i32, i32, i64, i32, i32]
             lib.oracle_swa_sink_decode.argtypes = [p, p, p, p, p, p, p, i64, i32, i32, i32, i64,
                                                    i32, i32]
+            lib.oracle_swa_sink_verify.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i32, i32,
+                                                   i32, i64, i32, i32]
             for f in (lib.oracle_swa_sink_fwd, lib.oracle_swa_sink_fwd_rows,
-                      lib.oracle_swa_sink_decode):
+                      lib.oracle_swa_sink_decode, lib.oracle_swa_sink_verify):
                 f.restype = i32
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -157,6 +160,38 @@ def swa_sink_fwd_rows(q, k, v, sink, W: int, rows, nthreads: int = 0):
                                           int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_swa_sink_fwd_rows failed ({rc})")
+    return out, lse
+
+
+def _pos64(pos):
+    try:
+        import torch
+        if isinstance(pos, torch.Tensor):
+            pos = pos.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(pos, dtype=np.int64)
+
+
+def swa_sink_verify(q, k_new, v_new, k_ring, v_ring, pos, sink, nthreads: int = 0):
+    """Multi-token verify oracle.  q [B,L,Hq,D], k_new/v_new [B,L,Hkv,D],
+    rings [B,Hkv,W,D] holding the positions before pos, pos [B] int64 = the
+    position of new token 0, sink [Hq].
+
+    Returns (out [B,L,Hq,D] float64, lse [B,Hq,L] float64).
+    """
+    (qa, kna, vna, kra, vra), code = _same_type(q, k_new, v_new, k_ring, v_ring)
+    B, L, Hq, D = qa.shape
+    Hkv, W = kra.shape[1], kra.shape[2]
+    pa = _pos64(pos)
+    s = _sink64(sink)
+    out = np.empty((B, L, Hq, D), dtype=np.float64)
+    lse = np.empty((B, Hq, L), dtype=np.float64)
+    rc = _load().oracle_swa_sink_verify(_ptr(qa), _ptr(kna), _ptr(vna), _ptr(kra), _ptr(vra),
+                                        _ptr(pa), _ptr(s), _ptr(out), _ptr(lse), B, L, Hq, Hkv,
+                                        D, W, code, int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_swa_sink_verify failed ({rc})")
     return out, lse
 
 

@@ -32,6 +32,12 @@
  *   p(s) = pos - ((pos - s) mod W); slots with p(s) < 0 are empty and skipped.
  *   Then the same formula as above over the valid slots.
  *
+ *   Multi-token verify: L drafted tokens at positions pos..pos+L-1 are checked
+ *   in one pass (the multi-token prediction drafts of the MiMo-V2-Flash
+ *   technical report summary, section 核心方法); their keys and values come
+ *   separately and the ring holds the tokens before pos.  Each new token takes
+ *   the keys of its own window, as in the prefill (see oracle_swa_sink_verify).
+ *
  * Inputs arrive in their storage type (dtype code 0 = fp32, 1 = bf16 bit
  * patterns, 2 = fp64) and are widened to fp64 exactly; all arithmetic is fp64
  * with libm exp/log.  Layouts: q [B,T,Hq,D], k/v [B,T,Hkv,D], out [B,T,Hq,D],
@@ -193,6 +199,80 @@ int oracle_swa_sink_decode(const void* q, const void* k_ring, const void* v_ring
       }
     }
     free(koff); free(x);
+  }
+  return bad ? -2 : 0;
+}
+
+/* Multi-token verify (speculative decoding with multi-token prediction: the
+ * drafted tokens are checked in one pass).  L new tokens sit at positions
+ * pos, ..., pos+L-1; their keys and values arrive in k_new / v_new, and the
+ * W-slot ring holds the tokens before them: slot s holds position
+ * p(s) = (pos-1) - ((pos-1-s) mod W), empty when p(s) < 0.  New token j
+ * attends to the positions [pos+j-W+1, pos+j] of the same definition as the
+ * prefill: the ring slots whose positions fall there, then new tokens 0..j.
+ * Layouts: q [B,L,Hq,D], k_new/v_new [B,L,Hkv,D], rings [B,Hkv,W,D],
+ * out [B,L,Hq,D], lse [B,Hq,L]. */
+int oracle_swa_sink_verify(const void* q, const void* k_new, const void* v_new,
+                           const void* k_ring, const void* v_ring, const int64_t* pos,
+                           const double* sink, double* out, double* lse, int64_t B, int64_t L,
+                           int Hq, int Hkv, int D, int64_t W, int dtype, int nthreads) {
+  if (B < 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || W <= 0) return -1;
+  for (int64_t b = 0; b < B; ++b)
+    if (pos[b] < 0) return -1;
+  const int64_t G = Hq / Hkv;
+  const int64_t nrows = B * L * Hq;
+  const double inv_sqrt_d = 1.0 / sqrt((double)D);
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
+  {
+    /* key n: source (0 = ring, 1 = new) and element offset of its vector */
+    int* src = (int*)malloc(sizeof(int) * (W + L));
+    int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (W + L));
+    double* x = (double*)malloc(sizeof(double) * (W + L));
+    if (!src || !koff || !x) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t b = r / (L * Hq), j = (r / Hq) % L, h = r % Hq, kv = h / G;
+        const int64_t p_now = pos[b] + j;          /* position of this query */
+        const int64_t lo = p_now - W + 1;          /* first position in its window */
+        int n = 0;
+        for (int64_t s = 0; s < W; ++s) {
+          const int64_t p = (pos[b] - 1) - (((pos[b] - 1 - s) % W + W) % W);
+          if (p < 0 || p < lo) continue;
+          src[n] = 0;
+          koff[n++] = ((b * Hkv + kv) * W + s) * D;
+        }
+        for (int64_t i = 0; i <= j; ++i) {
+          if (pos[b] + i < lo) continue;           /* only when W <= j */
+          src[n] = 1;
+          koff[n++] = ((b * L + i) * Hkv + kv) * D;
+        }
+        const int64_t qoff = ((b * L + j) * Hq + h) * D;
+        double m = sink[h];
+        for (int k = 0; k < n; ++k) {
+          const void* kb = src[k] ? k_new : k_ring;
+          double dot = 0.0;
+          for (int d = 0; d < D; ++d) dot += widen(q, dtype, qoff + d) * widen(kb, dtype, koff[k] + d);
+          x[k] = dot * inv_sqrt_d;
+          if (x[k] > m) m = x[k];
+        }
+        double l = exp(sink[h] - m);
+        double* o = out + qoff;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int k = 0; k < n; ++k) {
+          const void* vb = src[k] ? v_new : v_ring;
+          const double e = exp(x[k] - m);
+          l += e;
+          for (int d = 0; d < D; ++d) o[d] += e * widen(vb, dtype, koff[k] + d);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= l;
+        lse[(b * Hq + h) * L + j] = m + log(l);
+      }
+    }
+    free(src); free(koff); free(x);
   }
   return bad ? -2 : 0;
 }

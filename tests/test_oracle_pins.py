@@ -271,3 +271,64 @@ def test_decode_slot_mapping_wraps():
     ob, lb = brute_force(x.q, x.k, x.v, x.sink, W)
     np.testing.assert_allclose(o[0], ob[0, 10], rtol=0, atol=1e-12)
     np.testing.assert_allclose(l[0], lb[0, :, 10], rtol=0, atol=1e-12)
+
+
+def _verify_case(x, pos, L, W):
+    """Split a history into (ring before pos, L new tokens) for each sequence."""
+    B = x.q.shape[0]
+    kr, vr = gen.ring_from_history(x.k, x.v, pos - 1, W)
+    idx = [torch.arange(int(p), int(p) + L) for p in pos]
+    qn = torch.stack([x.q[b, idx[b]] for b in range(B)])
+    kn = torch.stack([x.k[b, idx[b]] for b in range(B)])
+    vn = torch.stack([x.v[b, idx[b]] for b in range(B)])
+    return qn, kn, vn, kr, vr
+
+
+@pytest.mark.parametrize("W", [1, 3, 8])
+@pytest.mark.parametrize("L", [1, 2, 4, 10])
+def test_verify_equals_prefill_rows(W, L):
+    # drafted tokens checked in one pass equal the prefill rows at their
+    # positions: the ring carries what precedes them, the window slides on
+    B, T, Hq, Hkv, D = 3, 40, 4, 2, 16
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=41 + W + L, dtype=torch.bfloat16)
+    o_pre, l_pre = oracle.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+    for pos_list in ([0, 1, 2], [W - 1, W, W + 1], [T - L, 13, 2 * W + 3]):
+        pos = torch.tensor([max(0, min(p, T - L)) for p in pos_list], dtype=torch.int64)
+        qn, kn, vn, kr, vr = _verify_case(x, pos, L, W)
+        o, l = oracle.swa_sink_verify(qn, kn, vn, kr, vr, pos, x.sink)
+        for b in range(B):
+            p = int(pos[b])
+            np.testing.assert_allclose(o[b], o_pre[b, p:p + L], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(l[b], l_pre[b, :, p:p + L], rtol=0, atol=1e-12)
+
+
+def test_verify_one_token_is_decode_after_append():
+    B, T, Hq, Hkv, D, W = 4, 30, 4, 1, 16, 8
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=51, dtype=torch.float32)
+    pos = torch.tensor([0, 5, 8, 29], dtype=torch.int64)
+    qn, kn, vn, kr, vr = _verify_case(x, pos, 1, W)
+    o, l = oracle.swa_sink_verify(qn, kn, vn, kr, vr, pos, x.sink)
+    kr2, vr2 = gen.ring_from_history(x.k, x.v, pos, W)   # token at pos appended
+    od, ld = oracle.swa_sink_decode(qn[:, 0], kr2, vr2, pos, x.sink)
+    np.testing.assert_allclose(o[:, 0], od, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l[:, :, 0], ld, rtol=0, atol=1e-12)
+
+
+def test_verify_ignores_slots_outside_every_window():
+    # the slot holding pos - W is outside the window of every new token, and
+    # slots of negative positions are empty: NaN there changes nothing
+    B, T, Hq, Hkv, D, W, L = 3, 30, 4, 2, 16, 8, 3
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=52, dtype=torch.float32)
+    pos = torch.tensor([3, 8, 20], dtype=torch.int64)
+    qn, kn, vn, kr, vr = _verify_case(x, pos, L, W)
+    ref = oracle.swa_sink_verify(qn, kn, vn, kr, vr, pos, x.sink)
+    for b in range(B):
+        p = int(pos[b])
+        for s in range(W):
+            ps = (p - 1) - ((p - 1 - s) % W)
+            if ps < 0 or ps < p - W + 1:
+                kr[b, :, s] = float("nan")
+                vr[b, :, s] = float("nan")
+    got = oracle.swa_sink_verify(qn, kn, vn, kr, vr, pos, x.sink)
+    assert np.all(np.isfinite(got[0]))
+    assert np.array_equal(ref[0], got[0]) and np.array_equal(ref[1], got[1])
