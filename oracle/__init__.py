@@ -63,8 +63,9 @@ def _load():
                                                    i32, i32]
             lib.oracle_swa_sink_verify.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i32, i32,
                                                    i32, i64, i32, i32]
+            lib.oracle_rope.argtypes = [p, p, p, i64, i64, i32, i32, i32, ctypes.c_double, i32]
             for f in (lib.oracle_swa_sink_fwd, lib.oracle_swa_sink_fwd_rows,
-                      lib.oracle_swa_sink_decode, lib.oracle_swa_sink_verify):
+                      lib.oracle_swa_sink_decode, lib.oracle_swa_sink_verify, lib.oracle_rope):
                 f.restype = i32
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -193,6 +194,20 @@ def swa_sink_verify(q, k_new, v_new, k_ring, v_ring, pos, sink, nthreads: int = 
     if rc != 0:
         raise ValueError(f"oracle_swa_sink_verify failed ({rc})")
     return out, lse
+
+
+def rope(x, pos0, rot_dim: int, theta: float):
+    """Rotary embedding of x [B,T,H,D] (token (b, t) at position pos0[b] + t),
+    rotate-half form over the first rot_dim dims.  Returns float64 [B,T,H,D]."""
+    (xa,), code = _same_type(x)
+    B, T, H, D = xa.shape
+    pa = _pos64(pos0)
+    y = np.empty((B, T, H, D), dtype=np.float64)
+    rc = _load().oracle_rope(_ptr(xa), _ptr(pa), _ptr(y), B, T, H, D, int(rot_dim),
+                             float(theta), code)
+    if rc != 0:
+        raise ValueError(f"oracle_rope failed ({rc})")
+    return y
 
 
 def swa_sink_decode(q, k_ring, v_ring, pos, sink, nthreads: int = 0):

@@ -277,4 +277,37 @@ int oracle_swa_sink_verify(const void* q, const void* k_new, const void* v_new,
   return bad ? -2 : 0;
 }
 
+/* Rotary position embedding, applied to q and k before attention (ICML 2026
+ * talk write-up, Q&A K: RoPE's theta is fixed at inference and the position
+ * index keeps counting up while the window slides, so each token is rotated
+ * at its absolute position).  The pages give no variant; this is the
+ * rotate-half form over the first rot_dim dimensions: for i < rot_dim / 2,
+ *   a_i = p * theta^(-2 i / rot_dim)
+ *   y[i]             = x[i] cos a_i - x[i + rot_dim/2] sin a_i
+ *   y[i + rot_dim/2] = x[i + rot_dim/2] cos a_i + x[i] sin a_i
+ * and y[d] = x[d] for d >= rot_dim.  x is [B, T, H, D] in its storage type,
+ * token (b, t) at position pos0[b] + t; y is written in fp64. */
+int oracle_rope(const void* x, const int64_t* pos0, double* y, int64_t B, int64_t T, int H,
+                int D, int rot_dim, double theta, int dtype) {
+  if (B < 0 || T < 0 || H <= 0 || D <= 0 || rot_dim < 0 || rot_dim > D || rot_dim % 2 ||
+      !(theta > 0.0))
+    return -1;
+  const int half = rot_dim / 2;
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t t = 0; t < T; ++t) {
+      const double p = (double)(pos0[b] + t);
+      for (int h = 0; h < H; ++h) {
+        const int64_t base = ((b * T + t) * H + h) * D;
+        for (int i = 0; i < half; ++i) {
+          const double a = p * pow(theta, -2.0 * i / rot_dim);
+          const double x0 = widen(x, dtype, base + i), x1 = widen(x, dtype, base + i + half);
+          y[base + i] = x0 * cos(a) - x1 * sin(a);
+          y[base + i + half] = x1 * cos(a) + x0 * sin(a);
+        }
+        for (int d = rot_dim; d < D; ++d) y[base + d] = widen(x, dtype, base + d);
+      }
+    }
+  return 0;
+}
+
 int oracle_num_threads(void) { return omp_get_max_threads(); }

@@ -332,3 +332,42 @@ def test_verify_ignores_slots_outside_every_window():
     got = oracle.swa_sink_verify(qn, kn, vn, kr, vr, pos, x.sink)
     assert np.all(np.isfinite(got[0]))
     assert np.array_equal(ref[0], got[0]) and np.array_equal(ref[1], got[1])
+
+
+# ---- rotary position embedding (applied to q and k before attention) -------
+def test_rope_position_zero_is_identity():
+    x = torch.randn(2, 1, 3, 16, dtype=torch.float64)
+    y = oracle.rope(x, torch.tensor([0, 0]), 16, 10000.0)
+    np.testing.assert_array_equal(y, x.numpy())
+
+
+def test_rope_two_dims_is_a_plane_rotation():
+    # D = 2: (x0, x1) rotated by the angle p (theta^0 = 1)
+    x = torch.tensor([[[[0.3, -1.7]]]], dtype=torch.float64).repeat(1, 5, 1, 1)
+    y = oracle.rope(x, torch.tensor([7]), 2, 10000.0)
+    for t in range(5):
+        a = 7.0 + t
+        np.testing.assert_allclose(y[0, t, 0], [0.3 * math.cos(a) + 1.7 * math.sin(a),
+                                                -1.7 * math.cos(a) + 0.3 * math.sin(a)],
+                                   rtol=0, atol=1e-14)
+
+
+def test_rope_preserves_norms_and_passes_the_rest():
+    x = torch.randn(1, 9, 2, 64, dtype=torch.float64)
+    y = oracle.rope(x, torch.tensor([100000]), 48, 5e5)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x.numpy(), axis=-1),
+                               rtol=1e-13)
+    np.testing.assert_array_equal(y[..., 48:], x.numpy()[..., 48:])
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    # <R(p) q, R(p') k> is a function of p - p': the property that lets the
+    # window slide over absolute positions
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(1, 1, 1, 32, generator=g, dtype=torch.float64)
+    k = torch.randn(1, 1, 1, 32, generator=g, dtype=torch.float64)
+    def score(p, pk):
+        return float((oracle.rope(q, torch.tensor([p]), 32, 10000.0) *
+                      oracle.rope(k, torch.tensor([pk]), 32, 10000.0)).sum())
+    for shift in (0, 129, 262000):
+        np.testing.assert_allclose(score(shift + 40, shift + 13), score(40, 13), rtol=1e-9)
