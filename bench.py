@@ -40,12 +40,14 @@ from hybrid_sliding_window_02_b300 import work  # noqa: E402
 METRIC = "SWA+sink prefill TFLOP/s & decode GB/s on 1 B300, as % of roofline vs CPU oracle"
 PREFILL = dict(B=4, T=8192, Hq=64, Hkv=8, D=128, W=128)
 DECODE = dict(B=256, Hq=64, Hkv=8, D=128, W=128)
+VERIFY = dict(B=256, L=4, Hq=64, Hkv=8, D=128, W=128)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # sources each kernel is built from (its traffic record is void once they change)
 KERNEL_SOURCES = {
     "swa_fwd_tc_kernel": ("csrc/tc_swa.cuh", "csrc/device_common.cuh"),
     "swa_fwd_tc_global_kernel": ("csrc/tc_global.cuh", "csrc/device_common.cuh"),
     "decode_tc_kernel": ("csrc/decode_tc.cuh", "csrc/device_common.cuh"),
+    "verify_tc_kernel": ("csrc/verify_tc.cuh", "csrc/device_common.cuh"),
 }
 
 
@@ -314,40 +316,94 @@ def time_prefill(swa, x, c, steps, warmup, dist, stream):
     return total_ms, per_launch_ms
 
 
-def time_decode(swa, c, steps, warmup, dev, stream, nsets=4):
-    """Decode calls rotating over input sets whose total exceeds L2."""
-    B, Hq, Hkv, D, W = (c[k] for k in ("B", "Hq", "Hkv", "D", "W"))
-    sets = [gen.decode_inputs(B, Hq, Hkv, D, W, seed=100 + i, device=dev) for i in range(nsets)]
-    out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
-    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+def time_graph(call, sets, steps, warmup, stream, per_graph=32):
+    """Mean device time (ms) of one call, launched back to back from a CUDA
+    graph of ``per_graph`` calls rotating over ``sets`` (so that the host's
+    per-call cost -- argument checks, tensor-map encoding, the launch -- does
+    not set the pace of a call shorter than it)."""
     with torch.cuda.stream(stream):
-        for i in range(warmup * nsets):
-            d = sets[i % nsets]
-            swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink, out, lse, stream=stream)
+        for i in range(warmup * len(sets)):
+            call(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(per_graph):
+            call(sets[i % len(sets)])
+    reps = max(1, steps // per_graph)
+    with torch.cuda.stream(stream):
+        g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(steps):
-            d = sets[i % nsets]
-            swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink, out, lse, stream=stream)
+        for _ in range(reps):
+            g.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps
+    del g
+    return e0.elapsed_time(e1) / (reps * per_graph)
+
+
+def time_decode(swa, c, steps, warmup, dev, stream, nsets=4):
+    """Decode calls rotating over input sets whose total exceeds L2; ms per call."""
+    B, Hq, Hkv, D, W = (c[k] for k in ("B", "Hq", "Hkv", "D", "W"))
+    sets = [gen.decode_inputs(B, Hq, Hkv, D, W, seed=100 + i, device=dev) for i in range(nsets)]
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+
+    def call(d):
+        swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink, out, lse, stream=stream)
+
+    return time_graph(call, sets, steps, warmup, stream)
+
+
+def time_verify(swa, c, steps, warmup, dev, stream, nsets=4):
+    """Verify calls (L drafted tokens per sequence) rotating over input sets
+    whose total exceeds L2; ms per call."""
+    B, L, Hq, Hkv, D, W = (c[k] for k in ("B", "L", "Hq", "Hkv", "D", "W"))
+    sets = [gen.verify_inputs(B, L, Hq, Hkv, D, W, seed=300 + i, device=dev)
+            for i in range(nsets)]
+    out = torch.empty(B, L, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, L, dtype=torch.float32, device=dev)
+
+    def call(d):
+        swa.swa_sink_verify(d.q, d.k_new, d.v_new, d.k_ring, d.v_ring, d.pos, d.sink, out, lse,
+                            stream=stream)
+
+    return time_graph(call, sets, steps, warmup, stream)
+
+
+def verify_line(swa, dev, stream, steps, hbm):
+    c = VERIFY
+    ms = time_verify(swa, c, steps, 3, dev, stream)
+    nbytes = work.verify_bytes(c["B"], c["L"], c["Hq"], c["Hkv"], c["D"], c["W"], 2)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    kpath = swa.verify_path(c["B"], c["L"], c["Hq"], c["Hkv"], c["D"], c["W"])
+    kernel = "verify_tc_kernel" if kpath == "tc_verify" else "verify_simt_kernel"
+    return {
+        "workload": f"swa_sink_verify B{c['B']} L{c['L']} Hq{c['Hq']} Hkv{c['Hkv']} D{c['D']} "
+                    f"W{c['W']} ring + {c['L']} drafted tokens, bf16->fp32+lse, 4 rotating sets "
+                    "(CUDA graph of 32 calls)",
+        "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
+        "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": recorded_traffic(kernel)},
+    }
 
 
 HYBRID = dict(T=32768, Hq=64, Hkv=8, D=128, W=128, n_swa=5, n_ga=1)
 
 
-def time_hybrid(swa, dev, stream, reps):
-    """One 5:1 hybrid block: five W=128 layers then one global layer (W = T),
+def time_hybrid(swa, dev, stream, reps, n_swa):
+    """One hybrid block: n_swa W=128 layers then one global layer (W = T),
     each on its own seeded inputs, one sequence of T=32768.  Returns per-layer
     mean launch times (ms) measured with events on the launching stream."""
     c = HYBRID
     T, Hq, Hkv, D = c["T"], c["Hq"], c["Hkv"], c["D"]
-    layers = gen.hybrid_block_inputs(T, Hq, Hkv, D, n_swa=c["n_swa"], n_ga=c["n_ga"], seed=200,
+    layers = gen.hybrid_block_inputs(T, Hq, Hkv, D, n_swa=n_swa, n_ga=c["n_ga"], seed=200,
                                      device=dev)
-    Ws = [c["W"]] * c["n_swa"] + [T] * c["n_ga"]
+    Ws = [c["W"]] * n_swa + [T] * c["n_ga"]
     out = torch.empty(1, T, Hq, D, dtype=torch.float32, device=dev)
     lse = torch.empty(1, Hq, T, dtype=torch.float32, device=dev)
 
@@ -379,10 +435,12 @@ def time_hybrid(swa, dev, stream, reps):
     return per_layer, total, Ws
 
 
-def hybrid_line(swa, dev, stream, reps, peaks):
-    c = HYBRID
+def hybrid_line(swa, dev, stream, reps, peaks, n_swa=None):
+    c = dict(HYBRID)
+    if n_swa is not None:
+        c["n_swa"] = n_swa
     T, Hq, D = c["T"], c["Hq"], c["D"]
-    per_layer, total_ms, Ws = time_hybrid(swa, dev, stream, reps)
+    per_layer, total_ms, Ws = time_hybrid(swa, dev, stream, reps, c["n_swa"])
     fl = [work.prefill_flops(1, T, Hq, D, W) for W in Ws]
     ga_ms = sum(t for t, W in zip(per_layer, Ws) if W >= T) / max(1, c["n_ga"])
     ga_fl = fl[-1]
@@ -405,6 +463,35 @@ def hybrid_line(swa, dev, stream, reps, peaks):
                      "algorithmic_flops_per_launch": ga_fl,
                      "traffic": recorded_traffic("swa_fwd_tc_global_kernel")},
     }
+
+
+def bf16_out_line(swa, x, c, steps, dev, stream, peaks):
+    """The headline prefill with bf16 output (out rounded from fp32, lse fp32)."""
+    B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
+    out = torch.empty(B, T, Hq, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = work.prefill_bytes(B, T, Hq, Hkv, D, 2, out_bytes=2)
+    flops = work.prefill_flops(B, T, Hq, D, W)
+    hbm = float(peaks["hbm_gbs"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": workload_name(c).replace("fp32+lse", "bf16 out + fp32 lse"),
+            "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_call": round(ms, 4),
+            "roofline": {"kernel": "swa_fwd_tc_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                         "algorithmic_bytes_per_launch": nbytes}}
 
 
 def time_e2e(swa, xh, c, steps, dev, stream):
@@ -510,7 +597,7 @@ def run_ours(args, dist):
         "roofline": prefill_roofline(kpath, flops, nbytes, launch_ms, peaks, peak_src),
         "decode": {
             "workload": "swa_sink_decode B256 Hq64 Hkv8 D128 W128 ring, bf16->fp32+lse, "
-                        "4 rotating input sets (590 MB)",
+                        "4 rotating input sets (590 MB), CUDA graph of 32 calls",
             "value": round(dec_gbs, 1), "unit": "GB/s", "us_per_call": round(dec_us, 2),
             "roofline": {"kernel": dec_kernel, "bound": "hbm",
                          "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
@@ -522,8 +609,15 @@ def run_ours(args, dist):
         "clocks": clk.summary(),
     }
 
+    line["prefill_bf16_out"] = bf16_out_line(swa, x, c, max(10, args.steps // 4), dev, stream,
+                                             peaks)
+    line["verify"] = verify_line(swa, dev, stream, args.decode_steps, hbm)
     if not args.no_hybrid:
         line["hybrid_block"] = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks)
+        # the 7:1 schedule of the later models: same kernels, seven window
+        # layers per global layer
+        line["hybrid_block_7to1"] = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks,
+                                                n_swa=7)
     if not args.no_e2e:
         xh = gen.PrefillInputs(*(t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.sink)))
         e2e_ms, h2d, d2h = time_e2e(swa, xh, c, max(3, args.steps // 50), dev, stream)

@@ -52,9 +52,22 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(LIB_PATH)
             p, i32 = ctypes.c_void_p, ctypes.c_int
             L.swa_sink_fwd.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p]
+            L.swa_sink_fwd_ex.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
+                                          p]
+            L.swa_sink_fwd_ex.restype = i32
             L.swa_sink_decode.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, p]
             L.swa_ring_append.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, p]
-            for f in (L.swa_sink_fwd, L.swa_sink_decode, L.swa_ring_append):
+            L.swa_sink_verify.argtypes = [p, p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32,
+                                          i32, p]
+            dbl = ctypes.c_double
+            L.swa_rope.argtypes = [p, p, i32, i32, i32, i32, i32, dbl, i32, p]
+            L.swa_rope_append.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, dbl,
+                                          i32, p]
+            L.swa_rope.restype = i32
+            L.swa_rope_append.restype = i32
+            L.swa_sink_verify_path.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.swa_sink_verify_path.restype = ctypes.c_char_p
+            for f in (L.swa_sink_fwd, L.swa_sink_decode, L.swa_ring_append, L.swa_sink_verify):
                 f.restype = i32
             L.swa_sink_fwd_path.argtypes = [i32, i32, i32, i32, i32, i32, i32]
             L.swa_sink_fwd_path.restype = ctypes.c_char_p
@@ -127,11 +140,12 @@ def decode_path(B, Hq, Hkv, D, W, dtype_code=SWA_BF16) -> str:
 
 
 def swa_sink_fwd(q, k, v, sink, W: int, out=None, lse=None, *, with_lse: bool = True,
-                 stream=None):
+                 out_dtype=None, stream=None):
     """Prefill.  q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16 or fp32), sink [Hq] fp32.
 
-    Returns (out [B,T,Hq,D] fp32, lse [B,Hq,T] fp32 or None).  W >= T is the
-    global (full causal) layer.
+    Returns (out [B,T,Hq,D], lse [B,Hq,T] fp32 or None).  W >= T is the global
+    (full causal) layer.  out is fp32 unless out_dtype (or a given out) is
+    torch.bfloat16, which the tensor-core kernels write rounded from fp32.
     """
     import torch
     B, T, Hq, D = q.shape
@@ -146,16 +160,19 @@ def swa_sink_fwd(q, k, v, sink, W: int, out=None, lse=None, *, with_lse: bool = 
     if sink.dtype != torch.float32 or sink.shape != (Hq,):
         raise ValueError("sink must be float32 [Hq]")
     if out is None:
-        out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=dev)
+        out = torch.empty(B, T, Hq, D, dtype=out_dtype or torch.float32, device=dev)
+    if out.dtype not in (torch.float32, torch.bfloat16) or out.shape != (B, T, Hq, D):
+        raise ValueError("out must be [B, T, Hq, D] float32 or bfloat16")
     if with_lse and lse is None:
         lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
     _cuda_contig("out", out, dev)
     if lse is not None:
         _cuda_contig("lse", lse, dev)
-    st = lib().swa_sink_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
-                            out.data_ptr(), lse.data_ptr() if lse is not None else None,
-                            B, T, Hq, Hkv, D, int(W), _dtype_code(q), _stream_handle(stream, dev))
-    _check("swa_sink_fwd", st)
+    st = lib().swa_sink_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
+                               out.data_ptr(), lse.data_ptr() if lse is not None else None,
+                               B, T, Hq, Hkv, D, int(W), _dtype_code(q), _dtype_code(out),
+                               _stream_handle(stream, dev))
+    _check("swa_sink_fwd_ex", st)
     return out, lse
 
 
@@ -190,6 +207,95 @@ def swa_sink_decode(q, k_ring, v_ring, pos, sink, out=None, lse=None, *, with_ls
                                B, Hq, Hkv, D, W, _dtype_code(q), _stream_handle(stream, dev))
     _check("swa_sink_decode", st)
     return out, lse
+
+
+def verify_path(B, L, Hq, Hkv, D, W, dtype_code=SWA_BF16) -> str:
+    """Name of the verify kernel the library selects for these sizes."""
+    return lib().swa_sink_verify_path(B, L, Hq, Hkv, D, W, dtype_code).decode()
+
+
+def swa_sink_verify(q, k_new, v_new, k_ring, v_ring, pos, sink, out=None, lse=None, *,
+                    with_lse=True, stream=None):
+    """Multi-token verify.  q [B,L,Hq,D], k_new/v_new [B,L,Hkv,D] (the drafted
+    tokens), rings [B,Hkv,W,D] holding the positions before pos, pos [B] int64
+    (position of drafted token 0), sink [Hq] fp32.
+
+    Returns (out [B,L,Hq,D] fp32, lse [B,Hq,L] fp32 or None).
+    """
+    import torch
+    B, L, Hq, D = q.shape
+    _, Hkv, W, _ = k_ring.shape
+    dev = q.device
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_ring", k_ring),
+                 ("v_ring", v_ring), ("pos", pos), ("sink", sink)):
+        _cuda_contig(n, t, dev)
+    if k_new.shape != (B, L, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be [B, L, Hkv, D] matching q")
+    if k_ring.shape != (B, Hkv, W, D) or v_ring.shape != k_ring.shape:
+        raise ValueError("rings must be [B, Hkv, W, D] matching q")
+    if pos.dtype != torch.int64 or pos.shape != (B,):
+        raise ValueError("pos must be int64 [B]")
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_ring", k_ring), ("v_ring", v_ring)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{n} must have the dtype of q")
+    if sink.dtype != torch.float32 or sink.shape != (Hq,):
+        raise ValueError("sink must be float32 [Hq]")
+    if out is None:
+        out = torch.empty(B, L, Hq, D, dtype=torch.float32, device=dev)
+    if with_lse and lse is None:
+        lse = torch.empty(B, Hq, L, dtype=torch.float32, device=dev)
+    st = lib().swa_sink_verify(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                               k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(),
+                               sink.data_ptr(), out.data_ptr(),
+                               lse.data_ptr() if lse is not None else None,
+                               B, L, Hq, Hkv, D, W, _dtype_code(q), _stream_handle(stream, dev))
+    _check("swa_sink_verify", st)
+    return out, lse
+
+
+def swa_rope(x, pos0, rot_dim: int, theta: float, *, stream=None):
+    """Rotary embedding in place on x [B,T,H,D] (bf16 or fp32); token (b, t)
+    is at position pos0[b] + t (pos0 int64 [B] on the device).  Returns x."""
+    import torch
+    B, T, H, D = x.shape
+    dev = x.device
+    _cuda_contig("x", x, dev)
+    _cuda_contig("pos0", pos0, dev)
+    if pos0.dtype != torch.int64 or pos0.shape != (B,):
+        raise ValueError("pos0 must be int64 [B]")
+    st = lib().swa_rope(x.data_ptr(), pos0.data_ptr(), B, T, H, D, int(rot_dim), float(theta),
+                        _dtype_code(x), _stream_handle(stream, dev))
+    _check("swa_rope", st)
+    return x
+
+
+def swa_rope_append(q, k, v, k_ring, v_ring, pos, rot_dim: int, theta: float, q_out=None, *,
+                    stream=None):
+    """Rotate the new token's q [B,Hq,D] and k [B,Hkv,D] at pos [B] and write k,
+    v [B,Hkv,D] into ring slot pos mod W of k_ring / v_ring [B,Hkv,W,D].
+    Returns the rotated q (q_out, a new tensor unless given; may be q)."""
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, W, _ = k_ring.shape
+    dev = q.device
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    for n, t in (("q", q), ("k", k), ("v", v), ("k_ring", k_ring), ("v_ring", v_ring),
+                 ("pos", pos), ("q_out", q_out)):
+        _cuda_contig(n, t, dev)
+    if k.shape != (B, Hkv, D) or v.shape != k.shape or v_ring.shape != k_ring.shape:
+        raise ValueError("shape mismatch between new tokens and rings")
+    if pos.dtype != torch.int64 or pos.shape != (B,):
+        raise ValueError("pos must be int64 [B]")
+    for n, t in (("k", k), ("v", v), ("k_ring", k_ring), ("v_ring", v_ring), ("q_out", q_out)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{n} must have the dtype of q")
+    st = lib().swa_rope_append(q.data_ptr(), k.data_ptr(), v.data_ptr(), q_out.data_ptr(),
+                               k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(), B, Hq, Hkv,
+                               D, W, int(rot_dim), float(theta), _dtype_code(q),
+                               _stream_handle(stream, dev))
+    _check("swa_rope_append", st)
+    return q_out
 
 
 def swa_ring_append(k_new, v_new, k_ring, v_ring, pos, *, stream=None):

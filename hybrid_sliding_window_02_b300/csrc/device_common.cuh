@@ -265,6 +265,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// 32 lanes x 32 columns of 32-bit values from TMEM: thread t of the warp gets
+// lane (base_lane + t), columns [col, col+32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
 // 16 lanes x 256 bits, repeated 16 times along the columns (128 columns):
 // for repetition j, thread t gets r[4j+0..1] = lane (base + t/4), columns
 // 8j + 2(t%4) + {0,1} and r[4j+2..3] = lane (base + 8 + t/4), same columns.
@@ -288,6 +304,11 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                  "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
                  "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+  reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(r));
+  reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
 }
 
 // 32 lanes x 8 columns of 32-bit values into TMEM (thread t -> lane base + t).
@@ -360,6 +381,10 @@ __device__ __forceinline__ void st_global_v4(float* p, uint32_t a, uint32_t b, u
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
+}
+
+__device__ __forceinline__ void st_global_b32(void* p, uint32_t a) {
+  asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
 }
 
 __device__ __forceinline__ void st_global_v2(float* p, uint32_t a, uint32_t b) {

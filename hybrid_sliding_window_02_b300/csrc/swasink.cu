@@ -15,9 +15,12 @@
 #include "decode.cuh"
 #include "decode_tc.cuh"
 #include "device_common.cuh"
+#include "rope.cuh"
 #include "simt_fwd.cuh"
 #include "tc_global.cuh"
 #include "tc_swa.cuh"
+#include "verify.cuh"
+#include "verify_tc.cuh"
 
 namespace {
 
@@ -36,9 +39,10 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  bool tc_attr = false;
-  bool tcg_attr = false;
+  bool tc_attr[2] = {false, false};   // [bf16 output]
+  bool tcg_attr[2] = {false, false};
   bool dectc_attr = false;
+  bool vertc_attr = false;
   bool decode_attr[2][2][5] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -127,6 +131,13 @@ swa_status check_launch(const char* what) {
 
 enum FwdPath { kPathInvalid, kPathSimt, kPathTcSwa, kPathTcGlobal };
 
+constexpr int kVerifyMaxL = 64;  // drafted tokens per verify call
+
+bool verify_tc_applies(int L, int Hq, int Hkv, int D, int W, swa_dtype dt) {
+  return dt == SWA_BF16 && D == swa::vertc::kD && W == swa::vertc::kW &&
+         Hq == Hkv * swa::vertc::kG && L >= 1 && L <= swa::vertc::kLmax;
+}
+
 FwdPath select_fwd(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype dt) {
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return kPathInvalid;
   if (dt != SWA_F32 && dt != SWA_BF16) return kPathInvalid;
@@ -162,22 +173,22 @@ swa_status launch_simt(const void* q, const void* k, const void* v, const float*
 }
 
 swa_status launch_tc_swa(const void* q, const void* k, const void* v, const float* sink,
-                         float* out, float* lse, int B, int T, int Hq, int Hkv, int W,
-                         cudaStream_t st) {
+                         void* out, float* lse, int B, int T, int Hq, int Hkv, int W,
+                         bool bf16_out, cudaStream_t st) {
   using namespace swa::tcswa;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
+  auto kern = bf16_out ? swa_fwd_tc_kernel<true> : swa_fwd_tc_kernel<false>;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].tc_attr) {
-      cudaError_t e = cudaFuncSetAttribute(swa_fwd_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!g_dev[dev].tc_attr[bf16_out]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].tc_attr = true;
+      g_dev[dev].tc_attr[bf16_out] = true;
     }
   }
   const long long ntiles_seq = (T + kNpos - 1) / kNpos;
@@ -202,29 +213,30 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
   p.W = W;
   p.ntiles_seq = (int)ntiles_seq;
   p.total_tiles = (int)total_tiles;
+  p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
   const long long grid = total_tiles < sms ? total_tiles : sms;
-  swa_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
   return check_launch("swa_fwd_tc_kernel");
 }
 
 swa_status launch_tc_global(const void* q, const void* k, const void* v, const float* sink,
-                            float* out, float* lse, int B, int T, int Hq, int Hkv, int W,
-                            cudaStream_t st) {
+                            void* out, float* lse, int B, int T, int Hq, int Hkv, int W,
+                            bool bf16_out, cudaStream_t st) {
   using namespace swa::tcglobal;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
+  auto kern = bf16_out ? swa_fwd_tc_global_kernel<true> : swa_fwd_tc_global_kernel<false>;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].tcg_attr) {
-      cudaError_t e = cudaFuncSetAttribute(swa_fwd_tc_global_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!g_dev[dev].tcg_attr[bf16_out]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_global_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].tcg_attr = true;
+      g_dev[dev].tcg_attr[bf16_out] = true;
     }
   }
   const long long nitem_seq = (T + kItemPos - 1) / kItemPos;
@@ -251,7 +263,7 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
   p.total_items = (int)total;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
   const long long grid = total < sms ? total : sms;
-  swa_fwd_tc_global_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
   return check_launch("swa_fwd_tc_global_kernel");
 }
 
@@ -328,6 +340,53 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   return check_launch("decode_tc_kernel");
 }
 
+swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const void* kr,
+                            const void* vr, const int64_t* pos, const float* sink, float* out,
+                            float* lse, int B, int L, int Hq, int Hkv, cudaStream_t st) {
+  using namespace swa::vertc;
+  int dev, sms;
+  if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev[dev].vertc_attr) {
+      cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+      if (e != cudaSuccess) {
+        set_cuda_error("cudaFuncSetAttribute(verify_tc_kernel)", e);
+        return SWA_ECUDA;
+      }
+      g_dev[dev].vertc_attr = true;
+    }
+  }
+  const long long units = (long long)B * Hkv;
+  if (units * kW >= (1LL << 31)) {
+    set_error_text("problem too large for the tensor-core verify kernel");
+    return SWA_EUNSUPPORTED;
+  }
+  CUtensorMap mk, mv, mq;
+  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, kD, units * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, kD, units * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, L, B, 64, kG, L))
+    return SWA_ECUDA;
+  Params p;
+  p.k_new = static_cast<const __nv_bfloat16*>(kn);
+  p.v_new = static_cast<const __nv_bfloat16*>(vn);
+  p.pos = pos;
+  p.sink = sink;
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.L = L;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.units = (int)units;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  const long long grid = units < sms ? units : sms;
+  verify_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, p);
+  return check_launch("verify_tc_kernel");
+}
+
 template <typename Tin, int D>
 swa_status launch_decode_g(const void* q, const void* kr, const void* vr, const int64_t* pos,
                            const float* sink, float* out, float* lse, int B, int Hq, int Hkv,
@@ -372,30 +431,44 @@ swa_status launch_decode_g(const void* q, const void* kr, const void* vr, const 
 
 extern "C" {
 
-swa_status swa_sink_fwd(const void* q, const void* k, const void* v, const float* sink,
-                        float* out, float* lse, int B, int T, int Hq, int Hkv, int D, int W,
-                        swa_dtype in_dtype, void* stream) {
+swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const float* sink,
+                           void* out, float* lse, int B, int T, int Hq, int Hkv, int D, int W,
+                           swa_dtype in_dtype, swa_dtype out_dtype, void* stream) {
   g_last_error[0] = '\0';
   if (!q || !k || !v || !sink || !out) return SWA_EINVAL;
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return SWA_EINVAL;
   if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
+  if (out_dtype != SWA_F32 && out_dtype != SWA_BF16) return SWA_EINVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       (lse && !aligned16(lse)))
     return SWA_EINVAL;
   if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf16_out = out_dtype == SWA_BF16;
   switch (select_fwd(B, T, Hq, Hkv, D, W, in_dtype)) {
     case kPathTcSwa:
-      return launch_tc_swa(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, st);
+      return launch_tc_swa(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, bf16_out, st);
     case kPathTcGlobal:
-      return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, st);
+      return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, bf16_out, st);
     case kPathSimt:
+      if (bf16_out) {
+        set_error_text("bf16 output is available on the tensor-core paths only");
+        return SWA_EUNSUPPORTED;
+      }
       if (in_dtype == SWA_F32)
-        return launch_simt<float>(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, st);
-      return launch_simt<__nv_bfloat16>(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, st);
+        return launch_simt<float>(q, k, v, sink, static_cast<float*>(out), lse, B, T, Hq, Hkv,
+                                  D, W, st);
+      return launch_simt<__nv_bfloat16>(q, k, v, sink, static_cast<float*>(out), lse, B, T, Hq,
+                                        Hkv, D, W, st);
     default:
       return SWA_EINVAL;
   }
+}
+
+swa_status swa_sink_fwd(const void* q, const void* k, const void* v, const float* sink,
+                        float* out, float* lse, int B, int T, int Hq, int Hkv, int D, int W,
+                        swa_dtype in_dtype, void* stream) {
+  return swa_sink_fwd_ex(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, in_dtype, SWA_F32, stream);
 }
 
 swa_status swa_sink_decode(const void* q, const void* k_ring, const void* v_ring,
@@ -453,6 +526,112 @@ swa_status swa_ring_append(const void* k_new, const void* v_new, void* k_ring, v
         static_cast<__nv_bfloat16*>(k_ring), static_cast<__nv_bfloat16*>(v_ring), pos, B, Hkv,
         D, W);
   return check_launch("ring_append_kernel");
+}
+
+swa_status swa_sink_verify(const void* q, const void* k_new, const void* v_new,
+                           const void* k_ring, const void* v_ring, const int64_t* pos,
+                           const float* sink, float* out, float* lse, int B, int L, int Hq,
+                           int Hkv, int D, int W, swa_dtype in_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k_new || !v_new || !k_ring || !v_ring || !pos || !sink || !out) return SWA_EINVAL;
+  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return SWA_EINVAL;
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_ring) ||
+      !aligned16(v_ring) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (reinterpret_cast<uintptr_t>(pos) & 7u))
+    return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  if (L > kVerifyMaxL) return SWA_EUNSUPPORTED;
+  const int esz = in_dtype == SWA_F32 ? 4 : 2;
+  if (2LL * W * D * esz > swa::kDecodeMaxRingBytes) return SWA_EUNSUPPORTED;
+  const long long rows = (long long)B * L * Hq;
+  const long long blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffffLL) return SWA_EUNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (verify_tc_applies(L, Hq, Hkv, D, W, in_dtype))
+    return launch_verify_tc(q, k_new, v_new, k_ring, v_ring, pos, sink, out, lse, B, L, Hq, Hkv,
+                            st);
+  const float scale = (float)(1.0 / std::sqrt((double)D));
+#define SWA_VERIFY_LAUNCH(T, DD)                                                              \
+  swa::verify_simt_kernel<T, DD><<<(unsigned)blocks, 256, 0, st>>>(                         \
+      static_cast<const T*>(q), static_cast<const T*>(k_new), static_cast<const T*>(v_new), \
+      static_cast<const T*>(k_ring), static_cast<const T*>(v_ring), pos, sink, out, lse, B,   \
+      L, Hq, Hkv, W, scale)
+  if (in_dtype == SWA_F32) {
+    if (D == 64) SWA_VERIFY_LAUNCH(float, 64);
+    else SWA_VERIFY_LAUNCH(float, 128);
+  } else {
+    if (D == 64) SWA_VERIFY_LAUNCH(__nv_bfloat16, 64);
+    else SWA_VERIFY_LAUNCH(__nv_bfloat16, 128);
+  }
+#undef SWA_VERIFY_LAUNCH
+  return check_launch("verify_simt_kernel");
+}
+
+static bool rope_args_ok(int D, int rot_dim, double theta) {
+  return rot_dim >= 2 && rot_dim <= D && rot_dim % 2 == 0 && rot_dim / 2 <= swa::kRopeMaxHalf &&
+         theta > 0.0 && std::isfinite(theta);
+}
+
+swa_status swa_rope(void* x, const int64_t* pos0, int B, int T, int H, int D, int rot_dim,
+                    double theta, swa_dtype dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (!x || !pos0) return SWA_EINVAL;
+  if (B < 1 || T < 1 || H < 1 || D < 1) return SWA_EINVAL;
+  if (dtype != SWA_F32 && dtype != SWA_BF16) return SWA_EINVAL;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(pos0) & 7u)) return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  if (!rope_args_ok(D, rot_dim, theta)) return SWA_EINVAL;
+  const long long ntok = (long long)B * T;
+  const unsigned grid = (unsigned)(ntok < 65536 ? ntok : 65536);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const double l2t = std::log2(theta);
+  if (dtype == SWA_F32)
+    swa::rope_inplace_kernel<float><<<grid, swa::kRopeThreads, 0, st>>>(
+        static_cast<float*>(x), pos0, B, T, H, D, rot_dim / 2, l2t);
+  else
+    swa::rope_inplace_kernel<__nv_bfloat16><<<grid, swa::kRopeThreads, 0, st>>>(
+        static_cast<__nv_bfloat16*>(x), pos0, B, T, H, D, rot_dim / 2, l2t);
+  return check_launch("rope_inplace_kernel");
+}
+
+swa_status swa_rope_append(const void* q_in, const void* k_in, const void* v_in, void* q_out,
+                           void* k_ring, void* v_ring, const int64_t* pos, int B, int Hq,
+                           int Hkv, int D, int W, int rot_dim, double theta, swa_dtype dtype,
+                           void* stream) {
+  g_last_error[0] = '\0';
+  if (!q_in || !k_in || !v_in || !q_out || !k_ring || !v_ring || !pos) return SWA_EINVAL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1) return SWA_EINVAL;
+  if (dtype != SWA_F32 && dtype != SWA_BF16) return SWA_EINVAL;
+  if (!aligned16(q_in) || !aligned16(k_in) || !aligned16(v_in) || !aligned16(q_out) ||
+      !aligned16(k_ring) || !aligned16(v_ring) || (reinterpret_cast<uintptr_t>(pos) & 7u))
+    return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  if (!rope_args_ok(D, rot_dim, theta)) return SWA_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const double l2t = std::log2(theta);
+  if (dtype == SWA_F32)
+    swa::rope_append_kernel<float><<<(unsigned)B, swa::kRopeThreads, 0, st>>>(
+        static_cast<const float*>(q_in), static_cast<const float*>(k_in),
+        static_cast<const float*>(v_in), static_cast<float*>(q_out), static_cast<float*>(k_ring),
+        static_cast<float*>(v_ring), pos, Hq, Hkv, D, W, rot_dim / 2, l2t);
+  else
+    swa::rope_append_kernel<__nv_bfloat16><<<(unsigned)B, swa::kRopeThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(q_in), static_cast<const __nv_bfloat16*>(k_in),
+        static_cast<const __nv_bfloat16*>(v_in), static_cast<__nv_bfloat16*>(q_out),
+        static_cast<__nv_bfloat16*>(k_ring), static_cast<__nv_bfloat16*>(v_ring), pos, Hq, Hkv,
+        D, W, rot_dim / 2, l2t);
+  return check_launch("rope_append_kernel");
+}
+
+const char* swa_sink_verify_path(int B, int L, int Hq, int Hkv, int D, int W, swa_dtype in_dtype) {
+  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || W < 1 || Hq % Hkv) return "invalid";
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return "invalid";
+  if (D != 64 && D != 128) return "invalid";
+  if (L > kVerifyMaxL) return "invalid";
+  const int esz = in_dtype == SWA_F32 ? 4 : 2;
+  if (2LL * W * D * esz > swa::kDecodeMaxRingBytes) return "invalid";
+  return verify_tc_applies(L, Hq, Hkv, D, W, in_dtype) ? "tc_verify" : "simt_verify";
 }
 
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype) {

@@ -83,7 +83,7 @@ __host__ __device__ constexpr uint32_t col_o(int i) { return 256u + 128u * (uint
 
 struct Params {
   const float* sink;
-  float* out;
+  void* out;          // float, or bf16 with kBf16Out
   float* lse;
   int B, T, Hq, Hkv, W;
   int nitem_seq;      // ceil(T / 32)
@@ -124,20 +124,6 @@ __device__ __forceinline__ bool cta_item(int k, const Params& p, Item& it) {
   return true;
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-}
-
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -151,17 +137,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-__device__ __forceinline__ void reg_fence32(uint32_t* r) {
-  reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(r));
-  reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
-}
-
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
+template <bool kBf16Out>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_global_kernel(const __grid_constant__ CUtensorMap map_q,
                              const __grid_constant__ CUtensorMap map_k,
@@ -437,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar(kBarOFull + ti), k & 1, kErrWaitOFull, abort_flag)) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
-      float* orow = p.out + (((long long)it.b * p.T + pos) * p.Hq + h) * kD;
+      const long long e0 = (((long long)it.b * p.T + pos) * p.Hq + h) * kD;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t o[32];
@@ -447,9 +429,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pos < p.T) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+          if constexpr (kBf16Out) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            st_global_v4(orow + c * 32 + 4 * e, o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+            float* orow = reinterpret_cast<float*>(static_cast<__nv_bfloat16*>(p.out) + e0 + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              st_global_v4(orow + 4 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          } else {
+            float* orow = static_cast<float*>(p.out) + e0 + c * 32;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              st_global_v4(orow + 4 * e, o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          }
         }
       }
       tc_fence_before();

@@ -27,7 +27,8 @@
 //                 O = P V     (TS: P from TMEM, V MN-major, N=128, K=16/block)
 //   warps 0..3  softmax: S (TMEM) -> mask, sink-seeded max/sum, normalised
 //               bf16 P -> TMEM; lse -> global
-//   warps 4..7  epilogue: O (TMEM, double-buffered) -> global.  The 16x256b
+//   warps 4..7  epilogue: O (TMEM, double-buffered) -> global (fp32, or bf16
+//               rounded from the same fp32 values).  The 16x256b
 //               TMEM read gives each group of 4 threads 32 contiguous bytes of
 //               a row, so every warp store fills 8 whole 32-byte sectors of 8
 //               lines (one position's 8 heads: 4 KB contiguous); this measured
@@ -78,12 +79,13 @@ constexpr uint32_t kColS = 0, kColP = 160, kColO0 = 256, kColO1 = 384;
 
 struct Params {
   const float* sink;
-  float* out;
+  void* out;            // float, or bf16 with kBf16Out
   float* lse;
   int B, T, Hq, Hkv, W;
   int ntiles_seq;       // ceil(T / 16)
   int total_tiles;      // B * Hkv * ntiles_seq (< 2^31, checked on the host)
   float scale_log2;     // log2(e) / sqrt(D)
+  int out_align32;      // out is 32-byte aligned (bf16 output stores whole sectors)
 };
 
 __device__ __forceinline__ void tile_coords(uint32_t u, const Params& p, int& b, int& kvh,
@@ -94,6 +96,7 @@ __device__ __forceinline__ void tile_coords(uint32_t u, const Params& p, int& b,
   kvh = (int)(bk - (uint32_t)b * (uint32_t)p.Hkv);
 }
 
+template <bool kBf16Out>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k,
@@ -396,8 +399,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ob = it & 1;
       if (!mbar_wait(bar(kBarOFull + ob), (it >> 1) & 1, kErrWaitOFull, abort_flag)) break;
       tc_fence_after();
-      uint32_t o0[64], o1[64];
       const uint32_t col = tmem + (ob ? kColO1 : kColO0);
+      if constexpr (kBf16Out) {
+        // thread = tile row (TMEM lane 32 sub + lane): position 4 sub + lane / 8,
+        // head lane % 8; 32 consecutive columns per load, rounded to bf16 and
+        // written as whole 32-byte sectors
+        uint32_t o[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(col + ((uint32_t)(sub * 32) << 16) + 32 * c, o[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence32(o[c]);
+        tc_fence_before();
+        mbar_arrive(bar(kBarOFree + ob));
+        const int pos = n * kNpos + 4 * sub + (lane >> 3);
+        if (pos < p.T) {
+          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                                (((long long)b * p.T + pos) * p.Hq + kvh * kG + (lane & 7)) * kD;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(o[c][2 * e]), __uint_as_float(o[c][2 * e + 1]));
+            float* dst = reinterpret_cast<float*>(orow + 32 * c);
+            if (p.out_align32) {
+              st_global_v8(dst, pk);
+              st_global_v8(dst + 8, pk + 8);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                st_global_v4(dst + 4 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            }
+          }
+        }
+        continue;
+      }
+      uint32_t o0[64], o1[64];
       tmem_ld_16x256b_x16(col + ((uint32_t)(sub * 32) << 16), o0);
       tmem_ld_16x256b_x16(col + ((uint32_t)(sub * 32 + 16) << 16), o1);
       tmem_ld_wait();
@@ -414,17 +452,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos0 = n * kNpos + 4 * sub;
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        if (pos0 + k < p.T) {
-          float* orow = p.out + (row0 + (long long)k * p.Hq) * kD + 2 * quad;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            st_global_v2(orow + 8 * j, o0[4 * j + 2 * k], o0[4 * j + 2 * k + 1]);
-        }
-        if (pos0 + 2 + k < p.T) {
-          float* orow = p.out + (row0 + (long long)(2 + k) * p.Hq) * kD + 2 * quad;
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t* o = half ? o1 : o0;
+          if (pos0 + 2 * half + k < p.T) {
+            const long long e0 = (row0 + (long long)(2 * half + k) * p.Hq) * kD + 2 * quad;
+            float* orow = static_cast<float*>(p.out) + e0;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            st_global_v2(orow + 8 * j, o1[4 * j + 2 * k], o1[4 * j + 2 * k + 1]);
+            for (int j = 0; j < 16; ++j)
+              st_global_v2(orow + 8 * j, o[4 * j + 2 * k], o[4 * j + 2 * k + 1]);
+          }
         }
       }
     }

@@ -15,6 +15,9 @@ Recipe (one ``torch.Generator`` per call, seeded; draws happen in a fixed order)
 * decode: ``q [B,Hq,D]``, ``k_ring [B,Hkv,W,D]``, ``v_ring [B,Hkv,W,D]``,
   ``sink [Hq]`` in that order, then ``pos [B]`` int64 uniform in
   ``[pos_lo, pos_hi)``.
+* verify (L drafted tokens): ``q [B,L,Hq,D]``, ``k_new [B,L,Hkv,D]``,
+  ``v_new [B,L,Hkv,D]``, ``k_ring``, ``v_ring [B,Hkv,W,D]``, ``sink [Hq]``, then
+  ``pos [B]`` int64 uniform in ``[pos_lo, pos_hi)``.
 
 The model these shapes come from (MiMo-V2-Flash technical report summary,
 "core method": 128-token sliding window, GQA, learnable per-head sink) fixes no
@@ -92,6 +95,34 @@ def decode_inputs(B: int, Hq: int, Hkv: int, D: int, W: int, *, seed: int = 0,
     sink = torch.randn(Hq, generator=g, device=device, dtype=f32)
     pos = torch.randint(pos_lo, pos_hi, (B,), generator=g, device=device, dtype=torch.int64)
     return DecodeInputs(q.to(dtype), k_ring.to(dtype), v_ring.to(dtype), sink, pos)
+
+
+@dataclass
+class VerifyInputs:
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    k_ring: torch.Tensor
+    v_ring: torch.Tensor
+    sink: torch.Tensor
+    pos: torch.Tensor
+
+
+def verify_inputs(B: int, L: int, Hq: int, Hkv: int, D: int, W: int, *, seed: int = 0,
+                  dtype: torch.dtype = torch.bfloat16, device="cpu", pos_lo: int = 128,
+                  pos_hi: int = 262144) -> VerifyInputs:
+    """Draw verify inputs: L drafted tokens per sequence and a full W-slot ring."""
+    g = _gen(seed, device)
+    f32 = torch.float32
+    q = torch.randn(B, L, Hq, D, generator=g, device=device, dtype=f32)
+    k_new = torch.randn(B, L, Hkv, D, generator=g, device=device, dtype=f32)
+    v_new = torch.randn(B, L, Hkv, D, generator=g, device=device, dtype=f32)
+    k_ring = torch.randn(B, Hkv, W, D, generator=g, device=device, dtype=f32)
+    v_ring = torch.randn(B, Hkv, W, D, generator=g, device=device, dtype=f32)
+    sink = torch.randn(Hq, generator=g, device=device, dtype=f32)
+    pos = torch.randint(pos_lo, pos_hi, (B,), generator=g, device=device, dtype=torch.int64)
+    return VerifyInputs(q.to(dtype), k_new.to(dtype), v_new.to(dtype), k_ring.to(dtype),
+                        v_ring.to(dtype), sink, pos)
 
 
 def ring_from_history(k_hist: torch.Tensor, v_hist: torch.Tensor, pos: torch.Tensor, W: int):

@@ -39,6 +39,25 @@ def decode_bytes(B: int, Hq: int, Hkv: int, D: int, W: int, in_bytes: int,
     return rd + wr
 
 
+def verify_pairs(L: int, W: int, pos: int) -> int:
+    """(query, key) pairs of one verify group row set: drafted token j at
+    position pos + j sees min(pos + j + 1, W) keys."""
+    return sum(min(pos + j + 1, W) for j in range(L))
+
+
+def verify_flops(B: int, L: int, Hq: int, D: int, W: int) -> int:
+    """FLOPs of a verify call with every window full (pos >= W - 1)."""
+    return 4 * D * B * Hq * L * W
+
+
+def verify_bytes(B: int, L: int, Hq: int, Hkv: int, D: int, W: int, in_bytes: int,
+                 with_lse: bool = True) -> int:
+    rd = (B * L * Hq * D * in_bytes + 2 * B * L * Hkv * D * in_bytes
+          + 2 * B * Hkv * W * D * in_bytes + B * 8 + Hq * 4)
+    wr = B * L * Hq * D * 4 + (B * Hq * L * 4 if with_lse else 0)
+    return rd + wr
+
+
 def hybrid_reduction(T: int, W: int = 128, n_swa: int = 5, n_ga: int = 1):
     """(attention-FLOP ratio, KV-cache ratio) of an all-global stack over a
     hybrid stack with n_swa window layers per n_ga global layers, at length T.

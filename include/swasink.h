@@ -67,6 +67,19 @@ swa_status swa_sink_fwd(const void* q, const void* k, const void* v, const float
                         swa_dtype in_dtype, void* stream);
 
 /*
+ * swa_sink_fwd_ex -- swa_sink_fwd with a choice of output type: out_dtype
+ * SWA_F32 is swa_sink_fwd; SWA_BF16 writes out [B, T, Hq, D] as bf16, each
+ * value the round-to-nearest-even of the fp32 value swa_sink_fwd would write
+ * (lse stays fp32).  The bf16 output is available where swa_sink_fwd_path
+ * names a tensor-core kernel ("tc_swa", "tc_global"); elsewhere the call
+ * returns SWA_EUNSUPPORTED.  It halves the output bytes, which dominate the
+ * sliding-window layer's memory traffic.
+ */
+swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const float* sink,
+                           void* out, float* lse, int B, int T, int Hq, int Hkv, int D, int W,
+                           swa_dtype in_dtype, swa_dtype out_dtype, void* stream);
+
+/*
  * swa_sink_decode -- one query token per sequence against a W-slot ring cache
  * ("pwwt.cn" MiMo-V2-Flash essay, section 1.1: the sliding-window KV cache has
  * a fixed size, O(W) memory; ICML 2026 talk write-up, Q&A K: positions keep
@@ -99,6 +112,64 @@ swa_status swa_ring_append(const void* k_new, const void* v_new, void* k_ring, v
                            const int64_t* pos, int B, int Hkv, int D, int W, swa_dtype dtype,
                            void* stream);
 
+/*
+ * swa_sink_verify -- multi-token verify: the attention of L drafted tokens at
+ * positions pos .. pos+L-1 in one pass, for speculative decoding with
+ * multi-token prediction ("MiMo-V2-Flash Technical Report" summary, section
+ * 核心方法: MTP drafts checked by the main model).  The drafts' keys and values
+ * come with the call; the ring holds the tokens BEFORE them and is not
+ * changed (append the accepted prefix afterwards with swa_ring_append).
+ *   q      [B, L, Hq, D]    in_dtype   (the drafted tokens, RoPE applied)
+ *   k_new  [B, L, Hkv, D]   in_dtype
+ *   v_new  [B, L, Hkv, D]   in_dtype
+ *   k_ring [B, Hkv, W, D]   in_dtype   slot s holds position (pos-1) - ((pos-1-s) mod W)
+ *   v_ring [B, Hkv, W, D]   in_dtype
+ *   pos    [B]              int64      position of drafted token 0 (device)
+ *   sink   [Hq]             float32
+ *   out    [B, L, Hq, D]    float32    (written)
+ *   lse    [B, Hq, L]       float32    (written; may be NULL)
+ *   Token j attends to positions [pos+j-W+1, pos+j]: the ring slots whose
+ *   positions fall there (slots of negative positions are empty and ignored,
+ *   whatever they hold) and drafted tokens 0..j; the result equals the
+ *   prefill rows pos .. pos+L-1 of the whole sequence.  A negative pos leaves
+ *   nothing to attend to: out = 0, lse = sink[h].  Requires 1 <= L <= 64, the
+ *   shape rules of swa_sink_decode, and k_new / v_new 16-byte aligned.
+ */
+swa_status swa_sink_verify(const void* q, const void* k_new, const void* v_new,
+                           const void* k_ring, const void* v_ring, const int64_t* pos,
+                           const float* sink, float* out, float* lse, int B, int L, int Hq,
+                           int Hkv, int D, int W, swa_dtype in_dtype, void* stream);
+
+/*
+ * swa_rope -- rotary position embedding in place, at absolute positions (ICML
+ * 2026 talk write-up, Q&A K: RoPE's theta is fixed at inference and position
+ * indices keep counting up while the window slides).  The pages give no
+ * variant; this is the rotate-half form over the first rot_dim dimensions:
+ * for i < rot_dim/2, a_i = p * theta^(-2 i / rot_dim) and the pair
+ * (x[i], x[i + rot_dim/2]) is rotated by a_i; dimensions >= rot_dim pass.
+ *   x    [B, T, H, D]  dtype   (updated; q or k of a prefill)
+ *   pos0 [B]           int64   token (b, t) is at position pos0[b] + t (device)
+ *   Requires D in {64, 128}, rot_dim even with 2 <= rot_dim <= D, theta > 0.
+ *   Angles are formed in fp64 and reduced modulo 2 pi before the fp32 rotation.
+ */
+swa_status swa_rope(void* x, const int64_t* pos0, int B, int T, int H, int D, int rot_dim,
+                    double theta, swa_dtype dtype, void* stream);
+
+/*
+ * swa_rope_append -- the step before a decode, fused: rotate the new token's
+ * query and key at position pos[b] (as swa_rope) and write key and value into
+ * ring slot pos[b] mod W (the fixed O(W) cache of the "pwwt.cn" essay,
+ * section 1.1).
+ *   q_in  [B, Hq, D]  dtype      q_out [B, Hq, D] dtype (written; may equal q_in)
+ *   k_in, v_in [B, Hkv, D] dtype (k before rotation)
+ *   k_ring, v_ring [B, Hkv, W, D] dtype (one slot per sequence updated)
+ *   pos   [B] int64 (device); a negative pos leaves q_out[b] and the rings untouched.
+ */
+swa_status swa_rope_append(const void* q_in, const void* k_in, const void* v_in, void* q_out,
+                           void* k_ring, void* v_ring, const int64_t* pos, int B, int Hq,
+                           int Hkv, int D, int W, int rot_dim, double theta, swa_dtype dtype,
+                           void* stream);
+
 /* Name of the prefill kernel swa_sink_fwd would launch for these sizes
  * ("tc_swa", "tc_global", "simt"), or "invalid". */
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
@@ -107,6 +178,10 @@ const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_d
  * ("tc_decode" for bf16, D = 128, W = 128, Hq = 8 Hkv; "simt_decode"
  * otherwise), or "invalid". */
 const char* swa_sink_decode_path(int B, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
+
+/* Name of the verify kernel swa_sink_verify would launch ("tc_verify",
+ * "simt_verify"), or "invalid". */
+const char* swa_sink_verify_path(int B, int L, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Static text for a status code. */
 const char* swa_status_str(swa_status s);

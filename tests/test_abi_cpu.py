@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("swa_sink_fwd", "swa_sink_decode", "swa_ring_append", "swa_status_str"):
+    for must in ("swa_sink_fwd", "swa_sink_decode", "swa_ring_append", "swa_sink_verify",
+                 "swa_status_str"):
         assert must in names
 
 
@@ -119,3 +120,65 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         mod.lib()
+
+
+def _ver(L_, q=A, kn=A, vn=A, kr=A, vr=A, pos=A, sink=A, out=A, lse=A, B=2, L=4, Hq=8, Hkv=1,
+         D=128, W=128, dt=1):
+    return L_.swa_sink_verify(q, kn, vn, kr, vr, pos, sink, out, lse, B, L, Hq, Hkv, D, W, dt,
+                              None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1), (dict(kn=None), -1), (dict(vn=None), -1), (dict(kr=None), -1),
+    (dict(vr=None), -1), (dict(pos=None), -1), (dict(sink=None), -1), (dict(out=None), -1),
+    (dict(B=0), -1), (dict(L=0), -1), (dict(Hq=6, Hkv=4), -1), (dict(W=0), -1),
+    (dict(kn=A + 8), -1), (dict(pos=A + 4), -1), (dict(dt=3), -1), (dict(D=32), -2),
+    (dict(L=65), -2), (dict(W=321), -2),
+])
+def test_verify_rejects_before_launch(L, kw, status):
+    assert _ver(L, **kw) == status
+
+
+def test_verify_path_selection(L):
+    assert swa.verify_path(2, 4, 8, 1, 128, 128) == "tc_verify"
+    assert swa.verify_path(2, 1, 64, 8, 128, 128) == "tc_verify"
+    assert swa.verify_path(2, 5, 64, 8, 128, 128) == "simt_verify"
+    assert swa.verify_path(2, 4, 64, 8, 128, 128, swa.SWA_F32) == "simt_verify"
+    assert swa.verify_path(2, 4, 8, 1, 64, 128) == "simt_verify"
+    assert swa.verify_path(2, 65, 8, 1, 128, 128) == "invalid"
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, A, 1, 4, 2, 128, 128, 1e4, 1), -1),
+    ((A, None, 1, 4, 2, 128, 128, 1e4, 1), -1),
+    ((A, A, 0, 4, 2, 128, 128, 1e4, 1), -1),
+    ((A + 8, A, 1, 4, 2, 128, 128, 1e4, 1), -1),
+    ((A, A, 1, 4, 2, 128, 127, 1e4, 1), -1),
+    ((A, A, 1, 4, 2, 128, 130, 1e4, 1), -1),
+    ((A, A, 1, 4, 2, 128, 0, 1e4, 1), -1),
+    ((A, A, 1, 4, 2, 128, 128, 0.0, 1), -1),
+    ((A, A, 1, 4, 2, 128, 128, float("inf"), 1), -1),
+    ((A, A, 1, 4, 2, 96, 96, 1e4, 1), -2),
+])
+def test_rope_rejects_before_launch(L, args, status):
+    assert L.swa_rope(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, A, A, A, A, A, A, 1, 8, 1, 128, 128, 128, 1e4, 1), -1),
+    ((A, A, A, A, A, None, A, 1, 8, 1, 128, 128, 128, 1e4, 1), -1),
+    ((A, A, A, A, A, A, A + 4, 1, 8, 1, 128, 128, 128, 1e4, 1), -1),
+    ((A, A, A, A, A, A, A, 1, 8, 1, 128, 0, 128, 1e4, 1), -1),
+    ((A, A, A, A, A, A, A, 1, 8, 1, 128, 128, 3, 1e4, 1), -1),
+    ((A, A, A, A, A, A, A, 1, 8, 1, 128, 128, 128, -1.0, 1), -1),
+    ((A, A, A, A, A, A, A, 1, 8, 1, 32, 128, 32, 1e4, 1), -2),
+])
+def test_rope_append_rejects_before_launch(L, args, status):
+    assert L.swa_rope_append(*args, None) == status
+
+
+def test_fwd_ex_rejects_before_launch(L):
+    ok = (A, A, A, A, A, A, 1, 16, 8, 1, 128, 4, 1)
+    assert L.swa_sink_fwd_ex(*ok, 7, None) == -1          # unknown output dtype
+    assert L.swa_sink_fwd_ex(*ok[:4], None, *ok[5:], 1, None) == -1
+    assert L.swa_sink_fwd_ex(*ok[:4], A + 8, *ok[5:], 1, None) == -1

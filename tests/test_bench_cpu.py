@@ -1,0 +1,35 @@
+"""bench.py without a GPU: its helpers exist and the reference arm (the fp64
+CPU oracle on a bounded sample) prints one well-formed JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_bench_helpers_exist():
+    for name in ("time_prefill", "time_decode", "time_verify", "time_graph", "time_hybrid",
+                 "hybrid_line", "verify_line", "bf16_out_line", "time_e2e", "prefill_roofline",
+                 "cpu_oracle_sample", "run_reference", "run_ours", "recorded_traffic"):
+        assert callable(getattr(bench, name)), name
+
+
+def test_reduce_without_process_group():
+    assert bench.reduce_value(None, 2.5, "max") == 2.5
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0

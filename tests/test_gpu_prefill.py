@@ -191,3 +191,27 @@ def test_hybrid_block_sampled(cuda_ok):
 
 def test_no_device_error_recorded(cuda_ok):
     assert swa.device_error() == 0
+
+
+# ---- bf16 output: the fp32 result rounded, bit for bit -----------------------
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", [
+    (1, 300, 8, 1, 128), (3, 1000, 16, 2, 128), (1, 700, 8, 1, 700), (2, 513, 16, 2, 300),
+])
+def test_bf16_output_is_rounded_fp32_output(cuda_ok, B, T, Hq, Hkv, W):
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=3000 + T + W, device="cuda")
+    o32, l32 = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+    o16, l16 = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(l16, l32)
+    o_ref, l_ref = oracle.swa_sink_fwd(x.q.cpu(), x.k.cpu(), x.v.cpu(), x.sink.cpu(), W)
+    assert_bf16_close(o16.float().cpu().numpy(), o_ref)
+
+
+def test_bf16_output_needs_a_tensor_core_path(cuda_ok):
+    x = gen.prefill_inputs(1, 64, 4, 1, 128, seed=9, device="cuda")
+    assert swa.fwd_path(1, 64, 4, 1, 128, 128) == "simt"
+    with pytest.raises(swa.SwaError) as e:
+        swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, 128, out_dtype=torch.bfloat16)
+    assert e.value.status == swa.SWA_EUNSUPPORTED

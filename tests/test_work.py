@@ -31,3 +31,25 @@ def test_hybrid_reduction_about_six():
     assert f256k > f32k and kv256k > kv32k          # tends to 6 as T grows
     f, kv = work.hybrid_reduction(10 ** 9)
     assert abs(f - 6) < 1e-3 and abs(kv - 6) < 1e-3
+
+
+def test_verify_work_counts():
+    from hybrid_sliding_window_02_b300 import work
+    # one drafted token is a decode against the ring plus itself: same bytes
+    # as decode except the new key/value rows instead of nothing
+    B, Hq, Hkv, D, W = 256, 64, 8, 128, 128
+    assert work.verify_bytes(B, 1, Hq, Hkv, D, W, 2) == (
+        work.decode_bytes(B, Hq, Hkv, D, W, 2) + 2 * B * Hkv * D * 2)
+    assert work.verify_pairs(4, 128, 1000) == 4 * 128
+    assert work.verify_pairs(3, 128, 0) == 1 + 2 + 3
+
+
+def test_hybrid_reduction_seven_to_one():
+    # the 7:1 schedule of the later models, stated as a 7x cut in attention
+    # FLOPs and KV cache ("MiMo-V2.5" ICML 2026 talk write-up, intro and 02):
+    # the closed form is about 7.6x / 7.8x at 32K and tends to 8x with length
+    from hybrid_sliding_window_02_b300 import work
+    flop, kv = work.hybrid_reduction(32768, 128, 7, 1)
+    assert 7.0 <= flop < 8.0 and 7.0 <= kv < 8.0
+    flop_long, kv_long = work.hybrid_reduction(262144, 128, 7, 1)
+    assert flop < flop_long < 8.0 and kv < kv_long < 8.0
