@@ -364,14 +364,14 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
     set_error_text("problem too large for the tensor-core verify kernel");
     return SWA_EUNSUPPORTED;
   }
-  CUtensorMap mk, mv, mq;
+  CUtensorMap mk, mv, mq, mkn, mvn;
   if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, kD, units * kW, 1, 1, 64, kW, 1) ||
       !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, kD, units * kW, 1, 1, 64, kW, 1) ||
-      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, L, B, 64, kG, L))
+      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, L, B, 64, kG, L) ||
+      !make_map_4d(&mkn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kn, kD, Hkv, L, B, 64, 1, L) ||
+      !make_map_4d(&mvn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vn, kD, Hkv, L, B, 64, 1, L))
     return SWA_ECUDA;
   Params p;
-  p.k_new = static_cast<const __nv_bfloat16*>(kn);
-  p.v_new = static_cast<const __nv_bfloat16*>(vn);
   p.pos = pos;
   p.sink = sink;
   p.out = out;
@@ -383,7 +383,7 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
   const long long grid = units < sms ? units : sms;
-  verify_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, p);
+  verify_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mkn, mvn, p);
   return check_launch("verify_tc_kernel");
 }
 

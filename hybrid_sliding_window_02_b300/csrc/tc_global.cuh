@@ -137,12 +137,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
 template <bool kBf16Out>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_global_kernel(const __grid_constant__ CUtensorMap map_q,

@@ -335,38 +335,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(kBarSFree));
 
-      // Mask.  Columns [16, 128) are inside every row's window whenever the
-      // warp's rows all have c_lo <= 16 and c_hi >= 127 (W = 128, n >= 8): then
-      // only the first and last key blocks need the per-column test.
-      float x[kN];
+      // Mask in place.  Columns [16, 128) are inside every row's window whenever
+      // the warp's rows all have c_lo <= 16 and c_hi >= 127 (W = 128, n >= 8):
+      // then only the first and last key blocks need the per-column test.
       const bool mid_ok = __all_sync(0xffffffffu, c_lo <= 16 && c_hi >= 127);
       if (mid_ok) {
 #pragma unroll
-        for (int c = 0; c < kN; ++c) {
-          const bool edge = c < 16 || c >= 128;
-          x[c] = (!edge || (c >= c_lo && c <= c_hi)) ? __uint_as_float(sr[c]) : -INFINITY;
-        }
+        for (int c = 0; c < kN; ++c)
+          if ((c < 16 || c >= 128) && (c < c_lo || c > c_hi)) sr[c] = __float_as_uint(-INFINITY);
       } else {
 #pragma unroll
         for (int c = 0; c < kN; ++c)
-          x[c] = (c >= c_lo && c <= c_hi) ? __uint_as_float(sr[c]) : -INFINITY;
+          if (c < c_lo || c > c_hi) sr[c] = __float_as_uint(-INFINITY);
       }
-      // max over the row: 8 independent chains, then a tree
+      // max over the row: 8 independent chains of 3-input max, then a tree
       float m8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = x[k];
+      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 8]));
 #pragma unroll
-      for (int c = 8; c < kN; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
-      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int c = 16; c < kN; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          m8[k] = max3f(m8[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+      const float mraw = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                               fmaxf(m8[6], m8[7]));
       const float mx = fmaxf(mraw * p.scale_log2, sk);  // scale > 0 commutes with max
+      // p = 2^(x scale - m) in place: scale-and-subtract and the sum two
+      // columns per instruction (f32x2)
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 nm2 = make_float2(-mx, -mx);
       float l8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) l8[k] = 0.f;
 #pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        x[c] = ex2_approx(fmaf(x[c], p.scale_log2, -mx));
-        l8[c & 7] += x[c];
+      for (int c = 0; c < kN; c += 2) {
+        const float2 xx = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                sc2, nm2);
+        const float a = ex2_approx(xx.x), bb = ex2_approx(xx.y);
+        sr[c] = __float_as_uint(a);
+        sr[c + 1] = __float_as_uint(bb);
+        l8[c & 7] += a;
+        l8[(c + 1) & 7] += bb;
       }
       float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       if (sk != -INFINITY) l += ex2_approx(sk - mx);
@@ -379,8 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kNB; ++c) {
         uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          pk[e] = pack_bf16x2(x[16 * c + 2 * e] * inv_l, x[16 * c + 2 * e + 1] * inv_l);
+        for (int e = 0; e < 8; ++e) {
+          pk[e] = pack_bf16x2(__uint_as_float(sr[16 * c + 2 * e]) * inv_l,
+                              __uint_as_float(sr[16 * c + 2 * e + 1]) * inv_l);
+        }
         tmem_st8(tmem + lane_addr + kColP + c * 8, pk);
       }
       tmem_st_wait();

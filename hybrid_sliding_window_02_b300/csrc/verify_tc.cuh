@@ -1,22 +1,33 @@
-// verify_tc.cuh -- multi-token verify against the 128-slot ring with the ring
+// verify_tc.cuh -- multi-token verify against the 128-slot ring with the
 // contractions on the 5th-generation tensor cores.
 //
 // Operation: as in verify.cuh (drafted tokens at positions pos .. pos+L-1
 // checked in one pass; "MiMo-V2-Flash Technical Report" summary, section
 // 核心方法), for bf16 inputs, D = 128, W = 128, groups of 8 query heads and
 // L <= 4 drafted tokens.  Per group (sequence b, kv head g) the 8L query rows
-// r = 8 j + h (token j, head h; padded to 32) meet the 128 ring slots and the
-// L new keys:
-//   S^T = K_ring Q^T       tcgen05, M = 128 slots, N = 32 rows, K = 128 dims
-//   new-key scores         CUDA cores: thread t takes row t / 4, new key t % 4
-//   O^T = V_ring^T P^T     tcgen05, M = 128 dims (V MN-major), N = 32, K = 128
-//   + P_new V_new          CUDA cores, thread = dim
-// Like the decode kernel: persistent CTAs, a producer thread keeping two
-// groups' K, V, Q and new K / V in flight (TMA; the new rows by bulk copies),
-// one MMA thread, two softmax warpgroups on alternate groups.  A softmax
-// thread holds one slot's 32 row scores; the max and the sum over slots are
-// transposing warp-shuffle reductions (31 shuffles leave lane l with row l)
-// finished across the four warps in shared memory.
+// r = 8 j + h (token j, head h) sit in the first lanes of a 128-row tile:
+//   S = Q K_ring^T             tcgen05 SS, M = 128 rows, N = 128 slots, K = 128
+//   new-key scores             CUDA cores (warps 1..3 of the warpgroup)
+//   O = P_ring V_ring + P_new V_new
+//                              tcgen05 TS: P (bf16) written over S in TMEM,
+//                              V MN-major; the new values as one K = 16 step
+// Thread = row: lane r of the warpgroup's first warp reads its 128 slot scores
+// and the new-key scores and runs the sink-seeded softmax alone (as the
+// global-attention kernel does per key block), so no reduction crosses lanes.
+// The rows past 8L are padding that no one reads.
+//
+// Masks.  Slot s holds position p(s) = (pos-1) - ((pos-1-s) mod W).  Once
+// pos >= W the ring is full and row j's window [pos+j-W+1, pos+j] leaves out
+// exactly the j+1 oldest slots, (pos + i) mod W for i <= j: only the 32-column
+// chunks that arc touches are tested column by column.  While pos < W the
+// slots s >= pos are empty (their values are zeroed in shared memory so that
+// 0 * V stays 0) and every column is tested.
+//
+// Persistent CTAs, two stages of K, V, Q and new K / V in flight (TMA), one
+// MMA thread, two warpgroups on alternate groups, each with its own S / O
+// pair in TMEM: S_w [256 w, 256 w + 128), O_w [256 w + 128, 256 w + 256).
+// S of group k overwrites P of group k - 2, so it is issued once that group's
+// PV has completed.
 #pragma once
 
 #include "device_common.cuh"
@@ -28,38 +39,31 @@ constexpr int kThreads = 320;
 constexpr int kWarpProducer = 8, kWarpMma = 9;
 constexpr int kG = 8;
 constexpr int kLmax = 4;
-constexpr int kN = 32;              // MMA N: rows 8 j + h, padded
 constexpr int kW = 128;
 constexpr int kD = 128;
+constexpr int kNewRows = 16;        // new keys padded to one K = 16 MMA step
 constexpr uint32_t kStages = 2;
 
-constexpr int kHalf = kW * 128;                 // 128 rows x 64 bf16
-constexpr int kQHalf = kN * 128;                // 32 rows x 64 bf16
+constexpr int kHalf = 128 * 128;                // 128 rows x 64 bf16 = 16 KB
+constexpr int kNewHalf = kNewRows * 128;        // 16 rows x 64 bf16 = 2 KB
 constexpr int kStageK = 0, kStageV = 2 * kHalf, kStageQ = 4 * kHalf;
-constexpr int kStageKn = kStageQ + 2 * kQHalf;  // new keys [4][128] bf16, plain rows
-constexpr int kStageVn = kStageKn + kLmax * kD * 2;
-constexpr int kStageBytes = kStageVn + kLmax * kD * 2;  // 74 KB
-constexpr int kPBytes = 2 * kQHalf;             // P^T: 32 rows x 128 slots bf16
+constexpr int kStageKn = 6 * kHalf, kStageVn = kStageKn + 2 * kNewHalf;
+constexpr int kStageBytes = kStageVn + 2 * kNewHalf;   // 104 KB
 constexpr int kOffStage = 0;
-constexpr int kOffP = kOffStage + (int)kStages * kStageBytes;
-// per warpgroup: red_max[4][32], red_sum[4][32], new_max[32], new_sum[32], pnew[32][4]
-constexpr int kRedFloats = 4 * 32 + 4 * 32 + 32 + 32 + 32 * 4;
-constexpr int kOffRed = kOffP + 2 * kPBytes;
-constexpr int kOffBar = kOffRed + 2 * kRedFloats * 4;
+constexpr int kOffSn = kOffStage + (int)kStages * kStageBytes;  // [wg][32 rows][4] floats
+constexpr int kOffBar = kOffSn + 2 * 32 * 4 * 4;
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarSFull = 2 * kStages,
-              kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarRed = kBarOFull + 2,
-              kBarDrain = kBarRed + 4, kNumBars = kBarDrain + 1;
+              kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarSnFull = kBarOFull + 2,
+              kBarDrain = kBarSnFull + 2, kNumBars = kBarDrain + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;
 
-constexpr uint32_t kTmemCols = 128;
-__host__ __device__ constexpr uint32_t col_s(int w) { return 64u * (uint32_t)w; }
-__host__ __device__ constexpr uint32_t col_o(int w) { return 64u * (uint32_t)w + 32u; }
+constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr uint32_t col_s(int w) { return 256u * (uint32_t)w; }
+__host__ __device__ constexpr uint32_t col_o(int w) { return 256u * (uint32_t)w + 128u; }
 
 struct Params {
-  const __nv_bfloat16* k_new;
-  const __nv_bfloat16* v_new;
   const int64_t* pos;
   const float* sink;
   float* out;
@@ -69,31 +73,12 @@ struct Params {
   float scale_log2;
 };
 
-// Lane l ends with the max (kMax) or sum over the warp's 32 lanes of v[l].
-template <bool kMax>
-__device__ __forceinline__ float warp_transpose_reduce32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = upper ? v[i] : v[i + n / 2];
-      const float keep = upper ? v[i + n / 2] : v[i];
-      const float got = __shfl_xor_sync(0xffffffffu, send, off);
-      v[i] = kMax ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  return v[0];
-}
-
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v,
-                     const __grid_constant__ CUtensorMap map_q, const Params p) {
+                     const __grid_constant__ CUtensorMap map_q,
+                     const __grid_constant__ CUtensorMap map_kn,
+                     const __grid_constant__ CUtensorMap map_vn, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -116,16 +101,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + w), 1);
       mbar_init(bar(kBarPFull + w), 128);
       mbar_init(bar(kBarOFull + w), 1);
-      mbar_init(bar(kBarRed + 2 * w), 128);
-      mbar_init(bar(kBarRed + 2 * w + 1), 128);
+      mbar_init(bar(kBarSnFull + w), 96);
     }
     mbar_init(bar(kBarDrain), 1);
     fence_mbar_init();
   }
-  // New-key rows L..3 of both stages are never written by a copy: zero them
-  // once (their weights are 0, and 0 * NaN would not be).
-  for (int i = tid; i < (int)kStages * 2 * kLmax * kD * 2 / 16; i += kThreads) {
-    const int st = i / (2 * kLmax * kD * 2 / 16), r = i % (2 * kLmax * kD * 2 / 16);
+  // new key / value rows L..15 of both stages are never written by a copy:
+  // zero them once (their weights are 0, and 0 * NaN would not be)
+  for (int i = tid; i < (int)kStages * 4 * kNewHalf / 16; i += kThreads) {
+    const int st = i / (4 * kNewHalf / 16), r = i % (4 * kNewHalf / 16);
     st_shared_v4(sbase + kOffStage + st * kStageBytes + kStageKn + 16 * r, 0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();
@@ -137,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&map_k);
     prefetch_tmap(&map_v);
     prefetch_tmap(&map_q);
+    prefetch_tmap(&map_kn);
+    prefetch_tmap(&map_vn);
   }
   tc_fence_before();
   __syncthreads();
@@ -146,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProducer) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      const uint32_t bytes = 4 * kHalf + 2 * (8 * L * 128) + 2 * (L * kD * 2);
+      const uint32_t bytes = 4 * kHalf + 2 * (8 * L * 128) + 4 * (L * 128);
       int k = 0;
       for (; k < nk; ++k) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
@@ -158,16 +144,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = sbase + kOffStage + s * kStageBytes;
         const uint32_t fb = bar(kBarFull + s);
         mbar_arrive_expect_tx(fb, bytes);
-        tma_load_4d(st + kStageK, &map_k, 0, u * kW, 0, 0, fb);
-        tma_load_4d(st + kStageK + kHalf, &map_k, 64, u * kW, 0, 0, fb);
-        tma_load_4d(st + kStageV, &map_v, 0, u * kW, 0, 0, fb);
-        tma_load_4d(st + kStageV + kHalf, &map_v, 64, u * kW, 0, 0, fb);
-        tma_load_4d(st + kStageQ, &map_q, 0, g * kG, 0, b, fb);
-        tma_load_4d(st + kStageQ + kQHalf, &map_q, 64, g * kG, 0, b, fb);
-        for (int i = 0; i < L; ++i) {
-          const int64_t row = ((int64_t)b * L + i) * p.Hkv + g;
-          tma_load_1d(st + kStageKn + i * kD * 2, p.k_new + row * kD, kD * 2, fb);
-          tma_load_1d(st + kStageVn + i * kD * 2, p.v_new + row * kD, kD * 2, fb);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load_4d(st + kStageK + hf * kHalf, &map_k, 64 * hf, u * kW, 0, 0, fb);
+          tma_load_4d(st + kStageV + hf * kHalf, &map_v, 64 * hf, u * kW, 0, 0, fb);
+          tma_load_4d(st + kStageQ + hf * kHalf, &map_q, 64 * hf, g * kG, 0, b, fb);
+          tma_load_4d(st + kStageKn + hf * kNewHalf, &map_kn, 64 * hf, g, 0, b, fb);
+          tma_load_4d(st + kStageVn + hf * kNewHalf, &map_vn, 64 * hf, g, 0, b, fb);
         }
       }
       if (k < nk) {
@@ -179,24 +162,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      const uint32_t idesc_s = umma_idesc_bf16(kN, false, false);
-      const uint32_t idesc_o = umma_idesc_bf16(kN, true, false);
+      const uint32_t idesc_s = umma_idesc_bf16(kW, false, false);
+      const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
       auto issue_s = [&](int k) -> bool {
         const uint32_t s = (uint32_t)k % kStages;
+        const int w = k & 1;
         if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
                        abort_flag))
           return false;
+        // S_w holds P of group k - 2 until that group's PV has completed
+        if (k >= 2 && !mbar_wait(bar(kBarOFull + w), (((uint32_t)k >> 1) - 1) & 1,
+                                 kErrWaitOFull, abort_flag))
+          return false;
         tc_fence_after();
         const uint32_t st = sbase + kOffStage + s * kStageBytes;
-        const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
         const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
+        const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t a_off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          const uint32_t b_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + col_s(k & 1), kdesc + a_off, qdesc + b_off, idesc_s, kk > 0);
+          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+          umma_bf16_ss(tmem + col_s(w), qdesc + off, kdesc + off, idesc_s, kk > 0);
         }
-        umma_commit(bar(kBarSFull + (k & 1)));
+        umma_commit(bar(kBarSFull + w));
         return true;
       };
       bool ok = nk > 0 && issue_s(0);
@@ -209,13 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t st = sbase + kOffStage + s * kStageBytes;
         const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
-        const uint64_t pdesc = umma_sdesc(sbase + kOffP + w * kPBytes, 16, 1024, 2);
+        const uint64_t vndesc = umma_sdesc(st + kStageVn, kNewHalf, 1024, 2);
 #pragma unroll
-        for (int kb = 0; kb < kW / 16; ++kb) {
-          const uint32_t a_off = (kb * 16 * 128) >> 4;
-          const uint32_t b_off = ((kb >> 2) * kQHalf + (kb & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + col_o(w), vdesc + a_off, pdesc + b_off, idesc_o, kb > 0);
-        }
+        for (int kb = 0; kb < kW / 16; ++kb)
+          umma_bf16_ts(tmem + col_o(w), tmem + col_s(w) + kb * 8,
+                       vdesc + (uint32_t)(kb * 16 * 128 >> 4), idesc_o, kb > 0);
+        umma_bf16_ts(tmem + col_o(w), tmem + col_s(w) + 64, vndesc, idesc_o, 1u);
         umma_commit(bar(kBarOFull + w));
         umma_commit(bar(kBarEmpty + s));
       }
@@ -224,172 +210,187 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= softmax + output (warps 0..7) =======================
-    const int w = warp >> 2;
-    const int quad = warp & 3;
-    const int t = quad * 32 + lane;            // slot (softmax) / dim (output)
-    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    float* red = reinterpret_cast<float*>(smem + kOffRed) + w * kRedFloats;
-    float* red_max = red;                      // [4][32]
-    float* red_sum = red + 128;                // [4][32]
-    float* new_max = red + 256;                // [32]
-    float* new_sum = red + 288;                // [32]
-    float* pnew = red + 320;                   // [32][4]
-    const uint32_t pbuf = sbase + kOffP + w * kPBytes;
-    const uint32_t bar_max = bar(kBarRed + 2 * w), bar_sum = bar(kBarRed + 2 * w + 1);
-    const int nrow = kG * L;                   // live rows of N
-    const int nr = t >> 2, ni = t & 3;         // new-key score pair of this thread
-    for (int k = w; k < nk; k += 2) {
-      const int u = (int)blockIdx.x + k * (int)gridDim.x;
-      const int b = u / p.Hkv, g = u - b * p.Hkv;
-      const uint32_t s = (uint32_t)k % kStages;
-      const uint32_t st = sbase + kOffStage + s * kStageBytes;
-      const int64_t p0 = p.pos[b];
-      // position held by slot t (ring of the tokens before p0); window of row c
-      // starts at p0 + c / 8 - (W - 1)
-      const int64_t a = p0 - 1 - t;
-      const int64_t pt = p0 - 1 - (((a % kW) + kW) % kW);
-      const bool live = p0 >= 0 && pt >= 0;
-      float sk8[kG];
+    const int w = warp >> 2;                       // warpgroup: groups k with k % 2 == w
+    const int wq = warp & 3;                       // warp within the warpgroup
+    float* sn = reinterpret_cast<float*>(smem + kOffSn) + w * 128;   // [32 rows][4]
+    const int nrow = kG * L;
+    if (wq == 0) {
+      // ============ softmax + output: thread = row r (TMEM lane r) ============
+      const int r = lane;
+      const int j = r >> 3, h = r & 7;
+      const uint32_t s_addr = tmem + col_s(w), o_addr = tmem + col_o(w);
+      for (int k = w; k < nk; k += 2) {
+        const int u = (int)blockIdx.x + k * (int)gridDim.x;
+        const int b = u / p.Hkv, g = u - b * p.Hkv;
+        const int64_t p0 = p.pos[b];
+        const float sk = p.sink[g * kG + h] * 1.4426950408889634f;
+        if (!mbar_wait(bar(kBarSFull + w), ((uint32_t)k >> 1) & 1, kErrWaitSFull, abort_flag))
+          break;
+        tc_fence_after();
+        uint32_t sr[kW];
 #pragma unroll
-      for (int h = 0; h < kG; ++h) sk8[h] = p.sink[g * kG + h] * 1.4426950408889634f;
-      if (!mbar_wait(bar(kBarSFull + w), ((uint32_t)k >> 1) & 1, kErrWaitSFull, abort_flag))
-        break;
-      // the stage's Q and new rows were written by copies this thread reads
-      if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull, abort_flag))
-        break;
-      tc_fence_after();
-      float x[kN];
-      {
-        uint32_t v[kN];
-        tmem_ld32(tmem + lane_addr + col_s(w), v);
+        for (int c = 0; c < kW / 32; ++c) tmem_ld32(s_addr + c * 32, sr + c * 32);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < kN; ++c) {
-          const bool ok = live && c < nrow && pt >= p0 + (c >> 3) - (kW - 1);
-          x[c] = ok ? __uint_as_float(v[c]) * p.scale_log2 : -INFINITY;
+        for (int c = 0; c < kW / 32; ++c) reg_fence32(sr + c * 32);
+        // ---- mask the ring slots outside row j's window ----
+        if (p0 >= kW) {
+          const int a0 = (int)(p0 & (kW - 1));     // slot of the oldest position
+#pragma unroll
+          for (int q = 0; q < kW / 32; ++q) {
+            // does the arc a0 .. a0 + L - 1 (mod W) touch columns [32 q, 32 q + 32)?
+            const bool touch = (((32 * q - a0) & (kW - 1)) < L) ||
+                               (((a0 - 32 * q) & (kW - 1)) < 32);
+            if (touch) {
+#pragma unroll
+              for (int c = 32 * q; c < 32 * q + 32; ++c)
+                if (((c - a0) & (kW - 1)) <= j) sr[c] = __float_as_uint(-INFINITY);
+            }
+          }
+        } else {
+          // partial ring: slot s holds position s when s < pos, else nothing
+          const int lo = (int)p0 + j - (kW - 1);   // first position of the window
+#pragma unroll
+          for (int c = 0; c < kW; ++c)
+            if (c >= p0 || c < lo) sr[c] = __float_as_uint(-INFINITY);
         }
-      }
-      // score of new key ni for row nr (drafts attend causally among themselves)
-      float sn = -INFINITY;
-      if (p0 >= 0 && nr < nrow && ni < L && ni <= (nr >> 3)) {
-        const uint32_t qrow = st + kStageQ + nr * 128;
-        const uint32_t krow = st + kStageKn + ni * kD * 2;
-        float acc = 0.f;
+        // ---- max over the window and the new keys, seeded with the sink ----
+        float m8[8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {   // 16 chunks of 8 dims
-          const uint32_t qa = qrow + (c >> 3) * kQHalf + ((((c & 7) ^ (nr & 7))) << 4);
-          uint32_t qv[4], kv[4];
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(qv[0]), "=r"(qv[1]), "=r"(qv[2]), "=r"(qv[3]) : "r"(qa));
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(kv[0]), "=r"(kv[1]), "=r"(kv[2]), "=r"(kv[3]) : "r"(krow + 16 * c));
+        for (int e = 0; e < 8; ++e)
+          m8[e] = fmaxf(__uint_as_float(sr[e]), __uint_as_float(sr[e + 8]));
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc = fmaf(__uint_as_float(qv[e] << 16), __uint_as_float(kv[e] << 16), acc);
-            acc = fmaf(__uint_as_float(qv[e] & 0xffff0000u), __uint_as_float(kv[e] & 0xffff0000u),
-                       acc);
+        for (int c = 16; c < kW; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            m8[e] = max3f(m8[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
+        const float mring = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                                  fmaxf(m8[6], m8[7])) * p.scale_log2;
+        if (!mbar_wait(bar(kBarSnFull + w), ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag))
+          break;
+        const float4 s4 = *reinterpret_cast<const float4*>(sn + 4 * r);
+        float m = fmaxf(fmaxf(mring, sk), fmaxf(fmaxf(s4.x, s4.y), fmaxf(s4.z, s4.w)));
+        if (m == -INFINITY) m = 0.f;                // nothing to attend to
+        // ---- weights: bf16 P over S columns [0, 64), new keys at [64, 72) ----
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm2 = make_float2(-m, -m);
+        float2 l2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) l2[e] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < kW / 16; ++c) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float2 xx = ffma2(make_float2(__uint_as_float(sr[16 * c + 2 * e]),
+                                                __uint_as_float(sr[16 * c + 2 * e + 1])),
+                                    sc2, nm2);
+            const float2 pp = make_float2(ex2_approx(xx.x), ex2_approx(xx.y));
+            l2[e & 3] = fadd2(l2[e & 3], pp);
+            pk[e] = pack_bf16x2(pp.x, pp.y);
+          }
+          tmem_st8(s_addr + c * 8, pk);
+        }
+        const float pn0 = ex2_approx(s4.x - m), pn1 = ex2_approx(s4.y - m);
+        const float pn2 = ex2_approx(s4.z - m), pn3 = ex2_approx(s4.w - m);
+        {
+          const uint32_t pk[8] = {pack_bf16x2(pn0, pn1), pack_bf16x2(pn2, pn3), 0u, 0u,
+                                  0u, 0u, 0u, 0u};
+          tmem_st8(s_addr + 64, pk);
+        }
+        float l;
+        {
+          const float2 a = fadd2(fadd2(l2[0], l2[1]), fadd2(l2[2], l2[3]));
+          l = (a.x + a.y) + ((pn0 + pn1) + (pn2 + pn3));
+          if (sk != -INFINITY) l += ex2_approx(sk - m);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull + w));
+        if (r < nrow && p.lse != nullptr)
+          p.lse[((int64_t)b * p.Hq + g * kG + h) * L + j] = (m + __log2f(l)) * 0.6931471805599453f;
+        // ---- output row: O / l ----
+        if (!mbar_wait(bar(kBarOFull + w), ((uint32_t)k >> 1) & 1, kErrWaitOFull, abort_flag))
+          break;
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        float* orow = p.out + (((int64_t)b * L + j) * p.Hq + g * kG + h) * kD;
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          tmem_ld_wait();
+          reg_fence32(o);
+          if (r < nrow) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              st_global_v4(orow + c * 32 + 4 * e,
+                           __float_as_uint(__uint_as_float(o[4 * e]) * inv_l),
+                           __float_as_uint(__uint_as_float(o[4 * e + 1]) * inv_l),
+                           __float_as_uint(__uint_as_float(o[4 * e + 2]) * inv_l),
+                           __float_as_uint(__uint_as_float(o[4 * e + 3]) * inv_l));
           }
         }
-        sn = acc * p.scale_log2;
+        tc_fence_before();
       }
-      // ---- max over slots and new keys, per row ----
-      {
-        float mv[kN];
+    } else {
+      // ============ new-key scores and empty-slot values (warps 1..3) ============
+      const int t = (wq - 1) * 32 + lane;        // 0 .. 95
+      for (int k = w; k < nk; k += 2) {
+        const int u = (int)blockIdx.x + k * (int)gridDim.x;
+        const int b = u / p.Hkv;
+        const uint32_t s = (uint32_t)k % kStages;
+        const uint32_t st = sbase + kOffStage + s * kStageBytes;
+        const int64_t p0 = p.pos[b];
+        // the stage's Q and new rows come from copies this warp reads
+        if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull, abort_flag))
+          break;
+        // the scores of group k - 2 must have been read by the softmax warp
+        if (k >= 2 && !mbar_wait(bar(kBarPFull + w), (((uint32_t)k >> 1) - 1) & 1, kErrWaitPFull,
+                                 abort_flag))
+          break;
+        for (int pr = t; pr < 32 * kLmax; pr += 96) {
+          const int r = pr >> 2, i = pr & 3;
+          float v = -INFINITY;
+          if (p0 >= 0 && r < nrow && i < L && i <= (r >> 3)) {
+            float acc = 0.f;
 #pragma unroll
-        for (int c = 0; c < kN; ++c) mv[c] = x[c];
-        red_max[quad * 32 + lane] = warp_transpose_reduce32<true>(mv, lane);
-        float nm = fmaxf(sn, __shfl_xor_sync(0xffffffffu, sn, 1));
-        nm = fmaxf(nm, __shfl_xor_sync(0xffffffffu, nm, 2));
-        if (ni == 0) new_max[nr] = nm;
-      }
-      mbar_arrive(bar_max);
-      if (!mbar_wait(bar_max, ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag)) break;
-      float m[kN];
+            for (int c = 0; c < 16; ++c) {   // 16 chunks of 8 dims (128-byte swizzle)
+              const uint32_t hoff = (c >> 3);
+              const uint32_t qa = st + kStageQ + hoff * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+              const uint32_t ka = st + kStageKn + hoff * kNewHalf + i * 128 + (((c & 7) ^ (i & 7)) << 4);
+              uint32_t qv[4], kv[4];
+              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(qv[0]), "=r"(qv[1]), "=r"(qv[2]), "=r"(qv[3]) : "r"(qa));
+              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(kv[0]), "=r"(kv[1]), "=r"(kv[2]), "=r"(kv[3]) : "r"(ka));
 #pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        const float mr = fmaxf(fmaxf(red_max[c], red_max[32 + c]),
-                               fmaxf(red_max[64 + c], red_max[96 + c]));
-        m[c] = fmaxf(fmaxf(mr, new_max[c]), sk8[c & 7]);
-        if (m[c] == -INFINITY) m[c] = 0.f;  // nothing to attend to: all weights 0
-      }
-      // ---- weights: ring part to shared memory (bf16 P^T), new part kept ----
-#pragma unroll
-      for (int c = 0; c < kN; ++c) x[c] = ex2_approx(x[c] - m[c]);
-      float pn = 0.f;
-      {
-        float mn = m[0];
-#pragma unroll
-        for (int c = 1; c < kN; ++c) mn = (nr == c) ? m[c] : mn;
-        pn = ex2_approx(sn - mn);
-        pnew[nr * 4 + ni] = pn;
-      }
-      const uint32_t p_off = (t >> 6) * kQHalf + 2 * (t & 7);
-      const int p_chunk = (t & 63) >> 3;
-#pragma unroll
-      for (int c = 0; c < kN; ++c)
-        st_shared_u16(pbuf + p_off + c * 128 + (((p_chunk ^ c) & 7) << 4),
-                      __bfloat16_as_ushort(__float2bfloat16_rn(x[c])));
-      if (!live) {  // empty slot: zero its values so that 0 * V stays 0
-        const uint32_t vrow = st + kStageV + t * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          st_shared_v4(vrow + 16 * c, 0u, 0u, 0u, 0u);
-          st_shared_v4(vrow + kHalf + 16 * c, 0u, 0u, 0u, 0u);
+              for (int e = 0; e < 4; ++e) {
+                acc = fmaf(__uint_as_float(qv[e] << 16), __uint_as_float(kv[e] << 16), acc);
+                acc = fmaf(__uint_as_float(qv[e] & 0xffff0000u),
+                           __uint_as_float(kv[e] & 0xffff0000u), acc);
+              }
+            }
+            v = acc * p.scale_log2;
+          }
+          sn[pr] = v;
         }
-      }
-      // this group's new values, read now: the stage is handed back to the
-      // producer as soon as the PV product completes
-      float vn[kLmax];
-      {
-        const uint16_t* vs = reinterpret_cast<const uint16_t*>(smem + s * kStageBytes + kStageVn);
+        mbar_arrive(bar(kBarSnFull + w));
+        // empty slots (pos < W): zero their values in the stage before the PV
+        if (p0 < kW) {
+          for (int sl = t; sl < kW; sl += 96) {
+            if (sl >= p0) {
+              const uint32_t vrow = st + kStageV + sl * 128;
 #pragma unroll
-        for (int i = 0; i < kLmax; ++i)
-          vn[i] = __uint_as_float((uint32_t)vs[i * kD + t] << 16);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPFull + w));
-      // ---- sums ----
-      red_sum[quad * 32 + lane] = warp_transpose_reduce32<false>(x, lane);
-      {
-        float ns = pn + __shfl_xor_sync(0xffffffffu, pn, 1);
-        ns += __shfl_xor_sync(0xffffffffu, ns, 2);
-        if (ni == 0) new_sum[nr] = ns;
-      }
-      mbar_arrive(bar_sum);
-      if (!mbar_wait(bar_sum, ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag)) break;
-      float inv_l[kN];
-#pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        float lt = (red_sum[c] + red_sum[32 + c]) + (red_sum[64 + c] + red_sum[96 + c]) +
-                   new_sum[c];
-        if (sk8[c & 7] != -INFINITY) lt += ex2_approx(sk8[c & 7] - m[c]);
-        inv_l[c] = lt > 0.f ? 1.f / lt : 0.f;
-        if (t == c && c < nrow && p.lse != nullptr)
-          p.lse[((int64_t)b * p.Hq + g * kG + (c & 7)) * L + (c >> 3)] =
-              (m[c] + __log2f(lt)) * 0.6931471805599453f;
-      }
-      // ---- output: O^T[dim t][row c] + sum_i pnew[c][i] v_new[i][t] ----
-      if (!mbar_wait(bar(kBarOFull + w), ((uint32_t)k >> 1) & 1, kErrWaitOFull, abort_flag))
-        break;
-      tc_fence_after();
-      uint32_t o[kN];
-      tmem_ld32(tmem + lane_addr + col_o(w), o);
-      tmem_ld_wait();
-      tc_fence_before();
-#pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        if (c < nrow) {
-          const float4 pw = *reinterpret_cast<const float4*>(pnew + 4 * c);
-          float acc = __uint_as_float(o[c]);
-          acc = fmaf(pw.x, vn[0], acc);
-          acc = fmaf(pw.y, vn[1], acc);
-          acc = fmaf(pw.z, vn[2], acc);
-          acc = fmaf(pw.w, vn[3], acc);
-          p.out[(((int64_t)b * L + (c >> 3)) * p.Hq + g * kG + (c & 7)) * kD + t] =
-              acc * inv_l[c];
+              for (int c = 0; c < 8; ++c) {
+                st_shared_v4(vrow + 16 * c, 0u, 0u, 0u, 0u);
+                st_shared_v4(vrow + kHalf + 16 * c, 0u, 0u, 0u, 0u);
+              }
+            }
+          }
+          fence_proxy_async_smem();
         }
+        mbar_arrive(bar(kBarPFull + w));
       }
     }
   }

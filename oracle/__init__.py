@@ -64,6 +64,12 @@ def _load():
             lib.oracle_swa_sink_verify.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i32, i32,
                                                    i32, i64, i32, i32]
             lib.oracle_rope.argtypes = [p, p, p, i64, i64, i32, i32, i32, ctypes.c_double, i32]
+            lib.oracle_block_max.argtypes = [p, p, p, i64, i64, i32, i32, i32, i64, i32, i32]
+            lib.oracle_topk_blocks.argtypes = [p, p, i64, i64, i32, i32, i32]
+            lib.oracle_sparse_fwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i32, i32, i32, i32,
+                                              i32, i32, i32]
+            for f in (lib.oracle_block_max, lib.oracle_topk_blocks, lib.oracle_sparse_fwd):
+                f.restype = i32
             for f in (lib.oracle_swa_sink_fwd, lib.oracle_swa_sink_fwd_rows,
                       lib.oracle_swa_sink_decode, lib.oracle_swa_sink_verify, lib.oracle_rope):
                 f.restype = i32
@@ -208,6 +214,58 @@ def rope(x, pos0, rot_dim: int, theta: float):
     if rc != 0:
         raise ValueError(f"oracle_rope failed ({rc})")
     return y
+
+
+def block_max(q, k, W: int, nthreads: int = 0):
+    """Block scores of a layer: [B, Hkv, ceil(T/4), ceil(T/128)] float64, the max
+    scaled logit over the valid pairs of each (kv head, 4-position query group,
+    128-key block); -inf where there is none."""
+    (qa, ka), code = _same_type(q, k)
+    B, T, Hq, D = qa.shape
+    Hkv = ka.shape[2]
+    out = np.empty((B, Hkv, (T + 3) // 4, (T + 127) // 128), dtype=np.float64)
+    rc = _load().oracle_block_max(_ptr(qa), _ptr(ka), _ptr(out), B, T, Hq, Hkv, D, int(W), code,
+                                  int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_block_max failed ({rc})")
+    return out
+
+
+def topk_blocks(scores, T: int, QB: int, topk: int):
+    """Block selection from scores [B, Hkv, ceil(T/4), ceil(T/128)] (cast to
+    float32): int32 [B, Hkv, ceil(T/QB), topk], increasing, padded with -1."""
+    sc = np.ascontiguousarray(np.asarray(scores, dtype=np.float32))
+    B, Hkv = sc.shape[0], sc.shape[1]
+    out = np.empty((B, Hkv, (T + QB - 1) // QB, topk), dtype=np.int32)
+    rc = _load().oracle_topk_blocks(_ptr(sc), _ptr(out), B, int(T), Hkv, int(QB), int(topk))
+    if rc != 0:
+        raise ValueError(f"oracle_topk_blocks failed ({rc})")
+    return out
+
+
+def sparse_fwd(q, k, v, sink, idx, QB: int, nthreads: int = 0):
+    """Attention over the selected key blocks: idx [B, Hkv, ceil(T/QB), topk]
+    int32.  Returns (out [B,T,Hq,D], lse [B,Hq,T]) float64."""
+    (qa, ka, va), code = _same_type(q, k, v)
+    B, T, Hq, D = qa.shape
+    Hkv = ka.shape[2]
+    try:
+        import torch
+        if isinstance(idx, torch.Tensor):
+            idx = idx.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    ia = np.ascontiguousarray(idx, dtype=np.int32)
+    topk = ia.shape[-1]
+    s = _sink64(sink)
+    out = np.empty((B, T, Hq, D), dtype=np.float64)
+    lse = np.empty((B, Hq, T), dtype=np.float64)
+    rc = _load().oracle_sparse_fwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(s), _ptr(ia), _ptr(out),
+                                   _ptr(lse), B, T, Hq, Hkv, D, int(QB), int(topk), code,
+                                   int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_sparse_fwd failed ({rc})")
+    return out, lse
 
 
 def swa_sink_decode(q, k_ring, v_ring, pos, sink, nthreads: int = 0):

@@ -310,4 +310,140 @@ int oracle_rope(const void* x, const int64_t* pos0, double* y, int64_t B, int64_
   return 0;
 }
 
+/* ---- High Sparse: block scores from a global layer, block selection, and
+ * attention over the selected blocks ("MiMo-V2.5" ICML 2026 talk write-up,
+ * section 02: the full-attention layers' FlashAttention block-level scores are
+ * reused, at no extra cost, to choose the tokens the sparse layers attend to;
+ * sparse layers share the full layer's KV cache; selection is by block with a
+ * configurable capacity).  The page gives no formula; the readings are:
+ *   block score  max over the scaled logits x_ij = q_i.k_j / sqrt(D) of the
+ *                valid (window / causal) pairs with query position i in a
+ *                group of 4 consecutive positions, query head h in kv group g,
+ *                key j in a block of 128; -inf when the block has none
+ *   selection    per query block of QB positions: the key block holding the
+ *                block's last position (the causal diagonal), then the
+ *                topk - 1 highest-scoring earlier blocks (score of a block =
+ *                max over the query block's groups; ties: smaller index
+ *                first); listed in increasing order, padded with -1
+ *   sparse layer causal attention of query i over the keys j <= i of the
+ *                blocks selected for its query block, sink in the denominator */
+
+/* blockmax [B, Hkv, ceil(T/4), ceil(T/128)] (fp64) */
+int oracle_block_max(const void* q, const void* k, double* blockmax, int64_t B, int64_t T,
+                     int Hq, int Hkv, int D, int64_t W, int dtype, int nthreads) {
+  if (B < 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || W <= 0) return -1;
+  const int64_t G = Hq / Hkv, nqg = (T + 3) / 4, nkb = (T + 127) / 128;
+  const double inv_sqrt_d = 1.0 / sqrt((double)D);
+  const int64_t n = B * Hkv * nqg;
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
+  for (int64_t r = 0; r < n; ++r) {
+    const int64_t b = r / (Hkv * nqg), g = (r / nqg) % Hkv, qg = r % nqg;
+    double* row = blockmax + r * nkb;
+    for (int64_t kb = 0; kb < nkb; ++kb) row[kb] = -INFINITY;
+    for (int64_t i = 4 * qg; i < 4 * qg + 4 && i < T; ++i) {
+      int64_t j0 = i - W + 1;
+      if (j0 < 0) j0 = 0;
+      for (int64_t hh = 0; hh < G; ++hh) {
+        const int64_t h = g * G + hh;
+        const int64_t qoff = ((b * T + i) * Hq + h) * D;
+        for (int64_t j = j0; j <= i; ++j) {
+          const int64_t koff = ((b * T + j) * Hkv + g) * D;
+          double dot = 0.0;
+          for (int d = 0; d < D; ++d) dot += widen(q, dtype, qoff + d) * widen(k, dtype, koff + d);
+          const double x = dot * inv_sqrt_d;
+          if (x > row[j / 128]) row[j / 128] = x;
+        }
+      }
+    }
+  }
+  return 0;
+}
+
+/* scores [B, Hkv, nqg, nkb] fp32 (block maxima as produced above, in any
+ * precision the caller chose); idx [B, Hkv, nqb, topk] int32 with
+ * nqb = ceil(T / QB).  QB must be a multiple of 4 and divide 128. */
+int oracle_topk_blocks(const float* scores, int32_t* idx, int64_t B, int64_t T, int Hkv, int QB,
+                       int topk) {
+  if (B < 0 || T <= 0 || Hkv <= 0 || QB <= 0 || QB % 4 || 128 % QB || topk <= 0) return -1;
+  const int64_t nqg = (T + 3) / 4, nkb = (T + 127) / 128, nqb = (T + QB - 1) / QB;
+  double* agg = (double*)malloc(sizeof(double) * (nkb > 0 ? nkb : 1));
+  unsigned char* taken = (unsigned char*)malloc(nkb > 0 ? nkb : 1);
+  if (!agg || !taken) { free(agg); free(taken); return -2; }
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t g = 0; g < Hkv; ++g)
+      for (int64_t qb = 0; qb < nqb; ++qb) {
+        int32_t* out = idx + ((b * Hkv + g) * nqb + qb) * topk;
+        int64_t last = qb * QB + QB - 1;
+        if (last > T - 1) last = T - 1;
+        const int64_t diag = last / 128;          /* the causal diagonal block */
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+          agg[kb] = -INFINITY;
+          taken[kb] = 0;
+        }
+        for (int64_t qg = qb * QB / 4; qg < (qb + 1) * QB / 4 && qg < nqg; ++qg)
+          for (int64_t kb = 0; kb <= diag; ++kb) {
+            const double v = scores[((b * Hkv + g) * nqg + qg) * nkb + kb];
+            if (v > agg[kb]) agg[kb] = v;
+          }
+        taken[diag] = 1;
+        /* topk - 1 rounds of "highest score, smallest index" among earlier blocks */
+        for (int t = 1; t < topk; ++t) {
+          int64_t best = -1;
+          for (int64_t kb = 0; kb < diag; ++kb) {
+            if (taken[kb]) continue;
+            if (best < 0 || agg[kb] > agg[best]) best = kb;
+          }
+          if (best < 0) break;
+          taken[best] = 1;
+        }
+        int n = 0;
+        for (int64_t kb = 0; kb <= diag; ++kb)
+          if (taken[kb]) out[n++] = (int32_t)kb;
+        while (n < topk) out[n++] = -1;
+      }
+  free(agg);
+  free(taken);
+  return 0;
+}
+
+/* Attention of the sparse layer over the selected blocks (see above).
+ * idx [B, Hkv, nqb, topk] int32 (-1 = unused); out [B,T,Hq,D], lse [B,Hq,T]. */
+int oracle_sparse_fwd(const void* q, const void* k, const void* v, const double* sink,
+                      const int32_t* idx, double* out, double* lse, int64_t B, int64_t T, int Hq,
+                      int Hkv, int D, int QB, int topk, int dtype, int nthreads) {
+  if (B < 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || QB <= 0 || topk <= 0)
+    return -1;
+  const int64_t G = Hq / Hkv, nqb = (T + QB - 1) / QB;
+  const int64_t nrows = B * Hq * T;
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
+  {
+    int64_t* koff = (int64_t*)malloc(sizeof(int64_t) * (int64_t)topk * 128);
+    double* x = (double*)malloc(sizeof(double) * (int64_t)topk * 128);
+    double* o = (double*)malloc(sizeof(double) * D);
+    if (!koff || !x || !o) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 64)
+      for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t b = r / (Hq * T), h = (r / T) % Hq, i = r % T, g = h / G;
+        const int32_t* sel = idx + ((b * Hkv + g) * nqb + i / QB) * topk;
+        int n = 0;
+        for (int t = 0; t < topk; ++t) {
+          if (sel[t] < 0) continue;
+          for (int64_t j = (int64_t)sel[t] * 128; j < (int64_t)sel[t] * 128 + 128 && j <= i; ++j)
+            koff[n++] = ((b * T + j) * Hkv + g) * D;
+        }
+        const double l = attend_row(q, ((b * T + i) * Hq + h) * D, k, v, koff, n, sink[h], D,
+                                    dtype, x, o);
+        memcpy(out + ((b * T + i) * Hq + h) * D, o, sizeof(double) * D);
+        lse[(b * Hq + h) * T + i] = l;
+      }
+    }
+    free(koff); free(x); free(o);
+  }
+  return bad ? -2 : 0;
+}
+
 int oracle_num_threads(void) { return omp_get_max_threads(); }

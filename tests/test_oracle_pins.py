@@ -371,3 +371,121 @@ def test_rope_scores_depend_on_relative_position_only():
                       oracle.rope(k, torch.tensor([pk]), 32, 10000.0)).sum())
     for shift in (0, 129, 262000):
         np.testing.assert_allclose(score(shift + 40, shift + 13), score(40, 13), rtol=1e-9)
+
+
+# ---- High Sparse: block scores, block selection, sparse attention ----------
+def _scores_np(q, k, W):
+    """Explicit scaled-logit matrix [B, Hq, T, T] with -inf outside the band."""
+    q64, k64 = _f64(q), _f64(k)
+    B, T, Hq, D = q64.shape
+    G = Hq // k64.shape[2]
+    kk = np.repeat(k64, G, axis=2)
+    x = np.einsum("bihd,bjhd->bhij", q64, kk) / math.sqrt(D)
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    x[:, :, ~((j <= i) & (j > i - W))] = -np.inf
+    return x
+
+
+@pytest.mark.parametrize("T,W", [(10, 10), (200, 200), (300, 150), (129, 7)])
+def test_block_max_is_brute_force(T, W):
+    B, Hq, Hkv, D = 2, 4, 2, 16
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=91 + T, dtype=torch.float32)
+    got = oracle.block_max(x.q, x.k, W)
+    s = _scores_np(x.q, x.k, W)                      # [B, Hq, T, T]
+    nqg, nkb = (T + 3) // 4, (T + 127) // 128
+    pad = np.full((B, Hq, nqg * 4, nkb * 128), -np.inf)
+    pad[:, :, :T, :T] = s
+    G = Hq // Hkv
+    ref = pad.reshape(B, Hkv, G, nqg, 4, nkb, 128).max(axis=(2, 4, 6))
+    np.testing.assert_array_equal(np.isinf(got), np.isinf(ref))
+    fin = np.isfinite(ref)
+    np.testing.assert_allclose(got[fin], ref[fin], rtol=0, atol=1e-12)
+
+
+def _topk_np(scores, T, QB, topk):
+    B, Hkv, nqg, nkb = scores.shape
+    nqb = (T + QB - 1) // QB
+    out = np.full((B, Hkv, nqb, topk), -1, dtype=np.int32)
+    for b in range(B):
+        for g in range(Hkv):
+            for qb in range(nqb):
+                diag = (min(qb * QB + QB, T) - 1) // 128
+                agg = scores[b, g, qb * QB // 4:(qb + 1) * QB // 4, :diag].astype(np.float64)
+                agg = agg.max(axis=0) if agg.shape[0] else np.full(diag, -np.inf)
+                order = np.lexsort((np.arange(diag), -agg))   # score desc, index asc
+                chosen = sorted([diag] + [int(c) for c in order[:topk - 1]])
+                out[b, g, qb, :len(chosen)] = chosen
+    return out
+
+
+@pytest.mark.parametrize("T,QB,topk", [(1000, 64, 3), (2048, 128, 5), (700, 32, 1), (300, 16, 9)])
+def test_topk_blocks_matches_ranking(T, QB, topk):
+    g = np.random.default_rng(T + QB + topk)
+    nqg, nkb = (T + 3) // 4, (T + 127) // 128
+    scores = g.normal(size=(2, 3, nqg, nkb)).astype(np.float32)
+    scores[..., 1] = scores[..., 2]                  # a tie: the smaller index wins
+    got = oracle.topk_blocks(scores, T, QB, topk)
+    np.testing.assert_array_equal(got, _topk_np(scores, T, QB, topk))
+    for b, gg, qb in np.ndindex(*got.shape[:3]):
+        sel = got[b, gg, qb]
+        live = sel[sel >= 0]
+        diag = (min(qb * QB + QB, T) - 1) // 128
+        assert diag in live and np.all(np.diff(live) > 0)
+        assert len(live) == min(topk, diag + 1)
+
+
+def test_sparse_with_every_block_is_the_global_layer():
+    B, T, Hq, Hkv, D, QB = 2, 300, 4, 2, 16, 32
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=95, dtype=torch.bfloat16)
+    nkb = (T + 127) // 128
+    idx = np.tile(np.arange(nkb, dtype=np.int32), (B, Hkv, (T + QB - 1) // QB, 1))
+    o, l = oracle.sparse_fwd(x.q, x.k, x.v, x.sink, idx, QB)
+    og, lg = oracle.swa_sink_fwd(x.q, x.k, x.v, x.sink, T)
+    np.testing.assert_allclose(o, og, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, lg, rtol=0, atol=1e-12)
+
+
+def test_sparse_is_brute_force_with_a_block_mask():
+    B, T, Hq, Hkv, D, QB, topk = 1, 400, 4, 2, 16, 16, 2
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=96, dtype=torch.float32)
+    g = np.random.default_rng(7)
+    nqb, nkb = (T + QB - 1) // QB, (T + 127) // 128
+    idx = np.full((B, Hkv, nqb, topk), -1, dtype=np.int32)
+    for gg in range(Hkv):
+        for qb in range(nqb):
+            diag = (min(qb * QB + QB, T) - 1) // 128
+            other = [int(c) for c in g.permutation(diag)[:topk - 1]]
+            sel = sorted(set([diag] + other))
+            idx[0, gg, qb, :len(sel)] = sel
+    o, l = oracle.sparse_fwd(x.q, x.k, x.v, x.sink, idx, QB)
+    s = _scores_np(x.q, x.k, T)                      # causal, [B, Hq, T, T]
+    G = Hq // Hkv
+    allowed = np.zeros((Hkv, T, T), dtype=bool)
+    for gg in range(Hkv):
+        for i in range(T):
+            for kb in idx[0, gg, i // QB]:
+                if kb >= 0:
+                    allowed[gg, i, kb * 128:kb * 128 + 128] = True
+    s[0][~np.repeat(allowed, G, axis=0)] = -np.inf
+    sk = _f64(x.sink)[None, :, None, None]
+    m = np.maximum(s.max(axis=-1, keepdims=True), sk)
+    e = np.exp(s - m)
+    lsum = e.sum(axis=-1, keepdims=True) + np.exp(sk - m)
+    vv = np.repeat(_f64(x.v), G, axis=2)
+    ref = np.einsum("bhij,bjhd->bihd", e / lsum, vv)
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, (m + np.log(lsum))[..., 0], rtol=0, atol=1e-12)
+
+
+def test_sparse_ignores_keys_outside_the_selection():
+    B, T, Hq, Hkv, D, QB = 1, 384, 2, 1, 16, 128
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=97, dtype=torch.float32)
+    idx = np.array([[[[0, -1], [1, -1], [0, 2]]]], dtype=np.int32)   # block 1 unused by qb 2
+    ref = oracle.sparse_fwd(x.q, x.k, x.v, x.sink, idx, QB)
+    k, v = x.k.clone(), x.v.clone()
+    k[:, 128:256] = float("nan")
+    v[:, 128:256] = float("nan")
+    got = oracle.sparse_fwd(x.q, k, v, x.sink, idx, QB)
+    np.testing.assert_array_equal(got[0][:, 256:], ref[0][:, 256:])
+    np.testing.assert_array_equal(got[0][:, :128], ref[0][:, :128])
