@@ -465,6 +465,78 @@ def hybrid_line(swa, dev, stream, reps, peaks, n_swa=None):
     }
 
 
+SPARSE = dict(T=32768, Hq=64, Hkv=8, D=128, QB=64, topk=16)
+
+
+def _event_ms(fn, reps, stream):
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def high_sparse_line(swa, dev, stream, reps, peaks):
+    """High Sparse on one sequence of T=32768: the global layer with and
+    without its block scores, the selection, and the sparse layer over the
+    selected blocks of the shared K/V."""
+    c = SPARSE
+    T, Hq, Hkv, D, QB, topk = (c[k] for k in ("T", "Hq", "Hkv", "D", "QB", "topk"))
+    x = gen.prefill_inputs(1, T, Hq, Hkv, D, seed=500, device=dev)
+    q2 = gen.prefill_inputs(1, T, Hq, Hkv, D, seed=501, device=dev).q
+    state = {}
+
+    def glb():
+        swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, T, stream=stream)
+
+    def glb_scores():
+        state["bm"] = swa.swa_sink_fwd_scores(x.q, x.k, x.v, x.sink, T, stream=stream)[2]
+
+    ms_g = _event_ms(glb, reps, stream)
+    ms_gs = _event_ms(glb_scores, reps, stream)
+    ms_sel = _event_ms(lambda: state.__setitem__(
+        "idx", swa.swa_topk_blocks(state["bm"], T, QB, topk, stream=stream)), reps, stream)
+    ms_sp = _event_ms(lambda: swa.swa_sink_sparse_fwd(q2, x.k, x.v, x.sink, state["idx"], QB,
+                                                      stream=stream), reps, stream)
+    # algorithmic work of the sparse layer: keys j <= i of the selected blocks
+    idx = state["idx"][0].cpu().numpy()              # [Hkv, nqb, topk]
+    pairs = 0
+    for g in range(Hkv):
+        for qb in range(idx.shape[1]):
+            for kb in idx[g, qb]:
+                if kb < 0:
+                    continue
+                i0, i1 = qb * QB, min(qb * QB + QB, T)
+                j0 = int(kb) * 128
+                for i in range(i0, i1):
+                    pairs += max(0, min(i, j0 + 127) - j0 + 1)
+    sp_flops = 4 * D * (Hq // Hkv) * pairs
+    gl_flops = work.prefill_flops(1, T, Hq, D, T)
+    del x, q2, state
+    torch.cuda.empty_cache()
+    return {
+        "workload": f"High Sparse B1 T{T} Hq{Hq} Hkv{Hkv} D{D}: global layer + block scores, "
+                    f"top-{topk} blocks per {QB}-position query block, sparse layer on the "
+                    "shared K/V",
+        "global_ms": round(ms_g, 3), "global_with_scores_ms": round(ms_gs, 3),
+        "score_overhead": round(ms_gs / ms_g - 1.0, 4),
+        "select_ms": round(ms_sel, 4),
+        "sparse_ms": round(ms_sp, 3),
+        "sparse_tflops": round(sp_flops / (ms_sp * 1e-3) / 1e12, 1),
+        "sparse_fraction_of_global_flops": round(sp_flops / gl_flops, 4),
+        "roofline": {"kernel": "swa_fwd_tc_global_kernel (sparse mode)", "bound": "tensor",
+                     "achieved": round(sp_flops / (ms_sp * 1e-3) / 1e12, 1),
+                     "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                     "frac": round(sp_flops / (ms_sp * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4)},
+    }
+
+
 def bf16_out_line(swa, x, c, steps, dev, stream, peaks):
     """The headline prefill with bf16 output (out rounded from fp32, lse fp32)."""
     B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
@@ -618,6 +690,7 @@ def run_ours(args, dist):
         # layers per global layer
         line["hybrid_block_7to1"] = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks,
                                                 n_swa=7)
+        line["high_sparse"] = high_sparse_line(swa, dev, stream, args.hybrid_reps, peaks)
     if not args.no_e2e:
         xh = gen.PrefillInputs(*(t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.sink)))
         e2e_ms, h2d, d2h = time_e2e(swa, xh, c, max(3, args.steps // 50), dev, stream)

@@ -65,6 +65,13 @@ def lib() -> ctypes.CDLL:
                                           i32, p]
             L.swa_rope.restype = i32
             L.swa_rope_append.restype = i32
+            L.swa_sink_fwd_scores.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32,
+                                              i32, i32, p]
+            L.swa_topk_blocks.argtypes = [p, p, i32, i32, i32, i32, i32, p]
+            L.swa_sink_sparse_fwd.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32,
+                                              i32, i32, i32, p]
+            for f in (L.swa_sink_fwd_scores, L.swa_topk_blocks, L.swa_sink_sparse_fwd):
+                f.restype = i32
             L.swa_sink_verify_path.argtypes = [i32, i32, i32, i32, i32, i32, i32]
             L.swa_sink_verify_path.restype = ctypes.c_char_p
             for f in (L.swa_sink_fwd, L.swa_sink_decode, L.swa_ring_append, L.swa_sink_verify):
@@ -296,6 +303,73 @@ def swa_rope_append(q, k, v, k_ring, v_ring, pos, rot_dim: int, theta: float, q_
                                _stream_handle(stream, dev))
     _check("swa_rope_append", st)
     return q_out
+
+
+def _prefill_checks(q, k, v, sink):
+    import torch
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v), ("sink", sink)):
+        _cuda_contig(n, t, dev)
+    if k.shape != (B, T, Hkv, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, T, Hkv, D] matching q")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if sink.dtype != torch.float32 or sink.shape != (Hq,):
+        raise ValueError("sink must be float32 [Hq]")
+    return B, T, Hq, Hkv, D, dev
+
+
+def swa_sink_fwd_scores(q, k, v, sink, W: int, *, out_dtype=None, stream=None):
+    """Prefill on the tensor-core global kernel that also returns the block
+    scores of High Sparse: (out, lse, blockmax [B, Hkv, ceil(T/4), ceil(T/128)]
+    fp32, -inf where a block holds no valid pair)."""
+    import torch
+    B, T, Hq, Hkv, D, dev = _prefill_checks(q, k, v, sink)
+    out = torch.empty(B, T, Hq, D, dtype=out_dtype or torch.float32, device=dev)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    bm = torch.full((B, Hkv, (T + 3) // 4, (T + 127) // 128), float("-inf"),
+                    dtype=torch.float32, device=dev)
+    st = lib().swa_sink_fwd_scores(q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
+                                   out.data_ptr(), lse.data_ptr(), bm.data_ptr(), B, T, Hq, Hkv,
+                                   D, int(W), _dtype_code(q), _dtype_code(out),
+                                   _stream_handle(stream, dev))
+    _check("swa_sink_fwd_scores", st)
+    return out, lse, bm
+
+
+def swa_topk_blocks(scores, T: int, QB: int, topk: int, *, stream=None):
+    """Block selection: int32 [B, Hkv, ceil(T/QB), topk], increasing, -1 padded."""
+    import torch
+    B, Hkv = scores.shape[0], scores.shape[1]
+    dev = scores.device
+    _cuda_contig("scores", scores, dev)
+    if scores.dtype != torch.float32 or scores.shape != (B, Hkv, (T + 3) // 4, (T + 127) // 128):
+        raise ValueError("scores must be float32 [B, Hkv, ceil(T/4), ceil(T/128)]")
+    idx = torch.empty(B, Hkv, (T + QB - 1) // QB, topk, dtype=torch.int32, device=dev)
+    st = lib().swa_topk_blocks(scores.data_ptr(), idx.data_ptr(), B, int(T), Hkv, int(QB),
+                               int(topk), _stream_handle(stream, dev))
+    _check("swa_topk_blocks", st)
+    return idx
+
+
+def swa_sink_sparse_fwd(q, k, v, sink, idx, QB: int, *, out_dtype=None, stream=None):
+    """A sparse layer: causal attention over the key blocks idx selects per
+    query block of QB positions.  Returns (out, lse)."""
+    import torch
+    B, T, Hq, Hkv, D, dev = _prefill_checks(q, k, v, sink)
+    _cuda_contig("idx", idx, dev)
+    if idx.dtype != torch.int32 or idx.dim() != 4 or idx.shape[:3] != (B, Hkv, (T + QB - 1) // QB):
+        raise ValueError("idx must be int32 [B, Hkv, ceil(T/QB), topk]")
+    out = torch.empty(B, T, Hq, D, dtype=out_dtype or torch.float32, device=dev)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    st = lib().swa_sink_sparse_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
+                                   idx.data_ptr(), out.data_ptr(), lse.data_ptr(), B, T, Hq, Hkv,
+                                   D, int(QB), int(idx.shape[3]), _dtype_code(q),
+                                   _dtype_code(out), _stream_handle(stream, dev))
+    _check("swa_sink_sparse_fwd", st)
+    return out, lse
 
 
 def swa_ring_append(k_new, v_new, k_ring, v_ring, pos, *, stream=None):

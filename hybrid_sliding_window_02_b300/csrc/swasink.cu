@@ -19,6 +19,7 @@
 #include "simt_fwd.cuh"
 #include "tc_global.cuh"
 #include "tc_swa.cuh"
+#include "topk.cuh"
 #include "verify.cuh"
 #include "verify_tc.cuh"
 
@@ -40,7 +41,8 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   bool tc_attr[2] = {false, false};   // [bf16 output]
-  bool tcg_attr[2] = {false, false};
+  bool tcg_attr[2][2] = {{false, false}, {false, false}};   // [bf16 output][scores]
+  bool topk_attr = false;
   bool dectc_attr = false;
   bool vertc_attr = false;
   bool decode_attr[2][2][5] = {};
@@ -220,23 +222,30 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
   return check_launch("swa_fwd_tc_kernel");
 }
 
+// blockmax: optional block-score output; blk_idx: optional block list (sparse
+// mode, query blocks of qb_size positions, topk entries each).
 swa_status launch_tc_global(const void* q, const void* k, const void* v, const float* sink,
                             void* out, float* lse, int B, int T, int Hq, int Hkv, int W,
-                            bool bf16_out, cudaStream_t st) {
+                            bool bf16_out, cudaStream_t st, float* blockmax = nullptr,
+                            const int* blk_idx = nullptr, int qb_size = 0, int topk = 0) {
   using namespace swa::tcglobal;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
-  auto kern = bf16_out ? swa_fwd_tc_global_kernel<true> : swa_fwd_tc_global_kernel<false>;
+  const bool scores = blockmax != nullptr;
+  auto kern = bf16_out ? (scores ? swa_fwd_tc_global_kernel<true, true>
+                                 : swa_fwd_tc_global_kernel<true, false>)
+                       : (scores ? swa_fwd_tc_global_kernel<false, true>
+                                 : swa_fwd_tc_global_kernel<false, false>);
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].tcg_attr[bf16_out]) {
+    if (!g_dev[dev].tcg_attr[bf16_out][scores]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_global_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].tcg_attr[bf16_out] = true;
+      g_dev[dev].tcg_attr[bf16_out][scores] = true;
     }
   }
   const long long nitem_seq = (T + kItemPos - 1) / kItemPos;
@@ -262,6 +271,13 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
   p.nitem_seq = (int)nitem_seq;
   p.total_items = (int)total;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  p.blockmax = blockmax;
+  p.nqg = (T + 3) / 4;
+  p.nkb = (T + kBlk - 1) / kBlk;
+  p.blk_idx = blk_idx;
+  p.qb_size = qb_size > 0 ? qb_size : kItemPos;
+  p.topk = topk;
+  p.nqb = (T + p.qb_size - 1) / p.qb_size;
   const long long grid = total < sms ? total : sms;
   kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
   return check_launch("swa_fwd_tc_global_kernel");
@@ -622,6 +638,84 @@ swa_status swa_rope_append(const void* q_in, const void* k_in, const void* v_in,
         static_cast<__nv_bfloat16*>(k_ring), static_cast<__nv_bfloat16*>(v_ring), pos, Hq, Hkv,
         D, W, rot_dim / 2, l2t);
   return check_launch("rope_append_kernel");
+}
+
+swa_status swa_sink_fwd_scores(const void* q, const void* k, const void* v, const float* sink,
+                               void* out, float* lse, float* blockmax, int B, int T, int Hq,
+                               int Hkv, int D, int W, swa_dtype in_dtype, swa_dtype out_dtype,
+                               void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k || !v || !sink || !out || !blockmax) return SWA_EINVAL;
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return SWA_EINVAL;
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
+  if (out_dtype != SWA_F32 && out_dtype != SWA_BF16) return SWA_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(blockmax) & 3u))
+    return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  if (!(in_dtype == SWA_BF16 && D == swa::tcglobal::kD && Hq == Hkv * swa::tcglobal::kG)) {
+    set_error_text("block scores come from the tensor-core global kernel (bf16, D 128, 8 heads per kv head)");
+    return SWA_EUNSUPPORTED;
+  }
+  return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, out_dtype == SWA_BF16,
+                          static_cast<cudaStream_t>(stream), blockmax);
+}
+
+swa_status swa_topk_blocks(const float* scores, int* idx, int B, int T, int Hkv, int QB,
+                           int topk, void* stream) {
+  g_last_error[0] = '\0';
+  if (!scores || !idx) return SWA_EINVAL;
+  if (B < 1 || T < 1 || Hkv < 1 || QB < 4 || QB % 4 || 128 % QB || topk < 1) return SWA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(scores) & 3u) || (reinterpret_cast<uintptr_t>(idx) & 3u))
+    return SWA_EINVAL;
+  const long long nkb = (T + 127LL) / 128;
+  if (nkb > swa::kTopkMaxBlocks || topk > swa::kTopkMax) return SWA_EUNSUPPORTED;
+  const long long units = (long long)B * Hkv * ((T + QB - 1LL) / QB);
+  const long long blocks = (units + swa::kTopkWarps - 1) / swa::kTopkWarps;
+  if (blocks > 0x7fffffffLL) return SWA_EUNSUPPORTED;
+  const size_t smem = (size_t)swa::kTopkWarps * (nkb * 4 + ((nkb + 31) / 32) * 4);
+  int dev;
+  if (!current_device(&dev)) return SWA_ECUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev[dev].topk_attr) {
+      const int most = swa::kTopkWarps * (swa::kTopkMaxBlocks * 4 + swa::kTopkMaxBlocks / 8);
+      cudaError_t e = cudaFuncSetAttribute(swa::topk_blocks_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+      if (e != cudaSuccess) {
+        set_cuda_error("cudaFuncSetAttribute(topk_blocks_kernel)", e);
+        return SWA_ECUDA;
+      }
+      g_dev[dev].topk_attr = true;
+    }
+  }
+  swa::topk_blocks_kernel<<<(unsigned)blocks, swa::kTopkWarps * 32, smem,
+                            static_cast<cudaStream_t>(stream)>>>(scores, idx, B, T, Hkv, QB,
+                                                                 topk);
+  return check_launch("topk_blocks_kernel");
+}
+
+swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, const float* sink,
+                               const int* idx, void* out, float* lse, int B, int T, int Hq,
+                               int Hkv, int D, int QB, int topk, swa_dtype in_dtype,
+                               swa_dtype out_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q || !k || !v || !sink || !idx || !out) return SWA_EINVAL;
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv || topk < 1) return SWA_EINVAL;
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
+  if (out_dtype != SWA_F32 && out_dtype != SWA_BF16) return SWA_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(idx) & 3u))
+    return SWA_EINVAL;
+  if (QB != 32 && QB != 64 && QB != 128) return SWA_EUNSUPPORTED;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  if (!(in_dtype == SWA_BF16 && D == swa::tcglobal::kD && Hq == Hkv * swa::tcglobal::kG)) {
+    set_error_text("sparse attention runs on the tensor-core global kernel (bf16, D 128, 8 heads per kv head)");
+    return SWA_EUNSUPPORTED;
+  }
+  // causal over the selected blocks: no window lower bound
+  return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, T, out_dtype == SWA_BF16,
+                          static_cast<cudaStream_t>(stream), nullptr, idx, QB, topk);
 }
 
 const char* swa_sink_verify_path(int B, int L, int Hq, int Hkv, int D, int W, swa_dtype in_dtype) {

@@ -89,11 +89,22 @@ struct Params {
   int nitem_seq;      // ceil(T / 32)
   int total_items;    // B * Hkv * nitem_seq (< 2^31, checked on the host)
   float scale_log2;   // log2(e) / sqrt(D)
+  // block scores (optional): blockmax[b][kvh][ceil(T/4)][ceil(T/128)], the max
+  // scaled logit of each (4-position group, 128-key block) over the group's
+  // 8 heads; written for the blocks an item visits
+  float* blockmax;
+  int nqg, nkb;
+  // sparse mode (optional): the item visits the key blocks listed in
+  // blk_idx[b][kvh][p0 / qb_size][0 .. topk) (increasing, -1 padded) instead
+  // of every block of its window
+  const int* blk_idx;
+  int qb_size, topk, nqb;
 };
 
 struct Item {
   int b, kvh, p0;     // first position of tile 0
-  int jlo, nb;        // key blocks jlo .. jlo + nb - 1
+  int jlo, nb;        // key blocks jlo .. jlo + nb - 1, or blocks[0 .. nb)
+  const int* blocks;  // sparse mode: the item's block list
 };
 
 // u-th item in order of decreasing causal length.
@@ -106,6 +117,15 @@ __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
   it.b = (int)(bk / (uint32_t)p.Hkv);
   it.kvh = (int)(bk - (uint32_t)it.b * (uint32_t)p.Hkv);
   it.p0 = n2 * kItemPos;
+  if (p.blk_idx != nullptr) {
+    it.blocks = p.blk_idx + (((int64_t)it.b * p.Hkv + it.kvh) * p.nqb + it.p0 / p.qb_size) * p.topk;
+    int nb = 0;
+    while (nb < p.topk && __ldg(it.blocks + nb) >= 0) ++nb;
+    it.jlo = 0;
+    it.nb = nb;
+    return it;
+  }
+  it.blocks = nullptr;
   const int last = min(it.p0 + kItemPos - 1, p.T - 1);
   const int first_key = max(0, it.p0 - p.W + 1);
   it.jlo = first_key / kBlk;
@@ -115,6 +135,11 @@ __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
 
 // The k-th item of CTA c: rounds of gridDim.x items, dealt in alternating
 // direction.  Returns false past the end.
+// key block of step t of an item
+__device__ __forceinline__ int item_block(const Item& it, int t) {
+  return it.blocks != nullptr ? __ldg(it.blocks + t) : it.jlo + t;
+}
+
 __device__ __forceinline__ bool cta_item(int k, const Params& p, Item& it) {
   const uint32_t g = gridDim.x;
   const uint32_t idx = (k & 1) ? (g - 1 - blockIdx.x) : blockIdx.x;
@@ -137,7 +162,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-template <bool kBf16Out>
+template <bool kBf16Out, bool kScores>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_global_kernel(const __grid_constant__ CUtensorMap map_q,
                              const __grid_constant__ CUtensorMap map_k,
@@ -209,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const CUtensorMap* map = (t & 1) ? &map_v : &map_k;
-          const int key = (it.jlo + (t >> 1)) * kBlk;
+          const int key = item_block(it, t >> 1) * kBlk;
           const uint32_t dst = sbase + kOffKV + slot * kSlotBytes;
           const uint32_t fb = bar(kBarKvFull + slot);
           mbar_arrive_expect_tx(fb, kSlotBytes);
@@ -324,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key_lo = max(0, pos - p.W + 1);
       bool ok = true;
       for (int t = 0; t < it.nb; ++t, ++npv) {
-        const int key0 = (it.jlo + t) * kBlk;
+        const int kblk = item_block(it, t);
+        const int key0 = kblk * kBlk;
         const int c_lo = key_lo - key0, c_hi = pos - key0;
         if (!mbar_wait(bar(kBarSFull + ti), npv & 1, kErrWaitSFull, abort_flag)) {
           ok = false;
@@ -356,6 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mraw = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
                                  fmaxf(m8[6], m8[7]));
         const float m_cand = mraw * p.scale_log2;  // scale > 0 commutes with max
+        if constexpr (kScores) {
+          // block score of this warp's 4 positions x 8 heads (rows past T excluded)
+          float bm = pos < p.T ? mraw : -INFINITY;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+          const int qg = (it.p0 + ti * kNpos + quad * 4) >> 2;
+          if (lane == 0 && qg < p.nqg)
+            p.blockmax[(((int64_t)it.b * p.Hkv + it.kvh) * p.nqg + qg) * p.nkb + kblk] =
+                bm * (p.scale_log2 * 0.6931471805599453f);
+        }
         const bool grow = m_cand > m_run + kRescaleLog2;  // false for -inf
         float f = 1.f;                                    // factor for O and l
         if (grow) {

@@ -170,6 +170,57 @@ swa_status swa_rope_append(const void* q_in, const void* k_in, const void* v_in,
                            int Hkv, int D, int W, int rot_dim, double theta, swa_dtype dtype,
                            void* stream);
 
+/*
+ * High Sparse ("MiMo-V2.5" ICML 2026 talk write-up, section 02): the
+ * full-attention layers' block-level scores are reused to choose the tokens
+ * the sparse layers attend to, the sparse layers share the full layer's KV
+ * cache, and selection is by block with a configurable capacity.  The page
+ * gives no formula; the three calls below follow the readings stated with
+ * each.
+ *
+ * swa_sink_fwd_scores -- swa_sink_fwd_ex on the tensor-core global kernel
+ * (bf16 inputs, D = 128, Hq = 8 Hkv, any W; W >= T is the full-attention
+ * layer) that also writes the block scores:
+ *   blockmax [B, Hkv, ceil(T/4), ceil(T/128)] float32:
+ *     blockmax[b,g,c,n] = max of q_i.k_j / sqrt(D) over query positions
+ *     i in [4c, 4c+4), the 8 query heads of kv head g, keys j in
+ *     [128n, 128n+128) with j in row i's window.
+ *   Entries of blocks with no such pair are not written: initialise the
+ *   buffer to -inf.  Other shapes return SWA_EUNSUPPORTED.
+ */
+swa_status swa_sink_fwd_scores(const void* q, const void* k, const void* v, const float* sink,
+                               void* out, float* lse, float* blockmax, int B, int T, int Hq,
+                               int Hkv, int D, int W, swa_dtype in_dtype, swa_dtype out_dtype,
+                               void* stream);
+
+/*
+ * swa_topk_blocks -- block selection from those scores.  For each kv head and
+ * query block of QB positions (QB a multiple of 4 dividing 128): the key block
+ * holding the query block's last position (the causal diagonal), then the
+ * topk - 1 earlier key blocks with the highest score (a block's score is the
+ * max over the query block's 4-position groups; ties go to the smaller index).
+ *   scores [B, Hkv, ceil(T/4), ceil(T/128)] float32
+ *   idx    [B, Hkv, ceil(T/QB), topk] int32 (written): increasing, -1 padded
+ *   Requires 1 <= topk <= 64 and ceil(T/128) <= 4096.
+ */
+swa_status swa_topk_blocks(const float* scores, int* idx, int B, int T, int Hkv, int QB,
+                           int topk, void* stream);
+
+/*
+ * swa_sink_sparse_fwd -- a sparse layer: causal attention of query i over
+ * the keys j <= i of the key blocks selected for its query block, sink bias in
+ * the denominator as in swa_sink_fwd.  k and v are the full-attention layer's
+ * (the shared KV cache).
+ *   idx [B, Hkv, ceil(T/QB), topk] int32: increasing block indices, -1 padded
+ *   (as swa_topk_blocks writes them); QB in {32, 64, 128}.
+ *   Other arguments as swa_sink_fwd_ex; bf16 inputs, D = 128, Hq = 8 Hkv only
+ *   (else SWA_EUNSUPPORTED).
+ */
+swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, const float* sink,
+                               const int* idx, void* out, float* lse, int B, int T, int Hq,
+                               int Hkv, int D, int QB, int topk, swa_dtype in_dtype,
+                               swa_dtype out_dtype, void* stream);
+
 /* Name of the prefill kernel swa_sink_fwd would launch for these sizes
  * ("tc_swa", "tc_global", "simt"), or "invalid". */
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);

@@ -182,3 +182,16 @@ def test_fwd_ex_rejects_before_launch(L):
     assert L.swa_sink_fwd_ex(*ok, 7, None) == -1          # unknown output dtype
     assert L.swa_sink_fwd_ex(*ok[:4], None, *ok[5:], 1, None) == -1
     assert L.swa_sink_fwd_ex(*ok[:4], A + 8, *ok[5:], 1, None) == -1
+
+
+def test_high_sparse_calls_reject_before_launch(L):
+    # scores: null blockmax; topk: bad query block, capacity; sparse: bad QB
+    assert L.swa_sink_fwd_scores(A, A, A, A, A, A, None, 1, 256, 8, 1, 128, 256, 1, 0, None) == -1
+    assert L.swa_sink_fwd_scores(A, A, A, A, A, A, A, 1, 256, 4, 1, 128, 256, 1, 0, None) == -2
+    assert L.swa_topk_blocks(A, A, 1, 1024, 2, 6, 4, None) == -1
+    assert L.swa_topk_blocks(A, A, 1, 1024, 2, 256, 4, None) == -1
+    assert L.swa_topk_blocks(A, A, 1, 1024, 2, 64, 0, None) == -1
+    assert L.swa_topk_blocks(A, A, 1, 1024, 2, 64, 65, None) == -2
+    assert L.swa_sink_sparse_fwd(A, A, A, A, A, A, A, 1, 1024, 8, 1, 128, 16, 4, 1, 0, None) == -2
+    assert L.swa_sink_sparse_fwd(A, A, A, A, None, A, A, 1, 1024, 8, 1, 128, 64, 4, 1, 0,
+                                 None) == -1

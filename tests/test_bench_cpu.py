@@ -14,7 +14,8 @@ import bench  # noqa: E402
 def test_bench_helpers_exist():
     for name in ("time_prefill", "time_decode", "time_verify", "time_graph", "time_hybrid",
                  "hybrid_line", "verify_line", "bf16_out_line", "time_e2e", "prefill_roofline",
-                 "cpu_oracle_sample", "run_reference", "run_ours", "recorded_traffic"):
+                 "cpu_oracle_sample", "run_reference", "run_ours", "recorded_traffic",
+                 "high_sparse_line", "_event_ms"):
         assert callable(getattr(bench, name)), name
 
 

@@ -1,0 +1,93 @@
+"""High Sparse on the GPU: block scores from the global kernel, block
+selection, and attention over the selected blocks, against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import hybrid_sliding_window_02_b300 as swa
+from hybrid_sliding_window_02_b300 import inputs as gen
+from gpu_helpers import assert_bf16_close, assert_lse_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", [(1, 300, 8, 1, 300), (2, 1000, 16, 2, 1000),
+                                          (1, 700, 8, 1, 200), (1, 130, 8, 1, 130)])
+def test_block_scores_match_oracle(cuda_ok, B, T, Hq, Hkv, W):
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4000 + T + W)
+    q, k, v, s = (t.cuda() for t in (x.q, x.k, x.v, x.sink))
+    out, lse, bm = swa.swa_sink_fwd_scores(q, k, v, s, W)
+    o2, l2 = swa.swa_sink_fwd(q, k, v, s, W)
+    torch.cuda.synchronize()
+    if W > 129:      # same kernel with and without scores: same results
+        assert torch.equal(out, o2) and torch.equal(lse, l2)
+    ref = oracle.block_max(x.q, x.k, W)
+    got = bm.cpu().double().numpy()
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+    fin = np.isfinite(ref)
+    assert np.abs(got[fin] - ref[fin]).max() <= 1e-3
+
+
+@pytest.mark.parametrize("T,QB,topk", [(1000, 64, 3), (4096, 128, 8), (700, 32, 1),
+                                       (3000, 4, 9), (32768, 64, 16)])
+def test_topk_matches_oracle_bit_exact(cuda_ok, T, QB, topk):
+    g = np.random.default_rng(T + QB + topk)
+    nqg, nkb = (T + 3) // 4, (T + 127) // 128
+    sc = g.normal(size=(2, 3, nqg, nkb)).astype(np.float32)
+    sc[..., 3] = sc[..., 5]                         # ties
+    sc[0, 0, :, 2] = -np.inf                        # a block with no valid pair
+    idx = swa.swa_topk_blocks(torch.from_numpy(sc).cuda(), T, QB, topk)
+    torch.cuda.synchronize()
+    ref = oracle.topk_blocks(sc, T, QB, topk)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
+def _selection(B, Hkv, T, QB, topk, seed):
+    g = np.random.default_rng(seed)
+    sc = g.normal(size=(B, Hkv, (T + 3) // 4, (T + 127) // 128)).astype(np.float32)
+    return oracle.topk_blocks(sc, T, QB, topk)
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,QB,topk", [(1, 600, 8, 1, 64, 2), (2, 1000, 16, 2, 32, 3),
+                                                (1, 1500, 8, 1, 128, 4)])
+def test_sparse_matches_oracle(cuda_ok, B, T, Hq, Hkv, QB, topk):
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4100 + T)
+    idx = _selection(B, Hkv, T, QB, topk, seed=T)
+    q, k, v, s = (t.cuda() for t in (x.q, x.k, x.v, x.sink))
+    out, lse = swa.swa_sink_sparse_fwd(q, k, v, s, torch.from_numpy(idx).cuda(), QB)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.sparse_fwd(x.q, x.k, x.v, x.sink, idx, QB)
+    assert_bf16_close(out.cpu().numpy(), o_ref)
+    assert_lse_close(lse.cpu().numpy(), l_ref)
+
+
+def test_sparse_with_every_block_is_the_global_kernel(cuda_ok):
+    B, T, Hq, Hkv, QB = 1, 1100, 16, 2, 64
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4200, device="cuda")
+    nkb = (T + 127) // 128
+    idx = torch.arange(nkb, dtype=torch.int32, device="cuda").expand(
+        B, Hkv, (T + QB - 1) // QB, nkb).contiguous()
+    o_s, l_s = swa.swa_sink_sparse_fwd(x.q, x.k, x.v, x.sink, idx, QB)
+    o_g, l_g = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, T)
+    torch.cuda.synchronize()
+    assert torch.equal(o_s, o_g) and torch.equal(l_s, l_g)
+
+
+def test_scores_select_sparse_pipeline(cuda_ok):
+    # global layer -> block scores -> selection -> sparse layer on the shared
+    # K/V: the selection agrees with the oracle's from the same fp32 scores,
+    # the sparse layer with the oracle given that selection
+    B, T, Hq, Hkv, QB, topk = 1, 2048, 16, 2, 64, 4
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4300, device="cuda")
+    _, _, bm = swa.swa_sink_fwd_scores(x.q, x.k, x.v, x.sink, T)
+    idx = swa.swa_topk_blocks(bm, T, QB, topk)
+    q2 = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4301, device="cuda").q   # next layer's queries
+    out, lse = swa.swa_sink_sparse_fwd(q2, x.k, x.v, x.sink, idx, QB)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), oracle.topk_blocks(bm.cpu().numpy(), T, QB, topk))
+    o_ref, l_ref = oracle.sparse_fwd(q2.cpu(), x.k.cpu(), x.v.cpu(), x.sink.cpu(),
+                                     idx.cpu().numpy(), QB)
+    assert_bf16_close(out.cpu().numpy(), o_ref)
+    assert_lse_close(lse.cpu().numpy(), l_ref)
+    assert swa.device_error() == 0
