@@ -22,25 +22,27 @@
 // Roles (320 threads):
 //   warp 8      TMA producer: the two Q tiles of an item, then K_j and V_j for
 //               every key block j into a ring of 32 KB slots
-//   warp 9      TMEM owner + single-thread tcgen05.mma issuer; per block j:
-//                 S_i = Q_i K_j^T  (SS, M = 128, N = 128, K = 128)   i = 0, 1
-//                 O_i += P_i V_j   (TS, P from TMEM, V MN-major, N = 128)
+//   warp 9      TMEM owner + single-thread tcgen05.mma issuer
+//                 S   = Q_i K_j^T  (SS, M = 128, N = 128, K = 128)
+//                 O_i += P_i V_j   (TS, P_i from TMEM, V MN-major, N = 128)
 //   warps 0..3  softmax of tile 0, warps 4..7 softmax of tile 1: thread =
-//               row; S -> mask -> running max / sum -> bf16 P written over S
-//               in TMEM; after the last block O / l -> out and the lse.
-// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i takes the
-// first 64 columns of S_i (bf16 pairs).  Because S_i(j+1) overwrites P_i(j),
-// it is issued only once O_i += P_i(j) V_j has completed (an MMA to another
-// accumulator is not ordered after it), so the order per block is
-// S0 S1 PV0 PV1 with the other tile's MMA in flight during every wait.
+//               row; S -> mask -> running max / sum -> bf16 P_i in TMEM;
+//               after the last block O / l -> out and the lse.
+// TMEM: S [0,128) shared by the two tiles, P0 [128,192), P1 [192,256) (bf16
+// pairs), O0 [256,384), O1 [384,512).  Per key block n the MMA order is
+//     S0(n)  PV1(n-1)  S1(n)  PV0(n)
+// S goes to one buffer that each softmax empties into registers at once, so
+// an S waits only for the other tile's read of the previous one (covered by
+// the PV between them), and P never shares columns with S: each tile's
+// softmax has two MMAs of the other tile (PV then S) to hide behind before its
+// own PV is due.  A softmax rewrites P_i (and rescales O_i) only after the
+// tile's previous PV has completed, which it learns from a commit barrier.
 //
 // Rescaling: the running max m only moves when a block's max exceeds it by
 // more than 8 (log2 units).  Otherwise p = 2^(x - m) <= 256 and the stale m
 // is kept; the final O / l is the same quotient.  When a row's max does move
-// after block 0, its warp rescales O in TMEM (read, multiply, write) before
-// releasing P: at that point every earlier PV of the tile has completed (the
-// S that the softmax just read was issued after it) and the next is not issued
-// until P is released.
+// after the item's first block, its warp rescales O_i in TMEM (read,
+// multiply, write) before releasing P_i.
 #pragma once
 
 #include "device_common.cuh"
@@ -56,7 +58,7 @@ constexpr int kNpos = 16;               // positions per Q tile
 constexpr int kTiles = 2;               // Q tiles per work item
 constexpr int kItemPos = kNpos * kTiles;
 constexpr int kBlk = 128;               // keys per block
-constexpr uint32_t kSlots = 4;          // K/V ring slots (one K or V block each)
+constexpr uint32_t kSlots = 5;          // K/V ring slots (one K or V block each)
 constexpr float kRescaleLog2 = 8.0f;    // move the running max only past this
 
 // shared memory (bytes); swizzled operands 1024-aligned
@@ -69,16 +71,17 @@ constexpr int kOffKV = kOffQ + kTiles * kQTile;
 constexpr int kOffBar = kOffKV + (int)kSlots * kSlotBytes;
 constexpr int kBarQFull = 0, kBarQEmpty = kBarQFull + kTiles, kBarKvFull = kBarQEmpty + kTiles,
               kBarKvEmpty = kBarKvFull + kSlots, kBarSFull = kBarKvEmpty + kSlots,
-              kBarPFull = kBarSFull + kTiles, kBarPvDone = kBarPFull + kTiles,
-              kBarOFull = kBarPvDone + kTiles, kBarDrain = kBarOFull + kTiles,
-              kNumBars = kBarDrain + 1;
+              kBarSFree = kBarSFull + kTiles, kBarPFull = kBarSFree + 1,
+              kBarPvDone = kBarPFull + kTiles, kBarOFull = kBarPvDone + kTiles,
+              kBarDrain = kBarOFull + kTiles, kNumBars = kBarDrain + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;  // + slack for 1024 alignment
 
 constexpr uint32_t kTmemCols = 512;
-// TMEM column of S_i / P_i and of O_i
-__host__ __device__ constexpr uint32_t col_s(int i) { return 128u * (uint32_t)i; }
+constexpr uint32_t kColS = 0;
+// TMEM column of P_i and of O_i
+__host__ __device__ constexpr uint32_t col_p(int i) { return 128u + 64u * (uint32_t)i; }
 __host__ __device__ constexpr uint32_t col_o(int i) { return 256u + 128u * (uint32_t)i; }
 
 struct Params {
@@ -108,6 +111,7 @@ struct Item {
 };
 
 // u-th item in order of decreasing causal length.
+// u-th item in order of decreasing causal length.
 __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
   Item it;
   const uint32_t bkn = (uint32_t)(p.B * p.Hkv);
@@ -133,13 +137,13 @@ __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
   return it;
 }
 
-// The k-th item of CTA c: rounds of gridDim.x items, dealt in alternating
-// direction.  Returns false past the end.
 // key block of step t of an item
 __device__ __forceinline__ int item_block(const Item& it, int t) {
   return it.blocks != nullptr ? __ldg(it.blocks + t) : it.jlo + t;
 }
 
+// The k-th item of CTA c: rounds of gridDim.x items, dealt in alternating
+// direction.  Returns false past the end.
 __device__ __forceinline__ bool cta_item(int k, const Params& p, Item& it) {
   const uint32_t g = gridDim.x;
   const uint32_t idx = (k & 1) ? (g - 1 - blockIdx.x) : blockIdx.x;
@@ -185,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPvDone + i), 1);
       mbar_init(bar(kBarOFull + i), 1);
     }
+    mbar_init(bar(kBarSFree), 128);
     for (uint32_t s = 0; s < kSlots; ++s) {
       mbar_init(bar(kBarKvFull + s), 1);
       mbar_init(bar(kBarKvEmpty + s), 1);
@@ -260,69 +265,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qdesc0 = umma_sdesc(sbase + kOffQ, 16, 1024, 2);
       const uint64_t kdesc0 = umma_sdesc(sbase + kOffKV, 16, 1024, 2);
       const uint64_t vdesc0 = umma_sdesc(sbase + kOffKV, kSlotHalf, 1024, 2);
-      uint32_t seq = 0;
-      uint32_t npv = 0;  // PV groups issued per tile (identical for both tiles)
+      uint32_t seq = 0;       // K/V loads consumed (K and V alternate)
+      uint32_t ns = 0;        // S products issued (S0 and S1 alternate)
+      uint32_t nblk = 0;      // key blocks whose PV0 has been issued
       bool ok = true;
+      // the block whose PV1 is still to be issued
+      bool pend = false, pend_first = false, pend_last = false;
+      uint32_t pend_vs = 0;
+
+      auto wait_kv = [&](uint32_t& slot) -> bool {
+        slot = seq % kSlots;
+        const bool r = mbar_wait(bar(kBarKvFull + slot), (seq / kSlots) & 1, kErrWaitKvFull,
+                                 abort_flag);
+        ++seq;
+        return r;
+      };
+      // S = Q_i K^T into the shared buffer, once the other tile's softmax has
+      // read the previous S out of it
+      auto issue_s = [&](int i, uint32_t ks) -> bool {
+        if (ns > 0 && !mbar_wait(bar(kBarSFree), (ns - 1) & 1, kErrWaitSFree, abort_flag))
+          return false;
+        tc_fence_after();
+        const uint64_t qd = qdesc0 + (uint32_t)(i * kQTile >> 4);
+        const uint64_t kd = kdesc0 + (ks * kSlotBytes >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+          const uint32_t b_off = ((kk >> 2) * kSlotHalf + (kk & 3) * 32) >> 4;
+          umma_bf16_ss(tmem + kColS, qd + a_off, kd + b_off, idesc_s, kk > 0);
+        }
+        umma_commit(bar(kBarSFull + i));
+        ++ns;
+        return true;
+      };
+      // O_i += P_i V for block b (its P_i is released as block number blk)
+      auto issue_pv = [&](int i, uint32_t vs, uint32_t blk, bool first, bool last) -> bool {
+        if (!mbar_wait(bar(kBarPFull + i), blk & 1, kErrWaitPFull, abort_flag)) return false;
+        tc_fence_after();
+        const uint64_t vd = vdesc0 + (vs * kSlotBytes >> 4);
+#pragma unroll
+        for (int kb = 0; kb < kBlk / 16; ++kb)
+          umma_bf16_ts(tmem + col_o(i), tmem + col_p(i) + kb * 8,
+                       vd + (uint32_t)(kb * 16 * 128 >> 4), idesc_o, (!first || kb > 0));
+        umma_commit(bar(kBarPvDone + i));
+        if (last) umma_commit(bar(kBarOFull + i));
+        return true;
+      };
+
       Item it;
       for (int k = 0; ok && cta_item(k, p, it); ++k) {
-        for (int i = 0; i < kTiles && ok; ++i)
-          ok = mbar_wait(bar(kBarQFull + i), k & 1, kErrWaitQFull, abort_flag);
-        for (int t = 0; ok && t < it.nb; ++t) {
-          // ---- S_i = Q_i K^T ----
-          const uint32_t ks = seq % kSlots;
-          if (!mbar_wait(bar(kBarKvFull + ks), (seq / kSlots) & 1, kErrWaitKvFull, abort_flag)) {
+        for (int t = 0; t < it.nb; ++t) {
+          uint32_t ks, vs;
+          // ---- S0(n) ----
+          if (!wait_kv(ks)) { ok = false; break; }
+          if (t == 0 && !mbar_wait(bar(kBarQFull + 0), k & 1, kErrWaitQFull, abort_flag)) {
             ok = false;
             break;
           }
-          ++seq;
-          for (int i = 0; i < kTiles; ++i) {
-            // S_i overwrites P_i of the previous block: its PV must be done
-            if (npv > 0 &&
-                !mbar_wait(bar(kBarPvDone + i), (npv - 1) & 1, kErrWaitPvDone, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t qd = qdesc0 + (uint32_t)(i * kQTile >> 4);
-            const uint64_t kd = kdesc0 + (ks * kSlotBytes >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
-              const uint32_t b_off = ((kk >> 2) * kSlotHalf + (kk & 3) * 32) >> 4;
-              umma_bf16_ss(tmem + col_s(i), qd + a_off, kd + b_off, idesc_s, kk > 0);
-            }
-            umma_commit(bar(kBarSFull + i));
+          if (!issue_s(0, ks)) { ok = false; break; }
+          // ---- PV1(n-1) ----
+          if (pend) {
+            if (!issue_pv(1, pend_vs, nblk - 1, pend_first, pend_last)) { ok = false; break; }
+            umma_commit(bar(kBarKvEmpty + pend_vs));
+            pend = false;
           }
-          if (!ok) break;
+          // ---- S1(n) ----
+          if (t == 0 && !mbar_wait(bar(kBarQFull + 1), k & 1, kErrWaitQFull, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (!issue_s(1, ks)) { ok = false; break; }
           umma_commit(bar(kBarKvEmpty + ks));
           if (t == it.nb - 1)
             for (int i = 0; i < kTiles; ++i) umma_commit(bar(kBarQEmpty + i));
-          // ---- O_i += P_i V ----
-          const uint32_t vs = seq % kSlots;
-          if (!mbar_wait(bar(kBarKvFull + vs), (seq / kSlots) & 1, kErrWaitKvFull, abort_flag)) {
-            ok = false;
-            break;
-          }
-          ++seq;
-          for (int i = 0; i < kTiles; ++i) {
-            if (!mbar_wait(bar(kBarPFull + i), npv & 1, kErrWaitPFull, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t vd = vdesc0 + (vs * kSlotBytes >> 4);
-#pragma unroll
-            for (int kb = 0; kb < kBlk / 16; ++kb)
-              umma_bf16_ts(tmem + col_o(i), tmem + col_s(i) + kb * 8,
-                           vd + (uint32_t)(kb * 16 * 128 >> 4), idesc_o, (t > 0 || kb > 0));
-            umma_commit(bar(kBarPvDone + i));
-            if (t == it.nb - 1) umma_commit(bar(kBarOFull + i));
-          }
-          if (!ok) break;
-          ++npv;
-          umma_commit(bar(kBarKvEmpty + vs));
+          // ---- PV0(n) ----
+          if (!wait_kv(vs)) { ok = false; break; }
+          if (!issue_pv(0, vs, nblk, t == 0, t == it.nb - 1)) { ok = false; break; }
+          pend = true;
+          pend_vs = vs;
+          pend_first = t == 0;
+          pend_last = t == it.nb - 1;
+          ++nblk;
         }
       }
+      if (ok && pend && issue_pv(1, pend_vs, nblk - 1, pend_first, pend_last))
+        umma_commit(bar(kBarKvEmpty + pend_vs));
       // every MMA issued so far completes before TMEM is released
       umma_commit(bar(kBarDrain));
       mbar_wait_drain(bar(kBarDrain), 0);
@@ -334,7 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;                      // TMEM lanes [32 quad, 32 quad + 32)
     const int r = quad * 32 + lane;                 // tile row
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    const uint32_t s_addr = tmem + lane_addr + col_s(ti);
+    const uint32_t s_addr = tmem + lane_addr + kColS;
+    const uint32_t p_addr = tmem + lane_addr + col_p(ti);
     const uint32_t o_addr = tmem + lane_addr + col_o(ti);
     const int g = r & 7;
     uint32_t npv = 0;
@@ -363,6 +391,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < kBlk / 32; ++c) reg_fence32(sr + c * 32);
+        // S is in registers: the other tile's S may overwrite the buffer
+        tc_fence_before();
+        mbar_arrive(bar(kBarSFree));
+        // P_i and O_i are free once the tile's previous PV has completed (in
+        // this order it ran before the S just read, so the wait is short)
+        if (npv > 0 &&
+            !mbar_wait(bar(kBarPvDone + ti), (npv - 1) & 1, kErrWaitPvDone, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         // mask in place: scores outside [c_lo, c_hi] become -inf
         const bool full = __all_sync(0xffffffffu, c_lo <= 0 && c_hi >= kBlk - 1);
         if (!full) {
@@ -400,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = m_cand;
         }
         const float mb = (m_run == -INFINITY) ? 0.f : m_run;
-        // p = 2^(x - m) -> bf16 pairs over the first 64 columns of S, 16 at a
-        // time; the scale-and-subtract and the running sum go two columns per
+        // p = 2^(x - m) -> bf16 pairs in P_i, 16 columns at a time; the
+        // scale-and-subtract and the running sum go two columns per
         // instruction (f32x2)
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nmb2 = make_float2(-mb, -mb);
@@ -420,14 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             l2[e & 3] = fadd2(l2[e & 3], pp);
             pk[e] = pack_bf16x2(pp.x, pp.y);
           }
-          tmem_st8(s_addr + c * 8, pk);
+          tmem_st8(p_addr + c * 8, pk);
         }
         {
           const float2 a = fadd2(fadd2(l2[0], l2[1]), fadd2(l2[2], l2[3]));
           l += a.x + a.y;
         }
-        // A moved max also rescales O, which holds the earlier blocks complete
-        // (every PV before this block's S has finished); block 0 has no O yet.
+        // A moved max also rescales O, which holds the earlier blocks of the
+        // item complete; the item's first block has no O yet.
         if (t > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
           for (int c = 0; c < kD / 32; ++c) {
