@@ -19,23 +19,34 @@
 // their 9 key blocks, so keys and values live in a ring of 16-key blocks in
 // shared memory and each key/value row is loaded from HBM once per run.
 //
-// Roles (320 threads), all connected by mbarriers:
-//   warp 8      TMA producer: Q tiles (4 stages, to cover the HBM latency seen
+// Roles (448 threads), all connected by mbarriers:
+//   warp 12     TMA producer: Q tiles (4 stages, to cover the HBM latency seen
 //               under full load) and new K/V blocks (12-slot ring)
-//   warp 9      TMEM owner + single-thread tcgen05.mma issuer
+//   warp 13     TMEM owner + single-thread tcgen05.mma issuer
 //                 S = Q K^T   (SS: M=128, N=144 split at the ring wrap, K=128)
 //                 O = P V     (TS: P from TMEM, V MN-major, N=128, K=16/block)
-//   warps 0..3  softmax: S (TMEM) -> mask, sink-seeded max/sum, normalised
-//               bf16 P -> TMEM; lse -> global
-//   warps 4..7  epilogue: O (TMEM, double-buffered) -> global (fp32, or bf16
+//   warps 0..7  softmax, two threads per row: warp w reads TMEM lanes
+//               [32 (w % 4), +32); warps 0..3 take columns [0, 72), warps
+//               4..7 columns [72, 144).  Each half forms 2^(x - m_half) and
+//               the half's log-sum-exp; the two halves swap that one value
+//               through TMEM (columns [232, 236), one per half and tile
+//               parity), combine it with the sink into the row's
+//               log-sum-exp L, and write bf16 P = 2^(x - L) to TMEM; lse ->
+//               global.  Two softmax warps per SM sub-partition hide each
+//               other's latencies; the exponentials stay exact single-pass.
+//   warps 8..11 epilogue: O (TMEM, double-buffered) -> global (fp32, or bf16
 //               rounded from the same fp32 values).  The 16x256b
 //               TMEM read gives each group of 4 threads 32 contiguous bytes of
 //               a row, so every warp store fills 8 whole 32-byte sectors of 8
 //               lines (one position's 8 heads: 4 KB contiguous); this measured
 //               clearly faster than one 32-byte store per thread per row.
-// TMEM: S [0,144), P [160,232) (bf16 pairs), O0 [256,384), O1 [384,512).
+// TMEM: S [0,144), P [160,232) (bf16 pairs), exchange [232,236),
+// O0 [256,384), O1 [384,512).
 // QK^T of tile t+1 runs while softmax works on tile t (S is read out at once),
 // and the epilogue of tile t overlaps softmax and MMAs of tile t+1.
+// 14 warps put 4 on two of the SM's sub-partitions, which caps registers at
+// 128 per thread: a softmax thread holds 72 scores, an epilogue thread 64
+// output values at a time.
 #pragma once
 
 #include "device_common.cuh"
@@ -43,14 +54,16 @@
 namespace swa {
 namespace tcswa {
 
-constexpr int kThreads = 320;
-constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr int kThreads = 448;
+constexpr int kWarpProducer = 12, kWarpMma = 13;
+constexpr int kWarpEpi0 = 8;
 constexpr int kG = 8;            // query heads per tile (one kv group)
 constexpr int kNpos = 16;        // positions per tile
 constexpr int kD = 128;
 constexpr int kBlk = 16;         // keys per ring block
 constexpr int kNB = 9;           // blocks per tile window
 constexpr int kN = kNB * kBlk;   // 144 score columns
+constexpr int kNh = kN / 2;      // 72 columns per softmax half
 constexpr uint32_t kRing = 12;   // ring slots
 constexpr uint32_t kQStages = 4;
 constexpr int kMaxW = (kNB - 1) * kBlk + 1;  // 129
@@ -68,14 +81,15 @@ constexpr int kOffBar = kOffV + 2 * kRingHalf;        // +48 KB
 constexpr int kBarQFull = 0, kBarQEmpty = kQStages, kBarKvFull = 2 * kQStages,
               kBarKvEmpty = kBarKvFull + kRing, kBarSFull = kBarKvEmpty + kRing,
               kBarSFree = kBarSFull + 1, kBarPFull = kBarSFree + 1, kBarPFree = kBarPFull + 1,
-              kBarOFull = kBarPFree + 1, kBarOFree = kBarOFull + 2, kNumBars = kBarOFree + 2;
+              kBarOFull = kBarPFree + 1, kBarOFree = kBarOFull + 2, kBarXchg = kBarOFree + 2,
+              kBarDrain = kBarXchg + 4, kNumBars = kBarDrain + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;      // + slack for 1024 alignment
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColP = 160, kColO0 = 256, kColO1 = 384;
+constexpr uint32_t kColS = 0, kColP = 160, kColX = 232, kColO0 = 256, kColO1 = 384;
 
 struct Params {
   const float* sink;
@@ -129,10 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarOFull + s), 1);
       mbar_init(bar(kBarOFree + s), 128);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(bar(kBarXchg + s), 64);
     mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarSFree), 128);
-    mbar_init(bar(kBarPFull), 128);
+    mbar_init(bar(kBarSFree), 256);
+    mbar_init(bar(kBarPFull), 256);
     mbar_init(bar(kBarPFree), 1);
+    mbar_init(bar(kBarDrain), 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -154,20 +170,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t seq = 0;  // key blocks loaded so far
       int prev_bk = -1;
-      for (int it = 0; it < ntile; ++it) {
+      int q_issued = 0;  // Q tiles loaded so far
+      bool ok = true;
+      for (int it = 0; it < ntile && ok; ++it) {
         int b, kvh, n;
         tile_coords(t_begin + it, p, b, kvh, n);
         const uint32_t qs = (uint32_t)it % kQStages;
         const uint32_t qph = ((uint32_t)it / kQStages) & 1;
-        if (!mbar_wait(bar(kBarQEmpty + qs), qph ^ 1, kErrWaitQEmpty, abort_flag)) break;
+        if (!mbar_wait(bar(kBarQEmpty + qs), qph ^ 1, kErrWaitQEmpty, abort_flag)) {
+          ok = false;
+          break;
+        }
         const uint32_t qdst = sbase + kOffQ + qs * kQStage;
         mbar_arrive_expect_tx(bar(kBarQFull + qs), kQStage);
         tma_load_4d(qdst, &map_q, 0, kvh * kG, n * kNpos, b, bar(kBarQFull + qs));
         tma_load_4d(qdst + kQHalf, &map_q, 64, kvh * kG, n * kNpos, b, bar(kBarQFull + qs));
+        ++q_issued;
         const int bk = b * p.Hkv + kvh;
         const int first_blk = (bk != prev_bk) ? n - (kNB - 1) : n;
         prev_bk = bk;
-        bool ok = true;
         for (int m = first_blk; m <= n; ++m, ++seq) {
           const uint32_t slot = seq % kRing;
           if (!mbar_wait(bar(kBarKvEmpty + slot), ((seq / kRing) & 1) ^ 1, kErrWaitKvEmpty,
@@ -184,7 +205,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(vdst, &map_v, 0, kvh, m * kBlk, b, kb);
           tma_load_4d(vdst + kRingHalf, &map_v, 64, kvh, m * kBlk, b, kb);
         }
-        if (!ok) break;
+      }
+      // Copies still in flight must land before the CTA exits: wait (bounded)
+      // for the last phase armed on every barrier a copy signals.
+      if (!ok) {
+        for (int j = (q_issued > (int)kQStages ? q_issued - (int)kQStages : 0); j < q_issued; ++j)
+          mbar_wait_drain(bar(kBarQFull + (uint32_t)j % kQStages), ((uint32_t)j / kQStages) & 1);
+        for (uint32_t s2 = (seq > kRing ? seq - kRing : 0); s2 < seq; ++s2)
+          mbar_wait_drain(bar(kBarKvFull + s2 % kRing), (s2 / kRing) & 1);
       }
     }
     __syncwarp();
@@ -307,13 +335,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         pending_run_end = run_end;
       }
       if (ok && pending >= 0) issue_pv(pending, pending_ws, true);
+      // every MMA issued so far completes before TMEM is released
+      umma_commit(bar(kBarDrain));
+      mbar_wait_drain(bar(kBarDrain), 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ======================= softmax (warps 0..3) =======================
-    const int r = warp * 32 + lane;           // tile row = TMEM lane
-    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+  } else if (warp < kWarpEpi0) {
+    // ======================= softmax (warps 0..7) =======================
+    const int quad = warp & 3, half = warp >> 2;
+    const int r = quad * 32 + lane;           // tile row = TMEM lane
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const int c0 = half * kNh;                // first score column of this half
     const int pos_in_tile = r >> 3, g = r & 7;
+    const uint32_t xbar = bar(kBarXchg + quad);
     for (int it = 0; it < ntile; ++it) {
       int b, kvh, n;
       tile_coords(t_begin + it, p, b, kvh, n);
@@ -321,54 +355,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sk = p.sink[h] * 1.4426950408889634f;
       const int i = n * kNpos + pos_in_tile;            // query position
       const int key0 = (n - (kNB - 1)) * kBlk;          // key of column 0
-      const int c_lo = max(0, i - p.W + 1) - key0;      // valid columns [c_lo, c_hi]
-      const int c_hi = i - key0;
+      // valid columns [lo, hi] of this half, in half-local indices
+      const int lo = max(0, i - p.W + 1) - key0 - c0;
+      const int hi = i - key0 - c0;
       if (!mbar_wait(bar(kBarSFull), it & 1, kErrWaitSFull, abort_flag)) break;
       tc_fence_after();
-      uint32_t sr[kN];
+      uint32_t sr[kNh];
+      {
+        // half 0: columns 0..71 as 16,16,16,16,8; half 1: 72..143 as 8,16,16,16,16
+        const uint32_t a = tmem + lane_addr + kColS + c0;
+        if (half == 0) {
 #pragma unroll
-      for (int c = 0; c < kNB; ++c)
-        tmem_ld16(tmem + lane_addr + kColS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[c * 16]));
+          for (int c = 0; c < 4; ++c)
+            tmem_ld16(a + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&sr[16 * c]));
+          tmem_ld8(a + 64, &sr[64]);
+        } else {
+          tmem_ld8(a, &sr[0]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_ld16(a + 8 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&sr[8 + 16 * c]));
+        }
+      }
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < kNB; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&sr[c * 16]));
+      for (int c = 0; c < kNh / 8; ++c) reg_fence8(&sr[8 * c]);
       tc_fence_before();
       mbar_arrive(bar(kBarSFree));
 
       // Mask in place.  Columns [16, 128) are inside every row's window whenever
-      // the warp's rows all have c_lo <= 16 and c_hi >= 127 (W = 128, n >= 8):
-      // then only the first and last key blocks need the per-column test.
-      const bool mid_ok = __all_sync(0xffffffffu, c_lo <= 16 && c_hi >= 127);
-      if (mid_ok) {
+      // the warp's rows all have their first valid column <= 16 and their last
+      // >= 127 (W = 128, n >= 8): then only the first key block (half 0) or the
+      // last one (half 1) needs the per-column test.
+      const bool mid_ok = __all_sync(0xffffffffu, lo + c0 <= 16 && hi + c0 >= 127);
+      if (mid_ok && half == 0) {
 #pragma unroll
-        for (int c = 0; c < kN; ++c)
-          if ((c < 16 || c >= 128) && (c < c_lo || c > c_hi)) sr[c] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < 16; ++c)
+          if (c < lo || c > hi) sr[c] = __float_as_uint(-INFINITY);
+      } else if (mid_ok) {
+#pragma unroll
+        for (int c = 128 - kNh; c < kNh; ++c)
+          if (c < lo || c > hi) sr[c] = __float_as_uint(-INFINITY);
       } else {
 #pragma unroll
-        for (int c = 0; c < kN; ++c)
-          if (c < c_lo || c > c_hi) sr[c] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < kNh; ++c)
+          if (c < lo || c > hi) sr[c] = __float_as_uint(-INFINITY);
       }
-      // max over the row: 8 independent chains of 3-input max, then a tree
+      // max over the half row: 8 independent chains of 3-input max, then a tree
       float m8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 8]));
 #pragma unroll
-      for (int c = 16; c < kN; c += 16)
+      for (int c = 16; c + 16 <= kNh; c += 16)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           m8[k] = max3f(m8[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], __uint_as_float(sr[kNh - 8 + k]));
       const float mraw = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
                                fmaxf(m8[6], m8[7]));
-      const float mx = fmaxf(mraw * p.scale_log2, sk);  // scale > 0 commutes with max
-      // p = 2^(x scale - m) in place: scale-and-subtract and the sum two
+      // exponent offset of this half: its max (scale > 0 commutes with max),
+      // or 0 when every column of the half is outside the window
+      const float mh = (mraw == -INFINITY) ? 0.f : mraw * p.scale_log2;
+      // p = 2^(x scale - mh) in place: scale-and-subtract and the sum two
       // columns per instruction (f32x2)
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-      const float2 nm2 = make_float2(-mx, -mx);
+      const float2 nm2 = make_float2(-mh, -mh);
       float l8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) l8[k] = 0.f;
 #pragma unroll
-      for (int c = 0; c < kN; c += 2) {
+      for (int c = 0; c < kNh; c += 2) {
         const float2 xx = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
                                 sc2, nm2);
         const float a = ex2_approx(xx.x), bb = ex2_approx(xx.y);
@@ -377,31 +433,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         l8[c & 7] += a;
         l8[(c + 1) & 7] += bb;
       }
-      float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      if (sk != -INFINITY) l += ex2_approx(sk - mx);
-      const float inv_l = 1.f / l;
-      // normalised bf16 P -> TMEM once the previous tile's PV has consumed it,
-      // packed and stored 16 columns at a time
+      const float lh = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      // log2-sum-exp of this half (-inf when empty), swapped with the other
+      // half of the row through TMEM column kColX + 2 (tile parity) + half
+      const float lse_h = (lh > 0.f) ? mh + __log2f(lh) : -INFINITY;
+      const uint32_t xcol = tmem + lane_addr + kColX + 2 * (it & 1);
+      {
+        const uint32_t v = __float_as_uint(lse_h);
+        tmem_st1(xcol + half, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(xbar);
+      if (!mbar_wait(xbar, it & 1, kErrWaitXchg, abort_flag)) break;
+      tc_fence_after();
+      const float lse_o = __uint_as_float(tmem_ld1(xcol + (half ^ 1)));
+      // row log2-sum-exp with the sink: L = log2(2^lse_h + 2^lse_o + 2^sk)
+      const float mm = fmaxf(fmaxf(lse_h, lse_o), sk);
+      const float L = mm + __log2f(ex2_approx(lse_h - mm) + ex2_approx(lse_o - mm) +
+                                   ex2_approx(sk - mm));
+      // P = 2^(x scale - L) = p 2^(mh - L); an empty half has p = 0
+      const float f = (lh > 0.f) ? ex2_approx(mh - L) : 0.f;
+      // bf16 P -> TMEM once the previous tile's PV has consumed it
       if (!mbar_wait(bar(kBarPFree), (it & 1) ^ 1, kErrWaitPFree, abort_flag)) break;
       tc_fence_after();
+      {
+        // packed columns [36 half, 36 half + 36): half 0 as 8,8,8,8,4;
+        // half 1 as 4,8,8,8,8 (each store aligned to its width)
+        const uint32_t pa = tmem + lane_addr + kColP + half * (kNh / 2);
+        uint32_t pk[kNh / 2];
 #pragma unroll
-      for (int c = 0; c < kNB; ++c) {
-        uint32_t pk[8];
+        for (int e = 0; e < kNh / 2; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(sr[2 * e]) * f, __uint_as_float(sr[2 * e + 1]) * f);
+        if (half == 0) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pk[e] = pack_bf16x2(__uint_as_float(sr[16 * c + 2 * e]) * inv_l,
-                              __uint_as_float(sr[16 * c + 2 * e + 1]) * inv_l);
+          for (int c = 0; c < 4; ++c)
+            tmem_st8(pa + 8 * c, *reinterpret_cast<const uint32_t(*)[8]>(&pk[8 * c]));
+          tmem_st4(pa + 32, &pk[32]);
+        } else {
+          tmem_st4(pa, &pk[0]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_st8(pa + 4 + 8 * c, *reinterpret_cast<const uint32_t(*)[8]>(&pk[4 + 8 * c]));
         }
-        tmem_st8(tmem + lane_addr + kColP + c * 8, pk);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull));
-      if (p.lse != nullptr && i < p.T)
-        p.lse[((long long)b * p.Hq + h) * p.T + i] = (mx + __log2f(l)) * 0.6931471805599453f;
+      if (half == 0 && p.lse != nullptr && i < p.T)
+        p.lse[((long long)b * p.Hq + h) * p.T + i] = L * 0.6931471805599453f;
     }
   } else {
-    // ======================= epilogue (warps 4..7) =======================
+    // ======================= epilogue (warps 8..11) =======================
     const int sub = warp & 3;                 // TMEM lanes [32 sub, 32 sub + 32)
     const int quad = lane & 3, rr = lane >> 2;
     for (int it = 0; it < ntile; ++it) {
@@ -410,64 +493,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ob = it & 1;
       if (!mbar_wait(bar(kBarOFull + ob), (it >> 1) & 1, kErrWaitOFull, abort_flag)) break;
       tc_fence_after();
-      const uint32_t col = tmem + (ob ? kColO1 : kColO0);
+      const uint32_t col = tmem + (ob ? kColO1 : kColO0) + ((uint32_t)(sub * 32) << 16);
       if constexpr (kBf16Out) {
         // thread = tile row (TMEM lane 32 sub + lane): position 4 sub + lane / 8,
-        // head lane % 8; 32 consecutive columns per load, rounded to bf16 and
+        // head lane % 8; 64 consecutive columns per round, rounded to bf16 and
         // written as whole 32-byte sectors
-        uint32_t o[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(col + ((uint32_t)(sub * 32) << 16) + 32 * c, o[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) reg_fence32(o[c]);
-        tc_fence_before();
-        mbar_arrive(bar(kBarOFree + ob));
         const int pos = n * kNpos + 4 * sub + (lane >> 3);
-        if (pos < p.T) {
-          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                                (((long long)b * p.T + pos) * p.Hq + kvh * kG + (lane & 7)) * kD;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                              (((long long)b * p.T + pos) * p.Hq + kvh * kG + (lane & 7)) * kD;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
+        for (int rd = 0; rd < 2; ++rd) {
+          uint32_t o[64];
+          tmem_ld32(col + 64 * rd, o);
+          tmem_ld32(col + 64 * rd + 32, o + 32);
+          tmem_ld_wait();
+          reg_fence32(o);
+          reg_fence32(o + 32);
+          if (rd == 1) {
+            tc_fence_before();
+            mbar_arrive(bar(kBarOFree + ob));
+          }
+          if (pos < p.T) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16x2(__uint_as_float(o[c][2 * e]), __uint_as_float(o[c][2 * e + 1]));
-            float* dst = reinterpret_cast<float*>(orow + 32 * c);
-            if (p.out_align32) {
-              st_global_v8(dst, pk);
-              st_global_v8(dst + 8, pk + 8);
-            } else {
+            for (int c = 0; c < 2; ++c) {
+              uint32_t pk[16];
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                st_global_v4(dst + 4 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+              for (int e = 0; e < 16; ++e)
+                pk[e] = pack_bf16x2(__uint_as_float(o[32 * c + 2 * e]),
+                                    __uint_as_float(o[32 * c + 2 * e + 1]));
+              float* dst = reinterpret_cast<float*>(orow + 64 * rd + 32 * c);
+              if (p.out_align32) {
+                st_global_v8(dst, pk);
+                st_global_v8(dst + 8, pk + 8);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  st_global_v4(dst + 4 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+              }
             }
           }
         }
         continue;
       }
-      uint32_t o0[64], o1[64];
-      tmem_ld_16x256b_x16(col + ((uint32_t)(sub * 32) << 16), o0);
-      tmem_ld_16x256b_x16(col + ((uint32_t)(sub * 32 + 16) << 16), o1);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o0[c * 16]));
-        reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o1[c * 16]));
-      }
-      tc_fence_before();
-      mbar_arrive(bar(kBarOFree + ob));
-      // rows of this thread: 32 sub + {0, 8, 16, 24} + rr, i.e. positions
-      // 4 sub + {0, 1, 2, 3}, head rr; columns 8j + 2 quad + {0, 1}
+      // rows of this thread: 32 sub + 16 hf + {0, 8} + rr, i.e. positions
+      // 4 sub + 2 hf + {0, 1}, head rr; columns 8j + 2 quad + {0, 1}
       const long long row0 = ((long long)b * p.T + n * kNpos + 4 * sub) * p.Hq + kvh * kG + rr;
       const int pos0 = n * kNpos + 4 * sub;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t o[64];
+        tmem_ld_16x256b_x16(col + ((uint32_t)(16 * hf) << 16), o);
+        tmem_ld_wait();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t* o = half ? o1 : o0;
-          if (pos0 + 2 * half + k < p.T) {
-            const long long e0 = (row0 + (long long)(2 * half + k) * p.Hq) * kD + 2 * quad;
+        for (int c = 0; c < 4; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o[c * 16]));
+        if (hf == 1) {
+          tc_fence_before();
+          mbar_arrive(bar(kBarOFree + ob));
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (pos0 + 2 * hf + k < p.T) {
+            const long long e0 = (row0 + (long long)(2 * hf + k) * p.Hq) * kD + 2 * quad;
             float* orow = static_cast<float*>(p.out) + e0;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
