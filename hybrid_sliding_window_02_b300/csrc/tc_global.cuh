@@ -19,24 +19,28 @@
 // direction, which keeps the per-CTA totals within about one item of each
 // other without any shared counter.
 //
-// Roles (320 threads):
+// Roles (352 threads):
 //   warp 8      TMA producer: the two Q tiles of an item, then K_j and V_j for
 //               every key block j into a ring of 32 KB slots
-//   warp 9      TMEM owner + single-thread tcgen05.mma issuer
-//                 S   = Q_i K_j^T  (SS, M = 128, N = 128, K = 128)
-//                 O_i += P_i V_j   (TS, P_i from TMEM, V MN-major, N = 128)
+//   warp 9      TMEM owner + issuer of S   = Q_i K_j^T  (SS, M = N = K = 128)
+//   warp 10     issuer of                O_i += P_i V_j   (TS, P_i from TMEM,
+//               V MN-major, N = 128)
 //   warps 0..3  softmax of tile 0, warps 4..7 softmax of tile 1: thread =
 //               row; S -> mask -> running max / sum -> bf16 P_i in TMEM;
 //               after the last block O / l -> out and the lse.
+// The tensor pipe accepts only a few MMAs ahead of the one executing, so a
+// single issuing thread that stops at a barrier between two groups of MMAs
+// leaves the pipe idle for that wait (about 100-200 cycles each, as the
+// issuing warp shares its sub-partition with two softmax warps).  With the S
+// and PV products issued from two threads, one thread's waits are covered by
+// the other's MMAs; each accumulator still receives its MMAs in order, so the
+// results are unchanged.
 // TMEM: S [0,128) shared by the two tiles, P0 [128,192), P1 [192,256) (bf16
-// pairs), O0 [256,384), O1 [384,512).  Per key block n the MMA order is
-//     S0(n)  PV1(n-1)  S1(n)  PV0(n)
-// S goes to one buffer that each softmax empties into registers at once, so
-// an S waits only for the other tile's read of the previous one (covered by
-// the PV between them), and P never shares columns with S: each tile's
-// softmax has two MMAs of the other tile (PV then S) to hide behind before its
-// own PV is due.  A softmax rewrites P_i (and rescales O_i) only after the
-// tile's previous PV has completed, which it learns from a commit barrier.
+// pairs), O0 [256,384), O1 [384,512).  S goes to one buffer that each softmax
+// empties into registers at once, so an S waits only for the other tile's
+// read of the previous one, and P never shares columns with S.  A softmax
+// rewrites P_i (and rescales O_i) only after the tile's previous PV has
+// completed, which it learns from a commit barrier.
 //
 // Rescaling: the running max m only moves when a block's max exceeds it by
 // more than 8 (log2 units).  Otherwise p = 2^(x - m) <= 256 and the stale m
@@ -50,8 +54,8 @@
 namespace swa {
 namespace tcglobal {
 
-constexpr int kThreads = 320;
-constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr int kThreads = 352;
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr int kG = 8;                   // query heads per tile (one kv group)
 constexpr int kD = 128;
 constexpr int kNpos = 16;               // positions per Q tile
@@ -73,7 +77,7 @@ constexpr int kBarQFull = 0, kBarQEmpty = kBarQFull + kTiles, kBarKvFull = kBarQ
               kBarKvEmpty = kBarKvFull + kSlots, kBarSFull = kBarKvEmpty + kSlots,
               kBarSFree = kBarSFull + kTiles, kBarPFull = kBarSFree + 1,
               kBarPvDone = kBarPFull + kTiles, kBarOFull = kBarPvDone + kTiles,
-              kBarDrain = kBarOFull + kTiles, kNumBars = kBarDrain + 1;
+              kBarDrain = kBarOFull + kTiles, kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;  // + slack for 1024 alignment
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarKvEmpty + s), 1);
     }
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain + 1), 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -257,28 +262,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ======================= MMA issuer =======================
+  } else if (warp == kWarpMma || warp == kWarpPv) {
+    // ============ MMA issuers: S products (warp 9), PV products (warp 10) ============
+    // Two issuing threads keep the tensor pipe fed while either one waits on
+    // a barrier; each accumulator still receives its MMAs in program order.
     if (lane == 0) {
+      const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_s = umma_idesc_bf16(kBlk, false, false);
       const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
       const uint64_t qdesc0 = umma_sdesc(sbase + kOffQ, 16, 1024, 2);
       const uint64_t kdesc0 = umma_sdesc(sbase + kOffKV, 16, 1024, 2);
       const uint64_t vdesc0 = umma_sdesc(sbase + kOffKV, kSlotHalf, 1024, 2);
-      uint32_t seq = 0;       // K/V loads consumed (K and V alternate)
+      uint32_t gblk = 0;      // key blocks consumed so far (all items)
       uint32_t ns = 0;        // S products issued (S0 and S1 alternate)
-      uint32_t nblk = 0;      // key blocks whose PV0 has been issued
       bool ok = true;
-      // the block whose PV1 is still to be issued
-      bool pend = false, pend_first = false, pend_last = false;
-      uint32_t pend_vs = 0;
-
-      auto wait_kv = [&](uint32_t& slot) -> bool {
+      // K of block g is ring load 2g, V of block g is load 2g + 1
+      auto wait_load = [&](uint32_t seq, uint32_t& slot) -> bool {
         slot = seq % kSlots;
-        const bool r = mbar_wait(bar(kBarKvFull + slot), (seq / kSlots) & 1, kErrWaitKvFull,
-                                 abort_flag);
-        ++seq;
-        return r;
+        return mbar_wait(bar(kBarKvFull + slot), (seq / kSlots) & 1, kErrWaitKvFull, abort_flag);
       };
       // S = Q_i K^T into the shared buffer, once the other tile's softmax has
       // read the previous S out of it
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++ns;
         return true;
       };
-      // O_i += P_i V for block b (its P_i is released as block number blk)
+      // O_i += P_i V for block number blk
       auto issue_pv = [&](int i, uint32_t vs, uint32_t blk, bool first, bool last) -> bool {
         if (!mbar_wait(bar(kBarPFull + i), blk & 1, kErrWaitPFull, abort_flag)) return false;
         tc_fence_after();
@@ -314,45 +315,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       Item it;
       for (int k = 0; ok && cta_item(k, p, it); ++k) {
-        for (int t = 0; t < it.nb; ++t) {
-          uint32_t ks, vs;
-          // ---- S0(n) ----
-          if (!wait_kv(ks)) { ok = false; break; }
-          if (t == 0 && !mbar_wait(bar(kBarQFull + 0), k & 1, kErrWaitQFull, abort_flag)) {
-            ok = false;
-            break;
+        for (int t = 0; t < it.nb; ++t, ++gblk) {
+          uint32_t slot;
+          if (s_side) {
+            if (!wait_load(2 * gblk, slot)) { ok = false; break; }
+            if (t == 0 && !mbar_wait(bar(kBarQFull + 0), k & 1, kErrWaitQFull, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (!issue_s(0, slot)) { ok = false; break; }
+            if (t == 0 && !mbar_wait(bar(kBarQFull + 1), k & 1, kErrWaitQFull, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (!issue_s(1, slot)) { ok = false; break; }
+            umma_commit(bar(kBarKvEmpty + slot));
+            if (t == it.nb - 1)
+              for (int i = 0; i < kTiles; ++i) umma_commit(bar(kBarQEmpty + i));
+          } else {
+            if (!wait_load(2 * gblk + 1, slot)) { ok = false; break; }
+            const bool first = t == 0, last = t == it.nb - 1;
+            if (!issue_pv(0, slot, gblk, first, last)) { ok = false; break; }
+            if (!issue_pv(1, slot, gblk, first, last)) { ok = false; break; }
+            umma_commit(bar(kBarKvEmpty + slot));
           }
-          if (!issue_s(0, ks)) { ok = false; break; }
-          // ---- PV1(n-1) ----
-          if (pend) {
-            if (!issue_pv(1, pend_vs, nblk - 1, pend_first, pend_last)) { ok = false; break; }
-            umma_commit(bar(kBarKvEmpty + pend_vs));
-            pend = false;
-          }
-          // ---- S1(n) ----
-          if (t == 0 && !mbar_wait(bar(kBarQFull + 1), k & 1, kErrWaitQFull, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (!issue_s(1, ks)) { ok = false; break; }
-          umma_commit(bar(kBarKvEmpty + ks));
-          if (t == it.nb - 1)
-            for (int i = 0; i < kTiles; ++i) umma_commit(bar(kBarQEmpty + i));
-          // ---- PV0(n) ----
-          if (!wait_kv(vs)) { ok = false; break; }
-          if (!issue_pv(0, vs, nblk, t == 0, t == it.nb - 1)) { ok = false; break; }
-          pend = true;
-          pend_vs = vs;
-          pend_first = t == 0;
-          pend_last = t == it.nb - 1;
-          ++nblk;
         }
       }
-      if (ok && pend && issue_pv(1, pend_vs, nblk - 1, pend_first, pend_last))
-        umma_commit(bar(kBarKvEmpty + pend_vs));
-      // every MMA issued so far completes before TMEM is released
-      umma_commit(bar(kBarDrain));
-      mbar_wait_drain(bar(kBarDrain), 0);
+      // every MMA this thread issued completes before TMEM is released
+      const uint32_t db = bar(kBarDrain + (s_side ? 0 : 1));
+      umma_commit(db);
+      mbar_wait_drain(db, 0);
     }
     __syncwarp();
   } else {
