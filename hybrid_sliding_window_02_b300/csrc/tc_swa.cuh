@@ -19,12 +19,16 @@
 // their 9 key blocks, so keys and values live in a ring of 16-key blocks in
 // shared memory and each key/value row is loaded from HBM once per run.
 //
-// Roles (448 threads), all connected by mbarriers:
+// Roles (480 threads), all connected by mbarriers:
 //   warp 12     TMA producer: Q tiles (4 stages, to cover the HBM latency seen
 //               under full load) and new K/V blocks (12-slot ring)
-//   warp 13     TMEM owner + single-thread tcgen05.mma issuer
-//                 S = Q K^T   (SS: M=128, N=144 split at the ring wrap, K=128)
-//                 O = P V     (TS: P from TMEM, V MN-major, N=128, K=16/block)
+//   warp 13     TMEM owner + issuer of S = Q K^T (SS: M=128, N=144 split at
+//               the ring wrap, K=128)
+//   warp 14     issuer of O = P V (TS: P from TMEM, V MN-major, N=128,
+//               K=16 per block); releases the ring blocks
+//               One issuing thread for both paced the kernel: its barrier
+//               waits and bookkeeping, slowed by sharing a sub-partition with
+//               three busy warps, came to ~5000 cycles per tile.
 //   warps 0..7  softmax, two threads per row: warp w reads TMEM lanes
 //               [32 (w % 4), +32); warps 0..3 take columns [0, 72), warps
 //               4..7 columns [72, 144).  Each half forms 2^(x - m_half) and
@@ -34,17 +38,21 @@
 //               log-sum-exp L, and write bf16 P = 2^(x - L) to TMEM; lse ->
 //               global.  Two softmax warps per SM sub-partition hide each
 //               other's latencies; the exponentials stay exact single-pass.
-//   warps 8..11 epilogue: O (TMEM, double-buffered) -> global (fp32, or bf16
+//   warps 8..11 epilogue: O (TMEM) -> global (fp32, or bf16
 //               rounded from the same fp32 values).  The 16x256b
 //               TMEM read gives each group of 4 threads 32 contiguous bytes of
 //               a row, so every warp store fills 8 whole 32-byte sectors of 8
 //               lines (one position's 8 heads: 4 KB contiguous); this measured
 //               clearly faster than one 32-byte store per thread per row.
-// TMEM: S [0,144), P [160,232) (bf16 pairs), exchange [232,236),
-// O0 [256,384), O1 [384,512).
-// QK^T of tile t+1 runs while softmax works on tile t (S is read out at once),
-// and the epilogue of tile t overlaps softmax and MMAs of tile t+1.
-// 14 warps put 4 on two of the SM's sub-partitions, which caps registers at
+// TMEM: S [0,144), P0 [144,216), P1 [216,288) (bf16 pairs), exchange
+// [288,292), O [384,512).
+// QK^T of tile t+1 runs while softmax works on tile t (S is read out at once).
+// P is double-buffered, so the softmax of tile t writes its P while tile
+// t-1's PV may still be running; O is single-buffered, as the epilogue
+// empties it into registers long before the next PV is issued (that PV waits
+// for the softmax of the next tile).  TMEM holds no more: S, two P, O and
+// the exchange take 420 of 512 columns, two O buffers would need 548.
+// 15 warps put 4 on three of the SM's sub-partitions, which caps registers at
 // 128 per thread: a softmax thread holds 72 scores, an epilogue thread 64
 // output values at a time.
 #pragma once
@@ -54,8 +62,8 @@
 namespace swa {
 namespace tcswa {
 
-constexpr int kThreads = 448;
-constexpr int kWarpProducer = 12, kWarpMma = 13;
+constexpr int kThreads = 480;
+constexpr int kWarpProducer = 12, kWarpMma = 13, kWarpPv = 14;
 constexpr int kWarpEpi0 = 8;
 constexpr int kG = 8;            // query heads per tile (one kv group)
 constexpr int kNpos = 16;        // positions per tile
@@ -80,16 +88,18 @@ constexpr int kOffBar = kOffV + 2 * kRingHalf;        // +48 KB
 // barriers
 constexpr int kBarQFull = 0, kBarQEmpty = kQStages, kBarKvFull = 2 * kQStages,
               kBarKvEmpty = kBarKvFull + kRing, kBarSFull = kBarKvEmpty + kRing,
-              kBarSFree = kBarSFull + 1, kBarPFull = kBarSFree + 1, kBarPFree = kBarPFull + 1,
-              kBarOFull = kBarPFree + 1, kBarOFree = kBarOFull + 2, kBarXchg = kBarOFree + 2,
-              kBarDrain = kBarXchg + 4, kNumBars = kBarDrain + 1;
+              kBarSFree = kBarSFull + 1, kBarPFull = kBarSFree + 1, kBarPFree = kBarPFull + 2,
+              kBarOFull = kBarPFree + 2, kBarOFree = kBarOFull + 1, kBarXchg = kBarOFree + 1,
+              kBarDrain = kBarXchg + 4, kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;      // + slack for 1024 alignment
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColP = 160, kColX = 232, kColO0 = 256, kColO1 = 384;
+constexpr uint32_t kColS = 0, kColX = 288, kColO = 384;
+// P of tile t goes to buffer t % 2: columns [144, 216) or [216, 288)
+__host__ __device__ constexpr uint32_t col_p(int b) { return 144u + 72u * (uint32_t)b; }
 
 struct Params {
   const float* sink;
@@ -109,6 +119,21 @@ __device__ __forceinline__ void tile_coords(uint32_t u, const Params& p, int& b,
   b = (int)(bk / (uint32_t)p.Hkv);
   kvh = (int)(bk - (uint32_t)b * (uint32_t)p.Hkv);
 }
+
+// Tile coordinates walked one tile at a time (no divisions after the start).
+struct TileWalk {
+  int b, kvh, n;
+  __device__ __forceinline__ void start(uint32_t u, const Params& p) { tile_coords(u, p, b, kvh, n); }
+  __device__ __forceinline__ void next(const Params& p) {
+    if (++n == p.ntiles_seq) {
+      n = 0;
+      if (++kvh == p.Hkv) {
+        kvh = 0;
+        ++b;
+      }
+    }
+  }
+};
 
 template <bool kBf16Out>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -140,15 +165,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarKvEmpty + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kBarOFull + s), 1);
-      mbar_init(bar(kBarOFree + s), 128);
+      mbar_init(bar(kBarPFull + s), 256);
+      mbar_init(bar(kBarPFree + s), 1);
     }
+    mbar_init(bar(kBarOFull), 1);
+    mbar_init(bar(kBarOFree), 128);
     for (int s = 0; s < 4; ++s) mbar_init(bar(kBarXchg + s), 64);
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarSFree), 256);
-    mbar_init(bar(kBarPFull), 256);
-    mbar_init(bar(kBarPFree), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain + 1), 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -172,9 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int prev_bk = -1;
       int q_issued = 0;  // Q tiles loaded so far
       bool ok = true;
-      for (int it = 0; it < ntile && ok; ++it) {
-        int b, kvh, n;
-        tile_coords(t_begin + it, p, b, kvh, n);
+      TileWalk w;
+      w.start(t_begin, p);
+      for (int it = 0; it < ntile && ok; ++it, w.next(p)) {
+        const int b = w.b, kvh = w.kvh, n = w.n;
         const uint32_t qs = (uint32_t)it % kQStages;
         const uint32_t qph = ((uint32_t)it / kQStages) & 1;
         if (!mbar_wait(bar(kBarQEmpty + qs), qph ^ 1, kErrWaitQEmpty, abort_flag)) {
@@ -216,9 +243,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ======================= MMA issuer =======================
+  } else if (warp == kWarpMma || warp == kWarpPv) {
+    // ============ MMA issuers: S = Q K^T (warp 13), O = P V (warp 14) ============
+    // Each issuing thread waits only on its own barriers, so one thread's
+    // waits and bookkeeping no longer hold back the other's MMAs.
     if (lane == 0) {
+      const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
       // Descriptors are built once; per operand they differ only in the
       // start-address field (address >> 4, bits 0..13), advanced by adding
@@ -228,116 +258,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vdesc0 = umma_sdesc(sbase + kOffV, kRingHalf, 1024, 2);
       uint32_t seq = 0;      // blocks loaded (mirrors the producer)
       int prev_bk = -1;
-      int pending = -1;      // tile whose PV is still to be issued
-      uint32_t pending_ws = 0;
-      bool pending_run_end = false;
       bool ok = true;
-
-      auto issue_pv = [&](int j, uint32_t ws, bool run_end) -> bool {
-        const int ob = j & 1;
-        if (!mbar_wait(bar(kBarPFull), j & 1, kErrWaitPFull, abort_flag)) return false;
-        if (!mbar_wait(bar(kBarOFree + ob), ((j >> 1) & 1) ^ 1, kErrWaitOFree, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t d_o = tmem + (ob ? kColO1 : kColO0);
-        uint32_t slot = ws % kRing;
-#pragma unroll
-        for (int kb = 0; kb < kNB; ++kb) {
-          umma_bf16_ts(d_o, tmem + kColP + kb * (kBlk / 2), vdesc0 + slot * (kBlkHalf >> 4),
-                       idesc_o, kb > 0 ? 1u : 0u);
-          slot = (slot + 1 == kRing) ? 0 : slot + 1;
-        }
-        umma_commit(bar(kBarOFull + ob));
-        umma_commit(bar(kBarPFree));
-        // release key blocks no later tile of this run needs
-        const int nrel = run_end ? kNB : 1;
-        slot = ws % kRing;
-        for (int r = 0; r < nrel; ++r) {
-          umma_commit(bar(kBarKvEmpty + slot));
-          slot = (slot + 1 == kRing) ? 0 : slot + 1;
-        }
-        return true;
-      };
-
+      TileWalk w;
+      w.start(t_begin, p);
       for (int it = 0; it < ntile && ok; ++it) {
-        int b, kvh, n;
-        tile_coords(t_begin + it, p, b, kvh, n);
-        const int bk = b * p.Hkv + kvh;
+        const int bk = w.b * p.Hkv + w.kvh;
         const bool new_run = (bk != prev_bk);
         prev_bk = bk;
         const int nnew = new_run ? kNB : 1;
-        // a new run needs the whole ring: finish the previous tile first
-        if (new_run && pending >= 0) {
-          if (!issue_pv(pending, pending_ws, true)) { ok = false; break; }
-          pending = -1;
-        }
-        // wait for this tile's Q and new key/value blocks
-        const uint32_t qs = (uint32_t)it % kQStages;
-        if (!mbar_wait(bar(kBarQFull + qs), ((uint32_t)it / kQStages) & 1, kErrWaitQFull,
-                       abort_flag)) {
-          ok = false;
-          break;
-        }
-        for (int r = 0; r < nnew; ++r) {
-          const uint32_t s = seq + r;
-          if (!mbar_wait(bar(kBarKvFull + s % kRing), (s / kRing) & 1, kErrWaitKvFull,
+        const uint32_t ws = seq + nnew - kNB;  // first block of this tile's window
+        w.next(p);
+        if (s_side) {
+          // wait for this tile's Q and new key/value blocks
+          const uint32_t qs = (uint32_t)it % kQStages;
+          if (!mbar_wait(bar(kBarQFull + qs), ((uint32_t)it / kQStages) & 1, kErrWaitQFull,
                          abort_flag)) {
             ok = false;
             break;
           }
-        }
-        if (!ok) break;
-        seq += nnew;
-        const uint32_t ws = seq - kNB;  // first block of this tile's window
-        if (!mbar_wait(bar(kBarSFree), (it & 1) ^ 1, kErrWaitSFree, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // S = Q K^T; the window's blocks may wrap around the ring end
-        const uint32_t slot0 = ws % kRing;
-        const uint32_t seg1 = (slot0 + kNB <= kRing) ? kNB : kRing - slot0;
-        const uint32_t d_s = tmem + kColS;
-        const uint32_t idesc1 = umma_idesc_bf16(seg1 * kBlk, false, false);
-        const uint32_t idesc2 = umma_idesc_bf16((kNB - seg1) * kBlk, false, false);
-        const uint64_t qd = qdesc0 + qs * (kQStage >> 4);
-        const uint64_t kd1 = kdesc0 + slot0 * (kBlkHalf >> 4);
-        if (seg1 == (uint32_t)kNB) {
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
-            const uint32_t k_off = ((kk >> 2) * kRingHalf + (kk & 3) * 32) >> 4;
-            umma_bf16_ss(d_s, qd + a_off, kd1 + k_off, idesc1, kk > 0);
+          for (int r = 0; r < nnew; ++r) {
+            const uint32_t s2 = seq + r;
+            if (!mbar_wait(bar(kBarKvFull + s2 % kRing), (s2 / kRing) & 1, kErrWaitKvFull,
+                           abort_flag)) {
+              ok = false;
+              break;
+            }
           }
+          if (!ok) break;
+          seq += nnew;
+          if (!mbar_wait(bar(kBarSFree), (it & 1) ^ 1, kErrWaitSFree, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // S = Q K^T; the window's blocks may wrap around the ring end
+          const uint32_t slot0 = ws % kRing;
+          const uint32_t seg1 = (slot0 + kNB <= kRing) ? kNB : kRing - slot0;
+          const uint32_t d_s = tmem + kColS;
+          const uint32_t idesc1 = umma_idesc_bf16(seg1 * kBlk, false, false);
+          const uint32_t idesc2 = umma_idesc_bf16((kNB - seg1) * kBlk, false, false);
+          const uint64_t qd = qdesc0 + qs * (kQStage >> 4);
+          const uint64_t kd1 = kdesc0 + slot0 * (kBlkHalf >> 4);
+          if (seg1 == (uint32_t)kNB) {
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+              const uint32_t k_off = ((kk >> 2) * kRingHalf + (kk & 3) * 32) >> 4;
+              umma_bf16_ss(d_s, qd + a_off, kd1 + k_off, idesc1, kk > 0);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+              const uint32_t k_off = ((kk >> 2) * kRingHalf + (kk & 3) * 32) >> 4;
+              umma_bf16_ss(d_s, qd + a_off, kd1 + k_off, idesc1, kk > 0);
+              umma_bf16_ss(d_s + seg1 * kBlk, qd + a_off, kdesc0 + k_off, idesc2, kk > 0);
+            }
+          }
+          umma_commit(bar(kBarSFull));
+          umma_commit(bar(kBarQEmpty + qs));
         } else {
+          seq += nnew;
+          // the last tile of a run releases every block of its window, the
+          // others only the oldest one (their S reads completed before the
+          // softmax that produced this P)
+          const bool run_end = (it + 1 >= ntile) || (w.b * p.Hkv + w.kvh != bk);
+          const int pb = it & 1;
+          if (!mbar_wait(bar(kBarPFull + pb), (it >> 1) & 1, kErrWaitPFull, abort_flag)) {
+            ok = false;
+            break;
+          }
+          // O is single-buffered: the epilogue has read tile it - 1's O out of it
+          if (!mbar_wait(bar(kBarOFree), (it & 1) ^ 1, kErrWaitOFree, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_o = tmem + kColO;
+          uint32_t slot = ws % kRing;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
-            const uint32_t k_off = ((kk >> 2) * kRingHalf + (kk & 3) * 32) >> 4;
-            umma_bf16_ss(d_s, qd + a_off, kd1 + k_off, idesc1, kk > 0);
-            umma_bf16_ss(d_s + seg1 * kBlk, qd + a_off, kdesc0 + k_off, idesc2, kk > 0);
+          for (int kb = 0; kb < kNB; ++kb) {
+            umma_bf16_ts(d_o, tmem + col_p(pb) + kb * (kBlk / 2),
+                         vdesc0 + slot * (kBlkHalf >> 4), idesc_o, kb > 0 ? 1u : 0u);
+            slot = (slot + 1 == kRing) ? 0 : slot + 1;
+          }
+          umma_commit(bar(kBarOFull));
+          umma_commit(bar(kBarPFree + pb));
+          const int nrel = run_end ? kNB : 1;
+          slot = ws % kRing;
+          for (int r = 0; r < nrel; ++r) {
+            umma_commit(bar(kBarKvEmpty + slot));
+            slot = (slot + 1 == kRing) ? 0 : slot + 1;
           }
         }
-        umma_commit(bar(kBarSFull));
-        umma_commit(bar(kBarQEmpty + qs));
-        if (pending >= 0) {
-          if (!issue_pv(pending, pending_ws, pending_run_end)) { ok = false; break; }
-        }
-        pending = it;
-        pending_ws = ws;
-        // is the next tile in the same run?
-        bool run_end = true;
-        if (it + 1 < ntile) {
-          int b2, kvh2, n2;
-          tile_coords(t_begin + it + 1, p, b2, kvh2, n2);
-          run_end = (b2 * p.Hkv + kvh2) != bk;
-        }
-        pending_run_end = run_end;
       }
-      if (ok && pending >= 0) issue_pv(pending, pending_ws, true);
-      // every MMA issued so far completes before TMEM is released
-      umma_commit(bar(kBarDrain));
-      mbar_wait_drain(bar(kBarDrain), 0);
+      // every MMA this thread issued completes before TMEM is released
+      const uint32_t db = bar(kBarDrain + (s_side ? 0 : 1));
+      umma_commit(db);
+      mbar_wait_drain(db, 0);
     }
     __syncwarp();
   } else if (warp < kWarpEpi0) {
@@ -348,9 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = half * kNh;                // first score column of this half
     const int pos_in_tile = r >> 3, g = r & 7;
     const uint32_t xbar = bar(kBarXchg + quad);
-    for (int it = 0; it < ntile; ++it) {
-      int b, kvh, n;
-      tile_coords(t_begin + it, p, b, kvh, n);
+    TileWalk w;
+    w.start(t_begin, p);
+    for (int it = 0; it < ntile; ++it, w.next(p)) {
+      const int b = w.b, kvh = w.kvh, n = w.n;
       const int h = kvh * kG + g;
       const float sk = p.sink[h] * 1.4426950408889634f;
       const int i = n * kNpos + pos_in_tile;            // query position
@@ -454,13 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    ex2_approx(sk - mm));
       // P = 2^(x scale - L) = p 2^(mh - L); an empty half has p = 0
       const float f = (lh > 0.f) ? ex2_approx(mh - L) : 0.f;
-      // bf16 P -> TMEM once the previous tile's PV has consumed it
-      if (!mbar_wait(bar(kBarPFree), (it & 1) ^ 1, kErrWaitPFree, abort_flag)) break;
+      // bf16 P -> TMEM buffer it % 2 once tile it - 2's PV has consumed it
+      const int pb = it & 1;
+      if (!mbar_wait(bar(kBarPFree + pb), ((it >> 1) & 1) ^ 1, kErrWaitPFree, abort_flag)) break;
       tc_fence_after();
       {
         // packed columns [36 half, 36 half + 36): half 0 as 8,8,8,8,4;
         // half 1 as 4,8,8,8,8 (each store aligned to its width)
-        const uint32_t pa = tmem + lane_addr + kColP + half * (kNh / 2);
+        const uint32_t pa = tmem + lane_addr + col_p(pb) + half * (kNh / 2);
         uint32_t pk[kNh / 2];
 #pragma unroll
         for (int e = 0; e < kNh / 2; ++e)
@@ -479,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(kBarPFull));
+      mbar_arrive(bar(kBarPFull + pb));
       if (half == 0 && p.lse != nullptr && i < p.T)
         p.lse[((long long)b * p.Hq + h) * p.T + i] = L * 0.6931471805599453f;
     }
@@ -487,13 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= epilogue (warps 8..11) =======================
     const int sub = warp & 3;                 // TMEM lanes [32 sub, 32 sub + 32)
     const int quad = lane & 3, rr = lane >> 2;
-    for (int it = 0; it < ntile; ++it) {
-      int b, kvh, n;
-      tile_coords(t_begin + it, p, b, kvh, n);
-      const int ob = it & 1;
-      if (!mbar_wait(bar(kBarOFull + ob), (it >> 1) & 1, kErrWaitOFull, abort_flag)) break;
+    TileWalk w;
+    w.start(t_begin, p);
+    for (int it = 0; it < ntile; ++it, w.next(p)) {
+      const int b = w.b, kvh = w.kvh, n = w.n;
+      if (!mbar_wait(bar(kBarOFull), it & 1, kErrWaitOFull, abort_flag)) break;
       tc_fence_after();
-      const uint32_t col = tmem + (ob ? kColO1 : kColO0) + ((uint32_t)(sub * 32) << 16);
+      const uint32_t col = tmem + kColO + ((uint32_t)(sub * 32) << 16);
       if constexpr (kBf16Out) {
         // thread = tile row (TMEM lane 32 sub + lane): position 4 sub + lane / 8,
         // head lane % 8; 64 consecutive columns per round, rounded to bf16 and
@@ -511,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_fence32(o + 32);
           if (rd == 1) {
             tc_fence_before();
-            mbar_arrive(bar(kBarOFree + ob));
+            mbar_arrive(bar(kBarOFree));
           }
           if (pos < p.T) {
 #pragma unroll
@@ -548,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o[c * 16]));
         if (hf == 1) {
           tc_fence_before();
-          mbar_arrive(bar(kBarOFree + ob));
+          mbar_arrive(bar(kBarOFree));
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
