@@ -18,7 +18,9 @@
 // Persistent CTAs (one per SM) take groups u = blockIdx.x, + gridDim.x, ...;
 // a producer thread keeps three groups' K, V and q in flight through a ring of
 // shared-memory stages (TMA, 128-byte swizzle), so HBM never waits on the
-// math.  Two softmax warpgroups take alternate groups: thread = slot reads
+// math.  Two threads issue the MMAs, one the S^T products and one the O^T
+// products, so that waiting for a stage to land never delays the PV of the
+// group before it (and with it the release of that group's stage).  Two softmax warpgroups take alternate groups: thread = slot reads
 // its 8 head scores from TMEM, the max and the sum over slots are warp-shuffle
 // reductions finished across the four warps in shared memory, the bf16 P^T
 // goes to shared memory for the second MMA, and after it thread = dim reads
@@ -30,8 +32,8 @@
 namespace swa {
 namespace dectc {
 
-constexpr int kThreads = 320;
-constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr int kThreads = 352;
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr int kG = 8;              // query heads per kv head
 constexpr int kN = 16;             // MMA N: heads padded to 16
 constexpr int kW = 128;            // ring slots
@@ -51,7 +53,7 @@ constexpr int kRedBytes = 2 * 4 * kG * 4;
 constexpr int kOffBar = kOffRed + 2 * kRedBytes;
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarSFull = 2 * kStages,
               kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarRed = kBarOFull + 2,
-              kBarDrain = kBarRed + 4, kNumBars = kBarDrain + 1;
+              kBarDrain = kBarRed + 4, kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarRed + 2 * w + 1), 128);
     }
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain + 1), 1);
     fence_mbar_init();
   }
   // P^T rows 8..15 (the padding heads) stay zero for the whole kernel
@@ -164,57 +167,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ======================= MMA issuer =======================
+  } else if (warp == kWarpMma || warp == kWarpPv) {
+    // ====== MMA issuers: S^T of every group (warp 9), O^T of every group (warp 10) ======
+    // Two threads, so that the wait for a group's stage to land (S side) never
+    // holds back the PV of the group before it and the release of its stage.
     if (lane == 0) {
+      const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_s = umma_idesc_bf16(kN, false, false);
       const uint32_t idesc_o = umma_idesc_bf16(kN, true, false);
-      // S^T of group k into TMEM buffer k % 2 once its stage has landed.  The
-      // buffer was last read by the softmax of group k - 2, which released it
-      // (P full) before this thread issued the PV of group k - 2.
-      auto issue_s = [&](int k) -> bool {
-        const uint32_t s = (uint32_t)k % kStages;
-        if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
-                       abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t st = sbase + kOffStage + s * kStageBytes;
-        const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
-        const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t a_off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          const uint32_t b_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + col_s(k & 1), kdesc + a_off, qdesc + b_off, idesc_s, kk > 0);
-        }
-        umma_commit(bar(kBarSFull + (k & 1)));
-        return true;
-      };
-      // S of the next group goes in before the wait for this group's P, so
-      // that the two softmax warpgroups work on consecutive groups at once.
-      bool ok = nk > 0 && issue_s(0);
+      bool ok = true;
       for (int k = 0; ok && k < nk; ++k) {
-        if (k + 1 < nk && !issue_s(k + 1)) break;
         const uint32_t s = (uint32_t)k % kStages;
         const int w = k & 1;
-        // O^T = V^T P^T once the softmax of this group has written P^T
-        if (!mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag))
-          break;
-        tc_fence_after();
         const uint32_t st = sbase + kOffStage + s * kStageBytes;
-        const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
-        const uint64_t pdesc = umma_sdesc(sbase + kOffP + w * kPBytes, 16, 1024, 2);
+        if (s_side) {
+          // S^T of group k into TMEM buffer k % 2 once its stage has landed and
+          // the softmax of group k - 2 has read that buffer (P full)
+          if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (k >= 2 && !mbar_wait(bar(kBarPFull + w), ((uint32_t)(k - 2) >> 1) & 1,
+                                   kErrWaitPFull, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
+          const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
 #pragma unroll
-        for (int kb = 0; kb < kW / 16; ++kb) {
-          const uint32_t a_off = (kb * 16 * 128) >> 4;
-          const uint32_t b_off = ((kb >> 2) * kQHalf + (kb & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + col_o(w), vdesc + a_off, pdesc + b_off, idesc_o, kb > 0);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t a_off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+            const uint32_t b_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+            umma_bf16_ss(tmem + col_s(w), kdesc + a_off, qdesc + b_off, idesc_s, kk > 0);
+          }
+          umma_commit(bar(kBarSFull + w));
+        } else {
+          // O^T = V^T P^T once the softmax of this group has written P^T; the
+          // stage is then free (its S^T completed before that softmax began)
+          if (!mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
+          const uint64_t pdesc = umma_sdesc(sbase + kOffP + w * kPBytes, 16, 1024, 2);
+#pragma unroll
+          for (int kb = 0; kb < kW / 16; ++kb) {
+            const uint32_t a_off = (kb * 16 * 128) >> 4;
+            const uint32_t b_off = ((kb >> 2) * kQHalf + (kb & 3) * 32) >> 4;
+            umma_bf16_ss(tmem + col_o(w), vdesc + a_off, pdesc + b_off, idesc_o, kb > 0);
+          }
+          umma_commit(bar(kBarOFull + w));
+          umma_commit(bar(kBarEmpty + s));
         }
-        umma_commit(bar(kBarOFull + w));
-        umma_commit(bar(kBarEmpty + s));
       }
-      umma_commit(bar(kBarDrain));
-      mbar_wait_drain(bar(kBarDrain), 0);
+      // every MMA this thread issued completes before TMEM is released
+      const uint32_t db = bar(kBarDrain + (s_side ? 0 : 1));
+      umma_commit(db);
+      mbar_wait_drain(db, 0);
     }
     __syncwarp();
   } else {

@@ -23,11 +23,13 @@
 // slots s >= pos are empty (their values are zeroed in shared memory so that
 // 0 * V stays 0) and every column is tested.
 //
-// Persistent CTAs, two stages of K, V, Q and new K / V in flight (TMA), one
-// MMA thread, two warpgroups on alternate groups, each with its own S / O
-// pair in TMEM: S_w [256 w, 256 w + 128), O_w [256 w + 128, 256 w + 256).
-// S of group k overwrites P of group k - 2, so it is issued once that group's
-// PV has completed.
+// Persistent CTAs, two stages of K, V, Q and new K / V in flight (TMA), two
+// MMA-issuing threads (one for the S products, one for the PV products, so
+// that waiting for a stage to land never delays the PV of the group before
+// it and the release of its stage), two warpgroups on alternate groups, each
+// with its own S / O pair in TMEM: S_w [256 w, 256 w + 128), O_w [256 w +
+// 128, 256 w + 256).  S of group k overwrites P of group k - 2, so it is
+// issued once that group's PV has completed.
 #pragma once
 
 #include "device_common.cuh"
@@ -35,8 +37,8 @@
 namespace swa {
 namespace vertc {
 
-constexpr int kThreads = 320;
-constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr int kThreads = 352;
+constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr int kG = 8;
 constexpr int kLmax = 4;
 constexpr int kW = 128;
@@ -54,7 +56,7 @@ constexpr int kOffSn = kOffStage + (int)kStages * kStageBytes;  // [wg][32 rows]
 constexpr int kOffBar = kOffSn + 2 * 32 * 4 * 4;
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarSFull = 2 * kStages,
               kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarSnFull = kBarOFull + 2,
-              kBarDrain = kBarSnFull + 2, kNumBars = kBarDrain + 1;
+              kBarDrain = kBarSnFull + 2, kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;
@@ -104,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSnFull + w), 96);
     }
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain + 1), 1);
     fence_mbar_init();
   }
   // new key / value rows L..15 of both stages are never written by a copy:
@@ -159,54 +162,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ======================= MMA issuer =======================
+  } else if (warp == kWarpMma || warp == kWarpPv) {
+    // ====== MMA issuers: S of every group (warp 9), O of every group (warp 10) ======
+    // Two threads, so that the wait for a group's stage to land (S side) never
+    // holds back the PV of the group before it and the release of its stage.
     if (lane == 0) {
+      const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_s = umma_idesc_bf16(kW, false, false);
       const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
-      auto issue_s = [&](int k) -> bool {
-        const uint32_t s = (uint32_t)k % kStages;
-        const int w = k & 1;
-        if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
-                       abort_flag))
-          return false;
-        // S_w holds P of group k - 2 until that group's PV has completed
-        if (k >= 2 && !mbar_wait(bar(kBarOFull + w), (((uint32_t)k >> 1) - 1) & 1,
-                                 kErrWaitOFull, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t st = sbase + kOffStage + s * kStageBytes;
-        const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
-        const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + col_s(w), qdesc + off, kdesc + off, idesc_s, kk > 0);
-        }
-        umma_commit(bar(kBarSFull + w));
-        return true;
-      };
-      bool ok = nk > 0 && issue_s(0);
+      bool ok = true;
       for (int k = 0; ok && k < nk; ++k) {
-        if (k + 1 < nk && !issue_s(k + 1)) break;
         const uint32_t s = (uint32_t)k % kStages;
         const int w = k & 1;
-        if (!mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag))
-          break;
-        tc_fence_after();
         const uint32_t st = sbase + kOffStage + s * kStageBytes;
-        const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
-        const uint64_t vndesc = umma_sdesc(st + kStageVn, kNewHalf, 1024, 2);
+        if (s_side) {
+          if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          // S_w holds P of group k - 2 until that group's PV has completed
+          if (k >= 2 && !mbar_wait(bar(kBarOFull + w), (((uint32_t)k >> 1) - 1) & 1,
+                                   kErrWaitOFull, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
+          const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
 #pragma unroll
-        for (int kb = 0; kb < kW / 16; ++kb)
-          umma_bf16_ts(tmem + col_o(w), tmem + col_s(w) + kb * 8,
-                       vdesc + (uint32_t)(kb * 16 * 128 >> 4), idesc_o, kb > 0);
-        umma_bf16_ts(tmem + col_o(w), tmem + col_s(w) + 64, vndesc, idesc_o, 1u);
-        umma_commit(bar(kBarOFull + w));
-        umma_commit(bar(kBarEmpty + s));
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+            umma_bf16_ss(tmem + col_s(w), qdesc + off, kdesc + off, idesc_s, kk > 0);
+          }
+          umma_commit(bar(kBarSFull + w));
+        } else {
+          // O = P V once the softmax of this group has written P; the stage is
+          // then free (its S completed before that softmax began)
+          if (!mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
+          const uint64_t vndesc = umma_sdesc(st + kStageVn, kNewHalf, 1024, 2);
+#pragma unroll
+          for (int kb = 0; kb < kW / 16; ++kb)
+            umma_bf16_ts(tmem + col_o(w), tmem + col_s(w) + kb * 8,
+                         vdesc + (uint32_t)(kb * 16 * 128 >> 4), idesc_o, kb > 0);
+          umma_bf16_ts(tmem + col_o(w), tmem + col_s(w) + 64, vndesc, idesc_o, 1u);
+          umma_commit(bar(kBarOFull + w));
+          umma_commit(bar(kBarEmpty + s));
+        }
       }
-      umma_commit(bar(kBarDrain));
-      mbar_wait_drain(bar(kBarDrain), 0);
+      // every MMA this thread issued completes before TMEM is released
+      const uint32_t db = bar(kBarDrain + (s_side ? 0 : 1));
+      umma_commit(db);
+      mbar_wait_drain(db, 0);
     }
     __syncwarp();
   } else {
