@@ -7,14 +7,19 @@
 // L <= 4 drafted tokens.  Per group (sequence b, kv head g) the 8L query rows
 // r = 8 j + h (token j, head h) sit in the first lanes of a 128-row tile:
 //   S = Q K_ring^T             tcgen05 SS, M = 128 rows, N = 128 slots, K = 128
-//   new-key scores             CUDA cores (warps 1..3 of the warpgroup)
+//   S_new = Q K_new^T          tcgen05 SS, N = 16 (the L <= 4 drafted keys,
+//                              rows L..15 zero), into the first 16 columns of
+//                              the warpgroup's O buffer, which are free from
+//                              the output of group k - 2 to the PV of group k
 //   O = P_ring V_ring + P_new V_new
 //                              tcgen05 TS: P (bf16) written over S in TMEM,
 //                              V MN-major; the new values as one K = 16 step
 // Thread = row: lane r of the warpgroup's first warp reads its 128 slot scores
-// and the new-key scores and runs the sink-seeded softmax alone (as the
+// and its new-key scores and runs the sink-seeded softmax alone (as the
 // global-attention kernel does per key block), so no reduction crosses lanes.
-// The rows past 8L are padding that no one reads.
+// The rows past 8L are padding that no one reads.  (Scoring the new keys on
+// the CUDA cores instead, as 128-long FMA chains on three warps, put ~1700
+// cycles per group on the softmax's critical path.)
 //
 // Masks.  Slot s holds position p(s) = (pos-1) - ((pos-1-s) mod W).  Once
 // pos >= W the ring is full and row j's window [pos+j-W+1, pos+j] leaves out
@@ -28,8 +33,9 @@
 // that waiting for a stage to land never delays the PV of the group before
 // it and the release of its stage), two warpgroups on alternate groups, each
 // with its own S / O pair in TMEM: S_w [256 w, 256 w + 128), O_w [256 w +
-// 128, 256 w + 256).  S of group k overwrites P of group k - 2, so it is
-// issued once that group's PV has completed.
+// 128, 256 w + 256).  S of group k overwrites P of group k - 2, and S_new
+// overwrites O of group k - 2, so both are issued once the output of group
+// k - 2 has been read out of TMEM (which follows that group's PV).
 #pragma once
 
 #include "device_common.cuh"
@@ -52,11 +58,10 @@ constexpr int kStageK = 0, kStageV = 2 * kHalf, kStageQ = 4 * kHalf;
 constexpr int kStageKn = 6 * kHalf, kStageVn = kStageKn + 2 * kNewHalf;
 constexpr int kStageBytes = kStageVn + 2 * kNewHalf;   // 104 KB
 constexpr int kOffStage = 0;
-constexpr int kOffSn = kOffStage + (int)kStages * kStageBytes;  // [wg][32 rows][4] floats
-constexpr int kOffBar = kOffSn + 2 * 32 * 4 * 4;
+constexpr int kOffBar = kOffStage + (int)kStages * kStageBytes;
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarSFull = 2 * kStages,
-              kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarSnFull = kBarOFull + 2,
-              kBarDrain = kBarSnFull + 2, kNumBars = kBarDrain + 2;
+              kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarODone = kBarOFull + 2,
+              kBarDrain = kBarODone + 2, kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + w), 1);
       mbar_init(bar(kBarPFull + w), 128);
       mbar_init(bar(kBarOFull + w), 1);
-      mbar_init(bar(kBarSnFull + w), 96);
+      mbar_init(bar(kBarODone + w), 32);
     }
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrain + 1), 1);
@@ -169,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_s = umma_idesc_bf16(kW, false, false);
+      const uint32_t idesc_n = umma_idesc_bf16(kNewRows, false, false);
       const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
       bool ok = true;
       for (int k = 0; ok && k < nk; ++k) {
@@ -181,8 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // S_w holds P of group k - 2 until that group's PV has completed
-          if (k >= 2 && !mbar_wait(bar(kBarOFull + w), (((uint32_t)k >> 1) - 1) & 1,
+          // S_w holds P of group k - 2 until that group's PV has completed, and
+          // O_w its output until the warpgroup has read it (which follows)
+          if (k >= 2 && !mbar_wait(bar(kBarODone + w), (((uint32_t)k >> 1) - 1) & 1,
                                    kErrWaitOFull, abort_flag)) {
             ok = false;
             break;
@@ -190,10 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
           const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
+          const uint64_t kndesc = umma_sdesc(st + kStageKn, 16, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
             umma_bf16_ss(tmem + col_s(w), qdesc + off, kdesc + off, idesc_s, kk > 0);
+          }
+          // S_new = Q K_new^T into O_w columns [0, 16)
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t qoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+            const uint32_t noff = ((kk >> 2) * kNewHalf + (kk & 3) * 32) >> 4;
+            umma_bf16_ss(tmem + col_o(w), qdesc + qoff, kndesc + noff, idesc_n, kk > 0);
           }
           umma_commit(bar(kBarSFull + w));
         } else {
@@ -224,7 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int w = warp >> 2;                       // warpgroup: groups k with k % 2 == w
     const int wq = warp & 3;                       // warp within the warpgroup
-    float* sn = reinterpret_cast<float*>(smem + kOffSn) + w * 128;   // [32 rows][4]
     const int nrow = kG * L;
     if (wq == 0) {
       // ============ softmax + output: thread = row r (TMEM lane r) ============
@@ -239,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kBarSFull + w), ((uint32_t)k >> 1) & 1, kErrWaitSFull, abort_flag))
           break;
         tc_fence_after();
-        uint32_t sr[kW];
+        uint32_t sr[kW], snr[8];
 #pragma unroll
         for (int c = 0; c < kW / 32; ++c) tmem_ld32(s_addr + c * 32, sr + c * 32);
+        tmem_ld8(o_addr, snr);                      // S_new: new keys 0..3 of row r
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < kW / 32; ++c) reg_fence32(sr + c * 32);
+        reg_fence8(snr);
         // ---- mask the ring slots outside row j's window ----
         if (p0 >= kW) {
           const int a0 = (int)(p0 & (kW - 1));     // slot of the oldest position
@@ -278,9 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             m8[e] = max3f(m8[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
         const float mring = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
                                   fmaxf(m8[6], m8[7])) * p.scale_log2;
-        if (!mbar_wait(bar(kBarSnFull + w), ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag))
-          break;
-        const float4 s4 = *reinterpret_cast<const float4*>(sn + 4 * r);
+        // new key i of row j counts when it exists (i < L), is causal (i <= j)
+        // and the sequence is live (pos >= 0)
+        float4 s4;
+        {
+          float sv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            sv[i] = (p0 >= 0 && i < L && i <= j) ? __uint_as_float(snr[i]) * p.scale_log2
+                                                 : -INFINITY;
+          s4 = make_float4(sv[0], sv[1], sv[2], sv[3]);
+        }
         float m = fmaxf(fmaxf(mring, sk), fmaxf(fmaxf(s4.x, s4.y), fmaxf(s4.z, s4.w)));
         if (m == -INFINITY) m = 0.f;                // nothing to attend to
         // ---- weights: bf16 P over S columns [0, 64), new keys at [64, 72) ----
@@ -333,6 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(o_addr + c * 32, o);
           tmem_ld_wait();
           reg_fence32(o);
+          if (c == kD / 32 - 1) {
+            // O_w has been read: S_new of group k + 2 may overwrite it
+            tc_fence_before();
+            mbar_arrive(bar(kBarODone + w));
+          }
           if (r < nrow) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -346,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
       }
     } else {
-      // ============ new-key scores and empty-slot values (warps 1..3) ============
+      // ============ empty-slot values (warps 1..3) ============
       const int t = (wq - 1) * 32 + lane;        // 0 .. 95
       for (int k = w; k < nk; k += 2) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
@@ -354,40 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s = (uint32_t)k % kStages;
         const uint32_t st = sbase + kOffStage + s * kStageBytes;
         const int64_t p0 = p.pos[b];
-        // the stage's Q and new rows come from copies this warp reads
         if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull, abort_flag))
           break;
-        // the scores of group k - 2 must have been read by the softmax warp
-        if (k >= 2 && !mbar_wait(bar(kBarPFull + w), (((uint32_t)k >> 1) - 1) & 1, kErrWaitPFull,
-                                 abort_flag))
-          break;
-        for (int pr = t; pr < 32 * kLmax; pr += 96) {
-          const int r = pr >> 2, i = pr & 3;
-          float v = -INFINITY;
-          if (p0 >= 0 && r < nrow && i < L && i <= (r >> 3)) {
-            float acc = 0.f;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {   // 16 chunks of 8 dims (128-byte swizzle)
-              const uint32_t hoff = (c >> 3);
-              const uint32_t qa = st + kStageQ + hoff * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-              const uint32_t ka = st + kStageKn + hoff * kNewHalf + i * 128 + (((c & 7) ^ (i & 7)) << 4);
-              uint32_t qv[4], kv[4];
-              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                           : "=r"(qv[0]), "=r"(qv[1]), "=r"(qv[2]), "=r"(qv[3]) : "r"(qa));
-              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                           : "=r"(kv[0]), "=r"(kv[1]), "=r"(kv[2]), "=r"(kv[3]) : "r"(ka));
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                acc = fmaf(__uint_as_float(qv[e] << 16), __uint_as_float(kv[e] << 16), acc);
-                acc = fmaf(__uint_as_float(qv[e] & 0xffff0000u),
-                           __uint_as_float(kv[e] & 0xffff0000u), acc);
-              }
-            }
-            v = acc * p.scale_log2;
-          }
-          sn[pr] = v;
-        }
-        mbar_arrive(bar(kBarSnFull + w));
         // empty slots (pos < W): zero their values in the stage before the PV
         if (p0 < kW) {
           for (int sl = t; sl < kW; sl += 96) {
