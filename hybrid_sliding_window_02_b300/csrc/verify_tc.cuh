@@ -28,7 +28,11 @@
 // slots s >= pos are empty (their values are zeroed in shared memory so that
 // 0 * V stays 0) and every column is tested.
 //
-// Persistent CTAs, two stages of K, V, Q and new K / V in flight (TMA), two
+// Persistent CTAs.  The loads go into two rings (TMA): K slots (Q, K ring,
+// K_new), released as soon as S and S_new complete, and V slots (V ring,
+// V_new), released when the PV completes; with whole-group stages only two
+// fitted in shared memory, and the producer spent most of each group waiting
+// for one to be released after its PV.  Two
 // MMA-issuing threads (one for the S products, one for the PV products, so
 // that waiting for a stage to land never delays the PV of the group before
 // it and the release of its stage), two warpgroups on alternate groups, each
@@ -50,16 +54,30 @@ constexpr int kLmax = 4;
 constexpr int kW = 128;
 constexpr int kD = 128;
 constexpr int kNewRows = 16;        // new keys padded to one K = 16 MMA step
-constexpr uint32_t kStages = 2;
 
+// Two rings in shared memory (128-byte swizzle everywhere):
+//   K slots (2): Q [2 halves x 4 KB: 32 rows], K ring [2 x 16 KB],
+//                K_new [2 x 1 KB: 4 rows].  Free once S and S_new complete.
+//   V slots (3): V ring [2 x 16 KB], V_new [2 x 2 KB: 16 rows, rows L..15
+//                zero].  Free once the PV completes.
+// An M = 128 MMA reads 128 rows (16 KB) from each Q half base, and the N = 16
+// S_new MMA reads 16 rows (2 KB) from each K_new half base: the rows past
+// those that hold data fall on later data in shared memory and only feed TMEM
+// lanes or columns that no one reads.
 constexpr int kHalf = 128 * 128;                // 128 rows x 64 bf16 = 16 KB
+constexpr int kQHalf = 32 * 128;                // 32 rows x 64 bf16 = 4 KB
+constexpr int kKnHalf = 8 * 128;                // 8 rows x 64 bf16 = 1 KB
 constexpr int kNewHalf = kNewRows * 128;        // 16 rows x 64 bf16 = 2 KB
-constexpr int kStageK = 0, kStageV = 2 * kHalf, kStageQ = 4 * kHalf;
-constexpr int kStageKn = 6 * kHalf, kStageVn = kStageKn + 2 * kNewHalf;
-constexpr int kStageBytes = kStageVn + 2 * kNewHalf;   // 104 KB
-constexpr int kOffStage = 0;
-constexpr int kOffBar = kOffStage + (int)kStages * kStageBytes;
-constexpr int kBarFull = 0, kBarEmpty = kStages, kBarSFull = 2 * kStages,
+constexpr uint32_t kKSlots = 2, kVSlots = 3;
+constexpr int kKQ = 0, kKK = 2 * kQHalf, kKKn = kKK + 2 * kHalf;
+constexpr int kKSlotBytes = kKKn + 2 * kKnHalf;        // 42 KB
+constexpr int kVV = 0, kVVn = 2 * kHalf;
+constexpr int kVSlotBytes = kVVn + 2 * kNewHalf;       // 36 KB
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + (int)kKSlots * kKSlotBytes;
+constexpr int kOffBar = kOffV + (int)kVSlots * kVSlotBytes;
+constexpr int kBarKFull = 0, kBarKEmpty = kBarKFull + kKSlots, kBarVFull = kBarKEmpty + kKSlots,
+              kBarVEmpty = kBarVFull + kVSlots, kBarSFull = kBarVEmpty + kVSlots,
               kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarODone = kBarOFull + 2,
               kBarDrain = kBarODone + 2, kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -100,9 +118,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (uint32_t s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarFull + s), 1);
-      mbar_init(bar(kBarEmpty + s), 1);
+    for (uint32_t s = 0; s < kKSlots; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+    }
+    for (uint32_t s = 0; s < kVSlots; ++s) {
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(kBarSFull + w), 1);
@@ -114,11 +136,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarDrain + 1), 1);
     fence_mbar_init();
   }
-  // new key / value rows L..15 of both stages are never written by a copy:
-  // zero them once (their weights are 0, and 0 * NaN would not be)
-  for (int i = tid; i < (int)kStages * 4 * kNewHalf / 16; i += kThreads) {
-    const int st = i / (4 * kNewHalf / 16), r = i % (4 * kNewHalf / 16);
-    st_shared_v4(sbase + kOffStage + st * kStageBytes + kStageKn + 16 * r, 0u, 0u, 0u, 0u);
+  // new value rows L..15 of every V slot are never written by a copy: zero
+  // them once (their weights are 0, and 0 * NaN would not be)
+  for (int i = tid; i < (int)kVSlots * 2 * kNewHalf / 16; i += kThreads) {
+    const int sl = i / (2 * kNewHalf / 16), r = i % (2 * kNewHalf / 16);
+    st_shared_v4(sbase + kOffV + sl * kVSlotBytes + kVVn + 16 * r, 0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();
   if (warp == kWarpMma) {
@@ -140,30 +162,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProducer) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      const uint32_t bytes = 4 * kHalf + 2 * (8 * L * 128) + 4 * (L * 128);
-      int k = 0;
-      for (; k < nk; ++k) {
+      const uint32_t kbytes = 2 * kHalf + 2 * (8 * L * 128) + 2 * (L * 128);
+      const uint32_t vbytes = 2 * kHalf + 2 * (L * 128);
+      int nkld = 0, nvld = 0;  // K / V slot loads issued
+      for (int k = 0; k < nk; ++k) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
         const int b = u / p.Hkv, g = u - b * p.Hkv;
-        const uint32_t s = (uint32_t)k % kStages;
-        if (!mbar_wait(bar(kBarEmpty + s), (((uint32_t)k / kStages) & 1) ^ 1, kErrWaitKvEmpty,
+        // K slot: Q, K ring, K_new
+        const uint32_t ks = (uint32_t)k % kKSlots;
+        if (!mbar_wait(bar(kBarKEmpty + ks), (((uint32_t)k / kKSlots) & 1) ^ 1, kErrWaitKvEmpty,
                        abort_flag))
           break;
-        const uint32_t st = sbase + kOffStage + s * kStageBytes;
-        const uint32_t fb = bar(kBarFull + s);
-        mbar_arrive_expect_tx(fb, bytes);
+        const uint32_t kst = sbase + kOffK + ks * kKSlotBytes;
+        const uint32_t kb = bar(kBarKFull + ks);
+        mbar_arrive_expect_tx(kb, kbytes);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          tma_load_4d(st + kStageK + hf * kHalf, &map_k, 64 * hf, u * kW, 0, 0, fb);
-          tma_load_4d(st + kStageV + hf * kHalf, &map_v, 64 * hf, u * kW, 0, 0, fb);
-          tma_load_4d(st + kStageQ + hf * kHalf, &map_q, 64 * hf, g * kG, 0, b, fb);
-          tma_load_4d(st + kStageKn + hf * kNewHalf, &map_kn, 64 * hf, g, 0, b, fb);
-          tma_load_4d(st + kStageVn + hf * kNewHalf, &map_vn, 64 * hf, g, 0, b, fb);
+          tma_load_4d(kst + kKQ + hf * kQHalf, &map_q, 64 * hf, g * kG, 0, b, kb);
+          tma_load_4d(kst + kKK + hf * kHalf, &map_k, 64 * hf, u * kW, 0, 0, kb);
+          tma_load_4d(kst + kKKn + hf * kKnHalf, &map_kn, 64 * hf, g, 0, b, kb);
         }
+        ++nkld;
+        // V slot: V ring, V_new
+        const uint32_t vs = (uint32_t)k % kVSlots;
+        if (!mbar_wait(bar(kBarVEmpty + vs), (((uint32_t)k / kVSlots) & 1) ^ 1, kErrWaitKvEmpty,
+                       abort_flag))
+          break;
+        const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
+        const uint32_t vb = bar(kBarVFull + vs);
+        mbar_arrive_expect_tx(vb, vbytes);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load_4d(vst + kVV + hf * kHalf, &map_v, 64 * hf, u * kW, 0, 0, vb);
+          tma_load_4d(vst + kVVn + hf * kNewHalf, &map_vn, 64 * hf, g, 0, b, vb);
+        }
+        ++nvld;
       }
-      if (k < nk) {
-        for (int j = (k > (int)kStages ? k - (int)kStages : 0); j < k; ++j)
-          mbar_wait_drain(bar(kBarFull + (uint32_t)j % kStages), ((uint32_t)j / kStages) & 1);
+      if (nvld < nk) {
+        // copies still in flight land before the CTA exits
+        for (int j = (nkld > (int)kKSlots ? nkld - (int)kKSlots : 0); j < nkld; ++j)
+          mbar_wait_drain(bar(kBarKFull + (uint32_t)j % kKSlots), ((uint32_t)j / kKSlots) & 1);
+        for (int j = (nvld > (int)kVSlots ? nvld - (int)kVSlots : 0); j < nvld; ++j)
+          mbar_wait_drain(bar(kBarVFull + (uint32_t)j % kVSlots), ((uint32_t)j / kVSlots) & 1);
       }
     }
     __syncwarp();
@@ -178,11 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
       bool ok = true;
       for (int k = 0; ok && k < nk; ++k) {
-        const uint32_t s = (uint32_t)k % kStages;
         const int w = k & 1;
-        const uint32_t st = sbase + kOffStage + s * kStageBytes;
         if (s_side) {
-          if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
+          const uint32_t ks = (uint32_t)k % kKSlots;
+          const uint32_t kst = sbase + kOffK + ks * kKSlotBytes;
+          if (!mbar_wait(bar(kBarKFull + ks), ((uint32_t)k / kKSlots) & 1, kErrWaitKvFull,
                          abort_flag)) {
             ok = false;
             break;
@@ -195,39 +235,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
-          const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
-          const uint64_t kndesc = umma_sdesc(st + kStageKn, 16, 1024, 2);
+          const uint64_t qdesc = umma_sdesc(kst + kKQ, 16, 1024, 2);
+          const uint64_t kdesc = umma_sdesc(kst + kKK, 16, 1024, 2);
+          const uint64_t kndesc = umma_sdesc(kst + kKKn, 16, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-            umma_bf16_ss(tmem + col_s(w), qdesc + off, kdesc + off, idesc_s, kk > 0);
+            const uint32_t qoff = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+            const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+            umma_bf16_ss(tmem + col_s(w), qdesc + qoff, kdesc + koff, idesc_s, kk > 0);
           }
           // S_new = Q K_new^T into O_w columns [0, 16)
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t qoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-            const uint32_t noff = ((kk >> 2) * kNewHalf + (kk & 3) * 32) >> 4;
+            const uint32_t qoff = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+            const uint32_t noff = ((kk >> 2) * kKnHalf + (kk & 3) * 32) >> 4;
             umma_bf16_ss(tmem + col_o(w), qdesc + qoff, kndesc + noff, idesc_n, kk > 0);
           }
           umma_commit(bar(kBarSFull + w));
+          umma_commit(bar(kBarKEmpty + ks));   // Q, K and K_new are no longer read
         } else {
-          // O = P V once the softmax of this group has written P; the stage is
-          // then free (its S completed before that softmax began)
-          if (!mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag)) {
+          // O = P V once the V slot has landed and the softmax of this group
+          // has written P
+          const uint32_t vs = (uint32_t)k % kVSlots;
+          const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
+          if (!mbar_wait(bar(kBarVFull + vs), ((uint32_t)k / kVSlots) & 1, kErrWaitKvFull,
+                         abort_flag) ||
+              !mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
-          const uint64_t vndesc = umma_sdesc(st + kStageVn, kNewHalf, 1024, 2);
+          const uint64_t vdesc = umma_sdesc(vst + kVV, kHalf, 1024, 2);
+          const uint64_t vndesc = umma_sdesc(vst + kVVn, kNewHalf, 1024, 2);
 #pragma unroll
           for (int kb = 0; kb < kW / 16; ++kb)
             umma_bf16_ts(tmem + col_o(w), tmem + col_s(w) + kb * 8,
                          vdesc + (uint32_t)(kb * 16 * 128 >> 4), idesc_o, kb > 0);
           umma_bf16_ts(tmem + col_o(w), tmem + col_s(w) + 64, vndesc, idesc_o, 1u);
           umma_commit(bar(kBarOFull + w));
-          umma_commit(bar(kBarEmpty + s));
+          umma_commit(bar(kBarVEmpty + vs));
         }
       }
       // every MMA this thread issued completes before TMEM is released
@@ -380,16 +426,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = w; k < nk; k += 2) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
         const int b = u / p.Hkv;
-        const uint32_t s = (uint32_t)k % kStages;
-        const uint32_t st = sbase + kOffStage + s * kStageBytes;
+        const uint32_t vs = (uint32_t)k % kVSlots;
+        const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
         const int64_t p0 = p.pos[b];
-        if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull, abort_flag))
+        if (!mbar_wait(bar(kBarVFull + vs), ((uint32_t)k / kVSlots) & 1, kErrWaitKvFull,
+                       abort_flag))
+          break;
+        // P full counts this group's arrivals only once group k - 2's phase
+        // has completed: arriving earlier would complete that phase without
+        // the softmax warp
+        if (k >= 2 && !mbar_wait(bar(kBarPFull + w), (((uint32_t)k >> 1) - 1) & 1, kErrWaitPFull,
+                                 abort_flag))
           break;
         // empty slots (pos < W): zero their values in the stage before the PV
         if (p0 < kW) {
           for (int sl = t; sl < kW; sl += 96) {
             if (sl >= p0) {
-              const uint32_t vrow = st + kStageV + sl * 128;
+              const uint32_t vrow = vst + kVV + sl * 128;
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
                 st_shared_v4(vrow + 16 * c, 0u, 0u, 0u, 0u);
