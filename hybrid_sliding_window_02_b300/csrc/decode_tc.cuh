@@ -16,9 +16,9 @@
 //   S^T = K q^T      M = 128 slots, N = 16 (8 heads + 8 unused), K = 128 dims
 //   O^T = V^T P^T    M = 128 dims (V read MN-major), N = 16, K = 128 slots
 // Persistent CTAs (one per SM) take groups u = blockIdx.x, + gridDim.x, ...;
-// a producer thread keeps three groups' K, V and q in flight through a ring of
-// shared-memory stages (TMA, 128-byte swizzle), so HBM never waits on the
-// math.  Two threads issue the MMAs, one the S^T products and one the O^T
+// a producer thread keeps groups' K and q (two slots, free once S^T is done)
+// and V (four slots, free once the PV is done) in flight through two rings of
+// shared memory (TMA, 128-byte swizzle), so HBM never waits on the math.  Two threads issue the MMAs, one the S^T products and one the O^T
 // products, so that waiting for a stage to land never delays the PV of the
 // group before it (and with it the release of that group's stage).  Two softmax warpgroups take alternate groups: thread = slot reads
 // its 8 head scores from TMEM, the max and the sum over slots are warp-shuffle
@@ -38,20 +38,25 @@ constexpr int kG = 8;              // query heads per kv head
 constexpr int kN = 16;             // MMA N: heads padded to 16
 constexpr int kW = 128;            // ring slots
 constexpr int kD = 128;
-constexpr uint32_t kStages = 3;
 
+// Two rings in shared memory (128-byte swizzle): K slots (2) hold K and q and
+// are free once S^T completes; V slots (4) hold V and are free once the PV
+// completes.  Whole-group stages (68 KB) fitted three times.
+constexpr uint32_t kKSlots = 2, kVSlots = 4;
 constexpr int kHalf = kW * 128;                 // 128 rows x 64 bf16 = 16 KB
 constexpr int kQHalf = kN * 128;                // 16 rows x 64 bf16 = 2 KB
-constexpr int kStageK = 0, kStageV = 2 * kHalf, kStageQ = 4 * kHalf;
-constexpr int kStageBytes = kStageQ + 2 * kQHalf;   // 68 KB
-constexpr int kLoadBytes = kStageBytes;             // bytes one stage's copies deliver
+constexpr int kKK = 0, kKQ = 2 * kHalf;
+constexpr int kKSlotBytes = kKQ + 2 * kQHalf;       // 36 KB
+constexpr int kVSlotBytes = 2 * kHalf;              // 32 KB
 constexpr int kPBytes = 2 * kQHalf;                 // P^T: 16 heads x 128 slots bf16
-constexpr int kOffStage = 0;
-constexpr int kOffP = kOffStage + (int)kStages * kStageBytes;   // 2 buffers (one per warpgroup)
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + (int)kKSlots * kKSlotBytes;
+constexpr int kOffP = kOffV + (int)kVSlots * kVSlotBytes;       // 2 buffers (one per warpgroup)
 constexpr int kOffRed = kOffP + 2 * kPBytes;                    // [wg][warp][head] floats
 constexpr int kRedBytes = 2 * 4 * kG * 4;
 constexpr int kOffBar = kOffRed + 2 * kRedBytes;
-constexpr int kBarFull = 0, kBarEmpty = kStages, kBarSFull = 2 * kStages,
+constexpr int kBarKFull = 0, kBarKEmpty = kBarKFull + kKSlots, kBarVFull = kBarKEmpty + kKSlots,
+              kBarVEmpty = kBarVFull + kVSlots, kBarSFull = kBarVEmpty + kVSlots,
               kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarRed = kBarOFull + 2,
               kBarDrain = kBarRed + 4, kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -107,9 +112,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (uint32_t s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarFull + s), 1);
-      mbar_init(bar(kBarEmpty + s), 1);
+    for (uint32_t s = 0; s < kKSlots; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+    }
+    for (uint32_t s = 0; s < kVSlots; ++s) {
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(kBarSFull + w), 1);
@@ -143,27 +152,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProducer) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      int k = 0;
-      for (; k < nk; ++k) {
+      int nkld = 0, nvld = 0;  // K / V slot loads issued
+      for (int k = 0; k < nk; ++k) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
         const int b = u / p.Hkv, g = u - b * p.Hkv;
-        const uint32_t s = (uint32_t)k % kStages;
-        if (!mbar_wait(bar(kBarEmpty + s), (((uint32_t)k / kStages) & 1) ^ 1, kErrWaitKvEmpty,
+        const uint32_t ks = (uint32_t)k % kKSlots;
+        if (!mbar_wait(bar(kBarKEmpty + ks), (((uint32_t)k / kKSlots) & 1) ^ 1, kErrWaitKvEmpty,
                        abort_flag))
           break;
-        const uint32_t st = sbase + kOffStage + s * kStageBytes;
-        const uint32_t fb = bar(kBarFull + s);
-        mbar_arrive_expect_tx(fb, kLoadBytes);
-        tma_load_4d(st + kStageK, &map_k, 0, u * kW, 0, 0, fb);
-        tma_load_4d(st + kStageK + kHalf, &map_k, 64, u * kW, 0, 0, fb);
-        tma_load_4d(st + kStageV, &map_v, 0, u * kW, 0, 0, fb);
-        tma_load_4d(st + kStageV + kHalf, &map_v, 64, u * kW, 0, 0, fb);
-        tma_load_4d(st + kStageQ, &map_q, 0, b * p.Hq + g * kG, 0, 0, fb);
-        tma_load_4d(st + kStageQ + kQHalf, &map_q, 64, b * p.Hq + g * kG, 0, 0, fb);
+        const uint32_t kst = sbase + kOffK + ks * kKSlotBytes;
+        const uint32_t kb = bar(kBarKFull + ks);
+        mbar_arrive_expect_tx(kb, kKSlotBytes);
+        tma_load_4d(kst + kKK, &map_k, 0, u * kW, 0, 0, kb);
+        tma_load_4d(kst + kKK + kHalf, &map_k, 64, u * kW, 0, 0, kb);
+        tma_load_4d(kst + kKQ, &map_q, 0, b * p.Hq + g * kG, 0, 0, kb);
+        tma_load_4d(kst + kKQ + kQHalf, &map_q, 64, b * p.Hq + g * kG, 0, 0, kb);
+        ++nkld;
+        const uint32_t vs = (uint32_t)k % kVSlots;
+        if (!mbar_wait(bar(kBarVEmpty + vs), (((uint32_t)k / kVSlots) & 1) ^ 1, kErrWaitKvEmpty,
+                       abort_flag))
+          break;
+        const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
+        const uint32_t vb = bar(kBarVFull + vs);
+        mbar_arrive_expect_tx(vb, kVSlotBytes);
+        tma_load_4d(vst, &map_v, 0, u * kW, 0, 0, vb);
+        tma_load_4d(vst + kHalf, &map_v, 64, u * kW, 0, 0, vb);
+        ++nvld;
       }
-      if (k < nk) {  // stopped early: let the copies already issued land
-        for (int j = (k > (int)kStages ? k - (int)kStages : 0); j < k; ++j)
-          mbar_wait_drain(bar(kBarFull + (uint32_t)j % kStages), ((uint32_t)j / kStages) & 1);
+      if (nvld < nk) {  // stopped early: let the copies already issued land
+        for (int j = (nkld > (int)kKSlots ? nkld - (int)kKSlots : 0); j < nkld; ++j)
+          mbar_wait_drain(bar(kBarKFull + (uint32_t)j % kKSlots), ((uint32_t)j / kKSlots) & 1);
+        for (int j = (nvld > (int)kVSlots ? nvld - (int)kVSlots : 0); j < nvld; ++j)
+          mbar_wait_drain(bar(kBarVFull + (uint32_t)j % kVSlots), ((uint32_t)j / kVSlots) & 1);
       }
     }
     __syncwarp();
@@ -177,13 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = umma_idesc_bf16(kN, true, false);
       bool ok = true;
       for (int k = 0; ok && k < nk; ++k) {
-        const uint32_t s = (uint32_t)k % kStages;
         const int w = k & 1;
-        const uint32_t st = sbase + kOffStage + s * kStageBytes;
         if (s_side) {
-          // S^T of group k into TMEM buffer k % 2 once its stage has landed and
+          // S^T of group k into TMEM buffer k % 2 once its K slot has landed and
           // the softmax of group k - 2 has read that buffer (P full)
-          if (!mbar_wait(bar(kBarFull + s), ((uint32_t)k / kStages) & 1, kErrWaitKvFull,
+          const uint32_t ks = (uint32_t)k % kKSlots;
+          const uint32_t kst = sbase + kOffK + ks * kKSlotBytes;
+          if (!mbar_wait(bar(kBarKFull + ks), ((uint32_t)k / kKSlots) & 1, kErrWaitKvFull,
                          abort_flag)) {
             ok = false;
             break;
@@ -194,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t kdesc = umma_sdesc(st + kStageK, 16, 1024, 2);
-          const uint64_t qdesc = umma_sdesc(st + kStageQ, 16, 1024, 2);
+          const uint64_t kdesc = umma_sdesc(kst + kKK, 16, 1024, 2);
+          const uint64_t qdesc = umma_sdesc(kst + kKQ, 16, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t a_off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
@@ -203,15 +223,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16_ss(tmem + col_s(w), kdesc + a_off, qdesc + b_off, idesc_s, kk > 0);
           }
           umma_commit(bar(kBarSFull + w));
+          umma_commit(bar(kBarKEmpty + ks));   // K and q are no longer read
         } else {
-          // O^T = V^T P^T once the softmax of this group has written P^T; the
-          // stage is then free (its S^T completed before that softmax began)
-          if (!mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag)) {
+          // O^T = V^T P^T once the V slot has landed and the softmax of this
+          // group has written P^T
+          const uint32_t vs = (uint32_t)k % kVSlots;
+          const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
+          if (!mbar_wait(bar(kBarVFull + vs), ((uint32_t)k / kVSlots) & 1, kErrWaitKvFull,
+                         abort_flag) ||
+              !mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t vdesc = umma_sdesc(st + kStageV, kHalf, 1024, 2);
+          const uint64_t vdesc = umma_sdesc(vst, kHalf, 1024, 2);
           const uint64_t pdesc = umma_sdesc(sbase + kOffP + w * kPBytes, 16, 1024, 2);
 #pragma unroll
           for (int kb = 0; kb < kW / 16; ++kb) {
@@ -220,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16_ss(tmem + col_o(w), vdesc + a_off, pdesc + b_off, idesc_o, kb > 0);
           }
           umma_commit(bar(kBarOFull + w));
-          umma_commit(bar(kBarEmpty + s));
+          umma_commit(bar(kBarVEmpty + vs));
         }
       }
       // every MMA this thread issued completes before TMEM is released
@@ -248,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = w; k < nk; k += 2) {
       const int u = (int)blockIdx.x + k * (int)gridDim.x;
       const int b = u / p.Hkv, g = u - b * p.Hkv;
-      const uint32_t s = (uint32_t)k % kStages;
+      const uint32_t vs = (uint32_t)k % kVSlots;
       const int64_t pnow = p.pos[b];
       const bool full_ring = pnow >= kW - 1;
       const bool valid = full_ring || (int64_t)t <= pnow;
@@ -295,8 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       __bfloat16_as_ushort(__float2bfloat16_rn(x[h])));
       // empty slots may hold anything (NaN included): zero their values so
       // that 0 * V stays 0 in the MMA
+      // (the V slot is waited for here: S^T needed only the K slot)
+      if (!full_ring &&
+          !mbar_wait(bar(kBarVFull + vs), ((uint32_t)k / kVSlots) & 1, kErrWaitKvFull, abort_flag))
+        break;
       if (!full_ring && !valid) {
-        const uint32_t vrow = sbase + kOffStage + s * kStageBytes + kStageV + t * 128;
+        const uint32_t vrow = sbase + kOffV + vs * kVSlotBytes + t * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           st_shared_v4(vrow + 16 * c, 0u, 0u, 0u, 0u);
