@@ -574,38 +574,31 @@ def bf16_out_line(swa, x, c, steps, dev, stream, peaks):
 
 
 def time_e2e(swa, xh, c, steps, dev, stream):
-    """Host (pinned) inputs -> device -> prefill -> host outputs, every step."""
+    """Host (pinned) inputs -> device -> prefill -> host outputs, every step,
+    through the library's host-buffer call (swa_sink_fwd_host: per sequence,
+    the copies in, the prefill and the copies out, with neighbouring sequences'
+    copies overlapping).  The sink is a resident layer parameter."""
     B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
-    qd = torch.empty_like(xh.q, device=dev)
-    kd = torch.empty_like(xh.k, device=dev)
-    vd = torch.empty_like(xh.v, device=dev)
-    sd = torch.empty_like(xh.sink, device=dev)
-    out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=dev)
-    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
-    out_h = torch.empty(out.shape, dtype=torch.float32, pin_memory=True)
-    lse_h = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
+    sink_d = xh.sink.to(dev)
+    out_h = torch.empty(B, T, Hq, D, dtype=torch.float32, pin_memory=True)
+    lse_h = torch.empty(B, Hq, T, dtype=torch.float32, pin_memory=True)
+    state = {"work": None}
 
     def step():
-        qd.copy_(xh.q, non_blocking=True)
-        kd.copy_(xh.k, non_blocking=True)
-        vd.copy_(xh.v, non_blocking=True)
-        sd.copy_(xh.sink, non_blocking=True)
-        swa.swa_sink_fwd(qd, kd, vd, sd, W, out, lse, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        _, _, state["work"] = swa.swa_sink_fwd_host(xh.q, xh.k, xh.v, sink_d, W, out_h, lse_h,
+                                                    work=state["work"], stream=stream)
 
-    with torch.cuda.stream(stream):
-        step()
+    step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
     torch.cuda.synchronize()
-    h2d = sum(t.numel() * t.element_size() for t in (xh.q, xh.k, xh.v, xh.sink))
-    d2h = out.numel() * 4 + lse.numel() * 4
+    h2d = sum(t.numel() * t.element_size() for t in (xh.q, xh.k, xh.v))
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    del state
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 

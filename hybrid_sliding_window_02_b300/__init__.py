@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
             L.swa_sink_fwd_ex.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
                                           p]
             L.swa_sink_fwd_ex.restype = i32
+            L.swa_sink_fwd_host.argtypes = [p] * 11 + [i32] * 8 + [p]
+            L.swa_sink_fwd_host.restype = i32
             L.swa_sink_decode.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, p]
             L.swa_ring_append.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, p]
             L.swa_sink_verify.argtypes = [p, p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32,
@@ -181,6 +183,67 @@ def swa_sink_fwd(q, k, v, sink, W: int, out=None, lse=None, *, with_lse: bool = 
                                _stream_handle(stream, dev))
     _check("swa_sink_fwd_ex", st)
     return out, lse
+
+
+def swa_sink_fwd_host(q_h, k_h, v_h, sink, W: int, out_h=None, lse_h=None, *, work=None,
+                      with_lse: bool = True, out_dtype=None, stream=None):
+    """Prefill from and to host memory, pipelined per sequence (copies of one
+    sequence overlap the compute of its neighbours).
+
+    q_h [B,T,Hq,D], k_h/v_h [B,T,Hkv,D]: CPU tensors (pin them for overlap);
+    sink [Hq] fp32 on the device.  work: optional tuple of device buffers
+    (q_d, k_d, v_d, out_d, lse_d) of the full sizes, reused across calls;
+    allocated here when omitted.  Returns (out_h, lse_h or None, work).  The
+    host outputs are complete once the stream has been synchronised.
+    """
+    import torch
+    B, T, Hq, D = q_h.shape
+    Hkv = k_h.shape[2]
+    for n, t in (("q_h", q_h), ("k_h", k_h), ("v_h", v_h)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU tensor")
+    if k_h.shape != (B, T, Hkv, D) or v_h.shape != k_h.shape:
+        raise ValueError("k_h and v_h must be [B, T, Hkv, D] matching q_h")
+    if k_h.dtype != q_h.dtype or v_h.dtype != q_h.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if sink.dtype != torch.float32 or sink.shape != (Hq,):
+        raise ValueError("sink must be float32 [Hq]")
+    dev = sink.device
+    _cuda_contig("sink", sink, dev)
+    odt = out_dtype or (out_h.dtype if out_h is not None else torch.float32)
+    pin = q_h.is_pinned()
+    if out_h is None:
+        out_h = torch.empty(B, T, Hq, D, dtype=odt, pin_memory=pin)
+    if with_lse and lse_h is None:
+        lse_h = torch.empty(B, Hq, T, dtype=torch.float32, pin_memory=pin)
+    if out_h.is_cuda or out_h.shape != (B, T, Hq, D) or not out_h.is_contiguous():
+        raise ValueError("out_h must be a contiguous CPU tensor [B, T, Hq, D]")
+    if work is None:
+        work = (torch.empty(q_h.shape, dtype=q_h.dtype, device=dev),
+                torch.empty(k_h.shape, dtype=k_h.dtype, device=dev),
+                torch.empty(v_h.shape, dtype=v_h.dtype, device=dev),
+                torch.empty(out_h.shape, dtype=out_h.dtype, device=dev),
+                torch.empty(B, Hq, T, dtype=torch.float32, device=dev) if lse_h is not None
+                else None)
+    q_d, k_d, v_d, out_d, lse_d = work
+    for n, t, ref in (("q_d", q_d, q_h), ("k_d", k_d, k_h), ("v_d", v_d, v_h),
+                      ("out_d", out_d, out_h)):
+        _cuda_contig(n, t, dev)
+        if t.shape != ref.shape or t.dtype != ref.dtype:
+            raise ValueError(f"{n} must match {tuple(ref.shape)} {ref.dtype}")
+    if (lse_h is None) != (lse_d is None):
+        raise ValueError("lse_h and lse_d go together")
+    if lse_d is not None:
+        _cuda_contig("lse_d", lse_d, dev)
+    st = lib().swa_sink_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), sink.data_ptr(),
+                                 out_h.data_ptr(),
+                                 lse_h.data_ptr() if lse_h is not None else None,
+                                 q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(), out_d.data_ptr(),
+                                 lse_d.data_ptr() if lse_d is not None else None,
+                                 B, T, Hq, Hkv, D, int(W), _dtype_code(q_h), _dtype_code(out_h),
+                                 _stream_handle(stream, dev))
+    _check("swa_sink_fwd_host", st)
+    return out_h, lse_h, work
 
 
 def swa_sink_decode(q, k_ring, v_ring, pos, sink, out=None, lse=None, *, with_lse=True,

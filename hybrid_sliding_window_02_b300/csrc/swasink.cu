@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/swasink.h"
 #include "decode.cuh"
@@ -485,6 +486,112 @@ swa_status swa_sink_fwd(const void* q, const void* k, const void* v, const float
                         float* out, float* lse, int B, int T, int Hq, int Hkv, int D, int W,
                         swa_dtype in_dtype, void* stream) {
   return swa_sink_fwd_ex(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, in_dtype, SWA_F32, stream);
+}
+
+// ---- prefill from and to host memory: per-sequence copy / compute / copy ----
+namespace {
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  std::vector<cudaEvent_t> ev;   // [0] start, [1] end, then per sequence: in, computed
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+bool pipe_events(HostPipe& hp, size_t n) {
+  while (hp.ev.size() < n) {
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (r != cudaSuccess) {
+      set_cuda_error("cudaEventCreateWithFlags", r);
+      return false;
+    }
+    hp.ev.push_back(e);
+  }
+  return true;
+}
+
+bool pipe_ready(HostPipe& hp) {
+  if (hp.ready) return true;
+  cudaError_t r = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
+  if (r == cudaSuccess) r = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+  if (r != cudaSuccess) {
+    set_cuda_error("cudaStreamCreateWithFlags", r);
+    return false;
+  }
+  hp.ready = true;
+  return true;
+}
+
+swa_status cuda_ok(cudaError_t r, const char* what) {
+  if (r == cudaSuccess) return SWA_OK;
+  set_cuda_error(what, r);
+  return SWA_ECUDA;
+}
+}  // namespace
+
+swa_status swa_sink_fwd_host(const void* q_h, const void* k_h, const void* v_h,
+                             const float* sink, void* out_h, float* lse_h, void* q_d,
+                             void* k_d, void* v_d, void* out_d, float* lse_d, int B, int T,
+                             int Hq, int Hkv, int D, int W, swa_dtype in_dtype,
+                             swa_dtype out_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q_h || !k_h || !v_h || !out_h || !q_d || !k_d || !v_d || !out_d || !sink)
+    return SWA_EINVAL;
+  if ((lse_h == nullptr) != (lse_d == nullptr)) return SWA_EINVAL;
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return SWA_EINVAL;
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
+  if (out_dtype != SWA_F32 && out_dtype != SWA_BF16) return SWA_EINVAL;
+  const size_t ie = in_dtype == SWA_BF16 ? 2 : 4, oe = out_dtype == SWA_BF16 ? 2 : 4;
+  const size_t q_seq = (size_t)T * Hq * D * ie, kv_seq = (size_t)T * Hkv * D * ie;
+  const size_t o_seq = (size_t)T * Hq * D * oe, l_seq = (size_t)Hq * T * 4;
+  // every per-sequence device pointer must keep the 16-byte alignment of its base
+  if (q_seq % 16 || kv_seq % 16 || o_seq % 16 || (lse_d && l_seq % 16)) return SWA_EINVAL;
+  int dev;
+  if (!current_device(&dev)) return SWA_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe& hp = g_pipe[dev];
+  if (!pipe_ready(hp) || !pipe_events(hp, 2 + 2 * (size_t)B)) return SWA_ECUDA;
+  cudaEvent_t ev_start = hp.ev[0], ev_end = hp.ev[1];
+  swa_status rc = cuda_ok(cudaEventRecord(ev_start, st), "cudaEventRecord");
+  if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(hp.h2d, ev_start, 0), "cudaStreamWaitEvent");
+  auto at = [](const void* base, size_t off) {
+    return const_cast<char*>(static_cast<const char*>(base)) + off;
+  };
+  for (int b = 0; rc == SWA_OK && b < B; ++b) {
+    cudaEvent_t ev_in = hp.ev[2 + 2 * b], ev_c = hp.ev[3 + 2 * b];
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    rc = cuda_ok(cudaMemcpyAsync(at(q_d, b * q_seq), at(q_h, b * q_seq), q_seq, h2d, hp.h2d),
+                 "cudaMemcpyAsync(q)");
+    if (rc == SWA_OK)
+      rc = cuda_ok(cudaMemcpyAsync(at(k_d, b * kv_seq), at(k_h, b * kv_seq), kv_seq, h2d, hp.h2d),
+                   "cudaMemcpyAsync(k)");
+    if (rc == SWA_OK)
+      rc = cuda_ok(cudaMemcpyAsync(at(v_d, b * kv_seq), at(v_h, b * kv_seq), kv_seq, h2d, hp.h2d),
+                   "cudaMemcpyAsync(v)");
+    if (rc == SWA_OK) rc = cuda_ok(cudaEventRecord(ev_in, hp.h2d), "cudaEventRecord");
+    if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(st, ev_in, 0), "cudaStreamWaitEvent");
+    if (rc == SWA_OK)
+      rc = swa_sink_fwd_ex(at(q_d, b * q_seq), at(k_d, b * kv_seq), at(v_d, b * kv_seq), sink,
+                           at(out_d, b * o_seq),
+                           lse_d ? reinterpret_cast<float*>(at(lse_d, b * l_seq)) : nullptr, 1, T,
+                           Hq, Hkv, D, W, in_dtype, out_dtype, stream);
+    if (rc == SWA_OK) rc = cuda_ok(cudaEventRecord(ev_c, st), "cudaEventRecord");
+    if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(hp.d2h, ev_c, 0), "cudaStreamWaitEvent");
+    if (rc == SWA_OK)
+      rc = cuda_ok(cudaMemcpyAsync(at(out_h, b * o_seq), at(out_d, b * o_seq), o_seq, d2h, hp.d2h),
+                   "cudaMemcpyAsync(out)");
+    if (rc == SWA_OK && lse_d)
+      rc = cuda_ok(cudaMemcpyAsync(at(lse_h, b * l_seq), at(lse_d, b * l_seq), l_seq, d2h, hp.d2h),
+                   "cudaMemcpyAsync(lse)");
+  }
+  // later work on `stream` follows every copy enqueued above, even after an error
+  const swa_status rc_end = cuda_ok(cudaEventRecord(ev_end, hp.d2h), "cudaEventRecord");
+  const swa_status rc_wait =
+      rc_end == SWA_OK ? cuda_ok(cudaStreamWaitEvent(st, ev_end, 0), "cudaStreamWaitEvent")
+                       : rc_end;
+  return rc != SWA_OK ? rc : rc_wait;
 }
 
 swa_status swa_sink_decode(const void* q, const void* k_ring, const void* v_ring,

@@ -80,6 +80,37 @@ swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const fl
                            swa_dtype in_dtype, swa_dtype out_dtype, void* stream);
 
 /*
+ * swa_sink_fwd_host -- swa_sink_fwd_ex with q, k, v taken from HOST memory and
+ * out, lse written to HOST memory, one sequence at a time: the inputs of
+ * sequence b are copied to the device, its prefill runs, and its outputs are
+ * copied back, while the copies of the neighbouring sequences run at the same
+ * time (host-to-device on one stream, the prefill on `stream`, device-to-host
+ * on another; each sequence's steps are chained by events).
+ *   q_h, k_h, v_h       host, layouts as swa_sink_fwd; pinned (page-locked)
+ *                       memory lets the copies overlap, pageable memory works
+ *                       but the copies then serialise with the host
+ *   sink                DEVICE [Hq] float32 (a layer parameter, resident)
+ *   out_h, lse_h        host outputs (lse_h may be NULL, then lse_d too)
+ *   q_d, k_d, v_d, out_d, lse_d
+ *                       device buffers of the full sizes of q, k, v, out and
+ *                       lse, owned by the caller (the library allocates no
+ *                       memory); they hold the data in transit
+ * The call is asynchronous with respect to the host, like the others: it is
+ * ordered after earlier work on `stream`, later work on `stream` sees the
+ * copies to the host completed, and out_h / lse_h may be read once `stream`
+ * has been synchronised.  The library keeps two CUDA streams and a set of
+ * events per device for these calls (created on first use); calls from
+ * several host threads are serialised while they enqueue.  Argument rules and
+ * return values are those of swa_sink_fwd_ex; on SWA_ECUDA part of the work
+ * may have been enqueued, and later work on `stream` still follows it.
+ */
+swa_status swa_sink_fwd_host(const void* q_h, const void* k_h, const void* v_h,
+                             const float* sink, void* out_h, float* lse_h, void* q_d,
+                             void* k_d, void* v_d, void* out_d, float* lse_d, int B, int T,
+                             int Hq, int Hkv, int D, int W, swa_dtype in_dtype,
+                             swa_dtype out_dtype, void* stream);
+
+/*
  * swa_sink_decode -- one query token per sequence against a W-slot ring cache
  * ("pwwt.cn" MiMo-V2-Flash essay, section 1.1: the sliding-window KV cache has
  * a fixed size, O(W) memory; ICML 2026 talk write-up, Q&A K: positions keep

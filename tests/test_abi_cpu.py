@@ -195,3 +195,15 @@ def test_high_sparse_calls_reject_before_launch(L):
     assert L.swa_sink_sparse_fwd(A, A, A, A, A, A, A, 1, 1024, 8, 1, 128, 16, 4, 1, 0, None) == -2
     assert L.swa_sink_sparse_fwd(A, A, A, A, None, A, A, 1, 1024, 8, 1, 128, 64, 4, 1, 0,
                                  None) == -1
+
+
+def test_fwd_host_rejects_before_launch(L):
+    # q_h k_h v_h sink out_h lse_h | q_d k_d v_d out_d lse_d | B T Hq Hkv D W in out
+    ok = (A, A, A, A, A, A, A, A, A, A, A, 2, 16, 8, 1, 128, 4, 1, 0)
+    assert L.swa_sink_fwd_host(*ok[:4], None, *ok[5:], None) == -1        # no out_h
+    assert L.swa_sink_fwd_host(*ok[:10], None, *ok[11:], None) == -1      # lse_h without lse_d
+    assert L.swa_sink_fwd_host(*ok[:5], None, *ok[6:], None) == -1        # lse_d without lse_h
+    assert L.swa_sink_fwd_host(*ok[:14], 3, *ok[15:], None) == -1         # Hq % Hkv != 0
+    assert L.swa_sink_fwd_host(*ok[:17], 7, ok[18], None) == -1           # unknown input dtype
+    # a sequence's fp32 lse slab (Hq * T * 4 bytes) must keep 16-byte alignment
+    assert L.swa_sink_fwd_host(*ok[:12], 1, 1, *ok[14:], None) == -1

@@ -1,0 +1,77 @@
+"""swa_sink_fwd_host (prefill from and to host memory, pipelined per sequence)
+against the device-buffer call and the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import hybrid_sliding_window_02_b300 as swa
+from hybrid_sliding_window_02_b300 import inputs as gen
+from gpu_helpers import assert_bf16_close, assert_lse_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_call(x, W, out_dtype=torch.float32):
+    out, lse = swa.swa_sink_fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), x.sink.cuda(), W,
+                                out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", [(3, 300, 16, 2, 128), (2, 1000, 8, 1, 1000),
+                                          (1, 77, 8, 1, 128)])
+def test_host_call_equals_device_call(cuda_ok, pinned, B, T, Hq, Hkv, W):
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=B + T)
+    q, k, v = (t.pin_memory() if pinned else t.clone() for t in (x.q, x.k, x.v))
+    out_h, lse_h, _ = swa.swa_sink_fwd_host(q, k, v, x.sink.cuda(), W)
+    torch.cuda.synchronize()
+    out_d, lse_d = _device_call(x, W)
+    assert torch.equal(out_h, out_d)
+    assert torch.equal(lse_h, lse_d)
+
+
+def test_host_call_matches_oracle_and_reuses_work(cuda_ok):
+    x = gen.prefill_inputs(2, 400, 16, 2, 128, seed=3)
+    q, k, v = (t.pin_memory() for t in (x.q, x.k, x.v))
+    sink = x.sink.cuda()
+    out_h, lse_h, work = swa.swa_sink_fwd_host(q, k, v, sink, 128)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.swa_sink_fwd(x.q, x.k, x.v, x.sink, 128)
+    assert_bf16_close(out_h.double().numpy(), o_ref)
+    assert_lse_close(lse_h.double().numpy(), l_ref)
+    # a second call through the same device buffers, with other inputs
+    y = gen.prefill_inputs(2, 400, 16, 2, 128, seed=4)
+    q2, k2, v2 = (t.pin_memory() for t in (y.q, y.k, y.v))
+    out2, lse2, _ = swa.swa_sink_fwd_host(q2, k2, v2, y.sink.cuda(), 128, work=work)
+    torch.cuda.synchronize()
+    o2, l2 = _device_call(y, 128)
+    assert torch.equal(out2, o2) and torch.equal(lse2, l2)
+
+
+def test_host_call_without_lse_and_bf16_output(cuda_ok):
+    x = gen.prefill_inputs(3, 256, 16, 2, 128, seed=5)
+    q, k, v = (t.pin_memory() for t in (x.q, x.k, x.v))
+    out_h, lse_h, _ = swa.swa_sink_fwd_host(q, k, v, x.sink.cuda(), 128, with_lse=False,
+                                            out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert lse_h is None and out_h.dtype == torch.bfloat16
+    out_d, _ = _device_call(x, 128, out_dtype=torch.bfloat16)
+    assert torch.equal(out_h, out_d)
+
+
+def test_host_call_orders_with_the_stream(cuda_ok):
+    # work enqueued on the same stream after the call sees the copies completed
+    x = gen.prefill_inputs(2, 300, 16, 2, 128, seed=6)
+    q, k, v = (t.pin_memory() for t in (x.q, x.k, x.v))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out_h, lse_h, work = swa.swa_sink_fwd_host(q, k, v, x.sink.cuda(), 128, stream=s)
+        flag = torch.ones(1, device="cuda")
+        flag_h = flag.to("cpu", non_blocking=True)
+    s.synchronize()
+    out_d, lse_d = _device_call(x, 128)
+    assert flag_h.item() == 1.0
+    assert torch.equal(out_h, out_d) and torch.equal(lse_h, lse_d)
+    assert swa.device_error() == 0
