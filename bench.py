@@ -228,11 +228,37 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def source_code_only(text: str) -> str:
+    """C/CUDA source with comments and whitespace removed (string literals kept):
+    what the traffic of a kernel depends on, so that editing a comment does not
+    retire a recorded measurement."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "hybrid_sliding_window_02_b300", rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "hybrid_sliding_window_02_b300", rel), encoding="utf-8") as f:
+            h.update(source_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

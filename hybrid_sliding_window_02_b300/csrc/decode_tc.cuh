@@ -18,13 +18,15 @@
 // Persistent CTAs (one per SM) take groups u = blockIdx.x, + gridDim.x, ...;
 // a producer thread keeps groups' K and q (two slots, free once S^T is done)
 // and V (four slots, free once the PV is done) in flight through two rings of
-// shared memory (TMA, 128-byte swizzle), so HBM never waits on the math.  Two threads issue the MMAs, one the S^T products and one the O^T
-// products, so that waiting for a stage to land never delays the PV of the
-// group before it (and with it the release of that group's stage).  Two softmax warpgroups take alternate groups: thread = slot reads
-// its 8 head scores from TMEM, the max and the sum over slots are warp-shuffle
-// reductions finished across the four warps in shared memory, the bf16 P^T
-// goes to shared memory for the second MMA, and after it thread = dim reads
-// O^T from TMEM and writes out[b, h, dim] (each warp 128 contiguous bytes).
+// shared memory (TMA, 128-byte swizzle), so HBM never waits on the math.  Two
+// threads issue the MMAs, one the S^T products and one the O^T products, so
+// that waiting for a group's K slot to land never delays the PV of the group
+// before it (and with it the release of that group's V slot).  Two softmax
+// warpgroups take alternate groups: thread = slot reads its 8 head scores
+// from TMEM, the max and the sum over slots are warp-shuffle reductions
+// finished across the four warps in shared memory, the bf16 P^T goes to
+// shared memory for the second MMA, and after it thread = dim reads O^T from
+// TMEM and writes out[b, h, dim] (each warp 128 contiguous bytes).
 #pragma once
 
 #include "device_common.cuh"
@@ -189,8 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpMma || warp == kWarpPv) {
     // ====== MMA issuers: S^T of every group (warp 9), O^T of every group (warp 10) ======
-    // Two threads, so that the wait for a group's stage to land (S side) never
-    // holds back the PV of the group before it and the release of its stage.
+    // Two threads, so that the wait for a group's K slot to land (S side)
+    // never holds back the PV of the group before it and the release of its
+    // V slot.
     if (lane == 0) {
       const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_s = umma_idesc_bf16(kN, false, false);

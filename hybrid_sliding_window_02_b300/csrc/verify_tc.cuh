@@ -7,8 +7,8 @@
 // L <= 4 drafted tokens.  Per group (sequence b, kv head g) the 8L query rows
 // r = 8 j + h (token j, head h) sit in the first lanes of a 128-row tile:
 //   S = Q K_ring^T             tcgen05 SS, M = 128 rows, N = 128 slots, K = 128
-//   S_new = Q K_new^T          tcgen05 SS, N = 16 (the L <= 4 drafted keys,
-//                              rows L..15 zero), into the first 16 columns of
+//   S_new = Q K_new^T          tcgen05 SS, N = 16 (the L <= 4 drafted keys;
+//                              columns L..15 are masked), into the first 16 columns of
 //                              the warpgroup's O buffer, which are free from
 //                              the output of group k - 2 to the PV of group k
 //   O = P_ring V_ring + P_new V_new
@@ -32,14 +32,14 @@
 // K_new), released as soon as S and S_new complete, and V slots (V ring,
 // V_new), released when the PV completes; with whole-group stages only two
 // fitted in shared memory, and the producer spent most of each group waiting
-// for one to be released after its PV.  Two
-// MMA-issuing threads (one for the S products, one for the PV products, so
-// that waiting for a stage to land never delays the PV of the group before
-// it and the release of its stage), two warpgroups on alternate groups, each
-// with its own S / O pair in TMEM: S_w [256 w, 256 w + 128), O_w [256 w +
-// 128, 256 w + 256).  S of group k overwrites P of group k - 2, and S_new
-// overwrites O of group k - 2, so both are issued once the output of group
-// k - 2 has been read out of TMEM (which follows that group's PV).
+// for one to be released after its PV.  Two MMA-issuing threads (one for the
+// S products, one for the PV products, so that waiting for a K slot to land
+// never delays the PV of the group before it and the release of its V slot),
+// two warpgroups on alternate groups, each with its own S / O pair in TMEM:
+// S_w [256 w, 256 w + 128), O_w [256 w + 128, 256 w + 256).  S of group k
+// overwrites P of group k - 2, and S_new overwrites O of group k - 2, so both
+// are issued once the output of group k - 2 has been read out of TMEM (which
+// follows that group's PV).
 #pragma once
 
 #include "device_common.cuh"
@@ -209,8 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpMma || warp == kWarpPv) {
     // ====== MMA issuers: S of every group (warp 9), O of every group (warp 10) ======
-    // Two threads, so that the wait for a group's stage to land (S side) never
-    // holds back the PV of the group before it and the release of its stage.
+    // Two threads, so that the wait for a group's K slot to land (S side)
+    // never holds back the PV of the group before it and the release of its
+    // V slot.
     if (lane == 0) {
       const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_s = umma_idesc_bf16(kW, false, false);
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (k >= 2 && !mbar_wait(bar(kBarPFull + w), (((uint32_t)k >> 1) - 1) & 1, kErrWaitPFull,
                                  abort_flag))
           break;
-        // empty slots (pos < W): zero their values in the stage before the PV
+        // empty slots (pos < W): zero their values in the V slot before the PV
         if (p0 < kW) {
           for (int sl = t; sl < kW; sl += 96) {
             if (sl >= p0) {

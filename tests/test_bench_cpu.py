@@ -34,3 +34,20 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_source_hash_ignores_comments_and_whitespace():
+    import bench
+    a = 'int f(int x) {\n  return x + 1;  // one\n}\n/* block */ const char* s = "a // b /* c */";\n'
+    b = 'int f(int x){return x+1;}\nconst char* s = "a // b /* c */";'
+    c = 'int f(int x) { return x + 2; }\nconst char* s = "a // b /* c */";'
+    assert bench.source_code_only(a) == bench.source_code_only(b)
+    assert bench.source_code_only(a) != bench.source_code_only(c)
+    assert '"a // b /* c */"' in bench.source_code_only(a)
+
+
+def test_recorded_traffic_matches_current_sources():
+    # every traffic record in profiles/ was taken from the code as it stands
+    import bench
+    for k in bench.KERNEL_SOURCES:
+        assert bench.recorded_traffic(k) is not None, k
