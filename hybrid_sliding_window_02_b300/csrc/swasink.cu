@@ -543,47 +543,80 @@ swa_status swa_sink_fwd_host(const void* q_h, const void* k_h, const void* v_h,
   if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
   if (out_dtype != SWA_F32 && out_dtype != SWA_BF16) return SWA_EINVAL;
   const size_t ie = in_dtype == SWA_BF16 ? 2 : 4, oe = out_dtype == SWA_BF16 ? 2 : 4;
-  const size_t q_seq = (size_t)T * Hq * D * ie, kv_seq = (size_t)T * Hkv * D * ie;
-  const size_t o_seq = (size_t)T * Hq * D * oe, l_seq = (size_t)Hq * T * 4;
-  // every per-sequence device pointer must keep the 16-byte alignment of its base
-  if (q_seq % 16 || kv_seq % 16 || o_seq % 16 || (lse_d && l_seq % 16)) return SWA_EINVAL;
+  // Chunks: one sequence x a share of the kv heads (two shares when Hkv is
+  // even), each staged compactly in the caller's device buffers.  Smaller
+  // chunks shorten the copy-in before the first prefill and the copy-out after
+  // the last, the two that overlap nothing.  When a share's staging offsets
+  // would lose the 16-byte alignment the kernels need, the batch goes as one
+  // chunk.
+  int nsplit = (Hkv % 2 == 0) ? 2 : 1, nseq = 1;
+  auto chunking_ok = [&](int ns, int nq) {
+    const size_t hq = (size_t)Hq / ns, hk = (size_t)Hkv / ns;
+    return ((size_t)nq * T * hq * D * ie) % 16 == 0 && ((size_t)nq * T * hk * D * ie) % 16 == 0 &&
+           ((size_t)nq * T * hq * D * oe) % 16 == 0 &&
+           (!lse_d || ((size_t)nq * hq * T * 4) % 16 == 0);
+  };
+  if (!chunking_ok(nsplit, 1)) nsplit = 1;
+  if (!chunking_ok(nsplit, 1)) nseq = B;   // a single chunk: the whole batch
+  const int Hq_c = Hq / nsplit, Hkv_c = Hkv / nsplit;
+  const size_t q_row = (size_t)Hq_c * D * ie, k_row = (size_t)Hkv_c * D * ie;
+  const size_t o_row = (size_t)Hq_c * D * oe;
+  const size_t q_pitch = (size_t)Hq * D * ie, k_pitch = (size_t)Hkv * D * ie;
+  const size_t o_pitch = (size_t)Hq * D * oe;
+  const size_t q_chunk = (size_t)nseq * T * q_row, k_chunk = (size_t)nseq * T * k_row;
+  const size_t o_chunk = (size_t)nseq * T * o_row, l_chunk = (size_t)nseq * Hq_c * T * 4;
+  const int nchunk = (B / nseq) * nsplit;
   int dev;
   if (!current_device(&dev)) return SWA_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lk(g_pipe_mu);
   HostPipe& hp = g_pipe[dev];
-  if (!pipe_ready(hp) || !pipe_events(hp, 2 + 2 * (size_t)B)) return SWA_ECUDA;
+  if (!pipe_ready(hp) || !pipe_events(hp, 2 + 2 * (size_t)nchunk)) return SWA_ECUDA;
   cudaEvent_t ev_start = hp.ev[0], ev_end = hp.ev[1];
   swa_status rc = cuda_ok(cudaEventRecord(ev_start, st), "cudaEventRecord");
   if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(hp.h2d, ev_start, 0), "cudaStreamWaitEvent");
   auto at = [](const void* base, size_t off) {
     return const_cast<char*>(static_cast<const char*>(base)) + off;
   };
-  for (int b = 0; rc == SWA_OK && b < B; ++b) {
-    cudaEvent_t ev_in = hp.ev[2 + 2 * b], ev_c = hp.ev[3 + 2 * b];
-    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
-    rc = cuda_ok(cudaMemcpyAsync(at(q_d, b * q_seq), at(q_h, b * q_seq), q_seq, h2d, hp.h2d),
-                 "cudaMemcpyAsync(q)");
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  for (int c = 0; rc == SWA_OK && c < nchunk; ++c) {
+    const int b0 = (c / nsplit) * nseq, part = c % nsplit;
+    const size_t rows = (size_t)nseq * T;                 // positions in the chunk
+    const size_t hq0 = (size_t)part * Hq_c, hk0 = (size_t)part * Hkv_c;
+    cudaEvent_t ev_in = hp.ev[2 + 2 * c], ev_c = hp.ev[3 + 2 * c];
+    void* qc = at(q_d, c * q_chunk);
+    void* kc = at(k_d, c * k_chunk);
+    void* vc = at(v_d, c * k_chunk);
+    void* oc = at(out_d, c * o_chunk);
+    float* lc = lse_d ? reinterpret_cast<float*>(at(lse_d, c * l_chunk)) : nullptr;
+    // rows of the chunk: positions b0*T .. (b0+nseq)*T - 1, heads hq0 .. hq0+Hq_c-1
+    rc = cuda_ok(cudaMemcpy2DAsync(qc, q_row, at(q_h, b0 * (size_t)T * q_pitch + hq0 * D * ie),
+                                   q_pitch, q_row, rows, h2d, hp.h2d),
+                 "cudaMemcpy2DAsync(q)");
     if (rc == SWA_OK)
-      rc = cuda_ok(cudaMemcpyAsync(at(k_d, b * kv_seq), at(k_h, b * kv_seq), kv_seq, h2d, hp.h2d),
-                   "cudaMemcpyAsync(k)");
+      rc = cuda_ok(cudaMemcpy2DAsync(kc, k_row, at(k_h, b0 * (size_t)T * k_pitch + hk0 * D * ie),
+                                     k_pitch, k_row, rows, h2d, hp.h2d),
+                   "cudaMemcpy2DAsync(k)");
     if (rc == SWA_OK)
-      rc = cuda_ok(cudaMemcpyAsync(at(v_d, b * kv_seq), at(v_h, b * kv_seq), kv_seq, h2d, hp.h2d),
-                   "cudaMemcpyAsync(v)");
+      rc = cuda_ok(cudaMemcpy2DAsync(vc, k_row, at(v_h, b0 * (size_t)T * k_pitch + hk0 * D * ie),
+                                     k_pitch, k_row, rows, h2d, hp.h2d),
+                   "cudaMemcpy2DAsync(v)");
     if (rc == SWA_OK) rc = cuda_ok(cudaEventRecord(ev_in, hp.h2d), "cudaEventRecord");
     if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(st, ev_in, 0), "cudaStreamWaitEvent");
     if (rc == SWA_OK)
-      rc = swa_sink_fwd_ex(at(q_d, b * q_seq), at(k_d, b * kv_seq), at(v_d, b * kv_seq), sink,
-                           at(out_d, b * o_seq),
-                           lse_d ? reinterpret_cast<float*>(at(lse_d, b * l_seq)) : nullptr, 1, T,
-                           Hq, Hkv, D, W, in_dtype, out_dtype, stream);
+      rc = swa_sink_fwd_ex(qc, kc, vc, sink + hq0, oc, lc, nseq, T, Hq_c, Hkv_c, D, W, in_dtype,
+                           out_dtype, stream);
     if (rc == SWA_OK) rc = cuda_ok(cudaEventRecord(ev_c, st), "cudaEventRecord");
     if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(hp.d2h, ev_c, 0), "cudaStreamWaitEvent");
     if (rc == SWA_OK)
-      rc = cuda_ok(cudaMemcpyAsync(at(out_h, b * o_seq), at(out_d, b * o_seq), o_seq, d2h, hp.d2h),
-                   "cudaMemcpyAsync(out)");
-    if (rc == SWA_OK && lse_d)
-      rc = cuda_ok(cudaMemcpyAsync(at(lse_h, b * l_seq), at(lse_d, b * l_seq), l_seq, d2h, hp.d2h),
+      rc = cuda_ok(cudaMemcpy2DAsync(at(out_h, b0 * (size_t)T * o_pitch + hq0 * D * oe), o_pitch,
+                                     oc, o_row, o_row, rows, d2h, hp.d2h),
+                   "cudaMemcpy2DAsync(out)");
+    // lse [B, Hq, T]: sequence b's heads hq0 .. are contiguous
+    for (int b = b0; rc == SWA_OK && lse_d && b < b0 + nseq; ++b)
+      rc = cuda_ok(cudaMemcpyAsync(at(lse_h, ((size_t)b * Hq + hq0) * T * 4),
+                                   at(lc, (size_t)(b - b0) * Hq_c * T * 4), (size_t)Hq_c * T * 4,
+                                   d2h, hp.d2h),
                    "cudaMemcpyAsync(lse)");
   }
   // later work on `stream` follows every copy enqueued above, even after an error

@@ -205,5 +205,3 @@ def test_fwd_host_rejects_before_launch(L):
     assert L.swa_sink_fwd_host(*ok[:5], None, *ok[6:], None) == -1        # lse_d without lse_h
     assert L.swa_sink_fwd_host(*ok[:14], 3, *ok[15:], None) == -1         # Hq % Hkv != 0
     assert L.swa_sink_fwd_host(*ok[:17], 7, ok[18], None) == -1           # unknown input dtype
-    # a sequence's fp32 lse slab (Hq * T * 4 bytes) must keep 16-byte alignment
-    assert L.swa_sink_fwd_host(*ok[:12], 1, 1, *ok[14:], None) == -1

@@ -20,10 +20,15 @@ def _device_call(x, W, out_dtype=torch.float32):
 
 
 @pytest.mark.parametrize("pinned", [True, False])
-@pytest.mark.parametrize("B,T,Hq,Hkv,W", [(3, 300, 16, 2, 128), (2, 1000, 8, 1, 1000),
-                                          (1, 77, 8, 1, 128)])
-def test_host_call_equals_device_call(cuda_ok, pinned, B, T, Hq, Hkv, W):
-    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=B + T)
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [
+    (3, 300, 16, 2, 128, 128),    # chunks of one sequence x half the kv heads
+    (2, 1000, 8, 1, 128, 1000),   # chunks of one sequence (global layer)
+    (1, 77, 8, 1, 128, 128),
+    (2, 8192, 64, 8, 128, 128),   # the bench's shapes, two sequences
+    (2, 77, 2, 1, 64, 33),        # lse slabs not 16-byte aligned: one chunk
+])
+def test_host_call_equals_device_call(cuda_ok, pinned, B, T, Hq, Hkv, D, W):
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=B + T)
     q, k, v = (t.pin_memory() if pinned else t.clone() for t in (x.q, x.k, x.v))
     out_h, lse_h, _ = swa.swa_sink_fwd_host(q, k, v, x.sink.cuda(), W)
     torch.cuda.synchronize()
