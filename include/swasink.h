@@ -19,8 +19,11 @@
  *
  * Conventions shared by every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller, row-major
- *     and contiguous in the layouts stated per call, 16-byte aligned.  The
- *     library allocates no memory and keeps no state between calls.
+ *     and contiguous in the layouts stated per call, 16-byte aligned (the
+ *     host-memory prefill, swa_sink_fwd_host, also takes HOST pointers).  The
+ *     library allocates no memory and keeps no state between calls beyond
+ *     per-device settings and, for swa_sink_fwd_host, two streams and a set of
+ *     events per device.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  Results are valid once the stream reaches them.
  *   - Arguments are validated on the host before anything is launched; an
@@ -97,7 +100,8 @@ swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const fl
  *   q_d, k_d, v_d, out_d, lse_d
  *                       device buffers of the full sizes of q, k, v, out and
  *                       lse, owned by the caller (the library allocates no
- *                       memory); they hold the data in transit
+ *                       memory); they hold the data in transit, in a layout
+ *                       of the library's choosing
  * The call is asynchronous with respect to the host, like the others: it is
  * ordered after earlier work on `stream`, later work on `stream` sees the
  * copies to the host completed, and out_h / lse_h may be read once `stream`
