@@ -515,6 +515,37 @@ def _event_ms(fn, reps, stream):
     return e0.elapsed_time(e1) / reps
 
 
+LONG = dict(B=1, T=262144, Hq=64, Hkv=8, D=128, W=128)
+
+
+def long_context_line(swa, dev, stream, reps, peaks):
+    """The long-context sliding-window prefill: one sequence of T=262144 with
+    every 97th key scaled by 8 (peaky scores) and sinks U(-4, 4)."""
+    c = LONG
+    B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=5, device=dev, sink_dist="uniform4",
+                           peaky_every=97)
+    out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    ms = _event_ms(lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream),
+                   reps, stream)
+    flops = work.prefill_flops(B, T, Hq, D, W)
+    nbytes = work.prefill_bytes(B, T, Hq, Hkv, D, 2)
+    hbm = float(peaks["hbm_gbs"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del x, out, lse
+    torch.cuda.empty_cache()
+    return {
+        "workload": f"swa_sink_prefill B{B} T{T} Hq{Hq} Hkv{Hkv} D{D} W{W} bf16->fp32+lse, every "
+                    f"97th key x8, sinks U(-4,4)",
+        "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "ms_per_call": round(ms, 4),
+        "roofline": {"kernel": "swa_fwd_tc_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "algorithmic_bytes_per_launch": nbytes},
+    }
+
+
 def high_sparse_line(swa, dev, stream, reps, peaks):
     """High Sparse on one sequence of T=32768: the global layer with and
     without its block scores, the selection, and the sparse layer over the
@@ -717,6 +748,7 @@ def run_ours(args, dist):
         line["hybrid_block_7to1"] = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks,
                                                 n_swa=7)
         line["high_sparse"] = high_sparse_line(swa, dev, stream, args.hybrid_reps, peaks)
+        line["long_context"] = long_context_line(swa, dev, stream, args.hybrid_reps, peaks)
     if not args.no_e2e:
         xh = gen.PrefillInputs(*(t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.sink)))
         e2e_ms, h2d, d2h = time_e2e(swa, xh, c, max(3, args.steps // 50), dev, stream)

@@ -15,7 +15,7 @@ def test_bench_helpers_exist():
     for name in ("time_prefill", "time_decode", "time_verify", "time_graph", "time_hybrid",
                  "hybrid_line", "verify_line", "bf16_out_line", "time_e2e", "prefill_roofline",
                  "cpu_oracle_sample", "run_reference", "run_ours", "recorded_traffic",
-                 "high_sparse_line", "_event_ms"):
+                 "high_sparse_line", "long_context_line", "job_rate", "_event_ms"):
         assert callable(getattr(bench, name)), name
 
 
