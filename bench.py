@@ -46,8 +46,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "swa_fwd_tc_kernel": ("csrc/tc_swa.cuh", "csrc/device_common.cuh"),
     "swa_fwd_tc_global_kernel": ("csrc/tc_global.cuh", "csrc/device_common.cuh"),
-    "decode_tc_kernel": ("csrc/decode_tc.cuh", "csrc/device_common.cuh"),
-    "verify_tc_kernel": ("csrc/verify_tc.cuh", "csrc/device_common.cuh"),
+    "decode_tc_kernel": ("csrc/decode_tc.cuh", "csrc/device_common.cuh", "csrc/griddep.cuh"),
+    "verify_tc_kernel": ("csrc/verify_tc.cuh", "csrc/device_common.cuh", "csrc/griddep.cuh"),
 }
 
 

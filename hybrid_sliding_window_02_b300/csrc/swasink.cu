@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/swasink.h"
@@ -130,6 +131,30 @@ swa_status check_launch(const char* what) {
     return SWA_ECUDA;
   }
   return SWA_OK;
+}
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the kernel before it on the stream is finishing, and orders its
+// memory accesses after that kernel itself (griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+swa_status launch_dependent(const char* what, void (*kern)(KArgs...), unsigned grid,
+                            unsigned block, int smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (e != cudaSuccess) {
+    set_cuda_error(what, e);
+    return SWA_ECUDA;
+  }
+  return check_launch(what);
 }
 
 enum FwdPath { kPathInvalid, kPathSimt, kPathTcSwa, kPathTcGlobal };
@@ -353,8 +378,7 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
   const long long grid = units < sms ? units : sms;
-  decode_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, p);
-  return check_launch("decode_tc_kernel");
+  return launch_dependent("decode_tc_kernel", decode_tc_kernel, (unsigned)grid, kThreads, kSmemBytes, st, mk, mv, mq, p);
 }
 
 swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const void* kr,
@@ -400,8 +424,7 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
   const long long grid = units < sms ? units : sms;
-  verify_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mk, mv, mq, mkn, mvn, p);
-  return check_launch("verify_tc_kernel");
+  return launch_dependent("verify_tc_kernel", verify_tc_kernel, (unsigned)grid, kThreads, kSmemBytes, st, mk, mv, mq, mkn, mvn, p);
 }
 
 template <typename Tin, int D>

@@ -43,6 +43,7 @@
 #pragma once
 
 #include "device_common.cuh"
+#include "griddep.cuh"
 
 namespace swa {
 namespace vertc {
@@ -158,6 +159,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+  // Launched as a programmatic dependent: the set-up above and an L2
+  // prefetch of this CTA's first K/V ring (a hint that reads nothing into
+  // the CTA) may overlap the previous kernel on the stream; every load and
+  // store below waits for that kernel to complete.
+  if (warp == kWarpProducer && lane == 0 && nk > 0) {
+    const int u0 = (int)blockIdx.x;
+    tma_prefetch_l2_4d(&map_k, 0, u0 * kW, 0, 0);
+    tma_prefetch_l2_4d(&map_k, 64, u0 * kW, 0, 0);
+    tma_prefetch_l2_4d(&map_v, 0, u0 * kW, 0, 0);
+    tma_prefetch_l2_4d(&map_v, 64, u0 * kW, 0, 0);
+  }
+  if (tid == 0) grid_dep_launch();
+  grid_dep_wait();
 
   if (warp == kWarpProducer) {
     // ======================= TMA producer =======================

@@ -26,6 +26,11 @@
  *     events per device.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  Results are valid once the stream reaches them.
+ *     The tensor-core decode and verify kernels are launched as programmatic
+ *     dependents: they may start their set-up, and an L2 prefetch of their
+ *     first K/V ring, while the kernel before them on the stream finishes,
+ *     but they read and write no buffer before that kernel has completed, so
+ *     stream order holds as for any launch.
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns an error and touches no memory.  A failed launch
  *     returns SWA_ECUDA (text in swa_last_error()).  Nothing traps on the
