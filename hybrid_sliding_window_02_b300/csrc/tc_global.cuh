@@ -115,7 +115,6 @@ struct Item {
 };
 
 // u-th item in order of decreasing causal length.
-// u-th item in order of decreasing causal length.
 __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
   Item it;
   const uint32_t bkn = (uint32_t)(p.B * p.Hkv);

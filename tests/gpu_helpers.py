@@ -94,3 +94,70 @@ def sample_rows(B, T, Hq, n_pos, seed, extra_pos=(), heads=None):
         for h in hs:
             rows.append((b, h, i))
     return rows
+
+
+def oracle_block_scores_from_slices(q, k, entries):
+    """Oracle block scores of the global layer (every causal pair, W >= T) at
+    selected entries (b, g, kb): query group g (positions 4g..4g+3), key block
+    kb (keys 128kb..128kb+127).  Returns [n, Hkv] fp64.
+
+    An entry depends only on those 4 query rows, those 128 key rows and on
+    which pairs satisfy j <= i.  Shifting every position by -128kb keeps the
+    block at keys 0..127.  A group that overlaps the block keeps its offset
+    (at most 124); a group past the block goes to sub-positions 128..131,
+    where it sees every key of the block, as it does in the whole sequence.
+    The oracle then runs on that short sequence alone.
+    """
+    out = []
+    for b, g, kb in entries:
+        p0, j0 = 4 * int(g), 128 * int(kb)
+        assert j0 <= p0 + 3, "block after the query group: no valid pair"
+        off = p0 - j0 if p0 - j0 < 128 else 128
+        L = off + 4
+        n = min(128, L)
+        qs = torch.zeros((1, L) + tuple(q.shape[2:]), dtype=q.dtype)
+        ks = torch.zeros((1, L) + tuple(k.shape[2:]), dtype=k.dtype)
+        qs[0, off:off + 4] = q[int(b), p0:p0 + 4].cpu()
+        ks[0, :n] = k[int(b), j0:j0 + n].cpu()
+        out.append(oracle.block_max(qs, ks, L)[0, :, off // 4, 0])
+    return np.array(out)
+
+
+def oracle_sparse_rows_from_slices(q, k, v, sink, idx, QB, rows):
+    """Oracle outputs of the sparse layer at selected rows (b, h, i), for the
+    block selection idx [B, Hkv, ceil(T/QB), topk] (-1 = none).
+
+    Row i of head h attends to the keys j <= i of the blocks selected for its
+    query block and its kv head, with the sink.  Those keys, gathered in
+    increasing order into a short sequence, followed by the query at the last
+    of its sub-positions, give a causal row that sees exactly them, so the
+    prefill oracle's row is the sparse layer's row.
+    Returns (out [n, D], lse [n]) fp64.
+    """
+    Hq, D = q.shape[2], q.shape[3]
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    idx = np.asarray(idx.cpu() if isinstance(idx, torch.Tensor) else idx)
+    sink_c = sink.detach().cpu()
+    out = np.zeros((len(rows), D))
+    lse = np.zeros(len(rows))
+    for r, (b, h, i) in enumerate(rows):
+        b, h, i = int(b), int(h), int(i)
+        kvh = h // G
+        sel = [int(kb) for kb in idx[b, kvh, i // QB] if kb >= 0 and 128 * kb <= i]
+        if not sel:
+            out[r] = 0.0
+            lse[r] = float(sink_c[h])
+            continue
+        J = torch.from_numpy(np.concatenate(
+            [np.arange(128 * kb, min(128 * kb + 128, i + 1)) for kb in sel]))
+        n = len(J)
+        qs = torch.zeros((1, n, G, D), dtype=q.dtype)
+        qs[0, n - 1] = q[b, i, kvh * G:(kvh + 1) * G].cpu()
+        ks = k[b, :, kvh:kvh + 1].cpu()[J].unsqueeze(0)
+        vs = v[b, :, kvh:kvh + 1].cpu()[J].unsqueeze(0)
+        o, l = oracle.swa_sink_fwd_rows(qs, ks, vs, sink_c[kvh * G:(kvh + 1) * G], n,
+                                        [[0, h - kvh * G, n - 1]])
+        out[r] = o[0]
+        lse[r] = l[0]
+    return out, lse

@@ -7,7 +7,9 @@ import torch
 import oracle
 import hybrid_sliding_window_02_b300 as swa
 from hybrid_sliding_window_02_b300 import inputs as gen
-from gpu_helpers import assert_bf16_close, assert_lse_close
+from gpu_helpers import (assert_bf16_close, assert_lse_close, gather_rows,
+                         oracle_block_scores_from_slices, oracle_rows_from_slices,
+                         oracle_sparse_rows_from_slices)
 
 pytestmark = pytest.mark.gpu
 
@@ -91,3 +93,50 @@ def test_scores_select_sparse_pipeline(cuda_ok):
     assert_bf16_close(out.cpu().numpy(), o_ref)
     assert_lse_close(lse.cpu().numpy(), l_ref)
     assert swa.device_error() == 0
+
+
+def test_high_sparse_full_size_sampled(cuda_ok):
+    # the High Sparse workload at full size (one sequence of T = 32768, Hq 64,
+    # Hkv 8, top-16 blocks per 64-position query block, the inputs' seeds as
+    # in the bench), in the same calls: scores, selection, sparse layer
+    T, Hq, Hkv, D, QB, topk = 32768, 64, 8, 128, 64, 16
+    x = gen.prefill_inputs(1, T, Hq, Hkv, D, seed=500, device="cuda")
+    q2 = gen.prefill_inputs(1, T, Hq, Hkv, D, seed=501, device="cuda").q
+    out_g, lse_g, bm = swa.swa_sink_fwd_scores(x.q, x.k, x.v, x.sink, T)
+    idx = swa.swa_topk_blocks(bm, T, QB, topk)
+    out, lse = swa.swa_sink_sparse_fwd(q2, x.k, x.v, x.sink, idx, QB)
+    torch.cuda.synchronize()
+    assert swa.device_error() == 0
+    bm_h = bm.cpu().numpy()
+    idx_h = idx.cpu().numpy()
+    # every entry: -inf exactly where the query group has no causal key in the block
+    last = 4 * np.arange(T // 4) + 3
+    has_pair = (128 * np.arange(T // 128))[None, :] <= last[:, None]
+    assert np.array_equal(np.isfinite(bm_h[0]), np.broadcast_to(has_pair, bm_h[0].shape))
+    # the selection from these fp32 scores, bit for bit
+    assert np.array_equal(idx_h, oracle.topk_blocks(bm_h, T, QB, topk))
+    # sampled scores
+    g = np.random.default_rng(17)
+    entries = [(0, 0, 0), (0, T // 4 - 1, 0), (0, T // 4 - 1, T // 128 - 1), (0, 4095, 127)]
+    for _ in range(40):
+        gg = int(g.integers(0, T // 4))
+        entries.append((0, gg, int(g.integers(0, (4 * gg + 3) // 128 + 1))))
+    ref = oracle_block_scores_from_slices(x.q, x.k, entries)
+    got = np.array([bm_h[0, :, gg, kb] for _, gg, kb in entries])
+    assert np.abs(got - ref).max() <= 1e-3
+    # sampled rows of the global layer that emitted the scores
+    rows = [(0, h, i) for i in (0, 4095, 16383, T - 1) for h in range(0, Hq, 9)]
+    o_ref, l_ref = oracle_rows_from_slices(x.q, x.k, x.v, x.sink, T, rows)
+    o, l = gather_rows(out_g, lse_g, rows)
+    assert_bf16_close(o, o_ref, what="global layer with scores")
+    assert_lse_close(l, l_ref)
+    # sampled rows of the sparse layer
+    rows = [(0, 0, 0), (0, Hq - 1, T - 1), (0, 17, QB - 1), (0, 40, QB)]
+    rows += [(0, int(g.integers(0, Hq)), int(g.integers(0, T))) for _ in range(60)]
+    o_ref, l_ref = oracle_sparse_rows_from_slices(q2, x.k, x.v, x.sink, idx_h, QB,
+                                                  [(0, h, i) for _, h, i in rows])
+    o, l = gather_rows(out, lse, rows)
+    assert_bf16_close(o, o_ref, what="sparse layer")
+    assert_lse_close(l, l_ref)
+    del x, q2, out_g, lse_g, bm, out, lse
+    torch.cuda.empty_cache()
