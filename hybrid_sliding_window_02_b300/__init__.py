@@ -187,8 +187,10 @@ def swa_sink_fwd(q, k, v, sink, W: int, out=None, lse=None, *, with_lse: bool = 
 
 def swa_sink_fwd_host(q_h, k_h, v_h, sink, W: int, out_h=None, lse_h=None, *, work=None,
                       with_lse: bool = True, out_dtype=None, stream=None):
-    """Prefill from and to host memory, pipelined per sequence (copies of one
-    sequence overlap the compute of its neighbours).
+    """Prefill from and to host memory, pipelined in chunks (one sequence x a
+    range of positions on the sliding-window tensor-core path, one sequence x
+    a share of the kv heads otherwise): the copies of one chunk overlap the
+    compute and the copies of its neighbours.
 
     q_h [B,T,Hq,D], k_h/v_h [B,T,Hkv,D]: CPU tensors (pin them for overlap);
     sink [Hq] fp32 on the device.  work: optional tuple of device buffers

@@ -200,9 +200,11 @@ swa_status launch_simt(const void* q, const void* k, const void* v, const float*
   return check_launch("simt_fwd_kernel");
 }
 
+// Tiles n_first .. n_first + n_tiles - 1 (16 positions each) of every
+// sequence; n_tiles < 0: to the end of the sequence.
 swa_status launch_tc_swa(const void* q, const void* k, const void* v, const float* sink,
                          void* out, float* lse, int B, int T, int Hq, int Hkv, int W,
-                         bool bf16_out, cudaStream_t st) {
+                         bool bf16_out, cudaStream_t st, int n_first = 0, int n_tiles = -1) {
   using namespace swa::tcswa;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
@@ -219,12 +221,13 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
       g_dev[dev].tc_attr[bf16_out] = true;
     }
   }
-  const long long ntiles_seq = (T + kNpos - 1) / kNpos;
+  const long long ntiles_seq = n_tiles >= 0 ? n_tiles : (T + kNpos - 1) / kNpos - n_first;
   const long long total_tiles = (long long)B * Hkv * ntiles_seq;
   if (total_tiles >= (1LL << 31)) {
     set_error_text("problem too large for the tensor-core kernel");
     return SWA_EUNSUPPORTED;
   }
+  if (total_tiles <= 0) return SWA_OK;
   CUtensorMap mq, mk, mv;
   if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, T, B, 64, kG, kNpos) ||
       !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, kD, Hkv, T, B, 64, 1, kBlk) ||
@@ -239,6 +242,7 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.W = W;
+  p.n_first = n_first;
   p.ntiles_seq = (int)ntiles_seq;
   p.total_tiles = (int)total_tiles;
   p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
@@ -551,6 +555,81 @@ swa_status cuda_ok(cudaError_t r, const char* what) {
   set_cuda_error(what, r);
   return SWA_ECUDA;
 }
+
+char* byte_at(const void* base, size_t off) {
+  return const_cast<char*>(static_cast<const char*>(base)) + off;
+}
+
+// The sliding-window tensor-core path: chunks of one sequence x a range of
+// positions, staged in the device buffers at their own places, so that every
+// copy is one contiguous range (the lse, [B, Hq, T], goes as Hq rows).  The
+// prefill of a chunk computes its tiles only; the keys of the window before
+// its first position came in with earlier chunks of the same sequence, on the
+// same stream, so they are in place when it runs.
+swa_status host_by_position(const void* q_h, const void* k_h, const void* v_h, const float* sink,
+                            void* out_h, float* lse_h, void* q_d, void* k_d, void* v_d,
+                            void* out_d, float* lse_d, int B, int T, int Hq, int Hkv, int W,
+                            bool bf16_out, cudaStream_t st, HostPipe& hp) {
+  constexpr int kD = swa::tcswa::kD, kNpos = swa::tcswa::kNpos;
+  if (!aligned16(q_d) || !aligned16(k_d) || !aligned16(v_d) || !aligned16(out_d) ||
+      (lse_d && !aligned16(lse_d)))
+    return SWA_EINVAL;
+  // about 16 chunks in all, of at least 512 positions, whole tiles except the last
+  int nper = (16 + B - 1) / B;
+  if (nper > T / 512) nper = T / 512;
+  if (nper < 1) nper = 1;
+  const int Tc = ((T + nper - 1) / nper + kNpos - 1) / kNpos * kNpos;
+  const int nchunk_seq = (T + Tc - 1) / Tc;
+  const int nchunk = B * nchunk_seq;
+  const size_t q_tok = (size_t)Hq * kD * 2, k_tok = (size_t)Hkv * kD * 2;
+  const size_t o_tok = (size_t)Hq * kD * (bf16_out ? 2 : 4);
+  if (!pipe_events(hp, 2 + 2 * (size_t)nchunk)) return SWA_ECUDA;
+  cudaEvent_t ev_start = hp.ev[0], ev_end = hp.ev[1];
+  swa_status rc = cuda_ok(cudaEventRecord(ev_start, st), "cudaEventRecord");
+  if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(hp.h2d, ev_start, 0), "cudaStreamWaitEvent");
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  for (int c = 0; rc == SWA_OK && c < nchunk; ++c) {
+    const int b = c / nchunk_seq, t0 = (c % nchunk_seq) * Tc;
+    const int t1 = t0 + Tc < T ? t0 + Tc : T;
+    const size_t row0 = (size_t)b * T + t0, n = (size_t)(t1 - t0), seq0 = (size_t)b * T;
+    cudaEvent_t ev_in = hp.ev[2 + 2 * c], ev_c = hp.ev[3 + 2 * c];
+    rc = cuda_ok(cudaMemcpyAsync(byte_at(q_d, row0 * q_tok), byte_at(q_h, row0 * q_tok),
+                                 n * q_tok, h2d, hp.h2d),
+                 "cudaMemcpyAsync(q)");
+    if (rc == SWA_OK)
+      rc = cuda_ok(cudaMemcpyAsync(byte_at(k_d, row0 * k_tok), byte_at(k_h, row0 * k_tok),
+                                   n * k_tok, h2d, hp.h2d),
+                   "cudaMemcpyAsync(k)");
+    if (rc == SWA_OK)
+      rc = cuda_ok(cudaMemcpyAsync(byte_at(v_d, row0 * k_tok), byte_at(v_h, row0 * k_tok),
+                                   n * k_tok, h2d, hp.h2d),
+                   "cudaMemcpyAsync(v)");
+    if (rc == SWA_OK) rc = cuda_ok(cudaEventRecord(ev_in, hp.h2d), "cudaEventRecord");
+    if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(st, ev_in, 0), "cudaStreamWaitEvent");
+    if (rc == SWA_OK)
+      rc = launch_tc_swa(byte_at(q_d, seq0 * q_tok), byte_at(k_d, seq0 * k_tok),
+                         byte_at(v_d, seq0 * k_tok), sink, byte_at(out_d, seq0 * o_tok),
+                         lse_d ? lse_d + (size_t)b * Hq * T : nullptr, 1, T, Hq, Hkv, W, bf16_out,
+                         st, t0 / kNpos, (t1 + kNpos - 1) / kNpos - t0 / kNpos);
+    if (rc == SWA_OK) rc = cuda_ok(cudaEventRecord(ev_c, st), "cudaEventRecord");
+    if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(hp.d2h, ev_c, 0), "cudaStreamWaitEvent");
+    if (rc == SWA_OK)
+      rc = cuda_ok(cudaMemcpyAsync(byte_at(out_h, row0 * o_tok), byte_at(out_d, row0 * o_tok),
+                                   n * o_tok, d2h, hp.d2h),
+                   "cudaMemcpyAsync(out)");
+    if (rc == SWA_OK && lse_d)
+      rc = cuda_ok(cudaMemcpy2DAsync(lse_h + (size_t)b * Hq * T + t0, (size_t)T * 4,
+                                     lse_d + (size_t)b * Hq * T + t0, (size_t)T * 4, n * 4, Hq,
+                                     d2h, hp.d2h),
+                   "cudaMemcpy2DAsync(lse)");
+  }
+  // later work on `stream` follows every copy enqueued above, even after an error
+  const swa_status rc_end = cuda_ok(cudaEventRecord(ev_end, hp.d2h), "cudaEventRecord");
+  const swa_status rc_wait =
+      rc_end == SWA_OK ? cuda_ok(cudaStreamWaitEvent(st, ev_end, 0), "cudaStreamWaitEvent")
+                       : rc_end;
+  return rc != SWA_OK ? rc : rc_wait;
+}
 }  // namespace
 
 swa_status swa_sink_fwd_host(const void* q_h, const void* k_h, const void* v_h,
@@ -565,8 +644,19 @@ swa_status swa_sink_fwd_host(const void* q_h, const void* k_h, const void* v_h,
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return SWA_EINVAL;
   if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
   if (out_dtype != SWA_F32 && out_dtype != SWA_BF16) return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  if (select_fwd(B, T, Hq, Hkv, D, W, in_dtype) == kPathTcSwa) {
+    int dev;
+    if (!current_device(&dev)) return SWA_ECUDA;
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    HostPipe& hp = g_pipe[dev];
+    if (!pipe_ready(hp)) return SWA_ECUDA;
+    return host_by_position(q_h, k_h, v_h, sink, out_h, lse_h, q_d, k_d, v_d, out_d, lse_d, B, T,
+                            Hq, Hkv, W, out_dtype == SWA_BF16, static_cast<cudaStream_t>(stream),
+                            hp);
+  }
   const size_t ie = in_dtype == SWA_BF16 ? 2 : 4, oe = out_dtype == SWA_BF16 ? 2 : 4;
-  // Chunks: one sequence x a share of the kv heads (two shares when Hkv is
+  // Other paths: chunks of one sequence x a share of the kv heads (two shares when Hkv is
   // even), each staged compactly in the caller's device buffers.  Smaller
   // chunks shorten the copy-in before the first prefill and the copy-out after
   // the last, the two that overlap nothing.  When a share's staging offsets

@@ -106,7 +106,8 @@ struct Params {
   void* out;            // float, or bf16 with kBf16Out
   float* lse;
   int B, T, Hq, Hkv, W;
-  int ntiles_seq;       // ceil(T / 16)
+  int n_first;          // first tile of each sequence computed (tiles of 16 positions)
+  int ntiles_seq;       // tiles computed per (sequence, kv head): n_first .. n_first + ntiles_seq - 1
   int total_tiles;      // B * Hkv * ntiles_seq (< 2^31, checked on the host)
   float scale_log2;     // log2(e) / sqrt(D)
   int out_align32;      // out is 32-byte aligned (bf16 output stores whole sectors)
@@ -115,7 +116,7 @@ struct Params {
 __device__ __forceinline__ void tile_coords(uint32_t u, const Params& p, int& b, int& kvh,
                                             int& n) {
   const uint32_t bk = u / (uint32_t)p.ntiles_seq;
-  n = (int)(u - bk * (uint32_t)p.ntiles_seq);
+  n = p.n_first + (int)(u - bk * (uint32_t)p.ntiles_seq);
   b = (int)(bk / (uint32_t)p.Hkv);
   kvh = (int)(bk - (uint32_t)b * (uint32_t)p.Hkv);
 }
@@ -125,8 +126,8 @@ struct TileWalk {
   int b, kvh, n;
   __device__ __forceinline__ void start(uint32_t u, const Params& p) { tile_coords(u, p, b, kvh, n); }
   __device__ __forceinline__ void next(const Params& p) {
-    if (++n == p.ntiles_seq) {
-      n = 0;
+    if (++n == p.n_first + p.ntiles_seq) {
+      n = p.n_first;
       if (++kvh == p.Hkv) {
         kvh = 0;
         ++b;

@@ -89,13 +89,19 @@ swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const fl
 
 /*
  * swa_sink_fwd_host -- swa_sink_fwd_ex with q, k, v taken from HOST memory and
- * out, lse written to HOST memory, in chunks of one sequence x a share of the
- * kv heads (half of them when Hkv is even; the whole batch as one chunk when
- * a share would break the 16-byte alignment of the staging): the chunk's
- * inputs are copied to the device, its prefill runs, and its outputs are
- * copied back, while the copies of the neighbouring chunks run at the same
- * time (host-to-device on one stream, the prefill on `stream`, device-to-host
- * on another; each chunk's steps are chained by events).  The results are
+ * out, lse written to HOST memory, in chunks: the chunk's inputs are copied to
+ * the device, its prefill runs, and its outputs are copied back, while the
+ * copies of the neighbouring chunks run at the same time (host-to-device on
+ * one stream, the prefill on `stream`, device-to-host on another; each
+ * chunk's steps are chained by events).  On the sliding-window tensor-core
+ * path (bf16, D = 128, 8 query heads per kv head, W <= 129) a chunk is one
+ * sequence x a range of positions (about 16 chunks in all, at least 512
+ * positions each), staged at its own place in the device buffers, so that
+ * every copy is one contiguous range; the prefill of a chunk computes its
+ * positions only, reading the window's earlier keys copied with the chunks
+ * before it.  On the other paths a chunk is one sequence x a share of the kv
+ * heads (half of them when Hkv is even; the whole batch as one chunk when a
+ * share would break the 16-byte alignment of the staging).  The results are
  * those of swa_sink_fwd_ex on the whole batch, bit for bit.
  *   q_h, k_h, v_h       host, layouts as swa_sink_fwd; pinned (page-locked)
  *                       memory lets the copies overlap, pageable memory works

@@ -21,11 +21,14 @@ def _device_call(x, W, out_dtype=torch.float32):
 
 @pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [
-    (3, 300, 16, 2, 128, 128),    # chunks of one sequence x half the kv heads
-    (2, 1000, 8, 1, 128, 1000),   # chunks of one sequence (global layer)
+    (3, 300, 16, 2, 128, 128),    # sliding window: one chunk per sequence
+    (1, 5000, 16, 2, 128, 128),   # 9 position chunks of 560, the last one ragged (520)
+    (3, 1030, 16, 2, 128, 33),    # 2 position chunks per sequence, narrow window
+    (2, 1000, 8, 1, 128, 1000),   # global layer: chunks of one sequence (Hkv = 1)
+    (2, 600, 16, 2, 128, 600),    # global layer: one sequence x half the kv heads
     (1, 77, 8, 1, 128, 128),
-    (2, 8192, 64, 8, 128, 128),   # the bench's shapes, two sequences
-    (2, 77, 2, 1, 64, 33),        # lse slabs not 16-byte aligned: one chunk
+    (2, 8192, 64, 8, 128, 128),   # the bench's shapes, two sequences: 8 chunks each
+    (2, 77, 2, 1, 64, 33),        # general kernel, lse slabs not 16-byte aligned: one chunk
 ])
 def test_host_call_equals_device_call(cuda_ok, pinned, B, T, Hq, Hkv, D, W):
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=B + T)
@@ -55,8 +58,9 @@ def test_host_call_matches_oracle_and_reuses_work(cuda_ok):
     assert torch.equal(out2, o2) and torch.equal(lse2, l2)
 
 
-def test_host_call_without_lse_and_bf16_output(cuda_ok):
-    x = gen.prefill_inputs(3, 256, 16, 2, 128, seed=5)
+@pytest.mark.parametrize("B,T", [(3, 256), (2, 2100)])
+def test_host_call_without_lse_and_bf16_output(cuda_ok, B, T):
+    x = gen.prefill_inputs(B, T, 16, 2, 128, seed=5)
     q, k, v = (t.pin_memory() for t in (x.q, x.k, x.v))
     out_h, lse_h, _ = swa.swa_sink_fwd_host(q, k, v, x.sink.cuda(), 128, with_lse=False,
                                             out_dtype=torch.bfloat16)
