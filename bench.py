@@ -493,6 +493,9 @@ def hybrid_line(swa, dev, stream, reps, peaks, n_swa=None):
                      "achieved": round(ga_tf, 1), "peak": float(peaks["bf16_tflops"]),
                      "unit": "TFLOP/s", "frac": round(ga_tf / float(peaks["bf16_tflops"]), 4),
                      "peak_source": "measured bf16_tflops (burst)",
+                     # the layer runs inside a seconds-long loop under the power
+                     # cap: its fraction of the sustained GEMM rate, for context
+                     "frac_of_sustained": round(ga_tf / float(peaks["bf16_tflops_sustained"]), 4),
                      "algorithmic_flops_per_launch": ga_fl,
                      "traffic": recorded_traffic("swa_fwd_tc_global_kernel")},
     }
