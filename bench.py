@@ -635,9 +635,9 @@ def bf16_out_line(swa, x, c, steps, dev, stream, peaks):
 
 def time_e2e(swa, xh, c, steps, dev, stream):
     """Host (pinned) inputs -> device -> prefill -> host outputs, every step,
-    through the library's host-buffer call (swa_sink_fwd_host: per sequence,
-    the copies in, the prefill and the copies out, with neighbouring sequences'
-    copies overlapping).  The sink is a resident layer parameter."""
+    through the library's host-buffer call (swa_sink_fwd_host: per chunk of
+    positions, the copies in, the prefill and the copies out, with neighbouring
+    chunks' copies overlapping).  The sink is a resident layer parameter."""
     B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
     sink_d = xh.sink.to(dev)
     out_h = torch.empty(B, T, Hq, D, dtype=torch.float32, pin_memory=True)

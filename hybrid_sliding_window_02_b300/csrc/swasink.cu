@@ -515,12 +515,12 @@ swa_status swa_sink_fwd(const void* q, const void* k, const void* v, const float
   return swa_sink_fwd_ex(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, in_dtype, SWA_F32, stream);
 }
 
-// ---- prefill from and to host memory: per-sequence copy / compute / copy ----
+// ---- prefill from and to host memory: per-chunk copy in / compute / copy out ----
 namespace {
 struct HostPipe {
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  std::vector<cudaEvent_t> ev;   // [0] start, [1] end, then per sequence: in, computed
+  std::vector<cudaEvent_t> ev;   // [0] start, [1] end, then per chunk: in, computed
 };
 HostPipe g_pipe[kMaxDevices];
 std::mutex g_pipe_mu;

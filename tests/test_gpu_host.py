@@ -1,4 +1,4 @@
-"""swa_sink_fwd_host (prefill from and to host memory, pipelined per sequence)
+"""swa_sink_fwd_host (prefill from and to host memory, pipelined in chunks)
 against the device-buffer call and the fp64 oracle."""
 import numpy as np
 import pytest
