@@ -503,30 +503,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar(kBarOFull + ti), k & 1, kErrWaitOFull, abort_flag)) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const long long e0 = (((long long)it.b * p.T + pos) * p.Hq + h) * kD;
+      if constexpr (kBf16Out) {
+        const long long e0 = (((long long)it.b * p.T + pos) * p.Hq + h) * kD;
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + c * 32, o);
-        tmem_ld_wait();
-        reg_fence32(o);
-        if (pos < p.T) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
-          if constexpr (kBf16Out) {
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          tmem_ld_wait();
+          reg_fence32(o);
+          if (pos < p.T) {
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+              pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
+                                  __uint_as_float(o[2 * e + 1]) * inv_l);
             float* orow = reinterpret_cast<float*>(static_cast<__nv_bfloat16*>(p.out) + e0 + c * 32);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               st_global_v4(orow + 4 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-          } else {
-            float* orow = static_cast<float*>(p.out) + e0 + c * 32;
+          }
+        }
+      } else {
+        // O read in the 16x256b shape: thread (rr, qd) = (lane / 4, lane % 4)
+        // holds rows 16 hf + 8 kk + rr of this warp's lanes, i.e. position
+        // 4 quad + 2 hf + kk of the tile and head rr, columns 8 j + 2 qd + {0, 1}.
+        // A quad then writes whole 32-byte sectors, and one store covers the
+        // 8 heads of a position (4 KB contiguous); each row's 1 / l comes from
+        // the thread that owns the row (lane 16 hf + 8 kk + rr).
+        const int rr = lane >> 2, qd = lane & 3;
+        const uint32_t o_warp = tmem + ((uint32_t)(quad * 32) << 16) + col_o(ti);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              st_global_v4(orow + 4 * e, o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t o[64];
+          tmem_ld_16x256b_x16(o_warp + ((uint32_t)(16 * hf) << 16), o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o[c * 16]));
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const float il = __shfl_sync(0xffffffffu, inv_l, 16 * hf + 8 * kk + rr);
+            const int pos_k = it.p0 + ti * kNpos + 4 * quad + 2 * hf + kk;
+            if (pos_k < p.T) {
+              float* orow = static_cast<float*>(p.out) +
+                            (((long long)it.b * p.T + pos_k) * p.Hq + it.kvh * kG + rr) * kD + 2 * qd;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                st_global_v2(orow + 8 * j,
+                             __float_as_uint(__uint_as_float(o[4 * j + 2 * kk]) * il),
+                             __float_as_uint(__uint_as_float(o[4 * j + 2 * kk + 1]) * il));
+            }
           }
         }
       }
