@@ -28,6 +28,7 @@ def _device_call(x, W, out_dtype=torch.float32):
     (2, 600, 16, 2, 128, 600),    # global layer: one sequence x half the kv heads
     (1, 77, 8, 1, 128, 128),
     (2, 8192, 64, 8, 128, 128),   # the bench's shapes, two sequences: 8 chunks each
+    (4, 8192, 64, 8, 128, 128),   # the bench's end-to-end workload: 4 chunks of 2048 each
     (2, 77, 2, 1, 64, 33),        # general kernel, lse slabs not 16-byte aligned: one chunk
 ])
 def test_host_call_equals_device_call(cuda_ok, pinned, B, T, Hq, Hkv, D, W):
