@@ -18,7 +18,9 @@ Pins (what ties these functions to something other than themselves) live in
 ``tests/test_oracle_pins.py``: brute force with explicit score matrices, the
 sink -> -inf / +inf limits, W >= T against a library causal-attention routine,
 weights + sink summing to one, the closed form at W = 1, decode = prefill row,
-verify = prefill rows, and poisoned out-of-window keys.
+verify = prefill rows, and poisoned out-of-window keys.  RoPE's frequency
+schedule and pair layout are pinned by hand-derived cos/sin values in
+``tests/golden/rope_hand_derived.json`` (``tests/test_golden.py``).
 """
 from __future__ import annotations
 

@@ -38,3 +38,18 @@ def test_oracle_tiny_regression():
     np.testing.assert_allclose(o[:, :8], np.array(g["out_first8"]), rtol=0, atol=1e-13)
     np.testing.assert_allclose(o.sum(axis=1), np.array(g["out_sum"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(l, np.array(g["lse"]), rtol=0, atol=1e-13)
+
+
+def test_rope_hand_derived_angles_and_pairs():
+    """RoPE frequency schedule and pair layout, pinned by hand-derived values:
+    the angle of pair i is p * theta^(-2i/rot_dim), the pairs are (i, i+rot_dim/2),
+    and token t of sequence b sits at position pos0[b] + t."""
+    g = _load("rope_hand_derived.json")
+    env = {"cos": math.cos, "sin": math.sin}
+    for case in g["cases"]:
+        x = torch.tensor(case["x"], dtype=torch.float64)
+        pos0 = torch.tensor(case["pos0"], dtype=torch.int64)
+        y = oracle.rope(x, pos0, case["rot_dim"], case["theta"])
+        want = np.vectorize(lambda s: float(eval(s, {}, env)))(np.array(case["y_expr"]))
+        assert y.shape == want.shape, case["name"]
+        np.testing.assert_allclose(y, want, rtol=0, atol=1e-12, err_msg=case["name"])
