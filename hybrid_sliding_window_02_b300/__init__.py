@@ -113,6 +113,25 @@ def _check(fn: str, status: int):
         raise SwaError(fn, status, last_error())
 
 
+def _call(fn: str, dev, *args):
+    """Call library entry point ``fn`` with ``dev`` as the current CUDA device:
+    the library launches on the current device and looks up its attributes
+    there, so the tensors' device must be current during the call."""
+    import torch
+    with torch.cuda.device(dev):
+        status = getattr(lib(), fn)(*args)
+    _check(fn, status)
+
+
+def _out_check(name, t, shape, dtypes, device):
+    """A caller-supplied output buffer: a contiguous tensor on ``device`` with
+    exactly ``shape`` and one of ``dtypes`` (the kernels write it in full)."""
+    _cuda_contig(name, t, device)
+    if tuple(t.shape) != tuple(shape) or t.dtype not in dtypes:
+        names = " or ".join(str(d).replace("torch.", "") for d in dtypes)
+        raise ValueError(f"{name} must be {names} {list(shape)}, got {t.dtype} {list(t.shape)}")
+
+
 def _dtype_code(t):
     import torch
     if t.dtype == torch.bfloat16:
@@ -170,18 +189,15 @@ def swa_sink_fwd(q, k, v, sink, W: int, out=None, lse=None, *, with_lse: bool = 
         raise ValueError("sink must be float32 [Hq]")
     if out is None:
         out = torch.empty(B, T, Hq, D, dtype=out_dtype or torch.float32, device=dev)
-    if out.dtype not in (torch.float32, torch.bfloat16) or out.shape != (B, T, Hq, D):
-        raise ValueError("out must be [B, T, Hq, D] float32 or bfloat16")
+    _out_check("out", out, (B, T, Hq, D), (torch.float32, torch.bfloat16), dev)
     if with_lse and lse is None:
         lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
-    _cuda_contig("out", out, dev)
     if lse is not None:
-        _cuda_contig("lse", lse, dev)
-    st = lib().swa_sink_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
-                               out.data_ptr(), lse.data_ptr() if lse is not None else None,
-                               B, T, Hq, Hkv, D, int(W), _dtype_code(q), _dtype_code(out),
-                               _stream_handle(stream, dev))
-    _check("swa_sink_fwd_ex", st)
+        _out_check("lse", lse, (B, Hq, T), (torch.float32,), dev)
+    _call("swa_sink_fwd_ex", dev, q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
+          out.data_ptr(), lse.data_ptr() if lse is not None else None,
+          B, T, Hq, Hkv, D, int(W), _dtype_code(q), _dtype_code(out),
+          _stream_handle(stream, dev))
     return out, lse
 
 
@@ -218,8 +234,7 @@ def swa_sink_fwd_host(q_h, k_h, v_h, sink, W: int, out_h=None, lse_h=None, *, wo
         out_h = torch.empty(B, T, Hq, D, dtype=odt, pin_memory=pin)
     if with_lse and lse_h is None:
         lse_h = torch.empty(B, Hq, T, dtype=torch.float32, pin_memory=pin)
-    if out_h.is_cuda or out_h.shape != (B, T, Hq, D) or not out_h.is_contiguous():
-        raise ValueError("out_h must be a contiguous CPU tensor [B, T, Hq, D]")
+    _host_out_check(out_h, lse_h, B, T, Hq, D)
     if work is None:
         work = (torch.empty(q_h.shape, dtype=q_h.dtype, device=dev),
                 torch.empty(k_h.shape, dtype=k_h.dtype, device=dev),
@@ -236,16 +251,27 @@ def swa_sink_fwd_host(q_h, k_h, v_h, sink, W: int, out_h=None, lse_h=None, *, wo
     if (lse_h is None) != (lse_d is None):
         raise ValueError("lse_h and lse_d go together")
     if lse_d is not None:
-        _cuda_contig("lse_d", lse_d, dev)
-    st = lib().swa_sink_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), sink.data_ptr(),
-                                 out_h.data_ptr(),
-                                 lse_h.data_ptr() if lse_h is not None else None,
-                                 q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(), out_d.data_ptr(),
-                                 lse_d.data_ptr() if lse_d is not None else None,
-                                 B, T, Hq, Hkv, D, int(W), _dtype_code(q_h), _dtype_code(out_h),
-                                 _stream_handle(stream, dev))
-    _check("swa_sink_fwd_host", st)
+        _out_check("lse_d", lse_d, (B, Hq, T), (torch.float32,), dev)
+    _call("swa_sink_fwd_host", dev, q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
+          sink.data_ptr(), out_h.data_ptr(), lse_h.data_ptr() if lse_h is not None else None,
+          q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(), out_d.data_ptr(),
+          lse_d.data_ptr() if lse_d is not None else None,
+          B, T, Hq, Hkv, D, int(W), _dtype_code(q_h), _dtype_code(out_h),
+          _stream_handle(stream, dev))
     return out_h, lse_h, work
+
+
+def _host_out_check(out_h, lse_h, B, T, Hq, D):
+    """Host outputs of the host-memory prefill: contiguous CPU tensors, out_h
+    [B, T, Hq, D] fp32 or bf16, lse_h [B, Hq, T] fp32 (or None)."""
+    import torch
+    if (out_h.is_cuda or tuple(out_h.shape) != (B, T, Hq, D) or not out_h.is_contiguous()
+            or out_h.dtype not in (torch.float32, torch.bfloat16)):
+        raise ValueError("out_h must be a contiguous CPU tensor [B, T, Hq, D], float32 or "
+                         "bfloat16")
+    if lse_h is not None and (lse_h.is_cuda or tuple(lse_h.shape) != (B, Hq, T) or
+                              lse_h.dtype != torch.float32 or not lse_h.is_contiguous()):
+        raise ValueError("lse_h must be a contiguous CPU float32 tensor [B, Hq, T]")
 
 
 def swa_sink_decode(q, k_ring, v_ring, pos, sink, out=None, lse=None, *, with_lse=True,
@@ -271,13 +297,15 @@ def swa_sink_decode(q, k_ring, v_ring, pos, sink, out=None, lse=None, *, with_ls
         raise ValueError("sink must be float32 [Hq]")
     if out is None:
         out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
+    _out_check("out", out, (B, Hq, D), (torch.float32,), dev)
     if with_lse and lse is None:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
-    st = lib().swa_sink_decode(q.data_ptr(), k_ring.data_ptr(), v_ring.data_ptr(),
-                               pos.data_ptr(), sink.data_ptr(), out.data_ptr(),
-                               lse.data_ptr() if lse is not None else None,
-                               B, Hq, Hkv, D, W, _dtype_code(q), _stream_handle(stream, dev))
-    _check("swa_sink_decode", st)
+    if lse is not None:
+        _out_check("lse", lse, (B, Hq), (torch.float32,), dev)
+    _call("swa_sink_decode", dev, q.data_ptr(), k_ring.data_ptr(), v_ring.data_ptr(),
+          pos.data_ptr(), sink.data_ptr(), out.data_ptr(),
+          lse.data_ptr() if lse is not None else None,
+          B, Hq, Hkv, D, W, _dtype_code(q), _stream_handle(stream, dev))
     return out, lse
 
 
@@ -314,14 +342,15 @@ def swa_sink_verify(q, k_new, v_new, k_ring, v_ring, pos, sink, out=None, lse=No
         raise ValueError("sink must be float32 [Hq]")
     if out is None:
         out = torch.empty(B, L, Hq, D, dtype=torch.float32, device=dev)
+    _out_check("out", out, (B, L, Hq, D), (torch.float32,), dev)
     if with_lse and lse is None:
         lse = torch.empty(B, Hq, L, dtype=torch.float32, device=dev)
-    st = lib().swa_sink_verify(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
-                               k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(),
-                               sink.data_ptr(), out.data_ptr(),
-                               lse.data_ptr() if lse is not None else None,
-                               B, L, Hq, Hkv, D, W, _dtype_code(q), _stream_handle(stream, dev))
-    _check("swa_sink_verify", st)
+    if lse is not None:
+        _out_check("lse", lse, (B, Hq, L), (torch.float32,), dev)
+    _call("swa_sink_verify", dev, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+          k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(), sink.data_ptr(), out.data_ptr(),
+          lse.data_ptr() if lse is not None else None,
+          B, L, Hq, Hkv, D, W, _dtype_code(q), _stream_handle(stream, dev))
     return out, lse
 
 
@@ -335,9 +364,8 @@ def swa_rope(x, pos0, rot_dim: int, theta: float, *, stream=None):
     _cuda_contig("pos0", pos0, dev)
     if pos0.dtype != torch.int64 or pos0.shape != (B,):
         raise ValueError("pos0 must be int64 [B]")
-    st = lib().swa_rope(x.data_ptr(), pos0.data_ptr(), B, T, H, D, int(rot_dim), float(theta),
-                        _dtype_code(x), _stream_handle(stream, dev))
-    _check("swa_rope", st)
+    _call("swa_rope", dev, x.data_ptr(), pos0.data_ptr(), B, T, H, D, int(rot_dim),
+          float(theta), _dtype_code(x), _stream_handle(stream, dev))
     return x
 
 
@@ -355,18 +383,17 @@ def swa_rope_append(q, k, v, k_ring, v_ring, pos, rot_dim: int, theta: float, q_
     for n, t in (("q", q), ("k", k), ("v", v), ("k_ring", k_ring), ("v_ring", v_ring),
                  ("pos", pos), ("q_out", q_out)):
         _cuda_contig(n, t, dev)
-    if k.shape != (B, Hkv, D) or v.shape != k.shape or v_ring.shape != k_ring.shape:
-        raise ValueError("shape mismatch between new tokens and rings")
+    if (k.shape != (B, Hkv, D) or v.shape != k.shape or k_ring.shape != (B, Hkv, W, D)
+            or v_ring.shape != k_ring.shape or q_out.shape != q.shape):
+        raise ValueError("shape mismatch between q, q_out, the new tokens and the rings")
     if pos.dtype != torch.int64 or pos.shape != (B,):
         raise ValueError("pos must be int64 [B]")
     for n, t in (("k", k), ("v", v), ("k_ring", k_ring), ("v_ring", v_ring), ("q_out", q_out)):
         if t.dtype != q.dtype:
             raise TypeError(f"{n} must have the dtype of q")
-    st = lib().swa_rope_append(q.data_ptr(), k.data_ptr(), v.data_ptr(), q_out.data_ptr(),
-                               k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(), B, Hq, Hkv,
-                               D, W, int(rot_dim), float(theta), _dtype_code(q),
-                               _stream_handle(stream, dev))
-    _check("swa_rope_append", st)
+    _call("swa_rope_append", dev, q.data_ptr(), k.data_ptr(), v.data_ptr(), q_out.data_ptr(),
+          k_ring.data_ptr(), v_ring.data_ptr(), pos.data_ptr(), B, Hq, Hkv, D, W, int(rot_dim),
+          float(theta), _dtype_code(q), _stream_handle(stream, dev))
     return q_out
 
 
@@ -396,11 +423,9 @@ def swa_sink_fwd_scores(q, k, v, sink, W: int, *, out_dtype=None, stream=None):
     lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
     bm = torch.full((B, Hkv, (T + 3) // 4, (T + 127) // 128), float("-inf"),
                     dtype=torch.float32, device=dev)
-    st = lib().swa_sink_fwd_scores(q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
-                                   out.data_ptr(), lse.data_ptr(), bm.data_ptr(), B, T, Hq, Hkv,
-                                   D, int(W), _dtype_code(q), _dtype_code(out),
-                                   _stream_handle(stream, dev))
-    _check("swa_sink_fwd_scores", st)
+    _call("swa_sink_fwd_scores", dev, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+          sink.data_ptr(), out.data_ptr(), lse.data_ptr(), bm.data_ptr(), B, T, Hq, Hkv, D,
+          int(W), _dtype_code(q), _dtype_code(out), _stream_handle(stream, dev))
     return out, lse, bm
 
 
@@ -413,9 +438,8 @@ def swa_topk_blocks(scores, T: int, QB: int, topk: int, *, stream=None):
     if scores.dtype != torch.float32 or scores.shape != (B, Hkv, (T + 3) // 4, (T + 127) // 128):
         raise ValueError("scores must be float32 [B, Hkv, ceil(T/4), ceil(T/128)]")
     idx = torch.empty(B, Hkv, (T + QB - 1) // QB, topk, dtype=torch.int32, device=dev)
-    st = lib().swa_topk_blocks(scores.data_ptr(), idx.data_ptr(), B, int(T), Hkv, int(QB),
-                               int(topk), _stream_handle(stream, dev))
-    _check("swa_topk_blocks", st)
+    _call("swa_topk_blocks", dev, scores.data_ptr(), idx.data_ptr(), B, int(T), Hkv,
+          int(QB), int(topk), _stream_handle(stream, dev))
     return idx
 
 
@@ -429,11 +453,10 @@ def swa_sink_sparse_fwd(q, k, v, sink, idx, QB: int, *, out_dtype=None, stream=N
         raise ValueError("idx must be int32 [B, Hkv, ceil(T/QB), topk]")
     out = torch.empty(B, T, Hq, D, dtype=out_dtype or torch.float32, device=dev)
     lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
-    st = lib().swa_sink_sparse_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), sink.data_ptr(),
-                                   idx.data_ptr(), out.data_ptr(), lse.data_ptr(), B, T, Hq, Hkv,
-                                   D, int(QB), int(idx.shape[3]), _dtype_code(q),
-                                   _dtype_code(out), _stream_handle(stream, dev))
-    _check("swa_sink_sparse_fwd", st)
+    _call("swa_sink_sparse_fwd", dev, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+          sink.data_ptr(), idx.data_ptr(), out.data_ptr(), lse.data_ptr(), B, T, Hq, Hkv, D,
+          int(QB), int(idx.shape[3]), _dtype_code(q), _dtype_code(out),
+          _stream_handle(stream, dev))
     return out, lse
 
 
@@ -449,7 +472,9 @@ def swa_ring_append(k_new, v_new, k_ring, v_ring, pos, *, stream=None):
         raise ValueError("shape mismatch between new tokens and rings")
     if pos.dtype != torch.int64 or pos.shape != (B,):
         raise ValueError("pos must be int64 [B]")
-    st = lib().swa_ring_append(k_new.data_ptr(), v_new.data_ptr(), k_ring.data_ptr(),
-                               v_ring.data_ptr(), pos.data_ptr(), B, Hkv, D, W,
-                               _dtype_code(k_ring), _stream_handle(stream, dev))
-    _check("swa_ring_append", st)
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("v_ring", v_ring)):
+        if t.dtype != k_ring.dtype:
+            raise TypeError(f"{n} must have the dtype of k_ring")
+    _call("swa_ring_append", dev, k_new.data_ptr(), v_new.data_ptr(), k_ring.data_ptr(),
+          v_ring.data_ptr(), pos.data_ptr(), B, Hkv, D, W, _dtype_code(k_ring),
+          _stream_handle(stream, dev))

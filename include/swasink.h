@@ -36,6 +36,9 @@
  *     returns SWA_ECUDA (text in swa_last_error()).  Nothing traps on the
  *     device: a device-side wait that runs past its time limit records a code
  *     readable with swa_device_error() and the kernel returns early.
+ *   - The current CUDA device (cudaSetDevice) must be the one that holds the
+ *     device buffers and owns `stream`: the library launches on the current
+ *     device and sets its kernels' attributes there.
  *   - Sizes are int; element offsets are computed in 64 bits.
  */
 #ifndef SWASINK_H
