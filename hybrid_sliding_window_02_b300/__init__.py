@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             L.swa_sink_fwd_ex.restype = i32
             L.swa_sink_fwd_host.argtypes = [p] * 11 + [i32] * 8 + [p]
             L.swa_sink_fwd_host.restype = i32
+            L.swa_sink_fwd_host_static.argtypes = [p] * 6 + [i32] * 8 + [p]
+            L.swa_sink_fwd_host_static.restype = i32
             L.swa_sink_decode.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, p]
             L.swa_ring_append.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, p]
             L.swa_sink_verify.argtypes = [p, p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32,
@@ -272,6 +274,43 @@ def _host_out_check(out_h, lse_h, B, T, Hq, D):
     if lse_h is not None and (lse_h.is_cuda or tuple(lse_h.shape) != (B, Hq, T) or
                               lse_h.dtype != torch.float32 or not lse_h.is_contiguous()):
         raise ValueError("lse_h must be a contiguous CPU float32 tensor [B, Hq, T]")
+
+
+def swa_sink_fwd_host_static(q_h, k_h, v_h, sink, W: int, out_h=None, lse_h=None, *,
+                             with_lse: bool = True, out_dtype=None, stream=None):
+    """swa_sink_fwd_host for callers that cannot allocate device memory: the
+    data in transit goes through the library's own static staging array
+    (SWA_HOST_STATIC_BYTES per GPU), so no device buffer is passed or made.
+    Raises SwaError (unsupported) when the sizes need more staging than that.
+    Calls whose GPU work overlaps share the array and race; order them on one
+    stream.  Returns (out_h, lse_h or None), complete once the stream has been
+    synchronised."""
+    import torch
+    B, T, Hq, D = q_h.shape
+    Hkv = k_h.shape[2]
+    for n, t in (("q_h", q_h), ("k_h", k_h), ("v_h", v_h)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU tensor")
+    if k_h.shape != (B, T, Hkv, D) or v_h.shape != k_h.shape:
+        raise ValueError("k_h and v_h must be [B, T, Hkv, D] matching q_h")
+    if k_h.dtype != q_h.dtype or v_h.dtype != q_h.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if sink.dtype != torch.float32 or sink.shape != (Hq,):
+        raise ValueError("sink must be float32 [Hq]")
+    dev = sink.device
+    _cuda_contig("sink", sink, dev)
+    odt = out_dtype or (out_h.dtype if out_h is not None else torch.float32)
+    pin = q_h.is_pinned()
+    if out_h is None:
+        out_h = torch.empty(B, T, Hq, D, dtype=odt, pin_memory=pin)
+    if with_lse and lse_h is None:
+        lse_h = torch.empty(B, Hq, T, dtype=torch.float32, pin_memory=pin)
+    _host_out_check(out_h, lse_h, B, T, Hq, D)
+    _call("swa_sink_fwd_host_static", dev, q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
+          sink.data_ptr(), out_h.data_ptr(), lse_h.data_ptr() if lse_h is not None else None,
+          B, T, Hq, Hkv, D, int(W), _dtype_code(q_h), _dtype_code(out_h),
+          _stream_handle(stream, dev))
+    return out_h, lse_h
 
 
 def swa_sink_decode(q, k_ring, v_ring, pos, sink, out=None, lse=None, *, with_lse=True,

@@ -740,6 +740,91 @@ swa_status swa_sink_fwd_host(const void* q_h, const void* k_h, const void* v_h,
   return rc != SWA_OK ? rc : rc_wait;
 }
 
+}  // extern "C"
+
+// ---- host-memory prefill with library-owned staging (no allocation) -------
+// Staging for swa_sink_fwd_host_static: one array per GPU, reserved when the
+// library's module is loaded on that GPU and held until the process exits.
+// Host code must not use the name as a device address; the address comes
+// from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_host_staging[SWA_HOST_STATIC_BYTES];
+
+namespace {
+struct StagingAddr {
+  bool ready = false;
+  unsigned char* ptr = nullptr;
+};
+StagingAddr g_staging_addr[kMaxDevices];
+std::mutex g_staging_mu;
+
+// Device address of g_host_staging on `dev`, which must be the current device.
+bool staging_base(int dev, unsigned char** base) {
+  std::lock_guard<std::mutex> lk(g_staging_mu);
+  StagingAddr& s = g_staging_addr[dev];
+  if (!s.ready) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_host_staging);
+    if (e != cudaSuccess) {
+      set_cuda_error("cudaGetSymbolAddress(staging)", e);
+      return false;
+    }
+    s.ptr = static_cast<unsigned char*>(p);
+    s.ready = true;
+  }
+  *base = s.ptr;
+  return true;
+}
+
+// a * b, saturated far above any staging size (sizes are positive ints).
+unsigned long long mul_sat(unsigned long long a, unsigned long long b) {
+  const unsigned long long cap = 1ull << 62;
+  return (a != 0 && b > cap / a) ? cap : a * b;
+}
+
+unsigned long long round256(unsigned long long n) { return (n + 255ull) & ~255ull; }
+}  // namespace
+
+extern "C" {
+
+swa_status swa_sink_fwd_host_static(const void* q_h, const void* k_h, const void* v_h,
+                                    const float* sink, void* out_h, float* lse_h, int B, int T,
+                                    int Hq, int Hkv, int D, int W, swa_dtype in_dtype,
+                                    swa_dtype out_dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (!q_h || !k_h || !v_h || !out_h || !sink) return SWA_EINVAL;
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return SWA_EINVAL;
+  if (in_dtype != SWA_F32 && in_dtype != SWA_BF16) return SWA_EINVAL;
+  if (out_dtype != SWA_F32 && out_dtype != SWA_BF16) return SWA_EINVAL;
+  if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
+  // staging for q, k, v, out and lse, each at a 256-byte boundary
+  const unsigned long long ie = in_dtype == SWA_BF16 ? 2 : 4, oe = out_dtype == SWA_BF16 ? 2 : 4;
+  const unsigned long long pos = mul_sat((unsigned long long)B, (unsigned long long)T);
+  const unsigned long long q_bytes = mul_sat(mul_sat(pos, (unsigned long long)Hq * D), ie);
+  const unsigned long long k_bytes = mul_sat(mul_sat(pos, (unsigned long long)Hkv * D), ie);
+  const unsigned long long o_bytes = mul_sat(mul_sat(pos, (unsigned long long)Hq * D), oe);
+  const unsigned long long l_bytes = lse_h ? mul_sat(pos, (unsigned long long)Hq * 4) : 0;
+  const unsigned long long off_k = round256(q_bytes), off_v = off_k + round256(k_bytes);
+  const unsigned long long off_o = off_v + round256(k_bytes);
+  const unsigned long long off_l = off_o + round256(o_bytes);
+  const unsigned long long need = off_l + round256(l_bytes);
+  if (need > (unsigned long long)SWA_HOST_STATIC_BYTES) {
+    snprintf(g_last_error, sizeof g_last_error,
+             "swa_sink_fwd_host_static: these sizes need %llu bytes of staging; the library's "
+             "static staging holds %llu (SWA_HOST_STATIC_BYTES)",
+             need, (unsigned long long)SWA_HOST_STATIC_BYTES);
+    return SWA_EUNSUPPORTED;
+  }
+  int dev;
+  if (!current_device(&dev)) return SWA_ECUDA;
+  unsigned char* base = nullptr;
+  if (!staging_base(dev, &base)) return SWA_ECUDA;
+  // Every byte the pipeline reads from the staging is written earlier in the
+  // same call, so nothing left by an earlier call is ever read: no clearing.
+  return swa_sink_fwd_host(q_h, k_h, v_h, sink, out_h, lse_h, base, base + off_k, base + off_v,
+                           base + off_o, lse_h ? reinterpret_cast<float*>(base + off_l) : nullptr,
+                           B, T, Hq, Hkv, D, W, in_dtype, out_dtype, stream);
+}
+
 swa_status swa_sink_decode(const void* q, const void* k_ring, const void* v_ring,
                            const int64_t* pos, const float* sink, float* out, float* lse, int B,
                            int Hq, int Hkv, int D, int W, swa_dtype in_dtype, void* stream) {

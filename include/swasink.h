@@ -131,6 +131,43 @@ swa_status swa_sink_fwd_host(const void* q_h, const void* k_h, const void* v_h,
                              int Hq, int Hkv, int D, int W, swa_dtype in_dtype,
                              swa_dtype out_dtype, void* stream);
 
+/* Size in bytes of the staging array swa_sink_fwd_host_static uses (64 MiB). */
+#define SWA_HOST_STATIC_BYTES (64u * 1024u * 1024u)
+
+/*
+ * swa_sink_fwd_host_static -- swa_sink_fwd_host without device buffers from
+ * the caller: the data in transit is staged in one array of
+ * SWA_HOST_STATIC_BYTES that the library reserves on each GPU that loads it,
+ * held until the process exits.  The pages have no counterpart to this call;
+ * it serves callers that cannot call cudaMalloc: code whose device memory is
+ * owned by another allocator (a framework's caching allocator, a budget fixed
+ * at start-up) and loops that must not call cudaMalloc or cudaFree, which can
+ * synchronise the whole device.  The call allocates no device memory itself.
+ *   q_h, k_h, v_h, sink, out_h, lse_h, sizes, dtypes and stream: as
+ *   swa_sink_fwd_host (lse_h may be NULL).
+ *   The staging needs q, k, v, out and (if lse_h is given) lse in full, each
+ *   rounded up to 256 bytes: with bf16 inputs, fp32 output and lse, D = 128,
+ *   Hq = 64 and Hkv = 8 that is 53,504 bytes per position, about 1250
+ *   positions in all.  Larger sizes return SWA_EUNSUPPORTED, with the bytes
+ *   needed in swa_last_error(), before anything is enqueued.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current) and keeps it; make that first call before any
+ *   stream capture.  The library keeps the streams and events of
+ *   swa_sink_fwd_host as well.
+ *   Every call on a device shares the one array, which keeps the last call's
+ *   contents; each call writes every staged byte before reading it, so
+ *   nothing needs clearing between calls.  Calls whose GPU work overlaps
+ *   (on different streams, or from several host threads) race on the array
+ *   and corrupt each other's results: order them on one stream, or
+ *   synchronise between them.
+ * Returns SWA_OK, SWA_EINVAL, SWA_EUNSUPPORTED or SWA_ECUDA as
+ * swa_sink_fwd_host does.
+ */
+swa_status swa_sink_fwd_host_static(const void* q_h, const void* k_h, const void* v_h,
+                                    const float* sink, void* out_h, float* lse_h, int B, int T,
+                                    int Hq, int Hkv, int D, int W, swa_dtype in_dtype,
+                                    swa_dtype out_dtype, void* stream);
+
 /*
  * swa_sink_decode -- one query token per sequence against a W-slot ring cache
  * ("pwwt.cn" MiMo-V2-Flash essay, section 1.1: the sliding-window KV cache has
