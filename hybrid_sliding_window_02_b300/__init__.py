@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
             L.swa_last_error.restype = ctypes.c_char_p
             L.swa_device_error.restype = i32
             L.swa_version.restype = i32
+            L.swa_test_withhold_loads.argtypes = [i32]
+            L.swa_test_withhold_loads.restype = i32
             _lib = L
     return _lib
 

@@ -1,19 +1,20 @@
 // decode_tc.cuh -- one-token decode against the 128-slot ring cache with the
 // per-group contractions on the 5th-generation tensor cores.
 //
-// Operation: for each sequence b and kv head g, the G = 8 query heads of the
-// group attend to the W = 128 ring slots of (b, g) with the sink-biased
+// Operation: for each sequence b and kv head g, the G query heads of the
+// group (G = 1, 2, 4, 8 or 16) attend to the W = 128 ring slots of (b, g) with
+// the sink-biased
 // softmax ("MiMo-V2-Flash Technical Report" summary, section 前置知识; the
 // fixed-size O(W) sliding-window cache of the "pwwt.cn" essay, section 1.1).
 // Slot s holds position pos - ((pos - s) mod W); while pos < W - 1 the slots
 // s > pos are empty and are ignored whatever they hold.
 //
 // The call moves about 147 MB (two 32 KB rings per group) and is bound by HBM
-// bandwidth, but each group's work is a dense contraction of 8 heads x 128
+// bandwidth, but each group's work is a dense contraction of G heads x 128
 // slots x 128 dims twice over: on the CUDA cores the FMAs alone take about
-// two thirds of the transfer time, so they run on the tensor cores instead
-// and the CUDA cores only do the softmax:
-//   S^T = K q^T      M = 128 slots, N = 16 (8 heads + 8 unused), K = 128 dims
+// two thirds of the transfer time (G = 8), so they run on the tensor cores
+// instead and the CUDA cores only do the softmax:
+//   S^T = K q^T      M = 128 slots, N = 16 (G heads + 16 - G unused), K = 128 dims
 //   O^T = V^T P^T    M = 128 dims (V read MN-major), N = 16, K = 128 slots
 // Persistent CTAs (one per SM) take groups u = blockIdx.x, + gridDim.x, ...;
 // a producer thread keeps groups' K and q (two slots, free once S^T is done)
@@ -22,9 +23,10 @@
 // threads issue the MMAs, one the S^T products and one the O^T products, so
 // that waiting for a group's K slot to land never delays the PV of the group
 // before it (and with it the release of that group's V slot).  Two softmax
-// warpgroups take alternate groups: thread = slot reads its 8 head scores
-// from TMEM, the max and the sum over slots are warp-shuffle reductions
-// finished across the four warps in shared memory, the bf16 P^T goes to
+// warpgroups take alternate groups: thread = slot reads its G head scores
+// from TMEM, the max and the sum over slots are warp-shuffle reductions (one
+// transposed butterfly for all heads) finished across the four warps in
+// shared memory, the bf16 P^T goes to
 // shared memory for the second MMA, and after it thread = dim reads O^T from
 // TMEM and writes out[b, h, dim] (each warp 128 contiguous bytes).
 #pragma once
@@ -37,8 +39,7 @@ namespace dectc {
 
 constexpr int kThreads = 352;
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
-constexpr int kG = 8;              // query heads per kv head
-constexpr int kN = 16;             // MMA N: heads padded to 16
+constexpr int kN = 16;             // MMA N: the G heads of a group padded to 16
 constexpr int kW = 128;            // ring slots
 constexpr int kD = 128;
 
@@ -56,7 +57,7 @@ constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + (int)kKSlots * kKSlotBytes;
 constexpr int kOffP = kOffV + (int)kVSlots * kVSlotBytes;       // 2 buffers (one per warpgroup)
 constexpr int kOffRed = kOffP + 2 * kPBytes;                    // [wg][warp][head] floats
-constexpr int kRedBytes = 2 * 4 * kG * 4;
+constexpr int kRedBytes = 2 * 4 * kN * 4;                       // room for G <= 16
 constexpr int kOffBar = kOffRed + 2 * kRedBytes;
 constexpr int kBarKFull = 0, kBarKEmpty = kBarKFull + kKSlots, kBarVFull = kBarKEmpty + kKSlots,
               kBarVEmpty = kBarVFull + kVSlots, kBarSFull = kBarVEmpty + kVSlots,
@@ -98,6 +99,40 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
+// Reduces v[h] over the 32 lanes of a warp for every head h < G (1, 2, 4, 8
+// or 16) with a transposed butterfly: at each of the first log2 G steps a lane
+// hands the half of its values it does not keep to its partner and combines
+// the half it keeps with the partner's, then the last 5 - log2 G steps
+// combine one value.  That is G - 1 + 5 - log2 G shuffles in all, against 5 G
+// for one butterfly per head (16 against 80 at G = 16).  Lane l ends with the
+// result for head l >> (5 - log2 G); v is used up.
+template <int kG, bool kMax>
+__device__ __forceinline__ float warp_reduce_heads(float (&v)[kG], int lane) {
+  constexpr int kLg = kG == 1 ? 0 : kG == 2 ? 1 : kG == 4 ? 2 : kG == 8 ? 3 : 4;
+  static_assert((1 << kLg) == kG, "G is a power of two up to 16");
+#pragma unroll
+  for (int st = 0; st < kLg; ++st) {
+    const int off = 16 >> st;
+    const int half = kG >> (st + 1);
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float give = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, give, off);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int off = 16 >> kLg; off > 0; off >>= 1) {
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], off);
+    v[0] = kMax ? fmaxf(v[0], got) : v[0] + got;
+  }
+  return v[0];
+}
+
+// G query heads per kv head (1, 2, 4, 8 or 16)
+template <int kG>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v,
@@ -134,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarDrain + 1), 1);
     fence_mbar_init();
   }
-  // P^T rows 8..15 (the padding heads) stay zero for the whole kernel
+  static_assert(kG >= 1 && kG <= kN, "a group's heads fill at most the 16 MMA columns");
+  // P^T rows G..15 (the padding heads) stay zero for the whole kernel
   for (int i = tid; i < 2 * kPBytes / 16; i += kThreads)
     st_shared_v4(sbase + kOffP + 16 * i, 0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
@@ -297,10 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar(kBarSFull + w), ((uint32_t)k >> 1) & 1, kErrWaitSFull, abort_flag))
         break;
       tc_fence_after();
-      uint32_t sr[8];
-      tmem_ld8(tmem + lane_addr + col_s(w), sr);
+      uint32_t sr[kG > 8 ? 16 : 8];
+      tmem_ld8(tmem + lane_addr + col_s(w), *reinterpret_cast<uint32_t(*)[8]>(&sr[0]));
+      if constexpr (kG > 8)
+        tmem_ld8(tmem + lane_addr + col_s(w) + 8, *reinterpret_cast<uint32_t(*)[8]>(&sr[8]));
       tmem_ld_wait();
-      reg_fence8(sr);
+      reg_fence8(*reinterpret_cast<uint32_t(*)[8]>(&sr[0]));
+      if constexpr (kG > 8) reg_fence8(*reinterpret_cast<uint32_t(*)[8]>(&sr[8]));
       float x[kG], m[kG];
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
@@ -308,14 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         m[h] = x[h];
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int h = 0; h < kG; ++h) m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], off));
       {
-        float mine = m[0];  // lane h < 8 publishes head h
-#pragma unroll
-        for (int h = 1; h < kG; ++h) mine = lane == h ? m[h] : mine;
-        if (lane < kG) red[quad * kG + lane] = mine;
+        // the warp's max for head lane >> (5 - log2 G); the first lane of each
+        // head publishes it
+        const float mine = warp_reduce_heads<kG, true>(m, lane);
+        if ((lane & (32 / kG - 1)) == 0) red[quad * kG + lane / (32 / kG)] = mine;
       }
       mbar_arrive(bar_max);
       if (!mbar_wait(bar_max, ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag)) break;
@@ -353,14 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + w));
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int h = 0; h < kG; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
       {
-        float mine = l[0];
-#pragma unroll
-        for (int h = 1; h < kG; ++h) mine = lane == h ? l[h] : mine;
-        if (lane < kG) red[4 * kG + quad * kG + lane] = mine;
+        const float mine = warp_reduce_heads<kG, false>(l, lane);
+        if ((lane & (32 / kG - 1)) == 0) red[4 * kG + quad * kG + lane / (32 / kG)] = mine;
       }
       mbar_arrive(bar_sum);
       if (!mbar_wait(bar_sum, ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag)) break;
@@ -373,14 +404,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == h && p.lse != nullptr)
           p.lse[(int64_t)b * p.Hq + g * kG + h] = (m[h] + __log2f(lt)) * 0.6931471805599453f;
       }
-      // O^T[dim t][h] -> out[b, g*8 + h, t]
+      // O^T[dim t][h] -> out[b, g*G + h, t]
       if (!mbar_wait(bar(kBarOFull + w), ((uint32_t)k >> 1) & 1, kErrWaitOFull, abort_flag))
         break;
       tc_fence_after();
-      uint32_t o[8];
-      tmem_ld8(tmem + lane_addr + col_o(w), o);
+      uint32_t o[kG > 8 ? 16 : 8];
+      tmem_ld8(tmem + lane_addr + col_o(w), *reinterpret_cast<uint32_t(*)[8]>(&o[0]));
+      if constexpr (kG > 8)
+        tmem_ld8(tmem + lane_addr + col_o(w) + 8, *reinterpret_cast<uint32_t(*)[8]>(&o[8]));
       tmem_ld_wait();
-      reg_fence8(o);
+      reg_fence8(*reinterpret_cast<uint32_t(*)[8]>(&o[0]));
+      if constexpr (kG > 8) reg_fence8(*reinterpret_cast<uint32_t(*)[8]>(&o[8]));
       tc_fence_before();
       float* ob = p.out + ((int64_t)b * p.Hq + g * kG) * kD + t;
 #pragma unroll

@@ -28,6 +28,9 @@
 namespace {
 
 thread_local char g_last_error[256] = "";
+// CTA of the next sliding-window tensor-core launch from this thread whose
+// loads are withheld (swa_test_withhold_loads); -1: none.
+thread_local int g_withhold_cta = -1;
 
 void set_cuda_error(const char* where, cudaError_t e) {
   snprintf(g_last_error, sizeof g_last_error, "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
@@ -42,11 +45,11 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  bool tc_attr[2] = {false, false};   // [bf16 output]
+  bool tc_attr[2][2] = {};   // [bf16 output][4 heads per tile]
   bool tcg_attr[2][2] = {{false, false}, {false, false}};   // [bf16 output][scores]
   bool topk_attr = false;
-  bool dectc_attr = false;
-  bool vertc_attr = false;
+  bool dectc_attr[5] = {};   // [log2 G]
+  bool vertc_attr[2] = {false, false};   // [64 query rows]
   bool decode_attr[2][2][5] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -166,13 +169,21 @@ bool verify_tc_applies(int L, int Hq, int Hkv, int D, int W, swa_dtype dt) {
          Hq == Hkv * swa::vertc::kG && L >= 1 && L <= swa::vertc::kLmax;
 }
 
+// Query heads per sliding-window tile: 4 when G = 4, else 8 (a kv head's G =
+// 8 R query heads then form R tile groups of 8 that share its keys).
+int tc_heads_per_tile(int G) { return G == 4 ? 4 : 8; }
+
 FwdPath select_fwd(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype dt) {
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || W < 1 || Hq % Hkv) return kPathInvalid;
   if (dt != SWA_F32 && dt != SWA_BF16) return kPathInvalid;
   if (D != 64 && D != 128) return kPathInvalid;
   const int G = Hq / Hkv;
-  if (dt == SWA_BF16 && D == swa::tcswa::kD && G == swa::tcswa::kG)
-    return W <= swa::tcswa::kMaxW ? kPathTcSwa : kPathTcGlobal;
+  if (dt == SWA_BF16 && D == swa::tcswa::kD) {
+    // G = 8 R: R sets of CTAs walk the sibling groups in step (R <= 64)
+    if (W <= swa::tcswa::kMaxW && (G == 4 || (G % swa::tcswa::kGroup == 0 && G <= 512)))
+      return kPathTcSwa;
+    if (W > swa::tcswa::kMaxW && G % swa::tcglobal::kG == 0) return kPathTcGlobal;
+  }
   return kPathSimt;
 }
 
@@ -200,36 +211,41 @@ swa_status launch_simt(const void* q, const void* k, const void* v, const float*
   return check_launch("simt_fwd_kernel");
 }
 
-// Tiles n_first .. n_first + n_tiles - 1 (16 positions each) of every
-// sequence; n_tiles < 0: to the end of the sequence.
+// Tiles n_first .. n_first + n_tiles - 1 (of 128 / heads-per-tile positions
+// each) of every sequence; n_tiles < 0: to the end of the sequence.
 swa_status launch_tc_swa(const void* q, const void* k, const void* v, const float* sink,
                          void* out, float* lse, int B, int T, int Hq, int Hkv, int W,
                          bool bf16_out, cudaStream_t st, int n_first = 0, int n_tiles = -1) {
   using namespace swa::tcswa;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
-  auto kern = bf16_out ? swa_fwd_tc_kernel<true> : swa_fwd_tc_kernel<false>;
+  const int gt = tc_heads_per_tile(Hq / Hkv);
+  const bool four = gt == 4;
+  const int kNpos = 128 / gt;
+  auto kern = bf16_out ? (four ? swa_fwd_tc_kernel<true, 4> : swa_fwd_tc_kernel<true, 8>)
+                       : (four ? swa_fwd_tc_kernel<false, 4> : swa_fwd_tc_kernel<false, 8>);
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].tc_attr[bf16_out]) {
+    if (!g_dev[dev].tc_attr[bf16_out][four]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].tc_attr[bf16_out] = true;
+      g_dev[dev].tc_attr[bf16_out][four] = true;
     }
   }
+  const int Hg = Hq / gt;
   const long long ntiles_seq = n_tiles >= 0 ? n_tiles : (T + kNpos - 1) / kNpos - n_first;
-  const long long total_tiles = (long long)B * Hkv * ntiles_seq;
+  const long long total_tiles = (long long)B * Hg * ntiles_seq;
   if (total_tiles >= (1LL << 31)) {
     set_error_text("problem too large for the tensor-core kernel");
     return SWA_EUNSUPPORTED;
   }
   if (total_tiles <= 0) return SWA_OK;
   CUtensorMap mq, mk, mv;
-  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, T, B, 64, kG, kNpos) ||
+  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, T, B, 64, gt, kNpos) ||
       !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, kD, Hkv, T, B, 64, 1, kBlk) ||
       !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, kD, Hkv, T, B, 64, 1, kBlk))
     return SWA_ECUDA;
@@ -242,12 +258,19 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.W = W;
+  p.Hg = Hg;
+  p.rep = Hg / Hkv;
   p.n_first = n_first;
   p.ntiles_seq = (int)ntiles_seq;
   p.total_tiles = (int)total_tiles;
   p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
-  const long long grid = total_tiles < sms ? total_tiles : sms;
+  p.withhold_cta = g_withhold_cta;   // one launch only
+  g_withhold_cta = -1;
+  // rep equal sets of CTAs, one per sibling group (the kernel's tile ranges)
+  const long long per_set = total_tiles / p.rep;
+  const long long cps = per_set < sms / p.rep ? per_set : sms / p.rep;
+  const long long grid = cps * p.rep;
   kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
   return check_launch("swa_fwd_tc_kernel");
 }
@@ -279,7 +302,8 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
     }
   }
   const long long nitem_seq = (T + kItemPos - 1) / kItemPos;
-  const long long total = (long long)B * Hkv * nitem_seq;
+  const int Hg = Hq / kG;   // groups of 8 query heads; the scores and sparse modes have Hg = Hkv
+  const long long total = (long long)B * Hg * nitem_seq;
   if (total >= (1LL << 31)) {
     set_error_text("problem too large for the tensor-core kernel");
     return SWA_EUNSUPPORTED;
@@ -298,6 +322,8 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.W = W;
+  p.Hg = Hg;
+  p.rep = Hg / Hkv;
   p.nitem_seq = (int)nitem_seq;
   p.total_items = (int)total;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
@@ -335,10 +361,23 @@ swa_status launch_decode_t(const void* q, const void* kr, const void* vr, const 
   return check_launch("decode_kernel");
 }
 
-// Tensor-core decode: bf16, D = 128, W = 128, groups of 8 query heads.
+// Tensor-core decode: bf16, D = 128, W = 128, groups of G = 1, 2, 4, 8 or 16
+// query heads per kv head.
+int log2_group(int Hq, int Hkv) {
+  if (Hkv < 1 || Hq % Hkv) return -1;
+  switch (Hq / Hkv) {
+    case 1: return 0;
+    case 2: return 1;
+    case 4: return 2;
+    case 8: return 3;
+    case 16: return 4;
+    default: return -1;
+  }
+}
+
 bool decode_tc_applies(int Hq, int Hkv, int D, int W, swa_dtype dt) {
   return dt == SWA_BF16 && D == swa::dectc::kD && W == swa::dectc::kW &&
-         Hq == Hkv * swa::dectc::kG;
+         log2_group(Hq, Hkv) >= 0;
 }
 
 swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const int64_t* pos,
@@ -347,17 +386,22 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   using namespace swa::dectc;
   int sms;
   if (!device_sms(dev, &sms)) return SWA_ECUDA;
+  const int lg = log2_group(Hq, Hkv);
+  void (*const kernels[5])(CUtensorMap, CUtensorMap, CUtensorMap, Params) = {
+      decode_tc_kernel<1>, decode_tc_kernel<2>, decode_tc_kernel<4>, decode_tc_kernel<8>,
+      decode_tc_kernel<16>};
+  if (lg < 0) return SWA_EUNSUPPORTED;
+  auto kern = kernels[lg];
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].dectc_attr) {
-      cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!g_dev[dev].dectc_attr[lg]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(decode_tc_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].dectc_attr = true;
+      g_dev[dev].dectc_attr[lg] = true;
     }
   }
   const long long units = (long long)B * Hkv;
@@ -382,7 +426,7 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
   const long long grid = units < sms ? units : sms;
-  return launch_dependent("decode_tc_kernel", decode_tc_kernel, (unsigned)grid, kThreads, kSmemBytes, st, mk, mv, mq, p);
+  return launch_dependent("decode_tc_kernel", kern, (unsigned)grid, kThreads, kSmemBytes, st, mk, mv, mq, p);
 }
 
 swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const void* kr,
@@ -391,17 +435,20 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
   using namespace swa::vertc;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
+  // 32 query rows per group up to L = 4, else 64
+  const bool rows64 = L * kG > 32;
+  auto kern = rows64 ? verify_tc_kernel<64> : verify_tc_kernel<32>;
+  const int smem = rows64 ? Layout<64>::kSmemBytes : Layout<32>::kSmemBytes;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].vertc_attr) {
-      cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kSmemBytes);
+    if (!g_dev[dev].vertc_attr[rows64]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           smem);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(verify_tc_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].vertc_attr = true;
+      g_dev[dev].vertc_attr[rows64] = true;
     }
   }
   const long long units = (long long)B * Hkv;
@@ -428,7 +475,7 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
   const long long grid = units < sms ? units : sms;
-  return launch_dependent("verify_tc_kernel", verify_tc_kernel, (unsigned)grid, kThreads, kSmemBytes, st, mk, mv, mq, mkn, mvn, p);
+  return launch_dependent("verify_tc_kernel", kern, (unsigned)grid, kThreads, smem, st, mk, mv, mq, mkn, mvn, p);
 }
 
 template <typename Tin, int D>
@@ -570,7 +617,9 @@ swa_status host_by_position(const void* q_h, const void* k_h, const void* v_h, c
                             void* out_h, float* lse_h, void* q_d, void* k_d, void* v_d,
                             void* out_d, float* lse_d, int B, int T, int Hq, int Hkv, int W,
                             bool bf16_out, cudaStream_t st, HostPipe& hp) {
-  constexpr int kD = swa::tcswa::kD, kNpos = swa::tcswa::kNpos;
+  constexpr int kD = swa::tcswa::kD;
+  // chunks of whole tiles for either tile shape (16 or 32 positions)
+  const int kNpos = 128 / tc_heads_per_tile(Hq / Hkv), kChunkAlign = 32;
   if (!aligned16(q_d) || !aligned16(k_d) || !aligned16(v_d) || !aligned16(out_d) ||
       (lse_d && !aligned16(lse_d)))
     return SWA_EINVAL;
@@ -578,7 +627,7 @@ swa_status host_by_position(const void* q_h, const void* k_h, const void* v_h, c
   int nper = (16 + B - 1) / B;
   if (nper > T / 512) nper = T / 512;
   if (nper < 1) nper = 1;
-  const int Tc = ((T + nper - 1) / nper + kNpos - 1) / kNpos * kNpos;
+  const int Tc = ((T + nper - 1) / nper + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
   const int nchunk_seq = (T + Tc - 1) / Tc;
   const int nchunk = B * nchunk_seq;
   const size_t q_tok = (size_t)Hq * kD * 2, k_tok = (size_t)Hkv * kD * 2;
@@ -1110,6 +1159,13 @@ int swa_device_error(void) {
     return SWA_ECUDA;
   }
   return (int)v;
+}
+
+swa_status swa_test_withhold_loads(int cta) {
+  g_last_error[0] = '\0';
+  if (cta < -1) return SWA_EINVAL;
+  g_withhold_cta = cta;
+  return SWA_OK;
 }
 
 int swa_version(void) { return 100; }

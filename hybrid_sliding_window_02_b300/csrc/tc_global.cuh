@@ -14,10 +14,10 @@
 // into two Q tiles of 16 positions x 8 query heads (128 MMA rows each, row r =
 // position r / 8, head r % 8).  Both tiles share every K/V block the CTA
 // loads, which halves the K/V traffic out of L2 against one tile per block.
-// Items go to persistent CTAs (one per SM) in order of decreasing length
-// (longest causal prefix first), dealt round by round in alternating
-// direction, which keeps the per-CTA totals within about one item of each
-// other without any shared counter.
+// Items go to persistent CTAs (one per SM), dealt round by round in
+// alternating direction, in an order whose item lengths change smoothly
+// (item_coords), which keeps the per-CTA totals within about one item of
+// each other without any shared counter.
 //
 // Roles (352 threads):
 //   warp 8      TMA producer: the two Q tiles of an item, then K_j and V_j for
@@ -93,8 +93,10 @@ struct Params {
   void* out;          // float, or bf16 with kBf16Out
   float* lse;
   int B, T, Hq, Hkv, W;
+  int Hg;             // groups of 8 query heads per sequence: Hq / 8
+  int rep;            // groups per kv head: Hq / (8 Hkv) (1 with scores or sparse mode)
   int nitem_seq;      // ceil(T / 32)
-  int total_items;    // B * Hkv * nitem_seq (< 2^31, checked on the host)
+  int total_items;    // B * Hg * nitem_seq (< 2^31, checked on the host)
   float scale_log2;   // log2(e) / sqrt(D)
   // block scores (optional): blockmax[b][kvh][ceil(T/4)][ceil(T/128)], the max
   // scaled logit of each (4-position group, 128-key block) over the group's
@@ -109,29 +111,49 @@ struct Params {
 };
 
 struct Item {
-  int b, kvh, p0;     // first position of tile 0
+  int b, grp, kvh, p0;  // query heads [8 grp, 8 grp + 8), kv head grp / rep; first position of tile 0
   int jlo, nb;        // key blocks jlo .. jlo + nb - 1, or blocks[0 .. nb)
   const int* blocks;  // sparse mode: the item's block list
 };
 
-// u-th item in order of decreasing causal length.
+// The u-th item.  Dense mode: the (sequence, head group) pairs one after
+// another, the items of each in order of decreasing causal length for the
+// last pair and every second one before it, increasing for the others (a
+// snake: lengths change smoothly from one pair to the next and the run ends
+// on the shortest items).  The CTAs then share one or two kv heads at any
+// moment, whose keys and values (16.8 MB per kv head at T = 32768) stay in L2;
+// dealt longest-first over all kv heads at once, the live keys and values of
+// all 8 heads (134 MB) overflowed it and were re-read from HBM (2.8x the
+// inputs).  Sparse mode: round by round over all (sequence, kv head) pairs,
+// longest first (items are of nearly equal length there, and spreading the
+// CTAs over the kv heads measured slightly faster).
 __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
   Item it;
-  const uint32_t bkn = (uint32_t)(p.B * p.Hkv);
-  const uint32_t r = u / bkn;
-  const uint32_t bk = u - r * bkn;
+  const uint32_t bkn = (uint32_t)(p.B * p.Hg);
+  uint32_t r, bk;
+  if (p.blk_idx != nullptr) {
+    r = u / bkn;
+    bk = u - r * bkn;
+  } else {
+    bk = u / (uint32_t)p.nitem_seq;
+    r = u - bk * (uint32_t)p.nitem_seq;
+    if ((bkn - 1 - bk) & 1u) r = (uint32_t)p.nitem_seq - 1 - r;
+  }
   const int n2 = p.nitem_seq - 1 - (int)r;
-  it.b = (int)(bk / (uint32_t)p.Hkv);
-  it.kvh = (int)(bk - (uint32_t)it.b * (uint32_t)p.Hkv);
+  it.b = (int)(bk / (uint32_t)p.Hg);
+  it.grp = (int)(bk - (uint32_t)it.b * (uint32_t)p.Hg);
+  it.kvh = it.grp / p.rep;
   it.p0 = n2 * kItemPos;
   if (p.blk_idx != nullptr) {
     it.blocks = p.blk_idx + (((int64_t)it.b * p.Hkv + it.kvh) * p.nqb + it.p0 / p.qb_size) * p.topk;
-    // the list is increasing and padded with -1 at its end: count the valid
-    // entries with independent loads (a loop that stops at the first -1
-    // chains one global-load latency per entry, ~10k cycles per item start)
-    int nb = 0;
+    // the item's blocks are the entries before the first negative one; the
+    // entries are read with independent loads (a loop that stops at the
+    // first -1 chains one global-load latency per entry, ~10k cycles per
+    // item start)
+    int nb = p.topk;
 #pragma unroll 8
-    for (int i = 0; i < p.topk; ++i) nb += __ldg(it.blocks + i) >= 0 ? 1 : 0;
+    for (int i = p.topk - 1; i >= 0; --i)
+      if (__ldg(it.blocks + i) < 0) nb = i;
     it.jlo = 0;
     it.nb = nb;
     return it;
@@ -235,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t qdst = sbase + kOffQ + i * kQTile;
           const int pos = it.p0 + i * kNpos;
           mbar_arrive_expect_tx(bar(kBarQFull + i), kQTile);
-          tma_load_4d(qdst, &map_q, 0, it.kvh * kG, pos, it.b, bar(kBarQFull + i));
-          tma_load_4d(qdst + kQHalf, &map_q, 64, it.kvh * kG, pos, it.b, bar(kBarQFull + i));
+          tma_load_4d(qdst, &map_q, 0, it.grp * kG, pos, it.b, bar(kBarQFull + i));
+          tma_load_4d(qdst + kQHalf, &map_q, 64, it.grp * kG, pos, it.b, bar(kBarQFull + i));
           ++q_armed[i];
         }
         // The next item's Q tiles and first key blocks go to L2 now, so that
@@ -247,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           Item nx;
           if (ok && cta_item(k + 1, p, nx)) {
             for (int i = 0; i < kTiles; ++i) {
-              tma_prefetch_l2_4d(&map_q, 0, nx.kvh * kG, nx.p0 + i * kNpos, nx.b);
-              tma_prefetch_l2_4d(&map_q, 64, nx.kvh * kG, nx.p0 + i * kNpos, nx.b);
+              tma_prefetch_l2_4d(&map_q, 0, nx.grp * kG, nx.p0 + i * kNpos, nx.b);
+              tma_prefetch_l2_4d(&map_q, 64, nx.grp * kG, nx.p0 + i * kNpos, nx.b);
             }
             for (int t = 0; t < 2 && t < nx.nb; ++t) {
               const int key = item_block(nx, t) * kBlk;
@@ -383,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t npv = 0;
     Item it;
     for (int k = 0; cta_item(k, p, it); ++k) {
-      const int h = it.kvh * kG + g;
+      const int h = it.grp * kG + g;
       const int pos = it.p0 + ti * kNpos + (r >> 3);
       const float sk = p.sink[h] * 1.4426950408889634f;  // log2 units
       float m_run = sk;                                   // -inf for no sink
@@ -545,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos_k = it.p0 + ti * kNpos + 4 * quad + 2 * hf + kk;
             if (pos_k < p.T) {
               float* orow = static_cast<float*>(p.out) +
-                            (((long long)it.b * p.T + pos_k) * p.Hq + it.kvh * kG + rr) * kD + 2 * qd;
+                            (((long long)it.b * p.T + pos_k) * p.Hq + it.grp * kG + rr) * kD + 2 * qd;
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 st_global_v2(orow + 8 * j,

@@ -2,59 +2,64 @@
 //
 // Operation: causal sliding-window attention with GQA and a per-head sink bias
 // in the softmax denominator ("MiMo-V2-Flash Technical Report" summary, section
-// 前置知识; 128-token window in section 核心方法).  This kernel covers W <= 129
-// (the window plus one 16-position tile spans at most 9 key blocks), bf16
-// inputs, D = 128 and groups of 8 query heads per kv head.
+// 前置知识; 128-token window in section 核心方法).  This kernel covers W <= 129,
+// bf16 inputs, D = 128, and G = 4 or any multiple of 8 query heads per kv head.
 //
-// Tiling.  One tile = 16 consecutive positions x the 8 query heads of one kv
-// head = 128 MMA rows (row r = position (r / 8), head (r % 8)).  The keys that
-// tile n needs span positions [16n - W + 1, 16n + 15], i.e. key blocks
-// n-8 .. n of 16 keys: a 128 x 144 score tile of which 89% is in the window
-// (a 128-position single-head tile would need 256 keys, 50% useful).  The
-// whole window fits in tensor memory, so the softmax is an exact single pass
-// seeded with the sink (no rescaling).
+// Tiling.  One tile = kNpos consecutive positions x kG query heads = 128 MMA
+// rows (row r = position (r / kG), head (r % kG)): 16 positions x 8 heads, or
+// 32 positions x 4 heads when G = 4.  With G = 8 R the kv head's query heads
+// form R groups of 8 ("tile groups") that share its keys and values; each
+// group is walked on its own.  The keys that tile n needs span positions
+// [n kNpos - W + 1, n kNpos + kNpos - 1], i.e. the key blocks of 16 from
+// n kNew - 8 to n kNew + kNew - 1 (kNew = kNpos / 16 new blocks per tile):
+// a 128 x 144 score tile for 8 heads (89% in the window) or 128 x 160 for 4
+// heads (80%), where a 128-position single-head tile would need 256 keys (50%
+// useful).  The whole window fits in tensor memory, so the softmax is an
+// exact single pass seeded with the sink (no rescaling).
 //
-// Persistent CTAs (one per SM) walk a contiguous range of tiles in
-// (b, kv head, n) order.  Consecutive tiles of one (b, kv head) share 8 of
-// their 9 key blocks, so keys and values live in a ring of 16-key blocks in
-// shared memory and each key/value row is loaded from HBM once per run.
+// Persistent CTAs (one per SM) walk a contiguous range of tiles (order in
+// TileWalk).  Consecutive tiles of one (b, tile group) share 8 of their key
+// blocks, so keys and values live in a ring of 16-key blocks in shared memory
+// and each key/value row is loaded once per run.
 //
 // Roles (480 threads), all connected by mbarriers:
 //   warp 12     TMA producer: Q tiles (4 stages, to cover the HBM latency seen
 //               under full load) and new K/V blocks (12-slot ring)
-//   warp 13     TMEM owner + issuer of S = Q K^T (SS: M=128, N=144 split at
-//               the ring wrap, K=128)
+//   warp 13     TMEM owner + issuer of S = Q K^T (SS: M=128, N=144 or 160
+//               split at the ring wrap, K=128)
 //   warp 14     issuer of O = P V (TS: P from TMEM, V MN-major, N=128,
 //               K=16 per block); releases the ring blocks
 //               One issuing thread for both paced the kernel: its barrier
 //               waits and bookkeeping, slowed by sharing a sub-partition with
 //               three busy warps, came to ~5000 cycles per tile.
 //   warps 0..7  softmax, two threads per row: warp w reads TMEM lanes
-//               [32 (w % 4), +32); warps 0..3 take columns [0, 72), warps
-//               4..7 columns [72, 144).  Each half forms 2^(x - m_half) and
-//               the half's log-sum-exp; the two halves swap that one value
-//               through TMEM (columns [232, 236), one per half and tile
-//               parity), combine it with the sink into the row's
+//               [32 (w % 4), +32); warps 0..3 take the first half of the
+//               score columns, warps 4..7 the second.  Each half forms
+//               2^(x - m_half) and the half's log-sum-exp; the two halves
+//               swap that one value through four TMEM columns (one per half
+//               and tile parity), combine it with the sink into the row's
 //               log-sum-exp L, and write bf16 P = 2^(x - L) to TMEM; lse ->
 //               global.  Two softmax warps per SM sub-partition hide each
 //               other's latencies; the exponentials stay exact single-pass.
 //   warps 8..11 epilogue: O (TMEM) -> global (fp32, or bf16
 //               rounded from the same fp32 values).  The 16x256b
 //               TMEM read gives each group of 4 threads 32 contiguous bytes of
-//               a row, so every warp store fills 8 whole 32-byte sectors of 8
-//               lines (one position's 8 heads: 4 KB contiguous); this measured
-//               clearly faster than one 32-byte store per thread per row.
-// TMEM: S [0,144), P0 [144,216), P1 [216,288) (bf16 pairs), exchange
-// [288,292), O [384,512).
+//               a row, so every warp store fills whole 32-byte sectors (8
+//               heads: one position's 4 KB contiguous; 4 heads: two
+//               positions' 2 KB each); this measured clearly faster than one
+//               32-byte store per thread per row.
+// TMEM (kN = 144 or 160 score columns): S [0, kN), P0 [kN, 1.5 kN), P1
+// [1.5 kN, 2 kN) (bf16 pairs), exchange [2 kN, 2 kN + 4), O [384, 512).
 // QK^T of tile t+1 runs while softmax works on tile t (S is read out at once).
 // P is double-buffered, so the softmax of tile t writes its P while tile
 // t-1's PV may still be running; O is single-buffered, as the epilogue
 // empties it into registers long before the next PV is issued (that PV waits
 // for the softmax of the next tile).  TMEM holds no more: S, two P, O and
-// the exchange take 420 of 512 columns, two O buffers would need 548.
+// the exchange take 420 (8 heads) or 452 (4 heads) of 512 columns, two O
+// buffers would need 548.
 // 15 warps put 4 on three of the SM's sub-partitions, which caps registers at
-// 128 per thread: a softmax thread holds 72 scores, an epilogue thread 64
-// output values at a time.
+// 128 per thread: a softmax thread holds 72 or 80 scores, an epilogue thread
+// 64 output values at a time.
 #pragma once
 
 #include "device_common.cuh"
@@ -65,16 +70,24 @@ namespace tcswa {
 constexpr int kThreads = 480;
 constexpr int kWarpProducer = 12, kWarpMma = 13, kWarpPv = 14;
 constexpr int kWarpEpi0 = 8;
-constexpr int kG = 8;            // query heads per tile (one kv group)
-constexpr int kNpos = 16;        // positions per tile
 constexpr int kD = 128;
 constexpr int kBlk = 16;         // keys per ring block
-constexpr int kNB = 9;           // blocks per tile window
-constexpr int kN = kNB * kBlk;   // 144 score columns
-constexpr int kNh = kN / 2;      // 72 columns per softmax half
 constexpr uint32_t kRing = 12;   // ring slots
 constexpr uint32_t kQStages = 4;
-constexpr int kMaxW = (kNB - 1) * kBlk + 1;  // 129
+constexpr int kMaxW = 8 * kBlk + 1;  // 129: 8 blocks before a tile's first key block
+constexpr int kGroup = 8;        // heads of a tile group when G is a multiple of 8
+
+// Tile shape for kG query heads per tile (8, or 4 when G = 4).
+template <int kG>
+struct Shape {
+  static constexpr int kNpos = 128 / kG;        // positions per tile
+  static constexpr int kNew = kNpos / kBlk;     // key blocks a tile adds to its run
+  static constexpr int kNB = 8 + kNew;          // key blocks per tile window
+  static constexpr int kN = kNB * kBlk;         // score columns: 144 or 160
+  static constexpr int kNh = kN / 2;            // columns per softmax half
+  static constexpr uint32_t kColP = kN;         // P buffers [kN, kN + kNh), [kN + kNh, 2 kN)
+  static constexpr uint32_t kColX = 2 * kN;     // half-row exchange, 4 columns
+};
 
 // shared-memory map (bytes); swizzled regions 1024-aligned
 constexpr int kQHalf = 128 * 128;                     // 128 rows x 64 bf16
@@ -97,50 +110,69 @@ constexpr int kSmemBytes = kOffAbort + 8 + 1024;      // + slack for 1024 alignm
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColX = 288, kColO = 384;
-// P of tile t goes to buffer t % 2: columns [144, 216) or [216, 288)
-__host__ __device__ constexpr uint32_t col_p(int b) { return 144u + 72u * (uint32_t)b; }
+constexpr uint32_t kColS = 0, kColO = 384;
+static_assert(2 * Shape<4>::kN + 4 <= (int)kColO && 2 * Shape<8>::kN + 4 <= (int)kColO,
+              "S, two P buffers and the exchange end before O");
 
 struct Params {
   const float* sink;
   void* out;            // float, or bf16 with kBf16Out
   float* lse;
   int B, T, Hq, Hkv, W;
-  int n_first;          // first tile of each sequence computed (tiles of 16 positions)
-  int ntiles_seq;       // tiles computed per (sequence, kv head): n_first .. n_first + ntiles_seq - 1
-  int total_tiles;      // B * Hkv * ntiles_seq (< 2^31, checked on the host)
+  int Hg;               // tile groups per sequence: Hq / (heads per tile)
+  int rep;              // tile groups per kv head (1 unless G = 16, 24, ...)
+  int n_first;          // first tile of each sequence computed
+  int ntiles_seq;       // tiles computed per (sequence, tile group): n_first .. n_first + ntiles_seq - 1
+  int total_tiles;      // B * Hg * ntiles_seq (< 2^31, checked on the host)
   float scale_log2;     // log2(e) / sqrt(D)
   int out_align32;      // out is 32-byte aligned (bf16 output stores whole sectors)
+  int withhold_cta;     // testing aid: this CTA's producer issues no load (-1: none), so
+                        // its waits run out and it takes the error path
 };
 
-__device__ __forceinline__ void tile_coords(uint32_t u, const Params& p, int& b, int& kvh,
-                                            int& n) {
-  const uint32_t bk = u / (uint32_t)p.ntiles_seq;
-  n = p.n_first + (int)(u - bk * (uint32_t)p.ntiles_seq);
-  b = (int)(bk / (uint32_t)p.Hkv);
-  kvh = (int)(bk - (uint32_t)b * (uint32_t)p.Hkv);
-}
-
-// Tile coordinates walked one tile at a time (no divisions after the start).
+// Tile order: (sibling r, sequence b, kv head, n), where the tile group is
+// grp = kv head x rep + r.  With rep > 1 the CTAs split into rep equal sets
+// that walk the same (b, kv head, n) tiles of sibling groups at the same
+// pace, so the second set reads each key/value row shortly after the first
+// one brought it into L2; walking a kv head's groups one after the other put
+// ~110 us of other traffic between the two reads and each row came from HBM
+// twice.
 struct TileWalk {
-  int b, kvh, n;
-  __device__ __forceinline__ void start(uint32_t u, const Params& p) { tile_coords(u, p, b, kvh, n); }
+  int b, kvh, r, n;
+  int grp;   // kvh * rep + r: query heads [grp kG, grp kG + kG)
+  __device__ __forceinline__ void start(uint32_t u, const Params& p) {
+    const uint32_t bk = u / (uint32_t)p.ntiles_seq;
+    n = p.n_first + (int)(u - bk * (uint32_t)p.ntiles_seq);
+    const uint32_t nbk = (uint32_t)(p.B * p.Hkv);
+    r = (int)(bk / nbk);
+    const uint32_t bk2 = bk - (uint32_t)r * nbk;
+    b = (int)(bk2 / (uint32_t)p.Hkv);
+    kvh = (int)(bk2 - (uint32_t)b * (uint32_t)p.Hkv);
+    grp = kvh * p.rep + r;
+  }
   __device__ __forceinline__ void next(const Params& p) {
     if (++n == p.n_first + p.ntiles_seq) {
       n = p.n_first;
       if (++kvh == p.Hkv) {
         kvh = 0;
-        ++b;
+        if (++b == p.B) {
+          b = 0;
+          ++r;
+        }
       }
+      grp = kvh * p.rep + r;
     }
   }
 };
 
-template <bool kBf16Out>
+template <bool kBf16Out, int kG>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const Params p) {
+  using S = Shape<kG>;
+  constexpr int kNpos = S::kNpos, kNew = S::kNew, kNB = S::kNB, kNh = S::kNh;
+  auto col_p = [](int b) { return S::kColP + (uint32_t)(kNh * b); };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -149,11 +181,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
-  // contiguous tile range of this CTA
-  const uint32_t per = (uint32_t)p.total_tiles / gridDim.x;
-  const uint32_t rem = (uint32_t)p.total_tiles % gridDim.x;
-  const uint32_t t_begin = blockIdx.x * per + (blockIdx.x < rem ? blockIdx.x : rem);
-  const int ntile = (int)(per + (blockIdx.x < rem ? 1 : 0));
+  // contiguous tile range of this CTA: the grid (a multiple of rep) splits
+  // into rep sets of CTAs, set r dividing the tiles of sibling r evenly, so
+  // that CTA c of every set walks the same (b, kv head, n) tiles in step
+  const uint32_t cps = gridDim.x / (uint32_t)p.rep;          // CTAs per set
+  const uint32_t set = blockIdx.x / cps, cc = blockIdx.x - set * cps;
+  const uint32_t tiles_set = (uint32_t)p.total_tiles / (uint32_t)p.rep;
+  const uint32_t per = tiles_set / cps;
+  const uint32_t rem = tiles_set % cps;
+  const uint32_t t_begin = set * tiles_set + cc * per + (cc < rem ? cc : rem);
+  const int ntile = (int)(per + (cc < rem ? 1 : 0));
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -194,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpProducer) {
     // ======================= TMA producer =======================
-    if (lane == 0) {
+    if (lane == 0 && (int)blockIdx.x != p.withhold_cta) {
       uint32_t seq = 0;  // key blocks loaded so far
       int prev_bk = -1;
       int q_issued = 0;  // Q tiles loaded so far
@@ -202,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileWalk w;
       w.start(t_begin, p);
       for (int it = 0; it < ntile && ok; ++it, w.next(p)) {
-        const int b = w.b, kvh = w.kvh, n = w.n;
+        const int b = w.b, grp = w.grp, n = w.n;
+        const int kvh = grp / p.rep;
         const uint32_t qs = (uint32_t)it % kQStages;
         const uint32_t qph = ((uint32_t)it / kQStages) & 1;
         if (!mbar_wait(bar(kBarQEmpty + qs), qph ^ 1, kErrWaitQEmpty, abort_flag)) {
@@ -211,13 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t qdst = sbase + kOffQ + qs * kQStage;
         mbar_arrive_expect_tx(bar(kBarQFull + qs), kQStage);
-        tma_load_4d(qdst, &map_q, 0, kvh * kG, n * kNpos, b, bar(kBarQFull + qs));
-        tma_load_4d(qdst + kQHalf, &map_q, 64, kvh * kG, n * kNpos, b, bar(kBarQFull + qs));
+        tma_load_4d(qdst, &map_q, 0, grp * kG, n * kNpos, b, bar(kBarQFull + qs));
+        tma_load_4d(qdst + kQHalf, &map_q, 64, grp * kG, n * kNpos, b, bar(kBarQFull + qs));
         ++q_issued;
-        const int bk = b * p.Hkv + kvh;
-        const int first_blk = (bk != prev_bk) ? n - (kNB - 1) : n;
+        const int bk = b * p.Hg + grp;
+        const int last_blk = n * kNew + kNew - 1;
+        const int first_blk = last_blk - ((bk != prev_bk) ? kNB : kNew) + 1;
         prev_bk = bk;
-        for (int m = first_blk; m <= n; ++m, ++seq) {
+        for (int m = first_blk; m <= last_blk; ++m, ++seq) {
           const uint32_t slot = seq % kRing;
           if (!mbar_wait(bar(kBarKvEmpty + slot), ((seq / kRing) & 1) ^ 1, kErrWaitKvEmpty,
                          abort_flag)) {
@@ -263,10 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileWalk w;
       w.start(t_begin, p);
       for (int it = 0; it < ntile && ok; ++it) {
-        const int bk = w.b * p.Hkv + w.kvh;
+        const int bk = w.b * p.Hg + w.grp;
         const bool new_run = (bk != prev_bk);
         prev_bk = bk;
-        const int nnew = new_run ? kNB : 1;
+        const int nnew = new_run ? kNB : kNew;
         const uint32_t ws = seq + nnew - kNB;  // first block of this tile's window
         w.next(p);
         if (s_side) {
@@ -321,9 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           seq += nnew;
           // the last tile of a run releases every block of its window, the
-          // others only the oldest one (their S reads completed before the
+          // others only the oldest kNew (their S reads completed before the
           // softmax that produced this P)
-          const bool run_end = (it + 1 >= ntile) || (w.b * p.Hkv + w.kvh != bk);
+          const bool run_end = (it + 1 >= ntile) || (w.b * p.Hg + w.grp != bk);
           const int pb = it & 1;
           if (!mbar_wait(bar(kBarPFull + pb), (it >> 1) & 1, kErrWaitPFull, abort_flag)) {
             ok = false;
@@ -345,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit(bar(kBarOFull));
           umma_commit(bar(kBarPFree + pb));
-          const int nrel = run_end ? kNB : 1;
+          const int nrel = run_end ? kNB : kNew;
           slot = ws % kRing;
           for (int r = 0; r < nrel; ++r) {
             umma_commit(bar(kBarKvEmpty + slot));
@@ -365,16 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;           // tile row = TMEM lane
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const int c0 = half * kNh;                // first score column of this half
-    const int pos_in_tile = r >> 3, g = r & 7;
+    const int pos_in_tile = r / kG, g = r % kG;
     const uint32_t xbar = bar(kBarXchg + quad);
     TileWalk w;
     w.start(t_begin, p);
     for (int it = 0; it < ntile; ++it, w.next(p)) {
-      const int b = w.b, kvh = w.kvh, n = w.n;
-      const int h = kvh * kG + g;
+      const int b = w.b, grp = w.grp, n = w.n;
+      const int h = grp * kG + g;
       const float sk = p.sink[h] * 1.4426950408889634f;
       const int i = n * kNpos + pos_in_tile;            // query position
-      const int key0 = (n - (kNB - 1)) * kBlk;          // key of column 0
+      const int key0 = (n * kNew - 8) * kBlk;           // key of column 0
       // valid columns [lo, hi] of this half, in half-local indices
       const int lo = max(0, i - p.W + 1) - key0 - c0;
       const int hi = i - key0 - c0;
@@ -382,9 +421,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t sr[kNh];
       {
-        // half 0: columns 0..71 as 16,16,16,16,8; half 1: 72..143 as 8,16,16,16,16
         const uint32_t a = tmem + lane_addr + kColS + c0;
-        if (half == 0) {
+        if constexpr (kNh % 16 == 0) {
+          // 80 columns per half, 16 at a time
+#pragma unroll
+          for (int c = 0; c < kNh / 16; ++c)
+            tmem_ld16(a + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&sr[16 * c]));
+        } else if (half == 0) {
+          // half 0: columns 0..71 as 16,16,16,16,8; half 1: 72..143 as 8,16,16,16,16
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tmem_ld16(a + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&sr[16 * c]));
@@ -402,14 +446,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(kBarSFree));
 
-      // Mask in place.  Columns [16, 128) are inside every row's window whenever
-      // the warp's rows all have their first valid column <= 16 and their last
-      // >= 127 (W = 128, n >= 8): then only the first key block (half 0) or the
-      // last one (half 1) needs the per-column test.
-      const bool mid_ok = __all_sync(0xffffffffu, lo + c0 <= 16 && hi + c0 >= 127);
+      // Mask in place.  Columns [kNpos, 128) are inside every row's window
+      // whenever the warp's rows all have their first valid column <= kNpos and
+      // their last >= 127 (W = 128, n past the first tiles): then only the
+      // first kNew key blocks (half 0) or the last kNew (half 1) need the
+      // per-column test.
+      const bool mid_ok = __all_sync(0xffffffffu, lo + c0 <= kNpos && hi + c0 >= 127);
       if (mid_ok && half == 0) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
+        for (int c = 0; c < kNpos; ++c)
           if (c < lo || c > hi) sr[c] = __float_as_uint(-INFINITY);
       } else if (mid_ok) {
 #pragma unroll
@@ -457,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // log2-sum-exp of this half (-inf when empty), swapped with the other
       // half of the row through TMEM column kColX + 2 (tile parity) + half
       const float lse_h = (lh > 0.f) ? mh + __log2f(lh) : -INFINITY;
-      const uint32_t xcol = tmem + lane_addr + kColX + 2 * (it & 1);
+      const uint32_t xcol = tmem + lane_addr + S::kColX + 2 * (it & 1);
       {
         const uint32_t v = __float_as_uint(lse_h);
         tmem_st1(xcol + half, v);
@@ -479,14 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar(kBarPFree + pb), ((it >> 1) & 1) ^ 1, kErrWaitPFree, abort_flag)) break;
       tc_fence_after();
       {
-        // packed columns [36 half, 36 half + 36): half 0 as 8,8,8,8,4;
-        // half 1 as 4,8,8,8,8 (each store aligned to its width)
+        // packed columns [kNh/2 half, kNh/2 (half + 1)): 8 heads: half 0 as
+        // 8,8,8,8,4 and half 1 as 4,8,8,8,8 (each store aligned to its width);
+        // 4 heads: 8 at a time
         const uint32_t pa = tmem + lane_addr + col_p(pb) + half * (kNh / 2);
         uint32_t pk[kNh / 2];
 #pragma unroll
         for (int e = 0; e < kNh / 2; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(sr[2 * e]) * f, __uint_as_float(sr[2 * e + 1]) * f);
-        if (half == 0) {
+        if constexpr ((kNh / 2) % 8 == 0) {
+#pragma unroll
+          for (int c = 0; c < kNh / 16; ++c)
+            tmem_st8(pa + 8 * c, *reinterpret_cast<const uint32_t(*)[8]>(&pk[8 * c]));
+        } else if (half == 0) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tmem_st8(pa + 8 * c, *reinterpret_cast<const uint32_t(*)[8]>(&pk[8 * c]));
@@ -511,17 +561,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     TileWalk w;
     w.start(t_begin, p);
     for (int it = 0; it < ntile; ++it, w.next(p)) {
-      const int b = w.b, kvh = w.kvh, n = w.n;
+      const int b = w.b, grp = w.grp, n = w.n;
       if (!mbar_wait(bar(kBarOFull), it & 1, kErrWaitOFull, abort_flag)) break;
       tc_fence_after();
       const uint32_t col = tmem + kColO + ((uint32_t)(sub * 32) << 16);
       if constexpr (kBf16Out) {
-        // thread = tile row (TMEM lane 32 sub + lane): position 4 sub + lane / 8,
-        // head lane % 8; 64 consecutive columns per round, rounded to bf16 and
-        // written as whole 32-byte sectors
-        const int pos = n * kNpos + 4 * sub + (lane >> 3);
+        // thread = tile row (TMEM lane 32 sub + lane): position (32 sub +
+        // lane) / kG, head lane % kG; 64 consecutive columns per round,
+        // rounded to bf16 and written as whole 32-byte sectors
+        const int pos = n * kNpos + (32 * sub + lane) / kG;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                              (((long long)b * p.T + pos) * p.Hq + kvh * kG + (lane & 7)) * kD;
+                              (((long long)b * p.T + pos) * p.Hq + grp * kG + lane % kG) * kD;
 #pragma unroll
         for (int rd = 0; rd < 2; ++rd) {
           uint32_t o[64];
@@ -554,12 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        continue;
-      }
-      // rows of this thread: 32 sub + 16 hf + {0, 8} + rr, i.e. positions
-      // 4 sub + 2 hf + {0, 1}, head rr; columns 8j + 2 quad + {0, 1}
-      const long long row0 = ((long long)b * p.T + n * kNpos + 4 * sub) * p.Hq + kvh * kG + rr;
-      const int pos0 = n * kNpos + 4 * sub;
+      } else {
+      // rows of this thread: 32 sub + 16 hf + 8 k + rr (k = 0, 1), i.e.
+      // position (row / kG), head (row % kG); columns 8j + 2 quad + {0, 1}
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t o[64];
@@ -573,14 +620,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          if (pos0 + 2 * hf + k < p.T) {
-            const long long e0 = (row0 + (long long)(2 * hf + k) * p.Hq) * kD + 2 * quad;
+          const int row = 32 * sub + 16 * hf + 8 * k + rr;
+          const int pos = n * kNpos + row / kG;
+          if (pos < p.T) {
+            const long long e0 =
+                (((long long)b * p.T + pos) * p.Hq + grp * kG + row % kG) * kD + 2 * quad;
             float* orow = static_cast<float*>(p.out) + e0;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               st_global_v2(orow + 8 * j, o[4 * j + 2 * k], o[4 * j + 2 * k + 1]);
           }
         }
+      }
       }
     }
   }

@@ -4,20 +4,23 @@
 // Operation: as in verify.cuh (drafted tokens at positions pos .. pos+L-1
 // checked in one pass; "MiMo-V2-Flash Technical Report" summary, section
 // 核心方法), for bf16 inputs, D = 128, W = 128, groups of 8 query heads and
-// L <= 4 drafted tokens.  Per group (sequence b, kv head g) the 8L query rows
+// L <= 8 drafted tokens.  Per group (sequence b, kv head g) the 8L query rows
 // r = 8 j + h (token j, head h) sit in the first lanes of a 128-row tile:
 //   S = Q K_ring^T             tcgen05 SS, M = 128 rows, N = 128 slots, K = 128
-//   S_new = Q K_new^T          tcgen05 SS, N = 16 (the L <= 4 drafted keys;
+//   S_new = Q K_new^T          tcgen05 SS, N = 16 (the L <= 8 drafted keys;
 //                              columns L..15 are masked), into the first 16 columns of
 //                              the warpgroup's O buffer, which are free from
 //                              the output of group k - 2 to the PV of group k
 //   O = P_ring V_ring + P_new V_new
 //                              tcgen05 TS: P (bf16) written over S in TMEM,
 //                              V MN-major; the new values as one K = 16 step
-// Thread = row: lane r of the warpgroup's first warp reads its 128 slot scores
-// and its new-key scores and runs the sink-seeded softmax alone (as the
-// global-attention kernel does per key block), so no reduction crosses lanes.
-// The rows past 8L are padding that no one reads.  (Scoring the new keys on
+// Thread = row: lane r of the warpgroup's first warp (rows 32..63, for L > 4,
+// of its second) reads its 128 slot scores and its new-key scores and runs
+// the sink-seeded softmax alone (as the global-attention kernel does per key
+// block), so no reduction crosses lanes.  The rows past 8L are padding that no
+// one reads.  The kernel comes in two sizes: up to 32 rows (L <= 4: one
+// softmax warp and three that zero empty slots per warpgroup) and up to 64
+// (L <= 8: two and two, and a Q staging area twice as large).  (Scoring the new keys on
 // the CUDA cores instead, as 128-long FMA chains on three warps, put ~1700
 // cycles per group on the softmax's critical path.)
 //
@@ -51,39 +54,45 @@ namespace vertc {
 constexpr int kThreads = 352;
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr int kG = 8;
-constexpr int kLmax = 4;
+constexpr int kLmax = 8;            // drafted tokens of the larger kernel size
 constexpr int kW = 128;
 constexpr int kD = 128;
 constexpr int kNewRows = 16;        // new keys padded to one K = 16 MMA step
 
 // Two rings in shared memory (128-byte swizzle everywhere):
-//   K slots (2): Q [2 halves x 4 KB: 32 rows], K ring [2 x 16 KB],
-//                K_new [2 x 1 KB: 4 rows].  Free once S and S_new complete.
+//   K slots (2): Q [2 halves x kRows rows: 4 or 8 KB each], K ring [2 x 16 KB],
+//                K_new [2 x 1 KB: 8 rows].  Free once S and S_new complete.
 //   V slots (3): V ring [2 x 16 KB], V_new [2 x 2 KB: 16 rows, rows L..15
 //                zero].  Free once the PV completes.
 // An M = 128 MMA reads 128 rows (16 KB) from each Q half base, and the N = 16
 // S_new MMA reads 16 rows (2 KB) from each K_new half base: the rows past
 // those that hold data fall on later data in shared memory and only feed TMEM
 // lanes or columns that no one reads.
-constexpr int kHalf = 128 * 128;                // 128 rows x 64 bf16 = 16 KB
-constexpr int kQHalf = 32 * 128;                // 32 rows x 64 bf16 = 4 KB
-constexpr int kKnHalf = 8 * 128;                // 8 rows x 64 bf16 = 1 KB
-constexpr int kNewHalf = kNewRows * 128;        // 16 rows x 64 bf16 = 2 KB
-constexpr uint32_t kKSlots = 2, kVSlots = 3;
-constexpr int kKQ = 0, kKK = 2 * kQHalf, kKKn = kKK + 2 * kHalf;
-constexpr int kKSlotBytes = kKKn + 2 * kKnHalf;        // 42 KB
-constexpr int kVV = 0, kVVn = 2 * kHalf;
-constexpr int kVSlotBytes = kVVn + 2 * kNewHalf;       // 36 KB
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + (int)kKSlots * kKSlotBytes;
-constexpr int kOffBar = kOffV + (int)kVSlots * kVSlotBytes;
-constexpr int kBarKFull = 0, kBarKEmpty = kBarKFull + kKSlots, kBarVFull = kBarKEmpty + kKSlots,
-              kBarVEmpty = kBarVFull + kVSlots, kBarSFull = kBarVEmpty + kVSlots,
-              kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarODone = kBarOFull + 2,
-              kBarDrain = kBarODone + 2, kNumBars = kBarDrain + 2;
-constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr int kOffAbort = kOffTmemSlot + 8;
-constexpr int kSmemBytes = kOffAbort + 8 + 1024;
+// kRows = 32 (L <= 4) or 64 (L <= 8) query rows per group.
+template <int kRows>
+struct Layout {
+  static constexpr int kHalf = 128 * 128;                // 128 rows x 64 bf16 = 16 KB
+  static constexpr int kQHalf = kRows * 128;             // kRows rows x 64 bf16
+  static constexpr int kKnHalf = 8 * 128;                // 8 rows x 64 bf16 = 1 KB
+  static constexpr int kNewHalf = kNewRows * 128;        // 16 rows x 64 bf16 = 2 KB
+  static constexpr uint32_t kKSlots = 2, kVSlots = 3;
+  static constexpr int kKQ = 0, kKK = 2 * kQHalf, kKKn = kKK + 2 * kHalf;
+  static constexpr int kKSlotBytes = kKKn + 2 * kKnHalf;        // 42 or 50 KB
+  static constexpr int kVV = 0, kVVn = 2 * kHalf;
+  static constexpr int kVSlotBytes = kVVn + 2 * kNewHalf;       // 36 KB
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + (int)kKSlots * kKSlotBytes;
+  static constexpr int kOffBar = kOffV + (int)kVSlots * kVSlotBytes;
+  static constexpr int kBarKFull = 0, kBarKEmpty = kBarKFull + kKSlots,
+                       kBarVFull = kBarKEmpty + kKSlots, kBarVEmpty = kBarVFull + kVSlots,
+                       kBarSFull = kBarVEmpty + kVSlots, kBarPFull = kBarSFull + 2,
+                       kBarOFull = kBarPFull + 2, kBarODone = kBarOFull + 2,
+                       kBarDrain = kBarODone + 2, kNumBars = kBarDrain + 2;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 8;
+  static constexpr int kSmemBytes = kOffAbort + 8 + 1024;
+};
+static_assert(Layout<64>::kSmemBytes <= 227 * 1024, "verify stages fit shared memory");
 
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int w) { return 256u * (uint32_t)w; }
@@ -99,12 +108,27 @@ struct Params {
   float scale_log2;
 };
 
+template <int kRows>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v,
                      const __grid_constant__ CUtensorMap map_q,
                      const __grid_constant__ CUtensorMap map_kn,
                      const __grid_constant__ CUtensorMap map_vn, const Params p) {
+  using Lay = Layout<kRows>;
+  constexpr int kHalf = Lay::kHalf, kQHalf = Lay::kQHalf, kKnHalf = Lay::kKnHalf,
+                kNewHalf = Lay::kNewHalf, kKQ = Lay::kKQ, kKK = Lay::kKK, kKKn = Lay::kKKn,
+                kKSlotBytes = Lay::kKSlotBytes, kVV = Lay::kVV, kVVn = Lay::kVVn,
+                kVSlotBytes = Lay::kVSlotBytes, kOffK = Lay::kOffK, kOffV = Lay::kOffV,
+                kOffBar = Lay::kOffBar, kOffTmemSlot = Lay::kOffTmemSlot,
+                kOffAbort = Lay::kOffAbort;
+  constexpr uint32_t kKSlots = Lay::kKSlots, kVSlots = Lay::kVSlots;
+  constexpr int kBarKFull = Lay::kBarKFull, kBarKEmpty = Lay::kBarKEmpty,
+                kBarVFull = Lay::kBarVFull, kBarVEmpty = Lay::kBarVEmpty,
+                kBarSFull = Lay::kBarSFull, kBarPFull = Lay::kBarPFull,
+                kBarOFull = Lay::kBarOFull, kBarODone = Lay::kBarODone,
+                kBarDrain = Lay::kBarDrain;
+  constexpr int kSoftWarps = kRows / 32;        // softmax warps per warpgroup
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -131,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + w), 1);
       mbar_init(bar(kBarPFull + w), 128);
       mbar_init(bar(kBarOFull + w), 1);
-      mbar_init(bar(kBarODone + w), 32);
+      mbar_init(bar(kBarODone + w), 32 * kSoftWarps);
     }
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrain + 1), 1);
@@ -301,11 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w = warp >> 2;                       // warpgroup: groups k with k % 2 == w
     const int wq = warp & 3;                       // warp within the warpgroup
     const int nrow = kG * L;
-    if (wq == 0) {
+    if (wq < kSoftWarps) {
       // ============ softmax + output: thread = row r (TMEM lane r) ============
-      const int r = lane;
+      const int r = 32 * wq + lane;
+      const uint32_t lane_addr = (uint32_t)(32 * wq) << 16;
       const int j = r >> 3, h = r & 7;
-      const uint32_t s_addr = tmem + col_s(w), o_addr = tmem + col_o(w);
+      const uint32_t s_addr = tmem + lane_addr + col_s(w), o_addr = tmem + lane_addr + col_o(w);
       for (int k = w; k < nk; k += 2) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
         const int b = u / p.Hkv, g = u - b * p.Hkv;
@@ -317,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[kW], snr[8];
 #pragma unroll
         for (int c = 0; c < kW / 32; ++c) tmem_ld32(s_addr + c * 32, sr + c * 32);
-        tmem_ld8(o_addr, snr);                      // S_new: new keys 0..3 of row r
+        tmem_ld8(o_addr, snr);                      // S_new: new keys 0..7 of row r
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < kW / 32; ++c) reg_fence32(sr + c * 32);
@@ -357,16 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   fmaxf(m8[6], m8[7])) * p.scale_log2;
         // new key i of row j counts when it exists (i < L), is causal (i <= j)
         // and the sequence is live (pos >= 0)
-        float4 s4;
-        {
-          float sv[4];
+        constexpr int kNew = kRows / kG;            // new keys a row may see: 4 or 8
+        float sv[kNew];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            sv[i] = (p0 >= 0 && i < L && i <= j) ? __uint_as_float(snr[i]) * p.scale_log2
-                                                 : -INFINITY;
-          s4 = make_float4(sv[0], sv[1], sv[2], sv[3]);
-        }
-        float m = fmaxf(fmaxf(mring, sk), fmaxf(fmaxf(s4.x, s4.y), fmaxf(s4.z, s4.w)));
+        for (int i = 0; i < kNew; ++i)
+          sv[i] = (p0 >= 0 && i < L && i <= j) ? __uint_as_float(snr[i]) * p.scale_log2
+                                               : -INFINITY;
+        float m = fmaxf(mring, sk);
+#pragma unroll
+        for (int i = 0; i < kNew; ++i) m = fmaxf(m, sv[i]);
         if (m == -INFINITY) m = 0.f;                // nothing to attend to
         // ---- weights: bf16 P over S columns [0, 64), new keys at [64, 72) ----
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
@@ -388,17 +412,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st8(s_addr + c * 8, pk);
         }
-        const float pn0 = ex2_approx(s4.x - m), pn1 = ex2_approx(s4.y - m);
-        const float pn2 = ex2_approx(s4.z - m), pn3 = ex2_approx(s4.w - m);
+        float pn[kNew], ln = 0.f;
+#pragma unroll
+        for (int i = 0; i < kNew; ++i) {
+          pn[i] = ex2_approx(sv[i] - m);
+          ln += pn[i];
+        }
         {
-          const uint32_t pk[8] = {pack_bf16x2(pn0, pn1), pack_bf16x2(pn2, pn3), 0u, 0u,
-                                  0u, 0u, 0u, 0u};
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pk[e] = 0u;
+#pragma unroll
+          for (int e = 0; e < kNew / 2; ++e) pk[e] = pack_bf16x2(pn[2 * e], pn[2 * e + 1]);
           tmem_st8(s_addr + 64, pk);
         }
         float l;
         {
           const float2 a = fadd2(fadd2(l2[0], l2[1]), fadd2(l2[2], l2[3]));
-          l = (a.x + a.y) + ((pn0 + pn1) + (pn2 + pn3));
+          l = (a.x + a.y) + ln;
           if (sk != -INFINITY) l += ex2_approx(sk - m);
         }
         tmem_st_wait();
@@ -436,8 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
       }
     } else {
-      // ============ empty-slot values (warps 1..3) ============
-      const int t = (wq - 1) * 32 + lane;        // 0 .. 95
+      // ============ empty-slot values (the other warps of the warpgroup) ============
+      constexpr int kHelpers = 32 * (4 - kSoftWarps);   // 96 or 64 threads
+      const int t = (wq - kSoftWarps) * 32 + lane;
       for (int k = w; k < nk; k += 2) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
         const int b = u / p.Hkv;
@@ -455,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         // empty slots (pos < W): zero their values in the V slot before the PV
         if (p0 < kW) {
-          for (int sl = t; sl < kW; sl += 96) {
+          for (int sl = t; sl < kW; sl += kHelpers) {
             if (sl >= p0) {
               const uint32_t vrow = vst + kVV + sl * 128;
 #pragma unroll

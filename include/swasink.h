@@ -193,7 +193,9 @@ swa_status swa_sink_decode(const void* q, const void* k_ring, const void* v_ring
 
 /*
  * swa_ring_append -- write one new token per sequence into its ring slot
- * (slot = pos[b] mod W), the cache update that precedes swa_sink_decode.
+ * (slot = pos[b] mod W), the cache update that precedes swa_sink_decode: the
+ * sliding-window KV cache of fixed size, O(W) memory whatever the sequence
+ * length ("pwwt.cn" MiMo-V2-Flash essay, section 1.1).
  *   k_new, v_new [B, Hkv, D] dtype;  k_ring, v_ring [B, Hkv, W, D] dtype (updated)
  *   pos [B] int64 >= 0 (device); a negative pos leaves that sequence's ring unchanged.
  */
@@ -301,7 +303,13 @@ swa_status swa_topk_blocks(const float* scores, int* idx, int B, int T, int Hkv,
  * the denominator as in swa_sink_fwd.  k and v are the full-attention layer's
  * (the shared KV cache).
  *   idx [B, Hkv, ceil(T/QB), topk] int32: increasing block indices, -1 padded
- *   (as swa_topk_blocks writes them); QB in {32, 64, 128}.
+ *   (as swa_topk_blocks writes them); QB in {32, 64, 128}.  A list is read up
+ *   to its first negative entry: entries after it are ignored.  The entries
+ *   before it must be distinct block indices in [0, ceil(T/128)); their
+ *   order does not change the result beyond rounding (each key is masked
+ *   causally on its own).  A repeated index counts its keys twice; an index
+ *   past the end gives unspecified values, but every access stays inside
+ *   q, k, v, out and lse (the loads are bounded by the tensor maps).
  *   Other arguments as swa_sink_fwd_ex; bf16 inputs, D = 128, Hq = 8 Hkv only
  *   (else SWA_EUNSUPPORTED).
  */
@@ -315,12 +323,13 @@ swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, cons
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Name of the decode kernel swa_sink_decode would launch for these sizes
- * ("tc_decode" for bf16, D = 128, W = 128, Hq = 8 Hkv; "simt_decode"
- * otherwise), or "invalid". */
+ * ("tc_decode" for bf16, D = 128, W = 128 and Hq / Hkv in {1, 2, 4, 8, 16};
+ * "simt_decode" otherwise), or "invalid". */
 const char* swa_sink_decode_path(int B, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
-/* Name of the verify kernel swa_sink_verify would launch ("tc_verify",
- * "simt_verify"), or "invalid". */
+/* Name of the verify kernel swa_sink_verify would launch ("tc_verify" for
+ * bf16, D = 128, W = 128, Hq = 8 Hkv and L <= 8; "simt_verify" otherwise), or
+ * "invalid". */
 const char* swa_sink_verify_path(int B, int L, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Static text for a status code. */
@@ -333,6 +342,19 @@ const char* swa_last_error(void);
  * (synchronises the device).  0 = none; otherwise a code naming the wait
  * that ran past its limit.  Returns SWA_ECUDA in *code's place on failure. */
 int swa_device_error(void);
+
+/*
+ * swa_test_withhold_loads -- testing aid for the failure path: in the next
+ * launch of the sliding-window tensor-core prefill kernel (swa_sink_fwd_path
+ * "tc_swa") made from the calling host thread, CTA number `cta` issues none
+ * of its loads.  Its waits then run past their 2 s limit: the first records
+ * a wait code (0x101..0x10c) in the device error word, the CTA's other roles
+ * see it and stop waiting, the CTA frees its tensor memory and returns,
+ * leaving its tiles' out and lse rows unwritten.  The other CTAs finish
+ * normally and the device stays usable.  Applies to one launch; -1 cancels.
+ * Returns SWA_EINVAL for cta < -1.  Not for production use.
+ */
+swa_status swa_test_withhold_loads(int cta);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int swa_version(void);

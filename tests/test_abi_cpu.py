@@ -54,6 +54,13 @@ def test_path_selection(L):
     assert swa.fwd_path(1, 512, 4, 1, 64, 128, swa.SWA_F32) == "simt"
     assert swa.fwd_path(1, 512, 64, 8, 128, 128, swa.SWA_F32) == "simt"
     assert swa.fwd_path(1, 512, 64, 64, 128, 128) == "simt"
+    assert swa.fwd_path(1, 512, 16, 4, 128, 128) == "tc_swa"       # 4 heads per kv head
+    assert swa.fwd_path(1, 512, 16, 4, 128, 130) == "simt"         # ... no global kernel for 4
+    assert swa.fwd_path(1, 512, 64, 4, 128, 128) == "tc_swa"       # 16: two groups of 8
+    assert swa.fwd_path(1, 512, 64, 4, 128, 512) == "tc_global"
+    assert swa.fwd_path(1, 512, 48, 2, 128, 128) == "tc_swa"       # 24
+    assert swa.fwd_path(1, 512, 32, 16, 128, 128) == "simt"        # 2 heads per kv head
+    assert swa.fwd_path(1, 512, 12, 1, 128, 128) == "simt"         # 12: not a multiple of 8
     assert swa.fwd_path(1, 512, 64, 7, 128, 128) == "invalid"
     assert swa.fwd_path(1, 512, 64, 8, 96, 128) == "invalid"
     assert swa.fwd_path(0, 512, 64, 8, 128, 128) == "invalid"
@@ -63,7 +70,11 @@ def test_decode_path_selection(L):
     assert swa.decode_path(256, 64, 8, 128, 128) == "tc_decode"
     assert swa.decode_path(256, 64, 8, 128, 128, swa.SWA_F32) == "simt_decode"
     assert swa.decode_path(256, 64, 8, 64, 128) == "simt_decode"
-    assert swa.decode_path(256, 32, 8, 128, 128) == "simt_decode"
+    assert swa.decode_path(256, 32, 8, 128, 128) == "tc_decode"      # 4 heads per kv head
+    assert swa.decode_path(256, 64, 4, 128, 128) == "tc_decode"      # 16
+    assert swa.decode_path(256, 8, 8, 128, 128) == "tc_decode"       # 1
+    assert swa.decode_path(256, 64, 2, 128, 128) == "simt_decode"    # 32: past the MMA's 16
+    assert swa.decode_path(256, 24, 8, 128, 128) == "simt_decode"    # 3
     assert swa.decode_path(256, 64, 8, 128, 320) == "simt_decode"
     assert swa.decode_path(256, 64, 8, 128, 321) == "invalid"
     assert swa.decode_path(256, 64, 7, 128, 128) == "invalid"
@@ -142,7 +153,9 @@ def test_verify_rejects_before_launch(L, kw, status):
 def test_verify_path_selection(L):
     assert swa.verify_path(2, 4, 8, 1, 128, 128) == "tc_verify"
     assert swa.verify_path(2, 1, 64, 8, 128, 128) == "tc_verify"
-    assert swa.verify_path(2, 5, 64, 8, 128, 128) == "simt_verify"
+    assert swa.verify_path(2, 5, 64, 8, 128, 128) == "tc_verify"
+    assert swa.verify_path(2, 8, 64, 8, 128, 128) == "tc_verify"
+    assert swa.verify_path(2, 9, 64, 8, 128, 128) == "simt_verify"
     assert swa.verify_path(2, 4, 64, 8, 128, 128, swa.SWA_F32) == "simt_verify"
     assert swa.verify_path(2, 4, 8, 1, 64, 128) == "simt_verify"
     assert swa.verify_path(2, 65, 8, 1, 128, 128) == "invalid"

@@ -27,6 +27,26 @@ def test_decode_full_size_workload(cuda_ok):
     assert_lse_close(l, l_ref)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv", [(37, 64, 16), (29, 64, 4), (11, 8, 4), (13, 4, 4),
+                                       (300, 16, 1)])
+def test_decode_tc_group_sizes(cuda_ok, B, Hq, Hkv):
+    # the tensor-core decode for 4, 16, 2 and 1 query heads per kv head (the
+    # 16 MMA columns hold the group's heads, the rest padding), partial and
+    # full rings, one and several groups per sequence
+    assert swa.decode_path(B, Hq, Hkv, 128, 128) == "tc_decode"
+    x = gen.decode_inputs(B, Hq, Hkv, 128, 128, seed=B + Hq, pos_lo=0, pos_hi=600)
+    for b in range(B):
+        p = int(x.pos[b])
+        if p < 127:   # empty slots may hold anything
+            x.k_ring[b, :, p + 1:] = float("nan")
+            x.v_ring[b, :, p + 1:] = float("nan")
+    o, l = _decode(x)
+    o_ref, l_ref = oracle.swa_sink_decode(x.q, x.k_ring, x.v_ring, x.pos, x.sink)
+    assert_bf16_close(o, o_ref)
+    assert_lse_close(l, l_ref)
+    assert swa.device_error() == 0
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,D,W,dt", [
     (3, 8, 1, 128, 128, torch.bfloat16), (5, 16, 1, 64, 64, torch.bfloat16),
     (4, 4, 2, 128, 33, torch.bfloat16), (2, 16, 16, 64, 7, torch.bfloat16),

@@ -47,6 +47,18 @@ def test_tc_global_matches_oracle(cuda_ok, B, T, Hq, Hkv, W):
     _full_check(x, W)
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", [
+    (1, 700, 16, 1, 700),     # 16 heads per kv head: two groups of 8 share its keys
+    (2, 600, 32, 2, 300),
+    (1, 500, 24, 1, 500),     # three groups of 8
+    (1, 1100, 64, 1, 1100),   # eight groups: the snake order over (sequence, group) pairs
+])
+def test_tc_global_group_sizes(cuda_ok, B, T, Hq, Hkv, W):
+    assert swa.fwd_path(B, T, Hq, Hkv, 128, W) == "tc_global"
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=2100 + T + W + Hq)
+    _full_check(x, W)
+
+
 def test_tc_global_running_max_moves(cuda_ok):
     # later keys score ever higher, so the running max moves block after block
     # and O is rescaled in tensor memory many times

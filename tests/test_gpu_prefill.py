@@ -53,6 +53,25 @@ def test_tc_swa_matches_oracle(cuda_ok, B, T, Hq, Hkv, W):
     _full_check(x, W)
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", [
+    (1, 300, 4, 1, 128),      # 4 heads per kv head: tiles of 32 positions x 4 heads
+    (2, 1000, 16, 4, 128),
+    (1, 77, 8, 2, 33),
+    (1, 300, 4, 1, 1),
+    (1, 300, 4, 1, 129),
+    (1, 4099, 32, 8, 128),    # many runs per CTA, ragged tail
+    (1, 300, 16, 1, 128),     # 16 heads per kv head: two groups of 8 share its keys
+    (2, 1000, 64, 4, 128),
+    (1, 513, 32, 2, 100),
+    (1, 200, 24, 1, 128),     # 24: three groups of 8
+    (1, 300, 64, 1, 128),     # 64: eight groups of 8
+])
+def test_tc_swa_group_sizes(cuda_ok, B, T, Hq, Hkv, W):
+    assert swa.fwd_path(B, T, Hq, Hkv, 128, W) == "tc_swa"
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=1100 + T + W + Hq)
+    _full_check(x, W)
+
+
 def test_tc_swa_sink_limits(cuda_ok):
     x = gen.prefill_inputs(1, 200, 8, 1, 128, seed=5)
     # no sink: plain windowed softmax
@@ -131,7 +150,8 @@ def test_simt_fp32_shapes(cuda_ok, B, T, Hq, Hkv, D, W):
 
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [
-    (1, 300, 4, 1, 128, 128), (2, 100, 8, 8, 64, 33), (1, 200, 4, 1, 128, 200),
+    (1, 300, 2, 1, 128, 128), (2, 100, 8, 8, 64, 33), (1, 200, 4, 1, 128, 200),
+    (1, 150, 12, 1, 128, 128),
 ])
 def test_simt_bf16_shapes(cuda_ok, B, T, Hq, Hkv, D, W):
     assert swa.fwd_path(B, T, Hq, Hkv, D, W) == "simt"
@@ -196,6 +216,7 @@ def test_no_device_error_recorded(cuda_ok):
 # ---- bf16 output: the fp32 result rounded, bit for bit -----------------------
 @pytest.mark.parametrize("B,T,Hq,Hkv,W", [
     (1, 300, 8, 1, 128), (3, 1000, 16, 2, 128), (1, 700, 8, 1, 700), (2, 513, 16, 2, 300),
+    (2, 600, 8, 2, 128), (1, 500, 32, 2, 128), (1, 400, 32, 2, 400),
 ])
 def test_bf16_output_is_rounded_fp32_output(cuda_ok, B, T, Hq, Hkv, W):
     x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=3000 + T + W, device="cuda")
@@ -210,8 +231,8 @@ def test_bf16_output_is_rounded_fp32_output(cuda_ok, B, T, Hq, Hkv, W):
 
 
 def test_bf16_output_needs_a_tensor_core_path(cuda_ok):
-    x = gen.prefill_inputs(1, 64, 4, 1, 128, seed=9, device="cuda")
-    assert swa.fwd_path(1, 64, 4, 1, 128, 128) == "simt"
+    x = gen.prefill_inputs(1, 64, 2, 1, 128, seed=9, device="cuda")
+    assert swa.fwd_path(1, 64, 2, 1, 128, 128) == "simt"
     with pytest.raises(swa.SwaError) as e:
         swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, 128, out_dtype=torch.bfloat16)
     assert e.value.status == swa.SWA_EUNSUPPORTED

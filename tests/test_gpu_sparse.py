@@ -64,6 +64,33 @@ def test_sparse_matches_oracle(cuda_ok, B, T, Hq, Hkv, QB, topk):
     assert_lse_close(lse.cpu().numpy(), l_ref)
 
 
+def test_sparse_block_list_is_read_up_to_its_first_negative_entry(cuda_ok):
+    # a caller-built list: entries after the first -1 are ignored, and the
+    # order of the entries before it does not matter (every key is masked
+    # causally on its own, and the online softmax does not depend on order)
+    B, T, Hq, Hkv, QB, topk = 1, 1000, 16, 2, 64, 4
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4150)
+    idx = _selection(B, Hkv, T, QB, topk, seed=77)
+    cut = idx.copy()
+    cut[..., 1] = -1                       # valid entries after it are dropped
+    want = cut.copy()
+    want[..., 2:] = -1
+    rev = idx.copy()
+    for b in range(B):
+        for g in range(Hkv):
+            for qb in range(idx.shape[2]):
+                n = int((idx[b, g, qb] >= 0).sum())
+                rev[b, g, qb, :n] = idx[b, g, qb, :n][::-1]
+    q, k, v, s = (t.cuda() for t in (x.q, x.k, x.v, x.sink))
+    for given, ref_idx in ((cut, want), (rev, idx)):
+        out, lse = swa.swa_sink_sparse_fwd(q, k, v, s, torch.from_numpy(given).cuda(), QB)
+        torch.cuda.synchronize()
+        o_ref, l_ref = oracle.sparse_fwd(x.q, x.k, x.v, x.sink, ref_idx, QB)
+        assert_bf16_close(out.cpu().numpy(), o_ref)
+        assert_lse_close(lse.cpu().numpy(), l_ref)
+    assert swa.device_error() == 0
+
+
 def test_sparse_with_every_block_is_the_global_kernel(cuda_ok):
     B, T, Hq, Hkv, QB = 1, 1100, 16, 2, 64
     x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4200, device="cuda")

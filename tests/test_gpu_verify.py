@@ -57,6 +57,41 @@ def test_verify_shapes(cuda_ok, B, L, Hq, Hkv, D, W, dt):
     _check(x, fp32=dt == torch.float32)
 
 
+@pytest.mark.parametrize("B,L,pos_hi", [(37, 5, 600), (29, 6, 300), (41, 8, 2000), (9, 8, 9)])
+def test_verify_tc_up_to_eight_drafts(cuda_ok, B, L, pos_hi):
+    # 5 to 8 drafted tokens on the tensor cores (64 query rows per group, two
+    # softmax warps per warpgroup), full and partial rings with NaN in the
+    # empty slots, positions where every window still starts at 0
+    assert swa.verify_path(B, L, 64, 8, 128, 128) == "tc_verify"
+    x = gen.verify_inputs(B, L, 64, 8, 128, 128, seed=B + L, pos_lo=0, pos_hi=pos_hi)
+    for b in range(B):
+        p = int(x.pos[b])
+        if p < 128:
+            x.k_ring[b, :, p:] = float("nan")
+            x.v_ring[b, :, p:] = float("nan")
+    _check(x)
+    assert swa.device_error() == 0
+
+
+def test_verify_eight_drafts_equal_prefill_rows(cuda_ok):
+    B, T, Hq, Hkv, D, W, L = 2, 600, 16, 2, 128, 128, 8
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=64, device="cuda")
+    out_pre, lse_pre = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+    pos = torch.tensor([5, 401], dtype=torch.int64)
+    kr, vr = gen.ring_from_history(x.k.cpu(), x.v.cpu(), pos - 1, W)
+    idx = [torch.arange(int(p), int(p) + L) for p in pos]
+    qn = torch.stack([x.q[b, idx[b]] for b in range(B)]).contiguous()
+    kn = torch.stack([x.k[b, idx[b]] for b in range(B)]).contiguous()
+    vn = torch.stack([x.v[b, idx[b]] for b in range(B)]).contiguous()
+    assert swa.verify_path(B, L, Hq, Hkv, D, W) == "tc_verify"
+    o, l = swa.swa_sink_verify(qn, kn, vn, kr.cuda(), vr.cuda(), pos.cuda(), x.sink)
+    torch.cuda.synchronize()
+    for b in range(B):
+        p = int(pos[b])
+        assert (o[b] - out_pre[b, p:p + L]).abs().max().item() < 2e-2
+        assert (l[b] - lse_pre[b, :, p:p + L]).abs().max().item() < 1e-3
+
+
 def test_verify_equals_prefill_rows_on_gpu(cuda_ok):
     # drafts checked against a ring laid from the history equal the GPU prefill
     B, T, Hq, Hkv, D, W, L = 3, 400, 16, 2, 128, 128, 4
