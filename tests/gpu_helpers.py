@@ -69,6 +69,20 @@ def oracle_rows_from_slices(q, k, v, sink, W, rows):
     return out, lse
 
 
+def oracle_by_slices(q, k, v, sink, W, b, s0, s1):
+    """Oracle values of positions s0..s1-1 of batch entry b, every head:
+    (out [s1-s0, Hq, D], lse [Hq, s1-s0]) in fp64.
+
+    The oracle runs on positions max(0, s0-W+1) .. s1-1 only.  A row i >= s0
+    reads keys [max(0, i-W+1), i], all inside that range, so its value is the
+    one the oracle gives on the whole sequence; the W-1 halo rows before s0
+    are computed with truncated windows and dropped."""
+    j0 = max(0, s0 - W + 1)
+    qs, ks, vs = (t[b:b + 1, j0:s1].cpu() for t in (q, k, v))
+    o, l = oracle.swa_sink_fwd(qs, ks, vs, sink.detach().cpu(), W)
+    return o[0, s0 - j0:], l[0, :, s0 - j0:]
+
+
 def gather_rows(out, lse, rows):
     """Kernel outputs at the selected rows, as fp64 numpy arrays."""
     idx_b = torch.tensor([r[0] for r in rows])

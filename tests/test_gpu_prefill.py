@@ -9,7 +9,7 @@ import oracle
 import hybrid_sliding_window_02_b300 as swa
 from hybrid_sliding_window_02_b300 import inputs as gen
 from gpu_helpers import (assert_bf16_close, assert_f32_close, assert_lse_close, gather_rows,
-                         oracle_rows_from_slices, sample_rows)
+                         oracle_by_slices, oracle_rows_from_slices, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -159,6 +159,37 @@ def test_simt_bf16_shapes(cuda_ok, B, T, Hq, Hkv, D, W):
     _full_check(x, W)
 
 
+# ---- full-size workloads, every output compared ----------------------------
+def test_prefill_full_size_in_full(cuda_ok):
+    # B=4, T=8192, Hq=64, Hkv=8, D=128, W=128, N(0,1) -> bf16, sink N(0,1):
+    # every element of out and lse against the oracle, one sequence at a time
+    B, T, Hq, Hkv, D, W = 4, 8192, 64, 8, 128, 128
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=0, device="cuda")
+    out, lse = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+    torch.cuda.synchronize()
+    for b in range(B):
+        o_ref, l_ref = oracle_by_slices(x.q, x.k, x.v, x.sink, W, b, 0, T)
+        assert_bf16_close(out[b].cpu().numpy(), o_ref, what=f"sequence {b}")
+        assert_lse_close(lse[b].cpu().numpy(), l_ref)
+
+
+def test_long_context_in_full(cuda_ok):
+    # B=1, T=262144, every 97th key x8 (peaky scores), sink U(-4, 4): every
+    # element, in slices of 32768 positions (each with its 127-key halo)
+    B, T, Hq, Hkv, D, W = 1, 262144, 64, 8, 128, 128
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=5, device="cuda", sink_dist="uniform4",
+                           peaky_every=97)
+    out, lse = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+    torch.cuda.synchronize()
+    S = 32768
+    for s0 in range(0, T, S):
+        o_ref, l_ref = oracle_by_slices(x.q, x.k, x.v, x.sink, W, 0, s0, s0 + S)
+        assert_bf16_close(out[0, s0:s0 + S].cpu().numpy(), o_ref, what=f"positions {s0}..")
+        assert_lse_close(lse[0, :, s0:s0 + S].cpu().numpy(), l_ref)
+    del x, out, lse
+    torch.cuda.empty_cache()
+
+
 # ---- full-size workloads, sampled rows -------------------------------------
 def test_prefill_full_size_sampled(cuda_ok):
     # B=4, T=8192, Hq=64, Hkv=8, D=128, W=128, N(0,1) -> bf16, sink N(0,1)
@@ -200,9 +231,10 @@ def test_hybrid_block_sampled(cuda_ok):
         out, lse = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
         torch.cuda.synchronize()
         assert torch.isfinite(out).all()
-        npos = 12 if layer < 5 else 6
-        rows = sample_rows(1, T, Hq, npos, seed=layer, extra_pos=(T - 1,),
-                           heads=range(0, Hq, 7 if layer == 5 else 1))
+        # window layers: 24 positions; the global layer: the 10 edge positions
+        # plus 64 drawn over the whole causal range, every head
+        npos = 24 if layer < 5 else 74
+        rows = sample_rows(1, T, Hq, npos, seed=layer, extra_pos=(T - 1,))
         o_ref, l_ref = oracle_rows_from_slices(x.q, x.k, x.v, x.sink, W, rows)
         o, l = gather_rows(out, lse, rows)
         assert_bf16_close(o, o_ref, what=f"layer {layer}")

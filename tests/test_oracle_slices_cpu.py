@@ -52,3 +52,15 @@ def test_sparse_rows_from_slices_with_no_selected_key():
     assert np.all(o[0] == 0.0) and l[0] == float(x.sink[3])
     assert np.allclose(o[1], o_whole[0, 130, 5], atol=1e-12)
     assert np.allclose(l, [l_whole[0, 3, 10], l_whole[0, 5, 130]], atol=1e-12)
+
+
+def test_prefill_by_slices_equal_whole_oracle():
+    # the oracle on positions s0-W+1 .. s1-1 gives rows s0 .. s1-1 exactly
+    from gpu_helpers import oracle_by_slices
+    B, T, Hq, Hkv, D = 2, 300, 8, 2, 64
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=33)
+    for W in (1, 32, 128, T):
+        o_all, l_all = oracle.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+        for b, s0, s1 in ((0, 0, 100), (1, 100, 233), (1, 233, T), (0, 7, 8)):
+            o, l = oracle_by_slices(x.q, x.k, x.v, x.sink, W, b, s0, s1)
+            assert np.array_equal(o, o_all[b, s0:s1]) and np.array_equal(l, l_all[b, :, s0:s1])
