@@ -112,10 +112,52 @@ def reduce_value(pg, x: float, op: str) -> float:
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
+class _NvmlLib:
+    """The few NVML calls the sampler needs, through ctypes on the driver's
+    libnvidia-ml (used when the pynvml module is not installed).  Reads only."""
+
+    CLOCK_SM = 1
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.L = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.L.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        rc = -1
+        try:  # match the CUDA device to its NVML handle by UUID
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            rc = self.L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+        except Exception:
+            rc = -1
+        if rc != 0 and self.L.nvmlDeviceGetHandleByIndex_v2(device_index,
+                                                            ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for the device")
+        self._reasons = getattr(self.L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.L.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_mhz(self):
+        v = self.ct.c_uint()
+        return v.value if self.L.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM,
+                                                         self.ct.byref(v)) == 0 else None
+
+    def sm_max_mhz(self):
+        v = self.ct.c_uint()
+        return v.value if self.L.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM,
+                                                            self.ct.byref(v)) == 0 else None
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        return v.value if self._reasons(self.h, self.ct.byref(v)) == 0 else 0
+
+
 class ClockSampler:
-    """Samples the SM clock and clock-event (throttle) reasons while the timed
-    region runs: through NVML in a thread, or, if NVML is unavailable, from an
-    ``nvidia-smi -lms`` subprocess."""
+    """Samples the SM clock and clock-event (throttle) reasons while a timed
+    region runs: through NVML (the pynvml module, else the driver's NVML
+    library through ctypes) in a thread about every millisecond, or, if NVML
+    is unavailable, from an ``nvidia-smi -lms`` subprocess."""
 
     REASONS = {
         "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
@@ -124,8 +166,9 @@ class ClockSampler:
     SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
                   "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
                   "clocks_event_reasons.hw_thermal_slowdown")
+    _nvml_cache = {}
 
-    def __init__(self, device_index: int, period_s: float = 0.02):
+    def __init__(self, device_index: int, period_s: float = 0.001):
         self.idx = device_index
         self.period = period_s
         self.samples = []
@@ -136,33 +179,55 @@ class ClockSampler:
         self._stop = threading.Event()
         self._thread = None
         self._proc = None
+        self._nv = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            h = None
-            try:  # match the CUDA device to its NVML handle by UUID
-                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-                h = pynvml.nvmlDeviceGetHandleByUUID(
-                    uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
-            except Exception:
-                h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self._h = h
-            self._reasons_fn = (getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
-                                or getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons"))
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self._nv = self._open(device_index)
+            self.max_mhz = self._nv.sm_max_mhz()
             self.source = "nvml"
         except Exception as e:  # fall back to nvidia-smi
             self._nv = None
             self.error = f"nvml: {type(e).__name__}: {e}"
             self.source = "nvidia-smi"
 
+    @classmethod
+    def _open(cls, device_index):
+        if device_index in cls._nvml_cache:
+            return cls._nvml_cache[device_index]
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            try:
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+                h = pynvml.nvmlDeviceGetHandleByUUID(
+                    uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            except Exception:
+                h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            rf = (getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                  or getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons"))
+
+            class _Py:
+                def sm_mhz(self):
+                    return pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+
+                def sm_max_mhz(self):
+                    return pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+
+                def reasons(self):
+                    return rf(h)
+            nv = _Py()
+        except ImportError:
+            nv = _NvmlLib(device_index)
+        cls._nvml_cache[device_index] = nv
+        return nv
+
     def _run_nvml(self):
         nv = self._nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                mask = self._reasons_fn(self._h)
+                mhz = nv.sm_mhz()
+                if mhz is not None:
+                    self.samples.append(float(mhz))
+                mask = nv.reasons()
                 for name, bit in self.REASONS.items():
                     if mask & bit:
                         self.reasons.add(name)
@@ -206,10 +271,13 @@ class ClockSampler:
                     if val.lower() == "active":
                         self.reasons.add(name)
 
+    def median(self):
+        return statistics.median(self.samples) if self.samples else None
+
     def summary(self):
-        d = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-             "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-             "samples": len(self.samples), "source": self.source}
+        d = {"sm_mhz": self.median(), "sm_max_mhz": self.max_mhz,
+             "reasons": sorted(self.reasons), "samples": len(self.samples),
+             "source": self.source}
         if not self.samples and self.error:
             d["error"] = self.error
         return d
@@ -302,13 +370,13 @@ def oracle_rows_rate(q, k, v, sink, W, i0, ts):
     return dt, 4 * D * Hq * npairs, len(rows)
 
 
-def cpu_oracle_sample(q, k, v, sink, W, target_s=12.0):
+def cpu_oracle_sample(q, k, v, sink, W, target_s=12.0, i0=None):
     """Time the fp64 oracle on consecutive full-window rows of batch entry 0
     (all heads), sized for about target_s seconds of host work."""
     import oracle
     nthr = oracle.num_threads()
     T, Hq = q.shape[1], q.shape[2]
-    i0 = min(W, T - 1)
+    i0 = min(W, T - 1) if i0 is None else i0
     ts = min(T - i0, 16)
     dt, flops, nrows = oracle_rows_rate(q, k, v, sink, W, i0, ts)
     while dt < target_s / 4 and ts < T - i0:
@@ -317,6 +385,37 @@ def cpu_oracle_sample(q, k, v, sink, W, target_s=12.0):
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": nthr, "kind": "oracle",
             "sample": f"batch entry 0, positions {i0}..{i0 + ts - 1}, all {Hq} heads "
                       f"({nrows} rows, {flops:.3e} FLOP) in {dt:.2f} s"}
+
+
+def cpu_oracle_call(fn, units, unit, sample):
+    """Time one oracle call over the whole workload of a line; ``units`` is the
+    line's work (bytes or FLOPs) and ``unit`` its rate unit."""
+    import oracle
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    scale = 1e9 if unit == "GB/s" else 1e12
+    return {"value": units / dt / scale, "unit": unit, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{sample} in {dt:.2f} s"}
+
+
+def cpu_global_layer(x, T):
+    """The fp64 oracle on the global layer's last 128 positions (all heads:
+    8192 rows, the longest ones), and the whole layer's time extrapolated from
+    that rate by its exact pair count."""
+    D, Hq = x.q.shape[3], x.q.shape[2]
+    dt, flops, nrows = oracle_rows_rate(x.q, x.k, x.v, x.sink, T, T - 128, 128)
+    full = work.prefill_flops(1, T, Hq, D, T)
+    return flops / dt, (f"global layer: positions {T - 128}..{T - 1}, all {Hq} heads ({nrows} "
+                        f"rows, {flops:.3e} FLOP) in {dt:.2f} s; the layer's "
+                        f"{full:.3e} FLOP extrapolated at that rate")
+
+
+def with_clocks(dev, fn):
+    """Run fn under a clock sampler; returns (fn's result, clock summary)."""
+    with ClockSampler(dev.index) as clk:
+        r = fn()
+    return r, clk.summary()
 
 
 # ---------------------------------------------------------------------------
@@ -377,8 +476,9 @@ def time_graph(call, sets, steps, warmup, stream, per_graph=32):
     return e0.elapsed_time(e1) / (reps * per_graph)
 
 
-def time_decode(swa, c, steps, warmup, dev, stream, nsets=4):
-    """Decode calls rotating over input sets whose total exceeds L2; ms per call."""
+def decode_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None):
+    """Decode calls rotating over input sets whose total exceeds L2."""
+    c = c or DECODE
     B, Hq, Hkv, D, W = (c[k] for k in ("B", "Hq", "Hkv", "D", "W"))
     sets = [gen.decode_inputs(B, Hq, Hkv, D, W, seed=100 + i, device=dev) for i in range(nsets)]
     out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
@@ -387,12 +487,33 @@ def time_decode(swa, c, steps, warmup, dev, stream, nsets=4):
     def call(d):
         swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink, out, lse, stream=stream)
 
-    return time_graph(call, sets, steps, warmup, stream)
+    ms, clocks = with_clocks(dev, lambda: time_graph(call, sets, steps, 3, stream))
+    nbytes = work.decode_bytes(B, Hq, Hkv, D, W, 2)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    kernel = ("decode_tc_kernel" if swa.decode_path(B, Hq, Hkv, D, W) == "tc_decode"
+              else "decode_kernel")
+    line = {
+        "workload": f"decode B{B} Hq{Hq} Hkv{Hkv} D{D} W{W} ring, bf16->fp32+lse, {nsets} sets "
+                    "(>L2), graph of 32",
+        "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
+        "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "bytes_per_launch": nbytes, "traffic": recorded_traffic(kernel)},
+        "clocks": clocks,
+    }
+    if cpu:
+        import oracle
+        d = sets[0]
+        hc = [t.cpu() for t in (d.q, d.k_ring, d.v_ring, d.pos, d.sink)]
+        line["cpu_baseline"] = cpu_oracle_call(
+            lambda: oracle.swa_sink_decode(*hc), nbytes, "GB/s", f"the whole call ({B} seqs)")
+    return line
 
 
-def time_verify(swa, c, steps, warmup, dev, stream, nsets=4):
+def verify_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None):
     """Verify calls (L drafted tokens per sequence) rotating over input sets
-    whose total exceeds L2; ms per call."""
+    whose total exceeds L2."""
+    c = c or VERIFY
     B, L, Hq, Hkv, D, W = (c[k] for k in ("B", "L", "Hq", "Hkv", "D", "W"))
     sets = [gen.verify_inputs(B, L, Hq, Hkv, D, W, seed=300 + i, device=dev)
             for i in range(nsets)]
@@ -403,40 +524,37 @@ def time_verify(swa, c, steps, warmup, dev, stream, nsets=4):
         swa.swa_sink_verify(d.q, d.k_new, d.v_new, d.k_ring, d.v_ring, d.pos, d.sink, out, lse,
                             stream=stream)
 
-    return time_graph(call, sets, steps, warmup, stream)
-
-
-def verify_line(swa, dev, stream, steps, hbm):
-    c = VERIFY
-    ms = time_verify(swa, c, steps, 3, dev, stream)
-    nbytes = work.verify_bytes(c["B"], c["L"], c["Hq"], c["Hkv"], c["D"], c["W"], 2)
+    ms, clocks = with_clocks(dev, lambda: time_graph(call, sets, steps, 3, stream))
+    nbytes = work.verify_bytes(B, L, Hq, Hkv, D, W, 2)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    kpath = swa.verify_path(c["B"], c["L"], c["Hq"], c["Hkv"], c["D"], c["W"])
+    kpath = swa.verify_path(B, L, Hq, Hkv, D, W)
     kernel = "verify_tc_kernel" if kpath == "tc_verify" else "verify_simt_kernel"
-    return {
-        "workload": f"swa_sink_verify B{c['B']} L{c['L']} Hq{c['Hq']} Hkv{c['Hkv']} D{c['D']} "
-                    f"W{c['W']} ring + {c['L']} drafted tokens, bf16->fp32+lse, 4 rotating sets "
-                    "(CUDA graph of 32 calls)",
+    line = {
+        "workload": f"verify B{B} L{L} Hq{Hq} Hkv{Hkv} D{D} W{W} ring + {L} drafts, "
+                    f"bf16->fp32+lse, {nsets} sets (>L2), graph of 32",
         "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                     "algorithmic_bytes_per_launch": nbytes,
-                     "traffic": recorded_traffic(kernel)},
+                     "bytes_per_launch": nbytes, "traffic": recorded_traffic(kernel)},
+        "clocks": clocks,
     }
+    if cpu:
+        import oracle
+        d = sets[0]
+        hc = [t.cpu() for t in (d.q, d.k_new, d.v_new, d.k_ring, d.v_ring, d.pos, d.sink)]
+        line["cpu_baseline"] = cpu_oracle_call(
+            lambda: oracle.swa_sink_verify(*hc), nbytes, "GB/s", f"the whole call ({B}x{L})")
+    return line
 
 
 HYBRID = dict(T=32768, Hq=64, Hkv=8, D=128, W=128, n_swa=5, n_ga=1)
 
 
-def time_hybrid(swa, dev, stream, reps, n_swa):
-    """One hybrid block: n_swa W=128 layers then one global layer (W = T),
-    each on its own seeded inputs, one sequence of T=32768.  Returns per-layer
+def time_hybrid(swa, dev, stream, reps, layers, Ws):
+    """One hybrid block: the window layers then the global layer (W = T), each
+    on its own seeded inputs, one sequence of T=32768.  Returns per-layer
     mean launch times (ms) measured with events on the launching stream."""
-    c = HYBRID
-    T, Hq, Hkv, D = c["T"], c["Hq"], c["Hkv"], c["D"]
-    layers = gen.hybrid_block_inputs(T, Hq, Hkv, D, n_swa=n_swa, n_ga=c["n_ga"], seed=200,
-                                     device=dev)
-    Ws = [c["W"]] * n_swa + [T] * c["n_ga"]
+    T, Hq, D = HYBRID["T"], HYBRID["Hq"], HYBRID["D"]
     out = torch.empty(1, T, Hq, D, dtype=torch.float32, device=dev)
     lse = torch.empty(1, Hq, T, dtype=torch.float32, device=dev)
 
@@ -463,42 +581,69 @@ def time_hybrid(swa, dev, stream, reps, n_swa):
             for li, (a, b) in enumerate(evs):
                 per_layer[li] += a.elapsed_time(b) / reps
             total += evs[0][0].elapsed_time(evs[-1][1]) / reps
-    del layers, out, lse
-    torch.cuda.empty_cache()
-    return per_layer, total, Ws
+    del out, lse
+    return per_layer, total
 
 
-def hybrid_line(swa, dev, stream, reps, peaks, n_swa=None):
+def hybrid_line(swa, dev, stream, reps, peaks, cpu, n_swa=None, cpu_rates=None):
     c = dict(HYBRID)
     if n_swa is not None:
         c["n_swa"] = n_swa
-    T, Hq, D = c["T"], c["Hq"], c["D"]
-    per_layer, total_ms, Ws = time_hybrid(swa, dev, stream, reps, c["n_swa"])
+    T, Hq, Hkv, D = c["T"], c["Hq"], c["Hkv"], c["D"]
+    layers = gen.hybrid_block_inputs(T, Hq, Hkv, D, n_swa=c["n_swa"], n_ga=c["n_ga"], seed=200,
+                                     device=dev)
+    Ws = [c["W"]] * c["n_swa"] + [T] * c["n_ga"]
+    (per_layer, total_ms), clocks = with_clocks(
+        dev, lambda: time_hybrid(swa, dev, stream, reps, layers, Ws))
     fl = [work.prefill_flops(1, T, Hq, D, W) for W in Ws]
     ga_ms = sum(t for t, W in zip(per_layer, Ws) if W >= T) / max(1, c["n_ga"])
     ga_fl = fl[-1]
     ga_tf = ga_fl / (ga_ms * 1e-3) / 1e12
     swa_ms = sum(t for t, W in zip(per_layer, Ws) if W < T) / c["n_swa"]
     flop_ratio, kv_ratio = work.hybrid_reduction(T, c["W"], c["n_swa"], c["n_ga"])
-    return {
+    peak = float(peaks["bf16_tflops"])
+    roof = {"kernel": "swa_fwd_tc_global_kernel", "bound": "tensor",
+            "achieved": round(ga_tf, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(ga_tf / peak, 4),
+            "peak_source": "measured bf16_tflops (burst)",
+            # the layer runs inside a seconds-long loop under the power
+            # cap: its fraction of the sustained GEMM rate, for context
+            "frac_of_sustained": round(ga_tf / float(peaks["bf16_tflops_sustained"]), 4),
+            "flops_per_launch": ga_fl,
+            "traffic": recorded_traffic("swa_fwd_tc_global_kernel")}
+    if clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        # time x clock: the layer's rate had it run at the maximum SM clock
+        # throughout (the median clock of the line's timed region stands in
+        # for the layer's own)
+        roof["frac_at_max_clock"] = round(
+            ga_tf / peak * clocks["sm_max_mhz"] / clocks["sm_mhz"], 4)
+    line = {
         "workload": f"hybrid block {c['n_swa']}x SWA (W={c['W']}) + {c['n_ga']}x global "
-                    f"(W=T), B1 T{T} Hq{Hq} Hkv{c['Hkv']} D{D} bf16->fp32+lse",
+                    f"(W=T), B1 T{T} Hq{Hq} Hkv{Hkv} D{D} bf16->fp32+lse",
         "value": round(sum(fl) / (total_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
         "ms_per_block": round(total_ms, 3), "reps": reps,
         "layer_ms": [round(t, 4) for t in per_layer],
         "swa_layer_ms": round(swa_ms, 4), "global_layer_ms": round(ga_ms, 4),
         "attention_flop_reduction_vs_all_global": round(flop_ratio, 3),
         "kv_cache_reduction_vs_all_global": round(kv_ratio, 3),
-        "roofline": {"kernel": "swa_fwd_tc_global_kernel", "bound": "tensor",
-                     "achieved": round(ga_tf, 1), "peak": float(peaks["bf16_tflops"]),
-                     "unit": "TFLOP/s", "frac": round(ga_tf / float(peaks["bf16_tflops"]), 4),
-                     "peak_source": "measured bf16_tflops (burst)",
-                     # the layer runs inside a seconds-long loop under the power
-                     # cap: its fraction of the sustained GEMM rate, for context
-                     "frac_of_sustained": round(ga_tf / float(peaks["bf16_tflops_sustained"]), 4),
-                     "algorithmic_flops_per_launch": ga_fl,
-                     "traffic": recorded_traffic("swa_fwd_tc_global_kernel")},
+        "roofline": roof, "clocks": clocks,
     }
+    if cpu:
+        if cpu_rates is None:
+            swa_s = cpu_oracle_sample(layers[0].q, layers[0].k, layers[0].v, layers[0].sink,
+                                      c["W"], target_s=3.0)
+            ga_rate, ga_sample = cpu_global_layer(layers[-1], T)
+            cpu_rates = (swa_s, ga_rate, ga_sample)
+        swa_s, ga_rate, ga_sample = cpu_rates
+        cpu_s = sum(f / (swa_s["value"] * 1e12) for f, W in zip(fl, Ws) if W < T) + \
+            sum(f / ga_rate for f, W in zip(fl, Ws) if W >= T)
+        line["cpu_baseline"] = {
+            "value": sum(fl) / cpu_s / 1e12, "unit": "TFLOP/s", "cores": swa_s["cores"],
+            "kind": "oracle", "extrapolated": True, "block_s": round(cpu_s, 1),
+            "sample": f"window layers: {swa_s['sample']} (layer 0); {ga_sample}"}
+    del layers
+    torch.cuda.empty_cache()
+    return line, cpu_rates
 
 
 SPARSE = dict(T=32768, Hq=64, Hkv=8, D=128, QB=64, topk=16)
@@ -521,7 +666,7 @@ def _event_ms(fn, reps, stream):
 LONG = dict(B=1, T=262144, Hq=64, Hkv=8, D=128, W=128)
 
 
-def long_context_line(swa, dev, stream, reps, peaks):
+def long_context_line(swa, dev, stream, reps, peaks, cpu):
     """The long-context sliding-window prefill: one sequence of T=262144 with
     every 97th key scaled by 8 (peaky scores) and sinks U(-4, 4)."""
     c = LONG
@@ -530,26 +675,32 @@ def long_context_line(swa, dev, stream, reps, peaks):
                            peaky_every=97)
     out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=dev)
     lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
-    ms = _event_ms(lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream),
-                   reps, stream)
+    ms, clocks = with_clocks(dev, lambda: _event_ms(
+        lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream),
+        reps, stream))
     flops = work.prefill_flops(B, T, Hq, D, W)
     nbytes = work.prefill_bytes(B, T, Hq, Hkv, D, 2)
     hbm = float(peaks["hbm_gbs"])
     gbs = nbytes / (ms * 1e-3) / 1e9
-    del x, out, lse
-    torch.cuda.empty_cache()
-    return {
+    line = {
         "workload": f"swa_sink_prefill B{B} T{T} Hq{Hq} Hkv{Hkv} D{D} W{W} bf16->fp32+lse, every "
                     f"97th key x8, sinks U(-4,4)",
         "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
         "ms_per_call": round(ms, 4),
         "roofline": {"kernel": "swa_fwd_tc_kernel", "bound": "hbm", "achieved": round(gbs, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                     "algorithmic_bytes_per_launch": nbytes},
+                     "bytes_per_launch": nbytes},
+        "clocks": clocks,
     }
+    if cpu:
+        line["cpu_baseline"] = cpu_oracle_sample(x.q, x.k, x.v, x.sink, W, target_s=3.0,
+                                                 i0=T // 2)
+    del x, out, lse
+    torch.cuda.empty_cache()
+    return line
 
 
-def high_sparse_line(swa, dev, stream, reps, peaks):
+def high_sparse_line(swa, dev, stream, reps, peaks, cpu):
     """High Sparse on one sequence of T=32768: the global layer with and
     without its block scores, the selection, and the sparse layer over the
     selected blocks of the shared K/V."""
@@ -565,12 +716,26 @@ def high_sparse_line(swa, dev, stream, reps, peaks):
     def glb_scores():
         state["bm"] = swa.swa_sink_fwd_scores(x.q, x.k, x.v, x.sink, T, stream=stream)[2]
 
-    ms_g = _event_ms(glb, reps, stream)
-    ms_gs = _event_ms(glb_scores, reps, stream)
-    ms_sel = _event_ms(lambda: state.__setitem__(
-        "idx", swa.swa_topk_blocks(state["bm"], T, QB, topk, stream=stream)), reps, stream)
-    ms_sp = _event_ms(lambda: swa.swa_sink_sparse_fwd(q2, x.k, x.v, x.sink, state["idx"], QB,
-                                                      stream=stream), reps, stream)
+    def sparse():
+        swa.swa_sink_sparse_fwd(q2, x.k, x.v, x.sink, state["idx"], QB, stream=stream)
+
+    def timed():
+        ms_g = _event_ms(glb, reps, stream)
+        ms_gs = _event_ms(glb_scores, reps, stream)
+        ms_sel = _event_ms(lambda: state.__setitem__(
+            "idx", swa.swa_topk_blocks(state["bm"], T, QB, topk, stream=stream)), reps, stream)
+        return ms_g, ms_gs, ms_sel
+
+    # a first pass makes the selection; the timed pass measures the pipeline
+    # in order (the sparse layer right after the global layers, under the
+    # power cap they bring on), then the sparse layer alone after one second
+    # of idle; each with the clocks of its own timed region
+    timed()
+    sparse()
+    (ms_g, ms_gs, ms_sel), _ = with_clocks(dev, timed)
+    ms_sp, clocks = with_clocks(dev, lambda: _event_ms(sparse, reps, stream))
+    time.sleep(1.0)
+    ms_sp_first, clocks_idle = with_clocks(dev, lambda: _event_ms(sparse, reps, stream))
     # algorithmic work of the sparse layer: keys j <= i of the selected blocks
     idx = state["idx"][0].cpu().numpy()              # [Hkv, nqb, topk]
     pairs = 0
@@ -585,52 +750,121 @@ def high_sparse_line(swa, dev, stream, reps, peaks):
                     pairs += max(0, min(i, j0 + 127) - j0 + 1)
     sp_flops = 4 * D * (Hq // Hkv) * pairs
     gl_flops = work.prefill_flops(1, T, Hq, D, T)
-    del x, q2, state
-    torch.cuda.empty_cache()
-    return {
+    peak = float(peaks["bf16_tflops"])
+    tf = sp_flops / (ms_sp * 1e-3) / 1e12
+    tf_first = sp_flops / (ms_sp_first * 1e-3) / 1e12
+    line = {
         "workload": f"High Sparse B1 T{T} Hq{Hq} Hkv{Hkv} D{D}: global layer + block scores, "
                     f"top-{topk} blocks per {QB}-position query block, sparse layer on the "
                     "shared K/V",
         "global_ms": round(ms_g, 3), "global_with_scores_ms": round(ms_gs, 3),
         "score_overhead": round(ms_gs / ms_g - 1.0, 4),
         "select_ms": round(ms_sel, 4),
-        "sparse_ms": round(ms_sp, 3),
-        "sparse_tflops": round(sp_flops / (ms_sp * 1e-3) / 1e12, 1),
+        "sparse_ms": round(ms_sp, 3), "sparse_ms_after_idle": round(ms_sp_first, 3),
+        "sparse_tflops": round(tf, 1),
         "sparse_fraction_of_global_flops": round(sp_flops / gl_flops, 4),
         "roofline": {"kernel": "swa_fwd_tc_global_kernel (sparse mode)", "bound": "tensor",
-                     "achieved": round(sp_flops / (ms_sp * 1e-3) / 1e12, 1),
-                     "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
-                     "frac": round(sp_flops / (ms_sp * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4)},
+                     "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 4),
+                     "frac_after_idle": round(tf_first / peak, 4)},
+        "clocks": clocks, "clocks_after_idle": clocks_idle,
     }
+    if clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        # time x clock: the rate had the layer run at the maximum SM clock
+        line["roofline"]["frac_at_max_clock"] = round(
+            tf / peak * clocks["sm_max_mhz"] / clocks["sm_mhz"], 4)
+    if cpu:
+        import oracle
+        # rows 0..Ts-1 of the sparse layer are its first query blocks exactly
+        Ts = 3072
+        nqb = Ts // QB
+        hc = [t[:, :Ts].cpu() for t in (q2, x.k, x.v)]
+        ic = state["idx"][:, :, :nqb].cpu()
+        pairs_s = 0
+        for g in range(Hkv):
+            for qb in range(nqb):
+                for kb in ic[0, g, qb].tolist():
+                    if kb >= 0:
+                        pairs_s += sum(max(0, min(i, 128 * kb + 127) - 128 * kb + 1)
+                                       for i in range(qb * QB, qb * QB + QB))
+        fl_s = 4 * D * (Hq // Hkv) * pairs_s
+        line["cpu_baseline"] = cpu_oracle_call(
+            lambda: oracle.sparse_fwd(hc[0], hc[1], hc[2], x.sink.cpu(), ic, QB), fl_s,
+            "TFLOP/s", f"sparse layer rows 0..{Ts - 1}, all {Hq} heads ({fl_s:.3e} FLOP)")
+    del x, q2, state
+    torch.cuda.empty_cache()
+    return line
 
 
-def bf16_out_line(swa, x, c, steps, dev, stream, peaks):
+def bf16_out_line(swa, x, c, steps, dev, stream, peaks, cpu_headline):
     """The headline prefill with bf16 output (out rounded from fp32, lse fp32)."""
     B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
     out = torch.empty(B, T, Hq, D, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+
+    def timed():
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms, clocks = with_clocks(dev, timed)
     nbytes = work.prefill_bytes(B, T, Hq, Hkv, D, 2, out_bytes=2)
     flops = work.prefill_flops(B, T, Hq, D, W)
     hbm = float(peaks["hbm_gbs"])
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"workload": workload_name(c).replace("fp32+lse", "bf16 out + fp32 lse"),
+    line = {"workload": workload_name(c).replace("fp32+lse", "bf16 out + fp32 lse"),
             "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_call": round(ms, 4),
             "roofline": {"kernel": "swa_fwd_tc_kernel", "bound": "hbm", "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                         "algorithmic_bytes_per_launch": nbytes}}
+                         "bytes_per_launch": nbytes},
+            "clocks": clocks}
+    if cpu_headline is not None:
+        # the oracle computes the same rows whatever the output type
+        line["cpu_baseline"] = dict(cpu_headline, sample="the headline line's sample (the "
+                                    "same rows; the output type does not change the oracle)")
+    return line
+
+
+# other group sizes and draft counts on the tensor-core kernels (same window,
+# head dimension and sequence counts as the main workloads)
+WIDE_PREFILL = {"g4": dict(B=4, T=8192, Hq=32, Hkv=8, D=128, W=128),
+                "g16": dict(B=4, T=8192, Hq=64, Hkv=4, D=128, W=128)}
+WIDE_DECODE = {"g4": dict(B=256, Hq=32, Hkv=8, D=128, W=128),
+               "g16": dict(B=256, Hq=64, Hkv=4, D=128, W=128)}
+WIDE_VERIFY = {"l8": dict(B=256, L=8, Hq=64, Hkv=8, D=128, W=128)}
+
+
+def wide_prefill_line(swa, c, steps, dev, stream, peaks):
+    """Sliding-window prefill of another group size: HBM roofline."""
+    B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
+    out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    ms, clocks = with_clocks(dev, lambda: _event_ms(
+        lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream),
+        steps, stream))
+    nbytes = work.prefill_bytes(B, T, Hq, Hkv, D, 2)
+    hbm = float(peaks["hbm_gbs"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    kpath = swa.fwd_path(B, T, Hq, Hkv, D, W)
+    del x, out, lse
+    torch.cuda.empty_cache()
+    return {"workload": workload_name(c), "value": round(gbs, 1), "unit": "GB/s",
+            "ms_per_call": round(ms, 4),
+            "roofline": {"kernel": KERNEL_OF_PATH.get(kpath, kpath), "bound": "hbm",
+                         "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "bytes_per_launch": nbytes},
+            "sm_mhz": clocks.get("sm_mhz")}
 
 
 def time_e2e(swa, xh, c, steps, dev, stream):
@@ -703,20 +937,13 @@ def run_ours(args, dist):
     nbytes = work.prefill_bytes(c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], 2)
     peaks, peak_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
+    cpu = dist.rank == 0 and not args.no_cpu
 
     with ClockSampler(dev.index) as clk:
         total_ms, launch_ms = time_prefill(swa, x, c, args.steps, args.warmup, dist, stream)
     rate, total_ms = job_rate(dist, flops * args.steps, total_ms)
     ms_per_step = total_ms / args.steps
     value = rate / 1e12
-
-    dec_us = time_decode(swa, DECODE, args.decode_steps, 3, dev, stream) * 1e3
-    dec_bytes = work.decode_bytes(DECODE["B"], DECODE["Hq"], DECODE["Hkv"], DECODE["D"],
-                                  DECODE["W"], 2)
-    dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
-    dec_kernel = ("decode_tc_kernel" if swa.decode_path(DECODE["B"], DECODE["Hq"], DECODE["Hkv"],
-                                                        DECODE["D"], DECODE["W"]) == "tc_decode"
-                  else "decode_kernel")
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
@@ -727,31 +954,9 @@ def run_ours(args, dist):
                    "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step)",
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": prefill_roofline(kpath, flops, nbytes, launch_ms, peaks, peak_src),
-        "decode": {
-            "workload": "swa_sink_decode B256 Hq64 Hkv8 D128 W128 ring, bf16->fp32+lse, "
-                        "4 rotating input sets (590 MB), CUDA graph of 32 calls",
-            "value": round(dec_gbs, 1), "unit": "GB/s", "us_per_call": round(dec_us, 2),
-            "roofline": {"kernel": dec_kernel, "bound": "hbm",
-                         "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(dec_gbs / hbm, 4),
-                         "algorithmic_bytes_per_launch": dec_bytes,
-                         "traffic": recorded_traffic(dec_kernel)},
-        },
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
-
-    line["prefill_bf16_out"] = bf16_out_line(swa, x, c, max(10, args.steps // 4), dev, stream,
-                                             peaks)
-    line["verify"] = verify_line(swa, dev, stream, args.decode_steps, hbm)
-    if not args.no_hybrid:
-        line["hybrid_block"] = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks)
-        # the 7:1 schedule of the later models: same kernels, seven window
-        # layers per global layer
-        line["hybrid_block_7to1"] = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks,
-                                                n_swa=7)
-        line["high_sparse"] = high_sparse_line(swa, dev, stream, args.hybrid_reps, peaks)
-        line["long_context"] = long_context_line(swa, dev, stream, args.hybrid_reps, peaks)
     if not args.no_e2e:
         xh = gen.PrefillInputs(*(t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.sink)))
         e2e_ms, h2d, d2h = time_e2e(swa, xh, c, max(3, args.steps // 50), dev, stream)
@@ -760,9 +965,37 @@ def run_ours(args, dist):
                        "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(e2e_ms, 3)}
         del xh
-    if dist.rank == 0 and not args.no_cpu:
+    if cpu:
         line["cpu_baseline"] = cpu_oracle_sample(x.q, x.k, x.v, x.sink, c["W"],
                                                  target_s=args.cpu_seconds)
+    # the other workloads; decode and verify come last so that they stay in
+    # the tail of the line when only its end is kept
+    line["prefill_bf16_out"] = bf16_out_line(swa, x, c, max(10, args.steps // 4), dev, stream,
+                                             peaks, line.get("cpu_baseline"))
+    if not args.no_hybrid:
+        line["hybrid_block"], rates = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks, cpu)
+        # the 7:1 schedule of the later models: same kernels, seven window
+        # layers per global layer (same per-layer CPU rates)
+        line["hybrid_block_7to1"], _ = hybrid_line(swa, dev, stream, args.hybrid_reps, peaks,
+                                                   cpu, n_swa=7, cpu_rates=rates)
+        line["high_sparse"] = high_sparse_line(swa, dev, stream, args.hybrid_reps, peaks, cpu)
+        line["long_context"] = long_context_line(swa, dev, stream, args.hybrid_reps, peaks, cpu)
+    if not args.no_wide:
+        wide = {}
+        for name, wc in WIDE_PREFILL.items():
+            wide["prefill_" + name] = wide_prefill_line(swa, wc, max(20, args.steps // 20), dev,
+                                                        stream, peaks)
+        for name, wc in WIDE_DECODE.items():
+            d = decode_line(swa, dev, stream, args.decode_steps, hbm, False, c=wc)
+            wide["decode_" + name] = {"workload": d["workload"], "value": d["value"],
+                                      "unit": "GB/s", "roofline": d["roofline"]}
+        for name, wc in WIDE_VERIFY.items():
+            d = verify_line(swa, dev, stream, args.decode_steps, hbm, False, c=wc)
+            wide["verify_" + name] = {"workload": d["workload"], "value": d["value"],
+                                      "unit": "GB/s", "roofline": d["roofline"]}
+        line["other_shapes"] = wide
+    line["verify"] = verify_line(swa, dev, stream, args.decode_steps, hbm, cpu)
+    line["decode"] = decode_line(swa, dev, stream, args.decode_steps, hbm, cpu)
     if swa.device_error() != 0:
         line["device_error"] = True
     return line
@@ -815,6 +1048,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--no-hybrid", action="store_true", help="skip the 5:1 hybrid-block line")
+    ap.add_argument("--no-wide", action="store_true",
+                    help="skip the lines of other group sizes and draft counts")
     ap.add_argument("--hybrid-reps", type=int, default=5)
     ap.add_argument("--window", type=int, default=0,
                     help="window of the timed prefill (default 128; W >= T is a global layer); "

@@ -12,10 +12,11 @@ import bench  # noqa: E402
 
 
 def test_bench_helpers_exist():
-    for name in ("time_prefill", "time_decode", "time_verify", "time_graph", "time_hybrid",
-                 "hybrid_line", "verify_line", "bf16_out_line", "time_e2e", "prefill_roofline",
-                 "cpu_oracle_sample", "run_reference", "run_ours", "recorded_traffic",
-                 "high_sparse_line", "long_context_line", "job_rate", "_event_ms"):
+    for name in ("time_prefill", "decode_line", "verify_line", "time_graph", "time_hybrid",
+                 "hybrid_line", "bf16_out_line", "time_e2e", "prefill_roofline",
+                 "cpu_oracle_sample", "cpu_oracle_call", "cpu_global_layer", "with_clocks",
+                 "run_reference", "run_ours", "recorded_traffic", "high_sparse_line",
+                 "long_context_line", "job_rate", "_event_ms"):
         assert callable(getattr(bench, name)), name
 
 
@@ -45,3 +46,33 @@ def test_source_hash_ignores_comments_and_whitespace():
     assert bench.source_code_only(a) != bench.source_code_only(c)
     assert '"a // b /* c */"' in bench.source_code_only(a)
 
+
+def test_clock_sampler_with_a_fake_nvml():
+    """The sampler's host logic: samples and clock-event reasons gathered in
+    a thread while the region runs (NVML replaced by a fake that reads
+    nothing from a GPU)."""
+    import time
+
+    class Fake:
+        n = 0
+
+        def sm_mhz(self):
+            Fake.n += 1
+            return 1900 + (Fake.n % 3)
+
+        def sm_max_mhz(self):
+            return 2032
+
+        def reasons(self):
+            return 0x4          # sw_power_cap
+
+    bench.ClockSampler._nvml_cache[97] = Fake()
+    try:
+        with bench.ClockSampler(97) as clk:
+            time.sleep(0.05)
+        d = clk.summary()
+    finally:
+        del bench.ClockSampler._nvml_cache[97]
+    assert d["source"] == "nvml" and d["samples"] >= 5
+    assert 1900 <= d["sm_mhz"] <= 1902 and d["sm_max_mhz"] == 2032
+    assert d["reasons"] == ["sw_power_cap"]
