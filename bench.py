@@ -867,6 +867,35 @@ def wide_prefill_line(swa, c, steps, dev, stream, peaks):
             "sm_mhz": clocks.get("sm_mhz")}
 
 
+def run_only(args):
+    """A few eager calls of one of the other-shape workloads, for a profiler
+    (``--only prefill_g4`` and so on); prints one JSON line with the mean
+    time of the timed calls."""
+    import hybrid_sliding_window_02_b300 as swa
+    swa.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    kind, name = args.only.split("_", 1)
+    if kind == "prefill":
+        c = WIDE_PREFILL[name]
+        B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
+        x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
+        call = lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, stream=stream)
+    elif kind == "decode":
+        c = WIDE_DECODE[name]
+        d = gen.decode_inputs(*(c[k] for k in ("B", "Hq", "Hkv", "D", "W")), seed=100, device=dev)
+        call = lambda: swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink, stream=stream)
+    else:
+        c = WIDE_VERIFY[name]
+        v = gen.verify_inputs(*(c[k] for k in ("B", "L", "Hq", "Hkv", "D", "W")), seed=300,
+                              device=dev)
+        call = lambda: swa.swa_sink_verify(v.q, v.k_new, v.v_new, v.k_ring, v.v_ring, v.pos,
+                                           v.sink, stream=stream)
+    ms = _event_ms(call, args.steps, stream)
+    return {"only": args.only, "workload": c, "ms_per_call": round(ms, 4)}
+
+
 def time_e2e(swa, xh, c, steps, dev, stream):
     """Host (pinned) inputs -> device -> prefill -> host outputs, every step,
     through the library's host-buffer call (swa_sink_fwd_host: per chunk of
@@ -1050,6 +1079,10 @@ def main(argv=None):
     ap.add_argument("--no-hybrid", action="store_true", help="skip the 5:1 hybrid-block line")
     ap.add_argument("--no-wide", action="store_true",
                     help="skip the lines of other group sizes and draft counts")
+    ap.add_argument("--only", default="",
+                    choices=[""] + [f"prefill_{n}" for n in WIDE_PREFILL] +
+                    [f"decode_{n}" for n in WIDE_DECODE] + [f"verify_{n}" for n in WIDE_VERIFY],
+                    help="run only a few calls of one other-shape workload (for a profiler)")
     ap.add_argument("--hybrid-reps", type=int, default=5)
     ap.add_argument("--window", type=int, default=0,
                     help="window of the timed prefill (default 128; W >= T is a global layer); "
@@ -1061,6 +1094,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.only:
+        print(json.dumps(run_only(args)), flush=True)
+        return
     dist = Dist()
     try:
         line = run_reference(args, dist) if args.impl == "reference" else run_ours(args, dist)
