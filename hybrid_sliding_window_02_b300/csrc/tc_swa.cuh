@@ -528,15 +528,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 8,8,8,8,4 and half 1 as 4,8,8,8,8 (each store aligned to its width);
         // 4 heads: 8 at a time
         const uint32_t pa = tmem + lane_addr + col_p(pb) + half * (kNh / 2);
+        if constexpr ((kNh / 2) % 8 == 0) {
+          // packed and stored 8 at a time, so that the scores already packed
+          // free their registers (80 scores plus 40 packed words overflowed
+          // the 128-register cap)
+#pragma unroll
+          for (int c = 0; c < kNh / 16; ++c) {
+            uint32_t pk8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk8[e] = pack_bf16x2(__uint_as_float(sr[16 * c + 2 * e]) * f,
+                                   __uint_as_float(sr[16 * c + 2 * e + 1]) * f);
+            tmem_st8(pa + 8 * c, pk8);
+          }
+        } else {
         uint32_t pk[kNh / 2];
 #pragma unroll
         for (int e = 0; e < kNh / 2; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(sr[2 * e]) * f, __uint_as_float(sr[2 * e + 1]) * f);
-        if constexpr ((kNh / 2) % 8 == 0) {
-#pragma unroll
-          for (int c = 0; c < kNh / 16; ++c)
-            tmem_st8(pa + 8 * c, *reinterpret_cast<const uint32_t(*)[8]>(&pk[8 * c]));
-        } else if (half == 0) {
+        if (half == 0) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tmem_st8(pa + 8 * c, *reinterpret_cast<const uint32_t(*)[8]>(&pk[8 * c]));
@@ -546,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tmem_st8(pa + 4 + 8 * c, *reinterpret_cast<const uint32_t(*)[8]>(&pk[4 + 8 * c]));
+        }
         }
       }
       tmem_st_wait();
