@@ -23,7 +23,8 @@
 // threads issue the MMAs, one the S^T products and one the O^T products, so
 // that waiting for a group's K slot to land never delays the PV of the group
 // before it (and with it the release of that group's V slot).  Two softmax
-// warpgroups take alternate groups: thread = slot reads its G head scores
+// warpgroups (three for G = 16) take the groups in turn: thread = slot reads
+// its G head scores
 // from TMEM, the max and the sum over slots are warp-shuffle reductions (one
 // transposed butterfly for all heads) finished across the four warps in
 // shared memory, the bf16 P^T goes to
@@ -37,8 +38,12 @@
 namespace swa {
 namespace dectc {
 
-constexpr int kThreads = 352;
-constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
+// Softmax warpgroups: two, taking alternate groups; three for 16 heads per kv
+// head, whose longer per-group chain (the softmax of 16 heads between the two
+// products) left HBM idle with two.  Then three special warps.
+__host__ __device__ constexpr int num_wg(int G) { return G > 8 ? 3 : 2; }
+__host__ __device__ constexpr int threads_for(int G) { return 32 * (4 * num_wg(G) + 3); }
+constexpr int kMaxWG = 3;
 constexpr int kN = 16;             // MMA N: the G heads of a group padded to 16
 constexpr int kW = 128;            // ring slots
 constexpr int kD = 128;
@@ -55,19 +60,20 @@ constexpr int kVSlotBytes = 2 * kHalf;              // 32 KB
 constexpr int kPBytes = 2 * kQHalf;                 // P^T: 16 heads x 128 slots bf16
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + (int)kKSlots * kKSlotBytes;
-constexpr int kOffP = kOffV + (int)kVSlots * kVSlotBytes;       // 2 buffers (one per warpgroup)
-constexpr int kOffRed = kOffP + 2 * kPBytes;                    // [wg][warp][head] floats
+constexpr int kOffP = kOffV + (int)kVSlots * kVSlotBytes;       // one buffer per warpgroup
+constexpr int kOffRed = kOffP + kMaxWG * kPBytes;               // [wg][warp][head] floats
 constexpr int kRedBytes = 2 * 4 * kN * 4;                       // room for G <= 16
-constexpr int kOffBar = kOffRed + 2 * kRedBytes;
+constexpr int kOffBar = kOffRed + kMaxWG * kRedBytes;
 constexpr int kBarKFull = 0, kBarKEmpty = kBarKFull + kKSlots, kBarVFull = kBarKEmpty + kKSlots,
               kBarVEmpty = kBarVFull + kVSlots, kBarSFull = kBarVEmpty + kVSlots,
-              kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarRed = kBarOFull + 2,
-              kBarDrain = kBarRed + 4, kNumBars = kBarDrain + 2;
+              kBarPFull = kBarSFull + kMaxWG, kBarOFull = kBarPFull + kMaxWG,
+              kBarRed = kBarOFull + kMaxWG, kBarDrain = kBarRed + 2 * kMaxWG,
+              kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;
 
-constexpr uint32_t kTmemCols = 64;
+static_assert(kSmemBytes <= 227 * 1024, "decode stages fit shared memory");
 // TMEM columns of S^T and O^T for warpgroup w (16 columns each)
 __host__ __device__ constexpr uint32_t col_s(int w) { return 32u * (uint32_t)w; }
 __host__ __device__ constexpr uint32_t col_o(int w) { return 32u * (uint32_t)w + 16u; }
@@ -133,10 +139,15 @@ __device__ __forceinline__ float warp_reduce_heads(float (&v)[kG], int lane) {
 
 // G query heads per kv head (1, 2, 4, 8 or 16)
 template <int kG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(kG), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v,
                      const __grid_constant__ CUtensorMap map_q, const Params p) {
+  static_assert(kG >= 1 && kG <= kN, "a group's heads fill at most the 16 MMA columns");
+  constexpr int kNWG = num_wg(kG);
+  constexpr int kThreads = threads_for(kG);
+  constexpr int kWarpProducer = 4 * kNWG, kWarpMma = kWarpProducer + 1, kWarpPv = kWarpProducer + 2;
+  constexpr uint32_t kTmemCols = kNWG > 2 ? 128 : 64;   // 32 columns per warpgroup
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -158,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVFull + s), 1);
       mbar_init(bar(kBarVEmpty + s), 1);
     }
-    for (int w = 0; w < 2; ++w) {
+    for (int w = 0; w < kNWG; ++w) {
       mbar_init(bar(kBarSFull + w), 1);
       mbar_init(bar(kBarPFull + w), 128);
       mbar_init(bar(kBarOFull + w), 1);
@@ -169,9 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarDrain + 1), 1);
     fence_mbar_init();
   }
-  static_assert(kG >= 1 && kG <= kN, "a group's heads fill at most the 16 MMA columns");
   // P^T rows G..15 (the padding heads) stay zero for the whole kernel
-  for (int i = tid; i < 2 * kPBytes / 16; i += kThreads)
+  for (int i = tid; i < kNWG * kPBytes / 16; i += kThreads)
     st_shared_v4(sbase + kOffP + 16 * i, 0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (warp == kWarpMma) {
@@ -250,10 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = umma_idesc_bf16(kN, true, false);
       bool ok = true;
       for (int k = 0; ok && k < nk; ++k) {
-        const int w = k & 1;
+        const int w = k % kNWG;
+        const uint32_t use = (uint32_t)(k / kNWG);   // uses of buffer w before this one
         if (s_side) {
-          // S^T of group k into TMEM buffer k % 2 once its K slot has landed and
-          // the softmax of group k - 2 has read that buffer (P full)
+          // S^T of group k into TMEM buffer k % kNWG once its K slot has landed
+          // and the softmax of group k - kNWG has read that buffer (P full)
           const uint32_t ks = (uint32_t)k % kKSlots;
           const uint32_t kst = sbase + kOffK + ks * kKSlotBytes;
           if (!mbar_wait(bar(kBarKFull + ks), ((uint32_t)k / kKSlots) & 1, kErrWaitKvFull,
@@ -261,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (k >= 2 && !mbar_wait(bar(kBarPFull + w), ((uint32_t)(k - 2) >> 1) & 1,
-                                   kErrWaitPFull, abort_flag)) {
+          if (k >= kNWG && !mbar_wait(bar(kBarPFull + w), (use - 1) & 1,
+                                      kErrWaitPFull, abort_flag)) {
             ok = false;
             break;
           }
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
           if (!mbar_wait(bar(kBarVFull + vs), ((uint32_t)k / kVSlots) & 1, kErrWaitKvFull,
                          abort_flag) ||
-              !mbar_wait(bar(kBarPFull + w), ((uint32_t)k >> 1) & 1, kErrWaitPFull, abort_flag)) {
+              !mbar_wait(bar(kBarPFull + w), use & 1, kErrWaitPFull, abort_flag)) {
             ok = false;
             break;
           }
@@ -309,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ======================= softmax + output (warps 0..7) =======================
-    const int w = warp >> 2;                   // warpgroup: takes groups k with k % 2 == w
+    const int w = warp >> 2;                   // warpgroup: takes groups k with k % kNWG == w
     const int quad = warp & 3;
     const int t = quad * 32 + lane;            // slot (softmax) / dim (output)
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
@@ -323,14 +334,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per reduction) rather than bar.sync, so that a timed-out wait elsewhere
     // can never leave the other warps blocked.
     const uint32_t bar_max = bar(kBarRed + 2 * w), bar_sum = bar(kBarRed + 2 * w + 1);
-    for (int k = w; k < nk; k += 2) {
+    for (int k = w; k < nk; k += kNWG) {
+      const uint32_t ph = (uint32_t)(k / kNWG) & 1;   // phase of this warpgroup's barriers
       const int u = (int)blockIdx.x + k * (int)gridDim.x;
       const int b = u / p.Hkv, g = u - b * p.Hkv;
       const uint32_t vs = (uint32_t)k % kVSlots;
       const int64_t pnow = p.pos[b];
       const bool full_ring = pnow >= kW - 1;
       const bool valid = full_ring || (int64_t)t <= pnow;
-      if (!mbar_wait(bar(kBarSFull + w), ((uint32_t)k >> 1) & 1, kErrWaitSFull, abort_flag))
+      if (!mbar_wait(bar(kBarSFull + w), ph, kErrWaitSFull, abort_flag))
         break;
       tc_fence_after();
       uint32_t sr[kG > 8 ? 16 : 8];
@@ -354,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((lane & (32 / kG - 1)) == 0) red[quad * kG + lane / (32 / kG)] = mine;
       }
       mbar_arrive(bar_max);
-      if (!mbar_wait(bar_max, ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag)) break;
+      if (!mbar_wait(bar_max, ph, kErrWaitDecode, abort_flag)) break;
       float sk[kG], l[kG];
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
@@ -394,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((lane & (32 / kG - 1)) == 0) red[4 * kG + quad * kG + lane / (32 / kG)] = mine;
       }
       mbar_arrive(bar_sum);
-      if (!mbar_wait(bar_sum, ((uint32_t)k >> 1) & 1, kErrWaitDecode, abort_flag)) break;
+      if (!mbar_wait(bar_sum, ph, kErrWaitDecode, abort_flag)) break;
       float inv_l[kG];
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
@@ -405,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse[(int64_t)b * p.Hq + g * kG + h] = (m[h] + __log2f(lt)) * 0.6931471805599453f;
       }
       // O^T[dim t][h] -> out[b, g*G + h, t]
-      if (!mbar_wait(bar(kBarOFull + w), ((uint32_t)k >> 1) & 1, kErrWaitOFull, abort_flag))
+      if (!mbar_wait(bar(kBarOFull + w), ph, kErrWaitOFull, abort_flag))
         break;
       tc_fence_after();
       uint32_t o[kG > 8 ? 16 : 8];

@@ -426,7 +426,8 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
   const long long grid = units < sms ? units : sms;
-  return launch_dependent("decode_tc_kernel", kern, (unsigned)grid, kThreads, kSmemBytes, st, mk, mv, mq, p);
+  return launch_dependent("decode_tc_kernel", kern, (unsigned)grid, threads_for(1 << lg), kSmemBytes,
+                          st, mk, mv, mq, p);
 }
 
 swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const void* kr,
