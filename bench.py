@@ -760,18 +760,26 @@ def high_sparse_line(swa, dev, stream, reps, peaks, cpu):
         "global_ms": round(ms_g, 3), "global_with_scores_ms": round(ms_gs, 3),
         "score_overhead": round(ms_gs / ms_g - 1.0, 4),
         "select_ms": round(ms_sel, 4),
-        "sparse_ms": round(ms_sp, 3), "sparse_ms_after_idle": round(ms_sp_first, 3),
-        "sparse_tflops": round(tf, 1),
+        "sparse_ms": round(ms_sp_first, 3), "sparse_ms_in_pipeline": round(ms_sp, 3),
+        "sparse_tflops": round(tf_first, 1),
         "sparse_fraction_of_global_flops": round(sp_flops / gl_flops, 4),
+        # the layer timed alone (after one second of idle) against the burst
+        # peak; timed inside the pipeline (right after ~100 ms of global
+        # layers) against the sustained one
         "roofline": {"kernel": "swa_fwd_tc_global_kernel (sparse mode)", "bound": "tensor",
-                     "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(tf / peak, 4),
-                     "frac_after_idle": round(tf_first / peak, 4)},
-        "clocks": clocks, "clocks_after_idle": clocks_idle,
+                     "achieved": round(tf_first, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tf_first / peak, 4),
+                     "peak_source": "measured bf16_tflops (burst), the layer timed alone"},
+        "in_pipeline": {"achieved": round(tf, 1), "unit": "TFLOP/s",
+                        "peak": float(peaks["bf16_tflops_sustained"]),
+                        "frac_of_sustained": round(tf / float(peaks["bf16_tflops_sustained"]), 4),
+                        "frac_of_burst": round(tf / peak, 4)},
+        "clocks": clocks_idle, "clocks_in_pipeline": clocks,
     }
     if clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
-        # time x clock: the rate had the layer run at the maximum SM clock
-        line["roofline"]["frac_at_max_clock"] = round(
+        # time x clock: the in-pipeline rate had the layer run at the maximum
+        # SM clock
+        line["in_pipeline"]["frac_of_burst_at_max_clock"] = round(
             tf / peak * clocks["sm_max_mhz"] / clocks["sm_mhz"], 4)
     if cpu:
         import oracle
@@ -844,7 +852,7 @@ WIDE_DECODE = {"g4": dict(B=256, Hq=32, Hkv=8, D=128, W=128),
 WIDE_VERIFY = {"l8": dict(B=256, L=8, Hq=64, Hkv=8, D=128, W=128)}
 
 
-def wide_prefill_line(swa, c, steps, dev, stream, peaks):
+def wide_prefill_line(swa, c, steps, dev, stream, peaks, cpu=False):
     """Sliding-window prefill of another group size: HBM roofline."""
     B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
@@ -857,14 +865,20 @@ def wide_prefill_line(swa, c, steps, dev, stream, peaks):
     hbm = float(peaks["hbm_gbs"])
     gbs = nbytes / (ms * 1e-3) / 1e9
     kpath = swa.fwd_path(B, T, Hq, Hkv, D, W)
-    del x, out, lse
-    torch.cuda.empty_cache()
-    return {"workload": workload_name(c), "value": round(gbs, 1), "unit": "GB/s",
+    line = {"workload": workload_name(c), "value": round(gbs, 1), "unit": "GB/s",
             "ms_per_call": round(ms, 4),
             "roofline": {"kernel": KERNEL_OF_PATH.get(kpath, kpath), "bound": "hbm",
                          "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbs / hbm, 4), "bytes_per_launch": nbytes},
             "sm_mhz": clocks.get("sm_mhz")}
+    if cpu:
+        # the oracle's rate in the line's unit: bytes of the sampled rows' share
+        smp = cpu_oracle_sample(x.q, x.k, x.v, x.sink, W, target_s=1.5)
+        line["cpu_baseline"] = dict(smp, value=smp["value"] * 1e12 / work.prefill_flops(
+            B, T, Hq, D, W) * nbytes / 1e9, unit="GB/s")
+    del x, out, lse
+    torch.cuda.empty_cache()
+    return line
 
 
 def run_only(args):
@@ -1013,15 +1027,15 @@ def run_ours(args, dist):
         wide = {}
         for name, wc in WIDE_PREFILL.items():
             wide["prefill_" + name] = wide_prefill_line(swa, wc, max(20, args.steps // 20), dev,
-                                                        stream, peaks)
+                                                        stream, peaks, cpu)
         for name, wc in WIDE_DECODE.items():
-            d = decode_line(swa, dev, stream, args.decode_steps, hbm, False, c=wc)
-            wide["decode_" + name] = {"workload": d["workload"], "value": d["value"],
-                                      "unit": "GB/s", "roofline": d["roofline"]}
+            d = decode_line(swa, dev, stream, args.decode_steps, hbm, cpu, c=wc)
+            wide["decode_" + name] = {k: d[k] for k in ("workload", "value", "unit", "roofline",
+                                                        "cpu_baseline") if k in d}
         for name, wc in WIDE_VERIFY.items():
-            d = verify_line(swa, dev, stream, args.decode_steps, hbm, False, c=wc)
-            wide["verify_" + name] = {"workload": d["workload"], "value": d["value"],
-                                      "unit": "GB/s", "roofline": d["roofline"]}
+            d = verify_line(swa, dev, stream, args.decode_steps, hbm, cpu, c=wc)
+            wide["verify_" + name] = {k: d[k] for k in ("workload", "value", "unit", "roofline",
+                                                        "cpu_baseline") if k in d}
         line["other_shapes"] = wide
     line["verify"] = verify_line(swa, dev, stream, args.decode_steps, hbm, cpu)
     line["decode"] = decode_line(swa, dev, stream, args.decode_steps, hbm, cpu)

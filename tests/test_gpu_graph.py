@@ -16,6 +16,11 @@ def test_graph_replay_equals_eager(cuda_ok):
     d = gen.decode_inputs(64, 64, 8, 128, 128, seed=81, device=dev)
     x = gen.prefill_inputs(1, 700, 64, 8, 128, seed=82, device=dev)
     vi = gen.verify_inputs(32, 4, 64, 8, 128, 128, seed=83, device=dev)
+    # the other instantiations: 16 and 4 heads per kv head, 8 drafted tokens
+    d16 = gen.decode_inputs(48, 64, 4, 128, 128, seed=84, device=dev)
+    x4 = gen.prefill_inputs(1, 500, 16, 4, 128, seed=85, device=dev)
+    x16 = gen.prefill_inputs(1, 500, 64, 4, 128, seed=86, device=dev)
+    v8 = gen.verify_inputs(24, 8, 64, 8, 128, 128, seed=87, device=dev)
     outs = {}
 
     def calls():
@@ -24,6 +29,13 @@ def test_graph_replay_equals_eager(cuda_ok):
         outs["glb"] = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, 700, stream=st)
         outs["ver"] = swa.swa_sink_verify(vi.q, vi.k_new, vi.v_new, vi.k_ring, vi.v_ring, vi.pos,
                                           vi.sink, stream=st)
+        outs["dec16"] = swa.swa_sink_decode(d16.q, d16.k_ring, d16.v_ring, d16.pos, d16.sink,
+                                            stream=st)
+        outs["swa4"] = swa.swa_sink_fwd(x4.q, x4.k, x4.v, x4.sink, 128, stream=st)
+        outs["swa16"] = swa.swa_sink_fwd(x16.q, x16.k, x16.v, x16.sink, 128, stream=st)
+        outs["glb16"] = swa.swa_sink_fwd(x16.q, x16.k, x16.v, x16.sink, 500, stream=st)
+        outs["ver8"] = swa.swa_sink_verify(v8.q, v8.k_new, v8.v_new, v8.k_ring, v8.v_ring, v8.pos,
+                                           v8.sink, stream=st)
 
     with torch.cuda.stream(st):
         calls()
