@@ -846,9 +846,11 @@ def bf16_out_line(swa, x, c, steps, dev, stream, peaks, cpu_headline):
 # other group sizes and draft counts on the tensor-core kernels (same window,
 # head dimension and sequence counts as the main workloads)
 WIDE_PREFILL = {"g4": dict(B=4, T=8192, Hq=32, Hkv=8, D=128, W=128),
-                "g16": dict(B=4, T=8192, Hq=64, Hkv=4, D=128, W=128)}
+                "g16": dict(B=4, T=8192, Hq=64, Hkv=4, D=128, W=128),
+                "d64": dict(B=4, T=8192, Hq=64, Hkv=8, D=64, W=128)}
 WIDE_DECODE = {"g4": dict(B=256, Hq=32, Hkv=8, D=128, W=128),
-               "g16": dict(B=256, Hq=64, Hkv=4, D=128, W=128)}
+               "g16": dict(B=256, Hq=64, Hkv=4, D=128, W=128),
+               "d64": dict(B=256, Hq=64, Hkv=8, D=64, W=128)}
 WIDE_VERIFY = {"l8": dict(B=256, L=8, Hq=64, Hkv=8, D=128, W=128)}
 
 

@@ -46,7 +46,7 @@ __host__ __device__ constexpr int threads_for(int G) { return 32 * (4 * num_wg(G
 constexpr int kMaxWG = 3;
 constexpr int kN = 16;             // MMA N: the G heads of a group padded to 16
 constexpr int kW = 128;            // ring slots
-constexpr int kD = 128;
+constexpr int kD = 128;            // largest head dimension (64 is the other)
 
 // Two rings in shared memory (128-byte swizzle): K slots (2) hold K and q and
 // are free once S^T completes; V slots (4) hold V and are free once the PV
@@ -137,8 +137,12 @@ __device__ __forceinline__ float warp_reduce_heads(float (&v)[kG], int lane) {
   return v[0];
 }
 
-// G query heads per kv head (1, 2, 4, 8 or 16)
-template <int kG>
+// G query heads per kv head (1, 2, 4, 8 or 16), head dimension kHd (64 or
+// 128).  With kHd = 64 only the first 64-dimension half of each staging
+// buffer is loaded; S^T is 4 K-steps deep, and O^T keeps M = 128 with the
+// second half of V^T pointed at the first, so TMEM lanes 64..127 hold a copy
+// that no thread reads.
+template <int kG, int kHd>
 __global__ void __launch_bounds__(threads_for(kG), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v,
@@ -148,6 +152,8 @@ __global__ void __launch_bounds__(threads_for(kG), 1)
   constexpr int kThreads = threads_for(kG);
   constexpr int kWarpProducer = 4 * kNWG, kWarpMma = kWarpProducer + 1, kWarpPv = kWarpProducer + 2;
   constexpr uint32_t kTmemCols = kNWG > 2 ? 128 : 64;   // 32 columns per warpgroup
+  static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");
+  constexpr int kHalves = kHd / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -224,11 +230,13 @@ __global__ void __launch_bounds__(threads_for(kG), 1)
           break;
         const uint32_t kst = sbase + kOffK + ks * kKSlotBytes;
         const uint32_t kb = bar(kBarKFull + ks);
-        mbar_arrive_expect_tx(kb, kKSlotBytes);
+        mbar_arrive_expect_tx(kb, kHalves * (kHalf + kQHalf));
         tma_load_4d(kst + kKK, &map_k, 0, u * kW, 0, 0, kb);
-        tma_load_4d(kst + kKK + kHalf, &map_k, 64, u * kW, 0, 0, kb);
         tma_load_4d(kst + kKQ, &map_q, 0, b * p.Hq + g * kG, 0, 0, kb);
-        tma_load_4d(kst + kKQ + kQHalf, &map_q, 64, b * p.Hq + g * kG, 0, 0, kb);
+        if constexpr (kHalves == 2) {
+          tma_load_4d(kst + kKK + kHalf, &map_k, 64, u * kW, 0, 0, kb);
+          tma_load_4d(kst + kKQ + kQHalf, &map_q, 64, b * p.Hq + g * kG, 0, 0, kb);
+        }
         ++nkld;
         const uint32_t vs = (uint32_t)k % kVSlots;
         if (!mbar_wait(bar(kBarVEmpty + vs), (((uint32_t)k / kVSlots) & 1) ^ 1, kErrWaitKvEmpty,
@@ -236,9 +244,9 @@ __global__ void __launch_bounds__(threads_for(kG), 1)
           break;
         const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
         const uint32_t vb = bar(kBarVFull + vs);
-        mbar_arrive_expect_tx(vb, kVSlotBytes);
+        mbar_arrive_expect_tx(vb, kHalves * kHalf);
         tma_load_4d(vst, &map_v, 0, u * kW, 0, 0, vb);
-        tma_load_4d(vst + kHalf, &map_v, 64, u * kW, 0, 0, vb);
+        if constexpr (kHalves == 2) tma_load_4d(vst + kHalf, &map_v, 64, u * kW, 0, 0, vb);
         ++nvld;
       }
       if (nvld < nk) {  // stopped early: let the copies already issued land
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(threads_for(kG), 1)
           const uint64_t kdesc = umma_sdesc(kst + kKK, 16, 1024, 2);
           const uint64_t qdesc = umma_sdesc(kst + kKQ, 16, 1024, 2);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < kHd / 16; ++kk) {
             const uint32_t a_off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
             const uint32_t b_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
             umma_bf16_ss(tmem + col_s(w), kdesc + a_off, qdesc + b_off, idesc_s, kk > 0);
@@ -300,7 +308,9 @@ __global__ void __launch_bounds__(threads_for(kG), 1)
             break;
           }
           tc_fence_after();
-          const uint64_t vdesc = umma_sdesc(vst, kHalf, 1024, 2);
+          // V^T as the M = 128 operand: its second 64-dimension atom is the
+          // slot's second half, or, at kHd = 64, the first again
+          const uint64_t vdesc = umma_sdesc(vst, kHalves == 2 ? kHalf : 0, 1024, 2);
           const uint64_t pdesc = umma_sdesc(sbase + kOffP + w * kPBytes, 16, 1024, 2);
 #pragma unroll
           for (int kb = 0; kb < kW / 16; ++kb) {
@@ -358,7 +368,6 @@ __global__ void __launch_bounds__(threads_for(kG), 1)
         x[h] = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
         m[h] = x[h];
       }
-#pragma unroll
       {
         // the warp's max for head lane >> (5 - log2 G); the first lane of each
         // head publishes it
@@ -394,13 +403,12 @@ __global__ void __launch_bounds__(threads_for(kG), 1)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           st_shared_v4(vrow + 16 * c, 0u, 0u, 0u, 0u);
-          st_shared_v4(vrow + kHalf + 16 * c, 0u, 0u, 0u, 0u);
+          if constexpr (kHalves == 2) st_shared_v4(vrow + kHalf + 16 * c, 0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + w));
-#pragma unroll
       {
         const float mine = warp_reduce_heads<kG, false>(l, lane);
         if ((lane & (32 / kG - 1)) == 0) red[4 * kG + quad * kG + lane / (32 / kG)] = mine;
@@ -428,9 +436,11 @@ __global__ void __launch_bounds__(threads_for(kG), 1)
       reg_fence8(*reinterpret_cast<uint32_t(*)[8]>(&o[0]));
       if constexpr (kG > 8) reg_fence8(*reinterpret_cast<uint32_t(*)[8]>(&o[8]));
       tc_fence_before();
-      float* ob = p.out + ((int64_t)b * p.Hq + g * kG) * kD + t;
+      float* ob = p.out + ((int64_t)b * p.Hq + g * kG) * kHd + t;
+      if (t < kHd) {
 #pragma unroll
-      for (int h = 0; h < kG; ++h) ob[h * kD] = __uint_as_float(o[h]) * inv_l[h];
+        for (int h = 0; h < kG; ++h) ob[h * kHd] = __uint_as_float(o[h]) * inv_l[h];
+      }
     }
   }
 

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <array>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -45,11 +46,11 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  bool tc_attr[2][2] = {};   // [bf16 output][4 heads per tile]
+  bool tc_attr[2][2][2] = {};   // [bf16 output][4 heads per tile][D = 64]
   bool tcg_attr[2][2] = {{false, false}, {false, false}};   // [bf16 output][scores]
   bool topk_attr = false;
-  bool dectc_attr[5] = {};   // [log2 G]
-  bool vertc_attr[2] = {false, false};   // [64 query rows]
+  bool dectc_attr[5][2] = {};   // [log2 G][D = 64]
+  bool vertc_attr[2][2] = {};   // [64 query rows][D = 64]
   bool decode_attr[2][2][5] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -165,7 +166,7 @@ enum FwdPath { kPathInvalid, kPathSimt, kPathTcSwa, kPathTcGlobal };
 constexpr int kVerifyMaxL = 64;  // drafted tokens per verify call
 
 bool verify_tc_applies(int L, int Hq, int Hkv, int D, int W, swa_dtype dt) {
-  return dt == SWA_BF16 && D == swa::vertc::kD && W == swa::vertc::kW &&
+  return dt == SWA_BF16 && (D == 128 || D == 64) && W == swa::vertc::kW &&
          Hq == Hkv * swa::vertc::kG && L >= 1 && L <= swa::vertc::kLmax;
 }
 
@@ -178,11 +179,12 @@ FwdPath select_fwd(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype dt) {
   if (dt != SWA_F32 && dt != SWA_BF16) return kPathInvalid;
   if (D != 64 && D != 128) return kPathInvalid;
   const int G = Hq / Hkv;
-  if (dt == SWA_BF16 && D == swa::tcswa::kD) {
+  if (dt == SWA_BF16) {
     // G = 8 R: R sets of CTAs walk the sibling groups in step (R <= 64)
     if (W <= swa::tcswa::kMaxW && (G == 4 || (G % swa::tcswa::kGroup == 0 && G <= 512)))
-      return kPathTcSwa;
-    if (W > swa::tcswa::kMaxW && G % swa::tcglobal::kG == 0) return kPathTcGlobal;
+      return kPathTcSwa;   // D = 64 or 128
+    if (D == swa::tcglobal::kD && W > swa::tcswa::kMaxW && G % swa::tcglobal::kG == 0)
+      return kPathTcGlobal;
   }
   return kPathSimt;
 }
@@ -214,26 +216,30 @@ swa_status launch_simt(const void* q, const void* k, const void* v, const float*
 // Tiles n_first .. n_first + n_tiles - 1 (of 128 / heads-per-tile positions
 // each) of every sequence; n_tiles < 0: to the end of the sequence.
 swa_status launch_tc_swa(const void* q, const void* k, const void* v, const float* sink,
-                         void* out, float* lse, int B, int T, int Hq, int Hkv, int W,
+                         void* out, float* lse, int B, int T, int Hq, int Hkv, int D, int W,
                          bool bf16_out, cudaStream_t st, int n_first = 0, int n_tiles = -1) {
   using namespace swa::tcswa;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
   const int gt = tc_heads_per_tile(Hq / Hkv);
-  const bool four = gt == 4;
+  const bool four = gt == 4, d64 = D == 64;
   const int kNpos = 128 / gt;
-  auto kern = bf16_out ? (four ? swa_fwd_tc_kernel<true, 4> : swa_fwd_tc_kernel<true, 8>)
-                       : (four ? swa_fwd_tc_kernel<false, 4> : swa_fwd_tc_kernel<false, 8>);
+  void (*const kernels[2][2][2])(CUtensorMap, CUtensorMap, CUtensorMap, Params) = {
+      {{swa_fwd_tc_kernel<false, 8, 128>, swa_fwd_tc_kernel<false, 8, 64>},
+       {swa_fwd_tc_kernel<false, 4, 128>, swa_fwd_tc_kernel<false, 4, 64>}},
+      {{swa_fwd_tc_kernel<true, 8, 128>, swa_fwd_tc_kernel<true, 8, 64>},
+       {swa_fwd_tc_kernel<true, 4, 128>, swa_fwd_tc_kernel<true, 4, 64>}}};
+  auto kern = kernels[bf16_out][four][d64];
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].tc_attr[bf16_out][four]) {
+    if (!g_dev[dev].tc_attr[bf16_out][four][d64]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].tc_attr[bf16_out][four] = true;
+      g_dev[dev].tc_attr[bf16_out][four][d64] = true;
     }
   }
   const int Hg = Hq / gt;
@@ -245,9 +251,9 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
   }
   if (total_tiles <= 0) return SWA_OK;
   CUtensorMap mq, mk, mv;
-  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, T, B, 64, gt, kNpos) ||
-      !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, kD, Hkv, T, B, 64, 1, kBlk) ||
-      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, kD, Hkv, T, B, 64, 1, kBlk))
+  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, Hq, T, B, 64, gt, kNpos) ||
+      !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, D, Hkv, T, B, 64, 1, kBlk) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, D, Hkv, T, B, 64, 1, kBlk))
     return SWA_ECUDA;
   Params p;
   p.sink = sink;
@@ -264,7 +270,7 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
   p.ntiles_seq = (int)ntiles_seq;
   p.total_tiles = (int)total_tiles;
   p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   p.withhold_cta = g_withhold_cta;   // one launch only
   g_withhold_cta = -1;
   // rep equal sets of CTAs, one per sibling group (the kernel's tile ranges)
@@ -376,32 +382,36 @@ int log2_group(int Hq, int Hkv) {
 }
 
 bool decode_tc_applies(int Hq, int Hkv, int D, int W, swa_dtype dt) {
-  return dt == SWA_BF16 && D == swa::dectc::kD && W == swa::dectc::kW &&
+  return dt == SWA_BF16 && (D == 128 || D == 64) && W == swa::dectc::kW &&
          log2_group(Hq, Hkv) >= 0;
 }
 
 swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const int64_t* pos,
                             const float* sink, float* out, float* lse, int B, int Hq, int Hkv,
-                            cudaStream_t st, int dev) {
+                            int D, cudaStream_t st, int dev) {
   using namespace swa::dectc;
   int sms;
   if (!device_sms(dev, &sms)) return SWA_ECUDA;
   const int lg = log2_group(Hq, Hkv);
-  void (*const kernels[5])(CUtensorMap, CUtensorMap, CUtensorMap, Params) = {
-      decode_tc_kernel<1>, decode_tc_kernel<2>, decode_tc_kernel<4>, decode_tc_kernel<8>,
-      decode_tc_kernel<16>};
+  const bool d64 = D == 64;
+  void (*const kernels[5][2])(CUtensorMap, CUtensorMap, CUtensorMap, Params) = {
+      {decode_tc_kernel<1, 128>, decode_tc_kernel<1, 64>},
+      {decode_tc_kernel<2, 128>, decode_tc_kernel<2, 64>},
+      {decode_tc_kernel<4, 128>, decode_tc_kernel<4, 64>},
+      {decode_tc_kernel<8, 128>, decode_tc_kernel<8, 64>},
+      {decode_tc_kernel<16, 128>, decode_tc_kernel<16, 64>}};
   if (lg < 0) return SWA_EUNSUPPORTED;
-  auto kern = kernels[lg];
+  auto kern = kernels[lg][d64];
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].dectc_attr[lg]) {
+    if (!g_dev[dev].dectc_attr[lg][d64]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(decode_tc_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].dectc_attr[lg] = true;
+      g_dev[dev].dectc_attr[lg][d64] = true;
     }
   }
   const long long units = (long long)B * Hkv;
@@ -410,9 +420,9 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
     return SWA_EUNSUPPORTED;
   }
   CUtensorMap mk, mv, mq;
-  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, kD, units * kW, 1, 1, 64, kW, 1) ||
-      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, kD, units * kW, 1, 1, 64, kW, 1) ||
-      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, (uint64_t)B * Hq, 1, 1, 64, kN,
+  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, D, units * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, D, units * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, (uint64_t)B * Hq, 1, 1, 64, kN,
                    1))
     return SWA_ECUDA;
   Params p;
@@ -424,7 +434,7 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.units = (int)units;
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const long long grid = units < sms ? units : sms;
   return launch_dependent("decode_tc_kernel", kern, (unsigned)grid, threads_for(1 << lg), kSmemBytes,
                           st, mk, mv, mq, p);
@@ -432,24 +442,27 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
 
 swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const void* kr,
                             const void* vr, const int64_t* pos, const float* sink, float* out,
-                            float* lse, int B, int L, int Hq, int Hkv, cudaStream_t st) {
+                            float* lse, int B, int L, int Hq, int Hkv, int D, cudaStream_t st) {
   using namespace swa::vertc;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
   // 32 query rows per group up to L = 4, else 64
-  const bool rows64 = L * kG > 32;
-  auto kern = rows64 ? verify_tc_kernel<64> : verify_tc_kernel<32>;
+  const bool rows64 = L * kG > 32, d64 = D == 64;
+  void (*const kernels[2][2])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                              Params) = {{verify_tc_kernel<32, 128>, verify_tc_kernel<32, 64>},
+                                         {verify_tc_kernel<64, 128>, verify_tc_kernel<64, 64>}};
+  auto kern = kernels[rows64][d64];
   const int smem = rows64 ? Layout<64>::kSmemBytes : Layout<32>::kSmemBytes;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].vertc_attr[rows64]) {
+    if (!g_dev[dev].vertc_attr[rows64][d64]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            smem);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(verify_tc_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].vertc_attr[rows64] = true;
+      g_dev[dev].vertc_attr[rows64][d64] = true;
     }
   }
   const long long units = (long long)B * Hkv;
@@ -458,11 +471,11 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
     return SWA_EUNSUPPORTED;
   }
   CUtensorMap mk, mv, mq, mkn, mvn;
-  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, kD, units * kW, 1, 1, 64, kW, 1) ||
-      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, kD, units * kW, 1, 1, 64, kW, 1) ||
-      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, L, B, 64, kG, L) ||
-      !make_map_4d(&mkn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kn, kD, Hkv, L, B, 64, 1, L) ||
-      !make_map_4d(&mvn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vn, kD, Hkv, L, B, 64, 1, L))
+  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, D, units * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, D, units * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, Hq, L, B, 64, kG, L) ||
+      !make_map_4d(&mkn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kn, D, Hkv, L, B, 64, 1, L) ||
+      !make_map_4d(&mvn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vn, D, Hkv, L, B, 64, 1, L))
     return SWA_ECUDA;
   Params p;
   p.pos = pos;
@@ -474,7 +487,7 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.units = (int)units;
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const long long grid = units < sms ? units : sms;
   return launch_dependent("verify_tc_kernel", kern, (unsigned)grid, kThreads, smem, st, mk, mv, mq, mkn, mvn, p);
 }
@@ -539,7 +552,7 @@ swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const fl
   const bool bf16_out = out_dtype == SWA_BF16;
   switch (select_fwd(B, T, Hq, Hkv, D, W, in_dtype)) {
     case kPathTcSwa:
-      return launch_tc_swa(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, bf16_out, st);
+      return launch_tc_swa(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, bf16_out, st);
     case kPathTcGlobal:
       return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, bf16_out, st);
     case kPathSimt:
@@ -616,9 +629,8 @@ char* byte_at(const void* base, size_t off) {
 // same stream, so they are in place when it runs.
 swa_status host_by_position(const void* q_h, const void* k_h, const void* v_h, const float* sink,
                             void* out_h, float* lse_h, void* q_d, void* k_d, void* v_d,
-                            void* out_d, float* lse_d, int B, int T, int Hq, int Hkv, int W,
-                            bool bf16_out, cudaStream_t st, HostPipe& hp) {
-  constexpr int kD = swa::tcswa::kD;
+                            void* out_d, float* lse_d, int B, int T, int Hq, int Hkv, int D,
+                            int W, bool bf16_out, cudaStream_t st, HostPipe& hp) {
   // chunks of whole tiles for either tile shape (16 or 32 positions)
   const int kNpos = 128 / tc_heads_per_tile(Hq / Hkv), kChunkAlign = 32;
   if (!aligned16(q_d) || !aligned16(k_d) || !aligned16(v_d) || !aligned16(out_d) ||
@@ -629,18 +641,33 @@ swa_status host_by_position(const void* q_h, const void* k_h, const void* v_h, c
   if (nper > T / 512) nper = T / 512;
   if (nper < 1) nper = 1;
   const int Tc = ((T + nper - 1) / nper + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
-  const int nchunk_seq = (T + Tc - 1) / Tc;
-  const int nchunk = B * nchunk_seq;
-  const size_t q_tok = (size_t)Hq * kD * 2, k_tok = (size_t)Hkv * kD * 2;
-  const size_t o_tok = (size_t)Hq * kD * (bf16_out ? 2 : 4);
+  // chunks {b, t0, t1}; the copy-in of the first and the copy-out of the last
+  // overlap nothing, so a short piece (kEdge positions) is split off each
+  constexpr int kEdge = 512;
+  std::vector<std::array<int, 3>> chunks;
+  for (int b = 0; b < B; ++b)
+    for (int t0 = 0; t0 < T; t0 += Tc) chunks.push_back({b, t0, t0 + Tc < T ? t0 + Tc : T});
+  if (chunks.front()[2] - chunks.front()[1] > 2 * kEdge) {
+    const std::array<int, 3> f = chunks.front();
+    chunks.front()[2] = f[1] + kEdge;
+    chunks.insert(chunks.begin() + 1, {f[0], f[1] + kEdge, f[2]});
+  }
+  if (chunks.back()[2] - chunks.back()[1] > 2 * kEdge) {
+    const std::array<int, 3> l = chunks.back();
+    const int cut = (l[2] - kEdge) / kChunkAlign * kChunkAlign;   // a tile boundary
+    chunks.back()[2] = cut;
+    chunks.push_back({l[0], cut, l[2]});
+  }
+  const int nchunk = (int)chunks.size();
+  const size_t q_tok = (size_t)Hq * D * 2, k_tok = (size_t)Hkv * D * 2;
+  const size_t o_tok = (size_t)Hq * D * (bf16_out ? 2 : 4);
   if (!pipe_events(hp, 2 + 2 * (size_t)nchunk)) return SWA_ECUDA;
   cudaEvent_t ev_start = hp.ev[0], ev_end = hp.ev[1];
   swa_status rc = cuda_ok(cudaEventRecord(ev_start, st), "cudaEventRecord");
   if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(hp.h2d, ev_start, 0), "cudaStreamWaitEvent");
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
   for (int c = 0; rc == SWA_OK && c < nchunk; ++c) {
-    const int b = c / nchunk_seq, t0 = (c % nchunk_seq) * Tc;
-    const int t1 = t0 + Tc < T ? t0 + Tc : T;
+    const int b = chunks[c][0], t0 = chunks[c][1], t1 = chunks[c][2];
     const size_t row0 = (size_t)b * T + t0, n = (size_t)(t1 - t0), seq0 = (size_t)b * T;
     cudaEvent_t ev_in = hp.ev[2 + 2 * c], ev_c = hp.ev[3 + 2 * c];
     rc = cuda_ok(cudaMemcpyAsync(byte_at(q_d, row0 * q_tok), byte_at(q_h, row0 * q_tok),
@@ -659,8 +686,8 @@ swa_status host_by_position(const void* q_h, const void* k_h, const void* v_h, c
     if (rc == SWA_OK)
       rc = launch_tc_swa(byte_at(q_d, seq0 * q_tok), byte_at(k_d, seq0 * k_tok),
                          byte_at(v_d, seq0 * k_tok), sink, byte_at(out_d, seq0 * o_tok),
-                         lse_d ? lse_d + (size_t)b * Hq * T : nullptr, 1, T, Hq, Hkv, W, bf16_out,
-                         st, t0 / kNpos, (t1 + kNpos - 1) / kNpos - t0 / kNpos);
+                         lse_d ? lse_d + (size_t)b * Hq * T : nullptr, 1, T, Hq, Hkv, D, W,
+                         bf16_out, st, t0 / kNpos, (t1 + kNpos - 1) / kNpos - t0 / kNpos);
     if (rc == SWA_OK) rc = cuda_ok(cudaEventRecord(ev_c, st), "cudaEventRecord");
     if (rc == SWA_OK) rc = cuda_ok(cudaStreamWaitEvent(hp.d2h, ev_c, 0), "cudaStreamWaitEvent");
     if (rc == SWA_OK)
@@ -702,8 +729,8 @@ swa_status swa_sink_fwd_host(const void* q_h, const void* k_h, const void* v_h,
     HostPipe& hp = g_pipe[dev];
     if (!pipe_ready(hp)) return SWA_ECUDA;
     return host_by_position(q_h, k_h, v_h, sink, out_h, lse_h, q_d, k_d, v_d, out_d, lse_d, B, T,
-                            Hq, Hkv, W, out_dtype == SWA_BF16, static_cast<cudaStream_t>(stream),
-                            hp);
+                            Hq, Hkv, D, W, out_dtype == SWA_BF16,
+                            static_cast<cudaStream_t>(stream), hp);
   }
   const size_t ie = in_dtype == SWA_BF16 ? 2 : 4, oe = out_dtype == SWA_BF16 ? 2 : 4;
   // Other paths: chunks of one sequence x a share of the kv heads (two shares when Hkv is
@@ -893,7 +920,7 @@ swa_status swa_sink_decode(const void* q, const void* k_ring, const void* v_ring
   if (!current_device(&dev)) return SWA_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (decode_tc_applies(Hq, Hkv, D, W, in_dtype))
-    return launch_decode_tc(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, st, dev);
+    return launch_decode_tc(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, D, st, dev);
   if (in_dtype == SWA_F32) {
     if (D == 64)
       return launch_decode_g<float, 64>(q, k_ring, v_ring, pos, sink, out, lse, B, Hq, Hkv, W, st, dev);
@@ -953,7 +980,7 @@ swa_status swa_sink_verify(const void* q, const void* k_new, const void* v_new,
   if (blocks > 0x7fffffffLL) return SWA_EUNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (verify_tc_applies(L, Hq, Hkv, D, W, in_dtype))
-    return launch_verify_tc(q, k_new, v_new, k_ring, v_ring, pos, sink, out, lse, B, L, Hq, Hkv,
+    return launch_verify_tc(q, k_new, v_new, k_ring, v_ring, pos, sink, out, lse, B, L, Hq, Hkv, D,
                             st);
   const float scale = (float)(1.0 / std::sqrt((double)D));
 #define SWA_VERIFY_LAUNCH(T, DD)                                                              \

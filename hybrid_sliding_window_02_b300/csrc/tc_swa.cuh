@@ -3,7 +3,10 @@
 // Operation: causal sliding-window attention with GQA and a per-head sink bias
 // in the softmax denominator ("MiMo-V2-Flash Technical Report" summary, section
 // 前置知识; 128-token window in section 核心方法).  This kernel covers W <= 129,
-// bf16 inputs, D = 128, and G = 4 or any multiple of 8 query heads per kv head.
+// bf16 inputs, D = 128 or 64, and G = 4 or any multiple of 8 query heads per
+// kv head.  With D = 64 the score products are 4 K-steps deep instead of 8, PV
+// has N = 64, O takes 64 TMEM columns, and only the first 64-dimension half
+// of each staging buffer is used (the layout is the same).
 //
 // Tiling.  One tile = kNpos consecutive positions x kG query heads = 128 MMA
 // rows (row r = position (r / kG), head (r % kG)): 16 positions x 8 heads, or
@@ -70,7 +73,7 @@ namespace tcswa {
 constexpr int kThreads = 480;
 constexpr int kWarpProducer = 12, kWarpMma = 13, kWarpPv = 14;
 constexpr int kWarpEpi0 = 8;
-constexpr int kD = 128;
+constexpr int kD = 128;          // largest head dimension (64 is the other)
 constexpr int kBlk = 16;         // keys per ring block
 constexpr uint32_t kRing = 12;   // ring slots
 constexpr uint32_t kQStages = 4;
@@ -165,13 +168,31 @@ struct TileWalk {
   }
 };
 
-template <bool kBf16Out, int kG>
+// 16 lanes x 256 bits, 8 repetitions along the columns (64 columns): as
+// tmem_ld_16x256b_x16 for the first 64 columns.
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+template <bool kBf16Out, int kG, int kHd>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const Params p) {
   using S = Shape<kG>;
   constexpr int kNpos = S::kNpos, kNew = S::kNew, kNB = S::kNB, kNh = S::kNh;
+  static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");
+  constexpr int kHalves = kHd / 64;   // 64-dimension halves of q, k, v rows
   auto col_p = [](int b) { return S::kColP + (uint32_t)(kNh * b); };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -248,9 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t qdst = sbase + kOffQ + qs * kQStage;
-        mbar_arrive_expect_tx(bar(kBarQFull + qs), kQStage);
+        mbar_arrive_expect_tx(bar(kBarQFull + qs), kHalves * kQHalf);
         tma_load_4d(qdst, &map_q, 0, grp * kG, n * kNpos, b, bar(kBarQFull + qs));
-        tma_load_4d(qdst + kQHalf, &map_q, 64, grp * kG, n * kNpos, b, bar(kBarQFull + qs));
+        if constexpr (kHalves == 2)
+          tma_load_4d(qdst + kQHalf, &map_q, 64, grp * kG, n * kNpos, b, bar(kBarQFull + qs));
         ++q_issued;
         const int bk = b * p.Hg + grp;
         const int last_blk = n * kNew + kNew - 1;
@@ -264,13 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t kb = bar(kBarKvFull + slot);
-          mbar_arrive_expect_tx(kb, 4 * kBlkHalf);
+          mbar_arrive_expect_tx(kb, 2 * kHalves * kBlkHalf);
           const uint32_t kdst = sbase + kOffK + slot * kBlkHalf;
           const uint32_t vdst = sbase + kOffV + slot * kBlkHalf;
           tma_load_4d(kdst, &map_k, 0, kvh, m * kBlk, b, kb);
-          tma_load_4d(kdst + kRingHalf, &map_k, 64, kvh, m * kBlk, b, kb);
           tma_load_4d(vdst, &map_v, 0, kvh, m * kBlk, b, kb);
-          tma_load_4d(vdst + kRingHalf, &map_v, 64, kvh, m * kBlk, b, kb);
+          if constexpr (kHalves == 2) {
+            tma_load_4d(kdst + kRingHalf, &map_k, 64, kvh, m * kBlk, b, kb);
+            tma_load_4d(vdst + kRingHalf, &map_v, 64, kvh, m * kBlk, b, kb);
+          }
         }
       }
       // Copies still in flight must land before the CTA exits: wait (bounded)
@@ -289,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // waits and bookkeeping no longer hold back the other's MMAs.
     if (lane == 0) {
       const bool s_side = (warp == kWarpMma);
-      const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
+      const uint32_t idesc_o = umma_idesc_bf16(kHd, false, true);
       // Descriptors are built once; per operand they differ only in the
       // start-address field (address >> 4, bits 0..13), advanced by adding
       // the byte offset >> 4 (shared addresses stay below 2^18: no carry).
@@ -341,14 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t kd1 = kdesc0 + slot0 * (kBlkHalf >> 4);
           if (seg1 == (uint32_t)kNB) {
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
+            for (int kk = 0; kk < kHd / 16; ++kk) {
               const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
               const uint32_t k_off = ((kk >> 2) * kRingHalf + (kk & 3) * 32) >> 4;
               umma_bf16_ss(d_s, qd + a_off, kd1 + k_off, idesc1, kk > 0);
             }
           } else {
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
+            for (int kk = 0; kk < kHd / 16; ++kk) {
               const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
               const uint32_t k_off = ((kk >> 2) * kRingHalf + (kk & 3) * 32) >> 4;
               umma_bf16_ss(d_s, qd + a_off, kd1 + k_off, idesc1, kk > 0);
@@ -582,16 +606,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rounded to bf16 and written as whole 32-byte sectors
         const int pos = n * kNpos + (32 * sub + lane) / kG;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                              (((long long)b * p.T + pos) * p.Hq + grp * kG + lane % kG) * kD;
+                              (((long long)b * p.T + pos) * p.Hq + grp * kG + lane % kG) * kHd;
 #pragma unroll
-        for (int rd = 0; rd < 2; ++rd) {
+        for (int rd = 0; rd < kHalves; ++rd) {
           uint32_t o[64];
           tmem_ld32(col + 64 * rd, o);
           tmem_ld32(col + 64 * rd + 32, o + 32);
           tmem_ld_wait();
           reg_fence32(o);
           reg_fence32(o + 32);
-          if (rd == 1) {
+          if (rd == kHalves - 1) {
             tc_fence_before();
             mbar_arrive(bar(kBarOFree));
           }
@@ -620,11 +644,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // position (row / kG), head (row % kG); columns 8j + 2 quad + {0, 1}
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t o[64];
-        tmem_ld_16x256b_x16(col + ((uint32_t)(16 * hf) << 16), o);
+        uint32_t o[kHd / 2];
+        if constexpr (kHd == 128)
+          tmem_ld_16x256b_x16(col + ((uint32_t)(16 * hf) << 16), o);
+        else
+          tmem_ld_16x256b_x8(col + ((uint32_t)(16 * hf) << 16), o);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o[c * 16]));
+        for (int c = 0; c < kHd / 32; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o[c * 16]));
         if (hf == 1) {
           tc_fence_before();
           mbar_arrive(bar(kBarOFree));
@@ -635,10 +662,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pos = n * kNpos + row / kG;
           if (pos < p.T) {
             const long long e0 =
-                (((long long)b * p.T + pos) * p.Hq + grp * kG + row % kG) * kD + 2 * quad;
+                (((long long)b * p.T + pos) * p.Hq + grp * kG + row % kG) * kHd + 2 * quad;
             float* orow = static_cast<float*>(p.out) + e0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
+            for (int j = 0; j < kHd / 8; ++j)
               st_global_v2(orow + 8 * j, o[4 * j + 2 * k], o[4 * j + 2 * k + 1]);
           }
         }

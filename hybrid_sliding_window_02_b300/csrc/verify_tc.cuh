@@ -56,7 +56,7 @@ constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr int kG = 8;
 constexpr int kLmax = 8;            // drafted tokens of the larger kernel size
 constexpr int kW = 128;
-constexpr int kD = 128;
+constexpr int kD = 128;            // largest head dimension (64 is the other)
 constexpr int kNewRows = 16;        // new keys padded to one K = 16 MMA step
 
 // Two rings in shared memory (128-byte swizzle everywhere):
@@ -108,7 +108,10 @@ struct Params {
   float scale_log2;
 };
 
-template <int kRows>
+// kRows query rows per group (32 or 64), head dimension kHd (64 or 128: with
+// 64 only the first 64-dimension half of each staging buffer is loaded, the
+// score products are 4 K-steps deep and PV has N = 64).
+template <int kRows, int kHd>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v,
@@ -129,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kBarOFull = Lay::kBarOFull, kBarODone = Lay::kBarODone,
                 kBarDrain = Lay::kBarDrain;
   constexpr int kSoftWarps = kRows / 32;        // softmax warps per warpgroup
+  static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");
+  constexpr int kHalves = kHd / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -200,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProducer) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      const uint32_t kbytes = 2 * kHalf + 2 * (8 * L * 128) + 2 * (L * 128);
-      const uint32_t vbytes = 2 * kHalf + 2 * (L * 128);
+      const uint32_t kbytes = kHalves * (kHalf + 8 * L * 128 + L * 128);
+      const uint32_t vbytes = kHalves * (kHalf + L * 128);
       int nkld = 0, nvld = 0;  // K / V slot loads issued
       for (int k = 0; k < nk; ++k) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kb = bar(kBarKFull + ks);
         mbar_arrive_expect_tx(kb, kbytes);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < kHalves; ++hf) {
           tma_load_4d(kst + kKQ + hf * kQHalf, &map_q, 64 * hf, g * kG, 0, b, kb);
           tma_load_4d(kst + kKK + hf * kHalf, &map_k, 64 * hf, u * kW, 0, 0, kb);
           tma_load_4d(kst + kKKn + hf * kKnHalf, &map_kn, 64 * hf, g, 0, b, kb);
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vb = bar(kBarVFull + vs);
         mbar_arrive_expect_tx(vb, vbytes);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < kHalves; ++hf) {
           tma_load_4d(vst + kVV + hf * kHalf, &map_v, 64 * hf, u * kW, 0, 0, vb);
           tma_load_4d(vst + kVVn + hf * kNewHalf, &map_vn, 64 * hf, g, 0, b, vb);
         }
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_s = umma_idesc_bf16(kW, false, false);
       const uint32_t idesc_n = umma_idesc_bf16(kNewRows, false, false);
-      const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
+      const uint32_t idesc_o = umma_idesc_bf16(kHd, false, true);
       bool ok = true;
       for (int k = 0; ok && k < nk; ++k) {
         const int w = k & 1;
@@ -278,14 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t kdesc = umma_sdesc(kst + kKK, 16, 1024, 2);
           const uint64_t kndesc = umma_sdesc(kst + kKKn, 16, 1024, 2);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < kHd / 16; ++kk) {
             const uint32_t qoff = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
             const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
             umma_bf16_ss(tmem + col_s(w), qdesc + qoff, kdesc + koff, idesc_s, kk > 0);
           }
           // S_new = Q K_new^T into O_w columns [0, 16)
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < kHd / 16; ++kk) {
             const uint32_t qoff = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
             const uint32_t noff = ((kk >> 2) * kKnHalf + (kk & 3) * 32) >> 4;
             umma_bf16_ss(tmem + col_o(w), qdesc + qoff, kndesc + noff, idesc_n, kk > 0);
@@ -442,14 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        float* orow = p.out + (((int64_t)b * L + j) * p.Hq + g * kG + h) * kD;
+        float* orow = p.out + (((int64_t)b * L + j) * p.Hq + g * kG + h) * kHd;
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
+        for (int c = 0; c < kHd / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(o_addr + c * 32, o);
           tmem_ld_wait();
           reg_fence32(o);
-          if (c == kD / 32 - 1) {
+          if (c == kHd / 32 - 1) {
             // O_w has been read: S_new of group k + 2 may overwrite it
             tc_fence_before();
             mbar_arrive(bar(kBarODone + w));
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
                 st_shared_v4(vrow + 16 * c, 0u, 0u, 0u, 0u);
-                st_shared_v4(vrow + kHalf + 16 * c, 0u, 0u, 0u, 0u);
+                if constexpr (kHalves == 2) st_shared_v4(vrow + kHalf + 16 * c, 0u, 0u, 0u, 0u);
               }
             }
           }

@@ -97,10 +97,11 @@ swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const fl
  * copies of the neighbouring chunks run at the same time (host-to-device on
  * one stream, the prefill on `stream`, device-to-host on another; each
  * chunk's steps are chained by events).  On the sliding-window tensor-core
- * path (swa_sink_fwd_path "tc_swa": bf16, D = 128, W <= 129, 4 or a
- * multiple of 8 query heads per kv head) a chunk is one
+ * path (swa_sink_fwd_path "tc_swa") a chunk is one
  * sequence x a range of positions (about 16 chunks in all, at least 512
- * positions each), staged at its own place in the device buffers, so that
+ * positions each, and a piece of 512 positions split off the first and the
+ * last, whose copies overlap nothing), staged at its own place in the device
+ * buffers, so that
  * every copy is one contiguous range; the prefill of a chunk computes its
  * positions only, reading the window's earlier keys copied with the chunks
  * before it.  On the other paths a chunk is one sequence x a share of the kv
@@ -320,20 +321,20 @@ swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, cons
                                swa_dtype out_dtype, void* stream);
 
 /* Name of the prefill kernel swa_sink_fwd would launch for these sizes, or
- * "invalid": bf16 inputs with D = 128 take "tc_swa" (the sliding-window
- * tensor-core kernel) when W <= 129 and Hq / Hkv is 4 or a multiple of 8 up to
- * 512, and "tc_global" (the online-softmax tensor-core kernel) when W > 129
- * and Hq / Hkv is a multiple of 8; everything else takes "simt" (CUDA cores,
- * fp32 or bf16 inputs). */
+ * "invalid": bf16 inputs take "tc_swa" (the sliding-window tensor-core kernel)
+ * when W <= 129 and Hq / Hkv is 4 or a multiple of 8 up to 512 (D = 64 or
+ * 128), and "tc_global" (the online-softmax tensor-core kernel) when W > 129,
+ * D = 128 and Hq / Hkv is a multiple of 8; everything else takes "simt" (CUDA
+ * cores, fp32 or bf16 inputs). */
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Name of the decode kernel swa_sink_decode would launch for these sizes
- * ("tc_decode" for bf16, D = 128, W = 128 and Hq / Hkv in {1, 2, 4, 8, 16};
+ * ("tc_decode" for bf16, D = 64 or 128, W = 128 and Hq / Hkv in {1, 2, 4, 8, 16};
  * "simt_decode" otherwise), or "invalid". */
 const char* swa_sink_decode_path(int B, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Name of the verify kernel swa_sink_verify would launch ("tc_verify" for
- * bf16, D = 128, W = 128, Hq = 8 Hkv and L <= 8; "simt_verify" otherwise), or
+ * bf16, D = 64 or 128, W = 128, Hq = 8 Hkv and L <= 8; "simt_verify" otherwise), or
  * "invalid". */
 const char* swa_sink_verify_path(int B, int L, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 

@@ -61,6 +61,9 @@ def test_path_selection(L):
     assert swa.fwd_path(1, 512, 48, 2, 128, 128) == "tc_swa"       # 24
     assert swa.fwd_path(1, 512, 32, 16, 128, 128) == "simt"        # 2 heads per kv head
     assert swa.fwd_path(1, 512, 12, 1, 128, 128) == "simt"         # 12: not a multiple of 8
+    assert swa.fwd_path(1, 512, 64, 8, 64, 128) == "tc_swa"        # head dimension 64
+    assert swa.fwd_path(1, 512, 16, 4, 64, 128) == "tc_swa"
+    assert swa.fwd_path(1, 512, 64, 8, 64, 512) == "simt"          # no global kernel at D 64
     assert swa.fwd_path(1, 512, 64, 7, 128, 128) == "invalid"
     assert swa.fwd_path(1, 512, 64, 8, 96, 128) == "invalid"
     assert swa.fwd_path(0, 512, 64, 8, 128, 128) == "invalid"
@@ -69,7 +72,8 @@ def test_path_selection(L):
 def test_decode_path_selection(L):
     assert swa.decode_path(256, 64, 8, 128, 128) == "tc_decode"
     assert swa.decode_path(256, 64, 8, 128, 128, swa.SWA_F32) == "simt_decode"
-    assert swa.decode_path(256, 64, 8, 64, 128) == "simt_decode"
+    assert swa.decode_path(256, 64, 8, 64, 128) == "tc_decode"       # head dimension 64
+    assert swa.decode_path(256, 64, 8, 64, 64) == "simt_decode"      # a 64-slot ring
     assert swa.decode_path(256, 32, 8, 128, 128) == "tc_decode"      # 4 heads per kv head
     assert swa.decode_path(256, 64, 4, 128, 128) == "tc_decode"      # 16
     assert swa.decode_path(256, 8, 8, 128, 128) == "tc_decode"       # 1
@@ -157,7 +161,8 @@ def test_verify_path_selection(L):
     assert swa.verify_path(2, 8, 64, 8, 128, 128) == "tc_verify"
     assert swa.verify_path(2, 9, 64, 8, 128, 128) == "simt_verify"
     assert swa.verify_path(2, 4, 64, 8, 128, 128, swa.SWA_F32) == "simt_verify"
-    assert swa.verify_path(2, 4, 8, 1, 64, 128) == "simt_verify"
+    assert swa.verify_path(2, 4, 8, 1, 64, 128) == "tc_verify"     # head dimension 64
+    assert swa.verify_path(2, 4, 8, 1, 64, 32) == "simt_verify"
     assert swa.verify_path(2, 65, 8, 1, 128, 128) == "invalid"
 
 

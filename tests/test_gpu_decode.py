@@ -47,6 +47,23 @@ def test_decode_tc_group_sizes(cuda_ok, B, Hq, Hkv):
     assert swa.device_error() == 0
 
 
+@pytest.mark.parametrize("B,Hq,Hkv", [(37, 64, 8), (29, 64, 4), (13, 8, 8), (50, 16, 4)])
+def test_decode_tc_head_dim_64(cuda_ok, B, Hq, Hkv):
+    # head dimension 64 on the tensor cores, partial rings with NaN in the empty slots
+    assert swa.decode_path(B, Hq, Hkv, 64, 128) == "tc_decode"
+    x = gen.decode_inputs(B, Hq, Hkv, 64, 128, seed=B + Hq + 64, pos_lo=0, pos_hi=600)
+    for b in range(B):
+        p = int(x.pos[b])
+        if p < 127:
+            x.k_ring[b, :, p + 1:] = float("nan")
+            x.v_ring[b, :, p + 1:] = float("nan")
+    o, l = _decode(x)
+    o_ref, l_ref = oracle.swa_sink_decode(x.q, x.k_ring, x.v_ring, x.pos, x.sink)
+    assert_bf16_close(o, o_ref)
+    assert_lse_close(l, l_ref)
+    assert swa.device_error() == 0
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,D,W,dt", [
     (3, 8, 1, 128, 128, torch.bfloat16), (5, 16, 1, 64, 64, torch.bfloat16),
     (4, 4, 2, 128, 33, torch.bfloat16), (2, 16, 16, 64, 7, torch.bfloat16),

@@ -32,6 +32,7 @@ def _device_call(x, W, out_dtype=torch.float32):
     (2, 77, 2, 1, 64, 33),        # general kernel, lse slabs not 16-byte aligned: one chunk
     (1, 5000, 16, 4, 128, 128),   # 4 heads per kv head: position chunks of whole 32-position tiles
     (2, 1500, 64, 4, 128, 128),   # 16 heads per kv head (two groups of 8)
+    (2, 2600, 64, 8, 64, 128),    # head dimension 64
 ])
 def test_host_call_equals_device_call(cuda_ok, pinned, B, T, Hq, Hkv, D, W):
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=B + T)

@@ -13,9 +13,9 @@ from gpu_helpers import assert_bf16_close, assert_lse_close, oracle_by_slices
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (64, 4)])
-def test_prefill_other_group_sizes_full_size(cuda_ok, Hq, Hkv):
-    B, T, D, W = 4, 8192, 128, 128
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (64, 4, 128), (64, 8, 64)])
+def test_prefill_other_group_sizes_full_size(cuda_ok, Hq, Hkv, D):
+    B, T, W = 4, 8192, 128
     assert swa.fwd_path(B, T, Hq, Hkv, D, W) == "tc_swa"
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device="cuda")
     out, lse = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
@@ -28,9 +28,9 @@ def test_prefill_other_group_sizes_full_size(cuda_ok, Hq, Hkv):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (64, 4)])
-def test_decode_other_group_sizes_full_size(cuda_ok, Hq, Hkv):
-    B, D, W = 256, 128, 128
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (64, 4, 128), (64, 8, 64)])
+def test_decode_other_group_sizes_full_size(cuda_ok, Hq, Hkv, D):
+    B, W = 256, 128
     assert swa.decode_path(B, Hq, Hkv, D, W) == "tc_decode"
     d = gen.decode_inputs(B, Hq, Hkv, D, W, seed=100, device="cuda")
     out, lse = swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink)

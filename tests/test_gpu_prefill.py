@@ -72,6 +72,23 @@ def test_tc_swa_group_sizes(cuda_ok, B, T, Hq, Hkv, W):
     _full_check(x, W)
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", [
+    (1, 300, 8, 1, 128),      # head dimension 64: 8 heads per tile
+    (2, 1000, 16, 4, 128),    # 4 heads per tile
+    (1, 700, 32, 2, 100),     # two groups of 8 per kv head
+    (1, 77, 8, 1, 1),
+    (1, 4099, 64, 8, 129),
+])
+def test_tc_swa_head_dim_64(cuda_ok, B, T, Hq, Hkv, W):
+    assert swa.fwd_path(B, T, Hq, Hkv, 64, W) == "tc_swa"
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 64, seed=1200 + T + W + Hq)
+    _full_check(x, W)
+    o16, l16 = swa.swa_sink_fwd(*(t.cuda() for t in (x.q, x.k, x.v, x.sink)), W,
+                                out_dtype=torch.bfloat16)
+    o32, l32 = _run(x, W)
+    assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(l16, l32)
+
+
 def test_tc_swa_sink_limits(cuda_ok):
     x = gen.prefill_inputs(1, 200, 8, 1, 128, seed=5)
     # no sink: plain windowed softmax

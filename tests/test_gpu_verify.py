@@ -73,6 +73,19 @@ def test_verify_tc_up_to_eight_drafts(cuda_ok, B, L, pos_hi):
     assert swa.device_error() == 0
 
 
+@pytest.mark.parametrize("B,L", [(33, 4), (21, 8), (7, 1)])
+def test_verify_tc_head_dim_64(cuda_ok, B, L):
+    assert swa.verify_path(B, L, 64, 8, 64, 128) == "tc_verify"
+    x = gen.verify_inputs(B, L, 64, 8, 64, 128, seed=B + L + 64, pos_lo=0, pos_hi=700)
+    for b in range(B):
+        p = int(x.pos[b])
+        if p < 128:
+            x.k_ring[b, :, p:] = float("nan")
+            x.v_ring[b, :, p:] = float("nan")
+    _check(x)
+    assert swa.device_error() == 0
+
+
 def test_verify_eight_drafts_equal_prefill_rows(cuda_ok):
     B, T, Hq, Hkv, D, W, L = 2, 600, 16, 2, 128, 128, 8
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=64, device="cuda")
