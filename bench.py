@@ -852,6 +852,7 @@ WIDE_DECODE = {"g4": dict(B=256, Hq=32, Hkv=8, D=128, W=128),
                "g16": dict(B=256, Hq=64, Hkv=4, D=128, W=128),
                "d64": dict(B=256, Hq=64, Hkv=8, D=64, W=128)}
 WIDE_VERIFY = {"l8": dict(B=256, L=8, Hq=64, Hkv=8, D=128, W=128)}
+WIDE_GLOBAL = {"d64": dict(B=1, T=16384, Hq=64, Hkv=8, D=64, W=16384)}
 
 
 def wide_prefill_line(swa, c, steps, dev, stream, peaks, cpu=False):
@@ -883,6 +884,38 @@ def wide_prefill_line(swa, c, steps, dev, stream, peaks, cpu=False):
     return line
 
 
+def wide_global_line(swa, c, steps, dev, stream, peaks, cpu=False):
+    """Global layer (W = T) of another head dimension: tensor roofline, the
+    burst peak (the call is timed alone), with the sustained one beside it."""
+    B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
+    out = torch.empty(B, T, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    ms, clocks = with_clocks(dev, lambda: _event_ms(
+        lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, out, lse, stream=stream),
+        steps, stream))
+    flops = work.prefill_flops(B, T, Hq, D, W)
+    tf = flops / (ms * 1e-3) / 1e12
+    burst = float(peaks["bf16_tflops"])
+    sust = float(peaks.get("bf16_tflops_sustained") or burst)
+    kpath = swa.fwd_path(B, T, Hq, Hkv, D, W)
+    line = {"workload": workload_name(c), "value": round(tf, 1), "unit": "TFLOP/s",
+            "ms_per_call": round(ms, 4),
+            "roofline": {"kernel": KERNEL_OF_PATH.get(kpath, kpath), "bound": "tensor",
+                         "achieved": round(tf, 1), "peak": burst, "unit": "TFLOP/s",
+                         "frac": round(tf / burst, 4), "flops_per_launch": flops,
+                         "frac_of_sustained": round(tf / sust, 4)},
+            "sm_mhz": clocks.get("sm_mhz")}
+    if cpu:
+        import oracle
+        rate, sample = cpu_global_layer(x, T)
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOP/s",
+                                "cores": oracle.num_threads(), "kind": "oracle", "sample": sample}
+    del x, out, lse
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_only(args):
     """A few eager calls of one of the other-shape workloads, for a profiler
     (``--only prefill_g4`` and so on); prints one JSON line with the mean
@@ -894,16 +927,21 @@ def run_only(args):
     stream = torch.cuda.Stream(device=dev)
     kind, name = args.only.split("_", 1)
     if kind == "prefill":
-        c = WIDE_PREFILL[name]
+        c = PREFILL if name == "main" else WIDE_PREFILL[name]
+        B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
+        x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
+        call = lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, stream=stream)
+    elif kind == "global":
+        c = WIDE_GLOBAL[name]
         B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
         x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
         call = lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, stream=stream)
     elif kind == "decode":
-        c = WIDE_DECODE[name]
+        c = DECODE if name == "main" else WIDE_DECODE[name]
         d = gen.decode_inputs(*(c[k] for k in ("B", "Hq", "Hkv", "D", "W")), seed=100, device=dev)
         call = lambda: swa.swa_sink_decode(d.q, d.k_ring, d.v_ring, d.pos, d.sink, stream=stream)
     else:
-        c = WIDE_VERIFY[name]
+        c = VERIFY if name == "main" else WIDE_VERIFY[name]
         v = gen.verify_inputs(*(c[k] for k in ("B", "L", "Hq", "Hkv", "D", "W")), seed=300,
                               device=dev)
         call = lambda: swa.swa_sink_verify(v.q, v.k_new, v.v_new, v.k_ring, v.v_ring, v.pos,
@@ -1030,6 +1068,8 @@ def run_ours(args, dist):
         for name, wc in WIDE_PREFILL.items():
             wide["prefill_" + name] = wide_prefill_line(swa, wc, max(20, args.steps // 20), dev,
                                                         stream, peaks, cpu)
+        for name, wc in WIDE_GLOBAL.items():
+            wide["global_" + name] = wide_global_line(swa, wc, 5, dev, stream, peaks, cpu)
         for name, wc in WIDE_DECODE.items():
             d = decode_line(swa, dev, stream, args.decode_steps, hbm, cpu, c=wc)
             wide["decode_" + name] = {k: d[k] for k in ("workload", "value", "unit", "roofline",
@@ -1096,9 +1136,10 @@ def main(argv=None):
     ap.add_argument("--no-wide", action="store_true",
                     help="skip the lines of other group sizes and draft counts")
     ap.add_argument("--only", default="",
-                    choices=[""] + [f"prefill_{n}" for n in WIDE_PREFILL] +
+                    choices=[""] + [f"{k}_main" for k in ("prefill", "decode", "verify")] +
+                    [f"prefill_{n}" for n in WIDE_PREFILL] + [f"global_{n}" for n in WIDE_GLOBAL] +
                     [f"decode_{n}" for n in WIDE_DECODE] + [f"verify_{n}" for n in WIDE_VERIFY],
-                    help="run only a few calls of one other-shape workload (for a profiler)")
+                    help="run only a few calls of one workload (for a profiler)")
     ap.add_argument("--hybrid-reps", type=int, default=5)
     ap.add_argument("--window", type=int, default=0,
                     help="window of the timed prefill (default 128; W >= T is a global layer); "

@@ -23,13 +23,12 @@
 // threads issue the MMAs, one the S^T products and one the O^T products, so
 // that waiting for a group's K slot to land never delays the PV of the group
 // before it (and with it the release of that group's V slot).  Two softmax
-// warpgroups (three for G = 16) take the groups in turn: thread = slot reads
-// its G head scores
-// from TMEM, the max and the sum over slots are warp-shuffle reductions (one
-// transposed butterfly for all heads) finished across the four warps in
-// shared memory, the bf16 P^T goes to
-// shared memory for the second MMA, and after it thread = dim reads O^T from
-// TMEM and writes out[b, h, dim] (each warp 128 contiguous bytes).
+// warpgroups (three for G = 16 or D = 64) take the groups in turn: thread =
+// slot reads its G head scores from TMEM, the max and the sum over slots are
+// warp-shuffle reductions (one transposed butterfly for all heads) finished
+// across the four warps in shared memory, the bf16 P^T goes to shared memory
+// for the second MMA, and after it thread = dim reads O^T from TMEM and writes
+// out[b, h, dim] (each warp 128 contiguous bytes).
 #pragma once
 
 #include "device_common.cuh"
@@ -40,9 +39,10 @@ namespace dectc {
 
 // Softmax warpgroups: two, taking alternate groups; three for 16 heads per kv
 // head, whose longer per-group chain (the softmax of 16 heads between the two
-// products) left HBM idle with two.  Then three special warps.
-__host__ __device__ constexpr int num_wg(int G) { return G > 8 ? 3 : 2; }
-__host__ __device__ constexpr int threads_for(int G) { return 32 * (4 * num_wg(G) + 3); }
+// products) left HBM idle with two, and for D = 64, whose groups carry half
+// the bytes for the same chain.  Then three special warps.
+__host__ __device__ constexpr int num_wg(int G, int D) { return (G > 8 || D == 64) ? 3 : 2; }
+__host__ __device__ constexpr int threads_for(int G, int D) { return 32 * (4 * num_wg(G, D) + 3); }
 constexpr int kMaxWG = 3;
 constexpr int kN = 16;             // MMA N: the G heads of a group padded to 16
 constexpr int kW = 128;            // ring slots
@@ -143,13 +143,13 @@ __device__ __forceinline__ float warp_reduce_heads(float (&v)[kG], int lane) {
 // second half of V^T pointed at the first, so TMEM lanes 64..127 hold a copy
 // that no thread reads.
 template <int kG, int kHd>
-__global__ void __launch_bounds__(threads_for(kG), 1)
+__global__ void __launch_bounds__(threads_for(kG, kHd), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v,
                      const __grid_constant__ CUtensorMap map_q, const Params p) {
   static_assert(kG >= 1 && kG <= kN, "a group's heads fill at most the 16 MMA columns");
-  constexpr int kNWG = num_wg(kG);
-  constexpr int kThreads = threads_for(kG);
+  constexpr int kNWG = num_wg(kG, kHd);
+  constexpr int kThreads = threads_for(kG, kHd);
   constexpr int kWarpProducer = 4 * kNWG, kWarpMma = kWarpProducer + 1, kWarpPv = kWarpProducer + 2;
   constexpr uint32_t kTmemCols = kNWG > 2 ? 128 : 64;   // 32 columns per warpgroup
   static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");

@@ -47,7 +47,7 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   bool tc_attr[2][2][2] = {};   // [bf16 output][4 heads per tile][D = 64]
-  bool tcg_attr[2][2] = {{false, false}, {false, false}};   // [bf16 output][scores]
+  bool tcg_attr[2][2][2] = {};   // [bf16 output][scores][D = 64]
   bool topk_attr = false;
   bool dectc_attr[5][2] = {};   // [log2 G][D = 64]
   bool vertc_attr[2][2] = {};   // [64 query rows][D = 64]
@@ -183,8 +183,7 @@ FwdPath select_fwd(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype dt) {
     // G = 8 R: R sets of CTAs walk the sibling groups in step (R <= 64)
     if (W <= swa::tcswa::kMaxW && (G == 4 || (G % swa::tcswa::kGroup == 0 && G <= 512)))
       return kPathTcSwa;   // D = 64 or 128
-    if (D == swa::tcglobal::kD && W > swa::tcswa::kMaxW && G % swa::tcglobal::kG == 0)
-      return kPathTcGlobal;
+    if (W > swa::tcswa::kMaxW && G % swa::tcglobal::kG == 0) return kPathTcGlobal;  // D = 64 or 128
   }
   return kPathSimt;
 }
@@ -284,27 +283,32 @@ swa_status launch_tc_swa(const void* q, const void* k, const void* v, const floa
 // blockmax: optional block-score output; blk_idx: optional block list (sparse
 // mode, query blocks of qb_size positions, topk entries each).
 swa_status launch_tc_global(const void* q, const void* k, const void* v, const float* sink,
-                            void* out, float* lse, int B, int T, int Hq, int Hkv, int W,
+                            void* out, float* lse, int B, int T, int Hq, int Hkv, int D, int W,
                             bool bf16_out, cudaStream_t st, float* blockmax = nullptr,
                             const int* blk_idx = nullptr, int qb_size = 0, int topk = 0) {
   using namespace swa::tcglobal;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
   const bool scores = blockmax != nullptr;
-  auto kern = bf16_out ? (scores ? swa_fwd_tc_global_kernel<true, true>
-                                 : swa_fwd_tc_global_kernel<true, false>)
-                       : (scores ? swa_fwd_tc_global_kernel<false, true>
-                                 : swa_fwd_tc_global_kernel<false, false>);
+  const bool d64 = D == 64;
+  using Kern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
+  // [bf16 output][scores][D = 64]
+  static const Kern kTable[2][2][2] = {
+      {{swa_fwd_tc_global_kernel<false, false, 128>, swa_fwd_tc_global_kernel<false, false, 64>},
+       {swa_fwd_tc_global_kernel<false, true, 128>, swa_fwd_tc_global_kernel<false, true, 64>}},
+      {{swa_fwd_tc_global_kernel<true, false, 128>, swa_fwd_tc_global_kernel<true, false, 64>},
+       {swa_fwd_tc_global_kernel<true, true, 128>, swa_fwd_tc_global_kernel<true, true, 64>}}};
+  const Kern kern = kTable[bf16_out][scores][d64];
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].tcg_attr[bf16_out][scores]) {
+    if (!g_dev[dev].tcg_attr[bf16_out][scores][d64]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_global_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].tcg_attr[bf16_out][scores] = true;
+      g_dev[dev].tcg_attr[bf16_out][scores][d64] = true;
     }
   }
   const long long nitem_seq = (T + kItemPos - 1) / kItemPos;
@@ -315,9 +319,9 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
     return SWA_EUNSUPPORTED;
   }
   CUtensorMap mq, mk, mv;
-  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, kD, Hq, T, B, 64, kG, kNpos) ||
-      !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, kD, Hkv, T, B, 64, 1, kBlk) ||
-      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, kD, Hkv, T, B, 64, 1, kBlk))
+  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, Hq, T, B, 64, kG, kNpos) ||
+      !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, D, Hkv, T, B, 64, 1, kBlk) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, D, Hkv, T, B, 64, 1, kBlk))
     return SWA_ECUDA;
   Params p;
   p.sink = sink;
@@ -332,7 +336,7 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
   p.rep = Hg / Hkv;
   p.nitem_seq = (int)nitem_seq;
   p.total_items = (int)total;
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kD));
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   p.blockmax = blockmax;
   p.nqg = (T + 3) / 4;
   p.nkb = (T + kBlk - 1) / kBlk;
@@ -436,7 +440,7 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const long long grid = units < sms ? units : sms;
-  return launch_dependent("decode_tc_kernel", kern, (unsigned)grid, threads_for(1 << lg), kSmemBytes,
+  return launch_dependent("decode_tc_kernel", kern, (unsigned)grid, threads_for(1 << lg, D), kSmemBytes,
                           st, mk, mv, mq, p);
 }
 
@@ -554,7 +558,7 @@ swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const fl
     case kPathTcSwa:
       return launch_tc_swa(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, bf16_out, st);
     case kPathTcGlobal:
-      return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, bf16_out, st);
+      return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, bf16_out, st);
     case kPathSimt:
       if (bf16_out) {
         set_error_text("bf16 output is available on the tensor-core paths only");
@@ -1068,11 +1072,11 @@ swa_status swa_sink_fwd_scores(const void* q, const void* k, const void* v, cons
       (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(blockmax) & 3u))
     return SWA_EINVAL;
   if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
-  if (!(in_dtype == SWA_BF16 && D == swa::tcglobal::kD && Hq == Hkv * swa::tcglobal::kG)) {
-    set_error_text("block scores come from the tensor-core global kernel (bf16, D 128, 8 heads per kv head)");
+  if (!(in_dtype == SWA_BF16 && Hq == Hkv * swa::tcglobal::kG)) {
+    set_error_text("block scores come from the tensor-core global kernel (bf16, 8 heads per kv head)");
     return SWA_EUNSUPPORTED;
   }
-  return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, W, out_dtype == SWA_BF16,
+  return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, W, out_dtype == SWA_BF16,
                           static_cast<cudaStream_t>(stream), blockmax);
 }
 
@@ -1124,12 +1128,12 @@ swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, cons
     return SWA_EINVAL;
   if (QB != 32 && QB != 64 && QB != 128) return SWA_EUNSUPPORTED;
   if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
-  if (!(in_dtype == SWA_BF16 && D == swa::tcglobal::kD && Hq == Hkv * swa::tcglobal::kG)) {
-    set_error_text("sparse attention runs on the tensor-core global kernel (bf16, D 128, 8 heads per kv head)");
+  if (!(in_dtype == SWA_BF16 && Hq == Hkv * swa::tcglobal::kG)) {
+    set_error_text("sparse attention runs on the tensor-core global kernel (bf16, 8 heads per kv head)");
     return SWA_EUNSUPPORTED;
   }
   // causal over the selected blocks: no window lower bound
-  return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, T, out_dtype == SWA_BF16,
+  return launch_tc_global(q, k, v, sink, out, lse, B, T, Hq, Hkv, D, T, out_dtype == SWA_BF16,
                           static_cast<cudaStream_t>(stream), nullptr, idx, QB, topk);
 }
 

@@ -5,8 +5,8 @@
 // kernel ("MiMo-V2-Flash Technical Report" summary, section 前置知识: the
 // global layers of the hybrid stack attend to the whole causal prefix; every
 // head adds a learnable bias to its softmax denominator), for bf16 inputs,
-// D = 128 and groups of 8 query heads per kv head, any window W (W >= T is the
-// global layer).  Keys are visited in blocks of 128 with an online softmax:
+// D = 64 or 128 and groups of 8 query heads per kv head, any window W (W >= T
+// is the global layer).  Keys are visited in blocks of 128 with an online softmax:
 // the running max starts at the sink logit and the running denominator at
 // exp(sink - max), so the sink is counted exactly once whatever the order.
 //
@@ -24,7 +24,7 @@
 //               every key block j into a ring of 32 KB slots
 //   warp 9      TMEM owner + issuer of S   = Q_i K_j^T  (SS, M = N = K = 128)
 //   warp 10     issuer of                O_i += P_i V_j   (TS, P_i from TMEM,
-//               V MN-major, N = 128)
+//               V MN-major, N = D)
 //   warps 0..3  softmax of tile 0, warps 4..7 softmax of tile 1: thread =
 //               row; S -> mask -> running max / sum -> bf16 P_i in TMEM;
 //               after the last block O / l -> out and the lse.
@@ -36,7 +36,7 @@
 // the other's MMAs; each accumulator still receives its MMAs in order, so the
 // results are unchanged.
 // TMEM: S [0,128) shared by the two tiles, P0 [128,192), P1 [192,256) (bf16
-// pairs), O0 [256,384), O1 [384,512).  S goes to one buffer that each softmax
+// pairs), O0 [256,256+D), O1 [384,384+D).  S goes to one buffer that each softmax
 // empties into registers at once, so an S waits only for the other tile's
 // read of the previous one, and P never shares columns with S.  A softmax
 // rewrites P_i (and rescales O_i) only after the tile's previous PV has
@@ -47,6 +47,11 @@
 // is kept; the final O / l is the same quotient.  When a row's max does move
 // after the item's first block, its warp rescales O_i in TMEM (read,
 // multiply, write) before releasing P_i.
+//
+// D = 64: a q, k or v row is one 128-byte swizzle atom instead of two, so
+// every load copies one half, S takes 4 K-steps instead of 8 and PV has
+// N = 64.  The shared-memory and TMEM layout stays that of D = 128 (the
+// second half of each buffer is unused).
 #pragma once
 
 #include "device_common.cuh"
@@ -57,7 +62,6 @@ namespace tcglobal {
 constexpr int kThreads = 352;
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr int kG = 8;                   // query heads per tile (one kv group)
-constexpr int kD = 128;
 constexpr int kNpos = 16;               // positions per Q tile
 constexpr int kTiles = 2;               // Q tiles per work item
 constexpr int kItemPos = kNpos * kTiles;
@@ -65,7 +69,7 @@ constexpr int kBlk = 128;               // keys per block
 constexpr uint32_t kSlots = 5;          // K/V ring slots (one K or V block each)
 constexpr float kRescaleLog2 = 8.0f;    // move the running max only past this
 
-// shared memory (bytes); swizzled operands 1024-aligned
+// shared memory (bytes), laid out for D = 128; swizzled operands 1024-aligned
 constexpr int kQHalf = 128 * 128;           // 128 rows x 64 bf16
 constexpr int kQTile = 2 * kQHalf;          // 32 KB
 constexpr int kSlotHalf = kBlk * 128;       // 128 keys x 64 bf16
@@ -195,11 +199,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-template <bool kBf16Out, bool kScores>
+template <bool kBf16Out, bool kScores, int kHd>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_global_kernel(const __grid_constant__ CUtensorMap map_q,
                              const __grid_constant__ CUtensorMap map_k,
                              const __grid_constant__ CUtensorMap map_v, const Params p) {
+  static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");
+  constexpr int kHalves = kHd / 64;   // 64-dimension halves of q, k, v rows
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -256,9 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t qdst = sbase + kOffQ + i * kQTile;
           const int pos = it.p0 + i * kNpos;
-          mbar_arrive_expect_tx(bar(kBarQFull + i), kQTile);
+          mbar_arrive_expect_tx(bar(kBarQFull + i), kHalves * kQHalf);
           tma_load_4d(qdst, &map_q, 0, it.grp * kG, pos, it.b, bar(kBarQFull + i));
-          tma_load_4d(qdst + kQHalf, &map_q, 64, it.grp * kG, pos, it.b, bar(kBarQFull + i));
+          if constexpr (kHalves == 2)
+            tma_load_4d(qdst + kQHalf, &map_q, 64, it.grp * kG, pos, it.b, bar(kBarQFull + i));
           ++q_armed[i];
         }
         // The next item's Q tiles and first key blocks go to L2 now, so that
@@ -268,16 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           Item nx;
           if (ok && cta_item(k + 1, p, nx)) {
-            for (int i = 0; i < kTiles; ++i) {
-              tma_prefetch_l2_4d(&map_q, 0, nx.grp * kG, nx.p0 + i * kNpos, nx.b);
-              tma_prefetch_l2_4d(&map_q, 64, nx.grp * kG, nx.p0 + i * kNpos, nx.b);
-            }
+            for (int i = 0; i < kTiles; ++i)
+              for (int hv = 0; hv < kHalves; ++hv)
+                tma_prefetch_l2_4d(&map_q, 64 * hv, nx.grp * kG, nx.p0 + i * kNpos, nx.b);
             for (int t = 0; t < 2 && t < nx.nb; ++t) {
               const int key = item_block(nx, t) * kBlk;
-              tma_prefetch_l2_4d(&map_k, 0, nx.kvh, key, nx.b);
-              tma_prefetch_l2_4d(&map_k, 64, nx.kvh, key, nx.b);
-              tma_prefetch_l2_4d(&map_v, 0, nx.kvh, key, nx.b);
-              tma_prefetch_l2_4d(&map_v, 64, nx.kvh, key, nx.b);
+              for (int hv = 0; hv < kHalves; ++hv) {
+                tma_prefetch_l2_4d(&map_k, 64 * hv, nx.kvh, key, nx.b);
+                tma_prefetch_l2_4d(&map_v, 64 * hv, nx.kvh, key, nx.b);
+              }
             }
           }
         }
@@ -292,9 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int key = item_block(it, t >> 1) * kBlk;
           const uint32_t dst = sbase + kOffKV + slot * kSlotBytes;
           const uint32_t fb = bar(kBarKvFull + slot);
-          mbar_arrive_expect_tx(fb, kSlotBytes);
+          mbar_arrive_expect_tx(fb, kHalves * kSlotHalf);
           tma_load_4d(dst, map, 0, it.kvh, key, it.b, fb);
-          tma_load_4d(dst + kSlotHalf, map, 64, it.kvh, key, it.b, fb);
+          if constexpr (kHalves == 2) tma_load_4d(dst + kSlotHalf, map, 64, it.kvh, key, it.b, fb);
         }
       }
       // Copies still in flight must land before the CTA exits: wait (bounded)
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const bool s_side = (warp == kWarpMma);
       const uint32_t idesc_s = umma_idesc_bf16(kBlk, false, false);
-      const uint32_t idesc_o = umma_idesc_bf16(kD, false, true);
+      const uint32_t idesc_o = umma_idesc_bf16(kHd, false, true);
       const uint64_t qdesc0 = umma_sdesc(sbase + kOffQ, 16, 1024, 2);
       const uint64_t kdesc0 = umma_sdesc(sbase + kOffKV, 16, 1024, 2);
       const uint64_t vdesc0 = umma_sdesc(sbase + kOffKV, kSlotHalf, 1024, 2);
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qd = qdesc0 + (uint32_t)(i * kQTile >> 4);
         const uint64_t kd = kdesc0 + (ks * kSlotBytes >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < kHd / 16; ++kk) {
           const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
           const uint32_t b_off = ((kk >> 2) * kSlotHalf + (kk & 3) * 32) >> 4;
           umma_bf16_ss(tmem + kColS, qd + a_off, kd + b_off, idesc_s, kk > 0);
@@ -506,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // item complete; the item's first block has no O yet.
         if (t > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-          for (int c = 0; c < kD / 32; ++c) {
+          for (int c = 0; c < kHd / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(o_addr + c * 32, o);
             tmem_ld_wait();
@@ -526,9 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       if constexpr (kBf16Out) {
-        const long long e0 = (((long long)it.b * p.T + pos) * p.Hq + h) * kD;
+        const long long e0 = (((long long)it.b * p.T + pos) * p.Hq + h) * kHd;
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
+        for (int c = 0; c < kHd / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(o_addr + c * 32, o);
           tmem_ld_wait();
@@ -550,26 +556,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // holds rows 16 hf + 8 kk + rr of this warp's lanes, i.e. position
         // 4 quad + 2 hf + kk of the tile and head rr, columns 8 j + 2 qd + {0, 1}.
         // A quad then writes whole 32-byte sectors, and one store covers the
-        // 8 heads of a position (4 KB contiguous); each row's 1 / l comes from
+        // 8 heads of a position (8 D floats, contiguous); each row's 1 / l comes from
         // the thread that owns the row (lane 16 hf + 8 kk + rr).
         const int rr = lane >> 2, qd = lane & 3;
         const uint32_t o_warp = tmem + ((uint32_t)(quad * 32) << 16) + col_o(ti);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          uint32_t o[64];
-          tmem_ld_16x256b_x16(o_warp + ((uint32_t)(16 * hf) << 16), o);
+          uint32_t o[kHd / 2];
+          if constexpr (kHd == 128)
+            tmem_ld_16x256b_x16(o_warp + ((uint32_t)(16 * hf) << 16), o);
+          else
+            tmem_ld_16x256b_x8(o_warp + ((uint32_t)(16 * hf) << 16), o);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o[c * 16]));
+          for (int c = 0; c < kHd / 32; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&o[c * 16]));
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             const float il = __shfl_sync(0xffffffffu, inv_l, 16 * hf + 8 * kk + rr);
             const int pos_k = it.p0 + ti * kNpos + 4 * quad + 2 * hf + kk;
             if (pos_k < p.T) {
               float* orow = static_cast<float*>(p.out) +
-                            (((long long)it.b * p.T + pos_k) * p.Hq + it.grp * kG + rr) * kD + 2 * qd;
+                            (((long long)it.b * p.T + pos_k) * p.Hq + it.grp * kG + rr) * kHd + 2 * qd;
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
+              for (int j = 0; j < kHd / 8; ++j)
                 st_global_v2(orow + 8 * j,
                              __float_as_uint(__uint_as_float(o[4 * j + 2 * kk]) * il),
                              __float_as_uint(__uint_as_float(o[4 * j + 2 * kk + 1]) * il));

@@ -272,8 +272,8 @@ swa_status swa_rope_append(const void* q_in, const void* k_in, const void* v_in,
  * each.
  *
  * swa_sink_fwd_scores -- swa_sink_fwd_ex on the tensor-core global kernel
- * (bf16 inputs, D = 128, Hq = 8 Hkv, any W; W >= T is the full-attention
- * layer) that also writes the block scores:
+ * (bf16 inputs, D = 64 or 128, Hq = 8 Hkv, any W; W >= T is the
+ * full-attention layer) that also writes the block scores:
  *   blockmax [B, Hkv, ceil(T/4), ceil(T/128)] float32:
  *     blockmax[b,g,c,n] = max of q_i.k_j / sqrt(D) over query positions
  *     i in [4c, 4c+4), the 8 query heads of kv head g, keys j in
@@ -312,8 +312,8 @@ swa_status swa_topk_blocks(const float* scores, int* idx, int B, int T, int Hkv,
  *   causally on its own).  A repeated index counts its keys twice; an index
  *   past the end gives unspecified values, but every access stays inside
  *   q, k, v, out and lse (the loads are bounded by the tensor maps).
- *   Other arguments as swa_sink_fwd_ex; bf16 inputs, D = 128, Hq = 8 Hkv only
- *   (else SWA_EUNSUPPORTED).
+ *   Other arguments as swa_sink_fwd_ex; bf16 inputs, D = 64 or 128, Hq = 8 Hkv
+ *   only (else SWA_EUNSUPPORTED).
  */
 swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, const float* sink,
                                const int* idx, void* out, float* lse, int B, int T, int Hq,
@@ -323,9 +323,9 @@ swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, cons
 /* Name of the prefill kernel swa_sink_fwd would launch for these sizes, or
  * "invalid": bf16 inputs take "tc_swa" (the sliding-window tensor-core kernel)
  * when W <= 129 and Hq / Hkv is 4 or a multiple of 8 up to 512 (D = 64 or
- * 128), and "tc_global" (the online-softmax tensor-core kernel) when W > 129,
- * D = 128 and Hq / Hkv is a multiple of 8; everything else takes "simt" (CUDA
- * cores, fp32 or bf16 inputs). */
+ * 128), and "tc_global" (the online-softmax tensor-core kernel) when W > 129
+ * and Hq / Hkv is a multiple of 8 (D = 64 or 128); everything else takes
+ * "simt" (CUDA cores, fp32 or bf16 inputs). */
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Name of the decode kernel swa_sink_decode would launch for these sizes

@@ -63,7 +63,7 @@ def test_path_selection(L):
     assert swa.fwd_path(1, 512, 12, 1, 128, 128) == "simt"         # 12: not a multiple of 8
     assert swa.fwd_path(1, 512, 64, 8, 64, 128) == "tc_swa"        # head dimension 64
     assert swa.fwd_path(1, 512, 16, 4, 64, 128) == "tc_swa"
-    assert swa.fwd_path(1, 512, 64, 8, 64, 512) == "simt"          # no global kernel at D 64
+    assert swa.fwd_path(1, 512, 64, 8, 64, 512) == "tc_global"     # D 64 on the global kernel
     assert swa.fwd_path(1, 512, 64, 7, 128, 128) == "invalid"
     assert swa.fwd_path(1, 512, 64, 8, 96, 128) == "invalid"
     assert swa.fwd_path(0, 512, 64, 8, 128, 128) == "invalid"

@@ -47,7 +47,8 @@ def test_decode_tc_group_sizes(cuda_ok, B, Hq, Hkv):
     assert swa.device_error() == 0
 
 
-@pytest.mark.parametrize("B,Hq,Hkv", [(37, 64, 8), (29, 64, 4), (13, 8, 8), (50, 16, 4)])
+@pytest.mark.parametrize("B,Hq,Hkv", [(37, 64, 8), (29, 64, 4), (13, 8, 8), (50, 16, 4), (41, 16, 8),
+                                      (300, 64, 8)])   # 16 or 17 groups per CTA: three warpgroups in turn
 def test_decode_tc_head_dim_64(cuda_ok, B, Hq, Hkv):
     # head dimension 64 on the tensor cores, partial rings with NaN in the empty slots
     assert swa.decode_path(B, Hq, Hkv, 64, 128) == "tc_decode"

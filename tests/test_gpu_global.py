@@ -136,5 +136,21 @@ def test_tc_global_wide_window_sampled(cuda_ok):
     assert_lse_close(l, l_ref)
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", [
+    (1, 700, 8, 1, 700),      # global layer, ragged last item
+    (2, 513, 16, 2, 300),     # window start inside a block, two groups per kv head
+    (1, 1100, 32, 4, 1100),
+])
+def test_tc_global_head_dim_64(cuda_ok, B, T, Hq, Hkv, W):
+    # D = 64: one 128-byte swizzle atom per row, 4 K-steps for S, PV with N = 64
+    assert swa.fwd_path(B, T, Hq, Hkv, 64, W) == "tc_global"
+    x = gen.prefill_inputs(B, T, Hq, Hkv, 64, seed=2300 + T + W)
+    o32, l32 = _full_check(x, W)
+    o16, l16 = swa.swa_sink_fwd(*(t.cuda() for t in (x.q, x.k, x.v, x.sink)), W,
+                                out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(l16, l32)
+
+
 def test_tc_global_no_device_error(cuda_ok):
     assert swa.device_error() == 0

@@ -14,10 +14,11 @@ from gpu_helpers import (assert_bf16_close, assert_lse_close, gather_rows,
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B,T,Hq,Hkv,W", [(1, 300, 8, 1, 300), (2, 1000, 16, 2, 1000),
-                                          (1, 700, 8, 1, 200), (1, 130, 8, 1, 130)])
-def test_block_scores_match_oracle(cuda_ok, B, T, Hq, Hkv, W):
-    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4000 + T + W)
+@pytest.mark.parametrize("B,T,Hq,Hkv,W,D", [(1, 300, 8, 1, 300, 128), (2, 1000, 16, 2, 1000, 128),
+                                            (1, 700, 8, 1, 200, 128), (1, 130, 8, 1, 130, 128),
+                                            (2, 900, 16, 2, 900, 64)])
+def test_block_scores_match_oracle(cuda_ok, B, T, Hq, Hkv, W, D):
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=4000 + T + W)
     q, k, v, s = (t.cuda() for t in (x.q, x.k, x.v, x.sink))
     out, lse, bm = swa.swa_sink_fwd_scores(q, k, v, s, W)
     o2, l2 = swa.swa_sink_fwd(q, k, v, s, W)
@@ -51,10 +52,10 @@ def _selection(B, Hkv, T, QB, topk, seed):
     return oracle.topk_blocks(sc, T, QB, topk)
 
 
-@pytest.mark.parametrize("B,T,Hq,Hkv,QB,topk", [(1, 600, 8, 1, 64, 2), (2, 1000, 16, 2, 32, 3),
-                                                (1, 1500, 8, 1, 128, 4)])
-def test_sparse_matches_oracle(cuda_ok, B, T, Hq, Hkv, QB, topk):
-    x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4100 + T)
+@pytest.mark.parametrize("B,T,Hq,Hkv,QB,topk,D", [(1, 600, 8, 1, 64, 2, 128), (2, 1000, 16, 2, 32, 3, 128),
+                                                  (1, 1500, 8, 1, 128, 4, 128), (2, 1100, 16, 2, 64, 3, 64)])
+def test_sparse_matches_oracle(cuda_ok, B, T, Hq, Hkv, QB, topk, D):
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=4100 + T)
     idx = _selection(B, Hkv, T, QB, topk, seed=T)
     q, k, v, s = (t.cuda() for t in (x.q, x.k, x.v, x.sink))
     out, lse = swa.swa_sink_sparse_fwd(q, k, v, s, torch.from_numpy(idx).cuda(), QB)
