@@ -35,7 +35,7 @@
 // and PV products issued from two threads, one thread's waits are covered by
 // the other's MMAs; each accumulator still receives its MMAs in order, so the
 // results are unchanged.
-// TMEM: S [0,128) shared by the two tiles, P0 [128,192), P1 [192,256) (bf16
+// TMEM (D = 128): S [0,128) shared by the two tiles, P0 [128,192), P1 [192,256) (bf16
 // pairs), O0 [256,256+D), O1 [384,384+D).  S goes to one buffer that each softmax
 // empties into registers at once, so an S waits only for the other tile's
 // read of the previous one, and P never shares columns with S.  A softmax
@@ -50,8 +50,13 @@
 //
 // D = 64: a q, k or v row is one 128-byte swizzle atom instead of two, so
 // every load copies one half, S takes 4 K-steps instead of 8 and PV has
-// N = 64.  The shared-memory and TMEM layout stays that of D = 128 (the
-// second half of each buffer is unused).
+// N = 64.  The shared-memory layout stays that of D = 128 (the second half of
+// each buffer is unused).  With O at 64 columns per tile, TMEM has room for
+// one S buffer per tile: S0 [0,128), S1 [128,256), P0 [256,320), P1
+// [320,384), O0 [384,448), O1 [448,512).  An S then waits only for its own
+// tile's softmax to read the previous one; with half the MMA work per block
+// for the same softmax, the chain through the shared buffer (S0, read, S1,
+// read, ...) would set the pace.
 #pragma once
 
 #include "device_common.cuh"
@@ -79,7 +84,7 @@ constexpr int kOffKV = kOffQ + kTiles * kQTile;
 constexpr int kOffBar = kOffKV + (int)kSlots * kSlotBytes;
 constexpr int kBarQFull = 0, kBarQEmpty = kBarQFull + kTiles, kBarKvFull = kBarQEmpty + kTiles,
               kBarKvEmpty = kBarKvFull + kSlots, kBarSFull = kBarKvEmpty + kSlots,
-              kBarSFree = kBarSFull + kTiles, kBarPFull = kBarSFree + 1,
+              kBarSFree = kBarSFull + kTiles, kBarPFull = kBarSFree + kTiles,
               kBarPvDone = kBarPFull + kTiles, kBarOFull = kBarPvDone + kTiles,
               kBarDrain = kBarOFull + kTiles, kNumBars = kBarDrain + 2;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -87,10 +92,21 @@ constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;  // + slack for 1024 alignment
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;
-// TMEM column of P_i and of O_i
-__host__ __device__ constexpr uint32_t col_p(int i) { return 128u + 64u * (uint32_t)i; }
-__host__ __device__ constexpr uint32_t col_o(int i) { return 256u + 128u * (uint32_t)i; }
+// TMEM columns of S_i, P_i and O_i: at D = 128 one S buffer shared by the two
+// tiles, at D = 64 one per tile (kSplitS)
+template <int kHd>
+struct Cols {
+  static constexpr bool kSplitS = kHd == 64;
+  __host__ __device__ static constexpr uint32_t s(int i) { return kSplitS ? 128u * (uint32_t)i : 0u; }
+  __host__ __device__ static constexpr uint32_t p(int i) {
+    return (kSplitS ? 256u : 128u) + 64u * (uint32_t)i;
+  }
+  __host__ __device__ static constexpr uint32_t o(int i) {
+    return kSplitS ? 384u + 64u * (uint32_t)i : 256u + 128u * (uint32_t)i;
+  }
+};
+static_assert(Cols<64>::o(1) + 64 <= kTmemCols && Cols<128>::o(1) + 128 <= kTmemCols,
+              "TMEM layout fits the allocation");
 
 struct Params {
   const float* sink;
@@ -206,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap map_v, const Params p) {
   static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");
   constexpr int kHalves = kHd / 64;   // 64-dimension halves of q, k, v rows
+  using C = Cols<kHd>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -224,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPvDone + i), 1);
       mbar_init(bar(kBarOFull + i), 1);
     }
-    mbar_init(bar(kBarSFree), 128);
+    for (int i = 0; i < kTiles; ++i) mbar_init(bar(kBarSFree + i), 128);
     for (uint32_t s = 0; s < kSlots; ++s) {
       mbar_init(bar(kBarKvFull + s), 1);
       mbar_init(bar(kBarKvEmpty + s), 1);
@@ -326,16 +343,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vdesc0 = umma_sdesc(sbase + kOffKV, kSlotHalf, 1024, 2);
       uint32_t gblk = 0;      // key blocks consumed so far (all items)
       uint32_t ns = 0;        // S products issued (S0 and S1 alternate)
+      uint32_t ns_t[kTiles] = {};   // per tile
       bool ok = true;
       // K of block g is ring load 2g, V of block g is load 2g + 1
       auto wait_load = [&](uint32_t seq, uint32_t& slot) -> bool {
         slot = seq % kSlots;
         return mbar_wait(bar(kBarKvFull + slot), (seq / kSlots) & 1, kErrWaitKvFull, abort_flag);
       };
-      // S = Q_i K^T into the shared buffer, once the other tile's softmax has
-      // read the previous S out of it
+      // S = Q_i K^T once the softmax that read the buffer's previous S (the
+      // other tile's with one shared buffer, this tile's with one per tile)
+      // has emptied it
       auto issue_s = [&](int i, uint32_t ks) -> bool {
-        if (ns > 0 && !mbar_wait(bar(kBarSFree), (ns - 1) & 1, kErrWaitSFree, abort_flag))
+        const uint32_t used = C::kSplitS ? ns_t[i] : ns;
+        if (used > 0 && !mbar_wait(bar(kBarSFree + (C::kSplitS ? i : 0)), (used - 1) & 1,
+                                   kErrWaitSFree, abort_flag))
           return false;
         tc_fence_after();
         const uint64_t qd = qdesc0 + (uint32_t)(i * kQTile >> 4);
@@ -344,10 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kHd / 16; ++kk) {
           const uint32_t a_off = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
           const uint32_t b_off = ((kk >> 2) * kSlotHalf + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + kColS, qd + a_off, kd + b_off, idesc_s, kk > 0);
+          umma_bf16_ss(tmem + C::s(i), qd + a_off, kd + b_off, idesc_s, kk > 0);
         }
         umma_commit(bar(kBarSFull + i));
         ++ns;
+        ++ns_t[i];
         return true;
       };
       // O_i += P_i V for block number blk
@@ -357,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t vd = vdesc0 + (vs * kSlotBytes >> 4);
 #pragma unroll
         for (int kb = 0; kb < kBlk / 16; ++kb)
-          umma_bf16_ts(tmem + col_o(i), tmem + col_p(i) + kb * 8,
+          umma_bf16_ts(tmem + C::o(i), tmem + C::p(i) + kb * 8,
                        vd + (uint32_t)(kb * 16 * 128 >> 4), idesc_o, (!first || kb > 0));
         umma_commit(bar(kBarPvDone + i));
         if (last) umma_commit(bar(kBarOFull + i));
@@ -404,9 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;                      // TMEM lanes [32 quad, 32 quad + 32)
     const int r = quad * 32 + lane;                 // tile row
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    const uint32_t s_addr = tmem + lane_addr + kColS;
-    const uint32_t p_addr = tmem + lane_addr + col_p(ti);
-    const uint32_t o_addr = tmem + lane_addr + col_o(ti);
+    const uint32_t s_addr = tmem + lane_addr + C::s(ti);
+    const uint32_t p_addr = tmem + lane_addr + C::p(ti);
+    const uint32_t o_addr = tmem + lane_addr + C::o(ti);
     const int g = r & 7;
     uint32_t npv = 0;
     Item it;
@@ -434,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < kBlk / 32; ++c) reg_fence32(sr + c * 32);
-        // S is in registers: the other tile's S may overwrite the buffer
+        // S is in registers: the next S may overwrite the buffer
         tc_fence_before();
-        mbar_arrive(bar(kBarSFree));
+        mbar_arrive(bar(kBarSFree + (C::kSplitS ? ti : 0)));
         // P_i and O_i are free once the tile's previous PV has completed (in
         // this order it ran before the S just read, so the wait is short)
         if (npv > 0 &&
@@ -559,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 8 heads of a position (8 D floats, contiguous); each row's 1 / l comes from
         // the thread that owns the row (lane 16 hf + 8 kk + rr).
         const int rr = lane >> 2, qd = lane & 3;
-        const uint32_t o_warp = tmem + ((uint32_t)(quad * 32) << 16) + col_o(ti);
+        const uint32_t o_warp = tmem + ((uint32_t)(quad * 32) << 16) + C::o(ti);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t o[kHd / 2];
