@@ -97,14 +97,12 @@ swa_status swa_sink_fwd_ex(const void* q, const void* k, const void* v, const fl
  * copies of the neighbouring chunks run at the same time (host-to-device on
  * one stream, the prefill on `stream`, device-to-host on another; each
  * chunk's steps are chained by events).  On the sliding-window tensor-core
- * path (swa_sink_fwd_path "tc_swa") a chunk is one
- * sequence x a range of positions (about 16 chunks in all, at least 512
- * positions each, and a piece of 512 positions split off the first and the
- * last, whose copies overlap nothing), staged at its own place in the device
- * buffers, so that
- * every copy is one contiguous range; the prefill of a chunk computes its
- * positions only, reading the window's earlier keys copied with the chunks
- * before it.  On the other paths a chunk is one sequence x a share of the kv
+ * path (swa_sink_fwd_path "tc_swa") a chunk is one sequence x a range of
+ * positions (about 16 chunks in all, at least 512 positions each, and a piece
+ * of 512 positions split off the first and the last, whose copies overlap
+ * nothing), staged at its own place in the device buffers, so that every copy
+ * is one contiguous range; the prefill of a chunk computes its positions
+ * only, reading the window's earlier keys copied with the chunks before it.  On the other paths a chunk is one sequence x a share of the kv
  * heads (half of them when Hkv is even; the whole batch as one chunk when a
  * share would break the 16-byte alignment of the staging).  The results are
  * those of swa_sink_fwd_ex on the whole batch, bit for bit.

@@ -21,6 +21,10 @@ def test_graph_replay_equals_eager(cuda_ok):
     x4 = gen.prefill_inputs(1, 500, 16, 4, 128, seed=85, device=dev)
     x16 = gen.prefill_inputs(1, 500, 64, 4, 128, seed=86, device=dev)
     v8 = gen.verify_inputs(24, 8, 64, 8, 128, 128, seed=87, device=dev)
+    # head dimension 64: prefill, global layer, decode and verify
+    x64 = gen.prefill_inputs(1, 600, 16, 2, 64, seed=88, device=dev)
+    d64 = gen.decode_inputs(40, 64, 8, 64, 128, seed=89, device=dev)
+    v64 = gen.verify_inputs(20, 4, 64, 8, 64, 128, seed=90, device=dev)
     outs = {}
 
     def calls():
@@ -36,6 +40,12 @@ def test_graph_replay_equals_eager(cuda_ok):
         outs["glb16"] = swa.swa_sink_fwd(x16.q, x16.k, x16.v, x16.sink, 500, stream=st)
         outs["ver8"] = swa.swa_sink_verify(v8.q, v8.k_new, v8.v_new, v8.k_ring, v8.v_ring, v8.pos,
                                            v8.sink, stream=st)
+        outs["swa64"] = swa.swa_sink_fwd(x64.q, x64.k, x64.v, x64.sink, 128, stream=st)
+        outs["glb64"] = swa.swa_sink_fwd(x64.q, x64.k, x64.v, x64.sink, 600, stream=st)
+        outs["dec64"] = swa.swa_sink_decode(d64.q, d64.k_ring, d64.v_ring, d64.pos, d64.sink,
+                                            stream=st)
+        outs["ver64"] = swa.swa_sink_verify(v64.q, v64.k_new, v64.v_new, v64.k_ring, v64.v_ring,
+                                            v64.pos, v64.sink, stream=st)
 
     with torch.cuda.stream(st):
         calls()
