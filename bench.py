@@ -330,10 +330,17 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
+def traffic_shape(**dims) -> str:
+    """The key a traffic record is stored under: the workload's sizes, e.g.
+    "B4 T8192 Hq64 Hkv8 D128 W128"."""
+    return " ".join(f"{k}{v}" for k, v in dims.items())
+
+
+def recorded_traffic(kernel: str, shape: str):
     """DRAM bytes (read + write) per launch of the bench workload, from the
-    committed ncu summary ``profiles/dram_traffic.txt``; None if absent or if
-    the kernel's sources have changed since the counters were taken."""
+    committed ncu summary ``profiles/dram_traffic.txt``; None if absent, if the
+    record was taken on another workload shape, or if the kernel's sources
+    have changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
@@ -346,6 +353,8 @@ def recorded_traffic(kernel: str):
             key, val = line.split(":", 1)
             rec[key.strip()] = val.strip()
     if rec.get(f"{kernel}.source_hash") != kernel_source_hash(kernel):
+        return None
+    if rec.get(f"{kernel}.shape") != shape:
         return None
     val = rec.get(f"{kernel}.bytes_per_launch")
     return int(float(val)) if val else None
@@ -498,7 +507,9 @@ def decode_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None):
         "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                     "bytes_per_launch": nbytes, "traffic": recorded_traffic(kernel)},
+                     "bytes_per_launch": nbytes,
+                     "traffic": recorded_traffic(kernel, traffic_shape(B=B, Hq=Hq, Hkv=Hkv, D=D,
+                                                                       W=W))},
         "clocks": clocks,
     }
     if cpu:
@@ -535,7 +546,9 @@ def verify_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None):
         "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                     "bytes_per_launch": nbytes, "traffic": recorded_traffic(kernel)},
+                     "bytes_per_launch": nbytes,
+                     "traffic": recorded_traffic(kernel, traffic_shape(B=B, L=L, Hq=Hq, Hkv=Hkv,
+                                                                       D=D, W=W))},
         "clocks": clocks,
     }
     if cpu:
@@ -610,7 +623,8 @@ def hybrid_line(swa, dev, stream, reps, peaks, cpu, n_swa=None, cpu_rates=None):
             # cap: its fraction of the sustained GEMM rate, for context
             "frac_of_sustained": round(ga_tf / float(peaks["bf16_tflops_sustained"]), 4),
             "flops_per_launch": ga_fl,
-            "traffic": recorded_traffic("swa_fwd_tc_global_kernel")}
+            "traffic": recorded_traffic("swa_fwd_tc_global_kernel",
+                                        traffic_shape(B=1, T=T, Hq=Hq, Hkv=c["Hkv"], D=D, W=T))}
     if clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
         # time x clock: the layer's rate had it run at the maximum SM clock
         # throughout (the median clock of the line's timed region stands in
@@ -983,15 +997,16 @@ KERNEL_OF_PATH = {"tc_swa": "swa_fwd_tc_kernel", "tc_global": "swa_fwd_tc_global
                   "simt": "simt_fwd_kernel"}
 
 
-def prefill_roofline(kpath, flops, nbytes, launch_ms, peaks, peak_src):
+def prefill_roofline(kpath, flops, nbytes, launch_ms, peaks, peak_src, shape=""):
     """Roofline of the prefill kernel: HBM-bound for the sliding window (fp32
-    output dominates the bytes), tensor-bound for the global layer."""
+    output dominates the bytes), tensor-bound for the global layer.  shape:
+    the workload's sizes (traffic_shape), which select the traffic record."""
     kernel = KERNEL_OF_PATH.get(kpath, kpath)
     gbs = nbytes / (launch_ms * 1e-3) / 1e9
     tfs = flops / (launch_ms * 1e-3) / 1e12
     common = {"kernel": kernel, "launch_ms": round(launch_ms, 4),
               "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
-              "traffic": recorded_traffic(kernel)}
+              "traffic": recorded_traffic(kernel, shape)}
     if kpath == "tc_global":
         peak = float(peaks["bf16_tflops"])
         return dict({"bound": "tensor", "achieved": round(tfs, 1), "peak": peak,
@@ -1036,7 +1051,9 @@ def run_ours(args, dist):
         "config": {"workload": workload_name(c), "seed": 0,
                    "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB moved per step)",
                    "parallelism": f"replicas x{dist.world}"},
-        "roofline": prefill_roofline(kpath, flops, nbytes, launch_ms, peaks, peak_src),
+        "roofline": prefill_roofline(kpath, flops, nbytes, launch_ms, peaks, peak_src,
+                                     traffic_shape(**{k: c[k] for k in ("B", "T", "Hq", "Hkv",
+                                                                         "D", "W")})),
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }

@@ -76,3 +76,15 @@ def test_clock_sampler_with_a_fake_nvml():
     assert d["source"] == "nvml" and d["samples"] >= 5
     assert 1900 <= d["sm_mhz"] <= 1902 and d["sm_max_mhz"] == 2032
     assert d["reasons"] == ["sw_power_cap"]
+
+
+def test_traffic_record_applies_to_its_own_workload_only():
+    # the committed record is per kernel and workload shape: another shape of
+    # the same kernel gets no traffic figure
+    shape = bench.traffic_shape(B=256, Hq=64, Hkv=8, D=128, W=128)
+    assert shape == "B256 Hq64 Hkv8 D128 W128"
+    assert bench.recorded_traffic("decode_tc_kernel", shape) is not None
+    assert bench.recorded_traffic("decode_tc_kernel",
+                                  bench.traffic_shape(B=256, Hq=32, Hkv=8, D=128, W=128)) is None
+    assert bench.recorded_traffic("swa_fwd_tc_kernel",
+                                  bench.traffic_shape(B=4, T=8192, Hq=64, Hkv=8, D=64, W=128)) is None
