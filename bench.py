@@ -1108,12 +1108,18 @@ def run_reference(args, dist):
     if dist.rank != 0:
         return None
     c = PREFILL
-    # same recipe as the GPU arm's workload, first 2048 positions of one sequence
-    x = gen.prefill_inputs(1, 2048, c["Hq"], c["Hkv"], c["D"], seed=0)
+    # same recipe as the GPU arm's workload: one of its sequences
+    x = gen.prefill_inputs(1, c["T"], c["Hq"], c["Hkv"], c["D"], seed=0)
     import oracle
     oracle.build()
     nthr = oracle.num_threads()
-    ts, i0 = 24, 1024  # full-window rows per step: about a second of host work
+    # full-window rows per step, sized from a first timed sample so that the
+    # whole run (warm-up and timed steps) takes about 90 s of host work, at
+    # most 2 s a step
+    i0 = c["W"]
+    dt0, _, _ = oracle_rows_rate(x.q, x.k, x.v, x.sink, c["W"], i0, 64)
+    target = min(2.0, max(0.02, 90.0 / max(1, args.steps + args.warmup)))
+    ts = max(16, min(c["T"] - i0, int(target * 64 / max(dt0, 1e-6))))
     for s in range(args.warmup):
         oracle_rows_rate(x.q, x.k, x.v, x.sink, c["W"], i0, ts)
     tot, flops = 0.0, 0
