@@ -371,7 +371,7 @@ swa_status launch_decode_t(const void* q, const void* kr, const void* vr, const 
   return check_launch("decode_kernel");
 }
 
-// Tensor-core decode: bf16, D = 128, W = 128, groups of G = 1, 2, 4, 8 or 16
+// Tensor-core decode: bf16, D = 64 or 128, W = 128, groups of G = 1, 2, 4, 8 or 16
 // query heads per kv head.
 int log2_group(int Hq, int Hkv) {
   if (Hkv < 1 || Hq % Hkv) return -1;

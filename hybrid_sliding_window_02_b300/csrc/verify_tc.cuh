@@ -3,7 +3,7 @@
 //
 // Operation: as in verify.cuh (drafted tokens at positions pos .. pos+L-1
 // checked in one pass; "MiMo-V2-Flash Technical Report" summary, section
-// 核心方法), for bf16 inputs, D = 128, W = 128, groups of 8 query heads and
+// 核心方法), for bf16 inputs, D = 64 or 128, W = 128, groups of 8 query heads and
 // L <= 8 drafted tokens.  Per group (sequence b, kv head g) the 8L query rows
 // r = 8 j + h (token j, head h) sit in the first lanes of a 128-row tile:
 //   S = Q K_ring^T             tcgen05 SS, M = 128 rows, N = 128 slots, K = 128
