@@ -194,10 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // store below waits for that kernel to complete.
   if (warp == kWarpProducer && lane == 0 && nk > 0) {
     const int u0 = (int)blockIdx.x;
-    tma_prefetch_l2_4d(&map_k, 0, u0 * kW, 0, 0);
-    tma_prefetch_l2_4d(&map_k, 64, u0 * kW, 0, 0);
-    tma_prefetch_l2_4d(&map_v, 0, u0 * kW, 0, 0);
-    tma_prefetch_l2_4d(&map_v, 64, u0 * kW, 0, 0);
+    for (int hv = 0; hv < kHalves; ++hv) {
+      tma_prefetch_l2_4d(&map_k, 64 * hv, u0 * kW, 0, 0);
+      tma_prefetch_l2_4d(&map_v, 64 * hv, u0 * kW, 0, 0);
+    }
   }
   if (tid == 0) grid_dep_launch();
   grid_dep_wait();
