@@ -33,6 +33,7 @@ def _device_call(x, W, out_dtype=torch.float32):
     (1, 5000, 16, 4, 128, 128),   # 4 heads per kv head: position chunks of whole 32-position tiles
     (2, 1500, 64, 4, 128, 128),   # 16 heads per kv head (two groups of 8)
     (2, 2600, 64, 8, 64, 128),    # head dimension 64
+    (2, 900, 32, 4, 64, 900),     # head dimension 64, global layer: half the kv heads per chunk
 ])
 def test_host_call_equals_device_call(cuda_ok, pinned, B, T, Hq, Hkv, D, W):
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=B + T)
