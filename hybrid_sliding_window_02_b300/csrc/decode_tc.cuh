@@ -2,10 +2,10 @@
 // per-group contractions on the 5th-generation tensor cores.
 //
 // Operation: for each sequence b and kv head g, the G query heads of the
-// group (G = 1, 2, 4, 8 or 16) attend to the W = 128 ring slots of (b, g) with
-// the sink-biased
-// softmax ("MiMo-V2-Flash Technical Report" summary, section 前置知识; the
-// fixed-size O(W) sliding-window cache of the "pwwt.cn" essay, section 1.1).
+// group (G = 1, 2, 4, 8 or 16; larger multiples of 8 as groups of 8) attend
+// to the W = 128 ring slots of (b, g) with the sink-biased softmax
+// ("MiMo-V2-Flash Technical Report" summary, section 前置知识; the fixed-size
+// O(W) sliding-window cache of the "pwwt.cn" essay, section 1.1).
 // Slot s holds position pos - ((pos - s) mod W); while pos < W - 1 the slots
 // s > pos are empty and are ignored whatever they hold.
 //
@@ -84,8 +84,29 @@ struct Params {
   float* out;
   float* lse;
   int B, Hq, Hkv;
-  int units;          // B * Hkv
+  int rep;            // query groups of kG heads per kv head (G / 8 for G = 24, 32, ...; else 1)
+  int units;          // B * Hkv * rep
   float scale_log2;   // log2(e) / sqrt(D)
+};
+
+// Group u of the call: ring unit ur = (sequence b, kv head g), and the query
+// heads [gq kG, gq kG + kG) it serves.  With G = 8 R (R > 2) the 8-head
+// instance runs R sibling groups per kv head, each reading the kv head's
+// rings; the siblings are consecutive, so neighbouring CTAs take them in the
+// same round and the later reads come from L2.
+struct GroupCoords {
+  int ur, b, g, gq;
+  __device__ __forceinline__ GroupCoords(int u, const Params& p) {
+    ur = u;
+    int sib = 0;
+    if (p.rep != 1) {
+      ur = u / p.rep;
+      sib = u - ur * p.rep;
+    }
+    b = ur / p.Hkv;
+    g = ur - b * p.Hkv;
+    gq = g * p.rep + sib;
+  }
 };
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
@@ -208,7 +229,7 @@ __global__ void __launch_bounds__(threads_for(kG, kHd), 1)
   // the CTA) may overlap the previous kernel on the stream; every load and
   // store below waits for that kernel to complete.
   if (warp == kWarpProducer && lane == 0 && nk > 0) {
-    const int u0 = (int)blockIdx.x;
+    const int u0 = GroupCoords((int)blockIdx.x, p).ur;   // ring of this CTA's first group
     for (int hv = 0; hv < kHalves; ++hv) {
       tma_prefetch_l2_4d(&map_k, 64 * hv, u0 * kW, 0, 0);
       tma_prefetch_l2_4d(&map_v, 64 * hv, u0 * kW, 0, 0);
@@ -222,8 +243,7 @@ __global__ void __launch_bounds__(threads_for(kG, kHd), 1)
     if (lane == 0) {
       int nkld = 0, nvld = 0;  // K / V slot loads issued
       for (int k = 0; k < nk; ++k) {
-        const int u = (int)blockIdx.x + k * (int)gridDim.x;
-        const int b = u / p.Hkv, g = u - b * p.Hkv;
+        const GroupCoords gc((int)blockIdx.x + k * (int)gridDim.x, p);
         const uint32_t ks = (uint32_t)k % kKSlots;
         if (!mbar_wait(bar(kBarKEmpty + ks), (((uint32_t)k / kKSlots) & 1) ^ 1, kErrWaitKvEmpty,
                        abort_flag))
@@ -231,11 +251,11 @@ __global__ void __launch_bounds__(threads_for(kG, kHd), 1)
         const uint32_t kst = sbase + kOffK + ks * kKSlotBytes;
         const uint32_t kb = bar(kBarKFull + ks);
         mbar_arrive_expect_tx(kb, kHalves * (kHalf + kQHalf));
-        tma_load_4d(kst + kKK, &map_k, 0, u * kW, 0, 0, kb);
-        tma_load_4d(kst + kKQ, &map_q, 0, b * p.Hq + g * kG, 0, 0, kb);
+        tma_load_4d(kst + kKK, &map_k, 0, gc.ur * kW, 0, 0, kb);
+        tma_load_4d(kst + kKQ, &map_q, 0, gc.b * p.Hq + gc.gq * kG, 0, 0, kb);
         if constexpr (kHalves == 2) {
-          tma_load_4d(kst + kKK + kHalf, &map_k, 64, u * kW, 0, 0, kb);
-          tma_load_4d(kst + kKQ + kQHalf, &map_q, 64, b * p.Hq + g * kG, 0, 0, kb);
+          tma_load_4d(kst + kKK + kHalf, &map_k, 64, gc.ur * kW, 0, 0, kb);
+          tma_load_4d(kst + kKQ + kQHalf, &map_q, 64, gc.b * p.Hq + gc.gq * kG, 0, 0, kb);
         }
         ++nkld;
         const uint32_t vs = (uint32_t)k % kVSlots;
@@ -245,8 +265,8 @@ __global__ void __launch_bounds__(threads_for(kG, kHd), 1)
         const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
         const uint32_t vb = bar(kBarVFull + vs);
         mbar_arrive_expect_tx(vb, kHalves * kHalf);
-        tma_load_4d(vst, &map_v, 0, u * kW, 0, 0, vb);
-        if constexpr (kHalves == 2) tma_load_4d(vst + kHalf, &map_v, 64, u * kW, 0, 0, vb);
+        tma_load_4d(vst, &map_v, 0, gc.ur * kW, 0, 0, vb);
+        if constexpr (kHalves == 2) tma_load_4d(vst + kHalf, &map_v, 64, gc.ur * kW, 0, 0, vb);
         ++nvld;
       }
       if (nvld < nk) {  // stopped early: let the copies already issued land
@@ -346,8 +366,8 @@ __global__ void __launch_bounds__(threads_for(kG, kHd), 1)
     const uint32_t bar_max = bar(kBarRed + 2 * w), bar_sum = bar(kBarRed + 2 * w + 1);
     for (int k = w; k < nk; k += kNWG) {
       const uint32_t ph = (uint32_t)(k / kNWG) & 1;   // phase of this warpgroup's barriers
-      const int u = (int)blockIdx.x + k * (int)gridDim.x;
-      const int b = u / p.Hkv, g = u - b * p.Hkv;
+      const GroupCoords gc((int)blockIdx.x + k * (int)gridDim.x, p);
+      const int b = gc.b, g = gc.gq;   // g: the query group (heads g kG ..)
       const uint32_t vs = (uint32_t)k % kVSlots;
       const int64_t pnow = p.pos[b];
       const bool full_ring = pnow >= kW - 1;

@@ -166,8 +166,8 @@ enum FwdPath { kPathInvalid, kPathSimt, kPathTcSwa, kPathTcGlobal };
 constexpr int kVerifyMaxL = 64;  // drafted tokens per verify call
 
 bool verify_tc_applies(int L, int Hq, int Hkv, int D, int W, swa_dtype dt) {
-  return dt == SWA_BF16 && (D == 128 || D == 64) && W == swa::vertc::kW &&
-         Hq == Hkv * swa::vertc::kG && L >= 1 && L <= swa::vertc::kLmax;
+  return dt == SWA_BF16 && (D == 128 || D == 64) && W == swa::vertc::kW && Hkv >= 1 &&
+         Hq % (Hkv * swa::vertc::kG) == 0 && L >= 1 && L <= swa::vertc::kLmax;
 }
 
 // Query heads per sliding-window tile: 4 when G = 4, else 8 (a kv head's G =
@@ -371,17 +371,24 @@ swa_status launch_decode_t(const void* q, const void* kr, const void* vr, const 
   return check_launch("decode_kernel");
 }
 
-// Tensor-core decode: bf16, D = 64 or 128, W = 128, groups of G = 1, 2, 4, 8 or 16
-// query heads per kv head.
-int log2_group(int Hq, int Hkv) {
+// Tensor-core decode: bf16, D = 64 or 128, W = 128, G = 1, 2, 4, 8 or 16 query
+// heads per kv head, or a larger multiple of 8 (R = G / 8 sibling groups of 8
+// per kv head on the 8-head instance).  Returns log2 of the instance's heads
+// per group and sets *rep = R (1 otherwise); -1 for other G.
+int log2_group(int Hq, int Hkv, int* rep = nullptr) {
+  if (rep) *rep = 1;
   if (Hkv < 1 || Hq % Hkv) return -1;
-  switch (Hq / Hkv) {
+  const int G = Hq / Hkv;
+  switch (G) {
     case 1: return 0;
     case 2: return 1;
     case 4: return 2;
     case 8: return 3;
     case 16: return 4;
-    default: return -1;
+    default:
+      if (G % 8 != 0) return -1;
+      if (rep) *rep = G / 8;
+      return 3;
   }
 }
 
@@ -396,7 +403,8 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   using namespace swa::dectc;
   int sms;
   if (!device_sms(dev, &sms)) return SWA_ECUDA;
-  const int lg = log2_group(Hq, Hkv);
+  int rep = 1;
+  const int lg = log2_group(Hq, Hkv, &rep);
   const bool d64 = D == 64;
   void (*const kernels[5][2])(CUtensorMap, CUtensorMap, CUtensorMap, Params) = {
       {decode_tc_kernel<1, 128>, decode_tc_kernel<1, 64>},
@@ -418,14 +426,15 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
       g_dev[dev].dectc_attr[lg][d64] = true;
     }
   }
-  const long long units = (long long)B * Hkv;
-  if (units * kW >= (1LL << 31) || (long long)B * Hq >= (1LL << 31)) {
+  const long long rings = (long long)B * Hkv;          // ring units (sequence, kv head)
+  const long long units = rings * rep;                 // groups of the instance's heads
+  if (rings * kW >= (1LL << 31) || units >= (1LL << 31) || (long long)B * Hq >= (1LL << 31)) {
     set_error_text("problem too large for the tensor-core decode kernel");
     return SWA_EUNSUPPORTED;
   }
   CUtensorMap mk, mv, mq;
-  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, D, units * kW, 1, 1, 64, kW, 1) ||
-      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, D, units * kW, 1, 1, 64, kW, 1) ||
+  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, D, rings * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, D, rings * kW, 1, 1, 64, kW, 1) ||
       !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, (uint64_t)B * Hq, 1, 1, 64, kN,
                    1))
     return SWA_ECUDA;
@@ -437,6 +446,7 @@ swa_status launch_decode_tc(const void* q, const void* kr, const void* vr, const
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
+  p.rep = rep;
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const long long grid = units < sms ? units : sms;
@@ -469,14 +479,16 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
       g_dev[dev].vertc_attr[rows64][d64] = true;
     }
   }
-  const long long units = (long long)B * Hkv;
-  if (units * kW >= (1LL << 31)) {
+  const int rep = Hq / (Hkv * kG);                     // groups of 8 query heads per kv head
+  const long long rings = (long long)B * Hkv;          // ring units (sequence, kv head)
+  const long long units = rings * rep;
+  if (rings * kW >= (1LL << 31) || units >= (1LL << 31)) {
     set_error_text("problem too large for the tensor-core verify kernel");
     return SWA_EUNSUPPORTED;
   }
   CUtensorMap mk, mv, mq, mkn, mvn;
-  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, D, units * kW, 1, 1, 64, kW, 1) ||
-      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, D, units * kW, 1, 1, 64, kW, 1) ||
+  if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, D, rings * kW, 1, 1, 64, kW, 1) ||
+      !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, D, rings * kW, 1, 1, 64, kW, 1) ||
       !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, Hq, L, B, 64, kG, L) ||
       !make_map_4d(&mkn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kn, D, Hkv, L, B, 64, 1, L) ||
       !make_map_4d(&mvn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vn, D, Hkv, L, B, 64, 1, L))
@@ -490,6 +502,7 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
   p.L = L;
   p.Hq = Hq;
   p.Hkv = Hkv;
+  p.rep = rep;
   p.units = (int)units;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const long long grid = units < sms ? units : sms;

@@ -3,8 +3,9 @@
 //
 // Operation: as in verify.cuh (drafted tokens at positions pos .. pos+L-1
 // checked in one pass; "MiMo-V2-Flash Technical Report" summary, section
-// 核心方法), for bf16 inputs, D = 64 or 128, W = 128, groups of 8 query heads and
-// L <= 8 drafted tokens.  Per group (sequence b, kv head g) the 8L query rows
+// 核心方法), for bf16 inputs, D = 64 or 128, W = 128, 8 query heads per kv
+// head (or a multiple of 8, as sibling groups of 8) and L <= 8 drafted
+// tokens.  Per group (sequence b, kv head g) the 8L query rows
 // r = 8 j + h (token j, head h) sit in the first lanes of a 128-row tile:
 //   S = Q K_ring^T             tcgen05 SS, M = 128 rows, N = 128 slots, K = 128
 //   S_new = Q K_new^T          tcgen05 SS, N = 16 (the L <= 8 drafted keys;
@@ -104,8 +105,29 @@ struct Params {
   float* out;
   float* lse;
   int B, L, Hq, Hkv;
-  int units;          // B * Hkv
+  int rep;            // groups of 8 query heads per kv head (G / 8)
+  int units;          // B * Hkv * rep
   float scale_log2;
+};
+
+// Group u of the call: ring unit ur = (sequence b, kv head g), and the query
+// heads [gq kG, gq kG + kG) it serves.  With G = 8 R the R sibling groups of
+// a kv head each read its rings and drafted keys and values; the siblings
+// are consecutive, so neighbouring CTAs take them in the same round and the
+// later reads come from L2.
+struct GroupCoords {
+  int ur, b, g, gq;
+  __device__ __forceinline__ GroupCoords(int u, const Params& p) {
+    ur = u;
+    int sib = 0;
+    if (p.rep != 1) {
+      ur = u / p.rep;
+      sib = u - ur * p.rep;
+    }
+    b = ur / p.Hkv;
+    g = ur - b * p.Hkv;
+    gq = g * p.rep + sib;
+  }
 };
 
 // kRows query rows per group (32 or 64), head dimension kHd (64 or 128: with
@@ -193,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the CTA) may overlap the previous kernel on the stream; every load and
   // store below waits for that kernel to complete.
   if (warp == kWarpProducer && lane == 0 && nk > 0) {
-    const int u0 = (int)blockIdx.x;
+    const int u0 = GroupCoords((int)blockIdx.x, p).ur;   // ring of this CTA's first group
     for (int hv = 0; hv < kHalves; ++hv) {
       tma_prefetch_l2_4d(&map_k, 64 * hv, u0 * kW, 0, 0);
       tma_prefetch_l2_4d(&map_v, 64 * hv, u0 * kW, 0, 0);
@@ -209,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t vbytes = kHalves * (kHalf + L * 128);
       int nkld = 0, nvld = 0;  // K / V slot loads issued
       for (int k = 0; k < nk; ++k) {
-        const int u = (int)blockIdx.x + k * (int)gridDim.x;
-        const int b = u / p.Hkv, g = u - b * p.Hkv;
+        const GroupCoords gc((int)blockIdx.x + k * (int)gridDim.x, p);
+        const int b = gc.b, g = gc.g;
         // K slot: Q, K ring, K_new
         const uint32_t ks = (uint32_t)k % kKSlots;
         if (!mbar_wait(bar(kBarKEmpty + ks), (((uint32_t)k / kKSlots) & 1) ^ 1, kErrWaitKvEmpty,
@@ -221,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(kb, kbytes);
 #pragma unroll
         for (int hf = 0; hf < kHalves; ++hf) {
-          tma_load_4d(kst + kKQ + hf * kQHalf, &map_q, 64 * hf, g * kG, 0, b, kb);
-          tma_load_4d(kst + kKK + hf * kHalf, &map_k, 64 * hf, u * kW, 0, 0, kb);
+          tma_load_4d(kst + kKQ + hf * kQHalf, &map_q, 64 * hf, gc.gq * kG, 0, b, kb);
+          tma_load_4d(kst + kKK + hf * kHalf, &map_k, 64 * hf, gc.ur * kW, 0, 0, kb);
           tma_load_4d(kst + kKKn + hf * kKnHalf, &map_kn, 64 * hf, g, 0, b, kb);
         }
         ++nkld;
@@ -236,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(vb, vbytes);
 #pragma unroll
         for (int hf = 0; hf < kHalves; ++hf) {
-          tma_load_4d(vst + kVV + hf * kHalf, &map_v, 64 * hf, u * kW, 0, 0, vb);
+          tma_load_4d(vst + kVV + hf * kHalf, &map_v, 64 * hf, gc.ur * kW, 0, 0, vb);
           tma_load_4d(vst + kVVn + hf * kNewHalf, &map_vn, 64 * hf, g, 0, b, vb);
         }
         ++nvld;
@@ -337,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = r >> 3, h = r & 7;
       const uint32_t s_addr = tmem + lane_addr + col_s(w), o_addr = tmem + lane_addr + col_o(w);
       for (int k = w; k < nk; k += 2) {
-        const int u = (int)blockIdx.x + k * (int)gridDim.x;
-        const int b = u / p.Hkv, g = u - b * p.Hkv;
+        const GroupCoords gc((int)blockIdx.x + k * (int)gridDim.x, p);
+        const int b = gc.b, g = gc.gq;   // g: the query group (heads g kG ..)
         const int64_t p0 = p.pos[b];
         const float sk = p.sink[g * kG + h] * 1.4426950408889634f;
         if (!mbar_wait(bar(kBarSFull + w), ((uint32_t)k >> 1) & 1, kErrWaitSFull, abort_flag))
@@ -476,8 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kHelpers = 32 * (4 - kSoftWarps);   // 96 or 64 threads
       const int t = (wq - kSoftWarps) * 32 + lane;
       for (int k = w; k < nk; k += 2) {
-        const int u = (int)blockIdx.x + k * (int)gridDim.x;
-        const int b = u / p.Hkv;
+        const int b = GroupCoords((int)blockIdx.x + k * (int)gridDim.x, p).b;
         const uint32_t vs = (uint32_t)k % kVSlots;
         const uint32_t vst = sbase + kOffV + vs * kVSlotBytes;
         const int64_t p0 = p.pos[b];

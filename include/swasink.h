@@ -327,13 +327,14 @@ swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, cons
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Name of the decode kernel swa_sink_decode would launch for these sizes
- * ("tc_decode" for bf16, D = 64 or 128, W = 128 and Hq / Hkv in {1, 2, 4, 8, 16};
- * "simt_decode" otherwise), or "invalid". */
+ * ("tc_decode" for bf16, D = 64 or 128, W = 128 and Hq / Hkv in {1, 2, 4, 8, 16}
+ * or a larger multiple of 8, run as groups of 8 heads; "simt_decode"
+ * otherwise), or "invalid". */
 const char* swa_sink_decode_path(int B, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Name of the verify kernel swa_sink_verify would launch ("tc_verify" for
- * bf16, D = 64 or 128, W = 128, Hq = 8 Hkv and L <= 8; "simt_verify" otherwise), or
- * "invalid". */
+ * bf16, D = 64 or 128, W = 128, Hq a multiple of 8 Hkv (groups of 8 heads)
+ * and L <= 8; "simt_verify" otherwise), or "invalid". */
 const char* swa_sink_verify_path(int B, int L, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Static text for a status code. */

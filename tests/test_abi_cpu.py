@@ -77,7 +77,9 @@ def test_decode_path_selection(L):
     assert swa.decode_path(256, 32, 8, 128, 128) == "tc_decode"      # 4 heads per kv head
     assert swa.decode_path(256, 64, 4, 128, 128) == "tc_decode"      # 16
     assert swa.decode_path(256, 8, 8, 128, 128) == "tc_decode"       # 1
-    assert swa.decode_path(256, 64, 2, 128, 128) == "simt_decode"    # 32: past the MMA's 16
+    assert swa.decode_path(256, 64, 2, 128, 128) == "tc_decode"      # 32: four groups of 8
+    assert swa.decode_path(256, 96, 4, 128, 128) == "tc_decode"      # 24: three groups of 8
+    assert swa.decode_path(256, 48, 4, 128, 128) == "simt_decode"    # 12: not a multiple of 8
     assert swa.decode_path(256, 24, 8, 128, 128) == "simt_decode"    # 3
     assert swa.decode_path(256, 64, 8, 128, 320) == "simt_decode"
     assert swa.decode_path(256, 64, 8, 128, 321) == "invalid"
@@ -164,6 +166,9 @@ def test_verify_path_selection(L):
     assert swa.verify_path(2, 4, 8, 1, 64, 128) == "tc_verify"     # head dimension 64
     assert swa.verify_path(2, 4, 8, 1, 64, 32) == "simt_verify"
     assert swa.verify_path(2, 65, 8, 1, 128, 128) == "invalid"
+    assert swa.verify_path(2, 4, 64, 4, 128, 128) == "tc_verify"    # 16 heads per kv head
+    assert swa.verify_path(2, 8, 96, 4, 64, 128) == "tc_verify"     # 24
+    assert swa.verify_path(2, 4, 32, 8, 128, 128) == "simt_verify"  # 4
 
 
 @pytest.mark.parametrize("args,status", [

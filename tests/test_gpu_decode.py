@@ -28,11 +28,12 @@ def test_decode_full_size_workload(cuda_ok):
 
 
 @pytest.mark.parametrize("B,Hq,Hkv", [(37, 64, 16), (29, 64, 4), (11, 8, 4), (13, 4, 4),
-                                       (300, 16, 1)])
+                                       (300, 16, 1), (20, 96, 4), (33, 64, 2), (77, 128, 4)])
 def test_decode_tc_group_sizes(cuda_ok, B, Hq, Hkv):
     # the tensor-core decode for 4, 16, 2 and 1 query heads per kv head (the
-    # 16 MMA columns hold the group's heads, the rest padding), partial and
-    # full rings, one and several groups per sequence
+    # 16 MMA columns hold the group's heads, the rest padding), and for 24, 32
+    # and 32 again as sibling groups of 8 on the same rings; partial and full
+    # rings, one and several groups per sequence
     assert swa.decode_path(B, Hq, Hkv, 128, 128) == "tc_decode"
     x = gen.decode_inputs(B, Hq, Hkv, 128, 128, seed=B + Hq, pos_lo=0, pos_hi=600)
     for b in range(B):

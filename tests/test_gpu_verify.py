@@ -86,6 +86,23 @@ def test_verify_tc_head_dim_64(cuda_ok, B, L):
     assert swa.device_error() == 0
 
 
+@pytest.mark.parametrize("B,L,Hq,Hkv,D", [(23, 4, 64, 4, 128), (17, 8, 96, 4, 128),
+                                          (30, 3, 32, 1, 64), (151, 2, 64, 4, 128)])
+def test_verify_tc_sibling_groups(cuda_ok, B, L, Hq, Hkv, D):
+    # 16, 24 and 32 query heads per kv head: sibling groups of 8 on the same
+    # rings and drafted keys; B = 151 with 4 kv heads and 2 siblings gives
+    # CTAs 8 or 9 groups, sibling pairs split across rounds
+    assert swa.verify_path(B, L, Hq, Hkv, D, 128) == "tc_verify"
+    x = gen.verify_inputs(B, L, Hq, Hkv, D, 128, seed=B + L + Hq, pos_lo=0, pos_hi=700)
+    for b in range(B):
+        p = int(x.pos[b])
+        if p < 128:
+            x.k_ring[b, :, p:] = float("nan")
+            x.v_ring[b, :, p:] = float("nan")
+    _check(x)
+    assert swa.device_error() == 0
+
+
 def test_verify_eight_drafts_equal_prefill_rows(cuda_ok):
     B, T, Hq, Hkv, D, W, L = 2, 600, 16, 2, 128, 128, 8
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=64, device="cuda")
