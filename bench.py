@@ -336,12 +336,12 @@ def traffic_shape(**dims) -> str:
     return " ".join(f"{k}{v}" for k, v in dims.items())
 
 
-def recorded_traffic(kernel: str, shape: str):
+def recorded_traffic(kernel: str, shape: str, path: str = ""):
     """DRAM bytes (read + write) per launch of the bench workload, from the
-    committed ncu summary ``profiles/dram_traffic.txt``; None if absent, if the
-    record was taken on another workload shape, or if the kernel's sources
-    have changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    committed ncu summary ``profiles/dram_traffic.txt`` (or ``path``); None if
+    absent, if the record was taken on another workload shape, or if the
+    kernel's sources have changed since the counters were taken."""
+    path = path or os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
     rec = {}

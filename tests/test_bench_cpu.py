@@ -78,13 +78,19 @@ def test_clock_sampler_with_a_fake_nvml():
     assert d["reasons"] == ["sw_power_cap"]
 
 
-def test_traffic_record_applies_to_its_own_workload_only():
-    # the committed record is per kernel and workload shape: another shape of
-    # the same kernel gets no traffic figure
+def test_traffic_record_applies_to_its_own_workload_only(tmp_path):
+    # a record is per kernel, workload shape and source hash: another shape of
+    # the same kernel, or changed sources, get no traffic figure
     shape = bench.traffic_shape(B=256, Hq=64, Hkv=8, D=128, W=128)
     assert shape == "B256 Hq64 Hkv8 D128 W128"
-    assert bench.recorded_traffic("decode_tc_kernel", shape) is not None
-    assert bench.recorded_traffic("decode_tc_kernel",
-                                  bench.traffic_shape(B=256, Hq=32, Hkv=8, D=128, W=128)) is None
-    assert bench.recorded_traffic("swa_fwd_tc_kernel",
-                                  bench.traffic_shape(B=4, T=8192, Hq=64, Hkv=8, D=64, W=128)) is None
+    rec = tmp_path / "traffic.txt"
+    rec.write_text("# comment\n"
+                   "decode_tc_kernel.bytes_per_launch: 123456\n"
+                   f"decode_tc_kernel.source_hash: {bench.kernel_source_hash('decode_tc_kernel')}\n"
+                   f"decode_tc_kernel.shape: {shape}\n")
+    assert bench.recorded_traffic("decode_tc_kernel", shape, str(rec)) == 123456
+    other = bench.traffic_shape(B=256, Hq=32, Hkv=8, D=128, W=128)
+    assert bench.recorded_traffic("decode_tc_kernel", other, str(rec)) is None
+    rec.write_text(rec.read_text().replace("source_hash: ", "source_hash: 0"))
+    assert bench.recorded_traffic("decode_tc_kernel", shape, str(rec)) is None
+    assert bench.recorded_traffic("verify_tc_kernel", shape, str(rec)) is None
