@@ -866,7 +866,8 @@ WIDE_DECODE = {"g4": dict(B=256, Hq=32, Hkv=8, D=128, W=128),
                "g16": dict(B=256, Hq=64, Hkv=4, D=128, W=128),
                "d64": dict(B=256, Hq=64, Hkv=8, D=64, W=128)}
 WIDE_VERIFY = {"l8": dict(B=256, L=8, Hq=64, Hkv=8, D=128, W=128)}
-WIDE_GLOBAL = {"d64": dict(B=1, T=16384, Hq=64, Hkv=8, D=64, W=16384)}
+WIDE_GLOBAL = {"d64": dict(B=1, T=16384, Hq=64, Hkv=8, D=64, W=16384),
+               "g4": dict(B=1, T=16384, Hq=32, Hkv=8, D=128, W=16384)}
 
 
 def wide_prefill_line(swa, c, steps, dev, stream, peaks, cpu=False):

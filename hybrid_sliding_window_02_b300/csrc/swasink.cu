@@ -47,7 +47,7 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   bool tc_attr[2][2][2] = {};   // [bf16 output][4 heads per tile][D = 64]
-  bool tcg_attr[2][2][2] = {};   // [bf16 output][scores][D = 64]
+  bool tcg_attr[2][2][2][2] = {};   // [bf16 output][scores][D = 64][4 heads per tile]
   bool topk_attr = false;
   bool dectc_attr[5][2] = {};   // [log2 G][D = 64]
   bool vertc_attr[2][2] = {};   // [64 query rows][D = 64]
@@ -183,7 +183,8 @@ FwdPath select_fwd(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype dt) {
     // G = 8 R: R sets of CTAs walk the sibling groups in step (R <= 64)
     if (W <= swa::tcswa::kMaxW && (G == 4 || (G % swa::tcswa::kGroup == 0 && G <= 512)))
       return kPathTcSwa;   // D = 64 or 128
-    if (W > swa::tcswa::kMaxW && G % swa::tcglobal::kG == 0) return kPathTcGlobal;  // D = 64 or 128
+    if (W > swa::tcswa::kMaxW && (G == 4 || G % swa::tcglobal::kG == 0))
+      return kPathTcGlobal;   // D = 64 or 128
   }
   return kPathSimt;
 }
@@ -293,33 +294,45 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
   const bool d64 = D == 64;
   using Kern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
   // [bf16 output][scores][D = 64]
+  // [bf16 output][scores][D = 64]: 8 heads per tile
   static const Kern kTable[2][2][2] = {
-      {{swa_fwd_tc_global_kernel<false, false, 128>, swa_fwd_tc_global_kernel<false, false, 64>},
-       {swa_fwd_tc_global_kernel<false, true, 128>, swa_fwd_tc_global_kernel<false, true, 64>}},
-      {{swa_fwd_tc_global_kernel<true, false, 128>, swa_fwd_tc_global_kernel<true, false, 64>},
-       {swa_fwd_tc_global_kernel<true, true, 128>, swa_fwd_tc_global_kernel<true, true, 64>}}};
-  const Kern kern = kTable[bf16_out][scores][d64];
+      {{swa_fwd_tc_global_kernel<false, false, 128, 8>, swa_fwd_tc_global_kernel<false, false, 64, 8>},
+       {swa_fwd_tc_global_kernel<false, true, 128, 8>, swa_fwd_tc_global_kernel<false, true, 64, 8>}},
+      {{swa_fwd_tc_global_kernel<true, false, 128, 8>, swa_fwd_tc_global_kernel<true, false, 64, 8>},
+       {swa_fwd_tc_global_kernel<true, true, 128, 8>, swa_fwd_tc_global_kernel<true, true, 64, 8>}}};
+  // [bf16 output][D = 64]: 4 heads per tile (G = 4), no block scores
+  static const Kern kTable4[2][2] = {
+      {swa_fwd_tc_global_kernel<false, false, 128, 4>, swa_fwd_tc_global_kernel<false, false, 64, 4>},
+      {swa_fwd_tc_global_kernel<true, false, 128, 4>, swa_fwd_tc_global_kernel<true, false, 64, 4>}};
+  const int gt = (Hq / Hkv == 4) ? 4 : kG;   // heads per tile
+  if (gt == 4 && (scores || blk_idx != nullptr)) {
+    set_error_text("block scores and sparse mode take 8 heads per kv head");
+    return SWA_EUNSUPPORTED;
+  }
+  const bool g4 = gt == 4;
+  const Kern kern = g4 ? kTable4[bf16_out][d64] : kTable[bf16_out][scores][d64];
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].tcg_attr[bf16_out][scores][d64]) {
+    if (!g_dev[dev].tcg_attr[bf16_out][scores][d64][g4]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_global_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].tcg_attr[bf16_out][scores][d64] = true;
+      g_dev[dev].tcg_attr[bf16_out][scores][d64][g4] = true;
     }
   }
-  const long long nitem_seq = (T + kItemPos - 1) / kItemPos;
-  const int Hg = Hq / kG;   // groups of 8 query heads; the scores and sparse modes have Hg = Hkv
+  const int item_pos = item_pos_for(gt), npos = npos_for(gt);
+  const long long nitem_seq = (T + item_pos - 1) / item_pos;
+  const int Hg = Hq / gt;   // head groups of a tile; the scores and sparse modes have Hg = Hkv
   const long long total = (long long)B * Hg * nitem_seq;
   if (total >= (1LL << 31)) {
     set_error_text("problem too large for the tensor-core kernel");
     return SWA_EUNSUPPORTED;
   }
   CUtensorMap mq, mk, mv;
-  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, Hq, T, B, 64, kG, kNpos) ||
+  if (!make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, Hq, T, B, 64, gt, npos) ||
       !make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, D, Hkv, T, B, 64, 1, kBlk) ||
       !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, D, Hkv, T, B, 64, 1, kBlk))
     return SWA_ECUDA;
@@ -334,6 +347,7 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
   p.W = W;
   p.Hg = Hg;
   p.rep = Hg / Hkv;
+  p.item_pos = item_pos;
   p.nitem_seq = (int)nitem_seq;
   p.total_items = (int)total;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
@@ -341,7 +355,7 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
   p.nqg = (T + 3) / 4;
   p.nkb = (T + kBlk - 1) / kBlk;
   p.blk_idx = blk_idx;
-  p.qb_size = qb_size > 0 ? qb_size : kItemPos;
+  p.qb_size = qb_size > 0 ? qb_size : item_pos;
   p.topk = topk;
   p.nqb = (T + p.qb_size - 1) / p.qb_size;
   const long long grid = total < sms ? total : sms;

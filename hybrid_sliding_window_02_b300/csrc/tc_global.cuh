@@ -5,14 +5,16 @@
 // kernel ("MiMo-V2-Flash Technical Report" summary, section 前置知识: the
 // global layers of the hybrid stack attend to the whole causal prefix; every
 // head adds a learnable bias to its softmax denominator), for bf16 inputs,
-// D = 64 or 128 and groups of 8 query heads per kv head, any window W (W >= T
-// is the global layer).  Keys are visited in blocks of 128 with an online softmax:
+// D = 64 or 128 and 4 or any multiple of 8 query heads per kv head, any
+// window W (W >= T is the global layer).  Keys are visited in blocks of 128 with an online softmax:
 // the running max starts at the sink logit and the running denominator at
 // exp(sink - max), so the sink is counted exactly once whatever the order.
 //
-// Work item = one kv head of one sequence x 32 consecutive positions, split
-// into two Q tiles of 16 positions x 8 query heads (128 MMA rows each, row r =
-// position r / 8, head r % 8).  Both tiles share every K/V block the CTA
+// Work item = one group of 8 query heads of one sequence x 32 consecutive
+// positions, split into two Q tiles of 16 positions x 8 heads (128 MMA rows
+// each, row r = position r / 8, head r % 8); with 4 query heads per kv head,
+// 64 positions in two tiles of 32 positions x 4 heads (row r = position
+// r / 4, head r % 4).  Both tiles share every K/V block the CTA
 // loads, which halves the K/V traffic out of L2 against one tile per block.
 // Items go to persistent CTAs (one per SM), dealt round by round in
 // alternating direction, in an order whose item lengths change smoothly
@@ -66,10 +68,11 @@ namespace tcglobal {
 
 constexpr int kThreads = 352;
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
-constexpr int kG = 8;                   // query heads per tile (one kv group)
-constexpr int kNpos = 16;               // positions per Q tile
+constexpr int kG = 8;                   // query heads per tile (one kv group), or 4 when G = 4
 constexpr int kTiles = 2;               // Q tiles per work item
-constexpr int kItemPos = kNpos * kTiles;
+// positions per Q tile and per work item for kGt heads per tile (128 rows)
+__host__ __device__ constexpr int npos_for(int kGt) { return 128 / kGt; }
+__host__ __device__ constexpr int item_pos_for(int kGt) { return kTiles * npos_for(kGt); }
 constexpr int kBlk = 128;               // keys per block
 constexpr uint32_t kSlots = 5;          // K/V ring slots (one K or V block each)
 constexpr float kRescaleLog2 = 8.0f;    // move the running max only past this
@@ -113,9 +116,10 @@ struct Params {
   void* out;          // float, or bf16 with kBf16Out
   float* lse;
   int B, T, Hq, Hkv, W;
-  int Hg;             // groups of 8 query heads per sequence: Hq / 8
-  int rep;            // groups per kv head: Hq / (8 Hkv) (1 with scores or sparse mode)
-  int nitem_seq;      // ceil(T / 32)
+  int Hg;             // head groups of a tile per sequence: Hq / (heads per tile)
+  int rep;            // groups per kv head: G / 8 for G = 8 R, else 1 (1 with scores or sparse mode)
+  int item_pos;       // positions per work item: 32 (8 heads per tile) or 64 (4)
+  int nitem_seq;      // ceil(T / item_pos)
   int total_items;    // B * Hg * nitem_seq (< 2^31, checked on the host)
   float scale_log2;   // log2(e) / sqrt(D)
   // block scores (optional): blockmax[b][kvh][ceil(T/4)][ceil(T/128)], the max
@@ -163,7 +167,7 @@ __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
   it.b = (int)(bk / (uint32_t)p.Hg);
   it.grp = (int)(bk - (uint32_t)it.b * (uint32_t)p.Hg);
   it.kvh = it.grp / p.rep;
-  it.p0 = n2 * kItemPos;
+  it.p0 = n2 * p.item_pos;
   if (p.blk_idx != nullptr) {
     it.blocks = p.blk_idx + (((int64_t)it.b * p.Hkv + it.kvh) * p.nqb + it.p0 / p.qb_size) * p.topk;
     // the item's blocks are the entries before the first negative one; the
@@ -179,7 +183,7 @@ __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
     return it;
   }
   it.blocks = nullptr;
-  const int last = min(it.p0 + kItemPos - 1, p.T - 1);
+  const int last = min(it.p0 + p.item_pos - 1, p.T - 1);
   const int first_key = max(0, it.p0 - p.W + 1);
   it.jlo = first_key / kBlk;
   it.nb = last / kBlk - it.jlo + 1;
@@ -215,12 +219,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-template <bool kBf16Out, bool kScores, int kHd>
+template <bool kBf16Out, bool kScores, int kHd, int kGt>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_fwd_tc_global_kernel(const __grid_constant__ CUtensorMap map_q,
                              const __grid_constant__ CUtensorMap map_k,
                              const __grid_constant__ CUtensorMap map_v, const Params p) {
   static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");
+  static_assert(kGt == 8 || (kGt == 4 && !kScores), "8 heads per tile, or 4 without block scores");
+  constexpr int kNpos = npos_for(kGt);   // positions per Q tile: row r = position r / kGt, head r % kGt
   constexpr int kHalves = kHd / 64;   // 64-dimension halves of q, k, v rows
   using C = Cols<kHd>;
   extern __shared__ uint8_t smem_raw[];
@@ -280,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t qdst = sbase + kOffQ + i * kQTile;
           const int pos = it.p0 + i * kNpos;
           mbar_arrive_expect_tx(bar(kBarQFull + i), kHalves * kQHalf);
-          tma_load_4d(qdst, &map_q, 0, it.grp * kG, pos, it.b, bar(kBarQFull + i));
+          tma_load_4d(qdst, &map_q, 0, it.grp * kGt, pos, it.b, bar(kBarQFull + i));
           if constexpr (kHalves == 2)
-            tma_load_4d(qdst + kQHalf, &map_q, 64, it.grp * kG, pos, it.b, bar(kBarQFull + i));
+            tma_load_4d(qdst + kQHalf, &map_q, 64, it.grp * kGt, pos, it.b, bar(kBarQFull + i));
           ++q_armed[i];
         }
         // The next item's Q tiles and first key blocks go to L2 now, so that
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && cta_item(k + 1, p, nx)) {
             for (int i = 0; i < kTiles; ++i)
               for (int hv = 0; hv < kHalves; ++hv)
-                tma_prefetch_l2_4d(&map_q, 64 * hv, nx.grp * kG, nx.p0 + i * kNpos, nx.b);
+                tma_prefetch_l2_4d(&map_q, 64 * hv, nx.grp * kGt, nx.p0 + i * kNpos, nx.b);
             for (int t = 0; t < 2 && t < nx.nb; ++t) {
               const int key = item_block(nx, t) * kBlk;
               for (int hv = 0; hv < kHalves; ++hv) {
@@ -429,12 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_addr = tmem + lane_addr + C::s(ti);
     const uint32_t p_addr = tmem + lane_addr + C::p(ti);
     const uint32_t o_addr = tmem + lane_addr + C::o(ti);
-    const int g = r & 7;
+    const int g = r % kGt;
     uint32_t npv = 0;
     Item it;
     for (int k = 0; cta_item(k, p, it); ++k) {
-      const int h = it.grp * kG + g;
-      const int pos = it.p0 + ti * kNpos + (r >> 3);
+      const int h = it.grp * kGt + g;
+      const int pos = it.p0 + ti * kNpos + r / kGt;
       const float sk = p.sink[h] * 1.4426950408889634f;  // log2 units
       float m_run = sk;                                   // -inf for no sink
       float l = (sk == -INFINITY) ? 0.f : 1.f;            // exp2(sk - m_run)
@@ -575,11 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // O read in the 16x256b shape: thread (rr, qd) = (lane / 4, lane % 4)
-        // holds rows 16 hf + 8 kk + rr of this warp's lanes, i.e. position
-        // 4 quad + 2 hf + kk of the tile and head rr, columns 8 j + 2 qd + {0, 1}.
-        // A quad then writes whole 32-byte sectors, and one store covers the
-        // 8 heads of a position (8 D floats, contiguous); each row's 1 / l comes from
-        // the thread that owns the row (lane 16 hf + 8 kk + rr).
+        // holds rows 16 hf + 8 kk + rr of this warp's lanes (tile row
+        // 32 quad + 16 hf + 8 kk + rr: position row / kGt, head row % kGt),
+        // columns 8 j + 2 qd + {0, 1}.  A quad then writes whole 32-byte
+        // sectors, and one store covers 8 consecutive rows (8 D floats, the
+        // heads of one or two positions); each row's 1 / l comes from the
+        // thread that owns the row (lane 16 hf + 8 kk + rr).
         const int rr = lane >> 2, qd = lane & 3;
         const uint32_t o_warp = tmem + ((uint32_t)(quad * 32) << 16) + C::o(ti);
 #pragma unroll
@@ -595,10 +602,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             const float il = __shfl_sync(0xffffffffu, inv_l, 16 * hf + 8 * kk + rr);
-            const int pos_k = it.p0 + ti * kNpos + 4 * quad + 2 * hf + kk;
+            const int row = 32 * quad + 16 * hf + 8 * kk + rr;   // tile row of these values
+            const int pos_k = it.p0 + ti * kNpos + row / kGt;
             if (pos_k < p.T) {
               float* orow = static_cast<float*>(p.out) +
-                            (((long long)it.b * p.T + pos_k) * p.Hq + it.grp * kG + rr) * kHd + 2 * qd;
+                            (((long long)it.b * p.T + pos_k) * p.Hq + it.grp * kGt + row % kGt) * kHd +
+                            2 * qd;
 #pragma unroll
               for (int j = 0; j < kHd / 8; ++j)
                 st_global_v2(orow + 8 * j,

@@ -322,7 +322,7 @@ swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, cons
  * "invalid": bf16 inputs take "tc_swa" (the sliding-window tensor-core kernel)
  * when W <= 129 and Hq / Hkv is 4 or a multiple of 8 up to 512 (D = 64 or
  * 128), and "tc_global" (the online-softmax tensor-core kernel) when W > 129
- * and Hq / Hkv is a multiple of 8 (D = 64 or 128); everything else takes
+ * and Hq / Hkv is 4 or a multiple of 8 (D = 64 or 128); everything else takes
  * "simt" (CUDA cores, fp32 or bf16 inputs). */
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 

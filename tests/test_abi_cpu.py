@@ -55,7 +55,8 @@ def test_path_selection(L):
     assert swa.fwd_path(1, 512, 64, 8, 128, 128, swa.SWA_F32) == "simt"
     assert swa.fwd_path(1, 512, 64, 64, 128, 128) == "simt"
     assert swa.fwd_path(1, 512, 16, 4, 128, 128) == "tc_swa"       # 4 heads per kv head
-    assert swa.fwd_path(1, 512, 16, 4, 128, 130) == "simt"         # ... no global kernel for 4
+    assert swa.fwd_path(1, 512, 16, 4, 128, 130) == "tc_global"    # ... and on the global kernel
+    assert swa.fwd_path(1, 512, 8, 4, 128, 512) == "simt"           # 2 heads per kv head
     assert swa.fwd_path(1, 512, 64, 4, 128, 128) == "tc_swa"       # 16: two groups of 8
     assert swa.fwd_path(1, 512, 64, 4, 128, 512) == "tc_global"
     assert swa.fwd_path(1, 512, 48, 2, 128, 128) == "tc_swa"       # 24

@@ -152,5 +152,37 @@ def test_tc_global_head_dim_64(cuda_ok, B, T, Hq, Hkv, W):
     assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(l16, l32)
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [
+    (1, 700, 4, 1, 128, 700),      # 4 heads per kv head: tiles of 32 positions x 4 heads
+    (2, 1000, 16, 4, 128, 1000),   # items of 64 positions, the last one ragged
+    (1, 900, 8, 2, 128, 300),      # window start inside a block
+    (3, 130, 4, 1, 128, 130),
+    (1, 1500, 32, 8, 64, 1500),    # head dimension 64
+])
+def test_tc_global_four_heads_per_kv_head(cuda_ok, B, T, Hq, Hkv, D, W):
+    assert swa.fwd_path(B, T, Hq, Hkv, D, W) == "tc_global"
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=2400 + T + W + D)
+    o32, l32 = _full_check(x, W)
+    o16, l16 = swa.swa_sink_fwd(*(t.cuda() for t in (x.q, x.k, x.v, x.sink)), W,
+                                out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(l16, l32)
+
+
+def test_tc_global_four_heads_per_kv_head_sampled(cuda_ok):
+    # B1 T16384 Hq32 Hkv8 D128 global layer: 10 edge positions plus 54 drawn
+    # over the causal range, every head
+    B, T, Hq, Hkv, D = 1, 16384, 32, 8, 128
+    assert swa.fwd_path(B, T, Hq, Hkv, D, T) == "tc_global"
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=2450, device="cuda")
+    out, lse = swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, T)
+    torch.cuda.synchronize()
+    rows = sample_rows(B, T, Hq, 64, seed=44)
+    o_ref, l_ref = oracle_rows_from_slices(x.q, x.k, x.v, x.sink, T, rows)
+    o, l = gather_rows(out, lse, rows)
+    assert_bf16_close(o, o_ref)
+    assert_lse_close(l, l_ref)
+
+
 def test_tc_global_no_device_error(cuda_ok):
     assert swa.device_error() == 0

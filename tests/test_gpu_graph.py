@@ -36,6 +36,7 @@ def test_graph_replay_equals_eager(cuda_ok):
         outs["dec16"] = swa.swa_sink_decode(d16.q, d16.k_ring, d16.v_ring, d16.pos, d16.sink,
                                             stream=st)
         outs["swa4"] = swa.swa_sink_fwd(x4.q, x4.k, x4.v, x4.sink, 128, stream=st)
+        outs["glb4"] = swa.swa_sink_fwd(x4.q, x4.k, x4.v, x4.sink, 500, stream=st)
         outs["swa16"] = swa.swa_sink_fwd(x16.q, x16.k, x16.v, x16.sink, 128, stream=st)
         outs["glb16"] = swa.swa_sink_fwd(x16.q, x16.k, x16.v, x16.sink, 500, stream=st)
         outs["ver8"] = swa.swa_sink_verify(v8.q, v8.k_new, v8.v_new, v8.k_ring, v8.v_ring, v8.pos,

@@ -34,6 +34,7 @@ def _device_call(x, W, out_dtype=torch.float32):
     (2, 1500, 64, 4, 128, 128),   # 16 heads per kv head (two groups of 8)
     (2, 2600, 64, 8, 64, 128),    # head dimension 64
     (2, 900, 32, 4, 64, 900),     # head dimension 64, global layer: half the kv heads per chunk
+    (2, 700, 16, 4, 128, 700),    # global layer with 4 heads per kv head
 ])
 def test_host_call_equals_device_call(cuda_ok, pinned, B, T, Hq, Hkv, D, W):
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=B + T)

@@ -167,8 +167,8 @@ def test_simt_fp32_shapes(cuda_ok, B, T, Hq, Hkv, D, W):
 
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [
-    (1, 300, 2, 1, 128, 128), (2, 100, 8, 8, 64, 33), (1, 200, 4, 1, 128, 200),
-    (1, 150, 12, 1, 128, 128),
+    (1, 300, 2, 1, 128, 128), (2, 100, 8, 8, 64, 33), (1, 200, 2, 1, 128, 200),
+    (1, 150, 12, 1, 128, 128), (1, 180, 12, 1, 64, 180),
 ])
 def test_simt_bf16_shapes(cuda_ok, B, T, Hq, Hkv, D, W):
     assert swa.fwd_path(B, T, Hq, Hkv, D, W) == "simt"
