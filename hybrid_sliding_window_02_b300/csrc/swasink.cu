@@ -47,10 +47,10 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   bool tc_attr[2][2][2] = {};   // [bf16 output][4 heads per tile][D = 64]
-  bool tcg_attr[2][2][2][2] = {};   // [bf16 output][scores][D = 64][4 heads per tile]
+  bool tcg_attr[2][2][2][4] = {};   // [bf16 output][scores][D = 64][heads per tile 1, 2, 4, 8]
   bool topk_attr = false;
   bool dectc_attr[5][2] = {};   // [log2 G][D = 64]
-  bool vertc_attr[2][2] = {};   // [64 query rows][D = 64]
+  bool vertc_attr[4][2][2] = {};   // [heads per group 1, 2, 4, 8][64 query rows][D = 64]
   bool decode_attr[2][2][5] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -166,8 +166,11 @@ enum FwdPath { kPathInvalid, kPathSimt, kPathTcSwa, kPathTcGlobal };
 constexpr int kVerifyMaxL = 64;  // drafted tokens per verify call
 
 bool verify_tc_applies(int L, int Hq, int Hkv, int D, int W, swa_dtype dt) {
-  return dt == SWA_BF16 && (D == 128 || D == 64) && W == swa::vertc::kW && Hkv >= 1 &&
-         Hq % (Hkv * swa::vertc::kG) == 0 && L >= 1 && L <= swa::vertc::kLmax;
+  if (!(dt == SWA_BF16 && (D == 128 || D == 64) && W == swa::vertc::kW && Hkv >= 1 &&
+        Hq % Hkv == 0 && L >= 1 && L <= swa::vertc::kLmax))
+    return false;
+  const int G = Hq / Hkv;
+  return G == 1 || G == 2 || G == 4 || G % swa::vertc::kG == 0;
 }
 
 // Query heads per sliding-window tile: 4 when G = 4, else 8 (a kv head's G =
@@ -183,7 +186,9 @@ FwdPath select_fwd(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype dt) {
     // G = 8 R: R sets of CTAs walk the sibling groups in step (R <= 64)
     if (W <= swa::tcswa::kMaxW && (G == 4 || (G % swa::tcswa::kGroup == 0 && G <= 512)))
       return kPathTcSwa;   // D = 64 or 128
-    if (W > swa::tcswa::kMaxW && (G == 4 || G % swa::tcglobal::kG == 0))
+    // the online-softmax kernel takes any window: wider ones, and the group
+    // sizes the sliding-window kernel's tiles do not fit (1, 2, above 512)
+    if (G == 1 || G == 2 || G == 4 || G % swa::tcglobal::kG == 0)
       return kPathTcGlobal;   // D = 64 or 128
   }
   return kPathSimt;
@@ -300,27 +305,32 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
        {swa_fwd_tc_global_kernel<false, true, 128, 8>, swa_fwd_tc_global_kernel<false, true, 64, 8>}},
       {{swa_fwd_tc_global_kernel<true, false, 128, 8>, swa_fwd_tc_global_kernel<true, false, 64, 8>},
        {swa_fwd_tc_global_kernel<true, true, 128, 8>, swa_fwd_tc_global_kernel<true, true, 64, 8>}}};
-  // [bf16 output][D = 64]: 4 heads per tile (G = 4), no block scores
-  static const Kern kTable4[2][2] = {
-      {swa_fwd_tc_global_kernel<false, false, 128, 4>, swa_fwd_tc_global_kernel<false, false, 64, 4>},
-      {swa_fwd_tc_global_kernel<true, false, 128, 4>, swa_fwd_tc_global_kernel<true, false, 64, 4>}};
-  const int gt = (Hq / Hkv == 4) ? 4 : kG;   // heads per tile
-  if (gt == 4 && (scores || blk_idx != nullptr)) {
+  // [heads per tile 1, 2, 4][bf16 output][D = 64]: G = 1, 2 or 4, no block scores
+  static const Kern kTableSmall[3][2][2] = {
+      {{swa_fwd_tc_global_kernel<false, false, 128, 1>, swa_fwd_tc_global_kernel<false, false, 64, 1>},
+       {swa_fwd_tc_global_kernel<true, false, 128, 1>, swa_fwd_tc_global_kernel<true, false, 64, 1>}},
+      {{swa_fwd_tc_global_kernel<false, false, 128, 2>, swa_fwd_tc_global_kernel<false, false, 64, 2>},
+       {swa_fwd_tc_global_kernel<true, false, 128, 2>, swa_fwd_tc_global_kernel<true, false, 64, 2>}},
+      {{swa_fwd_tc_global_kernel<false, false, 128, 4>, swa_fwd_tc_global_kernel<false, false, 64, 4>},
+       {swa_fwd_tc_global_kernel<true, false, 128, 4>, swa_fwd_tc_global_kernel<true, false, 64, 4>}}};
+  const int G = Hq / Hkv;
+  const int gt = G < kG ? G : kG;   // heads per tile: 1, 2, 4 or 8
+  const int gi = gt == 1 ? 0 : gt == 2 ? 1 : gt == 4 ? 2 : 3;
+  if (gt != kG && (scores || blk_idx != nullptr)) {
     set_error_text("block scores and sparse mode take 8 heads per kv head");
     return SWA_EUNSUPPORTED;
   }
-  const bool g4 = gt == 4;
-  const Kern kern = g4 ? kTable4[bf16_out][d64] : kTable[bf16_out][scores][d64];
+  const Kern kern = gt != kG ? kTableSmall[gi][bf16_out][d64] : kTable[bf16_out][scores][d64];
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].tcg_attr[bf16_out][scores][d64][g4]) {
+    if (!g_dev[dev].tcg_attr[bf16_out][scores][d64][gi]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kSmemBytes);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(swa_fwd_tc_global_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].tcg_attr[bf16_out][scores][d64][g4] = true;
+      g_dev[dev].tcg_attr[bf16_out][scores][d64][gi] = true;
     }
   }
   const int item_pos = item_pos_for(gt), npos = npos_for(gt);
@@ -474,26 +484,36 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
   using namespace swa::vertc;
   int dev, sms;
   if (!current_device(&dev) || !device_sms(dev, &sms)) return SWA_ECUDA;
-  // 32 query rows per group up to L = 4, else 64
-  const bool rows64 = L * kG > 32, d64 = D == 64;
-  void (*const kernels[2][2])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
-                              Params) = {{verify_tc_kernel<32, 128>, verify_tc_kernel<32, 64>},
-                                         {verify_tc_kernel<64, 128>, verify_tc_kernel<64, 64>}};
-  auto kern = kernels[rows64][d64];
+  // query heads per group: G = 1, 2, 4, else 8 (R sibling groups for G = 8 R);
+  // 32 query rows per group up to 32 (8 heads: L <= 4), else 64
+  const int G = Hq / Hkv;
+  const int gv = G < kG ? G : kG;
+  const int gi = gv == 1 ? 0 : gv == 2 ? 1 : gv == 4 ? 2 : 3;
+  const bool rows64 = L * gv > 32, d64 = D == 64;
+  using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
+  // [heads per group 1, 2, 4, 8][64 query rows][D = 64]
+  static const Kern kernels[4][2][2] = {
+      {{verify_tc_kernel<32, 128, 1>, verify_tc_kernel<32, 64, 1>}, {nullptr, nullptr}},
+      {{verify_tc_kernel<32, 128, 2>, verify_tc_kernel<32, 64, 2>}, {nullptr, nullptr}},
+      {{verify_tc_kernel<32, 128, 4>, verify_tc_kernel<32, 64, 4>}, {nullptr, nullptr}},
+      {{verify_tc_kernel<32, 128, 8>, verify_tc_kernel<32, 64, 8>},
+       {verify_tc_kernel<64, 128, 8>, verify_tc_kernel<64, 64, 8>}}};
+  const Kern kern = kernels[gi][rows64][d64];
+  if (kern == nullptr) return SWA_EUNSUPPORTED;   // L * G <= 32 below 8 heads (L <= 8)
   const int smem = rows64 ? Layout<64>::kSmemBytes : Layout<32>::kSmemBytes;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev[dev].vertc_attr[rows64][d64]) {
+    if (!g_dev[dev].vertc_attr[gi][rows64][d64]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            smem);
       if (e != cudaSuccess) {
         set_cuda_error("cudaFuncSetAttribute(verify_tc_kernel)", e);
         return SWA_ECUDA;
       }
-      g_dev[dev].vertc_attr[rows64][d64] = true;
+      g_dev[dev].vertc_attr[gi][rows64][d64] = true;
     }
   }
-  const int rep = Hq / (Hkv * kG);                     // groups of 8 query heads per kv head
+  const int rep = G / gv;                              // query groups per kv head
   const long long rings = (long long)B * Hkv;          // ring units (sequence, kv head)
   const long long units = rings * rep;
   if (rings * kW >= (1LL << 31) || units >= (1LL << 31)) {
@@ -503,7 +523,7 @@ swa_status launch_verify_tc(const void* q, const void* kn, const void* vn, const
   CUtensorMap mk, mv, mq, mkn, mvn;
   if (!make_map_4d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, D, rings * kW, 1, 1, 64, kW, 1) ||
       !make_map_4d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vr, D, rings * kW, 1, 1, 64, kW, 1) ||
-      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, Hq, L, B, 64, kG, L) ||
+      !make_map_4d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, D, Hq, L, B, 64, gv, L) ||
       !make_map_4d(&mkn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kn, D, Hkv, L, B, 64, 1, L) ||
       !make_map_4d(&mvn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vn, D, Hkv, L, B, 64, 1, L))
     return SWA_ECUDA;

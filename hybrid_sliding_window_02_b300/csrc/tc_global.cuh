@@ -5,16 +5,16 @@
 // kernel ("MiMo-V2-Flash Technical Report" summary, section 前置知识: the
 // global layers of the hybrid stack attend to the whole causal prefix; every
 // head adds a learnable bias to its softmax denominator), for bf16 inputs,
-// D = 64 or 128 and 4 or any multiple of 8 query heads per kv head, any
-// window W (W >= T is the global layer).  Keys are visited in blocks of 128 with an online softmax:
+// D = 64 or 128 and 1, 2, 4 or any multiple of 8 query heads per kv head,
+// any window W (W >= T is the global layer).  Keys are visited in blocks of 128 with an online softmax:
 // the running max starts at the sink logit and the running denominator at
 // exp(sink - max), so the sink is counted exactly once whatever the order.
 //
 // Work item = one group of 8 query heads of one sequence x 32 consecutive
 // positions, split into two Q tiles of 16 positions x 8 heads (128 MMA rows
-// each, row r = position r / 8, head r % 8); with 4 query heads per kv head,
-// 64 positions in two tiles of 32 positions x 4 heads (row r = position
-// r / 4, head r % 4).  Both tiles share every K/V block the CTA
+// each, row r = position r / 8, head r % 8); with G = 1, 2 or 4 query heads
+// per kv head, 256 / G positions in two tiles of 128 / G positions x G heads
+// (row r = position r / G, head r % G).  Both tiles share every K/V block the CTA
 // loads, which halves the K/V traffic out of L2 against one tile per block.
 // Items go to persistent CTAs (one per SM), dealt round by round in
 // alternating direction, in an order whose item lengths change smoothly
@@ -68,7 +68,7 @@ namespace tcglobal {
 
 constexpr int kThreads = 352;
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpPv = 10;
-constexpr int kG = 8;                   // query heads per tile (one kv group), or 4 when G = 4
+constexpr int kG = 8;                   // query heads per tile (one kv group), or G = 1, 2, 4
 constexpr int kTiles = 2;               // Q tiles per work item
 // positions per Q tile and per work item for kGt heads per tile (128 rows)
 __host__ __device__ constexpr int npos_for(int kGt) { return 128 / kGt; }
@@ -225,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap map_k,
                              const __grid_constant__ CUtensorMap map_v, const Params p) {
   static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");
-  static_assert(kGt == 8 || (kGt == 4 && !kScores), "8 heads per tile, or 4 without block scores");
+  static_assert(kGt == 8 || ((kGt == 1 || kGt == 2 || kGt == 4) && !kScores),
+                "8 heads per tile, or 1, 2 or 4 without block scores");
   constexpr int kNpos = npos_for(kGt);   // positions per Q tile: row r = position r / kGt, head r % kGt
   constexpr int kHalves = kHd / 64;   // 64-dimension halves of q, k, v rows
   using C = Cols<kHd>;

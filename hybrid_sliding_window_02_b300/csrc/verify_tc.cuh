@@ -3,9 +3,10 @@
 //
 // Operation: as in verify.cuh (drafted tokens at positions pos .. pos+L-1
 // checked in one pass; "MiMo-V2-Flash Technical Report" summary, section
-// 核心方法), for bf16 inputs, D = 64 or 128, W = 128, 8 query heads per kv
-// head (or a multiple of 8, as sibling groups of 8) and L <= 8 drafted
-// tokens.  Per group (sequence b, kv head g) the 8L query rows
+// 核心方法), for bf16 inputs, D = 64 or 128, W = 128, 1, 2, 4 or 8 query
+// heads per kv head (or a multiple of 8, as sibling groups of 8) and L <= 8
+// drafted tokens.  Per group (sequence b, kv head g) the 8L query rows (GL
+// for G < 8)
 // r = 8 j + h (token j, head h) sit in the first lanes of a 128-row tile:
 //   S = Q K_ring^T             tcgen05 SS, M = 128 rows, N = 128 slots, K = 128
 //   S_new = Q K_new^T          tcgen05 SS, N = 16 (the L <= 8 drafted keys;
@@ -111,7 +112,7 @@ struct Params {
 };
 
 // Group u of the call: ring unit ur = (sequence b, kv head g), and the query
-// heads [gq kG, gq kG + kG) it serves.  With G = 8 R the R sibling groups of
+// heads [gq kGv, gq kGv + kGv) it serves.  With G = 8 R the R sibling groups of
 // a kv head each read its rings and drafted keys and values; the siblings
 // are consecutive, so neighbouring CTAs take them in the same round and the
 // later reads come from L2.
@@ -132,8 +133,9 @@ struct GroupCoords {
 
 // kRows query rows per group (32 or 64), head dimension kHd (64 or 128: with
 // 64 only the first 64-dimension half of each staging buffer is loaded, the
-// score products are 4 K-steps deep and PV has N = 64).
-template <int kRows, int kHd>
+// score products are 4 K-steps deep and PV has N = 64), kGv query heads per
+// group (8, or G = 1, 2, 4 with kRows = 32): row r = kGv j + h.
+template <int kRows, int kHd, int kGv>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v,
@@ -154,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kBarOFull = Lay::kBarOFull, kBarODone = Lay::kBarODone,
                 kBarDrain = Lay::kBarDrain;
   constexpr int kSoftWarps = kRows / 32;        // softmax warps per warpgroup
+  static_assert(kGv == 8 || ((kGv == 1 || kGv == 2 || kGv == 4) && kRows == 32),
+                "8 query heads per group, or 1, 2 or 4 in 32 rows");
   static_assert(kHd == 64 || kHd == 128, "head dimension 64 or 128");
   constexpr int kHalves = kHd / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProducer) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      const uint32_t kbytes = kHalves * (kHalf + 8 * L * 128 + L * 128);
+      const uint32_t kbytes = kHalves * (kHalf + kGv * L * 128 + L * 128);
       const uint32_t vbytes = kHalves * (kHalf + L * 128);
       int nkld = 0, nvld = 0;  // K / V slot loads issued
       for (int k = 0; k < nk; ++k) {
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(kb, kbytes);
 #pragma unroll
         for (int hf = 0; hf < kHalves; ++hf) {
-          tma_load_4d(kst + kKQ + hf * kQHalf, &map_q, 64 * hf, gc.gq * kG, 0, b, kb);
+          tma_load_4d(kst + kKQ + hf * kQHalf, &map_q, 64 * hf, gc.gq * kGv, 0, b, kb);
           tma_load_4d(kst + kKK + hf * kHalf, &map_k, 64 * hf, gc.ur * kW, 0, 0, kb);
           tma_load_4d(kst + kKKn + hf * kKnHalf, &map_kn, 64 * hf, g, 0, b, kb);
         }
@@ -351,18 +355,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int w = warp >> 2;                       // warpgroup: groups k with k % 2 == w
     const int wq = warp & 3;                       // warp within the warpgroup
-    const int nrow = kG * L;
+    const int nrow = kGv * L;
     if (wq < kSoftWarps) {
       // ============ softmax + output: thread = row r (TMEM lane r) ============
       const int r = 32 * wq + lane;
       const uint32_t lane_addr = (uint32_t)(32 * wq) << 16;
-      const int j = r >> 3, h = r & 7;
+      const int j = r / kGv, h = r % kGv;
       const uint32_t s_addr = tmem + lane_addr + col_s(w), o_addr = tmem + lane_addr + col_o(w);
       for (int k = w; k < nk; k += 2) {
         const GroupCoords gc((int)blockIdx.x + k * (int)gridDim.x, p);
-        const int b = gc.b, g = gc.gq;   // g: the query group (heads g kG ..)
+        const int b = gc.b, g = gc.gq;   // g: the query group (heads g kGv ..)
         const int64_t p0 = p.pos[b];
-        const float sk = p.sink[g * kG + h] * 1.4426950408889634f;
+        const float sk = p.sink[g * kGv + h] * 1.4426950408889634f;
         if (!mbar_wait(bar(kBarSFull + w), ((uint32_t)k >> 1) & 1, kErrWaitSFull, abort_flag))
           break;
         tc_fence_after();
@@ -409,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   fmaxf(m8[6], m8[7])) * p.scale_log2;
         // new key i of row j counts when it exists (i < L), is causal (i <= j)
         // and the sequence is live (pos >= 0)
-        constexpr int kNew = kRows / kG;            // new keys a row may see: 4 or 8
+        // new keys a row may see: 4 or 8 (at most the 8 drafted tokens)
+        constexpr int kNew = kRows / kGv < kLmax ? kRows / kGv : kLmax;
         float sv[kNew];
 #pragma unroll
         for (int i = 0; i < kNew; ++i)
@@ -463,13 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(kBarPFull + w));
         if (r < nrow && p.lse != nullptr)
-          p.lse[((int64_t)b * p.Hq + g * kG + h) * L + j] = (m + __log2f(l)) * 0.6931471805599453f;
+          p.lse[((int64_t)b * p.Hq + g * kGv + h) * L + j] = (m + __log2f(l)) * 0.6931471805599453f;
         // ---- output row: O / l ----
         if (!mbar_wait(bar(kBarOFull + w), ((uint32_t)k >> 1) & 1, kErrWaitOFull, abort_flag))
           break;
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        float* orow = p.out + (((int64_t)b * L + j) * p.Hq + g * kG + h) * kHd;
+        float* orow = p.out + (((int64_t)b * L + j) * p.Hq + g * kGv + h) * kHd;
 #pragma unroll
         for (int c = 0; c < kHd / 32; ++c) {
           uint32_t o[32];

@@ -321,9 +321,9 @@ swa_status swa_sink_sparse_fwd(const void* q, const void* k, const void* v, cons
 /* Name of the prefill kernel swa_sink_fwd would launch for these sizes, or
  * "invalid": bf16 inputs take "tc_swa" (the sliding-window tensor-core kernel)
  * when W <= 129 and Hq / Hkv is 4 or a multiple of 8 up to 512 (D = 64 or
- * 128), and "tc_global" (the online-softmax tensor-core kernel) when W > 129
- * and Hq / Hkv is 4 or a multiple of 8 (D = 64 or 128); everything else takes
- * "simt" (CUDA cores, fp32 or bf16 inputs). */
+ * 128), and "tc_global" (the online-softmax tensor-core kernel, any window)
+ * for the other bf16 cases with Hq / Hkv 1, 2, 4 or a multiple of 8 (D = 64
+ * or 128); everything else takes "simt" (CUDA cores, fp32 or bf16 inputs). */
 const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Name of the decode kernel swa_sink_decode would launch for these sizes
@@ -333,8 +333,8 @@ const char* swa_sink_fwd_path(int B, int T, int Hq, int Hkv, int D, int W, swa_d
 const char* swa_sink_decode_path(int B, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Name of the verify kernel swa_sink_verify would launch ("tc_verify" for
- * bf16, D = 64 or 128, W = 128, Hq a multiple of 8 Hkv (groups of 8 heads)
- * and L <= 8; "simt_verify" otherwise), or "invalid". */
+ * bf16, D = 64 or 128, W = 128, Hq / Hkv 1, 2, 4 or a multiple of 8 (groups
+ * of 8 heads) and L <= 8; "simt_verify" otherwise), or "invalid". */
 const char* swa_sink_verify_path(int B, int L, int Hq, int Hkv, int D, int W, swa_dtype in_dtype);
 
 /* Static text for a status code. */

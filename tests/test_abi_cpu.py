@@ -53,14 +53,15 @@ def test_path_selection(L):
     assert swa.fwd_path(1, 32768, 64, 8, 128, 32768) == "tc_global"
     assert swa.fwd_path(1, 512, 4, 1, 64, 128, swa.SWA_F32) == "simt"
     assert swa.fwd_path(1, 512, 64, 8, 128, 128, swa.SWA_F32) == "simt"
-    assert swa.fwd_path(1, 512, 64, 64, 128, 128) == "simt"
+    assert swa.fwd_path(1, 512, 64, 64, 128, 128) == "tc_global"   # 1 head per kv head: any window
     assert swa.fwd_path(1, 512, 16, 4, 128, 128) == "tc_swa"       # 4 heads per kv head
     assert swa.fwd_path(1, 512, 16, 4, 128, 130) == "tc_global"    # ... and on the global kernel
-    assert swa.fwd_path(1, 512, 8, 4, 128, 512) == "simt"           # 2 heads per kv head
+    assert swa.fwd_path(1, 512, 8, 4, 128, 512) == "tc_global"      # 2 heads per kv head
+    assert swa.fwd_path(1, 512, 9, 3, 128, 512) == "simt"           # 3
     assert swa.fwd_path(1, 512, 64, 4, 128, 128) == "tc_swa"       # 16: two groups of 8
     assert swa.fwd_path(1, 512, 64, 4, 128, 512) == "tc_global"
     assert swa.fwd_path(1, 512, 48, 2, 128, 128) == "tc_swa"       # 24
-    assert swa.fwd_path(1, 512, 32, 16, 128, 128) == "simt"        # 2 heads per kv head
+    assert swa.fwd_path(1, 512, 32, 16, 128, 128) == "tc_global"   # 2 heads per kv head, W 128
     assert swa.fwd_path(1, 512, 12, 1, 128, 128) == "simt"         # 12: not a multiple of 8
     assert swa.fwd_path(1, 512, 64, 8, 64, 128) == "tc_swa"        # head dimension 64
     assert swa.fwd_path(1, 512, 16, 4, 64, 128) == "tc_swa"
@@ -169,7 +170,10 @@ def test_verify_path_selection(L):
     assert swa.verify_path(2, 65, 8, 1, 128, 128) == "invalid"
     assert swa.verify_path(2, 4, 64, 4, 128, 128) == "tc_verify"    # 16 heads per kv head
     assert swa.verify_path(2, 8, 96, 4, 64, 128) == "tc_verify"     # 24
-    assert swa.verify_path(2, 4, 32, 8, 128, 128) == "simt_verify"  # 4
+    assert swa.verify_path(2, 4, 32, 8, 128, 128) == "tc_verify"    # 4
+    assert swa.verify_path(2, 8, 16, 8, 64, 128) == "tc_verify"     # 2
+    assert swa.verify_path(2, 8, 8, 8, 128, 128) == "tc_verify"     # 1
+    assert swa.verify_path(2, 4, 24, 8, 128, 128) == "simt_verify"  # 3
 
 
 @pytest.mark.parametrize("args,status", [

@@ -169,6 +169,23 @@ def test_tc_global_four_heads_per_kv_head(cuda_ok, B, T, Hq, Hkv, D, W):
     assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(l16, l32)
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [
+    (1, 700, 2, 1, 128, 700),      # 2 heads per kv head: tiles of 64 positions x 2 heads
+    (2, 600, 8, 4, 64, 128),       # the sliding window on this kernel (its tiles do not fit G = 2)
+    (1, 900, 4, 4, 128, 900),      # 1 head per kv head: tiles of 128 positions
+    (2, 400, 2, 2, 128, 33),       # 1 head, narrow window
+    (1, 1000, 8, 8, 64, 300),
+])
+def test_tc_global_one_and_two_heads_per_kv_head(cuda_ok, B, T, Hq, Hkv, D, W):
+    assert swa.fwd_path(B, T, Hq, Hkv, D, W) == "tc_global"
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=2500 + T + W + D + Hq)
+    o32, l32 = _full_check(x, W)
+    o16, l16 = swa.swa_sink_fwd(*(t.cuda() for t in (x.q, x.k, x.v, x.sink)), W,
+                                out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(l16, l32)
+
+
 def test_tc_global_four_heads_per_kv_head_sampled(cuda_ok):
     # B1 T16384 Hq32 Hkv8 D128 global layer: 10 edge positions plus 54 drawn
     # over the causal range, every head

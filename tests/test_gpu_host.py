@@ -29,7 +29,8 @@ def _device_call(x, W, out_dtype=torch.float32):
     (1, 77, 8, 1, 128, 128),
     (2, 8192, 64, 8, 128, 128),   # the bench's shapes, two sequences: 8 chunks each
     (4, 8192, 64, 8, 128, 128),   # the bench's end-to-end workload: 4 chunks of 2048 each
-    (2, 77, 2, 1, 64, 33),        # general kernel, lse slabs not 16-byte aligned: one chunk
+    (2, 77, 3, 1, 64, 33),        # general kernel, lse slabs not 16-byte aligned: one chunk
+    (2, 300, 2, 1, 128, 128),     # 2 heads per kv head, W 128: the online-softmax kernel
     (1, 5000, 16, 4, 128, 128),   # 4 heads per kv head: position chunks of whole 32-position tiles
     (2, 1500, 64, 4, 128, 128),   # 16 heads per kv head (two groups of 8)
     (2, 2600, 64, 8, 64, 128),    # head dimension 64

@@ -167,7 +167,7 @@ def test_simt_fp32_shapes(cuda_ok, B, T, Hq, Hkv, D, W):
 
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,D,W", [
-    (1, 300, 2, 1, 128, 128), (2, 100, 8, 8, 64, 33), (1, 200, 2, 1, 128, 200),
+    (1, 300, 3, 1, 128, 128), (2, 100, 6, 2, 64, 33), (1, 200, 3, 1, 128, 200),
     (1, 150, 12, 1, 128, 128), (1, 180, 12, 1, 64, 180),
 ])
 def test_simt_bf16_shapes(cuda_ok, B, T, Hq, Hkv, D, W):
@@ -280,8 +280,8 @@ def test_bf16_output_is_rounded_fp32_output(cuda_ok, B, T, Hq, Hkv, W):
 
 
 def test_bf16_output_needs_a_tensor_core_path(cuda_ok):
-    x = gen.prefill_inputs(1, 64, 2, 1, 128, seed=9, device="cuda")
-    assert swa.fwd_path(1, 64, 2, 1, 128, 128) == "simt"
+    x = gen.prefill_inputs(1, 64, 3, 1, 128, seed=9, device="cuda")
+    assert swa.fwd_path(1, 64, 3, 1, 128, 128) == "simt"
     with pytest.raises(swa.SwaError) as e:
         swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, 128, out_dtype=torch.bfloat16)
     assert e.value.status == swa.SWA_EUNSUPPORTED

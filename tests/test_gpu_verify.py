@@ -103,6 +103,23 @@ def test_verify_tc_sibling_groups(cuda_ok, B, L, Hq, Hkv, D):
     assert swa.device_error() == 0
 
 
+@pytest.mark.parametrize("B,L,Hq,Hkv,D", [(19, 4, 16, 4, 128), (13, 8, 32, 8, 64),
+                                          (21, 3, 8, 4, 128), (9, 8, 4, 4, 128),
+                                          (150, 5, 8, 2, 128)])
+def test_verify_tc_small_groups(cuda_ok, B, L, Hq, Hkv, D):
+    # 4, 2 and 1 query heads per kv head: rows r = G j + h of one 32-row
+    # group; B = 150 with 2 kv heads gives CTAs 2 or 3 groups
+    assert swa.verify_path(B, L, Hq, Hkv, D, 128) == "tc_verify"
+    x = gen.verify_inputs(B, L, Hq, Hkv, D, 128, seed=B + L + Hq + 7, pos_lo=0, pos_hi=700)
+    for b in range(B):
+        p = int(x.pos[b])
+        if p < 128:
+            x.k_ring[b, :, p:] = float("nan")
+            x.v_ring[b, :, p:] = float("nan")
+    _check(x)
+    assert swa.device_error() == 0
+
+
 def test_verify_eight_drafts_equal_prefill_rows(cuda_ok):
     B, T, Hq, Hkv, D, W, L = 2, 600, 16, 2, 128, 128, 8
     x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=64, device="cuda")
