@@ -6,16 +6,18 @@
 // global layers of the hybrid stack attend to the whole causal prefix; every
 // head adds a learnable bias to its softmax denominator), for bf16 inputs,
 // D = 64 or 128 and 1, 2, 4 or any multiple of 8 query heads per kv head,
-// any window W (W >= T is the global layer).  Keys are visited in blocks of 128 with an online softmax:
-// the running max starts at the sink logit and the running denominator at
-// exp(sink - max), so the sink is counted exactly once whatever the order.
+// any window W (W >= T is the global layer).  Keys are visited in blocks of
+// 128 with an online softmax: the running max starts at the sink logit and
+// the running denominator at exp(sink - max), so the sink is counted exactly
+// once whatever the order.
 //
 // Work item = one group of 8 query heads of one sequence x 32 consecutive
 // positions, split into two Q tiles of 16 positions x 8 heads (128 MMA rows
 // each, row r = position r / 8, head r % 8); with G = 1, 2 or 4 query heads
 // per kv head, 256 / G positions in two tiles of 128 / G positions x G heads
-// (row r = position r / G, head r % G).  Both tiles share every K/V block the CTA
-// loads, which halves the K/V traffic out of L2 against one tile per block.
+// (row r = position r / G, head r % G).  Both tiles share every K/V block
+// the CTA loads, which halves the K/V traffic out of L2 against one tile per
+// block.
 // Items go to persistent CTAs (one per SM), dealt round by round in
 // alternating direction, in an order whose item lengths change smoothly
 // (item_coords), which keeps the per-CTA totals within about one item of
@@ -37,10 +39,11 @@
 // and PV products issued from two threads, one thread's waits are covered by
 // the other's MMAs; each accumulator still receives its MMAs in order, so the
 // results are unchanged.
-// TMEM (D = 128): S [0,128) shared by the two tiles, P0 [128,192), P1 [192,256) (bf16
-// pairs), O0 [256,256+D), O1 [384,384+D).  S goes to one buffer that each softmax
-// empties into registers at once, so an S waits only for the other tile's
-// read of the previous one, and P never shares columns with S.  A softmax
+// TMEM (D = 128): S [0,128) shared by the two tiles, P0 [128,192), P1
+// [192,256) (bf16 pairs), O0 [256,384), O1 [384,512).  S goes to one buffer
+// that each softmax empties into registers at once, so an S waits only for
+// the other tile's read of the previous one, and P never shares columns
+// with S.  A softmax
 // rewrites P_i (and rescales O_i) only after the tile's previous PV has
 // completed, which it learns from a commit barrier.
 //
