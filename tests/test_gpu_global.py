@@ -175,6 +175,9 @@ def test_tc_global_four_heads_per_kv_head(cuda_ok, B, T, Hq, Hkv, D, W):
     (1, 900, 4, 4, 128, 900),      # 1 head per kv head: tiles of 128 positions
     (2, 400, 2, 2, 128, 33),       # 1 head, narrow window
     (1, 1000, 8, 8, 64, 300),
+    (1, 1, 2, 2, 128, 128),        # a single position
+    (3, 5, 4, 2, 64, 1),           # W = 1: each row sees only its own key
+    (1, 257, 2, 1, 128, 257),      # one item (256 positions) and one position of the next
 ])
 def test_tc_global_one_and_two_heads_per_kv_head(cuda_ok, B, T, Hq, Hkv, D, W):
     assert swa.fwd_path(B, T, Hq, Hkv, D, W) == "tc_global"
