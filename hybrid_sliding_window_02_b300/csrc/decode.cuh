@@ -13,7 +13,10 @@
 // the G query rows of the group into shared memory, so the whole 64 KB per CTA
 // is in flight at once; scores start as soon as keys and queries land, while
 // values are still arriving.  Eight warps then compute the G x W scores,
-// the sink-seeded softmax and the G x D outputs from shared memory.
+// the sink-seeded softmax and the G x D outputs from shared memory.  G is
+// 1, 2, 4, 8 or 16 per CTA; a kv head with another number of query heads runs
+// as sibling CTAs of the largest of those that divides it, each reading the
+// rings.
 #pragma once
 
 #include "device_common.cuh"
@@ -75,15 +78,18 @@ template <typename Tin, int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k_ring, const Tin* __restrict__ v_ring,
     const int64_t* __restrict__ pos, const float* __restrict__ sink, float* __restrict__ out,
-    float* __restrict__ lse, int Hq, int Hkv, int W, float scale_log2) {
+    float* __restrict__ lse, int Hq, int Hkv, int W, int rep, float scale_log2) {
   constexpr int EPL = Vec16<Tin>::N;       // elements per 16-byte lane chunk
   constexpr int LPK = D / EPL;             // lanes per key row
   constexpr int KPW = 32 / LPK;            // keys per warp instruction
   extern __shared__ __align__(128) uint8_t smem[];
   const DecodeSmem L = decode_smem_layout<Tin, D, G>(W);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int bk = blockIdx.x;               // b * Hkv + kvh
-  const int b = bk / Hkv, kvh = bk % Hkv;
+  // CTA = (sequence b, kv head, sibling): a kv head's G R query heads run as
+  // R sibling CTAs of G heads each (rep = R), every one reading the rings
+  const int bk = blockIdx.x / rep;         // ring unit b * Hkv + kv head
+  const int b = bk / Hkv;
+  const int qg = (bk % Hkv) * rep + (int)(blockIdx.x % rep);   // query group: heads qg G ..
   const uint32_t bar_kq = smem_u32(smem + L.bar_off);
   const uint32_t bar_v = bar_kq + 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.bar_off + 16);
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_kq, ring_bytes + q_bytes);
     tma_load_1d(smem_u32(smem + L.k_off), k_ring + (int64_t)bk * ring_elems, ring_bytes, bar_kq);
-    tma_load_1d(smem_u32(smem + L.q_off), q + ((int64_t)b * Hq + kvh * G) * D, q_bytes, bar_kq);
+    tma_load_1d(smem_u32(smem + L.q_off), q + ((int64_t)b * Hq + qg * G) * D, q_bytes, bar_kq);
     mbar_arrive_expect_tx(bar_v, ring_bytes);
     tma_load_1d(smem_u32(smem + L.v_off), v_ring + (int64_t)bk * ring_elems, ring_bytes, bar_v);
   }
@@ -176,7 +182,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
   float* linv = reinterpret_cast<float*>(smem + L.linv_off);
   if (kq_ok) {
     for (int g = warp; g < G; g += kDecodeWarps) {
-      const int h = kvh * G + g;
+      const int h = qg * G + g;
       const float sk = sink[h] * 1.4426950408889634f;  // log2(e)
       float m = sk;
       for (int s = lane; s < W; s += 32) {
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
   }
   __syncthreads();
   if (v_ok) {
-    float* ob = out + ((int64_t)b * Hq + kvh * G) * D;
+    float* ob = out + ((int64_t)b * Hq + qg * G) * D;
     for (int o = tid; o < G * D; o += kDecodeThreads) {
       float a = 0.f;
 #pragma unroll

@@ -376,7 +376,7 @@ swa_status launch_tc_global(const void* q, const void* k, const void* v, const f
 template <typename Tin, int D, int G>
 swa_status launch_decode_t(const void* q, const void* kr, const void* vr, const int64_t* pos,
                            const float* sink, float* out, float* lse, int B, int Hq, int Hkv,
-                           int W, cudaStream_t st, bool* attr_done) {
+                           int W, int rep, cudaStream_t st, bool* attr_done) {
   const swa::DecodeSmem L = swa::decode_smem_layout<Tin, D, G>(W);
   auto kern = swa::decode_kernel<Tin, D, G>;
   if (!*attr_done) {
@@ -389,9 +389,9 @@ swa_status launch_decode_t(const void* q, const void* kr, const void* vr, const 
     *attr_done = true;
   }
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  kern<<<(unsigned)(B * Hkv), swa::kDecodeThreads, L.total, st>>>(
+  kern<<<(unsigned)(B * Hkv * rep), swa::kDecodeThreads, L.total, st>>>(
       static_cast<const Tin*>(q), static_cast<const Tin*>(kr), static_cast<const Tin*>(vr), pos,
-      sink, out, lse, Hq, Hkv, W, scale_log2);
+      sink, out, lse, Hq, Hkv, W, rep, scale_log2);
   return check_launch("decode_kernel");
 }
 
@@ -547,21 +547,19 @@ template <typename Tin, int D>
 swa_status launch_decode_g(const void* q, const void* kr, const void* vr, const int64_t* pos,
                            const float* sink, float* out, float* lse, int B, int Hq, int Hkv,
                            int W, cudaStream_t st, int dev) {
+  // heads per CTA: the largest of 16, 8, 4, 2, 1 that divides G; a kv head's
+  // G heads then run as rep = G / Gc sibling CTAs
   const int G = Hq / Hkv;
+  const int Gc = G % 16 == 0 ? 16 : G % 8 == 0 ? 8 : G % 4 == 0 ? 4 : G % 2 == 0 ? 2 : 1;
+  const int rep = G / Gc;
+  if ((long long)B * Hkv * rep >= (1LL << 31)) {
+    set_error_text("problem too large for the decode kernel");
+    return SWA_EUNSUPPORTED;
+  }
   const int ti = std::is_same<Tin, float>::value ? 0 : 1;
   const int di = D == 64 ? 0 : 1;
   bool* attr = nullptr;
-  int gi;
-  switch (G) {
-    case 1: gi = 0; break;
-    case 2: gi = 1; break;
-    case 4: gi = 2; break;
-    case 8: gi = 3; break;
-    case 16: gi = 4; break;
-    default:
-      set_error_text("decode supports Hq/Hkv in {1, 2, 4, 8, 16}");
-      return SWA_EUNSUPPORTED;
-  }
+  const int gi = Gc == 1 ? 0 : Gc == 2 ? 1 : Gc == 4 ? 2 : Gc == 8 ? 3 : 4;
   bool done;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -569,12 +567,12 @@ swa_status launch_decode_g(const void* q, const void* kr, const void* vr, const 
   }
   attr = &done;
   swa_status s;
-  switch (G) {
-    case 1: s = launch_decode_t<Tin, D, 1>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
-    case 2: s = launch_decode_t<Tin, D, 2>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
-    case 4: s = launch_decode_t<Tin, D, 4>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
-    case 8: s = launch_decode_t<Tin, D, 8>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
-    default: s = launch_decode_t<Tin, D, 16>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, st, attr); break;
+  switch (Gc) {
+    case 1: s = launch_decode_t<Tin, D, 1>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, rep, st, attr); break;
+    case 2: s = launch_decode_t<Tin, D, 2>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, rep, st, attr); break;
+    case 4: s = launch_decode_t<Tin, D, 4>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, rep, st, attr); break;
+    case 8: s = launch_decode_t<Tin, D, 8>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, rep, st, attr); break;
+    default: s = launch_decode_t<Tin, D, 16>(q, kr, vr, pos, sink, out, lse, B, Hq, Hkv, W, rep, st, attr); break;
   }
   if (done) {
     std::lock_guard<std::mutex> lk(g_dev_mu);

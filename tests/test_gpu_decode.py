@@ -70,6 +70,9 @@ def test_decode_tc_head_dim_64(cuda_ok, B, Hq, Hkv):
     (3, 8, 1, 128, 128, torch.bfloat16), (5, 16, 1, 64, 64, torch.bfloat16),
     (4, 4, 2, 128, 33, torch.bfloat16), (2, 16, 16, 64, 7, torch.bfloat16),
     (3, 8, 1, 128, 128, torch.float32), (2, 4, 4, 64, 300, torch.float32),
+    (3, 24, 8, 128, 64, torch.bfloat16),    # 3 heads per kv head: three 1-head sibling CTAs
+    (2, 48, 2, 64, 33, torch.bfloat16),     # 24: three 8-head siblings
+    (2, 12, 1, 128, 100, torch.float32),    # 12: three 4-head siblings
 ])
 def test_decode_shapes(cuda_ok, B, Hq, Hkv, D, W, dt):
     x = gen.decode_inputs(B, Hq, Hkv, D, W, seed=B + W, dtype=dt, pos_lo=0, pos_hi=4 * W)

@@ -1,0 +1,99 @@
+"""Seeded random shapes through every path selection: prefill (each kernel the
+sizes pick, bf16 and fp32), decode and verify, each compared element by element
+with the fp64 oracle.  The draws mix group sizes the tensor-core kernels take
+with ones they do not, windows on both sides of the sliding-window kernel's
+limit, ragged lengths and partial rings."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import hybrid_sliding_window_02_b300 as swa
+from hybrid_sliding_window_02_b300 import inputs as gen
+from gpu_helpers import assert_bf16_close, assert_f32_close, assert_lse_close
+
+pytestmark = pytest.mark.gpu
+
+GROUPS = (1, 2, 3, 4, 8, 16, 24)
+
+
+def _prefill_case(seed):
+    g = np.random.default_rng(seed)
+    G = int(g.choice(GROUPS))
+    Hkv = int(g.integers(1, 4))
+    D = int(g.choice((64, 128)))
+    T = int(g.integers(1, 700))
+    B = int(g.integers(1, 4))
+    W = int(g.choice((1, 17, 128, 129, 130, 300, T, T + 5)))
+    fp32 = bool(g.random() < 0.25)
+    return B, T, G * Hkv, Hkv, D, max(W, 1), fp32
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_prefill_shape(cuda_ok, seed):
+    B, T, Hq, Hkv, D, W, fp32 = _prefill_case(seed)
+    dt = torch.float32 if fp32 else torch.bfloat16
+    path = swa.fwd_path(B, T, Hq, Hkv, D, W, swa.SWA_F32 if fp32 else swa.SWA_BF16)
+    assert path in ("tc_swa", "tc_global", "simt")
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7000 + seed, dtype=dt)
+    out, lse = swa.swa_sink_fwd(*(t.cuda() for t in (x.q, x.k, x.v, x.sink)), W)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+    if fp32:
+        assert_f32_close(out.cpu().double().numpy(), o_ref, what=f"out ({path})")
+        assert_f32_close(lse.cpu().double().numpy(), l_ref, what=f"lse ({path})")
+    else:
+        assert_bf16_close(out.cpu().numpy(), o_ref, what=f"out ({path})")
+        assert_lse_close(lse.cpu().numpy(), l_ref)
+    assert swa.device_error() == 0
+
+
+def _ring_case(seed):
+    g = np.random.default_rng(seed)
+    G = int(g.choice(GROUPS))
+    Hkv = int(g.integers(1, 4))
+    D = int(g.choice((64, 128)))
+    B = int(g.integers(1, 60))
+    W = int(g.choice((128, 128, 64, 33)))
+    L = int(g.integers(1, 9))
+    return B, G * Hkv, Hkv, D, W, L
+
+
+def _poison_empty_slots(x, ring_pos):
+    # slots past the newest ring position of a young sequence are empty and
+    # may hold anything
+    W = x.k_ring.shape[2]
+    for b in range(x.k_ring.shape[0]):
+        p = int(ring_pos[b])          # -1: an empty ring
+        if p < W - 1:
+            x.k_ring[b, :, p + 1:] = float("nan")
+            x.v_ring[b, :, p + 1:] = float("nan")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_decode_shape(cuda_ok, seed):
+    B, Hq, Hkv, D, W, _ = _ring_case(seed)
+    x = gen.decode_inputs(B, Hq, Hkv, D, W, seed=7100 + seed, pos_lo=0, pos_hi=4 * W)
+    _poison_empty_slots(x, x.pos)
+    out, lse = swa.swa_sink_decode(*(t.cuda() for t in (x.q, x.k_ring, x.v_ring, x.pos, x.sink)))
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.swa_sink_decode(x.q, x.k_ring, x.v_ring, x.pos, x.sink)
+    path = swa.decode_path(B, Hq, Hkv, D, W)
+    assert_bf16_close(out.cpu().double().numpy(), o_ref, what=f"out ({path})")
+    assert_lse_close(lse.cpu().double().numpy(), l_ref)
+    assert swa.device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_verify_shape(cuda_ok, seed):
+    B, Hq, Hkv, D, W, L = _ring_case(seed + 100)
+    x = gen.verify_inputs(B, L, Hq, Hkv, D, W, seed=7200 + seed, pos_lo=0, pos_hi=4 * W)
+    _poison_empty_slots(x, x.pos - 1)   # the ring holds the tokens before pos
+    args = (x.q, x.k_new, x.v_new, x.k_ring, x.v_ring, x.pos, x.sink)
+    out, lse = swa.swa_sink_verify(*(t.cuda() for t in args))
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.swa_sink_verify(*args)
+    path = swa.verify_path(B, L, Hq, Hkv, D, W)
+    assert_bf16_close(out.cpu().double().numpy(), o_ref, what=f"out ({path})")
+    assert_lse_close(lse.cpu().double().numpy(), l_ref)
+    assert swa.device_error() == 0
