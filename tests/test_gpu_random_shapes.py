@@ -1,6 +1,7 @@
 """Seeded random shapes through every path selection: prefill (each kernel the
-sizes pick, bf16 and fp32), decode and verify, each compared element by element
-with the fp64 oracle.  The draws mix group sizes the tensor-core kernels take
+sizes pick, bf16 and fp32), decode, verify and the host-memory prefill, each
+compared element by element with the fp64 oracle (the host-memory prefill bit
+for bit with the device call).  The draws mix group sizes the tensor-core kernels take
 with ones they do not, windows on both sides of the sliding-window kernel's
 limit, ragged lengths and partial rings."""
 import numpy as np
@@ -29,7 +30,7 @@ def _prefill_case(seed):
     return B, T, G * Hkv, Hkv, D, max(W, 1), fp32
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", range(32))
 def test_random_prefill_shape(cuda_ok, seed):
     B, T, Hq, Hkv, D, W, fp32 = _prefill_case(seed)
     dt = torch.float32 if fp32 else torch.bfloat16
@@ -70,7 +71,7 @@ def _poison_empty_slots(x, ring_pos):
             x.v_ring[b, :, p + 1:] = float("nan")
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_decode_shape(cuda_ok, seed):
     B, Hq, Hkv, D, W, _ = _ring_case(seed)
     x = gen.decode_inputs(B, Hq, Hkv, D, W, seed=7100 + seed, pos_lo=0, pos_hi=4 * W)
@@ -84,7 +85,7 @@ def test_random_decode_shape(cuda_ok, seed):
     assert swa.device_error() == 0
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_verify_shape(cuda_ok, seed):
     B, Hq, Hkv, D, W, L = _ring_case(seed + 100)
     x = gen.verify_inputs(B, L, Hq, Hkv, D, W, seed=7200 + seed, pos_lo=0, pos_hi=4 * W)
@@ -96,4 +97,17 @@ def test_random_verify_shape(cuda_ok, seed):
     path = swa.verify_path(B, L, Hq, Hkv, D, W)
     assert_bf16_close(out.cpu().double().numpy(), o_ref, what=f"out ({path})")
     assert_lse_close(lse.cpu().double().numpy(), l_ref)
+    assert swa.device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_host_prefill_shape(cuda_ok, seed):
+    B, T, Hq, Hkv, D, W, fp32 = _prefill_case(seed + 500)
+    dt = torch.float32 if fp32 else torch.bfloat16
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7300 + seed, dtype=dt)
+    qh, kh, vh = (t.pin_memory() for t in (x.q, x.k, x.v))
+    out_h, lse_h, _ = swa.swa_sink_fwd_host(qh, kh, vh, x.sink.cuda(), W)
+    out_d, lse_d = swa.swa_sink_fwd(*(t.cuda() for t in (x.q, x.k, x.v, x.sink)), W)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
     assert swa.device_error() == 0
