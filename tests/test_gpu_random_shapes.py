@@ -111,3 +111,32 @@ def test_random_host_prefill_shape(cuda_ok, seed):
     torch.cuda.synchronize()
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
     assert swa.device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_high_sparse_pipeline(cuda_ok, seed):
+    # block scores of a global layer, top-k selection on them, and the sparse
+    # layer on the selection, each step against the oracle on the GPU's own
+    # input to that step
+    g = np.random.default_rng(7400 + seed)
+    B, Hkv = int(g.integers(1, 3)), int(g.integers(1, 3))
+    Hq, D = 8 * Hkv, int(g.choice((64, 128)))
+    T = int(g.integers(1, 1500))
+    QB, topk = int(g.choice((32, 64, 128))), int(g.integers(1, 9))
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7400 + seed)
+    q, k, v, s = (t.cuda() for t in (x.q, x.k, x.v, x.sink))
+    _, _, bm = swa.swa_sink_fwd_scores(q, k, v, s, T)
+    idx = swa.swa_topk_blocks(bm, T, QB, topk)
+    out, lse = swa.swa_sink_sparse_fwd(q, k, v, s, idx, QB)
+    torch.cuda.synchronize()
+    got = bm.cpu().double().numpy()
+    ref = oracle.block_max(x.q, x.k, T)
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+    fin = np.isfinite(ref)
+    if fin.any():
+        assert np.abs(got[fin] - ref[fin]).max() <= 1e-3
+    assert np.array_equal(idx.cpu().numpy(), oracle.topk_blocks(bm.cpu().numpy(), T, QB, topk))
+    o_ref, l_ref = oracle.sparse_fwd(x.q, x.k, x.v, x.sink, idx.cpu().numpy(), QB)
+    assert_bf16_close(out.cpu().numpy(), o_ref)
+    assert_lse_close(lse.cpu().numpy(), l_ref)
+    assert swa.device_error() == 0
