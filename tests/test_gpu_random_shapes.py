@@ -140,3 +140,25 @@ def test_random_high_sparse_pipeline(cuda_ok, seed):
     assert_bf16_close(out.cpu().numpy(), o_ref)
     assert_lse_close(lse.cpu().numpy(), l_ref)
     assert swa.device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_prefill_long(cuda_ok, seed):
+    # longer sequences: many tiles and items per CTA, every element compared
+    g = np.random.default_rng(7500 + seed)
+    G = int(g.choice((1, 2, 4, 8, 16)))
+    Hkv = 1 if G == 16 else int(g.integers(1, 3))
+    D = int(g.choice((64, 128)))
+    T = int(g.integers(1500, 5000))
+    B = int(g.integers(1, 3))
+    W = int(g.choice((128, 1000, T)))
+    Hq = G * Hkv
+    path = swa.fwd_path(B, T, Hq, Hkv, D, W)
+    assert path in ("tc_swa", "tc_global")
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7500 + seed)
+    out, lse = swa.swa_sink_fwd(*(t.cuda() for t in (x.q, x.k, x.v, x.sink)), W)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
+    assert_bf16_close(out.cpu().numpy(), o_ref, what=f"out ({path})")
+    assert_lse_close(lse.cpu().numpy(), l_ref)
+    assert swa.device_error() == 0
