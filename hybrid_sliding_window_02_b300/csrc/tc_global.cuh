@@ -281,9 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_armed[kTiles] = {};  // Q loads issued per tile
       Item it;
       bool ok = true;
+      uint32_t kn = 0;   // items with at least one key block so far
       for (int k = 0; ok && cta_item(k, p, it); ++k) {
+        // an empty block list (sparse mode) has no loads and no MMAs; the
+        // softmax warps write its rows from the sink alone
+        if (it.nb == 0) continue;
         for (int i = 0; i < kTiles; ++i) {
-          if (!mbar_wait(bar(kBarQEmpty + i), (k & 1) ^ 1, kErrWaitQEmpty, abort_flag)) {
+          if (!mbar_wait(bar(kBarQEmpty + i), (kn & 1) ^ 1, kErrWaitQEmpty, abort_flag)) {
             ok = false;
             break;
           }
@@ -329,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(dst, map, 0, it.kvh, key, it.b, fb);
           if constexpr (kHalves == 2) tma_load_4d(dst + kSlotHalf, map, 64, it.kvh, key, it.b, fb);
         }
+        ++kn;
       }
       // Copies still in flight must land before the CTA exits: wait (bounded)
       // for the last phase armed on every barrier a copy signals.
@@ -397,17 +402,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       Item it;
+      uint32_t kn = 0;   // items with at least one key block so far
       for (int k = 0; ok && cta_item(k, p, it); ++k) {
+        if (it.nb == 0) continue;   // no loads, no MMAs
         for (int t = 0; t < it.nb; ++t, ++gblk) {
           uint32_t slot;
           if (s_side) {
             if (!wait_load(2 * gblk, slot)) { ok = false; break; }
-            if (t == 0 && !mbar_wait(bar(kBarQFull + 0), k & 1, kErrWaitQFull, abort_flag)) {
+            if (t == 0 && !mbar_wait(bar(kBarQFull + 0), kn & 1, kErrWaitQFull, abort_flag)) {
               ok = false;
               break;
             }
             if (!issue_s(0, slot)) { ok = false; break; }
-            if (t == 0 && !mbar_wait(bar(kBarQFull + 1), k & 1, kErrWaitQFull, abort_flag)) {
+            if (t == 0 && !mbar_wait(bar(kBarQFull + 1), kn & 1, kErrWaitQFull, abort_flag)) {
               ok = false;
               break;
             }
@@ -423,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(bar(kBarKvEmpty + slot));
           }
         }
+        ++kn;
       }
       // every MMA this thread issued completes before TMEM is released
       const uint32_t db = bar(kBarDrain + (s_side ? 0 : 1));
@@ -441,10 +449,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tmem + lane_addr + C::o(ti);
     const int g = r % kGt;
     uint32_t npv = 0;
+    uint32_t kn = 0;   // items with at least one key block so far
     Item it;
     for (int k = 0; cta_item(k, p, it); ++k) {
       const int h = it.grp * kGt + g;
       const int pos = it.p0 + ti * kNpos + r / kGt;
+      if (it.nb == 0) {
+        // no key block selected: the sink alone, out = 0 and lse = sink
+        if (pos < p.T) {
+          const long long e0 = (((long long)it.b * p.T + pos) * p.Hq + h) * kHd;
+          if constexpr (kBf16Out) {
+            uint32_t* orow = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + e0);
+            for (int e = 0; e < kHd / 8; ++e) st_global_v4(reinterpret_cast<float*>(orow + 4 * e), 0u, 0u, 0u, 0u);
+          } else {
+            float* orow = static_cast<float*>(p.out) + e0;
+            for (int e = 0; e < kHd / 4; ++e) st_global_v4(orow + 4 * e, 0u, 0u, 0u, 0u);
+          }
+          if (p.lse != nullptr) p.lse[((long long)it.b * p.Hq + h) * p.T + pos] = p.sink[h];
+        }
+        continue;
+      }
       const float sk = p.sink[h] * 1.4426950408889634f;  // log2 units
       float m_run = sk;                                   // -inf for no sink
       float l = (sk == -INFINITY) ? 0.f : 1.f;            // exp2(sk - m_run)
@@ -560,7 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: out = O / l, lse ----
-      if (!mbar_wait(bar(kBarOFull + ti), k & 1, kErrWaitOFull, abort_flag)) break;
+      if (!mbar_wait(bar(kBarOFull + ti), kn & 1, kErrWaitOFull, abort_flag)) break;
+      ++kn;
       tc_fence_after();
       const float inv_l = 1.f / l;
       if constexpr (kBf16Out) {

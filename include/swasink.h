@@ -304,7 +304,9 @@ swa_status swa_topk_blocks(const float* scores, int* idx, int B, int T, int Hkv,
  * (the shared KV cache).
  *   idx [B, Hkv, ceil(T/QB), topk] int32: increasing block indices, -1 padded
  *   (as swa_topk_blocks writes them); QB in {32, 64, 128}.  A list is read up
- *   to its first negative entry: entries after it are ignored.  The entries
+ *   to its first negative entry: entries after it are ignored, and a list
+ *   whose first entry is negative selects no key (its rows get out = 0 and
+ *   lse = sink[h], the sink alone).  The entries
  *   before it must be distinct block indices in [0, ceil(T/128)); their
  *   order does not change the result beyond rounding (each key is masked
  *   causally on its own).  A repeated index counts its keys twice; an index

@@ -92,6 +92,28 @@ def test_sparse_block_list_is_read_up_to_its_first_negative_entry(cuda_ok):
     assert swa.device_error() == 0
 
 
+@pytest.mark.parametrize("QB,D", [(64, 128), (32, 64), (128, 128)])
+def test_sparse_empty_block_lists_give_the_sink_alone(cuda_ok, QB, D):
+    # a list that starts with -1 selects no key: those rows get out = 0 and
+    # lse = sink (no wait runs out, and the items after them are unaffected)
+    B, T, Hq, Hkv = 2, 1100, 16, 2
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=4170 + QB)
+    idx = _selection(B, Hkv, T, QB, 3, seed=QB)
+    idx[0, 0, 0, :] = -1                 # the first query block
+    idx[0, 1, 3:6, :] = -1               # consecutive empty lists
+    idx[1, :, -1, :] = -1                # the last (ragged) query block
+    q, k, v, s = (t.cuda() for t in (x.q, x.k, x.v, x.sink))
+    out, lse = swa.swa_sink_sparse_fwd(q, k, v, s, torch.from_numpy(idx).cuda(), QB)
+    o16, l16 = swa.swa_sink_sparse_fwd(q, k, v, s, torch.from_numpy(idx).cuda(), QB,
+                                       out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.sparse_fwd(x.q, x.k, x.v, x.sink, idx, QB)
+    assert_bf16_close(out.cpu().numpy(), o_ref)
+    assert_lse_close(lse.cpu().numpy(), l_ref)
+    assert torch.equal(o16, out.to(torch.bfloat16)) and torch.equal(l16, lse)
+    assert swa.device_error() == 0
+
+
 def test_sparse_with_every_block_is_the_global_kernel(cuda_ok):
     B, T, Hq, Hkv, QB = 1, 1100, 16, 2, 64
     x = gen.prefill_inputs(B, T, Hq, Hkv, 128, seed=4200, device="cuda")
