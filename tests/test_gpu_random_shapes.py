@@ -57,7 +57,18 @@ def _ring_case(seed):
     B = int(g.integers(1, 60))
     W = int(g.choice((128, 128, 64, 33)))
     L = int(g.integers(1, 9))
-    return B, G * Hkv, Hkv, D, W, L
+    fp32 = bool(g.random() < 0.25)
+    return B, G * Hkv, Hkv, D, W, L, fp32
+
+
+def _close(out, lse, o_ref, l_ref, fp32, path):
+    o, l = out.cpu().double().numpy(), lse.cpu().double().numpy()
+    if fp32:
+        assert_f32_close(o, o_ref, what=f"out ({path})")
+        assert_f32_close(l, l_ref, what=f"lse ({path})")
+    else:
+        assert_bf16_close(o, o_ref, what=f"out ({path})")
+        assert_lse_close(l, l_ref)
 
 
 def _poison_empty_slots(x, ring_pos):
@@ -73,30 +84,30 @@ def _poison_empty_slots(x, ring_pos):
 
 @pytest.mark.parametrize("seed", range(24))
 def test_random_decode_shape(cuda_ok, seed):
-    B, Hq, Hkv, D, W, _ = _ring_case(seed)
-    x = gen.decode_inputs(B, Hq, Hkv, D, W, seed=7100 + seed, pos_lo=0, pos_hi=4 * W)
+    B, Hq, Hkv, D, W, _, fp32 = _ring_case(seed)
+    dt = torch.float32 if fp32 else torch.bfloat16
+    x = gen.decode_inputs(B, Hq, Hkv, D, W, seed=7100 + seed, dtype=dt, pos_lo=0, pos_hi=4 * W)
     _poison_empty_slots(x, x.pos)
     out, lse = swa.swa_sink_decode(*(t.cuda() for t in (x.q, x.k_ring, x.v_ring, x.pos, x.sink)))
     torch.cuda.synchronize()
     o_ref, l_ref = oracle.swa_sink_decode(x.q, x.k_ring, x.v_ring, x.pos, x.sink)
-    path = swa.decode_path(B, Hq, Hkv, D, W)
-    assert_bf16_close(out.cpu().double().numpy(), o_ref, what=f"out ({path})")
-    assert_lse_close(lse.cpu().double().numpy(), l_ref)
+    path = swa.decode_path(B, Hq, Hkv, D, W, swa.SWA_F32 if fp32 else swa.SWA_BF16)
+    _close(out, lse, o_ref, l_ref, fp32, path)
     assert swa.device_error() == 0
 
 
 @pytest.mark.parametrize("seed", range(24))
 def test_random_verify_shape(cuda_ok, seed):
-    B, Hq, Hkv, D, W, L = _ring_case(seed + 100)
-    x = gen.verify_inputs(B, L, Hq, Hkv, D, W, seed=7200 + seed, pos_lo=0, pos_hi=4 * W)
+    B, Hq, Hkv, D, W, L, fp32 = _ring_case(seed + 100)
+    dt = torch.float32 if fp32 else torch.bfloat16
+    x = gen.verify_inputs(B, L, Hq, Hkv, D, W, seed=7200 + seed, dtype=dt, pos_lo=0, pos_hi=4 * W)
     _poison_empty_slots(x, x.pos - 1)   # the ring holds the tokens before pos
     args = (x.q, x.k_new, x.v_new, x.k_ring, x.v_ring, x.pos, x.sink)
     out, lse = swa.swa_sink_verify(*(t.cuda() for t in args))
     torch.cuda.synchronize()
     o_ref, l_ref = oracle.swa_sink_verify(*args)
-    path = swa.verify_path(B, L, Hq, Hkv, D, W)
-    assert_bf16_close(out.cpu().double().numpy(), o_ref, what=f"out ({path})")
-    assert_lse_close(lse.cpu().double().numpy(), l_ref)
+    path = swa.verify_path(B, L, Hq, Hkv, D, W, swa.SWA_F32 if fp32 else swa.SWA_BF16)
+    _close(out, lse, o_ref, l_ref, fp32, path)
     assert swa.device_error() == 0
 
 
