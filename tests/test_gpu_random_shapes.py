@@ -1,5 +1,5 @@
 """Seeded random shapes through every path selection: prefill (each kernel the
-sizes pick, bf16 and fp32), decode, verify and the host-memory prefill, each
+sizes pick), decode, verify and the host-memory prefill, in bf16 and fp32, each
 compared element by element with the fp64 oracle (the host-memory prefill bit
 for bit with the device call).  The draws mix group sizes the tensor-core kernels take
 with ones they do not, windows on both sides of the sliding-window kernel's
