@@ -160,8 +160,9 @@ class ClockSampler:
     is unavailable, from an ``nvidia-smi -lms`` subprocess."""
 
     REASONS = {
-        "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
-        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+        "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
+        "sync_boost": 0x10, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80,
     }
     SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
                   "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
