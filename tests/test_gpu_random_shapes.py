@@ -1,7 +1,8 @@
 """Seeded random shapes through every path selection: prefill (each kernel the
 sizes pick), decode, verify and the host-memory prefill, in bf16 and fp32, each
 compared element by element with the fp64 oracle (the host-memory prefill bit
-for bit with the device call).  The draws mix group sizes the tensor-core kernels take
+for bit with the device call); rotary embedding, the fused rotate-and-append
+step and the plain ring append likewise.  The draws mix group sizes the tensor-core kernels take
 with ones they do not, windows on both sides of the sliding-window kernel's
 limit, ragged lengths and partial rings."""
 import numpy as np
@@ -172,4 +173,102 @@ def test_random_prefill_long(cuda_ok, seed):
     o_ref, l_ref = oracle.swa_sink_fwd(x.q, x.k, x.v, x.sink, W)
     assert_bf16_close(out.cpu().numpy(), o_ref, what=f"out ({path})")
     assert_lse_close(lse.cpu().numpy(), l_ref)
+    assert swa.device_error() == 0
+
+
+def _rope_close(got, ref, fp32):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    # bf16: one rounding of the result (relative 2^-8); fp32: normwise 1e-5
+    tol = (1e-5 * np.abs(ref).max() + 1e-7) if fp32 else (2.0 ** -8 * np.abs(ref) + 1e-6)
+    assert (np.abs(got - ref) <= tol).all(), np.abs(got - ref).max()
+
+
+def _rope_case(g):
+    D = int(g.choice((64, 128)))
+    rot = int(g.choice((2, 16, D // 2, D - 2, D)))
+    theta = float(g.choice((100.0, 1e4, 5e5)))
+    fp32 = bool(g.random() < 0.5)
+    return D, rot, theta, fp32
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_rope_shape(cuda_ok, seed):
+    g = np.random.default_rng(7600 + seed)
+    D, rot, theta, fp32 = _rope_case(g)
+    B, T, H = int(g.integers(1, 4)), int(g.integers(1, 400)), int(g.integers(1, 20))
+    dt = torch.float32 if fp32 else torch.bfloat16
+    tg = torch.Generator().manual_seed(7600 + seed)
+    x = torch.randn(B, T, H, D, generator=tg).to(dt)
+    pos0 = torch.from_numpy(g.integers(0, 1 << 20, size=B)).to(torch.int64)
+    xd = x.cuda()
+    swa.swa_rope(xd, pos0.cuda(), rot, theta)
+    torch.cuda.synchronize()
+    _rope_close(xd.cpu().double().numpy(), oracle.rope(x, pos0, rot, theta), fp32)
+    assert torch.equal(xd[..., rot:].cpu(), x[..., rot:])
+    assert swa.device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_rope_append_shape(cuda_ok, seed):
+    g = np.random.default_rng(7700 + seed)
+    D, rot, theta, fp32 = _rope_case(g)
+    B, Hkv = int(g.integers(1, 40)), int(g.integers(1, 4))
+    Hq, W = Hkv * int(g.choice(GROUPS)), int(g.choice((1, 33, 128, 200)))
+    dt = torch.float32 if fp32 else torch.bfloat16
+    tg = torch.Generator().manual_seed(7700 + seed)
+    q = torch.randn(B, Hq, D, generator=tg).to(dt)
+    k = torch.randn(B, Hkv, D, generator=tg).to(dt)
+    v = torch.randn(B, Hkv, D, generator=tg).to(dt)
+    kr0 = torch.randn(B, Hkv, W, D, generator=tg).to(dt)
+    vr0 = torch.randn(B, Hkv, W, D, generator=tg).to(dt)
+    pos = torch.from_numpy(g.integers(-2, 1 << 19, size=B)).to(torch.int64)
+    kr, vr = kr0.cuda(), vr0.cuda()
+    q_out = torch.full((B, Hq, D), 7.0, dtype=dt, device="cuda")
+    swa.swa_rope_append(q.cuda(), k.cuda(), v.cuda(), kr, vr, pos.cuda(), rot, theta, q_out=q_out)
+    torch.cuda.synchronize()
+    pos_ok = pos.clamp(min=0)
+    q_ref = oracle.rope(q.unsqueeze(1), pos_ok, rot, theta)[:, 0]
+    k_ref = oracle.rope(k.unsqueeze(1), pos_ok, rot, theta)[:, 0]
+    kr_h, vr_h, qo_h = kr.cpu(), vr.cpu(), q_out.cpu()
+    for b in range(B):
+        p = int(pos[b])
+        if p < 0:   # a negative position writes nothing
+            assert torch.equal(kr_h[b], kr0[b]) and torch.equal(vr_h[b], vr0[b])
+            assert torch.all(qo_h[b] == 7.0)
+            continue
+        s = p % W
+        _rope_close(qo_h[b].double().numpy(), q_ref[b], fp32)
+        _rope_close(kr_h[b, :, s].double().numpy(), k_ref[b], fp32)
+        assert torch.equal(vr_h[b, :, s], v[b])
+        keep = [t for t in range(W) if t != s]
+        assert torch.equal(kr_h[b][:, keep], kr0[b][:, keep])
+        assert torch.equal(vr_h[b][:, keep], vr0[b][:, keep])
+    assert swa.device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_ring_append_shape(cuda_ok, seed):
+    g = np.random.default_rng(7800 + seed)
+    D = int(g.choice((64, 128)))
+    B, Hkv, W = int(g.integers(1, 60)), int(g.integers(1, 9)), int(g.choice((1, 33, 128, 200)))
+    dt = torch.float32 if g.random() < 0.5 else torch.bfloat16
+    tg = torch.Generator().manual_seed(7800 + seed)
+    k = torch.randn(B, Hkv, D, generator=tg).to(dt)
+    v = torch.randn(B, Hkv, D, generator=tg).to(dt)
+    kr0 = torch.randn(B, Hkv, W, D, generator=tg).to(dt)
+    vr0 = torch.randn(B, Hkv, W, D, generator=tg).to(dt)
+    pos = torch.from_numpy(g.integers(-2, 1 << 19, size=B)).to(torch.int64)
+    kr, vr = kr0.cuda(), vr0.cuda()
+    swa.swa_ring_append(k.cuda(), v.cuda(), kr, vr, pos.cuda())
+    torch.cuda.synchronize()
+    # expected: slot pos mod W of each sequence replaced (bit for bit), the
+    # rest unchanged; a negative position writes nothing
+    ek, ev = kr0.clone(), vr0.clone()
+    for b in range(B):
+        p = int(pos[b])
+        if p >= 0:
+            ek[b, :, p % W] = k[b]
+            ev[b, :, p % W] = v[b]
+    assert torch.equal(kr.cpu(), ek) and torch.equal(vr.cpu(), ev)
     assert swa.device_error() == 0
