@@ -337,11 +337,13 @@ def traffic_shape(**dims) -> str:
     return " ".join(f"{k}{v}" for k, v in dims.items())
 
 
-def recorded_traffic(kernel: str, shape: str, path: str = ""):
+def recorded_traffic(kernel: str, shape: str, path: str = "", record: str = ""):
     """DRAM bytes (read + write) per launch of the bench workload, from the
     committed ncu summary ``profiles/dram_traffic.txt`` (or ``path``); None if
     absent, if the record was taken on another workload shape, or if the
-    kernel's sources have changed since the counters were taken."""
+    kernel's sources have changed since the counters were taken.  ``record``
+    names a second record of the same kernel (another mode of it); it defaults
+    to the kernel's name."""
     path = path or os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
@@ -353,11 +355,12 @@ def recorded_traffic(kernel: str, shape: str, path: str = ""):
                 continue
             key, val = line.split(":", 1)
             rec[key.strip()] = val.strip()
-    if rec.get(f"{kernel}.source_hash") != kernel_source_hash(kernel):
+    record = record or kernel
+    if rec.get(f"{record}.source_hash") != kernel_source_hash(kernel):
         return None
-    if rec.get(f"{kernel}.shape") != shape:
+    if rec.get(f"{record}.shape") != shape:
         return None
-    val = rec.get(f"{kernel}.bytes_per_launch")
+    val = rec.get(f"{record}.bytes_per_launch")
     return int(float(val)) if val else None
 
 
@@ -784,7 +787,11 @@ def high_sparse_line(swa, dev, stream, reps, peaks, cpu):
         "roofline": {"kernel": "swa_fwd_tc_global_kernel (sparse mode)", "bound": "tensor",
                      "achieved": round(tf_first, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(tf_first / peak, 4),
-                     "peak_source": "measured bf16_tflops (burst), the layer timed alone"},
+                     "peak_source": "measured bf16_tflops (burst), the layer timed alone",
+                     "traffic": recorded_traffic(
+                         "swa_fwd_tc_global_kernel",
+                         traffic_shape(B=1, T=T, Hq=Hq, Hkv=Hkv, D=D, QB=QB, topk=topk),
+                         record="swa_fwd_tc_global_kernel.sparse")},
         "in_pipeline": {"achieved": round(tf, 1), "unit": "TFLOP/s",
                         "peak": float(peaks["bf16_tflops_sustained"]),
                         "frac_of_sustained": round(tf / float(peaks["bf16_tflops_sustained"]), 4),
@@ -933,9 +940,9 @@ def wide_global_line(swa, c, steps, dev, stream, peaks, cpu=False):
 
 
 def run_only(args):
-    """A few eager calls of one of the other-shape workloads, for a profiler
-    (``--only prefill_g4`` and so on); prints one JSON line with the mean
-    time of the timed calls."""
+    """A few eager calls of one workload, for a profiler (``--only prefill_g4``,
+    ``--only sparse_main`` and so on); prints one JSON line with the mean time
+    of the timed calls."""
     import hybrid_sliding_window_02_b300 as swa
     swa.lib()
     dev = torch.device("cuda", 0)
@@ -952,6 +959,16 @@ def run_only(args):
         B, T, Hq, Hkv, D, W = (c[k] for k in ("B", "T", "Hq", "Hkv", "D", "W"))
         x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
         call = lambda: swa.swa_sink_fwd(x.q, x.k, x.v, x.sink, W, stream=stream)
+    elif kind == "sparse":
+        # the High Sparse workload: one scored global layer and the selection
+        # (launched once each, before the timed calls), then the sparse layer
+        c = SPARSE
+        T, Hq, Hkv, D, QB, topk = (c[k] for k in ("T", "Hq", "Hkv", "D", "QB", "topk"))
+        x = gen.prefill_inputs(1, T, Hq, Hkv, D, seed=500, device=dev)
+        q2 = gen.prefill_inputs(1, T, Hq, Hkv, D, seed=501, device=dev).q
+        bm = swa.swa_sink_fwd_scores(x.q, x.k, x.v, x.sink, T, stream=stream)[2]
+        idx = swa.swa_topk_blocks(bm, T, QB, topk, stream=stream)
+        call = lambda: swa.swa_sink_sparse_fwd(q2, x.k, x.v, x.sink, idx, QB, stream=stream)
     elif kind == "decode":
         c = DECODE if name == "main" else WIDE_DECODE[name]
         d = gen.decode_inputs(*(c[k] for k in ("B", "Hq", "Hkv", "D", "W")), seed=100, device=dev)
@@ -1161,7 +1178,7 @@ def main(argv=None):
     ap.add_argument("--no-wide", action="store_true",
                     help="skip the lines of other group sizes and draft counts")
     ap.add_argument("--only", default="",
-                    choices=[""] + [f"{k}_main" for k in ("prefill", "decode", "verify")] +
+                    choices=[""] + [f"{k}_main" for k in ("prefill", "decode", "verify", "sparse")] +
                     [f"prefill_{n}" for n in WIDE_PREFILL] + [f"global_{n}" for n in WIDE_GLOBAL] +
                     [f"decode_{n}" for n in WIDE_DECODE] + [f"verify_{n}" for n in WIDE_VERIFY],
                     help="run only a few calls of one workload (for a profiler)")

@@ -143,29 +143,22 @@ struct Item {
   const int* blocks;  // sparse mode: the item's block list
 };
 
-// The u-th item.  Dense mode: the (sequence, head group) pairs one after
-// another, the items of each in order of decreasing causal length for the
-// last pair and every second one before it, increasing for the others (a
-// snake: lengths change smoothly from one pair to the next and the run ends
-// on the shortest items).  The CTAs then share one or two kv heads at any
-// moment, whose keys and values (16.8 MB per kv head at T = 32768) stay in L2;
-// dealt longest-first over all kv heads at once, the live keys and values of
-// all 8 heads (134 MB) overflowed it and were re-read from HBM (2.8x the
-// inputs).  Sparse mode: round by round over all (sequence, kv head) pairs,
-// longest first (items are of nearly equal length there, and spreading the
-// CTAs over the kv heads measured slightly faster).
+// The u-th item: the (sequence, head group) pairs one after another, the
+// items of each in order of decreasing causal length for the last pair and
+// every second one before it, increasing for the others (a snake: lengths
+// change smoothly from one pair to the next and the run ends on the shortest
+// items).  The CTAs then share one or two kv heads at any moment, whose keys
+// and values (16.8 MB per kv head at T = 32768) stay in L2.  Dealt over all
+// kv heads at once, the live keys and values of all 8 heads (134 MB)
+// overflowed it and were re-read from HBM: 2.8x the inputs in the dense
+// layer, 3.5x in the sparse one (its items are of nearly equal length, so
+// the order only decides which keys are live together).
 __device__ __forceinline__ Item item_coords(uint32_t u, const Params& p) {
   Item it;
   const uint32_t bkn = (uint32_t)(p.B * p.Hg);
-  uint32_t r, bk;
-  if (p.blk_idx != nullptr) {
-    r = u / bkn;
-    bk = u - r * bkn;
-  } else {
-    bk = u / (uint32_t)p.nitem_seq;
-    r = u - bk * (uint32_t)p.nitem_seq;
-    if ((bkn - 1 - bk) & 1u) r = (uint32_t)p.nitem_seq - 1 - r;
-  }
+  const uint32_t bk = u / (uint32_t)p.nitem_seq;
+  uint32_t r = u - bk * (uint32_t)p.nitem_seq;
+  if ((bkn - 1 - bk) & 1u) r = (uint32_t)p.nitem_seq - 1 - r;
   const int n2 = p.nitem_seq - 1 - (int)r;
   it.b = (int)(bk / (uint32_t)p.Hg);
   it.grp = (int)(bk - (uint32_t)it.b * (uint32_t)p.Hg);

@@ -94,3 +94,20 @@ def test_traffic_record_applies_to_its_own_workload_only(tmp_path):
     rec.write_text(rec.read_text().replace("source_hash: ", "source_hash: 0"))
     assert bench.recorded_traffic("decode_tc_kernel", shape, str(rec)) is None
     assert bench.recorded_traffic("verify_tc_kernel", shape, str(rec)) is None
+
+
+def test_traffic_record_of_a_kernel_mode(tmp_path):
+    # a second record of one kernel (its sparse mode) is keyed by its own name
+    # but checked against the kernel's source hash
+    k = "swa_fwd_tc_global_kernel"
+    shape = bench.traffic_shape(B=1, T=32768, Hq=64, Hkv=8, D=128, QB=64, topk=16)
+    rec = tmp_path / "traffic.txt"
+    rec.write_text(f"{k}.bytes_per_launch: 111\n"
+                   f"{k}.source_hash: {bench.kernel_source_hash(k)}\n"
+                   f"{k}.shape: B1 T32768 Hq64 Hkv8 D128 W32768\n"
+                   f"{k}.sparse.bytes_per_launch: 222\n"
+                   f"{k}.sparse.source_hash: {bench.kernel_source_hash(k)}\n"
+                   f"{k}.sparse.shape: {shape}\n")
+    assert bench.recorded_traffic(k, shape, str(rec), record=f"{k}.sparse") == 222
+    assert bench.recorded_traffic(k, shape, str(rec)) is None
+    assert bench.recorded_traffic(k, "B1 T32768 Hq64 Hkv8 D128 W32768", str(rec)) == 111
