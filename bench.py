@@ -525,6 +525,83 @@ def decode_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None):
     return line
 
 
+def decode_step_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None, theta=10000.0):
+    """One generated token per sequence: its k and v written into the ring
+    (alone: ``swa_ring_append``; fused with the rotation of its q and k:
+    ``swa_rope_append``), then decode of the rotated q.  Each part is timed on
+    its own and the step as a whole, from CUDA graphs rotating over input sets
+    whose total exceeds L2."""
+    c = c or DECODE
+    B, Hq, Hkv, D, W = (c[k] for k in ("B", "Hq", "Hkv", "D", "W"))
+    sets = []
+    for i in range(nsets):
+        d = gen.decode_inputs(B, Hq, Hkv, D, W, seed=100 + i, device=dev)
+        g = torch.Generator(device=dev).manual_seed(400 + i)
+        kn = torch.randn(B, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+        vn = torch.randn(B, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+        sets.append((d, kn, vn, torch.empty_like(d.q)))
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+
+    def append(x):
+        d, kn, vn, _ = x
+        swa.swa_ring_append(kn, vn, d.k_ring, d.v_ring, d.pos, stream=stream)
+
+    def rope_append(x):
+        d, kn, vn, qo = x
+        swa.swa_rope_append(d.q, kn, vn, d.k_ring, d.v_ring, d.pos, D, theta, q_out=qo,
+                            stream=stream)
+
+    def step(x):
+        rope_append(x)
+        d, _, _, qo = x
+        swa.swa_sink_decode(qo, d.k_ring, d.v_ring, d.pos, d.sink, out, lse, stream=stream)
+
+    ms_app = time_graph(append, sets, steps, 3, stream)
+    ms_rope = time_graph(rope_append, sets, steps, 3, stream)
+    ms_step, clocks = with_clocks(dev, lambda: time_graph(step, sets, steps, 3, stream))
+    b_app = work.append_bytes(B, Hkv, D, 2)
+    b_rope = work.rope_append_bytes(B, Hq, Hkv, D, 2)
+    b_step = b_rope + work.decode_bytes(B, Hq, Hkv, D, W, 2)
+    gbs = b_step / (ms_step * 1e-3) / 1e9
+    gbs_rope = b_rope / (ms_rope * 1e-3) / 1e9
+    line = {
+        "workload": f"decode step B{B} Hq{Hq} Hkv{Hkv} D{D} W{W}: rotate q, k and append k, v "
+                    f"(rot_dim {D}, theta {theta:g}), then decode; bf16->fp32+lse, {nsets} sets "
+                    "(>L2), graph of 32",
+        "value": round(gbs, 1), "unit": "GB/s", "us_per_step": round(ms_step * 1e3, 2),
+        "append_us": round(ms_app * 1e3, 2),
+        "append_gbs": round(b_app / (ms_app * 1e-3) / 1e9, 1),
+        "rope_append_us": round(ms_rope * 1e3, 2),
+        # the fused rotate-and-append moves ~10 MB: a few microseconds at any
+        # rate, so its fraction says more about launch latency than about HBM
+        "roofline": {"kernel": "rope_append_kernel", "bound": "hbm", "achieved": round(gbs_rope, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(gbs_rope / hbm, 4),
+                     "bytes_per_launch": b_rope, "traffic": None},
+        "step_frac_of_hbm": round(gbs / hbm, 4),
+        "clocks": clocks,
+    }
+    if cpu:
+        import oracle
+        d, kn, vn, _ = sets[0]
+        hq, hk, hv, kr, vr, pos, sk = (t.cpu() for t in (d.q, kn, vn, d.k_ring, d.v_ring, d.pos,
+                                                           d.sink))
+
+        def host_step():
+            p0 = pos.clamp(min=0)
+            qr = torch.from_numpy(oracle.rope(hq.unsqueeze(1), p0, D, theta)[:, 0])
+            kr_new = torch.from_numpy(oracle.rope(hk.unsqueeze(1), p0, D, theta)[:, 0])
+            k_ring, v_ring = kr.double(), vr.double()
+            for b in range(B):
+                if int(pos[b]) >= 0:
+                    k_ring[b, :, int(pos[b]) % W] = kr_new[b]
+                    v_ring[b, :, int(pos[b]) % W] = hv[b].double()
+            oracle.swa_sink_decode(qr, k_ring, v_ring, pos, sk)
+        line["cpu_baseline"] = cpu_oracle_call(host_step, b_step, "GB/s",
+                                               f"the whole step ({B} seqs)")
+    return line
+
+
 def verify_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None):
     """Verify calls (L drafted tokens per sequence) rotating over input sets
     whose total exceeds L2."""
@@ -1115,6 +1192,7 @@ def run_ours(args, dist):
             wide["verify_" + name] = {k: d[k] for k in ("workload", "value", "unit", "roofline",
                                                         "cpu_baseline") if k in d}
         line["other_shapes"] = wide
+    line["decode_step"] = decode_step_line(swa, dev, stream, args.decode_steps, hbm, cpu)
     line["verify"] = verify_line(swa, dev, stream, args.decode_steps, hbm, cpu)
     line["decode"] = decode_line(swa, dev, stream, args.decode_steps, hbm, cpu)
     if swa.device_error() != 0:

@@ -1053,6 +1053,14 @@ static bool rope_args_ok(int D, int rot_dim, double theta) {
          theta > 0.0 && std::isfinite(theta);
 }
 
+// f_i = theta^(-2 i / rot_dim) in fp64, the table the RoPE kernels read
+static swa::RopeFreq rope_freq(int rot_dim, double theta) {
+  swa::RopeFreq fr;
+  for (int i = 0; i < swa::kRopeMaxHalf; ++i)
+    fr.f[i] = i < rot_dim / 2 ? std::pow(theta, -2.0 * i / rot_dim) : 0.0;
+  return fr;
+}
+
 swa_status swa_rope(void* x, const int64_t* pos0, int B, int T, int H, int D, int rot_dim,
                     double theta, swa_dtype dtype, void* stream) {
   g_last_error[0] = '\0';
@@ -1065,13 +1073,13 @@ swa_status swa_rope(void* x, const int64_t* pos0, int B, int T, int H, int D, in
   const long long ntok = (long long)B * T;
   const unsigned grid = (unsigned)(ntok < 65536 ? ntok : 65536);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const double l2t = std::log2(theta);
+  const swa::RopeFreq fr = rope_freq(rot_dim, theta);
   if (dtype == SWA_F32)
     swa::rope_inplace_kernel<float><<<grid, swa::kRopeThreads, 0, st>>>(
-        static_cast<float*>(x), pos0, B, T, H, D, rot_dim / 2, l2t);
+        static_cast<float*>(x), pos0, B, T, H, D, rot_dim / 2, fr);
   else
     swa::rope_inplace_kernel<__nv_bfloat16><<<grid, swa::kRopeThreads, 0, st>>>(
-        static_cast<__nv_bfloat16*>(x), pos0, B, T, H, D, rot_dim / 2, l2t);
+        static_cast<__nv_bfloat16*>(x), pos0, B, T, H, D, rot_dim / 2, fr);
   return check_launch("rope_inplace_kernel");
 }
 
@@ -1088,19 +1096,29 @@ swa_status swa_rope_append(const void* q_in, const void* k_in, const void* v_in,
     return SWA_EINVAL;
   if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
   if (!rope_args_ok(D, rot_dim, theta)) return SWA_EINVAL;
+  if ((long long)Hq + 2LL * Hkv > (1LL << 20)) return SWA_EUNSUPPORTED;   // task counts fit an int
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const double l2t = std::log2(theta);
+  const swa::RopeFreq fr = rope_freq(rot_dim, theta);
+  // 16-byte chunks when the rotated half is a whole number of them (every
+  // buffer is 16-byte aligned and D is 64 or 128); a token's chunk tasks are
+  // shared by S blocks of kRopeThreads threads
+  const int half = rot_dim / 2;
+  const int V = dtype == SWA_F32 ? 4 : 8;
+  const int vec = half % V == 0;
+  const int ntask = vec ? swa::rope_append_tasks(Hq, Hkv, D, half, V, q_in != q_out).total() : 0;
+  const dim3 grid((unsigned)B, vec ? (unsigned)((ntask + swa::kRopeThreads - 1) / swa::kRopeThreads)
+                                   : 1u);
   if (dtype == SWA_F32)
-    swa::rope_append_kernel<float><<<(unsigned)B, swa::kRopeThreads, 0, st>>>(
+    swa::rope_append_kernel<float><<<grid, swa::kRopeThreads, 0, st>>>(
         static_cast<const float*>(q_in), static_cast<const float*>(k_in),
         static_cast<const float*>(v_in), static_cast<float*>(q_out), static_cast<float*>(k_ring),
-        static_cast<float*>(v_ring), pos, Hq, Hkv, D, W, rot_dim / 2, l2t);
+        static_cast<float*>(v_ring), pos, Hq, Hkv, D, W, half, vec, fr);
   else
-    swa::rope_append_kernel<__nv_bfloat16><<<(unsigned)B, swa::kRopeThreads, 0, st>>>(
+    swa::rope_append_kernel<__nv_bfloat16><<<grid, swa::kRopeThreads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(q_in), static_cast<const __nv_bfloat16*>(k_in),
         static_cast<const __nv_bfloat16*>(v_in), static_cast<__nv_bfloat16*>(q_out),
         static_cast<__nv_bfloat16*>(k_ring), static_cast<__nv_bfloat16*>(v_ring), pos, Hq, Hkv,
-        D, W, rot_dim / 2, l2t);
+        D, W, half, vec, fr);
   return check_launch("rope_append_kernel");
 }
 

@@ -39,6 +39,18 @@ def decode_bytes(B: int, Hq: int, Hkv: int, D: int, W: int, in_bytes: int,
     return rd + wr
 
 
+def append_bytes(B: int, Hkv: int, D: int, in_bytes: int) -> int:
+    """Ring append: the new token's k and v read, written into one ring slot
+    per (sequence, kv head); pos read."""
+    return 2 * (2 * B * Hkv * D * in_bytes) + B * 8
+
+
+def rope_append_bytes(B: int, Hq: int, Hkv: int, D: int, in_bytes: int) -> int:
+    """Fused rotate-and-append: the ring append plus the new token's q read and
+    its rotated copy written."""
+    return append_bytes(B, Hkv, D, in_bytes) + 2 * B * Hq * D * in_bytes
+
+
 def verify_pairs(L: int, W: int, pos: int) -> int:
     """(query, key) pairs of one verify group row set: drafted token j at
     position pos + j sees min(pos + j + 1, W) keys."""

@@ -255,6 +255,8 @@ swa_status swa_rope(void* x, const int64_t* pos0, int B, int T, int H, int D, in
  *   k_in, v_in [B, Hkv, D] dtype (k before rotation)
  *   k_ring, v_ring [B, Hkv, W, D] dtype (one slot per sequence updated)
  *   pos   [B] int64 (device); a negative pos leaves q_out[b] and the rings untouched.
+ *   Requires what swa_rope requires, 16-byte aligned buffers and Hq + 2 Hkv <=
+ *   2^20 (SWA_EUNSUPPORTED beyond); q_out overlaps no input other than q_in.
  */
 swa_status swa_rope_append(const void* q_in, const void* k_in, const void* v_in, void* q_out,
                            void* k_ring, void* v_ring, const int64_t* pos, int B, int Hq,

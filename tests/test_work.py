@@ -53,3 +53,13 @@ def test_hybrid_reduction_seven_to_one():
     assert 7.0 <= flop < 8.0 and 7.0 <= kv < 8.0
     flop_long, kv_long = work.hybrid_reduction(262144, 128, 7, 1)
     assert flop < flop_long < 8.0 and kv < kv_long < 8.0
+
+
+def test_append_byte_counts():
+    from hybrid_sliding_window_02_b300 import work
+    # 256 sequences, 8 kv heads, D = 128, bf16: k and v of the new token
+    # (2 x 512 KB) read and written once, pos 2 KB; the fused step adds q
+    # (4 MB) read and its rotated copy written
+    assert work.append_bytes(256, 8, 128, 2) == 4 * 524_288 + 2048
+    assert work.rope_append_bytes(256, 64, 8, 128, 2) == (
+        work.append_bytes(256, 8, 128, 2) + 2 * 4_194_304)
