@@ -525,6 +525,43 @@ def decode_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None):
     return line
 
 
+def rope_line(swa, dev, stream, reps, hbm, cpu, theta=10000.0):
+    """RoPE of a prefill, in place: q and k of the headline workload rotated at
+    positions 0 .. T-1 (rot_dim = D), two launches per step; inputs larger
+    than L2."""
+    c = PREFILL
+    B, T, Hq, Hkv, D = (c[k] for k in ("B", "T", "Hq", "Hkv", "D"))
+    x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
+    pos0 = torch.zeros(B, dtype=torch.int64, device=dev)
+
+    def call():
+        swa.swa_rope(x.q, pos0, D, theta, stream=stream)
+        swa.swa_rope(x.k, pos0, D, theta, stream=stream)
+
+    ms, clocks = with_clocks(dev, lambda: _event_ms(call, reps, stream))
+    nbytes = work.rope_bytes(B, T, Hq, D, 2) + work.rope_bytes(B, T, Hkv, D, 2)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "workload": f"RoPE in place of q [B{B} T{T} Hq{Hq} D{D}] and k [Hkv{Hkv}], bf16, rot_dim {D}, "
+                    f"theta {theta:g}, positions 0..{T - 1}",
+        "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+        "roofline": {"kernel": "rope_inplace_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "bytes_per_step": nbytes, "traffic": None},
+        "clocks": clocks,
+    }
+    if cpu:
+        import oracle
+        n = 512   # the first 512 positions of sequence 0, q and k
+        qs, ks = x.q[:1, :n].cpu(), x.k[:1, :n].cpu()
+        p0 = torch.zeros(1, dtype=torch.int64)
+        line["cpu_baseline"] = cpu_oracle_call(
+            lambda: (oracle.rope(qs, p0, D, theta), oracle.rope(ks, p0, D, theta)),
+            work.rope_bytes(1, n, Hq, D, 2) + work.rope_bytes(1, n, Hkv, D, 2), "GB/s",
+            f"q and k of positions 0..{n - 1} of sequence 0")
+    return line
+
+
 def decode_step_line(swa, dev, stream, steps, hbm, cpu, nsets=4, c=None, theta=10000.0):
     """One generated token per sequence: its k and v written into the ring
     (alone: ``swa_ring_append``; fused with the rotation of its q and k:
@@ -1192,6 +1229,7 @@ def run_ours(args, dist):
             wide["verify_" + name] = {k: d[k] for k in ("workload", "value", "unit", "roofline",
                                                         "cpu_baseline") if k in d}
         line["other_shapes"] = wide
+    line["rope"] = rope_line(swa, dev, stream, max(20, args.steps // 20), hbm, cpu)
     line["decode_step"] = decode_step_line(swa, dev, stream, args.decode_steps, hbm, cpu)
     line["verify"] = verify_line(swa, dev, stream, args.decode_steps, hbm, cpu)
     line["decode"] = decode_line(swa, dev, stream, args.decode_steps, hbm, cpu)

@@ -101,20 +101,56 @@ __device__ __forceinline__ void rope_pair_chunk(uint4 ra, uint4 rb, Tin* dst, in
 }
 
 // In place on x [B, T, H, D]: token (b, t) at position pos0[b] + t.  One block
-// per token (grid-stride over tokens).
+// per token (grid-stride over tokens).  With vec (half a multiple of V, rows
+// 16-byte aligned) a task is one 16-byte chunk pair of one head, two per
+// thread per round, and the first round's chunks are loaded before the
+// token's angles are formed; otherwise element by element.
 template <typename Tin>
 __global__ void __launch_bounds__(kRopeThreads) rope_inplace_kernel(
     Tin* __restrict__ x, const int64_t* __restrict__ pos0, int B, int T, int H, int D, int half,
-    const __grid_constant__ RopeFreq fr) {
+    int vec, const __grid_constant__ RopeFreq fr) {
   __shared__ float cs[kRopeMaxHalf], sn[kRopeMaxHalf];
+  constexpr int V = 16 / (int)sizeof(Tin);
+  const int nr = half / V;   // chunk pairs per head
+  const int n = H * nr;      // tasks per token
   const int64_t ntok = (int64_t)B * T;
   for (int64_t tok = blockIdx.x; tok < ntok; tok += gridDim.x) {
     const int b = (int)(tok / T);
     const int t = (int)(tok - (int64_t)b * T);
+    Tin* base = x + tok * H * D;
     __syncthreads();  // previous token's angles are no longer read
+    if (vec) {
+      uint4 ra[2], rb[2];
+      auto load = [&](int j0) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = j0 + k * (int)blockDim.x;
+          if (j < n) {
+            const int h = j / nr, i0 = (j - h * nr) * V;
+            const Tin* row = base + (int64_t)h * D;
+            ra[k] = *reinterpret_cast<const uint4*>(row + i0);
+            rb[k] = *reinterpret_cast<const uint4*>(row + i0 + half);
+          }
+        }
+      };
+      load(threadIdx.x);
+      rope_angles(pos0[b] + t, half, fr, cs, sn);
+      __syncthreads();
+      for (int j0 = threadIdx.x; j0 < n; j0 += 2 * (int)blockDim.x) {
+        if (j0 != (int)threadIdx.x) load(j0);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = j0 + k * (int)blockDim.x;
+          if (j < n) {
+            const int h = j / nr, i0 = (j - h * nr) * V;
+            rope_pair_chunk<Tin>(ra[k], rb[k], base + (int64_t)h * D, i0, half, cs, sn);
+          }
+        }
+      }
+      continue;
+    }
     rope_angles(pos0[b] + t, half, fr, cs, sn);
     __syncthreads();
-    Tin* base = x + tok * H * D;
     // thread -> (head, pair): pairs of consecutive threads share a head
     for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
       const int h = idx / half, i = idx - h * half;

@@ -1066,6 +1066,7 @@ swa_status swa_rope(void* x, const int64_t* pos0, int B, int T, int H, int D, in
   g_last_error[0] = '\0';
   if (!x || !pos0) return SWA_EINVAL;
   if (B < 1 || T < 1 || H < 1 || D < 1) return SWA_EINVAL;
+  if ((long long)H * D > (1LL << 30)) return SWA_EUNSUPPORTED;   // per-token counts fit an int
   if (dtype != SWA_F32 && dtype != SWA_BF16) return SWA_EINVAL;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(pos0) & 7u)) return SWA_EINVAL;
   if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
@@ -1074,12 +1075,14 @@ swa_status swa_rope(void* x, const int64_t* pos0, int B, int T, int H, int D, in
   const unsigned grid = (unsigned)(ntok < 65536 ? ntok : 65536);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const swa::RopeFreq fr = rope_freq(rot_dim, theta);
+  const int half = rot_dim / 2;
+  const int vec = half % (dtype == SWA_F32 ? 4 : 8) == 0;   // whole 16-byte chunks
   if (dtype == SWA_F32)
     swa::rope_inplace_kernel<float><<<grid, swa::kRopeThreads, 0, st>>>(
-        static_cast<float*>(x), pos0, B, T, H, D, rot_dim / 2, fr);
+        static_cast<float*>(x), pos0, B, T, H, D, half, vec, fr);
   else
     swa::rope_inplace_kernel<__nv_bfloat16><<<grid, swa::kRopeThreads, 0, st>>>(
-        static_cast<__nv_bfloat16*>(x), pos0, B, T, H, D, rot_dim / 2, fr);
+        static_cast<__nv_bfloat16*>(x), pos0, B, T, H, D, half, vec, fr);
   return check_launch("rope_inplace_kernel");
 }
 

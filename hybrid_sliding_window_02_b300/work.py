@@ -45,6 +45,11 @@ def append_bytes(B: int, Hkv: int, D: int, in_bytes: int) -> int:
     return 2 * (2 * B * Hkv * D * in_bytes) + B * 8
 
 
+def rope_bytes(B: int, T: int, H: int, D: int, in_bytes: int) -> int:
+    """RoPE in place on x [B, T, H, D]: x read and written once; pos0 read."""
+    return 2 * B * T * H * D * in_bytes + B * 8
+
+
 def rope_append_bytes(B: int, Hq: int, Hkv: int, D: int, in_bytes: int) -> int:
     """Fused rotate-and-append: the ring append plus the new token's q read and
     its rotated copy written."""

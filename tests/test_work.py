@@ -63,3 +63,10 @@ def test_append_byte_counts():
     assert work.append_bytes(256, 8, 128, 2) == 4 * 524_288 + 2048
     assert work.rope_append_bytes(256, 64, 8, 128, 2) == (
         work.append_bytes(256, 8, 128, 2) + 2 * 4_194_304)
+
+
+def test_rope_byte_count():
+    from hybrid_sliding_window_02_b300 import work
+    # q of the headline prefill (B4 T8192 Hq64 D128 bf16, 536,870,912 B) read
+    # and written, plus 4 int64 start positions
+    assert work.rope_bytes(4, 8192, 64, 128, 2) == 2 * 536_870_912 + 32
