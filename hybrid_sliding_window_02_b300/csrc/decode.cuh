@@ -20,6 +20,7 @@
 #pragma once
 
 #include "device_common.cuh"
+#include "griddep.cuh"
 
 namespace swa {
 
@@ -264,6 +265,9 @@ template <typename Tin>
 __global__ void ring_append_kernel(const Tin* __restrict__ k_new, const Tin* __restrict__ v_new,
                                    Tin* __restrict__ k_ring, Tin* __restrict__ v_ring,
                                    const int64_t* __restrict__ pos, int B, int Hkv, int D, int W) {
+  // a decode launched after the append may start its set-up now; it waits for
+  // this grid to complete before it touches memory
+  if (threadIdx.x == 0) grid_dep_launch();
   constexpr int EPV = 16 / sizeof(Tin);
   const int vecs_per_row = D / EPV;
   const int64_t total = (int64_t)B * Hkv * vecs_per_row;
