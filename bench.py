@@ -1083,6 +1083,30 @@ def run_only(args):
         bm = swa.swa_sink_fwd_scores(x.q, x.k, x.v, x.sink, T, stream=stream)[2]
         idx = swa.swa_topk_blocks(bm, T, QB, topk, stream=stream)
         call = lambda: swa.swa_sink_sparse_fwd(q2, x.k, x.v, x.sink, idx, QB, stream=stream)
+    elif kind == "rope":
+        # RoPE in place of the headline prefill's q and k (two launches)
+        c = PREFILL
+        B, T, Hq, Hkv, D = (c[k] for k in ("B", "T", "Hq", "Hkv", "D"))
+        x = gen.prefill_inputs(B, T, Hq, Hkv, D, seed=7, device=dev)
+        pos0 = torch.zeros(B, dtype=torch.int64, device=dev)
+
+        def call():
+            swa.swa_rope(x.q, pos0, D, 10000.0, stream=stream)
+            swa.swa_rope(x.k, pos0, D, 10000.0, stream=stream)
+    elif kind == "step":
+        # one decode step: rotate the new token's q and k, append k and v, decode
+        c = DECODE
+        B, Hq, Hkv, D, W = (c[k] for k in ("B", "Hq", "Hkv", "D", "W"))
+        d = gen.decode_inputs(B, Hq, Hkv, D, W, seed=100, device=dev)
+        g = torch.Generator(device=dev).manual_seed(400)
+        kn = torch.randn(B, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+        vn = torch.randn(B, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+        qo = torch.empty_like(d.q)
+
+        def call():
+            swa.swa_rope_append(d.q, kn, vn, d.k_ring, d.v_ring, d.pos, D, 10000.0, q_out=qo,
+                                stream=stream)
+            swa.swa_sink_decode(qo, d.k_ring, d.v_ring, d.pos, d.sink, stream=stream)
     elif kind == "decode":
         c = DECODE if name == "main" else WIDE_DECODE[name]
         d = gen.decode_inputs(*(c[k] for k in ("B", "Hq", "Hkv", "D", "W")), seed=100, device=dev)
@@ -1294,7 +1318,8 @@ def main(argv=None):
     ap.add_argument("--no-wide", action="store_true",
                     help="skip the lines of other group sizes and draft counts")
     ap.add_argument("--only", default="",
-                    choices=[""] + [f"{k}_main" for k in ("prefill", "decode", "verify", "sparse")] +
+                    choices=[""] + [f"{k}_main" for k in ("prefill", "decode", "verify", "sparse", "rope",
+                                                          "step")] +
                     [f"prefill_{n}" for n in WIDE_PREFILL] + [f"global_{n}" for n in WIDE_GLOBAL] +
                     [f"decode_{n}" for n in WIDE_DECODE] + [f"verify_{n}" for n in WIDE_VERIFY],
                     help="run only a few calls of one workload (for a profiler)")

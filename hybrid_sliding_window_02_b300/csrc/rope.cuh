@@ -24,6 +24,8 @@ namespace swa {
 constexpr int kRopeThreads = 256;
 constexpr int kRopeMaxHalf = 64;   // rot_dim <= 128
 
+constexpr int kRopeMaxTok = 8;   // tokens per block of rope_inplace_kernel
+
 // f[i] = theta^(-2 i / rot_dim), i < rot_dim / 2, computed on the host in fp64.
 struct RopeFreq {
   double f[kRopeMaxHalf];
@@ -40,20 +42,20 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
-// cos / sin of a_i = p * f_i for i < half, into shared memory.  The product
-// and the reduction to [-pi, pi] are fp64 (a multiply, a rint and an fma).
-__device__ __forceinline__ void rope_angles(int64_t p, int half, const RopeFreq& fr, float* cs,
-                                            float* sn) {
+// cos and sin of a = p * f: the product and its reduction to [-pi, pi] in
+// fp64 (a multiply, a rint and an fma), the sine and cosine in fp32.
+__device__ __forceinline__ void rope_angle(int64_t p, double f, float& c, float& s) {
   const double two_pi = 6.283185307179586476925286766559;
   const double inv_two_pi = 0.15915494309189533576888376337251;
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    const double a = (double)p * fr.f[i];
-    const double r = fma(-rint(a * inv_two_pi), two_pi, a);
-    float s, c;
-    sincosf((float)r, &s, &c);
-    cs[i] = c;
-    sn[i] = s;
-  }
+  const double a = (double)p * f;
+  const double r = fma(-rint(a * inv_two_pi), two_pi, a);
+  sincosf((float)r, &s, &c);
+}
+
+// cos / sin of a_i = p * f_i for i < half, into shared memory.
+__device__ __forceinline__ void rope_angles(int64_t p, int half, const RopeFreq& fr, float* cs,
+                                            float* sn) {
+  for (int i = threadIdx.x; i < half; i += blockDim.x) rope_angle(p, fr.f[i], cs[i], sn[i]);
 }
 
 // Rotate one D-vector (src -> dst; they may alias) with the angles in cs / sn.
@@ -100,64 +102,83 @@ __device__ __forceinline__ void rope_pair_chunk(uint4 ra, uint4 rb, Tin* dst, in
   *reinterpret_cast<uint4*>(dst + i0 + half) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
 }
 
-// In place on x [B, T, H, D]: token (b, t) at position pos0[b] + t.  One block
-// per token (grid-stride over tokens).  With vec (half a multiple of V, rows
-// 16-byte aligned) a task is one 16-byte chunk pair of one head, two per
-// thread per round, and the first round's chunks are loaded before the
-// token's angles are formed; otherwise element by element.
+// In place on x [B, T, H, D]: token (b, t) at position pos0[b] + t.  Each
+// block takes tpb consecutive tokens at a time (grid-stride), so that a
+// tensor with few heads still gives every thread work; the tokens' angles
+// are formed once per block.  With vec (half a multiple of V, rows 16-byte
+// aligned) a task is one 16-byte chunk pair of one head, two per thread per
+// round, and the first round's chunks are loaded before the angles are
+// formed; otherwise (tpb = 1) element by element.
 template <typename Tin>
 __global__ void __launch_bounds__(kRopeThreads) rope_inplace_kernel(
     Tin* __restrict__ x, const int64_t* __restrict__ pos0, int B, int T, int H, int D, int half,
-    int vec, const __grid_constant__ RopeFreq fr) {
-  __shared__ float cs[kRopeMaxHalf], sn[kRopeMaxHalf];
+    int vec, int tpb, const __grid_constant__ RopeFreq fr) {
+  __shared__ float cs[kRopeMaxTok][kRopeMaxHalf], sn[kRopeMaxTok][kRopeMaxHalf];
   constexpr int V = 16 / (int)sizeof(Tin);
   const int nr = half / V;   // chunk pairs per head
   const int n = H * nr;      // tasks per token
   const int64_t ntok = (int64_t)B * T;
-  for (int64_t tok = blockIdx.x; tok < ntok; tok += gridDim.x) {
-    const int b = (int)(tok / T);
-    const int t = (int)(tok - (int64_t)b * T);
-    Tin* base = x + tok * H * D;
-    __syncthreads();  // previous token's angles are no longer read
+  for (int64_t tok0 = (int64_t)blockIdx.x * tpb; tok0 < ntok; tok0 += (int64_t)gridDim.x * tpb) {
+    const int nt = (int)min((int64_t)tpb, ntok - tok0);
+    auto angles = [&]() {
+      for (int idx = threadIdx.x; idx < nt * half; idx += blockDim.x) {
+        const int tt = idx / half, i = idx - tt * half;
+        const int64_t tok = tok0 + tt;
+        const int b = (int)(tok / T);
+        const int64_t p = pos0[b] + (tok - (int64_t)b * T);
+        rope_angle(p, fr.f[i], cs[tt][i], sn[tt][i]);
+      }
+    };
+    __syncthreads();  // the previous tokens' angles are no longer read
     if (vec) {
+      const int ntask = nt * n;
       uint4 ra[2], rb[2];
+      auto row_of = [&](int j, int& i0) -> Tin* {
+        const int tt = j / n, jj = j - tt * n;
+        const int h = jj / nr;
+        i0 = (jj - h * nr) * V;
+        return x + ((tok0 + tt) * H + h) * D;
+      };
       auto load = [&](int j0) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int j = j0 + k * (int)blockDim.x;
-          if (j < n) {
-            const int h = j / nr, i0 = (j - h * nr) * V;
-            const Tin* row = base + (int64_t)h * D;
+          if (j < ntask) {
+            int i0;
+            const Tin* row = row_of(j, i0);
             ra[k] = *reinterpret_cast<const uint4*>(row + i0);
             rb[k] = *reinterpret_cast<const uint4*>(row + i0 + half);
           }
         }
       };
       load(threadIdx.x);
-      rope_angles(pos0[b] + t, half, fr, cs, sn);
+      angles();
       __syncthreads();
-      for (int j0 = threadIdx.x; j0 < n; j0 += 2 * (int)blockDim.x) {
+      for (int j0 = threadIdx.x; j0 < ntask; j0 += 2 * (int)blockDim.x) {
         if (j0 != (int)threadIdx.x) load(j0);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int j = j0 + k * (int)blockDim.x;
-          if (j < n) {
-            const int h = j / nr, i0 = (j - h * nr) * V;
-            rope_pair_chunk<Tin>(ra[k], rb[k], base + (int64_t)h * D, i0, half, cs, sn);
+          if (j < ntask) {
+            int i0;
+            Tin* row = row_of(j, i0);
+            const int tt = j / n;
+            rope_pair_chunk<Tin>(ra[k], rb[k], row, i0, half, cs[tt], sn[tt]);
           }
         }
       }
       continue;
     }
-    rope_angles(pos0[b] + t, half, fr, cs, sn);
+    angles();
     __syncthreads();
     // thread -> (head, pair): pairs of consecutive threads share a head
+    Tin* base = x + tok0 * H * D;
     for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
       const int h = idx / half, i = idx - h * half;
       Tin* v = base + (int64_t)h * D;
       const float x0 = to_f32(v[i]), x1 = to_f32(v[i + half]);
-      v[i] = from_f32<Tin>(x0 * cs[i] - x1 * sn[i]);
-      v[i + half] = from_f32<Tin>(x1 * cs[i] + x0 * sn[i]);
+      v[i] = from_f32<Tin>(x0 * cs[0][i] - x1 * sn[0][i]);
+      v[i + half] = from_f32<Tin>(x1 * cs[0][i] + x0 * sn[0][i]);
     }
   }
 }

@@ -1072,17 +1072,26 @@ swa_status swa_rope(void* x, const int64_t* pos0, int B, int T, int H, int D, in
   if (D != 64 && D != 128) return SWA_EUNSUPPORTED;
   if (!rope_args_ok(D, rot_dim, theta)) return SWA_EINVAL;
   const long long ntok = (long long)B * T;
-  const unsigned grid = (unsigned)(ntok < 65536 ? ntok : 65536);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const swa::RopeFreq fr = rope_freq(rot_dim, theta);
   const int half = rot_dim / 2;
-  const int vec = half % (dtype == SWA_F32 ? 4 : 8) == 0;   // whole 16-byte chunks
+  const int V = dtype == SWA_F32 ? 4 : 8;
+  const int vec = half % V == 0;   // whole 16-byte chunks
+  // tokens per block: enough that a token's chunk tasks (H x half/V) fill the
+  // block's threads at least once
+  const int per_tok = H * (half / V);
+  const int tpb = !vec ? 1
+                       : (per_tok >= swa::kRopeThreads ? 1
+                                                       : std::min(swa::kRopeMaxTok,
+                                                                  swa::kRopeThreads / per_tok));
+  const long long nblk = (ntok + tpb - 1) / tpb;
+  const unsigned grid = (unsigned)(nblk < 65536 ? nblk : 65536);
   if (dtype == SWA_F32)
     swa::rope_inplace_kernel<float><<<grid, swa::kRopeThreads, 0, st>>>(
-        static_cast<float*>(x), pos0, B, T, H, D, half, vec, fr);
+        static_cast<float*>(x), pos0, B, T, H, D, half, vec, tpb, fr);
   else
     swa::rope_inplace_kernel<__nv_bfloat16><<<grid, swa::kRopeThreads, 0, st>>>(
-        static_cast<__nv_bfloat16*>(x), pos0, B, T, H, D, half, vec, fr);
+        static_cast<__nv_bfloat16*>(x), pos0, B, T, H, D, half, vec, tpb, fr);
   return check_launch("rope_inplace_kernel");
 }
 
