@@ -101,3 +101,19 @@ def test_rotate_append_decode_equals_rotated_prefill(cuda_ok):
     assert worst <= 2e-2, worst
     assert lworst <= 1e-3, lworst
     assert swa.device_error() == 0
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("B,T,H", [(3, 5, 1), (4, 3, 2), (2, 9, 3)])
+def test_rope_groups_of_tokens_across_sequences(cuda_ok, dt, B, T, H):
+    # few heads per token: a block takes up to 8 tokens at a time, which here
+    # span several sequences with unrelated start positions
+    D, rot = 64, 64
+    g = torch.Generator().manual_seed(90 + B * T * H)
+    x = torch.randn(B, T, H, D, generator=g).to(dt)
+    pos0 = torch.tensor([7, 262140, 0, 99999][:B], dtype=torch.int64)
+    xd = x.cuda()
+    swa.swa_rope(xd, pos0.cuda(), rot, THETA)
+    torch.cuda.synchronize()
+    _close_to_rounding(xd.cpu().double().numpy(), oracle.rope(x, pos0, rot, THETA), dt)
+    assert swa.device_error() == 0
