@@ -448,6 +448,11 @@ def time_prefill(swa, x, c, steps, warmup, dist, stream):
     dist.barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
+        # a short device-side wait ahead of the first event, so that the host
+        # has queued the first launches before the stream reaches it: the
+        # events then time the kernels, not the host's first enqueue
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(400_000)
         e0.record(stream)
         for s in range(steps):
             ev[s][0].record(stream)
